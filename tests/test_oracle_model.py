@@ -1,0 +1,282 @@
+"""Pins of the fp64 oracle's model, loss and optimizer to things other than itself.
+
+Each test checks the oracle against finite differences, an independent
+autograd library, a closed form, a textbook value or an exact invariant, so
+that a dropped term, a wrong sign or index or a transposed operand in
+``oracle/model.py`` fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import model as om
+from synth import KIND_FFN, KIND_LM, Workload, param_specs
+
+TINY_LM = Workload("t_lm", KIND_LM, L=2, K=1, M=1, d=8, heads=2, ffn=16, seq=5, vocab=11,
+                   n=3, dtype="f32")
+TINY_FFN = Workload("t_ffn", KIND_FFN, L=2, K=1, M=1, d=8, heads=0, ffn=16, seq=1, vocab=0,
+                    n=3, dtype="f32")
+
+
+def _random_params(w, seed, scale=0.5):
+    """Every parameter random (not the init's 0/1) so every term matters."""
+    rng = np.random.default_rng(seed)
+    return {name: rng.standard_normal(shape) * scale + (1.0 if init == "ones" else 0.0)
+            for name, shape, init in param_specs(w)}
+
+
+def _batch(w, seed):
+    rng = np.random.default_rng(seed + 100)
+    if w.kind == KIND_FFN:
+        return {"x": rng.standard_normal((w.n, w.d)), "targets": rng.standard_normal((w.n, w.d))}
+    return {"tokens": rng.integers(0, w.vocab, size=(w.n, w.seq))}
+
+
+def _flat(grads, names):
+    return np.concatenate([np.ravel(grads[n]) for n in names])
+
+
+@pytest.mark.parametrize("w", [TINY_LM, TINY_FFN], ids=["lm", "ffn"])
+def test_finite_differences_every_parameter(w):
+    params = _random_params(w, 1)
+    batch = _batch(w, 1)
+    loss, grads, _ = om.loss_and_grads(w, params, batch)
+    names = [n for n, _, _ in param_specs(w)]
+    h = 1e-6
+    fd = {}
+    for name in names:
+        base = params[name]
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            orig = base[idx]
+            base[idx] = orig + h
+            lp, _ = om.forward_loss(w, params, batch)
+            base[idx] = orig - h
+            lm, _ = om.forward_loss(w, params, batch)
+            base[idx] = orig
+            g[idx] = (lp - lm) / (2 * h)
+        fd[name] = g
+    a, b = _flat(grads, names), _flat(fd, names)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rel <= 1e-6, rel
+    # every parameter group gets a non-trivial gradient
+    for name in names:
+        assert np.linalg.norm(fd[name]) > 0, name
+
+
+def test_finite_differences_input_ffn():
+    w = TINY_FFN
+    params = _random_params(w, 2)
+    batch = _batch(w, 2)
+    _, _, extras = om.loss_and_grads(w, params, batch)
+    h = 1e-6
+    x = batch["x"]
+    g = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        o = x[idx]
+        x[idx] = o + h
+        lp, _ = om.forward_loss(w, params, batch)
+        x[idx] = o - h
+        lm, _ = om.forward_loss(w, params, batch)
+        x[idx] = o
+        g[idx] = (lp - lm) / (2 * h)
+    assert np.linalg.norm(extras["dx0"] - g) / np.linalg.norm(g) <= 1e-6
+
+
+def _torch_loss(w, params_t, batch):
+    """The same model written with torch ops; autograd supplies the gradients."""
+    import torch
+    import torch.nn.functional as F
+    p = params_t
+    if w.kind == KIND_FFN:
+        x = torch.tensor(batch["x"], dtype=torch.float64)
+        t = torch.tensor(batch["targets"], dtype=torch.float64)
+        for l in range(w.L):
+            pre = f"l{l}."
+            u = F.layer_norm(x, (w.d,), p[pre + "ln_g"], p[pre + "ln_b"], eps=1e-5)
+            x = x + F.linear(F.gelu(F.linear(u, p[pre + "w1"], p[pre + "b1"])), p[pre + "w2"], p[pre + "b2"])
+        return ((x - t) ** 2).sum() / (w.n * w.d)
+    tok = torch.tensor(batch["tokens"], dtype=torch.long)
+    x = p["emb"][tok]
+    n, s = tok.shape
+    dh = w.d // w.heads
+    for l in range(w.L):
+        pre = f"l{l}."
+        u = F.layer_norm(x, (w.d,), p[pre + "ln1_g"], p[pre + "ln1_b"], eps=1e-5)
+        qkv = F.linear(u, p[pre + "w_qkv"], p[pre + "b_qkv"])
+        q, k, v = (qkv[..., i * w.d:(i + 1) * w.d].reshape(n, s, w.heads, dh).transpose(1, 2)
+                   for i in range(3))
+        o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+        a = o.transpose(1, 2).reshape(n, s, w.d)
+        x = x + F.linear(a, p[pre + "w_o"], p[pre + "b_o"])
+        u2 = F.layer_norm(x, (w.d,), p[pre + "ln2_g"], p[pre + "ln2_b"], eps=1e-5)
+        x = x + F.linear(F.gelu(F.linear(u2, p[pre + "w1"], p[pre + "b1"])), p[pre + "w2"], p[pre + "b2"])
+    hf = F.layer_norm(x, (w.d,), p["lnf_g"], p["lnf_b"], eps=1e-5)
+    z = hf @ p["emb"].T
+    return F.cross_entropy(z[:, :-1].reshape(-1, w.vocab), tok[:, 1:].reshape(-1), reduction="sum") / (n * (s - 1))
+
+
+@pytest.mark.parametrize("w", [TINY_LM, TINY_FFN,
+                               TINY_LM.replace(L=3, d=16, heads=4, ffn=24, seq=9, vocab=29, n=4)],
+                         ids=["lm", "ffn", "lm_wider"])
+def test_independent_autograd_library(w):
+    torch = pytest.importorskip("torch")
+    params = _random_params(w, 3)
+    batch = _batch(w, 3)
+    loss, grads, _ = om.loss_and_grads(w, params, batch)
+    pt = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in params.items()}
+    lt = _torch_loss(w, pt, batch)
+    lt.backward()
+    assert abs(lt.item() - loss) <= 1e-12 * abs(loss)
+    for k in params:
+        ref = pt[k].grad.numpy()
+        assert np.linalg.norm(grads[k] - ref) <= 1e-11 * max(np.linalg.norm(ref), 1e-300), k
+
+
+@pytest.mark.parametrize("w,M", [(TINY_LM.replace(n=6), 3), (TINY_LM.replace(n=6), 6),
+                                 (TINY_FFN.replace(n=8), 4)])
+def test_micro_batch_sum_equals_full_batch(w, M):
+    """The review's synchronous-update claim: the sum over M disjoint micro-batches
+    of their gradients (each normalised by the whole mini-batch's count) is the
+    full-batch gradient, because LayerNorm and attention act within a sample."""
+    params = _random_params(w, 4)
+    batch = _batch(w, 4)
+    loss, grads, _ = om.loss_and_grads(w, params, batch)
+    count = w.n * (w.d if w.kind == KIND_FFN else (w.seq - 1))
+    mb = w.n // M
+    acc_loss, acc = 0.0, {}
+    for m in range(M):
+        sl = {k: v[m * mb:(m + 1) * mb] for k, v in batch.items()}
+        lm, gm, _ = om.loss_and_grads(w, params, sl, count=count)
+        acc_loss += lm
+        for k, v in gm.items():
+            acc[k] = acc.get(k, 0) + v
+    assert abs(acc_loss - loss) <= 1e-12 * abs(loss)
+    for k in grads:
+        assert np.linalg.norm(acc[k] - grads[k]) <= 1e-12 * np.linalg.norm(grads[k]) + 1e-300, k
+
+
+def test_layer_norm_closed_form():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((7, 32)) * 1e-3 + 2.0      # small variance: eps matters
+    y, (xhat, rstd) = om.layer_norm(x, np.ones(32), np.zeros(32))
+    var = x.var(axis=-1)
+    assert np.allclose(y.mean(axis=-1), 0.0, atol=1e-12)
+    assert np.allclose(y.var(axis=-1), var / (var + 1e-5), rtol=1e-10)
+    y2, _ = om.layer_norm(x, np.full(32, 3.0), np.full(32, -1.0))
+    assert np.allclose(y2, 3.0 * y - 1.0, rtol=1e-12)
+
+
+def test_gelu_textbook_values():
+    # GELU(z) = z * Phi(z); Phi(1) = 0.8413447460685429, Phi(-1) = 0.15865525393145707
+    assert om.gelu(np.array(0.0)) == 0.0
+    assert abs(om.gelu(np.array(1.0)) - 0.8413447460685429) < 1e-15
+    assert abs(om.gelu(np.array(-1.0)) + 0.15865525393145707) < 1e-15
+    assert abs(om.gelu(np.array(8.0)) - 8.0) < 1e-12
+    assert abs(om.gelu(np.array(-8.0))) < 1e-12
+    assert abs(om.gelu_grad(np.array(0.0)) - 0.5) < 1e-15
+    # derivative at 1: Phi(1) + phi(1), phi(1) = exp(-1/2)/sqrt(2 pi) = 0.24197072451914337
+    assert abs(om.gelu_grad(np.array(1.0)) - (0.8413447460685429 + 0.24197072451914337)) < 1e-15
+
+
+def test_attention_causal_special_cases():
+    rng = np.random.default_rng(6)
+    S, dh = 6, 4
+    v = rng.standard_normal((1, 1, S, dh))
+    q = np.zeros((1, 1, S, dh))
+    k = rng.standard_normal((1, 1, S, dh))
+    o, p = om.causal_attention(q, k, v)
+    # zero queries: uniform weights over the visible prefix j <= i
+    for i in range(S):
+        assert np.allclose(o[0, 0, i], v[0, 0, :i + 1].mean(axis=0), atol=1e-14)
+    # the first position sees only itself
+    q2 = rng.standard_normal((1, 1, S, dh))
+    o2, p2 = om.causal_attention(q2, k, v)
+    assert np.allclose(o2[0, 0, 0], v[0, 0, 0], atol=1e-14)
+    assert np.allclose(np.triu(p2[0, 0], 1), 0.0)
+    # scale 1/sqrt(dh): two visible keys with score gap g give weights 1/(1+e^{-g/sqrt(dh)})
+    qa = np.zeros((1, 1, 2, dh)); qa[0, 0, 1, 0] = 3.0
+    ka = np.zeros((1, 1, 2, dh)); ka[0, 0, 1, 0] = 1.0
+    _, pa = om.causal_attention(qa, ka, v[:, :, :2])
+    w1 = 1.0 / (1.0 + math.exp(-3.0 / math.sqrt(dh)))
+    assert abs(pa[0, 0, 1, 1] - w1) < 1e-14
+
+
+def test_attention_future_tokens_do_not_leak():
+    w = TINY_LM.replace(n=1)
+    params = _random_params(w, 7)
+    tok = np.array([[1, 2, 3, 4, 5]])
+    tok2 = tok.copy(); tok2[0, 3] = 9
+    p = {k: np.asarray(v, dtype=np.float64) for k, v in params.items()}
+    outs = []
+    for t in (tok, tok2):
+        x = p["emb"][t]
+        for l in range(w.L):
+            x, _ = om.block_forward(1, p, f"l{l}.", x, w.heads)
+        outs.append(x)
+    assert np.array_equal(outs[0][0, :3], outs[1][0, :3])
+    assert not np.allclose(outs[0][0, 3:], outs[1][0, 3:])
+
+
+def test_linear_layout_out_by_in():
+    """Weights are stored [out, in]: a single 1 at W[o, i] copies input column i to output o."""
+    x = np.arange(12.0).reshape(3, 4)
+    W = np.zeros((5, 4)); W[2, 1] = 1.0
+    y = om.linear(x, W)
+    assert y.shape == (3, 5)
+    assert np.array_equal(y[:, 2], x[:, 1]) and np.count_nonzero(y[:, [0, 1, 3, 4]]) == 0
+
+
+def test_cross_entropy_special_cases():
+    V, n, s = 13, 2, 4
+    tok = np.array([[1, 2, 3, 4], [5, 6, 7, 8]])
+    z = np.zeros((n, s, V))
+    loss, dz, per = om.next_token_ce(z, tok, n * (s - 1))
+    assert abs(loss - math.log(V)) < 1e-14
+    assert np.allclose(dz.sum(axis=-1), 0.0, atol=1e-15)
+    assert np.all(dz[:, -1] == 0.0)                          # last position predicts nothing
+    # a confident correct prediction has loss log(1 + (V-1) e^{-c})
+    z2 = np.zeros((n, s, V))
+    for b in range(n):
+        for t in range(s - 1):
+            z2[b, t, tok[b, t + 1]] = 20.0
+    loss2, _, _ = om.next_token_ce(z2, tok, n * (s - 1))
+    assert abs(loss2 - math.log1p((V - 1) * math.exp(-20.0))) < 1e-15
+
+
+def test_ffn_zero_weights_reduce_to_residual_and_mse():
+    w = TINY_FFN
+    params = {name: np.zeros(shape) for name, shape, _ in param_specs(w)}
+    for l in range(w.L):
+        params[f"l{l}.ln_g"] = np.ones(w.d)
+        params[f"l{l}.b2"] = np.full(w.d, 0.25)
+    batch = _batch(w, 8)
+    loss, _ = om.forward_loss(w, params, batch)
+    y = batch["x"] + 0.25 * w.L
+    assert abs(loss - ((y - batch["targets"]) ** 2).mean()) < 1e-14
+
+
+def test_rmsprop_first_step_closed_form():
+    """From v = 0: v = (1-rho) g^2 and dw = -lr g / (sqrt(1-rho)|g| + eps)."""
+    g = np.array([1e-3, -2.0, 0.0, 5e-9, -7e-5])
+    params = {"a": np.ones(5)}
+    new_p, new_v = om.rmsprop(params, {"a": g}, {"a": np.zeros(5)}, lr=1e-3, decay=0.9, eps=1e-8)
+    dw = new_p["a"] - 1.0
+    expect = -1e-3 * g / (math.sqrt(0.1) * np.abs(g) + 1e-8)
+    assert np.allclose(dw, expect, rtol=1e-12, atol=0)
+    assert dw[2] == 0.0
+    assert abs(dw[1] - 1e-3 / math.sqrt(0.1)) < 1e-10   # g < 0: about +3.1623e-3 when |g| >> eps
+    assert np.allclose(new_v["a"], 0.1 * g * g, rtol=1e-15)
+    # second step uses the decayed state
+    new_p2, new_v2 = om.rmsprop(new_p, {"a": g}, new_v, lr=1e-3, decay=0.9, eps=1e-8)
+    assert np.allclose(new_v2["a"], 0.9 * 0.1 * g * g + 0.1 * g * g, rtol=1e-15)
+
+
+def test_step_loss_near_log_vocab_at_init():
+    """At the init (matrices N(0,1/d), LN gains 1) logits are O(1): loss ~ ln V."""
+    from synth import make_inputs
+    w = TINY_LM.replace(d=64, heads=1, ffn=128, vocab=50, seq=8, n=4)
+    inp = make_inputs(w)
+    loss, _ = om.forward_loss(w, inp["params"], inp)
+    assert abs(loss - math.log(50)) < 1.5
