@@ -1,0 +1,192 @@
+/*
+ * gpipe.h - C ABI of libgpipe: one synchronous GPipe training step on one GPU.
+ *
+ * Method: "GPipe technical review" (zzz0906.github.io, a review of Huang et
+ * al., "GPipe: Easy Scaling with Micro-Batch Pipeline Parallelism").
+ *   - Interface ("GPipe algorithm: minimal interface"): the user gives K (cells),
+ *     M (micro-batches) and a sequence of L layers, each with a forward, its
+ *     parameters and an optional cost estimate c_i.  GPipe cuts the layers into
+ *     K cells of consecutive layers, minimising the variance of the per-cell
+ *     summed cost.
+ *   - Step ("Pipeline flow", phases 1-3): the mini-batch of N samples is split
+ *     into M micro-batches; forward keeps only each cell's input (the
+ *     activations at cell boundaries); backward re-computes a cell's forward
+ *     before differentiating it; per-micro-batch gradients are accumulated and
+ *     applied once, after all M micro-batches.
+ *   - Bubble ("Bubble overhead analysis"): (K-1)/(M+K-1).
+ *   - Memory ("Preliminaries 5: re-materialisation"): peak activation memory
+ *     O(N + (L/K)(N/M)) instead of O(N L).
+ * Here all K cells run on one GPU, in the schedule's order, on one stream.
+ *
+ * Conventions for every function:
+ *   - Return value: 0 (GPIPE_OK) or a negative GPIPE_ERR_* code; the message of
+ *     the last failure is available from gpipe_last_error(ctx).
+ *   - Device pointers are CUDA device addresses owned by the caller; the
+ *     library never allocates device memory for them, never frees them and
+ *     keeps no pointer after the call returns (except inside a cached CUDA
+ *     graph, which is re-captured whenever any pointer changes).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is stream-ordered; only functions with a host output that depends on
+ *     device results (loss_out) synchronise the stream.
+ *   - No function is thread-safe on the same context.
+ */
+#ifndef GPIPE_H
+#define GPIPE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gpipe_ctx gpipe_ctx;  /* opaque, host-side, owned by the library */
+
+enum {
+  GPIPE_OK = 0,
+  GPIPE_ERR_INVALID_ARG = -1,     /* bad shape/argument; nothing was launched          */
+  GPIPE_ERR_NOT_PARTITIONED = -2, /* reserved: create always partitions                */
+  GPIPE_ERR_CUDA = -3,            /* a CUDA runtime/driver call failed                 */
+  GPIPE_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait gave up (error flag)   */
+  GPIPE_ERR_NONFINITE_LOSS = -5,  /* the step's loss is NaN or Inf                     */
+  GPIPE_ERR_UNSUPPORTED = -6      /* valid request this build does not implement       */
+};
+
+enum { GPIPE_KIND_FFN = 0, GPIPE_KIND_LM = 1 };
+enum { GPIPE_DTYPE_F32 = 0, GPIPE_DTYPE_BF16 = 1 };
+
+/* Layer dimensions shared by all L identical layers.
+ *   kind 0: y = x + W2 GELU(W1 LN(x) + b1) + b2, MSE loss on fp32 targets.
+ *   kind 1: pre-LN Transformer block (causal multi-head attention with head
+ *           width d/heads = 64, GELU FFN), final LN, tied-embedding head,
+ *           next-token cross-entropy over N(seq-1) targets.
+ * dtype 0: everything fp32 (kind 0 only).  dtype 1: bf16 GEMM/attention
+ * operands and activations with fp32 accumulation; fp32 master weights,
+ * gradients and RMSProp state.
+ * RMSProp: v = decay v + (1-decay) g^2;  w -= lr g / (sqrt(v) + eps).      */
+typedef struct {
+  int kind;
+  int d, heads, ffn, seq, vocab; /* seq = 1 and vocab = 0 for kind 0          */
+  int n;                         /* mini-batch N (sequences, or rows for kind 0) */
+  int dtype;
+  float lr, decay, eps;
+} gpipe_dims;
+
+/* Create a context for L layers cut into K cells and M micro-batches.
+ * cost: L per-layer cost estimates c_i (>= 1), or NULL for the layer's FLOPs.
+ * Validates 1 <= K <= L, M >= 1, N % M == 0; kind 1: d % 64 == 0,
+ * d/heads == 64, seq % 64 == 0, ffn % 64 == 0; kind 0: d % 8 == 0,
+ * ffn % 8 == 0; then partitions.
+ * On failure *out is NULL and the return code says why; gpipe_last_error(NULL)
+ * returns this thread's last message. */
+int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims,
+                 const int64_t* cost);
+
+/* Cell bounds of the variance-minimising partition ("minimal interface"):
+ * bounds_out[0] = 0 < bounds_out[1] < ... < bounds_out[K] = L; cell k holds
+ * layers [bounds_out[k], bounds_out[k+1]).  Exact integer objective
+ * (sum of squared cell costs); ties go to the lexicographically smallest
+ * bounds.  bounds_out: host array of K+1 int32. */
+int gpipe_partition(gpipe_ctx* ctx, int32_t* bounds_out);
+
+/* Parameter count and workspace bytes the caller must allocate.
+ * Parameter packing (same element offsets in every per-parameter buffer):
+ *   per layer l = 0..L-1, kind 1: ln1_g[d] ln1_b[d] w_qkv[3d,d] b_qkv[3d]
+ *     w_o[d,d] b_o[d] ln2_g[d] ln2_b[d] w1[ffn,d] b1[ffn] w2[d,ffn] b2[d];
+ *   kind 0: ln_g[d] ln_b[d] w1[ffn,d] b1[ffn] w2[d,ffn] b2[d];
+ *   then (kind 1) lnf_g[d] lnf_b[d] emb[vocab,d].
+ * Matrices are [out, in] row-major (a projection computes x W^T).  w_qkv stacks
+ * the query, key and value rows; head h owns rows h*64..h*64+63 of each.
+ * Either output pointer may be NULL. */
+int gpipe_sizes(const gpipe_ctx* ctx, size_t* param_elems, size_t* workspace_bytes);
+
+/* Write the bf16 compute copy of the fp32 master weights (dtype 1; a no-op for
+ * dtype 0).  Call once before the first step; every step's update rewrites it. */
+int gpipe_init_params(gpipe_ctx* ctx, const float* params_fp32, void* params_bf16, void* stream);
+
+/* One synchronous training step (forward of all M micro-batches through all K
+ * cells keeping only cell inputs, backward with re-computation and fp32
+ * gradient accumulation, then one RMSProp update of every parameter).
+ *   params_fp32 [P] fp32 master weights (updated in place)
+ *   params_bf16 [P] bf16 compute copy (dtype 1; rewritten by the update;
+ *               ignored and may be NULL for dtype 0)
+ *   grads_fp32  [P] fp32 gradient accumulator; must be all zero on entry; the
+ *               update leaves it zero again (unless GPIPE_OPT_KEEP_GRADS)
+ *   rms_v_fp32  [P] fp32 RMSProp state (zero before the first step)
+ *   batch_in    kind 1: int32 token ids [N, seq]; kind 0: fp32 x [N, d]
+ *   targets     kind 1: NULL (next-token targets come from batch_in);
+ *               kind 0: fp32 targets [N, d]
+ *   workspace   device buffer of gpipe_sizes' workspace_bytes, 256-B aligned;
+ *               holds the boundary stash, one cell's re-computed internals and
+ *               all scratch.  Its contents need no initialisation.
+ *   loss_out    host float* or NULL.  When non-NULL the stream is synchronised,
+ *               the device error flag is checked and the mean loss is written.
+ * The step is captured into a CUDA graph on first use (per pointer set) and
+ * replayed afterwards unless GPIPE_OPT_GRAPH is 0. */
+int gpipe_step(gpipe_ctx* ctx, float* params_fp32, void* params_bf16, float* grads_fp32,
+               float* rms_v_fp32, const void* batch_in, const void* targets,
+               void* workspace, void* stream, float* loss_out);
+
+/* (K-1)/(M+K-1), the review's bubble fraction for the context's K and M. */
+double gpipe_bubble_fraction(const gpipe_ctx* ctx);
+
+/* Discrete-event model of the GPipe clock on K devices for this context's K,
+ * M: t_f[k], t_b[k] are per-cell forward/backward times of one micro-batch
+ * (host arrays of K doubles, or NULL for the partition's cell costs with
+ * t_b = 2 t_f).  Outputs (any may be NULL): makespan, bubble fraction. */
+int gpipe_schedule_model(const gpipe_ctx* ctx, const double* t_f, const double* t_b,
+                         double* makespan, double* bubble);
+
+/* Activation memory of the step as laid out in the workspace (bytes):
+ *   peak_act_bytes    the workspace's activation high-water mark (boundary
+ *                     stash + the re-computed cell's internals + head + the
+ *                     gradients in flight); all of it is live at the peak;
+ *   model_bound_bytes the review's bound O(N + (L/K)(N/M)) with explicit
+ *                     constants: (K+1) T d e  +  Lc (T/M) a  +  (T/M) h,
+ *                     T = tokens per step, e = activation element bytes,
+ *                     Lc = largest cell's layer count, a = bytes one layer
+ *                     keeps per token, h = per-token head/gradient bytes.
+ * Either output may be NULL. */
+int gpipe_memory_report(const gpipe_ctx* ctx, size_t* peak_act_bytes, size_t* model_bound_bytes);
+
+/* Options (defaults in brackets). */
+enum {
+  GPIPE_OPT_KEEP_GRADS = 1,  /* [0] 1: the update does not zero the gradients       */
+  GPIPE_OPT_GRAPH = 2,       /* [1] 0: launch kernels directly, no CUDA graph        */
+  GPIPE_OPT_NO_REMAT = 3,    /* [0] 1: keep every layer's internals, no re-computing;
+                                set before gpipe_sizes (changes the workspace)       */
+  GPIPE_OPT_REMAT_CHECK = 4, /* [-1] m >= 0: keep micro-batch m's first-forward
+                                internals of every cell and count the bytes that
+                                differ from the re-computed ones
+                                (gpipe_debug_counters); set before gpipe_sizes       */
+  GPIPE_OPT_SKIP_UPDATE = 5  /* [0] 1: accumulate gradients but apply no update      */
+};
+int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
+
+/* Debug read-back after a step (synchronises `stream`):
+ *   remat_mismatch_bytes: bytes of re-computed internals that differ from the
+ *                         first forward (GPIPE_OPT_REMAT_CHECK), else 0;
+ *   error_flag:           the device error flag (0 = none); reading clears it. */
+int gpipe_debug_counters(gpipe_ctx* ctx, void* workspace, void* stream,
+                         uint64_t* remat_mismatch_bytes, int* error_flag);
+
+/* Per-target losses of the last step, copied to host (synchronises `stream`):
+ * kind 1: rows [N*seq] (row n*seq+t is the loss of predicting token t+1 of
+ * sequence n, 0 for t = seq-1), already divided by N(seq-1); kind 0: rows [N]
+ * (sum over the row of (y-t)^2 / (N d)).  host_out holds `count` floats. */
+int gpipe_loss_rows(gpipe_ctx* ctx, void* workspace, void* stream, float* host_out, size_t count);
+
+/* Number of kernels one step launches. */
+int64_t gpipe_launches_per_step(const gpipe_ctx* ctx);
+
+/* Message of the last failure on ctx (or of this thread's last failure when
+ * ctx is NULL).  Never NULL. */
+const char* gpipe_last_error(const gpipe_ctx* ctx);
+
+/* Destroy the context and its cached graph.  NULL-safe. */
+void gpipe_destroy(gpipe_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPIPE_H */

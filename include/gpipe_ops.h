@@ -1,0 +1,129 @@
+/*
+ * gpipe_ops.h - kernel-level entry points of libgpipe.
+ *
+ * Each call enqueues the kernel(s) of one operation of the GPipe step on
+ * `stream` (a cudaStream_t passed as void*; NULL = legacy default stream) and
+ * returns 0 or a negative GPIPE_ERR_* code from gpipe.h without launching on
+ * invalid arguments.  All pointers are caller-owned device addresses unless
+ * stated; nothing is allocated or freed.  They exist so that every kernel the
+ * step uses can be checked on its own; gpipe_step calls the same launchers.
+ * The operations are the pieces of the step of "GPipe technical review"
+ * (zzz0906.github.io), section "Pipeline flow": the layers' forward and
+ * backward, the loss, the gradient accumulation and the RMSProp update
+ * ("Preliminaries 2: the memory wall").
+ *
+ * dtype: 0 = fp32 operands/activations, 1 = bf16 operands/activations (fp32
+ * accumulation and fp32 statistics in both cases).
+ */
+#ifndef GPIPE_OPS_H
+#define GPIPE_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  GPIPE_EPI_STORE = 0,     /* C = acc (+ bias[n]) (+ resid[m,n])                  */
+  GPIPE_EPI_BIAS_GELU = 1, /* C = z = acc + bias[n];  C2 = GELU(z)  (exact erf)    */
+  GPIPE_EPI_GELU_BWD = 2,  /* C = acc * GELU'(aux[m,n])                              */
+  GPIPE_EPI_ACC_F32 = 3,   /* C (fp32) += acc                                        */
+  GPIPE_EPI_STORE_F32 = 4  /* C (fp32) = acc                                         */
+};
+
+/* C[m,n] = epilogue( sum_k A(m,k) B(n,k) ), 0 <= m < M, 0 <= n < N.
+ * A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m];
+ * B(n,k) = B[n*ldb + k] when b_kmajor, else B[k*ldb + n].
+ * So x W^T (W [out,in]) is (a_kmajor=1, b_kmajor=1); dY W is (1, 0); the weight
+ * gradient dY^T X is (0, 0).  C, C2, resid and aux are row-major with leading
+ * dimension ldc (C, C2), ldr (resid), ldaux (aux); element type = dtype except
+ * for the fp32 epilogues.  bias is fp32 [N] or NULL; resid may be NULL.
+ * dtype 1 runs the tcgen05/TMEM tensor-core kernel fed by TMA and needs every
+ * leading dimension a multiple of 8 elements and 16-byte aligned bases; it is
+ * built for (1,1) with STORE, BIAS_GELU, STORE_F32, ACC_F32; (1,0) with STORE,
+ * GELU_BWD, ACC_F32; (0,0) with STORE, ACC_F32 (others: GPIPE_ERR_UNSUPPORTED).
+ * dtype 0 runs an fp32 FFMA kernel (any layout and epilogue).
+ * Requires M, N, K >= 1. */
+int gpipe_op_gemm(int dtype, int M, int N, int K,
+                  const void* A, int64_t lda, int a_kmajor,
+                  const void* B, int64_t ldb, int b_kmajor,
+                  int epi, void* C, int64_t ldc,
+                  const float* bias, const void* resid, int64_t ldr,
+                  void* C2, const void* aux, int64_t ldaux, void* stream);
+
+/* Bytes of fp32 scratch the two-stage column reductions below need. */
+size_t gpipe_op_scratch_bytes(int rows, int cols);
+
+/* LayerNorm over rows of width d (eps 1e-5, biased variance):
+ * y = (x - mean) * rstd * g + b; mean and rstd (fp32 [rows]) are saved.
+ * d must be a multiple of 8 and at most 2048. */
+int gpipe_op_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g,
+                           const float* b, void* y, float* mean, float* rstd, void* stream);
+
+/* LayerNorm backward: dx = rstd (g dy - mean(g dy) - xhat mean(g dy xhat)) + dres
+ * (dres may be NULL); dg_acc += sum_rows dy xhat and db_acc += sum_rows dy,
+ * accumulated in a fixed order (two stages through `scratch`, of
+ * gpipe_op_scratch_bytes(rows, 2*d) bytes). */
+int gpipe_op_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x,
+                           const float* mean, const float* rstd, const float* g,
+                           const void* dres, void* dx, float* dg_acc, float* db_acc,
+                           float* scratch, void* stream);
+
+/* out_acc[c] += sum_r y[r*ldy + c] in a fixed order (bias gradients); scratch
+ * of gpipe_op_scratch_bytes(rows, cols) bytes. cols % 8 == 0, ldy % 8 == 0. */
+int gpipe_op_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy,
+                    float* out_acc, float* scratch, void* stream);
+
+/* Causal multi-head attention forward, bf16, head width 64, scale 1/8.
+ * qkv [nseq*seq, 3*heads*64] (query | key | value column blocks), output
+ * o [nseq*seq, heads*64], lse [nseq*seq, heads] fp32 natural-log
+ * log-sum-exp of the scaled scores.  seq % 64 == 0. */
+int gpipe_op_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o,
+                           float* lse, void* stream);
+
+/* Backward: dqkv [nseq*seq, 3*heads*64] gets dQ | dK | dV.  dvec is fp32
+ * scratch [nseq*seq, heads] (rowsum(dO o O)).  No atomics: dQ and dK/dV are
+ * produced by separate kernels, so results are bit-reproducible. */
+int gpipe_op_attention_bwd(int nseq, int seq, int heads, const void* qkv, const void* o,
+                           const void* dout, const float* lse, float* dvec, void* dqkv,
+                           void* stream);
+
+/* Next-token softmax cross-entropy on fp32 logits [rows, vocab].
+ * Row r is token row0 + r of the mini-batch (tokens [N*seq] int32); its target
+ * is tokens[row0 + r + 1] unless (row0 + r) % seq == seq - 1 (no target).
+ * loss_rows[r] = (lse - z_target) * inv_count (0 without target).
+ * want_grad: writes dz = (softmax - onehot) * inv_count as bf16 IN PLACE over
+ * the logits, row r at bf16 offset r * 2 * vocab (so the gradient matrix has
+ * leading dimension 2*vocab bf16 elements).  vocab % 4 == 0. */
+int gpipe_op_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, int row0,
+                           float inv_count, float* logits, float* loss_rows, int want_grad,
+                           void* stream);
+
+/* MSE rows: loss_rows[r] = sum_j (y - t)^2 * inv_count; dy = 2 (y - t) inv_count. */
+int gpipe_op_mse(int rows, int d, const float* y, const float* t, float inv_count,
+                 float* loss_rows, float* dy, void* stream);
+
+/* x[r,:] = emb[tokens[r],:] (bf16 rows of width d, d % 8 == 0). */
+int gpipe_op_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb_bf16,
+                           void* x, void* stream);
+
+/* demb[tokens[r],:] += dx[r,:] (fp32 accumulator, bf16 dx).  Deterministic: each
+ * embedding row is owned by one CTA, which adds its tokens in ascending r. */
+int gpipe_op_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens,
+                           const void* dx_bf16, float* demb, void* stream);
+
+/* RMSProp over n parameters: v = decay v + (1-decay) g^2; w -= lr g/(sqrt(v)+eps);
+ * w_bf16 (may be NULL) receives the round-to-nearest-even bf16 copy of w;
+ * zero_grad != 0 sets g = 0 afterwards. */
+int gpipe_op_rmsprop(size_t n, float* w, float* g, float* v, void* w_bf16, float lr,
+                     float decay, float eps, int zero_grad, void* stream);
+
+/* dst[i] = bf16(src[i]) (round to nearest even). */
+int gpipe_op_cast_bf16(size_t n, const float* src, void* dst, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPIPE_OPS_H */

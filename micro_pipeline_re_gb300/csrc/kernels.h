@@ -1,0 +1,86 @@
+// Host-side declarations of the kernel launchers (one per operation of the
+// step).  Every launcher validates its arguments, enqueues on `stream` and
+// returns 0 or a negative GPIPE_ERR_* code, recording a message with
+// set_error().  The step executor and the gpipe_op_* entry points call these.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gp {
+
+enum { DT_F32 = 0, DT_BF16 = 1 };
+enum { EPI_STORE = 0, EPI_BIAS_GELU = 1, EPI_GELU_BWD = 2, EPI_ACC_F32 = 3, EPI_STORE_F32 = 4 };
+
+// Error reporting (thread-local message; see launch.cu).
+int set_error(int code, const char* fmt, ...);
+const char* last_error_message();
+
+// Counts kernel launches made through the launchers (host side).
+void count_launch(int n = 1);
+int64_t launch_count();
+
+struct GemmDesc {
+  int dtype = DT_BF16;
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr;
+  int64_t lda = 0;
+  bool a_kmajor = true;
+  const void* B = nullptr;
+  int64_t ldb = 0;
+  bool b_kmajor = true;
+  int epi = EPI_STORE;
+  void* C = nullptr;
+  int64_t ldc = 0;
+  const float* bias = nullptr;
+  const void* resid = nullptr;
+  int64_t ldr = 0;
+  void* C2 = nullptr;
+  const void* aux = nullptr;
+  int64_t ldaux = 0;
+};
+
+int launch_gemm(const GemmDesc& g, cudaStream_t stream);       // dispatch by dtype
+int launch_gemm_tc(const GemmDesc& g, cudaStream_t stream);    // bf16, tcgen05 + TMA
+int launch_gemm_simt(const GemmDesc& g, cudaStream_t stream);  // fp32 or bf16, FFMA
+
+size_t colred_scratch_floats(int rows, int cols);
+
+int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
+                         float* mean, float* rstd, cudaStream_t stream);
+int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                         const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
+                         float* db_acc, float* scratch, cudaStream_t stream);
+int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, float* out_acc, float* scratch,
+                  cudaStream_t stream);
+
+int launch_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o, float* lse, cudaStream_t stream);
+int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const void* o, const void* dout,
+                         const float* lse, float* dvec, void* dqkv, cudaStream_t stream);
+
+int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, int row0, float inv_count,
+                         float* logits, float* loss_rows, int want_grad, cudaStream_t stream);
+int launch_mse(int rows, int d, const float* y, const float* t, float inv_count, float* loss_rows, float* dy,
+               cudaStream_t stream);
+
+int launch_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb_bf16, void* x,
+                         cudaStream_t stream);
+int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx_bf16, float* demb,
+                         cudaStream_t stream);
+
+int launch_rmsprop(size_t n, float* w, float* g, float* v, void* w_bf16, float lr, float decay, float eps,
+                   int zero_grad, cudaStream_t stream);
+int launch_cast_bf16(size_t n, const float* src, void* dst, cudaStream_t stream);
+
+// Deterministic sum of n floats into *out (one block, fixed order, fp64 partials).
+int launch_sum(const float* x, size_t n, float* out, cudaStream_t stream);
+// Copy n bytes (device to device) with a kernel.
+int launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+// counter[0] += number of bytes that differ between a and b.
+int launch_count_diff(const void* a, const void* b, size_t bytes, unsigned long long* counter,
+                      cudaStream_t stream);
+
+// Number of SMs of the current device (cached).
+int num_sms();
+
+}  // namespace gp
