@@ -1,0 +1,578 @@
+// Memory-bound kernels of the step: LayerNorm forward/backward, column sums
+// (bias gradients), next-token cross-entropy, MSE, embedding gather/scatter,
+// the fused RMSProp update and small utilities.  All reductions run in a fixed
+// order (no floating-point atomics), so every result is bit-reproducible and
+// a re-computed forward equals the first one byte for byte.
+#include <algorithm>
+
+#include "../../include/gpipe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gp {
+namespace {
+
+constexpr float kLnEps = 1e-5f;
+constexpr int kMaxChunks = 4;       // d <= 4 * 256 = 1024 per warp-row
+constexpr int kLnRowsPerWarp = 8;   // rows one warp folds into one partial row
+constexpr int kColRowsPerChunk = 32;
+
+inline int blocks_for(size_t n, int per_block) { return static_cast<int>((n + per_block - 1) / per_block); }
+
+int check_launch(const char* what) {
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  return GPIPE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// LayerNorm forward: one warp per row; lane owns 8-wide column groups
+// (c*32 + lane)*8 for chunk c.  Two passes over registers (mean, then
+// centred variance), fp32 statistics.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, const float* __restrict__ g,
+                                                     const float* __restrict__ b, T* __restrict__ y,
+                                                     float* __restrict__ mean, float* __restrict__ rstd, int rows,
+                                                     int d) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  if (row >= rows) return;
+  const T* xr = x + (int64_t)row * d;
+  float v[kMaxChunks][8];
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int col = (c * 32 + lane) * 8;
+    if (col < d) {
+      load8(xr + col, v[c]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s += v[c][j];
+    }
+  }
+  const float mu = warp_sum(s) / d;
+  float q = 0.f;
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int col = (c * 32 + lane) * 8;
+    if (col < d) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float t = v[c][j] - mu;
+        q += t * t;
+      }
+    }
+  }
+  const float var = warp_sum(q) / d;
+  const float rs = 1.0f / sqrtf(var + kLnEps);
+  T* yr = y + (int64_t)row * d;
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int col = (c * 32 + lane) * 8;
+    if (col < d) {
+      float gg[8], bb[8], o[8];
+      load8(g + col, gg);
+      load8(b + col, bb);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = (v[c][j] - mu) * rs * gg[j] + bb[j];
+      store8(yr + col, o);
+    }
+  }
+  if (lane == 0) {
+    mean[row] = mu;
+    rstd[row] = rs;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// LayerNorm backward.  Warp w of block b handles rows
+// (b*4 + w)*R .. +R-1 (R = kLnRowsPerWarp) and writes one partial row of
+// [dg | db] sums into scratch; col_reduce then adds the partial rows in order.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(128) ln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+                                                     const float* __restrict__ mean, const float* __restrict__ rstd,
+                                                     const float* __restrict__ g, const T* __restrict__ dres,
+                                                     T* __restrict__ dx, float* __restrict__ partial, int rows,
+                                                     int d) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pw = blockIdx.x * 4 + warp;  // partial row index
+  const int r0 = pw * kLnRowsPerWarp;
+  float pg[kMaxChunks][8], pb[kMaxChunks][8];
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pg[c][j] = pb[c][j] = 0.f;
+  for (int r = r0; r < min(r0 + kLnRowsPerWarp, rows); ++r) {
+    const float mu = mean[r], rs = rstd[r];
+    float xh[kMaxChunks][8], gd[kMaxChunks][8];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      const int col = (c * 32 + lane) * 8;
+      if (col < d) {
+        float xv[8], dv[8], gg[8];
+        load8(x + (int64_t)r * d + col, xv);
+        load8(dy + (int64_t)r * d + col, dv);
+        load8(g + col, gg);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          xh[c][j] = (xv[j] - mu) * rs;
+          gd[c][j] = gg[j] * dv[j];
+          s1 += gd[c][j];
+          s2 += gd[c][j] * xh[c][j];
+          pg[c][j] += dv[j] * xh[c][j];
+          pb[c][j] += dv[j];
+        }
+      }
+    }
+    const float m1 = warp_sum(s1) / d, m2 = warp_sum(s2) / d;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      const int col = (c * 32 + lane) * 8;
+      if (col < d) {
+        float o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = rs * (gd[c][j] - m1 - xh[c][j] * m2);
+        if (dres) {
+          float rv[8];
+          load8(dres + (int64_t)r * d + col, rv);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) o[j] += rv[j];
+        }
+        store8(dx + (int64_t)r * d + col, o);
+      }
+    }
+  }
+  if (r0 < rows) {
+    float* pr = partial + (int64_t)pw * 2 * d;
+#pragma unroll
+    for (int c = 0; c < kMaxChunks; ++c) {
+      const int col = (c * 32 + lane) * 8;
+      if (col < d) {
+        store8(pr + col, pg[c]);
+        store8(pr + d + col, pb[c]);
+      }
+    }
+  }
+}
+
+// out[c] += sum_{p < nparts} partial[p*ncols + c], fixed order (4 interleaved
+// accumulators combined in a fixed pattern).  Columns < split go to out_a,
+// the rest to out_b.
+__global__ void col_reduce_kernel(const float* __restrict__ partial, int nparts, int ncols, float* out_a,
+                                  int split, float* out_b) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= ncols) return;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int p = 0;
+  for (; p + 4 <= nparts; p += 4) {
+    a0 += partial[(int64_t)p * ncols + c];
+    a1 += partial[(int64_t)(p + 1) * ncols + c];
+    a2 += partial[(int64_t)(p + 2) * ncols + c];
+    a3 += partial[(int64_t)(p + 3) * ncols + c];
+  }
+  for (; p < nparts; ++p) a0 += partial[(int64_t)p * ncols + c];
+  const float s = (a0 + a1) + (a2 + a3);
+  if (c < split) out_a[c] += s;
+  else out_b[c - split] += s;
+}
+
+// Column sums of a [rows, cols] matrix: block (x, y) sums rows
+// y*kColRowsPerChunk.. of columns x*2048 + 8*tid .. +7 into partial row y.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict__ y, int64_t ldy, int rows,
+                                                             int cols, float* __restrict__ partial) {
+  const int col = (blockIdx.x * 256 + threadIdx.x) * 8;
+  if (col >= cols) return;
+  const int r0 = blockIdx.y * kColRowsPerChunk;
+  const int r1 = min(r0 + kColRowsPerChunk, rows);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int r = r0; r < r1; ++r) {
+    float v[8];
+    load8(y + (int64_t)r * ldy + col, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] += v[j];
+  }
+  store8(partial + (int64_t)blockIdx.y * cols + col, acc);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax cross-entropy on fp32 logits, one CTA (512 threads) per row.
+// ---------------------------------------------------------------------------
+constexpr int kCeThreads = 512;
+
+__global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logits, int vocab, int seq,
+                                                        const int32_t* __restrict__ tokens, int row0,
+                                                        float inv_count, float* __restrict__ loss_rows,
+                                                        int want_grad) {
+  __shared__ float sm_m[kCeThreads / 32], sm_s[kCeThreads / 32];
+  __shared__ float sh_lse;
+  const int r = blockIdx.x;
+  const int gidx = row0 + r;
+  const bool has_t = (gidx % seq) != seq - 1;
+  const int tgt = has_t ? tokens[gidx + 1] : -1;
+  float* z = logits + (int64_t)r * vocab;
+  const float4* z4 = reinterpret_cast<const float4*>(z);
+  const int n4 = vocab / 4;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // pass 1: running max and rescaled sum of exp
+  float m = -INFINITY, s = 0.f;
+  for (int i = tid; i < n4; i += kCeThreads) {
+    const float4 v = z4[i];
+    const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    if (mx > m) {
+      s *= expf(m - mx);
+      m = mx;
+    }
+    s += expf(v.x - m) + expf(v.y - m) + expf(v.z - m) + expf(v.w - m);
+  }
+  // warp combine
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, s, o);
+    const float nm = fmaxf(m, om);
+    s = (m == -INFINITY ? 0.f : s * expf(m - nm)) + (om == -INFINITY ? 0.f : os * expf(om - nm));
+    m = nm;
+  }
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_s[warp] = s;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float M = sm_m[0], S = sm_s[0];
+    for (int w = 1; w < kCeThreads / 32; ++w) {
+      const float nm = fmaxf(M, sm_m[w]);
+      S = S * expf(M - nm) + sm_s[w] * expf(sm_m[w] - nm);
+      M = nm;
+    }
+    const float lse = M + logf(S);
+    sh_lse = lse;
+    loss_rows[r] = has_t ? (lse - z[tgt]) * inv_count : 0.f;
+  }
+  __syncthreads();
+  if (!want_grad) return;
+  const float lse = sh_lse;
+  const float scale = has_t ? inv_count : 0.f;
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(z);
+  // pass 2: dz written in place.  Chunk c reads floats [4*512c, 4*512(c+1))
+  // and then writes bf16 elements of the same indices, i.e. floats
+  // [2*512c, 2*512(c+1)), all of which every thread has already read.
+  for (int base = 0; base < n4; base += kCeThreads) {
+    const int i = base + tid;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < n4) v = z4[i];
+    __syncthreads();
+    if (i < n4) {
+      float p[4] = {expf(v.x - lse) * scale, expf(v.y - lse) * scale, expf(v.z - lse) * scale,
+                    expf(v.w - lse) * scale};
+      const int c0 = 4 * i;
+      if (tgt >= c0 && tgt < c0 + 4) p[tgt - c0] -= scale;
+      uint2 u;
+      u.x = pack_bf16x2(p[0], p[1]);
+      u.y = pack_bf16x2(p[2], p[3]);
+      *reinterpret_cast<uint2*>(dz + c0) = u;
+    }
+  }
+}
+
+// MSE: one warp per row.
+__global__ void mse_kernel(const float* __restrict__ y, const float* __restrict__ t, int rows, int d,
+                           float inv_count, float* __restrict__ loss_rows, float* __restrict__ dy) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  if (r >= rows) return;
+  float s = 0.f;
+  for (int c = lane; c < d; c += 32) {
+    const float e = y[(int64_t)r * d + c] - t[(int64_t)r * d + c];
+    s += e * e;
+    dy[(int64_t)r * d + c] = 2.0f * e * inv_count;
+  }
+  s = warp_sum(s);
+  if (lane == 0) loss_rows[r] = s * inv_count;
+}
+
+// ---------------------------------------------------------------------------
+// Embedding
+// ---------------------------------------------------------------------------
+__global__ void embed_fwd_kernel(int rows, int d, const int32_t* __restrict__ tokens,
+                                 const __nv_bfloat16* __restrict__ emb, __nv_bfloat16* __restrict__ x) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element group
+  const int groups = d / 8;
+  if (i >= (int64_t)rows * groups) return;
+  const int r = static_cast<int>(i / groups), c = static_cast<int>(i % groups) * 8;
+  *reinterpret_cast<uint4*>(x + (int64_t)r * d + c) =
+      *reinterpret_cast<const uint4*>(emb + (int64_t)tokens[r] * d + c);
+}
+
+// CTA b owns embedding rows [b*vpc, (b+1)*vpc).  It scans the token list in
+// order, compacts the positions whose token it owns (order kept), and adds
+// each such dx row into its own embedding rows: one owner per row and a fixed
+// order, hence no atomics and a deterministic result.
+__global__ void __launch_bounds__(256) embed_bwd_kernel(int rows, int d, int vocab, int vpc,
+                                                        const int32_t* __restrict__ tokens,
+                                                        const __nv_bfloat16* __restrict__ dx,
+                                                        float* __restrict__ demb) {
+  __shared__ int list[256];
+  __shared__ int wcount[8];
+  const int v0 = blockIdx.x * vpc, v1 = min(v0 + vpc, vocab);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int base = 0; base < rows; base += 256) {
+    const int r = base + tid;
+    const int t = r < rows ? tokens[r] : -1;
+    const bool mine = t >= v0 && t < v1;
+    const unsigned bal = __ballot_sync(0xffffffffu, mine);
+    if (lane == 0) wcount[warp] = __popc(bal);
+    __syncthreads();
+    int off = 0, total = 0;
+    for (int w = 0; w < 8; ++w) {
+      if (w < warp) off += wcount[w];
+      total += wcount[w];
+    }
+    if (mine) list[off + __popc(bal & ((1u << lane) - 1u))] = r;
+    __syncthreads();
+    for (int i = 0; i < total; ++i) {
+      const int rr = list[i];
+      const int64_t vrow = tokens[rr];
+      for (int c = tid * 8; c < d; c += 256 * 8) {
+        float a[8], g[8];
+        load8(demb + vrow * d + c, a);
+        load8(dx + (int64_t)rr * d + c, g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] += g[j];
+        store8(demb + vrow * d + c, a);
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RMSProp, float4-vectorised, grid-stride; tail handled element-wise.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void rms_one(float& w, float& g, float& v, float lr, float decay, float omd, float eps) {
+  v = decay * v + omd * (g * g);
+  w = w - lr * g / (sqrtf(v) + eps);
+}
+
+__global__ void rmsprop_kernel(float* __restrict__ w, float* __restrict__ g, float* __restrict__ v,
+                               __nv_bfloat16* __restrict__ wb, size_t n, float lr, float decay, float eps,
+                               int zero_grad) {
+  const float omd = 1.0f - decay;
+  const size_t n4 = n / 4;
+  float4* w4 = reinterpret_cast<float4*>(w);
+  float4* g4 = reinterpret_cast<float4*>(g);
+  float4* v4 = reinterpret_cast<float4*>(v);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 W = w4[i], G = g4[i], V = v4[i];
+    rms_one(W.x, G.x, V.x, lr, decay, omd, eps);
+    rms_one(W.y, G.y, V.y, lr, decay, omd, eps);
+    rms_one(W.z, G.z, V.z, lr, decay, omd, eps);
+    rms_one(W.w, G.w, V.w, lr, decay, omd, eps);
+    w4[i] = W;
+    v4[i] = V;
+    if (zero_grad) g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (wb) {
+      uint2 u;
+      u.x = pack_bf16x2(W.x, W.y);
+      u.y = pack_bf16x2(W.z, W.w);
+      *reinterpret_cast<uint2*>(wb + 4 * i) = u;
+    }
+  }
+  if (blockIdx.x == 0) {
+    for (size_t i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) {
+      float W = w[i], G = g[i], V = v[i];
+      rms_one(W, G, V, lr, decay, omd, eps);
+      w[i] = W;
+      v[i] = V;
+      if (zero_grad) g[i] = 0.f;
+      if (wb) wb[i] = f2bf(W);
+    }
+  }
+}
+
+__global__ void cast_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, size_t n) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = f2bf(src[i]);
+}
+
+// One block of 1024 threads: fixed-order fp64 partial sums, fixed tree.
+__global__ void __launch_bounds__(1024) sum_kernel(const float* __restrict__ x, size_t n, float* out) {
+  __shared__ double sm[1024];
+  double s = 0.0;
+  for (size_t i = threadIdx.x; i < n; i += 1024) s += static_cast<double>(x[i]);
+  sm[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 512; o > 0; o >>= 1) {
+    if (threadIdx.x < o) sm[threadIdx.x] += sm[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = static_cast<float>(sm[0]);
+}
+
+__global__ void copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, size_t n16) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) dst[i] = src[i];
+}
+
+__global__ void count_diff_kernel(const uint32_t* __restrict__ a, const uint32_t* __restrict__ b, size_t n4,
+                                  unsigned long long* counter) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  unsigned int c = 0;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const uint32_t x = a[i] ^ b[i];
+    c += ((x & 0xffu) != 0) + ((x & 0xff00u) != 0) + ((x & 0xff0000u) != 0) + ((x & 0xff000000u) != 0);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0 && c) atomicAdd(counter, static_cast<unsigned long long>(c));
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+size_t colred_scratch_floats(int rows, int cols) {
+  const size_t parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
+  return parts * static_cast<size_t>(cols);
+}
+
+int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
+                         float* mean, float* rstd, cudaStream_t s) {
+  if (rows < 1 || d < 8 || d % 8 || d > 32 * 8 * kMaxChunks)
+    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm: need rows >= 1, d %% 8 == 0, 8 <= d <= 1024");
+  if (!al16(x) || !al16(y) || !al16(g) || !al16(b))
+    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm: pointers must be 16-B aligned");
+  const int grid = blocks_for(rows, 8);
+  if (dtype == DT_F32)
+    ln_fwd_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), g, b, static_cast<float*>(y), mean,
+                                              rstd, rows, d);
+  else
+    ln_fwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), g, b,
+                                                      static_cast<__nv_bfloat16*>(y), mean, rstd, rows, d);
+  return check_launch("layernorm_fwd");
+}
+
+int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                         const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
+                         float* db_acc, float* scratch, cudaStream_t s) {
+  if (rows < 1 || d < 8 || d % 8 || d > 32 * 8 * kMaxChunks)
+    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: need rows >= 1, d %% 8 == 0, 8 <= d <= 1024");
+  if (!al16(dy) || !al16(x) || !al16(dx) || !al16(g) || (dres && !al16(dres)) || !al16(scratch))
+    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: pointers must be 16-B aligned");
+  const int parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
+  const int grid = (parts + 3) / 4;
+  if (dtype == DT_F32)
+    ln_bwd_kernel<float><<<grid, 128, 0, s>>>(static_cast<const float*>(dy), static_cast<const float*>(x), mean,
+                                              rstd, g, static_cast<const float*>(dres), static_cast<float*>(dx),
+                                              scratch, rows, d);
+  else
+    ln_bwd_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean, rstd, g,
+        static_cast<const __nv_bfloat16*>(dres), static_cast<__nv_bfloat16*>(dx), scratch, rows, d);
+  int rc = check_launch("layernorm_bwd");
+  if (rc) return rc;
+  col_reduce_kernel<<<blocks_for(2 * d, 256), 256, 0, s>>>(scratch, parts, 2 * d, dg_acc, d, db_acc);
+  return check_launch("layernorm_bwd reduce");
+}
+
+int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, float* out_acc, float* scratch,
+                  cudaStream_t s) {
+  if (rows < 1 || cols < 8 || cols % 8 || ldy % 8 || ldy < cols)
+    return set_error(GPIPE_ERR_INVALID_ARG, "colsum: need rows >= 1, cols %% 8 == 0, ldy %% 8 == 0, ldy >= cols");
+  if (!al16(y) || !al16(scratch)) return set_error(GPIPE_ERR_INVALID_ARG, "colsum: pointers must be 16-B aligned");
+  const int chunks = (rows + kColRowsPerChunk - 1) / kColRowsPerChunk;
+  dim3 grid(blocks_for(cols, 256 * 8), chunks);
+  if (dtype == DT_F32)
+    colsum_partial_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(y), ldy, rows, cols, scratch);
+  else
+    colsum_partial_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(y), ldy, rows,
+                                                              cols, scratch);
+  int rc = check_launch("colsum");
+  if (rc) return rc;
+  col_reduce_kernel<<<blocks_for(cols, 256), 256, 0, s>>>(scratch, chunks, cols, out_acc, cols, nullptr);
+  return check_launch("colsum reduce");
+}
+
+int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, int row0, float inv_count,
+                         float* logits, float* loss_rows, int want_grad, cudaStream_t s) {
+  if (rows < 1 || vocab < 4 || vocab % 4 || seq < 1 || row0 < 0)
+    return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: need rows >= 1, vocab %% 4 == 0, seq >= 1");
+  if (!al16(logits)) return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: logits must be 16-B aligned");
+  ce_kernel<<<rows, kCeThreads, 0, s>>>(logits, vocab, seq, tokens, row0, inv_count, loss_rows, want_grad);
+  return check_launch("cross_entropy");
+}
+
+int launch_mse(int rows, int d, const float* y, const float* t, float inv_count, float* loss_rows, float* dy,
+               cudaStream_t s) {
+  if (rows < 1 || d < 1) return set_error(GPIPE_ERR_INVALID_ARG, "mse: need rows, d >= 1");
+  mse_kernel<<<blocks_for(rows, 8), 256, 0, s>>>(y, t, rows, d, inv_count, loss_rows, dy);
+  return check_launch("mse");
+}
+
+int launch_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb, void* x, cudaStream_t s) {
+  if (rows < 1 || d < 8 || d % 8 || !al16(emb) || !al16(x))
+    return set_error(GPIPE_ERR_INVALID_ARG, "embedding_fwd: need d %% 8 == 0 and 16-B aligned rows");
+  const int64_t n = (int64_t)rows * (d / 8);
+  embed_fwd_kernel<<<blocks_for(n, 256), 256, 0, s>>>(rows, d, tokens, static_cast<const __nv_bfloat16*>(emb),
+                                                      static_cast<__nv_bfloat16*>(x));
+  return check_launch("embedding_fwd");
+}
+
+int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx, float* demb,
+                         cudaStream_t s) {
+  if (rows < 1 || d < 8 || d % 8 || vocab < 1 || !al16(dx) || !al16(demb))
+    return set_error(GPIPE_ERR_INVALID_ARG, "embedding_bwd: need d %% 8 == 0 and 16-B aligned rows");
+  int ctas = 4 * num_sms();
+  const int vpc = (vocab + ctas - 1) / ctas;
+  ctas = (vocab + vpc - 1) / vpc;
+  embed_bwd_kernel<<<ctas, 256, 0, s>>>(rows, d, vocab, vpc, tokens, static_cast<const __nv_bfloat16*>(dx), demb);
+  return check_launch("embedding_bwd");
+}
+
+int launch_rmsprop(size_t n, float* w, float* g, float* v, void* wb, float lr, float decay, float eps,
+                   int zero_grad, cudaStream_t s) {
+  if (n == 0) return GPIPE_OK;
+  if (!al16(w) || !al16(g) || !al16(v) || (wb && (reinterpret_cast<uintptr_t>(wb) & 7u)))
+    return set_error(GPIPE_ERR_INVALID_ARG, "rmsprop: w, g, v must be 16-B aligned, w_bf16 8-B aligned");
+  const int grid = std::min<int64_t>(blocks_for(n / 4 + 1, 256), (int64_t)num_sms() * 8);
+  rmsprop_kernel<<<grid, 256, 0, s>>>(w, g, v, static_cast<__nv_bfloat16*>(wb), n, lr, decay, eps, zero_grad);
+  return check_launch("rmsprop");
+}
+
+int launch_cast_bf16(size_t n, const float* src, void* dst, cudaStream_t s) {
+  if (n == 0) return GPIPE_OK;
+  const int grid = std::min<int64_t>(blocks_for(n, 256), (int64_t)num_sms() * 8);
+  cast_bf16_kernel<<<grid, 256, 0, s>>>(src, static_cast<__nv_bfloat16*>(dst), n);
+  return check_launch("cast_bf16");
+}
+
+int launch_sum(const float* x, size_t n, float* out, cudaStream_t s) {
+  sum_kernel<<<1, 1024, 0, s>>>(x, n, out);
+  return check_launch("sum");
+}
+
+int launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+  if (bytes % 16 || !al16(dst) || !al16(src))
+    return set_error(GPIPE_ERR_INVALID_ARG, "copy: 16-B aligned buffers and sizes required");
+  if (bytes == 0) return GPIPE_OK;
+  const int grid = std::min<int64_t>(blocks_for(bytes / 16, 256), (int64_t)num_sms() * 8);
+  copy_kernel<<<grid, 256, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), bytes / 16);
+  return check_launch("copy");
+}
+
+int launch_count_diff(const void* a, const void* b, size_t bytes, unsigned long long* counter, cudaStream_t s) {
+  if (bytes % 4) return set_error(GPIPE_ERR_INVALID_ARG, "count_diff: size must be a multiple of 4");
+  if (bytes == 0) return GPIPE_OK;
+  const int grid = std::min<int64_t>(blocks_for(bytes / 4, 256), (int64_t)num_sms() * 8);
+  count_diff_kernel<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(a), static_cast<const uint32_t*>(b),
+                                         bytes / 4, counter);
+  return check_launch("count_diff");
+}
+
+}  // namespace gp

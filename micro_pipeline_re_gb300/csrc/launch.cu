@@ -1,0 +1,156 @@
+// Library-wide launch plumbing (error messages, the device error word, the
+// launch counter, SM count) and the gpipe_op_* kernel-level C entry points.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/gpipe.h"
+#include "../../include/gpipe_ops.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gp {
+
+namespace {
+thread_local std::string g_last_error = "no error";
+int64_t g_launches = 0;
+__device__ int g_device_error = 0;
+}  // namespace
+
+int set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+const char* last_error_message() { return g_last_error.c_str(); }
+
+void count_launch(int n) { g_launches += n; }
+int64_t launch_count() { return g_launches; }
+
+int* device_error_ptr() {
+  // One address per device; this library drives the current device only.
+  static int dev_cached = -1;
+  static int* ptr = nullptr;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != dev_cached) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptr = static_cast<int*>(p);
+    dev_cached = dev;
+  }
+  return ptr;
+}
+
+int num_sms() {
+  static int dev_cached = -1;
+  static int sms = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != dev_cached) {
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+    dev_cached = dev;
+  }
+  return sms;
+}
+
+}  // namespace gp
+
+using gp::set_error;
+
+extern "C" {
+
+int gpipe_op_gemm(int dtype, int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
+                  int64_t ldb, int b_kmajor, int epi, void* C, int64_t ldc, const float* bias, const void* resid,
+                  int64_t ldr, void* C2, const void* aux, int64_t ldaux, void* stream) {
+  gp::GemmDesc g;
+  g.dtype = dtype;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.A = A;
+  g.lda = lda;
+  g.a_kmajor = a_kmajor != 0;
+  g.B = B;
+  g.ldb = ldb;
+  g.b_kmajor = b_kmajor != 0;
+  g.epi = epi;
+  g.C = C;
+  g.ldc = ldc;
+  g.bias = bias;
+  g.resid = resid;
+  g.ldr = ldr;
+  g.C2 = C2;
+  g.aux = aux;
+  g.ldaux = ldaux;
+  return gp::launch_gemm(g, static_cast<cudaStream_t>(stream));
+}
+
+size_t gpipe_op_scratch_bytes(int rows, int cols) {
+  if (rows < 1 || cols < 1) return 0;
+  return gp::colred_scratch_floats(rows, cols) * sizeof(float);
+}
+
+int gpipe_op_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
+                           float* mean, float* rstd, void* stream) {
+  return gp::launch_layernorm_fwd(dtype, rows, d, x, g, b, y, mean, rstd, static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                           const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
+                           float* db_acc, float* scratch, void* stream) {
+  return gp::launch_layernorm_bwd(dtype, rows, d, dy, x, mean, rstd, g, dres, dx, dg_acc, db_acc, scratch,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, float* out_acc, float* scratch,
+                    void* stream) {
+  return gp::launch_colsum(dtype, rows, cols, y, ldy, out_acc, scratch, static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o, float* lse, void* stream) {
+  return gp::launch_attention_fwd(nseq, seq, heads, qkv, o, lse, static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_attention_bwd(int nseq, int seq, int heads, const void* qkv, const void* o, const void* dout,
+                           const float* lse, float* dvec, void* dqkv, void* stream) {
+  return gp::launch_attention_bwd(nseq, seq, heads, qkv, o, dout, lse, dvec, dqkv,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, int row0, float inv_count,
+                           float* logits, float* loss_rows, int want_grad, void* stream) {
+  return gp::launch_cross_entropy(rows, vocab, seq, tokens, row0, inv_count, logits, loss_rows, want_grad,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_mse(int rows, int d, const float* y, const float* t, float inv_count, float* loss_rows, float* dy,
+                 void* stream) {
+  return gp::launch_mse(rows, d, y, t, inv_count, loss_rows, dy, static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb_bf16, void* x, void* stream) {
+  return gp::launch_embedding_fwd(rows, d, tokens, emb_bf16, x, static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx_bf16, float* demb,
+                           void* stream) {
+  return gp::launch_embedding_bwd(rows, d, vocab, tokens, dx_bf16, demb, static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_rmsprop(size_t n, float* w, float* g, float* v, void* w_bf16, float lr, float decay, float eps,
+                     int zero_grad, void* stream) {
+  return gp::launch_rmsprop(n, w, g, v, w_bf16, lr, decay, eps, zero_grad, static_cast<cudaStream_t>(stream));
+}
+
+int gpipe_op_cast_bf16(size_t n, const float* src, void* dst, void* stream) {
+  return gp::launch_cast_bf16(n, src, dst, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
