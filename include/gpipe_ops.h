@@ -96,7 +96,8 @@ int gpipe_op_attention_bwd(int nseq, int seq, int heads, const void* qkv, const 
  * loss_rows[r] = (lse - z_target) * inv_count (0 without target).
  * want_grad: writes dz = (softmax - onehot) * inv_count as bf16 IN PLACE over
  * the logits, row r at bf16 offset r * 2 * vocab (so the gradient matrix has
- * leading dimension 2*vocab bf16 elements).  vocab % 4 == 0. */
+ * leading dimension 2*vocab bf16 elements).  vocab % 4 == 0.  A target id
+ * outside [0, vocab) is treated as "no target" and sets the device error flag. */
 int gpipe_op_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, int row0,
                            float inv_count, float* logits, float* loss_rows, int want_grad,
                            void* stream);
@@ -105,8 +106,10 @@ int gpipe_op_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, 
 int gpipe_op_mse(int rows, int d, const float* y, const float* t, float inv_count,
                  float* loss_rows, float* dy, void* stream);
 
-/* x[r,:] = emb[tokens[r],:] (bf16 rows of width d, d % 8 == 0). */
-int gpipe_op_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb_bf16,
+/* x[r,:] = emb[tokens[r],:] (bf16 rows of width d, d % 8 == 0, vocab rows).
+ * A token id outside [0, vocab) gives a zero row and sets the device error
+ * flag (read by gpipe_debug_counters) instead of reading out of bounds. */
+int gpipe_op_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb_bf16,
                            void* x, void* stream);
 
 /* demb[tokens[r],:] += dx[r,:] (fp32 accumulator, bf16 dx).  Deterministic: each

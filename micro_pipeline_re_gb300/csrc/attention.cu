@@ -436,6 +436,20 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
+int prepare_attention() {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e1 = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(DqSmem));
+    cudaError_t e2 = cudaFuncSetAttribute(attn_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(DkvSmem));
+    if (e1 != cudaSuccess || e2 != cudaSuccess)
+      return set_error(GPIPE_ERR_CUDA, "attention_bwd: shared-memory attribute failed");
+    attr_set = true;
+  }
+  return GPIPE_OK;
+}
+
 int launch_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o, float* lse, cudaStream_t s) {
   if (nseq < 1 || seq < BQ || seq % BQ || heads < 1 || heads > 65535)
     return set_error(GPIPE_ERR_INVALID_ARG, "attention: need nseq >= 1, seq %% 64 == 0, heads >= 1");
@@ -455,16 +469,8 @@ int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const vo
     return set_error(GPIPE_ERR_INVALID_ARG, "attention: need nseq >= 1, seq %% 64 == 0, heads >= 1");
   if (!al16(qkv) || !al16(o) || !al16(dout) || !al16(dqkv))
     return set_error(GPIPE_ERR_INVALID_ARG, "attention: pointers must be 16-B aligned");
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e1 = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(DqSmem));
-    cudaError_t e2 = cudaFuncSetAttribute(attn_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(DkvSmem));
-    if (e1 != cudaSuccess || e2 != cudaSuccess)
-      return set_error(GPIPE_ERR_CUDA, "attention_bwd: shared-memory attribute failed");
-    attr_set = true;
-  }
+  int rc = prepare_attention();
+  if (rc) return rc;
   dim3 grid(seq / BQ, heads, nseq);
   attn_bwd_dq_kernel<<<grid, 128, sizeof(DqSmem), s>>>(static_cast<const __nv_bfloat16*>(qkv),
                                           static_cast<const __nv_bfloat16*>(o),

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 namespace gp {
 
 // ---------------------------------------------------------------------------
@@ -16,11 +18,9 @@ enum DeviceError : int {
   DERR_TMA_WAIT = 1,   // producer waited too long for a free stage
   DERR_MMA_WAIT = 2,   // MMA issuer waited too long for a filled stage
   DERR_ACC_WAIT = 3,   // epilogue waited too long for the accumulator
-  DERR_DRAIN_WAIT = 4  // exit-time wait for in-flight copies gave up
+  DERR_DRAIN_WAIT = 4, // exit-time wait for in-flight copies gave up
+  DERR_BAD_TOKEN = 5   // a token id outside [0, vocab) (the read is skipped)
 };
-
-// Device address of the library's error word (defined in launch.cu).
-int* device_error_ptr();
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 

@@ -206,13 +206,17 @@ constexpr int kCeThreads = 512;
 __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logits, int vocab, int seq,
                                                         const int32_t* __restrict__ tokens, int row0,
                                                         float inv_count, float* __restrict__ loss_rows,
-                                                        int want_grad) {
+                                                        int want_grad, int* err) {
   __shared__ float sm_m[kCeThreads / 32], sm_s[kCeThreads / 32];
   __shared__ float sh_lse;
   const int r = blockIdx.x;
   const int gidx = row0 + r;
   const bool has_t = (gidx % seq) != seq - 1;
-  const int tgt = has_t ? tokens[gidx + 1] : -1;
+  int tgt = has_t ? tokens[gidx + 1] : -1;
+  if (tgt >= vocab || (has_t && tgt < 0)) {  // invalid id: no target, flag it
+    if (threadIdx.x == 0) atomicExch(err, DERR_BAD_TOKEN);
+    tgt = -1;
+  }
   float* z = logits + (int64_t)r * vocab;
   const float4* z4 = reinterpret_cast<const float4*>(z);
   const int n4 = vocab / 4;
@@ -252,12 +256,12 @@ __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logi
     }
     const float lse = M + logf(S);
     sh_lse = lse;
-    loss_rows[r] = has_t ? (lse - z[tgt]) * inv_count : 0.f;
+    loss_rows[r] = tgt >= 0 ? (lse - z[tgt]) * inv_count : 0.f;
   }
   __syncthreads();
   if (!want_grad) return;
   const float lse = sh_lse;
-  const float scale = has_t ? inv_count : 0.f;
+  const float scale = tgt >= 0 ? inv_count : 0.f;
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(z);
   // pass 2: dz written in place.  Chunk c reads floats [4*512c, 4*512(c+1))
   // and then writes bf16 elements of the same indices, i.e. floats
@@ -299,14 +303,19 @@ __global__ void mse_kernel(const float* __restrict__ y, const float* __restrict_
 // ---------------------------------------------------------------------------
 // Embedding
 // ---------------------------------------------------------------------------
-__global__ void embed_fwd_kernel(int rows, int d, const int32_t* __restrict__ tokens,
-                                 const __nv_bfloat16* __restrict__ emb, __nv_bfloat16* __restrict__ x) {
+__global__ void embed_fwd_kernel(int rows, int d, int vocab, const int32_t* __restrict__ tokens,
+                                 const __nv_bfloat16* __restrict__ emb, __nv_bfloat16* __restrict__ x, int* err) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element group
   const int groups = d / 8;
   if (i >= (int64_t)rows * groups) return;
   const int r = static_cast<int>(i / groups), c = static_cast<int>(i % groups) * 8;
-  *reinterpret_cast<uint4*>(x + (int64_t)r * d + c) =
-      *reinterpret_cast<const uint4*>(emb + (int64_t)tokens[r] * d + c);
+  const int tok = tokens[r];
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (tok >= 0 && tok < vocab)
+    v = *reinterpret_cast<const uint4*>(emb + (int64_t)tok * d + c);
+  else if (c == 0)
+    atomicExch(err, DERR_BAD_TOKEN);
+  *reinterpret_cast<uint4*>(x + (int64_t)r * d + c) = v;
 }
 
 // CTA b owns embedding rows [b*vpc, (b+1)*vpc).  It scans the token list in
@@ -504,7 +513,8 @@ int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, in
   if (rows < 1 || vocab < 4 || vocab % 4 || seq < 1 || row0 < 0)
     return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: need rows >= 1, vocab %% 4 == 0, seq >= 1");
   if (!al16(logits)) return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: logits must be 16-B aligned");
-  ce_kernel<<<rows, kCeThreads, 0, s>>>(logits, vocab, seq, tokens, row0, inv_count, loss_rows, want_grad);
+  ce_kernel<<<rows, kCeThreads, 0, s>>>(logits, vocab, seq, tokens, row0, inv_count, loss_rows, want_grad,
+                                        device_error_ptr());
   return check_launch("cross_entropy");
 }
 
@@ -515,12 +525,14 @@ int launch_mse(int rows, int d, const float* y, const float* t, float inv_count,
   return check_launch("mse");
 }
 
-int launch_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb, void* x, cudaStream_t s) {
+int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb, void* x,
+                         cudaStream_t s) {
   if (rows < 1 || d < 8 || d % 8 || !al16(emb) || !al16(x))
     return set_error(GPIPE_ERR_INVALID_ARG, "embedding_fwd: need d %% 8 == 0 and 16-B aligned rows");
   const int64_t n = (int64_t)rows * (d / 8);
-  embed_fwd_kernel<<<blocks_for(n, 256), 256, 0, s>>>(rows, d, tokens, static_cast<const __nv_bfloat16*>(emb),
-                                                      static_cast<__nv_bfloat16*>(x));
+  embed_fwd_kernel<<<blocks_for(n, 256), 256, 0, s>>>(rows, d, vocab, tokens,
+                                                      static_cast<const __nv_bfloat16*>(emb),
+                                                      static_cast<__nv_bfloat16*>(x), device_error_ptr());
   return check_launch("embedding_fwd");
 }
 

@@ -193,19 +193,27 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, i
 }
 
 template <bool A_K, bool B_K, int BN, int EPI>
+int set_attr() {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_K, B_K, BN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
+    if (e != cudaSuccess) return set_error(-3, "gemm: smem attribute: %s", cudaGetErrorString(e));
+    attr_set = true;
+  }
+  return 0;
+}
+
+template <bool A_K, bool B_K, int BN, int EPI>
 int run(const GemmDesc& g, cudaStream_t stream) {
   using Cfg = TcCfg<BN>;
   CUtensorMap ta, tb;
   bool ok = A_K ? make_tmap(&ta, g.A, g.K, g.M, g.lda, BM) : make_tmap(&ta, g.A, g.M, g.K, g.lda, 64);
   ok = ok && (B_K ? make_tmap(&tb, g.B, g.K, g.N, g.ldb, BN) : make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64));
   if (!ok) return set_error(-3, "gemm: cuTensorMapEncodeTiled failed");
-  static bool attr_set = false;
+  int rc = set_attr<A_K, B_K, BN, EPI>();
+  if (rc) return rc;
   auto kern = tc_gemm_kernel<A_K, B_K, BN, EPI>;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-    if (e != cudaSuccess) return set_error(-3, "gemm: smem attribute: %s", cudaGetErrorString(e));
-    attr_set = true;
-  }
   EpiArgs ep{g.C, g.ldc, g.bias, g.resid, g.ldr, g.C2, g.aux, g.ldaux, g.M, g.N};
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
   kern<<<grid, 128, Cfg::SMEM, stream>>>(ta, tb, ep, g.K, device_error_ptr());
@@ -246,6 +254,21 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+int prepare_gemm_tc() {
+  if (!encode_fn()) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled entry point not found");
+  int rc = 0;
+  rc = rc ? rc : set_attr<true, true, 128, EPI_STORE>();
+  rc = rc ? rc : set_attr<true, true, 128, EPI_BIAS_GELU>();
+  rc = rc ? rc : set_attr<true, true, 128, EPI_STORE_F32>();
+  rc = rc ? rc : set_attr<true, true, 128, EPI_ACC_F32>();
+  rc = rc ? rc : set_attr<true, false, 128, EPI_STORE>();
+  rc = rc ? rc : set_attr<true, false, 128, EPI_GELU_BWD>();
+  rc = rc ? rc : set_attr<true, false, 128, EPI_ACC_F32>();
+  rc = rc ? rc : set_attr<false, false, 128, EPI_STORE>();
+  rc = rc ? rc : set_attr<false, false, 128, EPI_ACC_F32>();
+  return rc;
+}
 
 int launch_gemm_tc(const GemmDesc& g, cudaStream_t stream) {
   if (g.M < 1 || g.N < 1 || g.K < 1) return set_error(GPIPE_ERR_INVALID_ARG, "gemm: M, N, K must be >= 1");

@@ -1,0 +1,633 @@
+// Step executor and the gpipe_* C ABI.
+//
+// One synchronous GPipe step ("GPipe technical review", zzz0906.github.io,
+// "Pipeline flow", phases 1-3) with all K cells on one GPU and one stream:
+//   phase 1  for m in 0..M-1, for k in 0..K-1: cell k forwards micro-batch m
+//            from the stashed cell input stash[k][m] and writes its output to
+//            stash[k+1][m]; internals go to the shared cell slots and are
+//            overwritten by the next cell (re-materialisation keeps only the
+//            boundary activations).  The last cell also computes the loss.
+//   phase 2  for m in 0..M-1, for k in K-1..0: re-compute cell k's forward
+//            from stash[k][m] into the slots (the output of its last layer is
+//            not needed and is skipped), then differentiate it layer by layer
+//            in reverse; weight gradients are added into the fp32 gradient
+//            buffer straight from the GEMM epilogue (accumulation across
+//            micro-batches, no update in between).
+//   phase 3  one RMSProp update of every parameter (and the bf16 copy).
+// The whole sequence is captured once into a CUDA graph and replayed.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/gpipe.h"
+#include "kernels.h"
+#include "planner.h"
+
+namespace {
+
+using namespace gp;
+
+struct StepPtrs {
+  float* p32;
+  void* p16;
+  float* g32;
+  float* v32;
+  const void* batch;
+  const void* targets;
+  char* ws;
+};
+
+struct GraphKey {
+  StepPtrs p;
+  int64_t opts[8];
+  bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
+};
+
+}  // namespace
+
+struct gpipe_ctx {
+  int L = 0, K = 0, M = 0;
+  Dims dm{};
+  std::vector<int64_t> cost;
+  std::vector<int32_t> bounds;
+  int max_cell = 0;
+  ParamLayout pl;
+  Workspace ws;
+  bool ws_stale = true;
+  // options
+  bool keep_grads = false, use_graph = true, no_remat = false, skip_update = false;
+  int64_t remat_check_m = -1;
+  // state
+  std::string err = "no error";
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  cudaGraph_t graph = nullptr;
+  GraphKey key{};
+  bool have_key = false;
+  int64_t launches_per_step = 0;
+
+  size_t T() const { return static_cast<size_t>(dm.n) * (dm.kind == 1 ? dm.seq : 1); }
+  size_t Tmb() const { return T() / M; }
+  size_t es() const { return dm.dtype == 0 ? 4 : 2; }
+  int fail(int code, const std::string& msg) {
+    err = msg;
+    return code;
+  }
+  int fail_from_launch(int code) {
+    err = last_error_message();
+    return code;
+  }
+  void refresh_ws() {
+    if (ws_stale) {
+      ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat);
+      ws_stale = false;
+    }
+  }
+  void drop_graph() {
+    if (gexec) cudaGraphExecDestroy(gexec);
+    if (graph) cudaGraphDestroy(graph);
+    gexec = nullptr;
+    graph = nullptr;
+    have_key = false;
+  }
+};
+
+namespace {
+
+thread_local std::string g_create_error = "no error";
+
+#define TRY(expr)                          \
+  do {                                     \
+    int _rc = (expr);                      \
+    if (_rc != GPIPE_OK) return _rc;       \
+  } while (0)
+
+// Pointers of one layer's slot.
+struct Slot {
+  char *u, *qkv, *o, *h1, *u2, *z1, *g, *y;
+  float *mean1, *rstd1, *mean2, *rstd2, *lse;
+};
+
+class Executor {
+ public:
+  Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t s) : c_(c), p_(p), s_(s) {}
+
+  int run_step() {
+    const Workspace& w = c_->ws;
+    const int M = c_->M, K = c_->K;
+    // zero the loss scalar and the debug counter
+    if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, s_) != cudaSuccess)
+      return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
+    // phase 1: forward of every micro-batch through every cell
+    for (int m = 0; m < M; ++m) {
+      TRY(cell0_input(m));
+      for (int k = 0; k < K; ++k) TRY(cell_forward(k, m, /*recompute=*/false));
+      TRY(head(m, /*backward=*/false));
+    }
+    // phase 2: backward with re-computation, micro-batches ascending, cells K-1..0
+    for (int m = 0; m < M; ++m) {
+      char* dy = ws(w.g0);
+      char* dx = ws(w.g1);
+      for (int k = K - 1; k >= 0; --k) {
+        if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
+        if (k == K - 1) TRY(head_backward(m, dy));
+        const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
+        for (int j = n - 1; j >= 0; --j) {
+          const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
+          TRY(layer_backward(first + j, x, slot(k, m, j), dy, dx));
+          std::swap(dy, dx);
+        }
+        if (k == 0 && c_->dm.kind == 1)
+          TRY(launch_embedding_bwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), dy,
+                                   grad(c_->pl.emb), s_));
+      }
+    }
+    // phase 3: one update after all micro-batches
+    if (!c_->skip_update)
+      TRY(launch_rmsprop(c_->pl.total, p_.p32, p_.g32, p_.v32, c_->dm.dtype == 1 ? p_.p16 : nullptr, c_->dm.lr,
+                         c_->dm.decay, c_->dm.eps, c_->keep_grads ? 0 : 1, s_));
+    TRY(launch_sum(reinterpret_cast<float*>(ws(w.loss_rows)), c_->T(), reinterpret_cast<float*>(ws(w.misc)), s_));
+    return GPIPE_OK;
+  }
+
+ private:
+  gpipe_ctx* c_;
+  StepPtrs p_;
+  cudaStream_t s_;
+
+  char* ws(size_t off) const { return p_.ws + off; }
+  const float* p32(size_t off) const { return p_.p32 + off; }
+  float* grad(size_t off) const { return p_.g32 + off; }
+  // GEMM operand weights: the bf16 compute copy, or the fp32 master for dtype 0
+  const void* wgt(size_t off) const {
+    return c_->dm.dtype == 1 ? static_cast<const void*>(static_cast<const char*>(p_.p16) + off * 2)
+                             : static_cast<const void*>(p_.p32 + off);
+  }
+  const int32_t* tokens(int m) const {
+    return static_cast<const int32_t*>(p_.batch) + static_cast<size_t>(m) * c_->Tmb();
+  }
+  char* stash(int k, int m) const {
+    return ws(c_->ws.stash) + (static_cast<size_t>(k) * c_->M + m) * c_->ws.stash_bytes;
+  }
+  const void* cell_input(int k, int m) const {
+    if (k == 0 && c_->dm.kind == 0)
+      return static_cast<const char*>(p_.batch) + static_cast<size_t>(m) * c_->Tmb() * c_->dm.d * 4;
+    return stash(k, m);
+  }
+  Slot slot(int k, int m, int j) const {
+    size_t idx = c_->no_remat ? static_cast<size_t>(m) * c_->L + c_->bounds[k] + j : static_cast<size_t>(j);
+    char* b = ws(c_->ws.slots) + idx * c_->ws.slot_bytes;
+    const SlotLayout& s = c_->ws.slot;
+    Slot r;
+    r.u = b + s.u;
+    r.qkv = b + s.qkv;
+    r.o = b + s.o;
+    r.h1 = b + s.h1;
+    r.u2 = b + s.u2;
+    r.z1 = b + s.z1;
+    r.g = b + s.g;
+    r.y = b + s.y;
+    r.mean1 = reinterpret_cast<float*>(b + s.mean1);
+    r.rstd1 = reinterpret_cast<float*>(b + s.rstd1);
+    r.mean2 = reinterpret_cast<float*>(b + s.mean2);
+    r.rstd2 = reinterpret_cast<float*>(b + s.rstd2);
+    r.lse = reinterpret_cast<float*>(b + s.lse);
+    return r;
+  }
+
+  int gemm(int M, int N, int K, const void* A, int64_t lda, bool ak, const void* B, int64_t ldb, bool bk, int epi,
+           void* C, int64_t ldc, const float* bias = nullptr, const void* resid = nullptr, int64_t ldr = 0,
+           void* C2 = nullptr, const void* aux = nullptr, int64_t ldaux = 0) {
+    GemmDesc g;
+    g.dtype = c_->dm.dtype == 0 ? DT_F32 : DT_BF16;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.A = A;
+    g.lda = lda;
+    g.a_kmajor = ak;
+    g.B = B;
+    g.ldb = ldb;
+    g.b_kmajor = bk;
+    g.epi = epi;
+    g.C = C;
+    g.ldc = ldc;
+    g.bias = bias;
+    g.resid = resid;
+    g.ldr = ldr;
+    g.C2 = C2;
+    g.aux = aux;
+    g.ldaux = ldaux;
+    return launch_gemm(g, s_);
+  }
+
+  int cell0_input(int m) {
+    if (c_->dm.kind != 1) return GPIPE_OK;  // kind 0 reads the caller's x directly
+    return launch_embedding_fwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), wgt(c_->pl.emb),
+                                stash(0, m), s_);
+  }
+
+  // Forward of cell k for micro-batch m.  recompute: re-materialisation pass
+  // of the backward (the last layer's output projection is skipped since its
+  // result, the cell output, is not needed to differentiate the cell).
+  int cell_forward(int k, int m, bool recompute) {
+    const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
+    for (int j = 0; j < n; ++j) {
+      const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
+      void* out = j == n - 1 ? static_cast<void*>(stash(k + 1, m)) : static_cast<void*>(slot(k, m, j).y);
+      TRY(layer_forward(first + j, x, slot(k, m, j), out, recompute && j == n - 1));
+    }
+    if (c_->remat_check_m == m && !c_->no_remat) TRY(remat_check(k, n, recompute));
+    return GPIPE_OK;
+  }
+
+  // Debug: keep the first forward's internals of micro-batch m and count the
+  // bytes that the re-computation reproduces differently.
+  int remat_check(int k, int n, bool recompute) {
+    const Workspace& w = c_->ws;
+    char* saved = ws(w.check) + static_cast<size_t>(k) * c_->max_cell * w.slot_bytes;
+    for (int j = 0; j < n; ++j) {
+      char* sl = ws(w.slots) + static_cast<size_t>(j) * w.slot_bytes;
+      const size_t bytes = j == n - 1 ? w.slot.compare_bytes_last : w.slot_bytes;
+      if (!recompute)
+        TRY(launch_copy(saved + j * w.slot_bytes, sl, bytes, s_));
+      else
+        TRY(launch_count_diff(saved + j * w.slot_bytes, sl, bytes,
+                              reinterpret_cast<unsigned long long*>(ws(w.misc) + 8), s_));
+    }
+    return GPIPE_OK;
+  }
+
+  int layer_forward(int l, const void* x, const Slot& s, void* out, bool skip_out_proj) {
+    const Dims& dm = c_->dm;
+    const LayerOff& o = c_->pl.layers[l];
+    const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = dm.ffn;
+    const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
+    TRY(launch_layernorm_fwd(dt, T, d, x, p32(o.ln1_g), p32(o.ln1_b), s.u, s.mean1, s.rstd1, s_));
+    const void* ffn_in = s.u;
+    const void* resid2 = x;
+    if (dm.kind == 1) {
+      TRY(gemm(T, 3 * d, d, s.u, d, true, wgt(o.w_qkv), d, true, EPI_STORE, s.qkv, 3 * d, p32(o.b_qkv)));
+      TRY(launch_attention_fwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, s.lse, s_));
+      TRY(gemm(T, d, d, s.o, d, true, wgt(o.w_o), d, true, EPI_STORE, s.h1, d, p32(o.b_o), x, d));
+      TRY(launch_layernorm_fwd(dt, T, d, s.h1, p32(o.ln2_g), p32(o.ln2_b), s.u2, s.mean2, s.rstd2, s_));
+      ffn_in = s.u2;
+      resid2 = s.h1;
+    }
+    TRY(gemm(T, f, d, ffn_in, d, true, wgt(o.w1), d, true, EPI_BIAS_GELU, s.z1, f, p32(o.b1), nullptr, 0, s.g));
+    if (!skip_out_proj)
+      TRY(gemm(T, d, f, s.g, f, true, wgt(o.w2), f, true, EPI_STORE, out, d, p32(o.b2), resid2, d));
+    return GPIPE_OK;
+  }
+
+  // dy: gradient of the layer output; writes the gradient of its input to dx.
+  int layer_backward(int l, const void* x, const Slot& s, const void* dy, void* dx) {
+    const Dims& dm = c_->dm;
+    const LayerOff& o = c_->pl.layers[l];
+    const Workspace& w = c_->ws;
+    const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = dm.ffn;
+    const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
+    float* scratch = reinterpret_cast<float*>(ws(w.scratch));
+    char* gf = ws(w.gf);
+    char* gt = ws(w.gt);
+    const void* ffn_in = dm.kind == 1 ? static_cast<const void*>(s.u2) : static_cast<const void*>(s.u);
+    // FFN: y = r + W2 GELU(W1 u + b1) + b2
+    TRY(gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f));
+    TRY(launch_colsum(dt, T, d, dy, d, grad(o.b2), scratch, s_));
+    TRY(gemm(T, f, d, dy, d, true, wgt(o.w2), f, false, EPI_GELU_BWD, gf, f, nullptr, nullptr, 0, nullptr, s.z1, f));
+    TRY(gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d));
+    TRY(launch_colsum(dt, T, f, gf, f, grad(o.b1), scratch, s_));
+    TRY(gemm(T, d, f, gf, f, true, wgt(o.w1), d, false, EPI_STORE, gt, d));
+    if (dm.kind == 0) {
+      return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g),
+                                  grad(o.ln1_b), scratch, s_);
+    }
+    char* gh = ws(w.gh);
+    char* gq = ws(w.gq);
+    // h1 -> LN2: dh1 = LN2'(du2) + dy
+    TRY(launch_layernorm_bwd(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g),
+                             grad(o.ln2_b), scratch, s_));
+    // attention output projection
+    TRY(gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d));
+    TRY(launch_colsum(dt, T, d, gh, d, grad(o.b_o), scratch, s_));
+    TRY(gemm(T, d, d, gh, d, true, wgt(o.w_o), d, false, EPI_STORE, gt, d));
+    TRY(launch_attention_bwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, gt, s.lse, scratch, gq, s_));
+    TRY(gemm(3 * d, d, T, gq, 3 * d, false, s.u, d, false, EPI_ACC_F32, grad(o.w_qkv), d));
+    TRY(launch_colsum(dt, T, 3 * d, gq, 3 * d, grad(o.b_qkv), scratch, s_));
+    TRY(gemm(T, d, 3 * d, gq, 3 * d, true, wgt(o.w_qkv), d, false, EPI_STORE, gt, d));
+    return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh, dx, grad(o.ln1_g),
+                                grad(o.ln1_b), scratch, s_);
+  }
+
+  // Loss of micro-batch m from the last cell's output stash[K][m]; with
+  // backward, also writes the gradient of that output into dy.
+  int head(int m, bool backward, char* dy = nullptr) {
+    const Dims& dm = c_->dm;
+    const Workspace& w = c_->ws;
+    const int T = static_cast<int>(c_->Tmb()), d = dm.d;
+    float* loss_rows = reinterpret_cast<float*>(ws(w.loss_rows)) + static_cast<size_t>(m) * T;
+    const char* xf = stash(c_->K, m);
+    if (dm.kind == 0) {
+      const float inv = 1.0f / (static_cast<float>(dm.n) * d);
+      const float* t = static_cast<const float*>(p_.targets) + static_cast<size_t>(m) * T * d;
+      float* dyp = backward ? reinterpret_cast<float*>(dy) : reinterpret_cast<float*>(ws(w.g1));
+      return launch_mse(T, d, reinterpret_cast<const float*>(xf), t, inv, loss_rows, dyp, s_);
+    }
+    const float inv = 1.0f / (static_cast<float>(dm.n) * (dm.seq - 1));
+    float* logits = reinterpret_cast<float*>(ws(w.logits));
+    TRY(launch_layernorm_fwd(DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(w.hf),
+                             reinterpret_cast<float*>(ws(w.meanf)), reinterpret_cast<float*>(ws(w.rstdf)), s_));
+    TRY(gemm(T, dm.vocab, d, ws(w.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
+    TRY(launch_cross_entropy(T, dm.vocab, dm.seq, static_cast<const int32_t*>(p_.batch), m * T, inv, logits,
+                             loss_rows, backward ? 1 : 0, s_));
+    if (!backward) return GPIPE_OK;
+    // dz (bf16, in place over the logits, leading dimension 2*vocab)
+    const int64_t ldz = 2 * static_cast<int64_t>(dm.vocab);
+    char* gt = ws(w.gt);
+    TRY(gemm(T, d, dm.vocab, logits, ldz, true, wgt(c_->pl.emb), d, false, EPI_STORE, gt, d));
+    TRY(gemm(dm.vocab, d, T, logits, ldz, false, ws(w.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d));
+    return launch_layernorm_bwd(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(w.meanf)),
+                                reinterpret_cast<float*>(ws(w.rstdf)), p32(c_->pl.lnf_g), nullptr, dy,
+                                grad(c_->pl.lnf_g), grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(w.scratch)),
+                                s_);
+  }
+  int head_backward(int m, char* dy) { return head(m, true, dy); }
+};
+
+int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
+  if (!dm) return why = "dims is NULL", GPIPE_ERR_INVALID_ARG;
+  if (L < 1) return why = "L must be >= 1", GPIPE_ERR_INVALID_ARG;
+  if (K < 1 || K > L) return why = "need 1 <= K <= L", GPIPE_ERR_INVALID_ARG;
+  if (M < 1) return why = "M must be >= 1", GPIPE_ERR_INVALID_ARG;
+  if (dm->n < 1 || dm->n % M) return why = "N must be a positive multiple of M", GPIPE_ERR_INVALID_ARG;
+  if (!(dm->lr > 0) || !(dm->decay >= 0 && dm->decay < 1) || !(dm->eps > 0))
+    return why = "need lr > 0, 0 <= decay < 1, eps > 0", GPIPE_ERR_INVALID_ARG;
+  if (dm->kind == GPIPE_KIND_FFN) {
+    if (dm->dtype != GPIPE_DTYPE_F32) return why = "the FFN-block model runs in fp32 (dtype 0)", GPIPE_ERR_UNSUPPORTED;
+    if (dm->d < 8 || dm->d % 8 || dm->d > 1024 || dm->ffn < 8 || dm->ffn % 8)
+      return why = "kind 0 needs d % 8 == 0, 8 <= d <= 1024, ffn % 8 == 0", GPIPE_ERR_INVALID_ARG;
+    return GPIPE_OK;
+  }
+  if (dm->kind != GPIPE_KIND_LM) return why = "unknown kind", GPIPE_ERR_INVALID_ARG;
+  if (dm->dtype != GPIPE_DTYPE_BF16) return why = "the Transformer model runs in bf16 (dtype 1)", GPIPE_ERR_UNSUPPORTED;
+  if (dm->d < 64 || dm->d % 64 || dm->d > 1024 || dm->heads < 1 || dm->d / dm->heads != 64 || dm->d % dm->heads)
+    return why = "kind 1 needs d % 64 == 0, d <= 1024 and d/heads == 64", GPIPE_ERR_INVALID_ARG;
+  if (dm->seq < 64 || dm->seq % 64) return why = "seq must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
+  if (dm->ffn < 64 || dm->ffn % 64) return why = "ffn must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
+  if (dm->vocab < 64 || dm->vocab % 64) return why = "vocab must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
+  return GPIPE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims, const int64_t* cost) {
+  if (!out) {
+    g_create_error = "out is NULL";
+    return GPIPE_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  std::string why;
+  int rc = validate(L, K, M, dims, why);
+  if (rc) {
+    g_create_error = why;
+    set_error(rc, "%s", why.c_str());
+    return rc;
+  }
+  gpipe_ctx* c = new gpipe_ctx();
+  c->L = L;
+  c->K = K;
+  c->M = M;
+  c->dm = Dims{dims->kind, dims->d, dims->heads, dims->ffn, dims->seq, dims->vocab, dims->n, dims->dtype,
+               dims->lr, dims->decay, dims->eps};
+  // default cost: the layer's forward FLOPs per token (all layers identical)
+  const int64_t d = dims->d, f = dims->ffn;
+  const int64_t default_cost =
+      dims->kind == 1 ? 2 * (4 * d * d + 2 * d * f) + 2 * d * (dims->seq + 1) : 2 * (2 * d * f);
+  c->cost.resize(L);
+  for (int i = 0; i < L; ++i) {
+    c->cost[i] = cost ? cost[i] : default_cost;
+    if (c->cost[i] < 1) {
+      delete c;
+      g_create_error = "layer costs must be >= 1";
+      return GPIPE_ERR_INVALID_ARG;
+    }
+  }
+  if (!partition_min_variance(c->cost, K, c->bounds)) {
+    delete c;
+    g_create_error = "partition failed";
+    return GPIPE_ERR_INVALID_ARG;
+  }
+  c->max_cell = 0;
+  for (int k = 0; k < K; ++k) c->max_cell = std::max(c->max_cell, c->bounds[k + 1] - c->bounds[k]);
+  c->pl = make_param_layout(c->dm, L);
+  c->refresh_ws();
+  *out = c;
+  return GPIPE_OK;
+}
+
+int gpipe_partition(gpipe_ctx* c, int32_t* bounds_out) {
+  if (!c || !bounds_out) return GPIPE_ERR_INVALID_ARG;
+  std::copy(c->bounds.begin(), c->bounds.end(), bounds_out);
+  return GPIPE_OK;
+}
+
+int gpipe_sizes(const gpipe_ctx* cc, size_t* param_elems, size_t* workspace_bytes) {
+  if (!cc) return GPIPE_ERR_INVALID_ARG;
+  gpipe_ctx* c = const_cast<gpipe_ctx*>(cc);
+  c->refresh_ws();
+  if (param_elems) *param_elems = c->pl.total;
+  if (workspace_bytes) *workspace_bytes = c->ws.total;
+  return GPIPE_OK;
+}
+
+int gpipe_init_params(gpipe_ctx* c, const float* p32, void* p16, void* stream) {
+  if (!c) return GPIPE_ERR_INVALID_ARG;
+  if (c->dm.dtype != 1) return GPIPE_OK;
+  if (!p32 || !p16) return c->fail(GPIPE_ERR_INVALID_ARG, "NULL parameter buffer");
+  int rc = launch_cast_bf16(c->pl.total, p32, p16, static_cast<cudaStream_t>(stream));
+  return rc ? c->fail_from_launch(rc) : GPIPE_OK;
+}
+
+static int check_ptr(const void* p, const char* what, std::string& err) {
+  if (!p) {
+    err = std::string(what) + " is NULL";
+    return GPIPE_ERR_INVALID_ARG;
+  }
+  if (reinterpret_cast<uintptr_t>(p) & 15u) {
+    err = std::string(what) + " must be 16-byte aligned";
+    return GPIPE_ERR_INVALID_ARG;
+  }
+  return GPIPE_OK;
+}
+
+int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, const void* batch, const void* targets,
+               void* workspace, void* stream, float* loss_out) {
+  if (!c) return GPIPE_ERR_INVALID_ARG;
+  std::string e;
+  int rc = check_ptr(p32, "params_fp32", e);
+  if (!rc && c->dm.dtype == 1) rc = check_ptr(p16, "params_bf16", e);
+  if (!rc) rc = check_ptr(g32, "grads_fp32", e);
+  if (!rc) rc = check_ptr(v32, "rms_v_fp32", e);
+  if (!rc) rc = check_ptr(batch, "batch_in", e);
+  if (!rc && c->dm.kind == 0) rc = check_ptr(targets, "targets", e);
+  if (!rc) rc = check_ptr(workspace, "workspace", e);
+  if (rc) return c->fail(rc, e);
+  c->refresh_ws();
+  rc = prepare_kernels();
+  if (rc) return c->fail_from_launch(rc);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StepPtrs ptrs{p32, p16, g32, v32, batch, targets, static_cast<char*>(workspace)};
+  if (!c->use_graph) {
+    const int64_t before = launch_count();
+    Executor ex(c, ptrs, s);
+    rc = ex.run_step();
+    if (rc) return c->fail_from_launch(rc);
+    c->launches_per_step = launch_count() - before;
+  } else {
+    GraphKey key{};
+    key.p = ptrs;
+    key.opts[0] = c->keep_grads;
+    key.opts[1] = c->no_remat;
+    key.opts[2] = c->skip_update;
+    key.opts[3] = c->remat_check_m;
+    if (!c->have_key || !(key == c->key)) {
+      c->drop_graph();
+      if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return c->fail(GPIPE_ERR_CUDA, "cannot create the capture stream");
+      if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+        return c->fail(GPIPE_ERR_CUDA, "cudaStreamBeginCapture failed");
+      const int64_t before = launch_count();
+      Executor ex(c, ptrs, c->cap_stream);
+      rc = ex.run_step();
+      cudaGraph_t g = nullptr;
+      cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &g);
+      if (rc) {
+        if (g) cudaGraphDestroy(g);
+        return c->fail_from_launch(rc);
+      }
+      if (ce != cudaSuccess || !g)
+        return c->fail(GPIPE_ERR_CUDA, std::string("graph capture failed: ") + cudaGetErrorString(ce));
+      c->launches_per_step = launch_count() - before;
+      c->graph = g;
+      ce = cudaGraphInstantiate(&c->gexec, g, 0);
+      if (ce != cudaSuccess) {
+        c->drop_graph();
+        return c->fail(GPIPE_ERR_CUDA, std::string("graph instantiate failed: ") + cudaGetErrorString(ce));
+      }
+      c->key = key;
+      c->have_key = true;
+    }
+    cudaError_t ce = cudaGraphLaunch(c->gexec, s);
+    if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, std::string("graph launch failed: ") + cudaGetErrorString(ce));
+  }
+  if (loss_out) {
+    float loss = 0.f;
+    int derr = 0;
+    cudaError_t ce = cudaMemcpyAsync(&loss, static_cast<char*>(workspace) + c->ws.misc, 4, cudaMemcpyDeviceToHost, s);
+    if (ce == cudaSuccess) ce = cudaMemcpyAsync(&derr, device_error_ptr(), 4, cudaMemcpyDeviceToHost, s);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+    if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, std::string("step failed: ") + cudaGetErrorString(ce));
+    *loss_out = loss;
+    if (derr) return c->fail(GPIPE_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (device error flag " +
+                                                           std::to_string(derr) + ")");
+    if (!std::isfinite(loss)) return c->fail(GPIPE_ERR_NONFINITE_LOSS, "loss is not finite");
+  }
+  return GPIPE_OK;
+}
+
+double gpipe_bubble_fraction(const gpipe_ctx* c) {
+  if (!c) return -1.0;
+  return static_cast<double>(c->K - 1) / static_cast<double>(c->M + c->K - 1);
+}
+
+int gpipe_schedule_model(const gpipe_ctx* c, const double* t_f, const double* t_b, double* makespan, double* bubble) {
+  if (!c) return GPIPE_ERR_INVALID_ARG;
+  std::vector<double> tf(c->K), tb(c->K);
+  for (int k = 0; k < c->K; ++k) {
+    double cellcost = 0.0;
+    for (int l = c->bounds[k]; l < c->bounds[k + 1]; ++l) cellcost += static_cast<double>(c->cost[l]);
+    tf[k] = t_f ? t_f[k] : cellcost;
+    tb[k] = t_b ? t_b[k] : 2.0 * cellcost;
+  }
+  double b = 0.0;
+  double ms = simulate_gpipe(c->K, c->M, tf.data(), tb.data(), &b);
+  if (makespan) *makespan = ms;
+  if (bubble) *bubble = b;
+  return GPIPE_OK;
+}
+
+int gpipe_memory_report(const gpipe_ctx* cc, size_t* peak_act_bytes, size_t* model_bound_bytes) {
+  if (!cc) return GPIPE_ERR_INVALID_ARG;
+  gpipe_ctx* c = const_cast<gpipe_ctx*>(cc);
+  c->refresh_ws();
+  if (peak_act_bytes) *peak_act_bytes = c->ws.act_bytes;
+  if (model_bound_bytes) *model_bound_bytes = c->ws.bound_bytes;
+  return GPIPE_OK;
+}
+
+int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
+  if (!c) return GPIPE_ERR_INVALID_ARG;
+  switch (option) {
+    case GPIPE_OPT_KEEP_GRADS: c->keep_grads = value != 0; break;
+    case GPIPE_OPT_GRAPH: c->use_graph = value != 0; break;
+    case GPIPE_OPT_NO_REMAT: c->no_remat = value != 0; c->ws_stale = true; break;
+    case GPIPE_OPT_REMAT_CHECK:
+      if (value >= c->M) return c->fail(GPIPE_ERR_INVALID_ARG, "remat check micro-batch out of range");
+      c->remat_check_m = value < 0 ? -1 : value;
+      c->ws_stale = true;
+      break;
+    case GPIPE_OPT_SKIP_UPDATE: c->skip_update = value != 0; break;
+    default: return c->fail(GPIPE_ERR_INVALID_ARG, "unknown option");
+  }
+  c->drop_graph();
+  return GPIPE_OK;
+}
+
+int gpipe_debug_counters(gpipe_ctx* c, void* workspace, void* stream, uint64_t* remat_mismatch, int* error_flag) {
+  if (!c || !workspace) return GPIPE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long cnt = 0;
+  int derr = 0;
+  cudaError_t ce = cudaMemcpyAsync(&cnt, static_cast<char*>(workspace) + c->ws.misc + 8, 8, cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(&derr, device_error_ptr(), 4, cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  if (ce == cudaSuccess && derr) ce = cudaMemsetAsync(device_error_ptr(), 0, 4, s);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, cudaGetErrorString(ce));
+  if (remat_mismatch) *remat_mismatch = cnt;
+  if (error_flag) *error_flag = derr;
+  return GPIPE_OK;
+}
+
+int gpipe_loss_rows(gpipe_ctx* c, void* workspace, void* stream, float* host_out, size_t count) {
+  if (!c || !workspace || !host_out) return GPIPE_ERR_INVALID_ARG;
+  if (count > c->T()) return c->fail(GPIPE_ERR_INVALID_ARG, "count exceeds the number of loss rows");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaMemcpyAsync(host_out, static_cast<char*>(workspace) + c->ws.loss_rows, count * 4,
+                                   cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, cudaGetErrorString(ce));
+  return GPIPE_OK;
+}
+
+int64_t gpipe_launches_per_step(const gpipe_ctx* c) { return c ? c->launches_per_step : -1; }
+
+const char* gpipe_last_error(const gpipe_ctx* c) {
+  if (!c) return g_create_error.c_str();
+  return c->err.c_str();
+}
+
+void gpipe_destroy(gpipe_ctx* c) {
+  if (!c) return;
+  c->drop_graph();
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+  delete c;
+}
+
+}  // extern "C"

@@ -16,6 +16,10 @@ enum { EPI_STORE = 0, EPI_BIAS_GELU = 1, EPI_GELU_BWD = 2, EPI_ACC_F32 = 3, EPI_
 int set_error(int code, const char* fmt, ...);
 const char* last_error_message();
 
+// Device address of the library's error word (set by bounded device waits
+// that give up; see common.cuh).
+int* device_error_ptr();
+
 // Counts kernel launches made through the launchers (host side).
 void count_launch(int n = 1);
 int64_t launch_count();
@@ -63,7 +67,7 @@ int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, in
 int launch_mse(int rows, int d, const float* y, const float* t, float inv_count, float* loss_rows, float* dy,
                cudaStream_t stream);
 
-int launch_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb_bf16, void* x,
+int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb_bf16, void* x,
                          cudaStream_t stream);
 int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx_bf16, float* demb,
                          cudaStream_t stream);
@@ -79,6 +83,12 @@ int launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 // counter[0] += number of bytes that differ between a and b.
 int launch_count_diff(const void* a, const void* b, size_t bytes, unsigned long long* counter,
                       cudaStream_t stream);
+
+// Sets the shared-memory attributes of every kernel that needs more than the
+// default and resolves driver entry points, outside any stream capture.
+int prepare_kernels();
+int prepare_gemm_tc();
+int prepare_attention();
 
 // Number of SMs of the current device (cached).
 int num_sms();

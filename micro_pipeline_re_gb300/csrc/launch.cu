@@ -60,6 +60,16 @@ int num_sms() {
   return sms;
 }
 
+int prepare_kernels() {
+  int rc = prepare_gemm_tc();
+  if (rc) return rc;
+  rc = prepare_attention();
+  if (rc) return rc;
+  if (!device_error_ptr()) return set_error(GPIPE_ERR_CUDA, "cannot resolve the device error flag");
+  num_sms();
+  return GPIPE_OK;
+}
+
 }  // namespace gp
 
 using gp::set_error;
@@ -135,8 +145,9 @@ int gpipe_op_mse(int rows, int d, const float* y, const float* t, float inv_coun
   return gp::launch_mse(rows, d, y, t, inv_count, loss_rows, dy, static_cast<cudaStream_t>(stream));
 }
 
-int gpipe_op_embedding_fwd(int rows, int d, const int32_t* tokens, const void* emb_bf16, void* x, void* stream) {
-  return gp::launch_embedding_fwd(rows, d, tokens, emb_bf16, x, static_cast<cudaStream_t>(stream));
+int gpipe_op_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb_bf16, void* x,
+                           void* stream) {
+  return gp::launch_embedding_fwd(rows, d, vocab, tokens, emb_bf16, x, static_cast<cudaStream_t>(stream));
 }
 
 int gpipe_op_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx_bf16, float* demb,

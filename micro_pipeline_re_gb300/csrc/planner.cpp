@@ -1,0 +1,215 @@
+// Host planner of the GPipe step.
+//
+// Partition: "GPipe technical review" (zzz0906.github.io), "GPipe algorithm:
+// minimal interface" - consecutive layers are cut into K cells and balanced
+// by minimising the variance of the per-cell estimated cost.  With the total
+// fixed, variance = (1/K) sum S_k^2 - mean^2, so the exact integer objective
+// sum S_k^2 is minimised by dynamic programming over suffixes.
+//
+// Clock model: "Pipeline flow" (phases 1-3) and "Bubble overhead analysis";
+// with equal cells the bubble is (K-1)/(M+K-1).
+//
+// Workspace: "Preliminaries 5: re-materialisation" - only the cell-boundary
+// activations of every micro-batch are kept (stash), plus the internals of
+// the one cell being differentiated for one micro-batch, giving the review's
+// O(N + (L/K)(N/M)) peak instead of O(N L).
+#include "planner.h"
+
+#include <algorithm>
+#include <limits>
+
+namespace gp {
+
+using i128 = __int128;
+
+bool partition_min_variance(const std::vector<int64_t>& costs, int K, std::vector<int32_t>& bounds) {
+  const int L = static_cast<int>(costs.size());
+  if (K < 1 || K > L) return false;
+  std::vector<i128> pre(L + 1, 0);
+  for (int i = 0; i < L; ++i) pre[i + 1] = pre[i] + costs[i];
+  const i128 INF = (static_cast<i128>(1) << 126);
+  // best[c][i]: minimum sum of squared cell sums splitting layers [i, L) into c cells
+  std::vector<std::vector<i128>> best(K + 1, std::vector<i128>(L + 1, INF));
+  best[0][L] = 0;
+  for (int c = 1; c <= K; ++c) {
+    for (int i = L - c; i >= 0; --i) {
+      i128 b = INF;
+      for (int j = i + 1; j <= L - (c - 1); ++j) {
+        if (best[c - 1][j] >= INF) continue;
+        const i128 s = pre[j] - pre[i];
+        const i128 v = s * s + best[c - 1][j];
+        if (v < b) b = v;
+      }
+      best[c][i] = b;
+    }
+  }
+  bounds.assign(1, 0);
+  int i = 0;
+  for (int c = K; c >= 1; --c) {
+    for (int j = i + 1; j <= L - (c - 1); ++j) {
+      if (best[c - 1][j] >= INF) continue;
+      const i128 s = pre[j] - pre[i];
+      if (s * s + best[c - 1][j] == best[c][i]) {
+        bounds.push_back(j);
+        i = j;
+        break;
+      }
+    }
+  }
+  return static_cast<int>(bounds.size()) == K + 1 && bounds.back() == L;
+}
+
+double simulate_gpipe(int K, int M, const double* t_f, const double* t_b, double* bubble) {
+  std::vector<double> fe(static_cast<size_t>(M) * K, 0.0), be(static_cast<size_t>(M) * K, 0.0);
+  auto F = [&](int m, int k) -> double& { return fe[static_cast<size_t>(m) * K + k]; };
+  auto B = [&](int m, int k) -> double& { return be[static_cast<size_t>(m) * K + k]; };
+  for (int m = 0; m < M; ++m)
+    for (int k = 0; k < K; ++k) {
+      double s = 0.0;
+      if (m > 0) s = std::max(s, F(m - 1, k));
+      if (k > 0) s = std::max(s, F(m, k - 1));
+      F(m, k) = s + t_f[k];
+    }
+  for (int m = 0; m < M; ++m)
+    for (int k = K - 1; k >= 0; --k) {
+      double s = F(M - 1, k);
+      if (m > 0) s = std::max(s, B(m - 1, k));
+      if (k < K - 1) s = std::max(s, B(m, k + 1));
+      B(m, k) = s + t_b[k];
+    }
+  double makespan = 0.0, busy = 0.0;
+  for (int m = 0; m < M; ++m) makespan = std::max(makespan, B(m, 0));
+  for (int k = 0; k < K; ++k) busy += M * (t_f[k] + t_b[k]);
+  if (bubble) *bubble = makespan > 0 ? 1.0 - busy / (K * makespan) : 0.0;
+  return makespan;
+}
+
+ParamLayout make_param_layout(const Dims& dm, int L) {
+  ParamLayout p;
+  const size_t d = dm.d, f = dm.ffn;
+  size_t o = 0;
+  for (int l = 0; l < L; ++l) {
+    LayerOff lo{};
+    if (dm.kind == 0) {
+      lo.ln1_g = o; o += d;
+      lo.ln1_b = o; o += d;
+      lo.w1 = o; o += f * d;
+      lo.b1 = o; o += f;
+      lo.w2 = o; o += d * f;
+      lo.b2 = o; o += d;
+    } else {
+      lo.ln1_g = o; o += d;
+      lo.ln1_b = o; o += d;
+      lo.w_qkv = o; o += 3 * d * d;
+      lo.b_qkv = o; o += 3 * d;
+      lo.w_o = o; o += d * d;
+      lo.b_o = o; o += d;
+      lo.ln2_g = o; o += d;
+      lo.ln2_b = o; o += d;
+      lo.w1 = o; o += f * d;
+      lo.b1 = o; o += f;
+      lo.w2 = o; o += d * f;
+      lo.b2 = o; o += d;
+    }
+    p.layers.push_back(lo);
+  }
+  if (dm.kind == 1) {
+    p.lnf_g = o; o += d;
+    p.lnf_b = o; o += d;
+    p.emb = o; o += static_cast<size_t>(dm.vocab) * d;
+  }
+  p.total = o;
+  return p;
+}
+
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+}  // namespace
+
+Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check) {
+  Workspace w;
+  const size_t es = dm.dtype == 0 ? 4 : 2;
+  const size_t T = static_cast<size_t>(dm.n) * (dm.kind == 1 ? dm.seq : 1);
+  const size_t Tmb = T / M;
+  const size_t d = dm.d, f = dm.ffn, H = dm.kind == 1 ? dm.heads : 0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  // slot layout (per layer, per micro-batch of Tmb tokens)
+  SlotLayout s{};
+  size_t so = 0;
+  auto stake = [&](size_t bytes) {
+    size_t at = so;
+    so += align256(bytes);
+    return at;
+  };
+  s.u = stake(Tmb * d * es);
+  if (dm.kind == 1) {
+    s.qkv = stake(Tmb * 3 * d * es);
+    s.o = stake(Tmb * d * es);
+    s.h1 = stake(Tmb * d * es);
+    s.u2 = stake(Tmb * d * es);
+  }
+  s.z1 = stake(Tmb * f * es);
+  s.g = stake(Tmb * f * es);
+  s.mean1 = stake(Tmb * 4);
+  s.rstd1 = stake(Tmb * 4);
+  if (dm.kind == 1) {
+    s.mean2 = stake(Tmb * 4);
+    s.rstd2 = stake(Tmb * 4);
+    s.lse = stake(Tmb * H * 4);
+  }
+  s.compare_bytes_last = so;
+  s.y = stake(Tmb * d * es);
+  s.bytes = so;
+  w.slot = s;
+  w.slot_bytes = s.bytes;
+
+  w.stash_bytes = Tmb * d * es;
+  w.stash = take(static_cast<size_t>(K + 1) * M * w.stash_bytes);
+  w.nslots = remat ? static_cast<size_t>(max_cell_layers) : static_cast<size_t>(L) * M;
+  w.slots = take(w.nslots * w.slot_bytes);
+  size_t head_start = off;
+  if (dm.kind == 1) {
+    w.hf = take(Tmb * d * es);
+    w.meanf = take(Tmb * 4);
+    w.rstdf = take(Tmb * 4);
+    w.logits = take(Tmb * static_cast<size_t>(dm.vocab) * 4);
+  }
+  w.g0 = take(Tmb * d * es);
+  w.g1 = take(Tmb * d * es);
+  w.gt = take(Tmb * d * es);
+  w.gf = take(Tmb * f * es);
+  if (dm.kind == 1) {
+    w.gh = take(Tmb * d * es);
+    w.gq = take(Tmb * 3 * d * es);
+  }
+  const size_t rows_for_scratch = Tmb;
+  size_t cols = std::max<size_t>(2 * d, f);
+  if (dm.kind == 1) cols = std::max<size_t>(cols, 3 * d);
+  const size_t parts = (rows_for_scratch + 7) / 8;
+  w.scratch_bytes = std::max(parts * cols * 4, Tmb * std::max<size_t>(H, 1) * 4);
+  w.scratch = take(w.scratch_bytes);
+  w.loss_rows = take(T * 4);
+  const size_t per_token_tail = (off - head_start) / std::max<size_t>(Tmb, 1) + 1;
+  w.act_bytes = off;
+  w.misc = take(256);
+  if (remat && remat_check) {
+    w.check_bytes = static_cast<size_t>(K) * max_cell_layers * w.slot_bytes;
+    w.check = take(w.check_bytes);
+  }
+  w.total = off;
+  // The review's bound O(N + (L/K)(N/M)) with explicit constants: the
+  // boundary stash (K+1 tensors per micro-batch, i.e. proportional to N),
+  // one cell of Lc layers of kept internals for one micro-batch (proportional
+  // to (L/K)(N/M)), and the per-micro-batch head/gradient/scratch term.
+  const size_t a = w.slot_bytes / std::max<size_t>(Tmb, 1) + 1;  // kept bytes per token per layer
+  const size_t cell_layers = remat ? static_cast<size_t>(max_cell_layers) : static_cast<size_t>(L) * M;
+  w.bound_bytes = static_cast<size_t>(K + 1) * T * d * es + cell_layers * Tmb * a + Tmb * per_token_tail;
+  return w;
+}
+
+}  // namespace gp

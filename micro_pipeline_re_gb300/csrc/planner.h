@@ -1,0 +1,64 @@
+// Host planner: variance-minimising partition, GPipe clock model, parameter
+// packing and the workspace (activation memory) layout.  Pure host code.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include <vector>
+
+namespace gp {
+
+// Contiguous K-way cut of costs[0..L) minimising sum_k S_k^2 (equivalently
+// the variance of the cell sums S_k, whose total is fixed); every cell holds
+// >= 1 layer; among optima the lexicographically smallest bounds.  Exact in
+// 128-bit integers.  Returns false if K is out of range.
+bool partition_min_variance(const std::vector<int64_t>& costs, int K, std::vector<int32_t>& bounds);
+
+// Discrete-event GPipe clock: forwards of micro-batches 0..M-1 flow through
+// cells 0..K-1, then backwards (micro-batches ascending, cells K-1..0); a
+// cell starts an op when it finished its previous op and the neighbour handed
+// it the data.  Returns makespan; bubble = 1 - sum busy / (K makespan).
+double simulate_gpipe(int K, int M, const double* t_f, const double* t_b, double* bubble);
+
+struct Dims {
+  int kind, d, heads, ffn, seq, vocab, n, dtype;
+  float lr, decay, eps;
+};
+
+// Element offsets of one layer's parameters in the flat packing.
+struct LayerOff {
+  size_t ln1_g, ln1_b, w_qkv, b_qkv, w_o, b_o, ln2_g, ln2_b, w1, b1, w2, b2;
+};
+
+struct ParamLayout {
+  std::vector<LayerOff> layers;
+  size_t lnf_g = 0, lnf_b = 0, emb = 0;
+  size_t total = 0;
+};
+ParamLayout make_param_layout(const Dims& dm, int L);
+
+// Byte offsets of one layer's kept internals inside a slot.
+struct SlotLayout {
+  size_t u, qkv, o, h1, u2, z1, g, mean1, rstd1, mean2, rstd2, lse, y;
+  size_t compare_bytes_last;  // bytes that are defined when the layer's output is not written (all but y)
+  size_t bytes;
+};
+
+struct Workspace {
+  size_t stash = 0, stash_bytes = 0;        // (K+1) x M boundary tensors [Tmb, d]
+  size_t slots = 0, slot_bytes = 0, nslots = 0;
+  SlotLayout slot{};
+  size_t hf = 0, meanf = 0, rstdf = 0, logits = 0;  // head (kind 1)
+  size_t g0 = 0, g1 = 0, gh = 0, gt = 0, gf = 0, gq = 0;  // gradients in flight
+  size_t scratch = 0, scratch_bytes = 0;
+  size_t loss_rows = 0, misc = 0;            // misc: loss (float) at +0, remat counter (u64) at +8
+  size_t check = 0, check_bytes = 0;         // re-materialisation check copies (debug)
+  size_t act_bytes = 0;                      // activation bytes (everything but misc/check)
+  size_t total = 0;
+  // bound of the review's form with explicit constants
+  size_t bound_bytes = 0;
+};
+
+Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check);
+
+}  // namespace gp

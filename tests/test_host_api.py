@@ -1,0 +1,164 @@
+"""CPU-only tests of libgpipe's host side through the C ABI: exported symbols,
+argument validation, the partitioner, the GPipe clock model and the
+activation-memory plan.  No CUDA call is made here."""
+import os
+import re
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import partition as op
+from oracle import schedule as osch
+from synth import KIND_FFN, KIND_LM, SWEEP_GRID, WORKLOADS, Workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from micro_pipeline_re_gb300 import _build
+    _build.build()
+    from micro_pipeline_re_gb300 import binding as b
+    b.lib()
+    return b
+
+
+def _declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(gpipe_\w+)\s*\(", txt))
+    return names
+
+
+def test_library_exports_every_declared_symbol(binding):
+    declared = _declared_functions()
+    assert len(declared) >= 20
+    lib = binding.lib()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(binding.exported_names())
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(L=4, K=5, M=1), -1),          # K > L
+    (dict(L=4, K=0, M=1), -1),          # K < 1
+    (dict(L=4, K=2, M=3), -1),          # N % M != 0 (N = 32)
+    (dict(L=4, K=2, M=0), -1),
+])
+def test_create_rejects_bad_shapes(binding, kwargs, code):
+    w = WORKLOADS["tiny_ffn"]
+    with pytest.raises(binding.GpipeError) as e:
+        binding.GPipe(kwargs["L"], kwargs["K"], kwargs["M"], kind=0, d=w.d, heads=0, ffn=w.ffn, seq=1, vocab=0,
+                      n=w.n, dtype=0)
+    assert e.value.code == code
+
+
+def test_create_rejects_bad_layer_dims(binding):
+    with pytest.raises(binding.GpipeError) as e:   # head width must be 64
+        binding.GPipe(2, 1, 1, kind=1, d=256, heads=8, ffn=512, seq=64, vocab=256, n=2, dtype=1)
+    assert e.value.code == -1
+    with pytest.raises(binding.GpipeError) as e:   # seq multiple of 64
+        binding.GPipe(2, 1, 1, kind=1, d=128, heads=2, ffn=512, seq=100, vocab=256, n=2, dtype=1)
+    assert e.value.code == -1
+    with pytest.raises(binding.GpipeError) as e:   # the LM runs in bf16
+        binding.GPipe(2, 1, 1, kind=1, d=128, heads=2, ffn=512, seq=64, vocab=256, n=2, dtype=0)
+    assert e.value.code == -6
+    with pytest.raises(binding.GpipeError) as e:   # bad optimizer constants
+        binding.GPipe(2, 1, 1, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=2, dtype=0, decay=1.0)
+    assert e.value.code == -1
+
+
+def test_partition_matches_brute_force(binding):
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        L = int(rng.integers(1, 13))
+        K = int(rng.integers(1, L + 1))
+        costs = [int(c) for c in rng.integers(1, 40, size=L)]
+        g = binding.GPipe(L, K, 1, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=4, dtype=0, cost=costs)
+        got = g.partition()
+        want, _ = op.partition(costs, K)
+        assert got == want, (costs, K, got, want)
+        g.close()
+
+
+def test_partition_huge_costs_exact(binding):
+    """Costs near 1e15 (layer FLOPs of large models): squares need 128-bit."""
+    costs = [10**15 + i for i in (5, 1, 3, 2, 9, 4, 7, 8)]
+    g = binding.GPipe(8, 3, 1, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=4, dtype=0, cost=costs)
+    assert g.partition() == op.partition(costs, 3)[0]
+
+
+def test_default_costs_split_identical_layers_evenly(binding):
+    for name in ("lm_small", "lm_wide", "lm_deep"):
+        w = WORKLOADS[name]
+        g = binding.GPipe.from_workload(w)
+        assert g.partition() == [k * (w.L // w.K) for k in range(w.K + 1)]
+
+
+@pytest.mark.parametrize("K,M", [(1, 1), (2, 1), (4, 32), (8, 32), (4, 4), (3, 7)])
+def test_bubble_fraction_and_clock_model(binding, K, M):
+    g = binding.GPipe(8 * K, K, M, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=M * 2, dtype=0)
+    assert g.bubble_fraction() == pytest.approx(float(Fraction(K - 1, M + K - 1)), abs=1e-15)
+    mk, bub = g.schedule_model([1.0] * K, [2.0] * K)
+    sim = osch.simulate(K, M, 1, 2)
+    assert mk == pytest.approx(float(sim["makespan"]), rel=1e-12)
+    assert bub == pytest.approx(float(sim["bubble"]), abs=1e-12)
+
+
+def test_clock_model_unequal_cells(binding):
+    rng = np.random.default_rng(3)
+    for _ in range(10):
+        K, M = int(rng.integers(1, 6)), int(rng.integers(1, 9))
+        tf = [float(x) for x in rng.integers(1, 9, size=K)]
+        tb = [float(x) for x in rng.integers(1, 9, size=K)]
+        g = binding.GPipe(K, K, M, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=M, dtype=0)
+        mk, bub = g.schedule_model(tf, tb)
+        sim = osch.simulate(K, M, [int(x) for x in tf], [int(x) for x in tb])
+        assert mk == pytest.approx(float(sim["makespan"]), rel=1e-12)
+        assert bub == pytest.approx(float(sim["bubble"]), abs=1e-12)
+
+
+def _report(binding, w, K, M, no_remat=False):
+    g = binding.GPipe.from_workload(w, K=K, M=M)
+    if no_remat:
+        g.set_option(binding.OPT_NO_REMAT, 1)
+    peak, bound = g.memory_report()
+    P, ws = g.sizes()
+    return peak, bound, ws
+
+
+def test_memory_within_bound_and_workspace(binding):
+    for name, w in WORKLOADS.items():
+        peak, bound, ws = _report(binding, w, w.K, w.M)
+        assert peak <= bound, name
+        assert ws >= peak
+
+
+def test_memory_scales_as_review_bound_over_sweep_grid(binding):
+    """Peak activation bytes over the micro-batch sweep grid follow
+    a (K+1) N + b (L/K)(N/M) + c (N/M) (the review's O(N + (L/K)(N/M)))."""
+    w = WORKLOADS["lm_sweep"]
+    rows, ys = [], []
+    for K, M in SWEEP_GRID:
+        peak, bound, _ = _report(binding, w, K, M)
+        assert peak <= bound
+        T = w.tokens
+        rows.append([(K + 1) * T, (w.L / K) * T / M, T / M])
+        ys.append(peak)
+    A, y = np.array(rows, dtype=float), np.array(ys, dtype=float)
+    coef, *_ = np.linalg.lstsq(A, y, rcond=None)
+    resid = np.abs(A @ coef - y) / y
+    assert resid.max() <= 0.10, resid
+    assert np.all(coef > 0)
+
+
+def test_rematerialisation_saves_memory(binding):
+    w = WORKLOADS["lm_wide"]
+    peak, _, _ = _report(binding, w, w.K, w.M)
+    peak_nr, _, _ = _report(binding, w, w.K, w.M, no_remat=True)
+    # without re-materialisation every layer keeps its internals for every micro-batch
+    assert peak_nr > 10 * peak
