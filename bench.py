@@ -1,0 +1,318 @@
+"""Throughput of one synchronous GPipe training step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line.  A step is one full pass of the hot path: forward of all
+M micro-batches through all K cells (boundary stash), backward with
+re-materialisation and fp32 gradient accumulation, one RMSProp update.
+`value` is training tokens/s over the timed steps with every input resident
+in HBM; `e2e` times the same through the C ABI from pinned host buffers
+(tokens copied in, loss copied out, every step).  The step does not shard
+(all cells on one GPU, no collectives): with N > 1 ranks each GPU runs an
+independent replica ("replicas only") and `value` adds their tokens.
+
+--impl reference times the CPU fp64 oracle (full-batch step, no micro-batches)
+on this machine's host cores on a bounded sub-batch of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "training tokens/sec per synchronous step (1×GB300) and MFU vs BF16 peak"
+
+
+def model_flops(w):
+    """Model FLOPs of one step (forward + backward, no re-computation): 3 F_fwd T."""
+    d, f, L, V, S = w.d, w.ffn, w.L, w.vocab, w.seq
+    per_tok = 2 * (4 * d * d + 2 * d * f) * L + 2 * 2 * d * (S + 1) / 2 * L + 2 * d * V
+    return 3.0 * per_tok * w.tokens
+
+
+def recompute_flops(w, bounds):
+    """FLOPs the re-materialisation adds: every cell's forward again, except
+    the output projection of each cell's last layer; plus the head forward."""
+    d, f, S, V = w.d, w.ffn, w.seq, w.vocab
+    layer = 2 * (4 * d * d + 2 * d * f) + 2 * 2 * d * (S + 1) / 2
+    out_proj = 2 * d * f
+    tot = 0.0
+    for k in range(len(bounds) - 1):
+        n = bounds[k + 1] - bounds[k]
+        tot += n * layer - out_proj
+    return (tot + 2 * d * V) * w.tokens
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        self.out.seek(0)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.out.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, budget_s=15.0):
+    """Time the oracle's full step on a sub-batch sized to about budget_s."""
+    from oracle import model as om
+    from synth import make_inputs
+    n = 1
+    sub = w.replace(n=n, M=1, K=1)
+    inp = make_inputs(sub)
+    t0 = time.perf_counter()
+    om.step(sub, inp["params"], inp)
+    dt = time.perf_counter() - t0
+    while dt < budget_s / 3 and n * 2 <= w.n:
+        n *= 2
+        sub = w.replace(n=n, M=1, K=1)
+        inp = make_inputs(sub)
+        t0 = time.perf_counter()
+        om.step(sub, inp["params"], inp)
+        dt = time.perf_counter() - t0
+    return sub, inp, dt
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import model as om
+    sub, inp, _ = oracle_sample(w, budget_s=6.0)
+    for _ in range(args.warmup):
+        om.step(sub, inp["params"], inp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        om.step(sub, inp["params"], inp)
+    dt = (time.perf_counter() - t0) / args.steps
+    toks = sub.tokens / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": toks, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg(w, args),
+        "cpu_baseline": {"value": toks, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"full-batch fp64 step on a sub-batch of {sub.n} sequences x {sub.seq} tokens "
+                                   f"of the {w.name} layers (no micro-batching)"},
+        "e2e": {"value": toks, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cfg(w, args):
+    return {"workload": w.name, "L": w.L, "K": w.K, "M": w.M, "d": w.d, "heads": w.heads, "ffn": w.ffn,
+            "seq_len": w.seq, "vocab": w.vocab, "global_batch": w.n * max(args.gpus, 1),
+            "parallelism": "replicas" if args.gpus > 1 else "single-gpu (all K cells on one GPU)",
+            "l2": "working set larger than L2 (parameters, gradients and RMSProp state alone exceed 129 MB)"}
+
+
+def gemm_roofline(b, w, peaks, stream):
+    """Time the dominant kernel class (tcgen05 GEMM, FFN first projection at
+    the step's micro-batch shape) with CUDA events on the launching stream."""
+    import torch
+    T, d, f = w.tokens // w.M, w.d, w.ffn
+    A = torch.randn(T, d, device="cuda").to(torch.bfloat16)
+    Bw = torch.randn(f, d, device="cuda").to(torch.bfloat16)
+    bias = torch.zeros(f, device="cuda")
+    Z = torch.empty(T, f, device="cuda", dtype=torch.bfloat16)
+    G = torch.empty(T, f, device="cuda", dtype=torch.bfloat16)
+    lib = b.lib()
+
+    def launch():
+        rc = lib.gpipe_op_gemm(1, T, f, d, A.data_ptr(), d, 1, Bw.data_ptr(), d, 1, 1, Z.data_ptr(), f,
+                               bias.data_ptr(), None, 0, G.data_ptr(), None, 0, stream)
+        assert rc == 0
+    for _ in range(5):
+        launch()
+    reps = 200
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        launch()
+    e.record()
+    torch.cuda.synchronize()
+    dt = s.elapsed_time(e) / 1e3 / reps
+    flops = 2.0 * T * f * d
+    ach = flops / dt / 1e12
+    return {"bound": "tensor", "kernel": f"tc_gemm bias+GELU {T}x{f}x{d}", "achieved": ach, "peak": peaks["bf16"],
+            "unit": "TFLOP/s", "frac": ach / peaks["bf16"], "traffic": None,
+            "peak_source": peaks["source"] + " (burst)", "avg_launch_us": dt * 1e6}
+
+
+def run_ours(args, w):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__ as ge
+    if rank == 0 or world == 1:
+        ge.build()
+    if dist:
+        dist.barrier()
+    from micro_pipeline_re_gb300 import binding as b
+    from synth import make_inputs
+    peaks = load_peaks()
+    inp = make_inputs(w)
+    gp = b.GPipe.from_workload(w)
+    st = b.DeviceState(gp, w, inp)
+    stream = st.stream
+    for _ in range(args.warmup):
+        st.step(want_loss=False)
+    loss = st.step()  # checks the error flag and a finite loss
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        ev0.record()
+        for _ in range(args.steps):
+            st.step(want_loss=False)
+        ev1.record()
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_step = ev0.elapsed_time(ev1) / 1e3 / args.steps
+    clocks = clk.summary()
+    if dist:
+        tt = torch.tensor([t_step], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = tt.item()
+    tokens_all = w.tokens * world
+    value = tokens_all / t_step
+    mf = model_flops(w)
+    bounds = gp.partition()
+    hf = mf + recompute_flops(w, bounds)
+    launches = gp.launches_per_step()
+
+    # end to end through the C ABI from pinned host memory (tokens in, loss out)
+    host_tok = torch.from_numpy(inp["tokens"]).pin_memory()
+    e2e_steps = max(3, args.steps // 2)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        st.batch.copy_(host_tok, non_blocking=True)
+        st.step(want_loss=True)
+    t_e2e = (time.perf_counter() - t0) / e2e_steps
+    if dist:
+        tt = torch.tensor([t_e2e], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = tt.item()
+    roof = gemm_roofline(b, w, peaks, stream)
+    peak_act, bound = gp.memory_report()
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            sub, _, dt = oracle_sample(w)
+            cpu = {"value": sub.tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"one full-batch fp64 oracle step on {sub.n} sequence(s) x {sub.seq} tokens of the "
+                             f"{w.name} layers ({dt:.1f} s)"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (uniform random token ids, N(0,1/d) weights)",
+            "config": cfg(w, args),
+            "mfu": mf / t_step / (peaks["bf16_sus"] * 1e12) * 1.0,
+            "hfu": hf / t_step / (peaks["bf16_sus"] * 1e12),
+            "mfu_peak": f"{peaks['bf16_sus']} TFLOP/s bf16 sustained ({peaks['source']})",
+            "loss": loss, "bubble_model": gp.bubble_fraction(), "peak_activation_bytes": peak_act,
+            "activation_bound_bytes": bound,
+            "e2e": {"value": tokens_all / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(host_tok.numel() * 4),
+                    "d2h_bytes_per_step": 4},
+            "gpu_launches": int(launches * args.steps), "launches_per_step": int(launches),
+            "roofline": roof, "cpu_baseline": cpu, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="lm_small")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _release_test_tensors():
+    yield
+    import sys as _sys
+    gu = _sys.modules.get("tests.gpu_util")
+    if gu is not None:
+        gu.KEEP.clear()

@@ -13,6 +13,12 @@ def rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
 
+# Tensors made by dev() stay alive until the end of the test (conftest clears
+# this list), so a pointer taken inline from a temporary stays valid while the
+# kernel that was given it runs.
+KEEP = []
+
+
 def dev(x, dtype=None):
     """numpy -> cuda tensor (float arrays become fp32, or bf16 with dtype='bf16')."""
     t = torch()
@@ -21,8 +27,10 @@ def dev(x, dtype=None):
         tt = t.from_numpy(x.astype(np.float32)).cuda()
         if dtype == "bf16":
             tt = tt.to(t.bfloat16)
-        return tt
-    return t.from_numpy(x).cuda()
+    else:
+        tt = t.from_numpy(x).cuda()
+    KEEP.append(tt)
+    return tt
 
 
 def host(t_):

@@ -94,10 +94,11 @@ def test_gemm_fp32_ffma(b, ak, bk, epi):
     aux = rng.standard_normal((M, N)).astype(np.float32)
     C0 = rng.standard_normal((M, N)).astype(np.float32)
     dC, dC2 = dev(C0), dev(np.zeros((M, N), np.float32))
-    rc = b.lib().gpipe_op_gemm(0, M, N, K, dev(A).data_ptr(), A.shape[1], ak, dev(B).data_ptr(), B.shape[1], bk, epi,
-                               dC.data_ptr(), N, dev(bias).data_ptr() if epi < 2 else None,
-                               dev(resid).data_ptr() if epi == 0 else None, N, dC2.data_ptr() if epi == 1 else None,
-                               dev(aux).data_ptr() if epi == 2 else None, N, stream())
+    keep = [dev(A), dev(B), dev(bias), dev(resid), dev(aux)]  # hold device buffers until the kernel ran
+    rc = b.lib().gpipe_op_gemm(0, M, N, K, keep[0].data_ptr(), A.shape[1], ak, keep[1].data_ptr(), B.shape[1], bk,
+                               epi, dC.data_ptr(), N, keep[2].data_ptr() if epi < 2 else None,
+                               keep[3].data_ptr() if epi == 0 else None, N, dC2.data_ptr() if epi == 1 else None,
+                               keep[4].data_ptr() if epi == 2 else None, N, stream())
     assert rc == 0
     sync()
     if epi == 0:
