@@ -75,7 +75,7 @@ typedef struct {
 /* Create a context for L layers cut into K cells and M micro-batches.
  * cost: L per-layer cost estimates c_i (>= 1), or NULL for the layer's FLOPs.
  * Validates 1 <= K <= L, M >= 1, N % M == 0; kind 1: d % 64 == 0,
- * d/heads == 64, seq % 64 == 0, ffn % 64 == 0; kind 0: d % 8 == 0,
+ * d/heads == 64, seq % 64 == 0, ffn % 64 == 0, vocab % 8 == 0; kind 0: d % 8 == 0,
  * ffn % 8 == 0; then partitions.
  * On failure *out is NULL and the return code says why; gpipe_last_error(NULL)
  * returns this thread's last message. */

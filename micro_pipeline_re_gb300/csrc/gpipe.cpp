@@ -378,7 +378,7 @@ int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
     return why = "kind 1 needs d % 64 == 0, d <= 1024 and d/heads == 64", GPIPE_ERR_INVALID_ARG;
   if (dm->seq < 64 || dm->seq % 64) return why = "seq must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
   if (dm->ffn < 64 || dm->ffn % 64) return why = "ffn must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
-  if (dm->vocab < 64 || dm->vocab % 64) return why = "vocab must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
+  if (dm->vocab < 8 || dm->vocab % 8) return why = "vocab must be a positive multiple of 8", GPIPE_ERR_INVALID_ARG;
   return GPIPE_OK;
 }
 
