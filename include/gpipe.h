@@ -179,8 +179,9 @@ int gpipe_loss_rows(gpipe_ctx* ctx, void* workspace, void* stream, float* host_o
 /* Number of kernels one step launches. */
 int64_t gpipe_launches_per_step(const gpipe_ctx* ctx);
 
-/* Message of the last failure on ctx (or of this thread's last failure when
- * ctx is NULL).  Never NULL. */
+/* Message of the last failure on ctx, or, when ctx is NULL, of this thread's
+ * last failed call of any entry point (gpipe_create and the gpipe_op_* calls
+ * included).  Never NULL. */
 const char* gpipe_last_error(const gpipe_ctx* ctx);
 
 /* Destroy the context and its cached graph.  NULL-safe. */

@@ -98,8 +98,6 @@ struct gpipe_ctx {
 
 namespace {
 
-thread_local std::string g_create_error = "no error";
-
 #define TRY(expr)                          \
   do {                                     \
     int _rc = (expr);                      \
@@ -387,18 +385,11 @@ int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
 extern "C" {
 
 int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims, const int64_t* cost) {
-  if (!out) {
-    g_create_error = "out is NULL";
-    return GPIPE_ERR_INVALID_ARG;
-  }
+  if (!out) return set_error(GPIPE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   std::string why;
   int rc = validate(L, K, M, dims, why);
-  if (rc) {
-    g_create_error = why;
-    set_error(rc, "%s", why.c_str());
-    return rc;
-  }
+  if (rc) return set_error(rc, "%s", why.c_str());
   gpipe_ctx* c = new gpipe_ctx();
   c->L = L;
   c->K = K;
@@ -414,14 +405,12 @@ int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims, c
     c->cost[i] = cost ? cost[i] : default_cost;
     if (c->cost[i] < 1) {
       delete c;
-      g_create_error = "layer costs must be >= 1";
-      return GPIPE_ERR_INVALID_ARG;
+      return set_error(GPIPE_ERR_INVALID_ARG, "layer costs must be >= 1");
     }
   }
   if (!partition_min_variance(c->cost, K, c->bounds)) {
     delete c;
-    g_create_error = "partition failed";
-    return GPIPE_ERR_INVALID_ARG;
+    return set_error(GPIPE_ERR_INVALID_ARG, "partition failed");
   }
   c->max_cell = 0;
   for (int k = 0; k < K; ++k) c->max_cell = std::max(c->max_cell, c->bounds[k + 1] - c->bounds[k]);
@@ -619,7 +608,7 @@ int gpipe_loss_rows(gpipe_ctx* c, void* workspace, void* stream, float* host_out
 int64_t gpipe_launches_per_step(const gpipe_ctx* c) { return c ? c->launches_per_step : -1; }
 
 const char* gpipe_last_error(const gpipe_ctx* c) {
-  if (!c) return g_create_error.c_str();
+  if (!c) return last_error_message();
   return c->err.c_str();
 }
 

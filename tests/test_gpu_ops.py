@@ -339,9 +339,10 @@ def test_rmsprop_and_bf16_copy(b):
                                     1, stream()) == 0
     sync()
     new_p, new_v = om.rmsprop({"a": w}, {"a": g.astype(np.float64)}, {"a": v}, 1e-3, 0.9, 1e-8)
-    # the master is stored in fp32: within 2 fp32 ulps of the fp64 update
+    # fp32 master: within one fp32 ulp of w plus the fp32 rounding of the
+    # update term itself (about 2^-24 relative, taken with margin as 1e-6)
     ulp = np.spacing(np.abs(new_p["a"]).astype(np.float32)).astype(np.float64)
-    assert np.all(np.abs(host(dw) - new_p["a"]) <= 2 * ulp)
+    assert np.all(np.abs(host(dw) - new_p["a"]) <= ulp + 1e-6 * np.abs(new_p["a"] - w))
     assert rel(host(dv), new_v["a"]) <= 1e-6
     assert not np.any(host(dg))
     # bf16 copy is the round-to-nearest-even of the updated fp32 master

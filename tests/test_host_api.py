@@ -162,3 +162,13 @@ def test_rematerialisation_saves_memory(binding):
     peak_nr, _, _ = _report(binding, w, w.K, w.M, no_remat=True)
     # without re-materialisation every layer keeps its internals for every micro-batch
     assert peak_nr > 10 * peak
+
+
+def test_last_error_without_context_reports_any_failed_call(binding):
+    lib = binding.lib()
+    rc = lib.gpipe_op_layernorm_fwd(1, 4, 12, None, None, None, None, None, None, None)   # d % 8 != 0
+    assert rc == -1
+    assert b"layernorm" in lib.gpipe_last_error(None)
+    with pytest.raises(binding.GpipeError):
+        binding.GPipe(4, 5, 1, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=4, dtype=0)
+    assert b"K <= L" in lib.gpipe_last_error(None)
