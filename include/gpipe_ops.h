@@ -71,6 +71,25 @@ int gpipe_op_layernorm_bwd(int dtype, int rows, int d, const void* dy, const voi
                            const void* dres, void* dx, float* dg_acc, float* db_acc,
                            float* scratch, void* stream);
 
+/* The same LayerNorm backward for callers that cannot allocate device memory
+ * when they call it: for instance a plugin inside a host framework that owns
+ * all device memory through its own pool, or a latency-critical path that must
+ * never enter the CUDA allocator.  The paper has no counterpart; this is a
+ * convenience of this library.  Instead of a caller `scratch` buffer it uses a
+ * fixed array of 2^20 floats (4 MiB) inside the library's device image, which
+ * every GPU that loads the library keeps until the process exits; it calls no
+ * allocation routine.  Limit: ceil(rows / 8) * 2 * d <= 2^20 (for d = 1024,
+ * rows <= 4096); larger sizes return GPIPE_ERR_INVALID_ARG with a message.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array: every partial sum the call reads is written by the
+ * same call, so nothing needs clearing, but calls that overlap on the GPU (on
+ * different streams, or from different threads) race on it. */
+int gpipe_op_layernorm_bwd_noalloc(int dtype, int rows, int d, const void* dy, const void* x,
+                                   const float* mean, const float* rstd, const float* g,
+                                   const void* dres, void* dx, float* dg_acc, float* db_acc,
+                                   void* stream);
+
 /* out_acc[c] += sum_r y[r*ldy + c] in a fixed order (bias gradients); scratch
  * of gpipe_op_scratch_bytes(rows, cols) bytes. cols % 8 == 0, ldy % 8 == 0. */
 int gpipe_op_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy,

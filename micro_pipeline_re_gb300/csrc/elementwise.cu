@@ -4,6 +4,7 @@
 // order (no floating-point atomics), so every result is bit-reproducible and
 // a re-computed forward equals the first one byte for byte.
 #include <algorithm>
+#include <mutex>
 
 #include "../../include/gpipe.h"
 #include "common.cuh"
@@ -585,6 +586,60 @@ int launch_count_diff(const void* a, const void* b, size_t bytes, unsigned long 
   count_diff_kernel<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(a), static_cast<const uint32_t*>(b),
                                          bytes / 4, counter);
   return check_launch("count_diff");
+}
+
+
+// ---------------------------------------------------------------------------
+// LayerNorm backward without caller-provided scratch.
+//
+// For callers that cannot allocate device memory at call time (for example a
+// plugin whose host framework owns every byte of device memory through its
+// own pool, or a latency-critical path that must not enter the CUDA
+// allocator), the two-stage reduction's partial sums live in a fixed array in
+// the library's device image instead of a caller buffer.  Every GPU that
+// loads the library holds this array until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 20;  // 4 MiB of fp32 partial sums
+static __device__ __align__(256) float g_ln_bwd_scratch[kNoAllocScratchFloats];
+}  // namespace
+
+size_t layernorm_bwd_noalloc_max_floats() { return kNoAllocScratchFloats; }
+
+int launch_layernorm_bwd_noalloc(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                                 const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
+                                 float* db_acc, cudaStream_t s) {
+  if (rows < 1 || d < 8 || d % 8 || d > 32 * 8 * kMaxChunks)
+    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd_noalloc: need rows >= 1, d %% 8 == 0, 8 <= d <= 1024");
+  const size_t need = colred_scratch_floats(rows, 2 * d);
+  if (need > kNoAllocScratchFloats)
+    return set_error(GPIPE_ERR_INVALID_ARG,
+                     "layernorm_bwd_noalloc: rows=%d, d=%d needs %zu scratch floats, more than the fixed %zu "
+                     "(ceil(rows/8) * 2d must not exceed %zu)",
+                     rows, d, need, kNoAllocScratchFloats, kNoAllocScratchFloats);
+  // The array's host-side name is only a stand-in; resolve its device address
+  // once per device, with that device current.
+  static std::mutex mu;
+  static float* addr[256] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 256)
+    return set_error(GPIPE_ERR_CUDA, "layernorm_bwd_noalloc: no current device");
+  float* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_ln_bwd_scratch);
+      if (e != cudaSuccess)
+        return set_error(GPIPE_ERR_CUDA, "layernorm_bwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      addr[dev] = static_cast<float*>(p);
+    }
+    scratch = addr[dev];
+  }
+  // Every partial row the reduction reads is written by this call, so nothing
+  // needs clearing first.
+  return launch_layernorm_bwd(dtype, rows, d, dy, x, mean, rstd, g, dres, dx, dg_acc, db_acc, scratch, s);
 }
 
 }  // namespace gp

@@ -55,6 +55,12 @@ int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float*
 int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
                          const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
                          float* db_acc, float* scratch, cudaStream_t stream);
+// LayerNorm backward whose reduction scratch is a fixed static device array
+// (no caller scratch); rejects sizes beyond layernorm_bwd_noalloc_max_floats().
+int launch_layernorm_bwd_noalloc(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                                 const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
+                                 float* db_acc, cudaStream_t stream);
+size_t layernorm_bwd_noalloc_max_floats();
 int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, float* out_acc, float* scratch,
                   cudaStream_t stream);
 

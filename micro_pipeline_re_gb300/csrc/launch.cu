@@ -119,6 +119,13 @@ int gpipe_op_layernorm_bwd(int dtype, int rows, int d, const void* dy, const voi
                                   static_cast<cudaStream_t>(stream));
 }
 
+int gpipe_op_layernorm_bwd_noalloc(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                                   const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
+                                   float* db_acc, void* stream) {
+  return gp::launch_layernorm_bwd_noalloc(dtype, rows, d, dy, x, mean, rstd, g, dres, dx, dg_acc, db_acc,
+                                          static_cast<cudaStream_t>(stream));
+}
+
 int gpipe_op_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, float* out_acc, float* scratch,
                     void* stream) {
   return gp::launch_colsum(dtype, rows, cols, y, ldy, out_acc, scratch, static_cast<cudaStream_t>(stream));
