@@ -39,7 +39,10 @@ enum {
  * So x W^T (W [out,in]) is (a_kmajor=1, b_kmajor=1); dY W is (1, 0); the weight
  * gradient dY^T X is (0, 0).  C, C2, resid and aux are row-major with leading
  * dimension ldc (C, C2), ldr (resid), ldaux (aux); element type = dtype except
- * for the fp32 epilogues.  bias is fp32 [N] or NULL; resid may be NULL.
+ * for the fp32 epilogues.  bias is fp32 [N] (read) or NULL for the forward
+ * epilogues; for GPIPE_EPI_ACC_F32 a non-NULL bias is an fp32 [M] accumulator
+ * that receives += sum_k A(m,k) (the bias gradient that goes with a weight
+ * gradient dY^T X, computed by the same launch).  resid may be NULL.
  * dtype 1 runs the tcgen05/TMEM tensor-core kernel fed by TMA and needs every
  * leading dimension a multiple of 8 elements and 16-byte aligned bases; it is
  * built for (1,1) with STORE, BIAS_GELU, STORE_F32, ACC_F32; (1,0) with STORE,
@@ -50,7 +53,7 @@ int gpipe_op_gemm(int dtype, int M, int N, int K,
                   const void* A, int64_t lda, int a_kmajor,
                   const void* B, int64_t ldb, int b_kmajor,
                   int epi, void* C, int64_t ldc,
-                  const float* bias, const void* resid, int64_t ldr,
+                  float* bias, const void* resid, int64_t ldr,
                   void* C2, const void* aux, int64_t ldaux, void* stream);
 
 /* Bytes of fp32 scratch the two-stage column reductions below need. */

@@ -18,13 +18,15 @@ constexpr int TM = 64, TN = 64, TK = 16;
 template <typename T, int EPI>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const T* __restrict__ A, int64_t lda, int a_k,
                                                         const T* __restrict__ B, int64_t ldb, int b_k, int M, int N,
-                                                        int K, EpiArgs ep) {
+                                                        int K, EpiArgs ep, float* __restrict__ dbias) {
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   const int tid = threadIdx.x;
   const int tx = tid % 16, ty = tid / 16;
   const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
   float acc[4][4] = {};
+  float rowsum[4] = {0.f, 0.f, 0.f, 0.f};  // sum_k A(m,k) for the bias gradient (first N tile)
+  const bool do_db = dbias != nullptr && blockIdx.x == 0 && tx == 0;
   for (int k0 = 0; k0 < K; k0 += TK) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -45,6 +47,12 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const T* __restrict__ A,
       Bs[kk][nn] = vb;
     }
     __syncthreads();
+    if (do_db) {
+#pragma unroll
+      for (int kk = 0; kk < TK; ++kk)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rowsum[i] += As[kk][ty * 4 + i];
+    }
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
       float a[4], b[4];
@@ -58,6 +66,11 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const T* __restrict__ A,
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     __syncthreads();
+  }
+  if (do_db) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (m0 + ty * 4 + i < M) dbias[m0 + ty * 4 + i] += rowsum[i];
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -78,12 +91,13 @@ int run_simt(const GemmDesc& g, cudaStream_t s) {
   const T* A = static_cast<const T*>(g.A);
   const T* B = static_cast<const T*>(g.B);
   int ak = g.a_kmajor ? 1 : 0, bk = g.b_kmajor ? 1 : 0;
+  float* db = g.epi == EPI_ACC_F32 ? g.dbias : nullptr;
   switch (g.epi) {
-    case EPI_STORE: simt_gemm_kernel<T, EPI_STORE><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep); break;
-    case EPI_BIAS_GELU: simt_gemm_kernel<T, EPI_BIAS_GELU><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep); break;
-    case EPI_GELU_BWD: simt_gemm_kernel<T, EPI_GELU_BWD><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep); break;
-    case EPI_ACC_F32: simt_gemm_kernel<T, EPI_ACC_F32><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep); break;
-    case EPI_STORE_F32: simt_gemm_kernel<T, EPI_STORE_F32><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep); break;
+    case EPI_STORE: simt_gemm_kernel<T, EPI_STORE><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_BIAS_GELU: simt_gemm_kernel<T, EPI_BIAS_GELU><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_GELU_BWD: simt_gemm_kernel<T, EPI_GELU_BWD><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_ACC_F32: simt_gemm_kernel<T, EPI_ACC_F32><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_STORE_F32: simt_gemm_kernel<T, EPI_STORE_F32><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
     default: return set_error(GPIPE_ERR_INVALID_ARG, "gemm: unknown epilogue %d", g.epi);
   }
   count_launch();

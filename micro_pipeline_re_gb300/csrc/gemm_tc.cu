@@ -3,24 +3,34 @@
 // C[m,n] = epilogue( sum_k A(m,k) B(n,k) ) with A and B each K-major or
 // MN-major in global memory.  One CTA computes a 128 x BN output tile:
 //   warp 0 / lane 0   TMA producer: 128-byte-swizzled tiles of A and B into a
-//                     ring of STAGES shared-memory stages (mbarrier complete_tx)
+//                     ring of STAGES shared-memory stages (mbarrier complete_tx);
+//                     first it also loads the epilogue's input tile (residual or
+//                     GELU pre-activation) so it lands during the main loop
 //   warp 1 / lane 0   MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16,
-//                     accumulator in tensor memory (BN fp32 columns x 128 lanes),
-//                     tcgen05.commit frees each stage and finally signals the
-//                     epilogue
-//   warps 0..3        epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 rows),
-//                     fused bias / residual / GELU / fp32 accumulate, stores.
+//                     fp32 accumulator in tensor memory; tcgen05.commit frees
+//                     each stage and finally signals the epilogue.  For the
+//                     weight-gradient GEMM of the first N tile it also issues
+//                     an M=128, N=16 MMA against a tile of ones, which leaves
+//                     sum_k A(m,k) (the bias gradient) in TMEM column BN
+//   warps 0..3        epilogue: tcgen05.ld of their 32 TMEM lanes (= rows),
+//                     fused bias / residual / GELU, written into a 128B-swizzled
+//                     shared tile that one thread sends out with TMA stores
+//                     (or, for the fp32 gradient, TMA reduce-add, so the
+//                     read-modify-write happens in L2 and the SM never waits on
+//                     a global read)
 // Every mbarrier wait is bounded (2 s); a timed-out wait sets the library's
 // device error flag and the CTA still releases its tensor memory and waits for
 // its own in-flight copies before exiting.
 //
-// Shared-memory tile layouts (both 128 B swizzle, 1024-B aligned):
+// Shared-memory tile layouts (128 B swizzle, 1024-B aligned):
 //   K-major operand: row r holds k = 0..63 of that row (128 B); 8-row groups
 //     are 1024 B apart (stride byte offset 1024).  The k-th 16-wide slice
 //     starts 32 B into each row.
 //   MN-major operand: 64-wide MN chunks, each [64 k-rows][64 mn] (8 KB);
 //     chunks 8192 B apart (leading byte offset), 8-k-row groups 1024 B apart
 //     (stride byte offset); the k-th 16-deep slice starts 2048 B further.
+//   Epilogue tile: boxes of [128 rows][128 B] (64 bf16 or 32 fp32 columns),
+//     16 KB each; the 16-B unit u of row r sits at r*128 + ((u ^ (r&7)) * 16).
 #include <cuda.h>
 
 #include "../../include/gpipe.h"
@@ -33,36 +43,63 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+constexpr int BOX = 16384;  // one epilogue box: 128 rows x 128 B
 
-template <int BN>
+template <int BN, int EPI>
 struct TcCfg {
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = 4;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
+  static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
+  static constexpr int OUT_BOXES = F32_OUT ? BN / 32 : BN / 64;            // boxes of one output tile
+  static constexpr int EPI_BYTES = (EPI == EPI_BIAS_GELU ? 2 : 1) * OUT_BOXES * BOX;
+  static constexpr int ONES_BYTES = (EPI == EPI_ACC_F32) ? 2048 : 0;
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_ONES = OFF_EPI + EPI_BYTES;
+  static constexpr int OFF_BIAS = OFF_ONES + ONES_BYTES;
+  static constexpr int OFF_BAR = OFF_BIAS + BN * 4;
+  static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
+
+struct TcArgs {
+  const float* bias;  // forward epilogues: fp32 [N] or NULL
+  float* dbias;       // EPI_ACC_F32: fp32 [M] accumulator of sum_k A(m,k), or NULL
+  int M, N, K;
+  int has_x;          // the epilogue input tile (residual / GELU pre-activation) is used
+};
+
+__device__ __forceinline__ uint32_t swz(int r, int unit) {
+  return static_cast<uint32_t>(r * 128 + ((unit ^ (r & 7)) << 4));
+}
 
 template <bool A_K, bool B_K, int BN, int EPI>
 __global__ void __launch_bounds__(128, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiArgs ep,
-                   int K, int* err) {
-  using Cfg = TcCfg<BN>;
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
+                   const __grid_constant__ CUtensorMap tmX, TcArgs args, int* err) {
+  using Cfg = TcCfg<BN, EPI>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
+  uint8_t* sB = smem + Cfg::OFF_B;
+  uint8_t* sE = smem + Cfg::OFF_EPI;
+  uint8_t* sOnes = smem + Cfg::OFF_ONES;
+  float* sBias = reinterpret_cast<float*>(smem + Cfg::OFF_BIAS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* accb = empty + STAGES;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(accb + 1);
+  uint64_t* epib = accb + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(epib + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM;
   const int n0 = blockIdx.x * BN;
-  const int nk = (K + BK - 1) / BK;
+  const int nk = (args.K + BK - 1) / BK;
+  const bool do_db = (EPI == EPI_ACC_F32) && args.dbias != nullptr && blockIdx.x == 0;
+  const uint32_t tcols = do_db ? 256u : static_cast<uint32_t>(BN);
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -72,10 +109,21 @@ __global__ void __launch_bounds__(128, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(accb, 1);
+    mbar_init(epib, 1);
     fence_barrier_init();
   }
+  if (EPI != EPI_ACC_F32 && EPI != EPI_STORE_F32 && EPI != EPI_GELU_BWD) {
+    if (threadIdx.x < BN) {
+      const int n = n0 + threadIdx.x;
+      sBias[threadIdx.x] = (args.bias != nullptr && n < args.N) ? args.bias[n] : 0.f;
+    }
+  }
+  if (do_db) {  // 16 rows x 64 bf16 of 1.0
+    reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
   if (warp == 1) {
-    tmem_alloc(tslot, BN);
+    tmem_alloc(tslot, tcols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -84,6 +132,11 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = *tslot;
 
   if (warp == 0 && lane == 0) {
+    // Epilogue input tile first: it has the whole main loop to arrive.
+    if (args.has_x) {
+      mbar_arrive_expect_tx(epib, (BN / 64) * BOX);
+      for (int b = 0; b < BN / 64; ++b) tma_load_2d(sE + b * BOX, &tmX, n0 + 64 * b, m0, epib);
+    }
     int issued = 0;
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % STAGES;
@@ -110,8 +163,11 @@ __global__ void __launch_bounds__(128, 1)
     // No copy may still be landing in shared memory when the CTA exits.
     for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
       mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1, err, DERR_DRAIN_WAIT);
+    if (args.has_x) mbar_wait_bounded(epib, 0, err, DERR_DRAIN_WAIT);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = mma_idesc_bf16(BM, BN, !A_K, !B_K);
+    constexpr uint32_t idesc_db = mma_idesc_bf16(BM, 16, !A_K, false);
+    const uint32_t ones = smem_u32(sOnes);
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
@@ -123,7 +179,9 @@ __global__ void __launch_bounds__(128, 1)
       for (int kk = 0; kk < BK / 16; ++kk) {
         const uint64_t ad = A_K ? sw128_desc(a + kk * 32, 16, 1024) : sw128_desc(a + kk * 2048, 8192, 1024);
         const uint64_t bd = B_K ? sw128_desc(b + kk * 32, 16, 1024) : sw128_desc(b + kk * 2048, 8192, 1024);
-        tc_mma_f16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+        tc_mma_f16(tmem, ad, bd, idesc, acc);
+        if (do_db) tc_mma_f16(tmem + BN, ad, sw128_desc(ones + kk * 32, 16, 1024), idesc_db, acc);
       }
       tc_commit(&empty[s]);
     }
@@ -131,30 +189,87 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncwarp();
 
-  // Epilogue: warp w owns TMEM lanes 32w..32w+31, i.e. tile rows 32w + lane.
+  // ---- epilogue: warp w owns TMEM lanes 32w..32w+31 = tile rows 32w + lane ----
+  const int r = warp * 32 + lane;
   const bool ok = mbar_wait_bounded(accb, 0, err, DERR_ACC_WAIT);
   tc_fence_after();
-  if (ok) {
-    const int row = m0 + warp * 32 + lane;
-    const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  bool ok_x = true;
+  if (args.has_x) ok_x = mbar_wait_bounded(epib, 0, err, DERR_ACC_WAIT);
+  const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  if (ok && ok_x) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
-      const int col0 = n0 + c * 32;
-      if (col0 >= ep.N) break;  // uniform across the warp
-      uint32_t r[32];
-      tmem_ld32(tbase + c * 32, r);
+      uint32_t rr[32];
+      tmem_ld32(tbase + c * 32, rr);
       tmem_ld_wait();
       float v[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-      if (row < ep.M) epi_row32_bf16<EPI>(ep, row, col0, v);
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
+      if (Cfg::F32_OUT) {
+        uint8_t* box = sE + c * BOX;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4*>(box + swz(r, u)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+      } else {
+        uint8_t* box = sE + (c >> 1) * BOX;
+        const int u0 = (c & 1) * 4;
+        if (EPI == EPI_STORE || EPI == EPI_BIAS_GELU) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += sBias[c * 32 + j];
+        }
+        if (args.has_x) {  // residual (store) or GELU pre-activation (GELU backward)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float t[8];
+            load8(reinterpret_cast<const __nv_bfloat16*>(box + swz(r, u0 + u)), t);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (EPI == EPI_GELU_BWD) v[8 * u + q] *= gelu_grad_f(t[q]);
+              else v[8 * u + q] += t[q];
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) store8(reinterpret_cast<__nv_bfloat16*>(box + swz(r, u0 + u)), v + 8 * u);
+        if (EPI == EPI_BIAS_GELU) {
+          uint8_t* box2 = sE + (Cfg::OUT_BOXES + (c >> 1)) * BOX;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float t[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) t[q] = gelu_f(v[8 * u + q]);
+            store8(reinterpret_cast<__nv_bfloat16*>(box2 + swz(r, u0 + u)), t);
+          }
+        }
+      }
+    }
+    if (do_db) {
+      uint32_t rr[32];
+      tmem_ld32(tbase + BN, rr);
+      tmem_ld_wait();
+      const int m = m0 + r;
+      if (m < args.M) args.dbias[m] += __uint_as_float(rr[0]);
     }
   }
+  fence_proxy_async_smem();
   tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && ok && ok_x) {
+    constexpr int COLS = Cfg::F32_OUT ? 32 : 64;
+    for (int b = 0; b < Cfg::OUT_BOXES; ++b) {
+      const int x = n0 + b * COLS;
+      if (x >= args.N) break;
+      if (EPI == EPI_ACC_F32) tma_reduce_add_2d(&tmC, x, m0, sE + b * BOX);
+      else tma_store_2d(&tmC, x, m0, sE + b * BOX);
+      if (EPI == EPI_BIAS_GELU) tma_store_2d(&tmC2, x, m0, sE + (Cfg::OUT_BOXES + b) * BOX);
+    }
+    bulk_commit();
+    bulk_wait_all();
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, tcols);
   }
 }
 
@@ -178,17 +293,20 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer][inner] with row stride ld elements; box {64, box_outer}.
-bool make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+// 2-D tensor [outer][inner] (row stride ld elements) with a box of
+// box_inner x box_outer elements, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64_t outer, int64_t ld, int box_inner,
+               int box_outer) {
   EncodeFn enc = encode_fn();
   if (!enc) return false;
+  const int es = f32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -197,30 +315,43 @@ int set_attr() {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_K, B_K, BN, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
-    if (e != cudaSuccess) return set_error(-3, "gemm: smem attribute: %s", cudaGetErrorString(e));
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN, EPI>::SMEM);
+    if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
     attr_set = true;
   }
-  return 0;
+  return GPIPE_OK;
 }
 
 template <bool A_K, bool B_K, int BN, int EPI>
 int run(const GemmDesc& g, cudaStream_t stream) {
-  using Cfg = TcCfg<BN>;
-  CUtensorMap ta, tb;
-  bool ok = A_K ? make_tmap(&ta, g.A, g.K, g.M, g.lda, BM) : make_tmap(&ta, g.A, g.M, g.K, g.lda, 64);
-  ok = ok && (B_K ? make_tmap(&tb, g.B, g.K, g.N, g.ldb, BN) : make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64));
-  if (!ok) return set_error(-3, "gemm: cuTensorMapEncodeTiled failed");
+  using Cfg = TcCfg<BN, EPI>;
+  CUtensorMap ta, tb, tc, tc2, tx;
+  bool ok = A_K ? make_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, BM) : make_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
+  ok = ok && (B_K ? make_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, BN)
+                  : make_tmap(&tb, g.B, false, g.N, g.K, g.ldb, 64, 64));
+  ok = ok && make_tmap(&tc, g.C, Cfg::F32_OUT, g.N, g.M, g.ldc, Cfg::F32_OUT ? 32 : 64, BM);
+  tc2 = tc;
+  tx = tc;
+  if (EPI == EPI_BIAS_GELU) ok = ok && make_tmap(&tc2, g.C2, false, g.N, g.M, g.ldc, 64, BM);
+  int has_x = 0;
+  if (EPI == EPI_STORE && g.resid) {
+    ok = ok && make_tmap(&tx, g.resid, false, g.N, g.M, g.ldr, 64, BM);
+    has_x = 1;
+  }
+  if (EPI == EPI_GELU_BWD) {
+    ok = ok && make_tmap(&tx, g.aux, false, g.N, g.M, g.ldaux, 64, BM);
+    has_x = 1;
+  }
+  if (!ok) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed");
   int rc = set_attr<A_K, B_K, BN, EPI>();
   if (rc) return rc;
-  auto kern = tc_gemm_kernel<A_K, B_K, BN, EPI>;
-  EpiArgs ep{g.C, g.ldc, g.bias, g.resid, g.ldr, g.C2, g.aux, g.ldaux, g.M, g.N};
+  TcArgs args{g.bias, g.dbias, g.M, g.N, g.K, has_x};
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
-  kern<<<grid, 128, Cfg::SMEM, stream>>>(ta, tb, ep, g.K, device_error_ptr());
+  tc_gemm_kernel<A_K, B_K, BN, EPI><<<grid, 128, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, tx, args, device_error_ptr());
   count_launch();
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return set_error(-3, "gemm launch: %s", cudaGetErrorString(e));
-  return 0;
+  if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
+  return GPIPE_OK;
 }
 
 // Instantiated combinations: the forward projections and logits (K-major A
@@ -247,7 +378,8 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
       case EPI_ACC_F32: return run<false, false, 128, EPI_ACC_F32>(g, s);
     }
   }
-  return set_error(GPIPE_ERR_UNSUPPORTED, "gemm (tensor core): layout a_kmajor=%d b_kmajor=%d with epilogue %d not built",
+  return set_error(GPIPE_ERR_UNSUPPORTED,
+                   "gemm (tensor core): layout a_kmajor=%d b_kmajor=%d with epilogue %d not built",
                    (int)g.a_kmajor, (int)g.b_kmajor, g.epi);
 }
 
@@ -257,7 +389,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int prepare_gemm_tc() {
   if (!encode_fn()) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled entry point not found");
-  int rc = 0;
+  int rc = GPIPE_OK;
   rc = rc ? rc : set_attr<true, true, 128, EPI_STORE>();
   rc = rc ? rc : set_attr<true, true, 128, EPI_BIAS_GELU>();
   rc = rc ? rc : set_attr<true, true, 128, EPI_STORE_F32>();
@@ -279,11 +411,10 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t stream) {
     return set_error(GPIPE_ERR_INVALID_ARG, "gemm: leading dimension smaller than the matrix");
   if (g.epi == EPI_BIAS_GELU && (!g.C2 || !aligned16(g.C2)))
     return set_error(GPIPE_ERR_INVALID_ARG, "gemm: GELU epilogue needs an aligned C2");
-  if (g.epi == EPI_GELU_BWD && (!g.aux || g.ldaux % 8 || !aligned16(g.aux)))
+  if (g.epi == EPI_GELU_BWD && (!g.aux || g.ldaux % 8 || g.ldaux < g.N || !aligned16(g.aux)))
     return set_error(GPIPE_ERR_INVALID_ARG, "gemm: GELU backward needs an aligned aux");
-  if (g.resid && (g.ldr % 8 || !aligned16(g.resid)))
+  if (g.resid && (g.ldr % 8 || g.ldr < g.N || !aligned16(g.resid)))
     return set_error(GPIPE_ERR_INVALID_ARG, "gemm: residual must be aligned");
-  if (g.bias && !aligned16(g.bias)) return set_error(GPIPE_ERR_INVALID_ARG, "gemm: bias must be 16-B aligned");
   return run_epi(g, stream);
 }
 

@@ -199,7 +199,7 @@ class Executor {
 
   int gemm(int M, int N, int K, const void* A, int64_t lda, bool ak, const void* B, int64_t ldb, bool bk, int epi,
            void* C, int64_t ldc, const float* bias = nullptr, const void* resid = nullptr, int64_t ldr = 0,
-           void* C2 = nullptr, const void* aux = nullptr, int64_t ldaux = 0) {
+           void* C2 = nullptr, const void* aux = nullptr, int64_t ldaux = 0, float* dbias = nullptr) {
     GemmDesc g;
     g.dtype = c_->dm.dtype == 0 ? DT_F32 : DT_BF16;
     g.M = M;
@@ -215,6 +215,7 @@ class Executor {
     g.C = C;
     g.ldc = ldc;
     g.bias = bias;
+    g.dbias = dbias;
     g.resid = resid;
     g.ldr = ldr;
     g.C2 = C2;
@@ -294,11 +295,11 @@ class Executor {
     char* gt = ws(w.gt);
     const void* ffn_in = dm.kind == 1 ? static_cast<const void*>(s.u2) : static_cast<const void*>(s.u);
     // FFN: y = r + W2 GELU(W1 u + b1) + b2
-    TRY(gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f));
-    TRY(launch_colsum(dt, T, d, dy, d, grad(o.b2), scratch, s_));
+    TRY(gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f, nullptr, nullptr, 0, nullptr,
+             nullptr, 0, grad(o.b2)));
     TRY(gemm(T, f, d, dy, d, true, wgt(o.w2), f, false, EPI_GELU_BWD, gf, f, nullptr, nullptr, 0, nullptr, s.z1, f));
-    TRY(gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d));
-    TRY(launch_colsum(dt, T, f, gf, f, grad(o.b1), scratch, s_));
+    TRY(gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d, nullptr, nullptr, 0, nullptr,
+             nullptr, 0, grad(o.b1)));
     TRY(gemm(T, d, f, gf, f, true, wgt(o.w1), d, false, EPI_STORE, gt, d));
     if (dm.kind == 0) {
       return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g),
@@ -310,12 +311,12 @@ class Executor {
     TRY(launch_layernorm_bwd(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g),
                              grad(o.ln2_b), scratch, s_));
     // attention output projection
-    TRY(gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d));
-    TRY(launch_colsum(dt, T, d, gh, d, grad(o.b_o), scratch, s_));
+    TRY(gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d, nullptr, nullptr, 0, nullptr,
+             nullptr, 0, grad(o.b_o)));
     TRY(gemm(T, d, d, gh, d, true, wgt(o.w_o), d, false, EPI_STORE, gt, d));
     TRY(launch_attention_bwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, gt, s.lse, scratch, gq, s_));
-    TRY(gemm(3 * d, d, T, gq, 3 * d, false, s.u, d, false, EPI_ACC_F32, grad(o.w_qkv), d));
-    TRY(launch_colsum(dt, T, 3 * d, gq, 3 * d, grad(o.b_qkv), scratch, s_));
+    TRY(gemm(3 * d, d, T, gq, 3 * d, false, s.u, d, false, EPI_ACC_F32, grad(o.w_qkv), d, nullptr, nullptr, 0,
+             nullptr, nullptr, 0, grad(o.b_qkv)));
     TRY(gemm(T, d, 3 * d, gq, 3 * d, true, wgt(o.w_qkv), d, false, EPI_STORE, gt, d));
     return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh, dx, grad(o.ln1_g),
                                 grad(o.ln1_b), scratch, s_);

@@ -36,7 +36,8 @@ struct GemmDesc {
   int epi = EPI_STORE;
   void* C = nullptr;
   int64_t ldc = 0;
-  const float* bias = nullptr;
+  const float* bias = nullptr;  // forward epilogues: fp32 [N]
+  float* dbias = nullptr;        // EPI_ACC_F32: fp32 [M] accumulator, += sum_k A(m,k)
   const void* resid = nullptr;
   int64_t ldr = 0;
   void* C2 = nullptr;

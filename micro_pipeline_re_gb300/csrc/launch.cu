@@ -77,7 +77,7 @@ using gp::set_error;
 extern "C" {
 
 int gpipe_op_gemm(int dtype, int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
-                  int64_t ldb, int b_kmajor, int epi, void* C, int64_t ldc, const float* bias, const void* resid,
+                  int64_t ldb, int b_kmajor, int epi, void* C, int64_t ldc, float* bias, const void* resid,
                   int64_t ldr, void* C2, const void* aux, int64_t ldaux, void* stream) {
   gp::GemmDesc g;
   g.dtype = dtype;
@@ -93,7 +93,8 @@ int gpipe_op_gemm(int dtype, int M, int N, int K, const void* A, int64_t lda, in
   g.epi = epi;
   g.C = C;
   g.ldc = ldc;
-  g.bias = bias;
+  if (epi == gp::EPI_ACC_F32) g.dbias = bias;  // bias-gradient accumulator
+  else g.bias = bias;
   g.resid = resid;
   g.ldr = ldr;
   g.C2 = C2;

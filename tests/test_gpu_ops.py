@@ -53,12 +53,16 @@ def test_gemm_tensor_core(b, shape, ak, bk, epi):
     if epi in (3, 4):
         C0 = rng.standard_normal((M, N)).astype(np.float32) if epi == 3 else np.zeros((M, N), np.float32)
         dC = dev(C0)
+        db0 = rng.standard_normal(M).astype(np.float32)
+        ddb = dev(db0) if epi == 3 else None   # fused bias gradient: += sum_k A(m,k)
         rc = b.lib().gpipe_op_gemm(1, M, N, K, dA.data_ptr(), lda, ak, dB.data_ptr(), ldb, bk, epi, dC.data_ptr(), N,
-                                   None, None, 0, None, None, 0, stream())
+                                   ddb.data_ptr() if epi == 3 else None, None, 0, None, None, 0, stream())
         assert rc == 0, b.lib().gpipe_last_error(None)
         sync()
         want = acc + (C0 if epi == 3 else 0)
         assert rel(host(dC), want) <= 1e-5
+        if epi == 3:
+            assert rel(host(ddb), db0 + (A if ak else A.T).sum(axis=1)) <= 1e-5
         return
     dC = t.empty((M, N), dtype=t.bfloat16, device="cuda")
     dC2 = t.empty((M, N), dtype=t.bfloat16, device="cuda")
@@ -95,8 +99,11 @@ def test_gemm_fp32_ffma(b, ak, bk, epi):
     C0 = rng.standard_normal((M, N)).astype(np.float32)
     dC, dC2 = dev(C0), dev(np.zeros((M, N), np.float32))
     keep = [dev(A), dev(B), dev(bias), dev(resid), dev(aux)]  # hold device buffers until the kernel ran
+    db0 = rng.standard_normal(M).astype(np.float32)
+    ddb = dev(db0)
     rc = b.lib().gpipe_op_gemm(0, M, N, K, keep[0].data_ptr(), A.shape[1], ak, keep[1].data_ptr(), B.shape[1], bk,
-                               epi, dC.data_ptr(), N, keep[2].data_ptr() if epi < 2 else None,
+                               epi, dC.data_ptr(), N,
+                               keep[2].data_ptr() if epi < 2 else (ddb.data_ptr() if epi == 3 else None),
                                keep[3].data_ptr() if epi == 0 else None, N, dC2.data_ptr() if epi == 1 else None,
                                keep[4].data_ptr() if epi == 2 else None, N, stream())
     assert rc == 0
@@ -110,6 +117,7 @@ def test_gemm_fp32_ffma(b, ak, bk, epi):
         assert rel(host(dC), acc * om.gelu_grad(aux)) <= 1e-6
     else:
         assert rel(host(dC), C0 + acc) <= 1e-6
+        assert rel(host(ddb), db0 + (A if ak else A.T).astype(np.float64).sum(axis=1)) <= 1e-6
 
 
 def test_gemm_rejects_misaligned_leading_dimension(b):
