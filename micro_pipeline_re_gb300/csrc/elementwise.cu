@@ -15,7 +15,7 @@ namespace {
 
 constexpr float kLnEps = 1e-5f;
 constexpr int kMaxChunks = 4;       // d <= 4 * 256 = 1024 per warp-row
-constexpr int kLnRowsPerWarp = 8;   // rows one warp folds into one partial row
+constexpr int kLnRowsPerWarp = 8;   // rows one block (8 warps) folds into one partial row
 constexpr int kColRowsPerChunk = 32;
 
 inline int blocks_for(size_t n, int per_block) { return static_cast<int>((n + per_block - 1) / per_block); }
@@ -87,25 +87,27 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, co
 }
 
 // ---------------------------------------------------------------------------
-// LayerNorm backward.  Warp w of block b handles rows
-// (b*4 + w)*R .. +R-1 (R = kLnRowsPerWarp) and writes one partial row of
-// [dg | db] sums into scratch; col_reduce then adds the partial rows in order.
+// LayerNorm backward.  Block b (8 warps) handles rows 8b .. 8b+7, one row per
+// warp; the warps then add their [dg | db] column sums into shared memory in
+// warp order and the block writes one partial row of scratch; col_reduce adds
+// the partial rows in order.  Both orders are fixed, so results are
+// bit-reproducible.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(128) ln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+__global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
                                                      const float* __restrict__ mean, const float* __restrict__ rstd,
                                                      const float* __restrict__ g, const T* __restrict__ dres,
                                                      T* __restrict__ dx, float* __restrict__ partial, int rows,
                                                      int d) {
+  __shared__ __align__(16) float acc_s[2 * 32 * 8 * kMaxChunks];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pw = blockIdx.x * 4 + warp;  // partial row index
-  const int r0 = pw * kLnRowsPerWarp;
+  const int r = blockIdx.x * kLnRowsPerWarp + warp;
   float pg[kMaxChunks][8], pb[kMaxChunks][8];
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c)
 #pragma unroll
     for (int j = 0; j < 8; ++j) pg[c][j] = pb[c][j] = 0.f;
-  for (int r = r0; r < min(r0 + kLnRowsPerWarp, rows); ++r) {
+  if (r < rows) {
     const float mu = mean[r], rs = rstd[r];
     float xh[kMaxChunks][8], gd[kMaxChunks][8];
     float s1 = 0.f, s2 = 0.f;
@@ -123,8 +125,8 @@ __global__ void __launch_bounds__(128) ln_bwd_kernel(const T* __restrict__ dy, c
           gd[c][j] = gg[j] * dv[j];
           s1 += gd[c][j];
           s2 += gd[c][j] * xh[c][j];
-          pg[c][j] += dv[j] * xh[c][j];
-          pb[c][j] += dv[j];
+          pg[c][j] = dv[j] * xh[c][j];
+          pb[c][j] = dv[j];
         }
       }
     }
@@ -146,17 +148,31 @@ __global__ void __launch_bounds__(128) ln_bwd_kernel(const T* __restrict__ dy, c
       }
     }
   }
-  if (r0 < rows) {
-    float* pr = partial + (int64_t)pw * 2 * d;
+  // fold the 8 warps' column sums in warp order
+  for (int w = 0; w < 8; ++w) {
+    if (warp == w) {
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
-      const int col = (c * 32 + lane) * 8;
-      if (col < d) {
-        store8(pr + col, pg[c]);
-        store8(pr + d + col, pb[c]);
+      for (int c = 0; c < kMaxChunks; ++c) {
+        const int col = (c * 32 + lane) * 8;
+        if (col < d) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (w == 0) {
+              acc_s[col + j] = pg[c][j];
+              acc_s[d + col + j] = pb[c][j];
+            } else {
+              acc_s[col + j] += pg[c][j];
+              acc_s[d + col + j] += pb[c][j];
+            }
+          }
+        }
       }
     }
+    __syncthreads();
   }
+  float* pr = partial + (int64_t)blockIdx.x * 2 * d;
+  for (int i = threadIdx.x * 4; i < 2 * d; i += 256 * 4)
+    *reinterpret_cast<float4*>(pr + i) = *reinterpret_cast<const float4*>(acc_s + i);
 }
 
 // out[c] += sum_{p < nparts} partial[p*ncols + c], fixed order (4 interleaved
@@ -476,13 +492,13 @@ int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void*
   if (!al16(dy) || !al16(x) || !al16(dx) || !al16(g) || (dres && !al16(dres)) || !al16(scratch))
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: pointers must be 16-B aligned");
   const int parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
-  const int grid = (parts + 3) / 4;
+  const int grid = parts;
   if (dtype == DT_F32)
-    ln_bwd_kernel<float><<<grid, 128, 0, s>>>(static_cast<const float*>(dy), static_cast<const float*>(x), mean,
+    ln_bwd_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(dy), static_cast<const float*>(x), mean,
                                               rstd, g, static_cast<const float*>(dres), static_cast<float*>(dx),
                                               scratch, rows, d);
   else
-    ln_bwd_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
+    ln_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean, rstd, g,
         static_cast<const __nv_bfloat16*>(dres), static_cast<__nv_bfloat16*>(dx), scratch, rows, d);
   int rc = check_launch("layernorm_bwd");
