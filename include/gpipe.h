@@ -159,7 +159,10 @@ enum {
                                 internals of every cell and count the bytes that
                                 differ from the re-computed ones
                                 (gpipe_debug_counters); set before gpipe_sizes       */
-  GPIPE_OPT_SKIP_UPDATE = 5  /* [0] 1: accumulate gradients but apply no update      */
+  GPIPE_OPT_SKIP_UPDATE = 5, /* [0] 1: accumulate gradients but apply no update     */
+  GPIPE_OPT_CONCURRENT = 6   /* [1] run weight-gradient GEMMs and the loss-only head
+                                forward on a second stream (ordered by events); 0:
+                                one stream in program order.  Results are identical. */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

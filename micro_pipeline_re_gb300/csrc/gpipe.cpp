@@ -64,6 +64,9 @@ struct gpipe_ctx {
   // state
   std::string err = "no error";
   cudaStream_t cap_stream = nullptr;
+  bool concurrent = true;              // weight gradients and loss-only head on a side stream
+  cudaStream_t side_stream = nullptr;
+  cudaEvent_t ev[8] = {};
   cudaGraphExec_t gexec = nullptr;
   cudaGraph_t graph = nullptr;
   GraphKey key{};
@@ -87,6 +90,17 @@ struct gpipe_ctx {
       ws_stale = false;
     }
   }
+  // side stream and its events (created on first use, on the current device)
+  int ensure_side() {
+    if (!concurrent) return GPIPE_OK;
+    if (!side_stream && cudaStreamCreateWithFlags(&side_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return fail(GPIPE_ERR_CUDA, "cannot create the side stream");
+    for (auto& e : ev)
+      if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+        return fail(GPIPE_ERR_CUDA, "cannot create an event");
+    return GPIPE_OK;
+  }
+  cudaStream_t side() const { return concurrent ? side_stream : nullptr; }
   void drop_graph() {
     if (gexec) cudaGraphExecDestroy(gexec);
     if (graph) cudaGraphDestroy(graph);
@@ -110,9 +124,14 @@ struct Slot {
   float *mean1, *rstd1, *mean2, *rstd2, *lse;
 };
 
+// Events that order the side stream against the main stream.
+enum { EV_FORK, EV_GF, EV_GH, EV_GQ, EV_DY0, EV_DY1, EV_HEAD, EV_HEADF, EV_COUNT };
+
 class Executor {
  public:
-  Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t s) : c_(c), p_(p), s_(s) {}
+  // side == nullptr runs everything on s in program order.
+  Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t s, cudaStream_t side)
+      : c_(c), p_(p), s_(s), side_(side), cur_(s) {}
 
   int run_step() {
     const Workspace& w = c_->ws;
@@ -120,30 +139,40 @@ class Executor {
     // zero the loss scalar and the debug counter
     if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, s_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
-    // phase 1: forward of every micro-batch through every cell
+    // phase 1: forward of every micro-batch through every cell; the loss-only
+    // head forward of micro-batch m runs on the side stream while cell 0
+    // starts micro-batch m+1
     for (int m = 0; m < M; ++m) {
       TRY(cell0_input(m));
       for (int k = 0; k < K; ++k) TRY(cell_forward(k, m, /*recompute=*/false));
+      TRY(fork());
+      cur_ = side();
       TRY(head(m, /*backward=*/false));
+      cur_ = s_;
+      TRY(mark(EV_HEADF));
     }
+    TRY(join_all());
     // phase 2: backward with re-computation, micro-batches ascending, cells K-1..0
     for (int m = 0; m < M; ++m) {
-      char* dy = ws(w.g0);
-      char* dx = ws(w.g1);
+      dyi_ = 0;
       for (int k = K - 1; k >= 0; --k) {
+        TRY(join_all());  // side work still reading this micro-batch's slots / logits
         if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
-        if (k == K - 1) TRY(head_backward(m, dy));
+        if (k == K - 1) TRY(head_backward(m, gbuf(dyi_)));
         const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
         for (int j = n - 1; j >= 0; --j) {
           const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
-          TRY(layer_backward(first + j, x, slot(k, m, j), dy, dx));
-          std::swap(dy, dx);
+          TRY(layer_backward(first + j, x, slot(k, m, j), gbuf(dyi_), gbuf(1 - dyi_)));
+          dyi_ = 1 - dyi_;
         }
-        if (k == 0 && c_->dm.kind == 1)
-          TRY(launch_embedding_bwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), dy,
+        if (k == 0 && c_->dm.kind == 1) {
+          TRY(join(EV_HEAD));  // the head's dE accumulation (side) before the embedding's (main)
+          TRY(launch_embedding_bwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), gbuf(dyi_),
                                    grad(c_->pl.emb), s_));
+        }
       }
     }
+    TRY(join_all());
     // phase 3: one update after all micro-batches
     if (!c_->skip_update)
       TRY(launch_rmsprop(c_->pl.total, p_.p32, p_.g32, p_.v32, c_->dm.dtype == 1 ? p_.p16 : nullptr, c_->dm.lr,
@@ -155,7 +184,48 @@ class Executor {
  private:
   gpipe_ctx* c_;
   StepPtrs p_;
-  cudaStream_t s_;
+  cudaStream_t s_;     // main stream (critical path)
+  cudaStream_t side_;  // weight gradients / loss-only head, or nullptr
+  cudaStream_t cur_;   // stream the gemm() helper launches on
+  bool rec_[EV_COUNT] = {};
+  int dyi_ = 0;        // which of the two gradient buffers holds dy
+
+  cudaStream_t side() const { return side_ ? side_ : s_; }
+  char* gbuf(int i) const { return ws(i == 0 ? c_->ws.g0 : c_->ws.g1); }
+  int cuda_ok(cudaError_t e, const char* what) {
+    return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  }
+  // side stream starts after everything issued so far on the main stream
+  int fork() {
+    if (!side_) return GPIPE_OK;
+    TRY(cuda_ok(cudaEventRecord(c_->ev[EV_FORK], s_), "event record"));
+    return cuda_ok(cudaStreamWaitEvent(side_, c_->ev[EV_FORK], 0), "stream wait");
+  }
+  // mark the side stream's progress so far with event e
+  int mark(int e) {
+    if (!side_) return GPIPE_OK;
+    rec_[e] = true;
+    return cuda_ok(cudaEventRecord(c_->ev[e], side_), "event record");
+  }
+  // main stream waits for the side work marked by e
+  int join(int e) {
+    if (!side_ || !rec_[e]) return GPIPE_OK;
+    return cuda_ok(cudaStreamWaitEvent(s_, c_->ev[e], 0), "stream wait");
+  }
+  int join_all() {
+    for (int e = EV_GF; e < EV_COUNT; ++e) TRY(join(e));
+    return GPIPE_OK;
+  }
+  // run a weight-gradient GEMM on the side stream, marking event e afterwards
+  template <typename F>
+  int on_side(int e, F&& f) {
+    TRY(fork());
+    cur_ = side();
+    int rc = f();
+    cur_ = s_;
+    if (rc) return rc;
+    return mark(e);
+  }
 
   char* ws(size_t off) const { return p_.ws + off; }
   const float* p32(size_t off) const { return p_.p32 + off; }
@@ -221,7 +291,7 @@ class Executor {
     g.C2 = C2;
     g.aux = aux;
     g.ldaux = ldaux;
-    return launch_gemm(g, s_);
+    return launch_gemm(g, cur_);
   }
 
   int cell0_input(int m) {
@@ -294,30 +364,47 @@ class Executor {
     char* gf = ws(w.gf);
     char* gt = ws(w.gt);
     const void* ffn_in = dm.kind == 1 ? static_cast<const void*>(s.u2) : static_cast<const void*>(s.u);
+    // dy is gradient buffer dyi_, dx the other one.  Weight gradients run on
+    // the side stream; before the main stream overwrites a buffer that a side
+    // GEMM reads, it joins that GEMM's event.
+    const int ev_dy = dyi_ ? EV_DY1 : EV_DY0, ev_dx = dyi_ ? EV_DY0 : EV_DY1;
     // FFN: y = r + W2 GELU(W1 u + b1) + b2
-    TRY(gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f, nullptr, nullptr, 0, nullptr,
-             nullptr, 0, grad(o.b2)));
+    TRY(on_side(ev_dy, [&] {
+      return gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f, nullptr, nullptr, 0, nullptr,
+                  nullptr, 0, grad(o.b2));
+    }));
+    TRY(join(EV_GF));
     TRY(gemm(T, f, d, dy, d, true, wgt(o.w2), f, false, EPI_GELU_BWD, gf, f, nullptr, nullptr, 0, nullptr, s.z1, f));
-    TRY(gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d, nullptr, nullptr, 0, nullptr,
-             nullptr, 0, grad(o.b1)));
+    TRY(on_side(EV_GF, [&] {
+      return gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d, nullptr, nullptr, 0, nullptr,
+                  nullptr, 0, grad(o.b1));
+    }));
     TRY(gemm(T, d, f, gf, f, true, wgt(o.w1), d, false, EPI_STORE, gt, d));
     if (dm.kind == 0) {
+      TRY(join(ev_dx));
       return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g),
                                   grad(o.ln1_b), scratch, s_);
     }
     char* gh = ws(w.gh);
     char* gq = ws(w.gq);
     // h1 -> LN2: dh1 = LN2'(du2) + dy
+    TRY(join(EV_GH));
     TRY(launch_layernorm_bwd(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g),
                              grad(o.ln2_b), scratch, s_));
     // attention output projection
-    TRY(gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d, nullptr, nullptr, 0, nullptr,
-             nullptr, 0, grad(o.b_o)));
+    TRY(on_side(EV_GH, [&] {
+      return gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d, nullptr, nullptr, 0, nullptr,
+                  nullptr, 0, grad(o.b_o));
+    }));
     TRY(gemm(T, d, d, gh, d, true, wgt(o.w_o), d, false, EPI_STORE, gt, d));
+    TRY(join(EV_GQ));
     TRY(launch_attention_bwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, gt, s.lse, scratch, gq, s_));
-    TRY(gemm(3 * d, d, T, gq, 3 * d, false, s.u, d, false, EPI_ACC_F32, grad(o.w_qkv), d, nullptr, nullptr, 0,
-             nullptr, nullptr, 0, grad(o.b_qkv)));
+    TRY(on_side(EV_GQ, [&] {
+      return gemm(3 * d, d, T, gq, 3 * d, false, s.u, d, false, EPI_ACC_F32, grad(o.w_qkv), d, nullptr, nullptr, 0,
+                  nullptr, nullptr, 0, grad(o.b_qkv));
+    }));
     TRY(gemm(T, d, 3 * d, gq, 3 * d, true, wgt(o.w_qkv), d, false, EPI_STORE, gt, d));
+    TRY(join(ev_dx));
     return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh, dx, grad(o.ln1_g),
                                 grad(o.ln1_b), scratch, s_);
   }
@@ -334,21 +421,23 @@ class Executor {
       const float inv = 1.0f / (static_cast<float>(dm.n) * d);
       const float* t = static_cast<const float*>(p_.targets) + static_cast<size_t>(m) * T * d;
       float* dyp = backward ? reinterpret_cast<float*>(dy) : reinterpret_cast<float*>(ws(w.g1));
-      return launch_mse(T, d, reinterpret_cast<const float*>(xf), t, inv, loss_rows, dyp, s_);
+      return launch_mse(T, d, reinterpret_cast<const float*>(xf), t, inv, loss_rows, dyp, cur_);
     }
     const float inv = 1.0f / (static_cast<float>(dm.n) * (dm.seq - 1));
     float* logits = reinterpret_cast<float*>(ws(w.logits));
     TRY(launch_layernorm_fwd(DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(w.hf),
-                             reinterpret_cast<float*>(ws(w.meanf)), reinterpret_cast<float*>(ws(w.rstdf)), s_));
+                             reinterpret_cast<float*>(ws(w.meanf)), reinterpret_cast<float*>(ws(w.rstdf)), cur_));
     TRY(gemm(T, dm.vocab, d, ws(w.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
     TRY(launch_cross_entropy(T, dm.vocab, dm.seq, static_cast<const int32_t*>(p_.batch), m * T, inv, logits,
-                             loss_rows, backward ? 1 : 0, s_));
+                             loss_rows, backward ? 1 : 0, cur_));
     if (!backward) return GPIPE_OK;
     // dz (bf16, in place over the logits, leading dimension 2*vocab)
     const int64_t ldz = 2 * static_cast<int64_t>(dm.vocab);
     char* gt = ws(w.gt);
     TRY(gemm(T, d, dm.vocab, logits, ldz, true, wgt(c_->pl.emb), d, false, EPI_STORE, gt, d));
-    TRY(gemm(dm.vocab, d, T, logits, ldz, false, ws(w.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d));
+    TRY(on_side(EV_HEAD, [&] {
+      return gemm(dm.vocab, d, T, logits, ldz, false, ws(w.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d);
+    }));
     return launch_layernorm_bwd(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(w.meanf)),
                                 reinterpret_cast<float*>(ws(w.rstdf)), p32(c_->pl.lnf_g), nullptr, dy,
                                 grad(c_->pl.lnf_g), grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(w.scratch)),
@@ -474,8 +563,10 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StepPtrs ptrs{p32, p16, g32, v32, batch, targets, static_cast<char*>(workspace)};
   if (!c->use_graph) {
+    rc = c->ensure_side();
+    if (rc) return rc;
     const int64_t before = launch_count();
-    Executor ex(c, ptrs, s);
+    Executor ex(c, ptrs, s, c->side());
     rc = ex.run_step();
     if (rc) return c->fail_from_launch(rc);
     c->launches_per_step = launch_count() - before;
@@ -486,14 +577,17 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[1] = c->no_remat;
     key.opts[2] = c->skip_update;
     key.opts[3] = c->remat_check_m;
+    key.opts[4] = c->concurrent;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
         return c->fail(GPIPE_ERR_CUDA, "cannot create the capture stream");
       if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
         return c->fail(GPIPE_ERR_CUDA, "cudaStreamBeginCapture failed");
+      rc = c->ensure_side();
+      if (rc) return rc;
       const int64_t before = launch_count();
-      Executor ex(c, ptrs, c->cap_stream);
+      Executor ex(c, ptrs, c->cap_stream, c->side());
       rc = ex.run_step();
       cudaGraph_t g = nullptr;
       cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &g);
@@ -573,6 +667,7 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
       c->ws_stale = true;
       break;
     case GPIPE_OPT_SKIP_UPDATE: c->skip_update = value != 0; break;
+    case GPIPE_OPT_CONCURRENT: c->concurrent = value != 0; break;
     default: return c->fail(GPIPE_ERR_INVALID_ARG, "unknown option");
   }
   c->drop_graph();
@@ -617,6 +712,9 @@ void gpipe_destroy(gpipe_ctx* c) {
   if (!c) return;
   c->drop_graph();
   if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+  if (c->side_stream) cudaStreamDestroy(c->side_stream);
+  for (auto& e : c->ev)
+    if (e) cudaEventDestroy(e);
   delete c;
 }
 

@@ -155,6 +155,20 @@ def test_steps_are_bit_reproducible_and_graph_equals_direct(b):
         assert np.array_equal(o[2], outs[0][2])
 
 
+def test_concurrent_schedule_is_bit_identical_to_serial(b):
+    """Weight gradients on a side stream (events order every shared buffer)
+    give exactly the single-stream result, with and without the CUDA graph."""
+    for w in (SMALL_LM, WORKLOADS["tiny_ffn"]):
+        inp = make_inputs(w)
+        outs = []
+        for conc, graph in ((0, 1), (1, 1), (1, 0)):
+            _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_CONCURRENT, conc), (b.OPT_GRAPH, graph)])
+            outs.append((loss, st.g32.cpu().numpy().copy()))
+        for o in outs[1:]:
+            assert o[0] == outs[0][0]
+            assert np.array_equal(o[1], outs[0][1])
+
+
 def test_no_rematerialisation_mode_is_identical(b):
     w = SMALL_LM
     inp = make_inputs(w)
