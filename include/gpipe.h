@@ -160,9 +160,14 @@ enum {
                                 differ from the re-computed ones
                                 (gpipe_debug_counters); set before gpipe_sizes       */
   GPIPE_OPT_SKIP_UPDATE = 5, /* [0] 1: accumulate gradients but apply no update     */
-  GPIPE_OPT_CONCURRENT = 6   /* [1] run weight-gradient GEMMs and the loss-only head
-                                forward on a second stream (ordered by events); 0:
-                                one stream in program order.  Results are identical. */
+  GPIPE_OPT_CONCURRENT = 6,  /* [1] run weight-gradient GEMMs and the loss-only head
+                                forward on a second stream per lane (ordered by
+                                events); 0: in program order.  Results are identical. */
+  GPIPE_OPT_PIPELINE = 7     /* [1] run the K cells as K concurrent lanes, each with its
+                                own cell workspace: cell k works on micro-batch m while
+                                cell k+1 works on m-1, as the review's K accelerators
+                                do; 0: one lane, cells in turn (least memory).  Results
+                                are identical.  Set before gpipe_sizes. */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

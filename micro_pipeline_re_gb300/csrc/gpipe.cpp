@@ -64,9 +64,14 @@ struct gpipe_ctx {
   // state
   std::string err = "no error";
   cudaStream_t cap_stream = nullptr;
-  bool concurrent = true;              // weight gradients and loss-only head on a side stream
-  cudaStream_t side_stream = nullptr;
-  cudaEvent_t ev[8] = {};
+  bool concurrent = true;  // weight gradients and the loss-only head on each lane's side stream
+  bool pipelined = true;   // cells run as concurrent lanes (the review's pipeline on one GPU)
+  static constexpr int kMaxLanes = 64;
+  static constexpr int kLaneEvents = 9;
+  cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
+  cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
+  cudaEvent_t ev_origin = nullptr, ev_fwd[kMaxLanes] = {}, ev_bdone[kMaxLanes][2] = {}, ev_bfree[kMaxLanes][2] = {},
+              ev_lane_end[kMaxLanes] = {};
   cudaGraphExec_t gexec = nullptr;
   cudaGraph_t graph = nullptr;
   GraphKey key{};
@@ -86,21 +91,29 @@ struct gpipe_ctx {
   }
   void refresh_ws() {
     if (ws_stale) {
-      ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat);
+      ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat,
+                          pipelined && K <= kMaxLanes);
       ws_stale = false;
     }
   }
-  // side stream and its events (created on first use, on the current device)
-  int ensure_side() {
-    if (!concurrent) return GPIPE_OK;
-    if (!side_stream && cudaStreamCreateWithFlags(&side_stream, cudaStreamNonBlocking) != cudaSuccess)
-      return fail(GPIPE_ERR_CUDA, "cannot create the side stream");
-    for (auto& e : ev)
-      if (!e && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
-        return fail(GPIPE_ERR_CUDA, "cannot create an event");
-    return GPIPE_OK;
+  // lane streams and events (created on first use, on the current device)
+  int ensure_lanes() {
+    auto mk_ev = [&](cudaEvent_t& e) {
+      return e || cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+    };
+    auto mk_st = [&](cudaStream_t& st) {
+      return st || cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
+    };
+    bool ok = mk_ev(ev_origin);
+    for (int i = 0; i < ws.nlanes && ok; ++i) {
+      ok = mk_st(lane_main[i]) && mk_st(lane_side[i]) && mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
+      for (int e = 0; e < kLaneEvents && ok; ++e) ok = mk_ev(lane_ev[i][e]);
+    }
+    for (int k = 0; k < K && k < kMaxLanes && ok; ++k)
+      ok = mk_ev(ev_bdone[k][0]) && mk_ev(ev_bdone[k][1]) && mk_ev(ev_bfree[k][0]) && mk_ev(ev_bfree[k][1]) &&
+           mk_ev(ev_fwd[k]);
+    return ok ? GPIPE_OK : fail(GPIPE_ERR_CUDA, "cannot create the lane streams/events");
   }
-  cudaStream_t side() const { return concurrent ? side_stream : nullptr; }
   void drop_graph() {
     if (gexec) cudaGraphExecDestroy(gexec);
     if (graph) cudaGraphDestroy(graph);
@@ -124,107 +137,173 @@ struct Slot {
   float *mean1, *rstd1, *mean2, *rstd2, *lse;
 };
 
-// Events that order the side stream against the main stream.
-enum { EV_FORK, EV_GF, EV_GH, EV_GQ, EV_DY0, EV_DY1, EV_HEAD, EV_HEADF, EV_COUNT };
+// Events that order a lane's side stream against its main stream.
+enum { EV_FORK, EV_GF, EV_GH, EV_GQ, EV_DY0, EV_DY1, EV_DYB, EV_HEAD, EV_HEADF, EV_COUNT };
+constexpr int BUF_EXT = 2;  // "dy lives outside the lane" (boundary ring / head output)
 
+// Issues one step.  Host issue order is the serial GPipe order (phase 1:
+// micro-batch-major forward; phase 2: micro-batch-major backward, cells K-1..0;
+// phase 3: update).  When the cells are pipelined, cell k's work goes to lane
+// k's streams, and events carry exactly the dependencies of the review's
+// pipeline: cell k forwards micro-batch m after cell k-1 handed it m; cell k
+// differentiates m after cell k+1 handed it the gradient of m; a lane
+// processes micro-batches in order.  So cell k can work on micro-batch m while
+// cell k+1 works on m-1, as the review's K accelerators do.  Per-cell
+// weight-gradient accumulation stays in micro-batch order on one stream, so
+// the result does not depend on the interleaving.
 class Executor {
  public:
-  // side == nullptr runs everything on s in program order.
-  Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t s, cudaStream_t side)
-      : c_(c), p_(p), s_(s), side_(side), cur_(s) {}
+  Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t origin) : c_(c), p_(p), origin_(origin) {}
 
   int run_step() {
     const Workspace& w = c_->ws;
     const int M = c_->M, K = c_->K;
-    // zero the loss scalar and the debug counter
-    if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, s_) != cudaSuccess)
+    // zero the loss scalar and the debug counter, then start every lane
+    if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, origin_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
-    // phase 1: forward of every micro-batch through every cell; the loss-only
-    // head forward of micro-batch m runs on the side stream while cell 0
-    // starts micro-batch m+1
+    TRY(cuda_ok(cudaEventRecord(c_->ev_origin, origin_), "event record"));
+    for (int i = 0; i < w.nlanes; ++i)
+      TRY(cuda_ok(cudaStreamWaitEvent(c_->lane_main[i], c_->ev_origin, 0), "stream wait"));
+
+    // phase 1: forward of every micro-batch through every cell
     for (int m = 0; m < M; ++m) {
       TRY(cell0_input(m));
-      for (int k = 0; k < K; ++k) TRY(cell_forward(k, m, /*recompute=*/false));
-      TRY(fork());
-      cur_ = side();
-      TRY(head(m, /*backward=*/false));
-      cur_ = s_;
-      TRY(mark(EV_HEADF));
+      for (int k = 0; k < K; ++k) {
+        if (k > 0) TRY(cross_wait(k, c_->ev_fwd[k - 1], fwd_rec_[k - 1], k - 1));
+        TRY(cell_forward(k, m, /*recompute=*/false));
+        if (k < K - 1) TRY(cross_record(k, c_->ev_fwd[k], fwd_rec_[k]));
+      }
+      // loss-only head forward on the last lane's side stream
+      const int lk = lane_of(K - 1);
+      TRY(fork(lk));
+      cur_ = side(lk);
+      TRY(head(m, /*backward=*/false, nullptr));
+      cur_ = nullptr;
+      TRY(mark(lk, EV_HEADF));
     }
-    TRY(join_all());
-    // phase 2: backward with re-computation, micro-batches ascending, cells K-1..0
+    // phase 2: backward with re-computation
     for (int m = 0; m < M; ++m) {
-      dyi_ = 0;
+      const int p = m & 1;
       for (int k = K - 1; k >= 0; --k) {
-        TRY(join_all());  // side work still reading this micro-batch's slots / logits
+        const int lk = lane_of(k);
+        cur_lane_ = lk;
+        TRY(join_all(lk));  // side work still reading this lane's slots / head buffers
         if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
-        if (k == K - 1) TRY(head_backward(m, gbuf(dyi_)));
+        // gradient of the cell's output
+        char* dy;
+        int dy_buf;
+        if (k == K - 1) {
+          dy = lbuf(lk, 0);
+          dy_buf = 0;
+          TRY(head(m, /*backward=*/true, dy));
+        } else {
+          TRY(cross_wait(k, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
+          dy = bgrad(k + 1, p);
+          dy_buf = BUF_EXT;
+        }
         const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
         for (int j = n - 1; j >= 0; --j) {
           const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
-          TRY(layer_backward(first + j, x, slot(k, m, j), gbuf(dyi_), gbuf(1 - dyi_)));
-          dyi_ = 1 - dyi_;
+          char* dx;
+          int dx_buf;
+          if (j == 0 && k > 0) {
+            // hand the input gradient to cell k-1 through the ring
+            if (bfree_rec_[k][p]) TRY(cross_wait(k, c_->ev_bfree[k][p], bfree_rec_[k][p], k - 1));
+            dx = bgrad(k, p);
+            dx_buf = BUF_EXT;
+          } else if (j == 0 && c_->dm.kind == 1) {
+            dx = dx0(m);  // the embedding's input gradient, scattered once at the end
+            dx_buf = BUF_EXT;
+          } else {
+            dx_buf = dy_buf == 0 ? 1 : 0;
+            dx = lbuf(lk, dx_buf);
+          }
+          TRY(layer_backward(first + j, x, slot(k, m, j), dy, dy_buf, dx, dx_buf));
+          dy = dx;
+          dy_buf = dx_buf;
         }
-        if (k == 0 && c_->dm.kind == 1) {
-          TRY(join(EV_HEAD));  // the head's dE accumulation (side) before the embedding's (main)
-          TRY(launch_embedding_bwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), gbuf(dyi_),
-                                   grad(c_->pl.emb), s_));
+        if (k > 0) TRY(cross_record(k, c_->ev_bdone[k][p], bdone_rec_[k][p]));
+        if (k < K - 1) {  // this cell has finished reading the ring slot of cell k+1
+          TRY(join(lk, EV_DYB));
+          TRY(cross_record(k, c_->ev_bfree[k + 1][p], bfree_rec_[k + 1][p]));
         }
       }
     }
-    TRY(join_all());
-    // phase 3: one update after all micro-batches
+    // every lane (and its side stream) back into the origin stream
+    for (int i = 0; i < w.nlanes; ++i) {
+      TRY(join_all(i));
+      TRY(cuda_ok(cudaEventRecord(c_->ev_lane_end[i], c_->lane_main[i]), "event record"));
+      TRY(cuda_ok(cudaStreamWaitEvent(origin_, c_->ev_lane_end[i], 0), "stream wait"));
+    }
+    // phase 3: the embedding scatter of all micro-batches (after the head's
+    // contributions, in token order), then one update of every parameter
+    if (c_->dm.kind == 1)
+      TRY(launch_embedding_bwd(static_cast<int>(c_->T()), c_->dm.d, c_->dm.vocab,
+                               static_cast<const int32_t*>(p_.batch), dx0(0), grad(c_->pl.emb), origin_));
     if (!c_->skip_update)
       TRY(launch_rmsprop(c_->pl.total, p_.p32, p_.g32, p_.v32, c_->dm.dtype == 1 ? p_.p16 : nullptr, c_->dm.lr,
-                         c_->dm.decay, c_->dm.eps, c_->keep_grads ? 0 : 1, s_));
-    TRY(launch_sum(reinterpret_cast<float*>(ws(w.loss_rows)), c_->T(), reinterpret_cast<float*>(ws(w.misc)), s_));
+                         c_->dm.decay, c_->dm.eps, c_->keep_grads ? 0 : 1, origin_));
+    TRY(launch_sum(reinterpret_cast<float*>(ws(w.loss_rows)), c_->T(), reinterpret_cast<float*>(ws(w.misc)),
+                   origin_));
     return GPIPE_OK;
   }
 
  private:
   gpipe_ctx* c_;
   StepPtrs p_;
-  cudaStream_t s_;     // main stream (critical path)
-  cudaStream_t side_;  // weight gradients / loss-only head, or nullptr
-  cudaStream_t cur_;   // stream the gemm() helper launches on
-  bool rec_[EV_COUNT] = {};
-  int dyi_ = 0;        // which of the two gradient buffers holds dy
+  cudaStream_t origin_;
+  cudaStream_t cur_ = nullptr;  // stream override for gemm()/launch helpers (nullptr: the lane's main stream)
+  int cur_lane_ = 0;            // lane whose main stream receives the current cell's work
+  bool rec_[64][EV_COUNT] = {};
+  bool fwd_rec_[64] = {};
+  bool bdone_rec_[64][2] = {};
+  bool bfree_rec_[64][2] = {};
 
-  cudaStream_t side() const { return side_ ? side_ : s_; }
-  char* gbuf(int i) const { return ws(i == 0 ? c_->ws.g0 : c_->ws.g1); }
+  int lane_of(int k) const { return c_->ws.nlanes > 1 ? k : 0; }
+  cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
+  cudaStream_t side(int lane) const { return c_->concurrent ? c_->lane_side[lane] : c_->lane_main[lane]; }
+  cudaStream_t st() const { return cur_ ? cur_ : c_->lane_main[cur_lane_]; }
   int cuda_ok(cudaError_t e, const char* what) {
     return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   }
-  // side stream starts after everything issued so far on the main stream
-  int fork() {
-    if (!side_) return GPIPE_OK;
-    TRY(cuda_ok(cudaEventRecord(c_->ev[EV_FORK], s_), "event record"));
-    return cuda_ok(cudaStreamWaitEvent(side_, c_->ev[EV_FORK], 0), "stream wait");
+  // cross-lane handshakes (no-ops when both cells share a lane)
+  int cross_record(int k, cudaEvent_t e, bool& rec) {
+    if (c_->ws.nlanes == 1) return GPIPE_OK;
+    rec = true;
+    return cuda_ok(cudaEventRecord(e, main_s(lane_of(k))), "event record");
   }
-  // mark the side stream's progress so far with event e
-  int mark(int e) {
-    if (!side_) return GPIPE_OK;
-    rec_[e] = true;
-    return cuda_ok(cudaEventRecord(c_->ev[e], side_), "event record");
+  int cross_wait(int k, cudaEvent_t e, bool rec, int from_k) {
+    if (c_->ws.nlanes == 1 || !rec || lane_of(k) == lane_of(from_k)) return GPIPE_OK;
+    return cuda_ok(cudaStreamWaitEvent(main_s(lane_of(k)), e, 0), "stream wait");
   }
-  // main stream waits for the side work marked by e
-  int join(int e) {
-    if (!side_ || !rec_[e]) return GPIPE_OK;
-    return cuda_ok(cudaStreamWaitEvent(s_, c_->ev[e], 0), "stream wait");
+  // a lane's side stream starts after everything issued so far on its main stream
+  int fork(int lane) {
+    if (!c_->concurrent) return GPIPE_OK;
+    TRY(cuda_ok(cudaEventRecord(c_->lane_ev[lane][EV_FORK], main_s(lane)), "event record"));
+    return cuda_ok(cudaStreamWaitEvent(c_->lane_side[lane], c_->lane_ev[lane][EV_FORK], 0), "stream wait");
   }
-  int join_all() {
-    for (int e = EV_GF; e < EV_COUNT; ++e) TRY(join(e));
+  int mark(int lane, int e) {
+    if (!c_->concurrent) return GPIPE_OK;
+    rec_[lane][e] = true;
+    return cuda_ok(cudaEventRecord(c_->lane_ev[lane][e], c_->lane_side[lane]), "event record");
+  }
+  int join(int lane, int e) {
+    if (!c_->concurrent || !rec_[lane][e]) return GPIPE_OK;
+    return cuda_ok(cudaStreamWaitEvent(main_s(lane), c_->lane_ev[lane][e], 0), "stream wait");
+  }
+  int join_all(int lane) {
+    for (int e = EV_GF; e < EV_COUNT; ++e) TRY(join(lane, e));
     return GPIPE_OK;
   }
-  // run a weight-gradient GEMM on the side stream, marking event e afterwards
   template <typename F>
   int on_side(int e, F&& f) {
-    TRY(fork());
-    cur_ = side();
+    const int lane = cur_lane_;
+    TRY(fork(lane));
+    cur_ = side(lane);
     int rc = f();
-    cur_ = s_;
+    cur_ = nullptr;
     if (rc) return rc;
-    return mark(e);
+    return mark(lane, e);
   }
 
   char* ws(size_t off) const { return p_.ws + off; }
@@ -241,14 +320,21 @@ class Executor {
   char* stash(int k, int m) const {
     return ws(c_->ws.stash) + (static_cast<size_t>(k) * c_->M + m) * c_->ws.stash_bytes;
   }
+  char* dx0(int m) const { return ws(c_->ws.dx0) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
+  char* bgrad(int k, int p) const { return ws(c_->ws.bgrad) + (static_cast<size_t>(k) * 2 + p) * c_->ws.stash_bytes; }
+  char* lane_base(int lane) const { return ws(c_->ws.lanes) + static_cast<size_t>(lane) * c_->ws.lane.bytes; }
+  char* lbuf(int lane, int i) const { return lane_base(lane) + (i == 0 ? c_->ws.lane.g0 : c_->ws.lane.g1); }
   const void* cell_input(int k, int m) const {
     if (k == 0 && c_->dm.kind == 0)
       return static_cast<const char*>(p_.batch) + static_cast<size_t>(m) * c_->Tmb() * c_->dm.d * 4;
     return stash(k, m);
   }
   Slot slot(int k, int m, int j) const {
-    size_t idx = c_->no_remat ? static_cast<size_t>(m) * c_->L + c_->bounds[k] + j : static_cast<size_t>(j);
-    char* b = ws(c_->ws.slots) + idx * c_->ws.slot_bytes;
+    char* b;
+    if (c_->no_remat)
+      b = ws(c_->ws.noremat_slots) + (static_cast<size_t>(m) * c_->L + c_->bounds[k] + j) * c_->ws.slot_bytes;
+    else
+      b = lane_base(lane_of(k)) + c_->ws.lane.slots + static_cast<size_t>(j) * c_->ws.slot_bytes;
     const SlotLayout& s = c_->ws.slot;
     Slot r;
     r.u = b + s.u;
@@ -291,19 +377,22 @@ class Executor {
     g.C2 = C2;
     g.aux = aux;
     g.ldaux = ldaux;
-    return launch_gemm(g, cur_);
+    return launch_gemm(g, st());
   }
 
   int cell0_input(int m) {
     if (c_->dm.kind != 1) return GPIPE_OK;  // kind 0 reads the caller's x directly
+    cur_lane_ = lane_of(0);
     return launch_embedding_fwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), wgt(c_->pl.emb),
-                                stash(0, m), s_);
+                                stash(0, m), st());
   }
 
   // Forward of cell k for micro-batch m.  recompute: re-materialisation pass
   // of the backward (the last layer's output projection is skipped since its
-  // result, the cell output, is not needed to differentiate the cell).
+  // result, the cell output, is already stashed and not needed to
+  // differentiate the cell).
   int cell_forward(int k, int m, bool recompute) {
+    cur_lane_ = lane_of(k);
     const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
     for (int j = 0; j < n; ++j) {
       const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
@@ -319,14 +408,15 @@ class Executor {
   int remat_check(int k, int n, bool recompute) {
     const Workspace& w = c_->ws;
     char* saved = ws(w.check) + static_cast<size_t>(k) * c_->max_cell * w.slot_bytes;
+    char* slots = lane_base(lane_of(k)) + w.lane.slots;
     for (int j = 0; j < n; ++j) {
-      char* sl = ws(w.slots) + static_cast<size_t>(j) * w.slot_bytes;
+      char* sl = slots + static_cast<size_t>(j) * w.slot_bytes;
       const size_t bytes = j == n - 1 ? w.slot.compare_bytes_last : w.slot_bytes;
       if (!recompute)
-        TRY(launch_copy(saved + j * w.slot_bytes, sl, bytes, s_));
+        TRY(launch_copy(saved + j * w.slot_bytes, sl, bytes, st()));
       else
         TRY(launch_count_diff(saved + j * w.slot_bytes, sl, bytes,
-                              reinterpret_cast<unsigned long long*>(ws(w.misc) + 8), s_));
+                              reinterpret_cast<unsigned long long*>(ws(w.misc) + 8), st()));
     }
     return GPIPE_OK;
   }
@@ -336,14 +426,14 @@ class Executor {
     const LayerOff& o = c_->pl.layers[l];
     const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = dm.ffn;
     const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
-    TRY(launch_layernorm_fwd(dt, T, d, x, p32(o.ln1_g), p32(o.ln1_b), s.u, s.mean1, s.rstd1, s_));
+    TRY(launch_layernorm_fwd(dt, T, d, x, p32(o.ln1_g), p32(o.ln1_b), s.u, s.mean1, s.rstd1, st()));
     const void* ffn_in = s.u;
     const void* resid2 = x;
     if (dm.kind == 1) {
       TRY(gemm(T, 3 * d, d, s.u, d, true, wgt(o.w_qkv), d, true, EPI_STORE, s.qkv, 3 * d, p32(o.b_qkv)));
-      TRY(launch_attention_fwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, s.lse, s_));
+      TRY(launch_attention_fwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, s.lse, st()));
       TRY(gemm(T, d, d, s.o, d, true, wgt(o.w_o), d, true, EPI_STORE, s.h1, d, p32(o.b_o), x, d));
-      TRY(launch_layernorm_fwd(dt, T, d, s.h1, p32(o.ln2_g), p32(o.ln2_b), s.u2, s.mean2, s.rstd2, s_));
+      TRY(launch_layernorm_fwd(dt, T, d, s.h1, p32(o.ln2_g), p32(o.ln2_b), s.u2, s.mean2, s.rstd2, st()));
       ffn_in = s.u2;
       resid2 = s.h1;
     }
@@ -353,27 +443,30 @@ class Executor {
     return GPIPE_OK;
   }
 
-  // dy: gradient of the layer output; writes the gradient of its input to dx.
-  int layer_backward(int l, const void* x, const Slot& s, const void* dy, void* dx) {
+  // Backward of layer l: dy (the gradient of its output) lives in lane buffer
+  // dy_buf (0/1) or outside the lane (BUF_EXT); writes the gradient of its
+  // input into dx (lane buffer dx_buf, or outside).  Weight gradients run on
+  // the lane's side stream; before the main stream overwrites a buffer that a
+  // side GEMM reads, it joins that GEMM's event.
+  int layer_backward(int l, const void* x, const Slot& s, const void* dy, int dy_buf, void* dx, int dx_buf) {
     const Dims& dm = c_->dm;
     const LayerOff& o = c_->pl.layers[l];
-    const Workspace& w = c_->ws;
+    const LaneLayout& ll = c_->ws.lane;
+    const int lane = cur_lane_;
+    char* lb = lane_base(lane);
     const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = dm.ffn;
     const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
-    float* scratch = reinterpret_cast<float*>(ws(w.scratch));
-    char* gf = ws(w.gf);
-    char* gt = ws(w.gt);
+    float* scratch = reinterpret_cast<float*>(lb + ll.scratch);
+    char* gf = lb + ll.gf;
+    char* gt = lb + ll.gt;
     const void* ffn_in = dm.kind == 1 ? static_cast<const void*>(s.u2) : static_cast<const void*>(s.u);
-    // dy is gradient buffer dyi_, dx the other one.  Weight gradients run on
-    // the side stream; before the main stream overwrites a buffer that a side
-    // GEMM reads, it joins that GEMM's event.
-    const int ev_dy = dyi_ ? EV_DY1 : EV_DY0, ev_dx = dyi_ ? EV_DY0 : EV_DY1;
+    const int ev_dy = dy_buf == 0 ? EV_DY0 : (dy_buf == 1 ? EV_DY1 : EV_DYB);
     // FFN: y = r + W2 GELU(W1 u + b1) + b2
     TRY(on_side(ev_dy, [&] {
       return gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f, nullptr, nullptr, 0, nullptr,
                   nullptr, 0, grad(o.b2));
     }));
-    TRY(join(EV_GF));
+    TRY(join(lane, EV_GF));
     TRY(gemm(T, f, d, dy, d, true, wgt(o.w2), f, false, EPI_GELU_BWD, gf, f, nullptr, nullptr, 0, nullptr, s.z1, f));
     TRY(on_side(EV_GF, [&] {
       return gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d, nullptr, nullptr, 0, nullptr,
@@ -381,69 +474,69 @@ class Executor {
     }));
     TRY(gemm(T, d, f, gf, f, true, wgt(o.w1), d, false, EPI_STORE, gt, d));
     if (dm.kind == 0) {
-      TRY(join(ev_dx));
+      if (dx_buf != BUF_EXT) TRY(join(lane, dx_buf == 0 ? EV_DY0 : EV_DY1));
       return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g),
-                                  grad(o.ln1_b), scratch, s_);
+                                  grad(o.ln1_b), scratch, st());
     }
-    char* gh = ws(w.gh);
-    char* gq = ws(w.gq);
+    char* gh = lb + ll.gh;
+    char* gq = lb + ll.gq;
     // h1 -> LN2: dh1 = LN2'(du2) + dy
-    TRY(join(EV_GH));
+    TRY(join(lane, EV_GH));
     TRY(launch_layernorm_bwd(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g),
-                             grad(o.ln2_b), scratch, s_));
+                             grad(o.ln2_b), scratch, st()));
     // attention output projection
     TRY(on_side(EV_GH, [&] {
       return gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d, nullptr, nullptr, 0, nullptr,
                   nullptr, 0, grad(o.b_o));
     }));
     TRY(gemm(T, d, d, gh, d, true, wgt(o.w_o), d, false, EPI_STORE, gt, d));
-    TRY(join(EV_GQ));
-    TRY(launch_attention_bwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, gt, s.lse, scratch, gq, s_));
+    TRY(join(lane, EV_GQ));
+    TRY(launch_attention_bwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, gt, s.lse, scratch, gq, st()));
     TRY(on_side(EV_GQ, [&] {
       return gemm(3 * d, d, T, gq, 3 * d, false, s.u, d, false, EPI_ACC_F32, grad(o.w_qkv), d, nullptr, nullptr, 0,
                   nullptr, nullptr, 0, grad(o.b_qkv));
     }));
     TRY(gemm(T, d, 3 * d, gq, 3 * d, true, wgt(o.w_qkv), d, false, EPI_STORE, gt, d));
-    TRY(join(ev_dx));
+    if (dx_buf != BUF_EXT) TRY(join(lane, dx_buf == 0 ? EV_DY0 : EV_DY1));
     return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh, dx, grad(o.ln1_g),
-                                grad(o.ln1_b), scratch, s_);
+                                grad(o.ln1_b), scratch, st());
   }
 
   // Loss of micro-batch m from the last cell's output stash[K][m]; with
-  // backward, also writes the gradient of that output into dy.
-  int head(int m, bool backward, char* dy = nullptr) {
+  // backward, also writes the gradient of that output into dy (lane buffer 0).
+  int head(int m, bool backward, char* dy) {
     const Dims& dm = c_->dm;
     const Workspace& w = c_->ws;
+    cur_lane_ = lane_of(c_->K - 1);
     const int T = static_cast<int>(c_->Tmb()), d = dm.d;
     float* loss_rows = reinterpret_cast<float*>(ws(w.loss_rows)) + static_cast<size_t>(m) * T;
     const char* xf = stash(c_->K, m);
     if (dm.kind == 0) {
       const float inv = 1.0f / (static_cast<float>(dm.n) * d);
       const float* t = static_cast<const float*>(p_.targets) + static_cast<size_t>(m) * T * d;
-      float* dyp = backward ? reinterpret_cast<float*>(dy) : reinterpret_cast<float*>(ws(w.g1));
-      return launch_mse(T, d, reinterpret_cast<const float*>(xf), t, inv, loss_rows, dyp, cur_);
+      float* dyp = backward ? reinterpret_cast<float*>(dy) : reinterpret_cast<float*>(lbuf(cur_lane_, 1));
+      return launch_mse(T, d, reinterpret_cast<const float*>(xf), t, inv, loss_rows, dyp, st());
     }
     const float inv = 1.0f / (static_cast<float>(dm.n) * (dm.seq - 1));
     float* logits = reinterpret_cast<float*>(ws(w.logits));
     TRY(launch_layernorm_fwd(DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(w.hf),
-                             reinterpret_cast<float*>(ws(w.meanf)), reinterpret_cast<float*>(ws(w.rstdf)), cur_));
+                             reinterpret_cast<float*>(ws(w.meanf)), reinterpret_cast<float*>(ws(w.rstdf)), st()));
     TRY(gemm(T, dm.vocab, d, ws(w.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
     TRY(launch_cross_entropy(T, dm.vocab, dm.seq, static_cast<const int32_t*>(p_.batch), m * T, inv, logits,
-                             loss_rows, backward ? 1 : 0, cur_));
+                             loss_rows, backward ? 1 : 0, st()));
     if (!backward) return GPIPE_OK;
     // dz (bf16, in place over the logits, leading dimension 2*vocab)
     const int64_t ldz = 2 * static_cast<int64_t>(dm.vocab);
-    char* gt = ws(w.gt);
+    char* gt = lane_base(cur_lane_) + w.lane.gt;
     TRY(gemm(T, d, dm.vocab, logits, ldz, true, wgt(c_->pl.emb), d, false, EPI_STORE, gt, d));
     TRY(on_side(EV_HEAD, [&] {
       return gemm(dm.vocab, d, T, logits, ldz, false, ws(w.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d);
     }));
     return launch_layernorm_bwd(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(w.meanf)),
                                 reinterpret_cast<float*>(ws(w.rstdf)), p32(c_->pl.lnf_g), nullptr, dy,
-                                grad(c_->pl.lnf_g), grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(w.scratch)),
-                                s_);
+                                grad(c_->pl.lnf_g), grad(c_->pl.lnf_b),
+                                reinterpret_cast<float*>(lane_base(cur_lane_) + w.lane.scratch), st());
   }
-  int head_backward(int m, char* dy) { return head(m, true, dy); }
 };
 
 int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
@@ -563,10 +656,10 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StepPtrs ptrs{p32, p16, g32, v32, batch, targets, static_cast<char*>(workspace)};
   if (!c->use_graph) {
-    rc = c->ensure_side();
+    rc = c->ensure_lanes();
     if (rc) return rc;
     const int64_t before = launch_count();
-    Executor ex(c, ptrs, s, c->side());
+    Executor ex(c, ptrs, s);
     rc = ex.run_step();
     if (rc) return c->fail_from_launch(rc);
     c->launches_per_step = launch_count() - before;
@@ -578,16 +671,17 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[2] = c->skip_update;
     key.opts[3] = c->remat_check_m;
     key.opts[4] = c->concurrent;
+    key.opts[5] = c->pipelined;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
         return c->fail(GPIPE_ERR_CUDA, "cannot create the capture stream");
       if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
         return c->fail(GPIPE_ERR_CUDA, "cudaStreamBeginCapture failed");
-      rc = c->ensure_side();
+      rc = c->ensure_lanes();
       if (rc) return rc;
       const int64_t before = launch_count();
-      Executor ex(c, ptrs, c->cap_stream, c->side());
+      Executor ex(c, ptrs, c->cap_stream);
       rc = ex.run_step();
       cudaGraph_t g = nullptr;
       cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &g);
@@ -668,6 +762,7 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
       break;
     case GPIPE_OPT_SKIP_UPDATE: c->skip_update = value != 0; break;
     case GPIPE_OPT_CONCURRENT: c->concurrent = value != 0; break;
+    case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     default: return c->fail(GPIPE_ERR_INVALID_ARG, "unknown option");
   }
   c->drop_graph();
@@ -712,9 +807,16 @@ void gpipe_destroy(gpipe_ctx* c) {
   if (!c) return;
   c->drop_graph();
   if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
-  if (c->side_stream) cudaStreamDestroy(c->side_stream);
-  for (auto& e : c->ev)
-    if (e) cudaEventDestroy(e);
+  for (int i = 0; i < gpipe_ctx::kMaxLanes; ++i) {
+    if (c->lane_main[i]) cudaStreamDestroy(c->lane_main[i]);
+    if (c->lane_side[i]) cudaStreamDestroy(c->lane_side[i]);
+    for (auto& e : c->lane_ev[i])
+      if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : {c->ev_fwd[i], c->ev_bdone[i][0], c->ev_bdone[i][1], c->ev_bfree[i][0], c->ev_bfree[i][1],
+                          c->ev_lane_end[i]})
+      if (e) cudaEventDestroy(e);
+  }
+  if (c->ev_origin) cudaEventDestroy(c->ev_origin);
   delete c;
 }
 

@@ -126,18 +126,13 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
-Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check) {
+Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check,
+                         bool pipelined) {
   Workspace w;
   const size_t es = dm.dtype == 0 ? 4 : 2;
   const size_t T = static_cast<size_t>(dm.n) * (dm.kind == 1 ? dm.seq : 1);
   const size_t Tmb = T / M;
   const size_t d = dm.d, f = dm.ffn, H = dm.kind == 1 ? dm.heads : 0;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    size_t at = off;
-    off += align256(bytes);
-    return at;
-  };
   // slot layout (per layer, per micro-batch of Tmb tokens)
   SlotLayout s{};
   size_t so = 0;
@@ -168,33 +163,52 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.slot = s;
   w.slot_bytes = s.bytes;
 
+  // lane layout
+  LaneLayout ln{};
+  size_t lo = 0;
+  auto ltake = [&](size_t bytes) {
+    size_t at = lo;
+    lo += align256(bytes);
+    return at;
+  };
+  ln.slots = ltake(remat ? static_cast<size_t>(max_cell_layers) * w.slot_bytes : 0);
+  ln.g0 = ltake(Tmb * d * es);
+  ln.g1 = ltake(Tmb * d * es);
+  ln.gt = ltake(Tmb * d * es);
+  ln.gf = ltake(Tmb * f * es);
+  if (dm.kind == 1) {
+    ln.gh = ltake(Tmb * d * es);
+    ln.gq = ltake(Tmb * 3 * d * es);
+  }
+  size_t cols = std::max<size_t>(2 * d, f);
+  if (dm.kind == 1) cols = std::max<size_t>(cols, 3 * d);
+  const size_t parts = (Tmb + 7) / 8;
+  w.scratch_bytes = std::max(parts * cols * 4, Tmb * std::max<size_t>(H, 1) * 4);
+  ln.scratch = ltake(w.scratch_bytes);
+  ln.bytes = lo;
+  w.lane = ln;
+  w.nlanes = pipelined ? K : 1;
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
   w.stash_bytes = Tmb * d * es;
   w.stash = take(static_cast<size_t>(K + 1) * M * w.stash_bytes);
-  w.nslots = remat ? static_cast<size_t>(max_cell_layers) : static_cast<size_t>(L) * M;
-  w.slots = take(w.nslots * w.slot_bytes);
-  size_t head_start = off;
+  w.dx0 = take(dm.kind == 1 ? static_cast<size_t>(M) * w.stash_bytes : 0);
+  w.bgrad = take(static_cast<size_t>(K) * 2 * w.stash_bytes);
+  w.lanes = take(static_cast<size_t>(w.nlanes) * ln.bytes);
+  w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
+  w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
   if (dm.kind == 1) {
     w.hf = take(Tmb * d * es);
     w.meanf = take(Tmb * 4);
     w.rstdf = take(Tmb * 4);
     w.logits = take(Tmb * static_cast<size_t>(dm.vocab) * 4);
   }
-  w.g0 = take(Tmb * d * es);
-  w.g1 = take(Tmb * d * es);
-  w.gt = take(Tmb * d * es);
-  w.gf = take(Tmb * f * es);
-  if (dm.kind == 1) {
-    w.gh = take(Tmb * d * es);
-    w.gq = take(Tmb * 3 * d * es);
-  }
-  const size_t rows_for_scratch = Tmb;
-  size_t cols = std::max<size_t>(2 * d, f);
-  if (dm.kind == 1) cols = std::max<size_t>(cols, 3 * d);
-  const size_t parts = (rows_for_scratch + 7) / 8;
-  w.scratch_bytes = std::max(parts * cols * 4, Tmb * std::max<size_t>(H, 1) * 4);
-  w.scratch = take(w.scratch_bytes);
   w.loss_rows = take(T * 4);
-  const size_t per_token_tail = (off - head_start) / std::max<size_t>(Tmb, 1) + 1;
   w.act_bytes = off;
   w.misc = take(256);
   if (remat && remat_check) {
@@ -202,13 +216,17 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     w.check = take(w.check_bytes);
   }
   w.total = off;
-  // The review's bound O(N + (L/K)(N/M)) with explicit constants: the
-  // boundary stash (K+1 tensors per micro-batch, i.e. proportional to N),
-  // one cell of Lc layers of kept internals for one micro-batch (proportional
-  // to (L/K)(N/M)), and the per-micro-batch head/gradient/scratch term.
-  const size_t a = w.slot_bytes / std::max<size_t>(Tmb, 1) + 1;  // kept bytes per token per layer
-  const size_t cell_layers = remat ? static_cast<size_t>(max_cell_layers) : static_cast<size_t>(L) * M;
-  w.bound_bytes = static_cast<size_t>(K + 1) * T * d * es + cell_layers * Tmb * a + Tmb * per_token_tail;
+  // The review's bound O(N + (L/K)(N/M)) per accelerator, with explicit
+  // constants, summed over the lanes: the boundary tensors (stash, the
+  // embedding's input gradient and the gradient ring; proportional to N), and
+  // per lane one cell of Lc layers of kept internals for one micro-batch plus
+  // that lane's gradient buffers (proportional to (L/K)(N/M)); the head's
+  // logits and the per-row losses.
+  const size_t boundary = static_cast<size_t>(K + 2) * T * d * es + static_cast<size_t>(K) * 2 * Tmb * d * es;
+  const size_t per_lane = ln.bytes + 4096;
+  const size_t head = dm.kind == 1 ? Tmb * (d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + 4096 : 0;
+  const size_t cell_all = remat ? 0 : static_cast<size_t>(L) * M * w.slot_bytes;
+  w.bound_bytes = boundary + static_cast<size_t>(w.nlanes) * per_lane + cell_all + head + T * 4 + 8192;
   return w;
 }
 

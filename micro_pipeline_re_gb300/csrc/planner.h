@@ -44,21 +44,36 @@ struct SlotLayout {
   size_t bytes;
 };
 
+// Per-lane region (one lane per cell when the cells run as a pipeline of
+// concurrent lanes; a single lane shared by all cells otherwise).
+struct LaneLayout {
+  size_t slots = 0;                             // re-materialised internals of one cell (Lc slots)
+  size_t g0 = 0, g1 = 0, gt = 0, gf = 0, gh = 0, gq = 0;  // gradients in flight
+  size_t scratch = 0;                           // reduction partials / attention row sums
+  size_t bytes = 0;
+};
+
 struct Workspace {
   size_t stash = 0, stash_bytes = 0;        // (K+1) x M boundary tensors [Tmb, d]
-  size_t slots = 0, slot_bytes = 0, nslots = 0;
+  size_t dx0 = 0;                           // M x [Tmb, d]: gradient w.r.t. the embedding output (kind 1)
+  size_t bgrad = 0;                         // K x 2 x [Tmb, d]: gradient w.r.t. cell k's input, 2-deep ring
+  size_t lanes = 0;                         // nlanes x lane
+  int nlanes = 1;
+  LaneLayout lane{};
+  size_t slot_bytes = 0;
   SlotLayout slot{};
+  size_t noremat_slots = 0, nslots_noremat = 0;  // L x M slots when re-materialisation is off
   size_t hf = 0, meanf = 0, rstdf = 0, logits = 0;  // head (kind 1)
-  size_t g0 = 0, g1 = 0, gh = 0, gt = 0, gf = 0, gq = 0;  // gradients in flight
-  size_t scratch = 0, scratch_bytes = 0;
+  size_t scratch_bytes = 0;
   size_t loss_rows = 0, misc = 0;            // misc: loss (float) at +0, remat counter (u64) at +8
   size_t check = 0, check_bytes = 0;         // re-materialisation check copies (debug)
   size_t act_bytes = 0;                      // activation bytes (everything but misc/check)
   size_t total = 0;
-  // bound of the review's form with explicit constants
+  // the review's bound O(N + (L/K)(N/M)) per lane, with explicit constants
   size_t bound_bytes = 0;
 };
 
-Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check);
+Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check,
+                         bool pipelined);
 
 }  // namespace gp

@@ -155,18 +155,22 @@ def test_steps_are_bit_reproducible_and_graph_equals_direct(b):
         assert np.array_equal(o[2], outs[0][2])
 
 
-def test_concurrent_schedule_is_bit_identical_to_serial(b):
-    """Weight gradients on a side stream (events order every shared buffer)
-    give exactly the single-stream result, with and without the CUDA graph."""
-    for w in (SMALL_LM, WORKLOADS["tiny_ffn"]):
-        inp = make_inputs(w)
-        outs = []
-        for conc, graph in ((0, 1), (1, 1), (1, 0)):
-            _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_CONCURRENT, conc), (b.OPT_GRAPH, graph)])
-            outs.append((loss, st.g32.cpu().numpy().copy()))
-        for o in outs[1:]:
-            assert o[0] == outs[0][0]
-            assert np.array_equal(o[1], outs[0][1])
+@pytest.mark.parametrize("wname", ["small_lm", "tiny_ffn", "lm_small"])
+def test_schedules_are_bit_identical(b, wname):
+    """Cells as concurrent lanes (the review's pipeline on one GPU) and weight
+    gradients on side streams give exactly the one-stream, cells-in-turn
+    result, with and without the CUDA graph."""
+    w = SMALL_LM if wname == "small_lm" else WORKLOADS[wname]
+    inp = make_inputs(w)
+    outs = []
+    for pipe, conc, graph in ((0, 0, 1), (1, 1, 1), (1, 0, 1), (0, 1, 1), (1, 1, 0)):
+        _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_PIPELINE, pipe), (b.OPT_CONCURRENT, conc),
+                                                     (b.OPT_GRAPH, graph)])
+        outs.append((loss, st.g32.cpu().numpy().copy(), st.p32.cpu().numpy().copy()))
+    for o in outs[1:]:
+        assert o[0] == outs[0][0]
+        assert np.array_equal(o[1], outs[0][1])
+        assert np.array_equal(o[2], outs[0][2])
 
 
 def test_no_rematerialisation_mode_is_identical(b):

@@ -122,10 +122,12 @@ def test_clock_model_unequal_cells(binding):
         assert bub == pytest.approx(float(sim["bubble"]), abs=1e-12)
 
 
-def _report(binding, w, K, M, no_remat=False):
+def _report(binding, w, K, M, no_remat=False, pipelined=True):
     g = binding.GPipe.from_workload(w, K=K, M=M)
     if no_remat:
         g.set_option(binding.OPT_NO_REMAT, 1)
+    if not pipelined:
+        g.set_option(binding.OPT_PIPELINE, 0)
     peak, bound = g.memory_report()
     P, ws = g.sizes()
     return peak, bound, ws
@@ -133,27 +135,43 @@ def _report(binding, w, K, M, no_remat=False):
 
 def test_memory_within_bound_and_workspace(binding):
     for name, w in WORKLOADS.items():
-        peak, bound, ws = _report(binding, w, w.K, w.M)
-        assert peak <= bound, name
-        assert ws >= peak
+        for pipelined in (True, False):
+            peak, bound, ws = _report(binding, w, w.K, w.M, pipelined=pipelined)
+            assert peak <= bound, name
+            assert ws >= peak
 
 
-def test_memory_scales_as_review_bound_over_sweep_grid(binding):
-    """Peak activation bytes over the micro-batch sweep grid follow
-    a (K+1) N + b (L/K)(N/M) + c (N/M) (the review's O(N + (L/K)(N/M)))."""
+@pytest.mark.parametrize("pipelined", [False, True])
+def test_memory_scales_as_review_bound_over_sweep_grid(binding, pipelined):
+    """Peak activation bytes over the micro-batch sweep grid follow the
+    review's O(N + (L/K)(N/M)) per accelerator: boundary tensors a (K+2) N,
+    plus per lane (L/K)(N/M) kept internals and (N/M) gradient buffers.  One
+    lane (cells in turn): a (K+2)N + b (L/K)(N/M) + c (N/M); K concurrent
+    lanes: a (K+2)N + b L (N/M) + c K (N/M)."""
     w = WORKLOADS["lm_sweep"]
     rows, ys = [], []
     for K, M in SWEEP_GRID:
-        peak, bound, _ = _report(binding, w, K, M)
+        peak, bound, _ = _report(binding, w, K, M, pipelined=pipelined)
         assert peak <= bound
         T = w.tokens
-        rows.append([(K + 1) * T, (w.L / K) * T / M, T / M])
+        lanes = K if pipelined else 1
+        rows.append([(K + 2) * T, lanes * (w.L / K) * T / M, lanes * T / M])
         ys.append(peak)
     A, y = np.array(rows, dtype=float), np.array(ys, dtype=float)
     coef, *_ = np.linalg.lstsq(A, y, rcond=None)
     resid = np.abs(A @ coef - y) / y
     assert resid.max() <= 0.10, resid
     assert np.all(coef > 0)
+
+
+def test_pipelined_lanes_cost_memory_only_per_cell(binding):
+    """K lanes hold K cells' internals at once (one per lane), so the extra
+    memory over the one-lane schedule is (K-1) lanes' worth, not L layers x M."""
+    w = WORKLOADS["lm_wide"]
+    serial, _, _ = _report(binding, w, w.K, w.M, pipelined=False)
+    piped, _, _ = _report(binding, w, w.K, w.M, pipelined=True)
+    noremat, _, _ = _report(binding, w, w.K, w.M, no_remat=True, pipelined=False)
+    assert serial < piped < noremat / 4
 
 
 def test_rematerialisation_saves_memory(binding):
