@@ -47,7 +47,7 @@ constexpr int BOX = 16384;  // one epilogue box: 128 rows x 128 B
 
 template <int BN, int EPI>
 struct TcCfg {
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = BN == 64 ? 3 : 4;  // BN=64: two CTAs fit on one SM
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
@@ -73,8 +73,10 @@ __device__ __forceinline__ uint32_t swz(int r, int unit) {
   return static_cast<uint32_t>(r * 128 + ((unit ^ (r & 7)) << 4));
 }
 
+constexpr int THREADS = 256;  // 8 warps: producer (w0), MMA issuer (w1), all 8 share the epilogue
+
 template <bool A_K, bool B_K, int BN, int EPI>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                    const __grid_constant__ CUtensorMap tmX, TcArgs args, int* err) {
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(128, 1)
   const int n0 = blockIdx.x * BN;
   const int nk = (args.K + BK - 1) / BK;
   const bool do_db = (EPI == EPI_ACC_F32) && args.dbias != nullptr && blockIdx.x == 0;
-  const uint32_t tcols = do_db ? 256u : static_cast<uint32_t>(BN);
+  const uint32_t tcols = do_db ? static_cast<uint32_t>(BN == 64 ? 128 : 256) : static_cast<uint32_t>(BN);
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(128, 1)
       sBias[threadIdx.x] = (args.bias != nullptr && n < args.N) ? args.bias[n] : 0.f;
     }
   }
-  if (do_db) {  // 16 rows x 64 bf16 of 1.0
+  if (do_db && threadIdx.x < 128) {  // 16 rows x 64 bf16 of 1.0
     reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_proxy_async_smem();
   }
@@ -189,16 +191,17 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncwarp();
 
-  // ---- epilogue: warp w owns TMEM lanes 32w..32w+31 = tile rows 32w + lane ----
-  const int r = warp * 32 + lane;
+  // ---- epilogue: warp w reads TMEM lanes 32(w%4).. (tile rows 32(w%4) + lane);
+  //      warps w and w+4 split the tile's 32-column chunks ----
+  const int r = (warp & 3) * 32 + lane;
   const bool ok = mbar_wait_bounded(accb, 0, err, DERR_ACC_WAIT);
   tc_fence_after();
   bool ok_x = true;
   if (args.has_x) ok_x = mbar_wait_bounded(epib, 0, err, DERR_ACC_WAIT);
-  const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t tbase = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   if (ok && ok_x) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = warp >> 2; c < BN / 32; c += 2) {
       uint32_t rr[32];
       tmem_ld32(tbase + c * 32, rr);
       tmem_ld_wait();
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
-    if (do_db) {
+    if (do_db && warp < 4) {
       uint32_t rr[32];
       tmem_ld32(tbase + BN, rr);
       tmem_ld_wait();
@@ -347,7 +350,8 @@ int run(const GemmDesc& g, cudaStream_t stream) {
   if (rc) return rc;
   TcArgs args{g.bias, g.dbias, g.M, g.N, g.K, has_x};
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
-  tc_gemm_kernel<A_K, B_K, BN, EPI><<<grid, 128, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, tx, args, device_error_ptr());
+  tc_gemm_kernel<A_K, B_K, BN, EPI><<<grid, THREADS, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, tx, args,
+                                                                           device_error_ptr());
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
@@ -358,24 +362,25 @@ int run(const GemmDesc& g, cudaStream_t stream) {
 // and B), input gradients (K-major A, MN-major B) and weight gradients
 // (MN-major A and B); a plain store / fp32 accumulate for each, so every
 // operand layout can be checked with the simplest epilogue.
-int run_epi(const GemmDesc& g, cudaStream_t s) {
+template <int BN>
+int run_epi_bn(const GemmDesc& g, cudaStream_t s) {
   if (g.a_kmajor && g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return run<true, true, 128, EPI_STORE>(g, s);
-      case EPI_BIAS_GELU: return run<true, true, 128, EPI_BIAS_GELU>(g, s);
-      case EPI_STORE_F32: return run<true, true, 128, EPI_STORE_F32>(g, s);
-      case EPI_ACC_F32: return run<true, true, 128, EPI_ACC_F32>(g, s);
+      case EPI_STORE: return run<true, true, BN, EPI_STORE>(g, s);
+      case EPI_BIAS_GELU: return run<true, true, BN, EPI_BIAS_GELU>(g, s);
+      case EPI_STORE_F32: return run<true, true, BN, EPI_STORE_F32>(g, s);
+      case EPI_ACC_F32: return run<true, true, BN, EPI_ACC_F32>(g, s);
     }
   } else if (g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return run<true, false, 128, EPI_STORE>(g, s);
-      case EPI_GELU_BWD: return run<true, false, 128, EPI_GELU_BWD>(g, s);
-      case EPI_ACC_F32: return run<true, false, 128, EPI_ACC_F32>(g, s);
+      case EPI_STORE: return run<true, false, BN, EPI_STORE>(g, s);
+      case EPI_GELU_BWD: return run<true, false, BN, EPI_GELU_BWD>(g, s);
+      case EPI_ACC_F32: return run<true, false, BN, EPI_ACC_F32>(g, s);
     }
   } else if (!g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return run<false, false, 128, EPI_STORE>(g, s);
-      case EPI_ACC_F32: return run<false, false, 128, EPI_ACC_F32>(g, s);
+      case EPI_STORE: return run<false, false, BN, EPI_STORE>(g, s);
+      case EPI_ACC_F32: return run<false, false, BN, EPI_ACC_F32>(g, s);
     }
   }
   return set_error(GPIPE_ERR_UNSUPPORTED,
@@ -383,23 +388,41 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
                    (int)g.a_kmajor, (int)g.b_kmajor, g.epi);
 }
 
+// Instantiated combinations: the forward projections and logits (K-major A
+// and B), input gradients (K-major A, MN-major B) and weight gradients
+// (MN-major A and B); a plain store / fp32 accumulate for each, so every
+// operand layout can be checked with the simplest epilogue.  Tile width:
+// 128 columns when that already gives at least one CTA per SM, else 64
+// (twice the CTAs, each with half the operand traffic and epilogue work).
+int run_epi(const GemmDesc& g, cudaStream_t s) {
+  const int64_t tiles128 = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 127) / 128);
+  if (tiles128 >= num_sms()) return run_epi_bn<128>(g, s);
+  return run_epi_bn<64>(g, s);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
+template <int BN>
+int prepare_bn() {
+  int rc = GPIPE_OK;
+  rc = rc ? rc : set_attr<true, true, BN, EPI_STORE>();
+  rc = rc ? rc : set_attr<true, true, BN, EPI_BIAS_GELU>();
+  rc = rc ? rc : set_attr<true, true, BN, EPI_STORE_F32>();
+  rc = rc ? rc : set_attr<true, true, BN, EPI_ACC_F32>();
+  rc = rc ? rc : set_attr<true, false, BN, EPI_STORE>();
+  rc = rc ? rc : set_attr<true, false, BN, EPI_GELU_BWD>();
+  rc = rc ? rc : set_attr<true, false, BN, EPI_ACC_F32>();
+  rc = rc ? rc : set_attr<false, false, BN, EPI_STORE>();
+  rc = rc ? rc : set_attr<false, false, BN, EPI_ACC_F32>();
+  return rc;
+}
+
 int prepare_gemm_tc() {
   if (!encode_fn()) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled entry point not found");
-  int rc = GPIPE_OK;
-  rc = rc ? rc : set_attr<true, true, 128, EPI_STORE>();
-  rc = rc ? rc : set_attr<true, true, 128, EPI_BIAS_GELU>();
-  rc = rc ? rc : set_attr<true, true, 128, EPI_STORE_F32>();
-  rc = rc ? rc : set_attr<true, true, 128, EPI_ACC_F32>();
-  rc = rc ? rc : set_attr<true, false, 128, EPI_STORE>();
-  rc = rc ? rc : set_attr<true, false, 128, EPI_GELU_BWD>();
-  rc = rc ? rc : set_attr<true, false, 128, EPI_ACC_F32>();
-  rc = rc ? rc : set_attr<false, false, 128, EPI_STORE>();
-  rc = rc ? rc : set_attr<false, false, 128, EPI_ACC_F32>();
-  return rc;
+  int rc = prepare_bn<128>();
+  return rc ? rc : prepare_bn<64>();
 }
 
 int launch_gemm_tc(const GemmDesc& g, cudaStream_t stream) {

@@ -29,7 +29,9 @@ def _gemm_ref(A, B, ak, bk):
 
 
 # (M, N, K): several tiles with ragged tails in every dimension
-SHAPES = [(384, 640, 512), (200, 136, 200), (128, 128, 64), (1000, 96, 72)]
+# (the last one has enough 128-wide tiles to take the 128-column variant;
+# the others take the 64-column one)
+SHAPES = [(384, 640, 512), (200, 136, 200), (128, 128, 64), (1000, 96, 72), (1700, 1700, 200)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
