@@ -67,6 +67,12 @@ struct TcArgs {
   float* dbias;       // EPI_ACC_F32: fp32 [M] accumulator of sum_k A(m,k), or NULL
   int M, N, K;
   int has_x;          // the epilogue input tile (residual / GELU pre-activation) is used
+  // split-K epilogue (plain global accesses): output, its leading dimension,
+  // and the residual / GELU pre-activation matrix (or NULL) with its own
+  void* C;
+  int64_t ldc;
+  const void* xsrc;
+  int64_t ldx;
 };
 
 __device__ __forceinline__ uint32_t swz(int r, int unit) {
@@ -75,7 +81,12 @@ __device__ __forceinline__ uint32_t swz(int r, int unit) {
 
 constexpr int THREADS = 256;  // 8 warps: producer (w0), MMA issuer (w1), all 8 share the epilogue
 
-template <bool A_K, bool B_K, int BN, int EPI>
+// SPLIT: the S = gridDim.z CTAs of a (1,1,S) cluster split K; each keeps its
+// fp32 partial tile in shared memory, and after a cluster barrier CTA rank q
+// sums rows [q*128/S, (q+1)*128/S) of all S partials in rank order (through
+// distributed shared memory), applies the epilogue and stores.  Deterministic,
+// no workspace, one launch.
+template <bool A_K, bool B_K, int BN, int EPI, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
@@ -99,7 +110,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * BM;
   const int n0 = blockIdx.x * BN;
-  const int nk = (args.K + BK - 1) / BK;
+  const int nk_all = (args.K + BK - 1) / BK;
+  const int S = SPLIT ? static_cast<int>(gridDim.z) : 1;
+  const int kb_begin = SPLIT ? static_cast<int>(blockIdx.z) * nk_all / S : 0;
+  const int nk = (SPLIT ? (static_cast<int>(blockIdx.z) + 1) * nk_all / S : nk_all) - kb_begin;
   const bool do_db = (EPI == EPI_ACC_F32) && args.dbias != nullptr && blockIdx.x == 0;
   const uint32_t tcols = do_db ? static_cast<uint32_t>(BN == 64 ? 128 : 256) : static_cast<uint32_t>(BN);
 
@@ -145,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t ph = (kb / STAGES) & 1;
       if (!mbar_wait_bounded(&empty[s], ph ^ 1, err, DERR_TMA_WAIT)) break;
       mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES + Cfg::B_BYTES);
-      const int k0 = kb * BK;
+      const int k0 = (kb_begin + kb) * BK;
       uint8_t* a = sA + s * Cfg::A_BYTES;
       uint8_t* b = sB + s * Cfg::B_BYTES;
       if (A_K) {
@@ -194,6 +208,70 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- epilogue: warp w reads TMEM lanes 32(w%4).. (tile rows 32(w%4) + lane);
   //      warps w and w+4 split the tile's 32-column chunks ----
   const int r = (warp & 3) * 32 + lane;
+  if (SPLIT) {
+    constexpr int PLD = BN + 4;  // padded fp32 row of the partial tile (in the now idle stage buffers)
+    float* P = reinterpret_cast<float*>(sA);
+    const bool okp = mbar_wait_bounded(accb, 0, err, DERR_ACC_WAIT);
+    tc_fence_after();
+    if (okp) {
+      const uint32_t tb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+#pragma unroll 1
+      for (int c = warp >> 2; c < BN / 32; c += 2) {
+        uint32_t rr[32];
+        tmem_ld32(tb + c * 32, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4*>(P + r * PLD + c * 32 + 4 * u) =
+              make_float4(__uint_as_float(rr[4 * u]), __uint_as_float(rr[4 * u + 1]), __uint_as_float(rr[4 * u + 2]),
+                          __uint_as_float(rr[4 * u + 3]));
+      }
+    }
+    tc_fence_before();
+    cluster_sync();  // every partial of the cluster is in place
+    const int R = BM / S;
+    const int rank = static_cast<int>(cluster_ctarank());
+    uint32_t peer[8];
+    for (int q = 0; q < S; ++q) peer[q] = map_peer(smem_u32(P), static_cast<uint32_t>(q));
+    const int groups = R * (BN / 8);
+    for (int gi = threadIdx.x; gi < groups; gi += THREADS) {
+      const int rr = rank * R + gi / (BN / 8);
+      const int cc = (gi % (BN / 8)) * 8;
+      const int m = m0 + rr, n = n0 + cc;
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const uint32_t off = static_cast<uint32_t>((rr * PLD + cc) * 4);
+      for (int q = 0; q < S; ++q) {
+        const float4 a = ld_peer_f4(peer[q] + off), b = ld_peer_f4(peer[q] + off + 16);
+        v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+        v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+      }
+      if (m < args.M && n < args.N) {
+        if (EPI == EPI_STORE && args.bias) {
+          float bb[8];
+          load8(args.bias + n, bb);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] += bb[j];
+        }
+        if (args.xsrc) {  // residual (store) or GELU pre-activation (GELU backward)
+          float t[8];
+          load8(static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx + n, t);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (EPI == EPI_GELU_BWD) v[j] *= gelu_grad_f(t[j]);
+            else v[j] += t[j];
+          }
+        }
+        store8(static_cast<__nv_bfloat16*>(args.C) + static_cast<int64_t>(m) * args.ldc + n, v);
+      }
+    }
+    cluster_sync();  // peers have finished reading this CTA's partial
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, tcols);
+    }
+    return;
+  }
   const bool ok = mbar_wait_bounded(accb, 0, err, DERR_ACC_WAIT);
   tc_fence_after();
   bool ok_x = true;
@@ -313,11 +391,11 @@ bool make_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64_
   return r == CUDA_SUCCESS;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
+template <bool A_K, bool B_K, int BN, int EPI, bool SPLIT = false>
 int set_attr() {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_K, B_K, BN, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN, EPI>::SMEM);
     if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
     attr_set = true;
@@ -325,8 +403,8 @@ int set_attr() {
   return GPIPE_OK;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
-int run(const GemmDesc& g, cudaStream_t stream) {
+template <bool A_K, bool B_K, int BN, int EPI, bool SPLIT = false>
+int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
   using Cfg = TcCfg<BN, EPI>;
   CUtensorMap ta, tb, tc, tc2, tx;
   bool ok = A_K ? make_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, BM) : make_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
@@ -337,44 +415,85 @@ int run(const GemmDesc& g, cudaStream_t stream) {
   tx = tc;
   if (EPI == EPI_BIAS_GELU) ok = ok && make_tmap(&tc2, g.C2, false, g.N, g.M, g.ldc, 64, BM);
   int has_x = 0;
+  const void* xsrc = nullptr;
+  int64_t ldx = 0;
   if (EPI == EPI_STORE && g.resid) {
-    ok = ok && make_tmap(&tx, g.resid, false, g.N, g.M, g.ldr, 64, BM);
-    has_x = 1;
+    xsrc = g.resid;
+    ldx = g.ldr;
   }
   if (EPI == EPI_GELU_BWD) {
-    ok = ok && make_tmap(&tx, g.aux, false, g.N, g.M, g.ldaux, 64, BM);
+    xsrc = g.aux;
+    ldx = g.ldaux;
+  }
+  if (xsrc && !SPLIT) {
+    ok = ok && make_tmap(&tx, xsrc, false, g.N, g.M, ldx, 64, BM);
     has_x = 1;
   }
   if (!ok) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed");
-  int rc = set_attr<A_K, B_K, BN, EPI>();
+  int rc = set_attr<A_K, B_K, BN, EPI, SPLIT>();
   if (rc) return rc;
-  TcArgs args{g.bias, g.dbias, g.M, g.N, g.K, has_x};
-  dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
-  tc_gemm_kernel<A_K, B_K, BN, EPI><<<grid, THREADS, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, tx, args,
-                                                                           device_error_ptr());
+  TcArgs args{g.bias, g.dbias, g.M, g.N, g.K, has_x, g.C, g.ldc, xsrc, ldx};
+  dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, SPLIT ? S : 1);
+  cudaError_t e;
+  if (SPLIT) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = S;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>, ta, tb, tc, tc2, tx, args,
+                           device_error_ptr());
+  } else {
+    tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT><<<grid, THREADS, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, tx, args,
+                                                                                  device_error_ptr());
+    e = cudaGetLastError();
+  }
   count_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "gemm launch: %s", cudaGetErrorString(e));
   return GPIPE_OK;
 }
 
-// Instantiated combinations: the forward projections and logits (K-major A
-// and B), input gradients (K-major A, MN-major B) and weight gradients
-// (MN-major A and B); a plain store / fp32 accumulate for each, so every
-// operand layout can be checked with the simplest epilogue.
+// Split-K factor for a bf16-output GEMM: while the tiles (with their K
+// split S ways) still fit the machine at two CTAs per SM and every CTA keeps
+// at least 4 k-blocks, double S (at most 8, a portable cluster).
+int split_factor(const GemmDesc& g, int BN) {
+  const int64_t tiles = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int nk = (g.K + BK - 1) / BK;
+  int S = 1;
+  while (S < 8 && tiles * S * 2 <= 2 * static_cast<int64_t>(num_sms()) && nk / (S * 2) >= 4) S *= 2;
+  return S;
+}
+
 template <int BN>
 int run_epi_bn(const GemmDesc& g, cudaStream_t s) {
   if (g.a_kmajor && g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return run<true, true, BN, EPI_STORE>(g, s);
+      case EPI_STORE: {
+        const int S = split_factor(g, BN);
+        return S > 1 ? run<true, true, BN, EPI_STORE, true>(g, s, S) : run<true, true, BN, EPI_STORE>(g, s);
+      }
       case EPI_BIAS_GELU: return run<true, true, BN, EPI_BIAS_GELU>(g, s);
       case EPI_STORE_F32: return run<true, true, BN, EPI_STORE_F32>(g, s);
       case EPI_ACC_F32: return run<true, true, BN, EPI_ACC_F32>(g, s);
     }
   } else if (g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return run<true, false, BN, EPI_STORE>(g, s);
-      case EPI_GELU_BWD: return run<true, false, BN, EPI_GELU_BWD>(g, s);
+      case EPI_STORE: {
+        const int S = split_factor(g, BN);
+        return S > 1 ? run<true, false, BN, EPI_STORE, true>(g, s, S) : run<true, false, BN, EPI_STORE>(g, s);
+      }
+      case EPI_GELU_BWD: {
+        const int S = split_factor(g, BN);
+        return S > 1 ? run<true, false, BN, EPI_GELU_BWD, true>(g, s, S) : run<true, false, BN, EPI_GELU_BWD>(g, s);
+      }
       case EPI_ACC_F32: return run<true, false, BN, EPI_ACC_F32>(g, s);
     }
   } else if (!g.a_kmajor && !g.b_kmajor) {
@@ -416,6 +535,9 @@ int prepare_bn() {
   rc = rc ? rc : set_attr<true, false, BN, EPI_ACC_F32>();
   rc = rc ? rc : set_attr<false, false, BN, EPI_STORE>();
   rc = rc ? rc : set_attr<false, false, BN, EPI_ACC_F32>();
+  rc = rc ? rc : set_attr<true, true, BN, EPI_STORE, true>();
+  rc = rc ? rc : set_attr<true, false, BN, EPI_STORE, true>();
+  rc = rc ? rc : set_attr<true, false, BN, EPI_GELU_BWD, true>();
   return rc;
 }
 
