@@ -461,14 +461,14 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
   return GPIPE_OK;
 }
 
-// Split-K factor for a bf16-output GEMM: while the tiles (with their K
-// split S ways) still fit the machine at two CTAs per SM and every CTA keeps
-// at least 4 k-blocks, double S (at most 8, a portable cluster).
+// Split-K factor for a bf16-output GEMM: only K long enough that every split
+// keeps at least 32 k-blocks (so the per-CTA set-up stays small against its
+// work), up to 8 (a portable cluster) and never more CTAs than two per SM.
 int split_factor(const GemmDesc& g, int BN) {
   const int64_t tiles = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int nk = (g.K + BK - 1) / BK;
   int S = 1;
-  while (S < 8 && tiles * S * 2 <= 2 * static_cast<int64_t>(num_sms()) && nk / (S * 2) >= 4) S *= 2;
+  while (S < 8 && nk / (S * 2) >= 32 && tiles * S * 2 <= 2 * static_cast<int64_t>(num_sms())) S *= 2;
   return S;
 }
 
@@ -514,8 +514,12 @@ int run_epi_bn(const GemmDesc& g, cudaStream_t s) {
 // 128 columns when that already gives at least one CTA per SM, else 64
 // (twice the CTAs, each with half the operand traffic and epilogue work).
 int run_epi(const GemmDesc& g, cudaStream_t s) {
+  // Tile width: 128 columns when that gives at least one CTA per SM of this
+  // GEMM's share of the machine, else 64 (twice the CTAs, each with half the
+  // operand traffic and epilogue work).
+  const int budget = g.sm_budget > 0 ? g.sm_budget : num_sms();
   const int64_t tiles128 = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 127) / 128);
-  if (tiles128 >= num_sms()) return run_epi_bn<128>(g, s);
+  if (tiles128 >= budget) return run_epi_bn<128>(g, s);
   return run_epi_bn<64>(g, s);
 }
 

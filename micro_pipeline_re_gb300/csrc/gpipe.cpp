@@ -377,6 +377,7 @@ class Executor {
     g.C2 = C2;
     g.aux = aux;
     g.ldaux = ldaux;
+    g.sm_budget = num_sms() / c_->ws.nlanes;  // lanes share the machine
     return launch_gemm(g, st());
   }
 

@@ -43,6 +43,7 @@ struct GemmDesc {
   void* C2 = nullptr;
   const void* aux = nullptr;
   int64_t ldaux = 0;
+  int sm_budget = 0;  // SMs this GEMM may expect to itself (0: all); picks tile width and split-K
 };
 
 int launch_gemm(const GemmDesc& g, cudaStream_t stream);       // dispatch by dtype

@@ -34,7 +34,7 @@ def _gemm_ref(A, B, ak, bk):
 # (1704^2 has enough 128-wide tiles for the 128-column variant; the others
 # take the 64-column one; the two long-K shapes split K across a cluster)
 SHAPES = [(384, 640, 512), (200, 136, 200), (128, 128, 64), (1000, 96, 72), (1704, 1704, 200),
-          (200, 256, 2048), (256, 136, 4096)]
+          (200, 256, 16384), (256, 136, 4096)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
