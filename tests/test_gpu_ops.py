@@ -65,9 +65,11 @@ def test_gemm_tensor_core(b, shape, ak, bk, epi):
         assert rc == 0, b.lib().gpipe_last_error(None)
         sync()
         want = acc + (C0 if epi == 3 else 0)
-        assert rel(host(dC), want) <= 1e-5
+        # fp32 accumulation over K terms: relative error grows like sqrt(K) 2^-24
+        tol = 1e-5 * max(1.0, (K / 1024) ** 0.5)
+        assert rel(host(dC), want) <= tol
         if epi == 3:
-            assert rel(host(ddb), db0 + (A if ak else A.T).sum(axis=1)) <= 1e-5
+            assert rel(host(ddb), db0 + (A if ak else A.T).sum(axis=1)) <= tol
         return
     dC = t.empty((M, N), dtype=t.bfloat16, device="cuda")
     dC2 = t.empty((M, N), dtype=t.bfloat16, device="cuda")
