@@ -167,13 +167,15 @@ def cfg(w, args):
             "l2": "working set larger than L2 (parameters, gradients and RMSProp state alone exceed 129 MB)"}
 
 
-def gemm_roofline(b, w, peaks, eager_launches=5, reps=100):
+def gemm_roofline(b, w, peaks, eager_launches=5, reps=100, shape=None):
     """Time the dominant kernel class (tcgen05 GEMM, FFN first projection with
     bias+GELU at the step's micro-batch shape) with CUDA events around a CUDA
     graph of `reps` launches on the launching stream (host launch cost is not
     in the number)."""
     import torch
     T, d, f = w.tokens // w.M, w.d, w.ffn
+    if shape is not None:
+        T, f, d = shape  # M, N, K
     A = torch.randn(T, d, device="cuda").to(torch.bfloat16)
     Bw = torch.randn(f, d, device="cuda").to(torch.bfloat16)
     bias = torch.zeros(f, device="cuda")
@@ -317,6 +319,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--probe-gemm", action="store_true",
                     help="only run the roofline GEMM (5 eager launches, then a timed graph); for profilers")
+    ap.add_argument("--shape", default=None, help="M,N,K for --probe-gemm (default: the workload's FFN1)")
+    ap.add_argument("--reps", type=int, default=100)
     args = ap.parse_args()
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
@@ -325,7 +329,8 @@ def main():
         import __graft_entry__ as ge
         ge.build()
         from micro_pipeline_re_gb300 import binding as b
-        print(json.dumps(gemm_roofline(b, w, load_peaks())), flush=True)
+        shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
+        print(json.dumps(gemm_roofline(b, w, load_peaks(), reps=args.reps, shape=shape)), flush=True)
         return
     if args.impl == "reference":
         run_reference(args, w)
