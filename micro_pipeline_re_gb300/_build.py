@@ -12,7 +12,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgpipe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CUDA_SOURCES = ["gemm_tc.cu", "gemm_simt.cu", "attention.cu", "elementwise.cu", "launch.cu"]
+CUDA_SOURCES = ["gemm_tc.cu", "gemm_persistent.cu", "gemm_simt.cu", "attention.cu", "elementwise.cu", "launch.cu"]
 CXX_SOURCES = ["planner.cpp", "gpipe.cpp"]
 
 

@@ -1,0 +1,433 @@
+// Persistent bf16 GEMM on tcgen05 for GEMMs with more output tiles than SMs.
+//
+// One CTA per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... (m
+// fastest, so CTAs working at the same time share the B tile and the small A
+// stays in L2).  Each tile is computed by exactly one CTA: deterministic.
+//   warp 0 / lane 0   TMA producer over all (tile, k-block) pairs, through a
+//                     ring of STAGES operand stages
+//   warp 1            allocates TMEM; lane 0 issues tcgen05.mma into one of two
+//                     accumulators (2 x BN columns), so the MMAs of tile i+1
+//                     run while the epilogue drains tile i
+//   warps 2..9        epilogue: each reads 32 TMEM lanes (rows) x 32 columns per
+//                     64-column step, applies bias / residual / GELU, writes a
+//                     128B-swizzled staging box; one thread TMA-stores each
+//                     box (staging is double-buffered, so the store of step s
+//                     overlaps step s+1), or TMA-reduce-adds the fp32 gradient
+// Bounded waits as in the single-tile kernel.
+#include <cuda.h>
+
+#include "../../include/gpipe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gp {
+namespace {
+
+constexpr int PM = 128;
+constexpr int PK = 64;
+constexpr int P_THREADS = 320;      // 10 warps
+constexpr int P_EPI_THREADS = 256;  // warps 2..9
+constexpr int PBOX = 16384;         // staging box: 128 rows x 128 B
+constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
+
+template <int BN, int EPI>
+struct PCfg {
+  static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
+  static constexpr int A_BYTES = PM * PK * 2;
+  static constexpr int B_BYTES = BN * PK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // per 64-column step: bf16 -> one box (two for bias+GELU: z and GELU(z)); fp32 -> two boxes
+  static constexpr int STEP_BOXES = F32_OUT ? 2 : (EPI == EPI_BIAS_GELU ? 2 : 1);
+  static constexpr int STAGING = 2 * STEP_BOXES * PBOX;  // double-buffered
+  static constexpr int ONES_BYTES = EPI == EPI_ACC_F32 ? 2048 : 0;
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - STAGING - ONES_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+  static constexpr int OFF_STG = STAGES * STAGE_BYTES;
+  static constexpr int OFF_ONES = OFF_STG + STAGING;
+  static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
+  static constexpr int SMEM = 1024 + OFF_BAR + 512;
+  // TMEM: two accumulators of BN columns (+ 2 x 16 bias-gradient columns)
+  static constexpr int TCOLS = (2 * BN + (EPI == EPI_ACC_F32 ? 32 : 0)) <= 256 ? 256 : 512;
+  static_assert(STAGES >= 2, "not enough shared memory for two stages");
+  static_assert(SMEM <= 232448, "over the 227 KB per-CTA shared memory limit");
+  static_assert(2 * BN + (EPI == EPI_ACC_F32 ? 32 : 0) <= 512, "accumulators exceed tensor memory");
+};
+
+struct PArgs {
+  const float* bias;   // fp32 [N] (store / bias+GELU) or NULL
+  float* dbias;        // EPI_ACC_F32: fp32 [M] += sum_k A(m,k), or NULL
+  const void* xsrc;    // residual (store) or GELU pre-activation (GELU backward), bf16, or NULL
+  int64_t ldx;
+  int M, N, K;
+  int m_tiles, n_tiles;
+};
+
+__device__ __forceinline__ uint32_t pswz(int r, int unit) {
+  return static_cast<uint32_t>(r * 128 + ((unit ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(P_EPI_THREADS) : "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait that gives up at once after any earlier give-up in the CTA.
+__device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, int* err, int code, volatile int* abort) {
+  if (*abort) return false;
+  if (mbar_wait_bounded(bar, parity, err, code)) return true;
+  *abort = 1;
+  return false;
+}
+
+template <bool A_K, bool B_K, int BN, int EPI>
+__global__ void __launch_bounds__(P_THREADS, 1)
+    tc_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
+                       PArgs args, int* err) {
+  using Cfg = PCfg<BN, EPI>;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sStg = smem + Cfg::OFF_STG;
+  uint8_t* sOnes = smem + Cfg::OFF_ONES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accf = empty + STAGES;  // accumulator b holds a finished tile
+  uint64_t* acce = accf + 2;        // accumulator b has been drained
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(acce + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = args.m_tiles * args.n_tiles;
+  const int nk = (args.K + PK - 1) / PK;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 8);  // one arrival per epilogue warp
+    }
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (EPI == EPI_ACC_F32 && threadIdx.x < 128) {  // 16 rows x 64 bf16 of 1.0
+    reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, Cfg::TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const int m0 = (t % args.m_tiles) * PM, n0 = (t / args.m_tiles) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!pwait(&empty[s], ((it / STAGES) & 1) ^ 1, err, DERR_TMA_WAIT, abort)) break;
+          mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+          uint8_t* a = smem + s * Cfg::STAGE_BYTES;
+          uint8_t* b = a + Cfg::A_BYTES;
+          const int k0 = kb * PK;
+          if (A_K) {
+            tma_load_2d(a, &tmA, k0, m0, &full[s]);
+          } else {
+            tma_load_2d(a, &tmA, m0, k0, &full[s]);
+            tma_load_2d(a + 8192, &tmA, m0 + 64, k0, &full[s]);
+          }
+          if (B_K) {
+            tma_load_2d(b, &tmB, k0, n0, &full[s]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b + j * 8192, &tmB, n0 + 64 * j, k0, &full[s]);
+          }
+        }
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+        mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, err, DERR_DRAIN_WAIT);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = mma_idesc_bf16(PM, BN, !A_K, !B_K);
+      constexpr uint32_t idesc_db = mma_idesc_bf16(PM, 16, !A_K, false);
+      const uint32_t ones = smem_u32(sOnes);
+      int it = 0, i = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (!pwait(&acce[b], ((i >> 1) & 1) ^ 1, err, DERR_MMA_WAIT, abort)) break;
+        tc_fence_after();
+        const bool do_db = EPI == EPI_ACC_F32 && args.dbias != nullptr && t / args.m_tiles == 0;
+        const uint32_t dacc = tmem + b * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!pwait(&full[s], (it / STAGES) & 1, err, DERR_MMA_WAIT, abort)) break;
+          tc_fence_after();
+          const uint32_t a = smem_u32(smem + s * Cfg::STAGE_BYTES);
+          const uint32_t bb = a + Cfg::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < PK / 16; ++kk) {
+            const uint64_t ad = A_K ? sw128_desc(a + kk * 32, 16, 1024) : sw128_desc(a + kk * 2048, 8192, 1024);
+            const uint64_t bd = B_K ? sw128_desc(bb + kk * 32, 16, 1024) : sw128_desc(bb + kk * 2048, 8192, 1024);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            tc_mma_f16(dacc, ad, bd, idesc, acc);
+            if (do_db) tc_mma_f16(tmem + 2 * BN + 16 * b, ad, sw128_desc(ones + kk * 32, 16, 1024), idesc_db, acc);
+          }
+          tc_commit(&empty[s]);
+        }
+        tc_commit(&accf[b]);  // fires once this tile's MMAs have completed
+      }
+    }
+  } else {
+    // ---- epilogue warps 2..9: TMEM lane quarter q, column half h of each 64-column step ----
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    const int etid = threadIdx.x - 64;
+    int step = 0, i = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      const int m0 = (t % args.m_tiles) * PM, n0 = (t / args.m_tiles) * BN;
+      const int m = m0 + r;
+      pwait(&accf[b], (i >> 1) & 1, err, DERR_ACC_WAIT, abort);
+      tc_fence_after();
+      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 64; ++c, ++step) {
+        uint8_t* stg = sStg + (step & 1) * Cfg::STEP_BOXES * PBOX;
+        if (etid == 0) bulk_wait_read_1();  // the store that last used this buffer has read it
+        epi_bar();
+        uint32_t rr[32];
+        tmem_ld32(tb + c * 64 + h * 32, rr);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
+        const int ncol0 = n0 + c * 64 + h * 32;
+        if (Cfg::F32_OUT) {
+          uint8_t* box = stg + h * PBOX;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(box + pswz(r, u)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        } else {
+          const bool full_cols = ncol0 + 32 <= args.N;
+          if ((EPI == EPI_STORE || EPI == EPI_BIAS_GELU) && args.bias) {
+            if (full_cols) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                float bb8[8];
+                load8(args.bias + ncol0 + j, bb8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[j + e] += bb8[e];
+              }
+            } else {
+              for (int j = 0; j < 32; ++j)
+                if (ncol0 + j < args.N) v[j] += args.bias[ncol0 + j];
+            }
+          }
+          if (args.xsrc && m < args.M) {
+            const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx;
+            float xv[32];
+            if (full_cols) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) load8(xr + ncol0 + j, xv + j);
+            } else {
+              for (int j = 0; j < 32; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xr[ncol0 + j]) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (EPI == EPI_GELU_BWD) v[j] *= gelu_grad_f(xv[j]);
+              else v[j] += xv[j];
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) store8(reinterpret_cast<__nv_bfloat16*>(stg + pswz(r, h * 4 + u)), v + 8 * u);
+          if (EPI == EPI_BIAS_GELU) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float gv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) gv[e] = gelu_f(v[8 * u + e]);
+              store8(reinterpret_cast<__nv_bfloat16*>(stg + PBOX + pswz(r, h * 4 + u)), gv);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        epi_bar();
+        if (etid == 0 && !*abort) {
+          if (Cfg::F32_OUT) {
+            for (int bx = 0; bx < 2; ++bx) {
+              const int x = n0 + c * 64 + bx * 32;
+              if (x >= args.N) break;
+              if (EPI == EPI_ACC_F32) tma_reduce_add_2d(&tmC, x, m0, stg + bx * PBOX);
+              else tma_store_2d(&tmC, x, m0, stg + bx * PBOX);
+            }
+          } else {
+            const int x = n0 + c * 64;
+            if (x < args.N) {
+              tma_store_2d(&tmC, x, m0, stg);
+              if (EPI == EPI_BIAS_GELU) tma_store_2d(&tmC2, x, m0, stg + PBOX);
+            }
+          }
+          bulk_commit();
+        }
+      }
+      if (EPI == EPI_ACC_F32 && args.dbias != nullptr && n0 == 0 && h == 0) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * BN + 16 * b, rr);
+        tmem_ld_wait();
+        if (m < args.M && !*abort) args.dbias[m] += __uint_as_float(rr[0]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[b]);  // this warp has drained accumulator b
+    }
+    if (etid == 0) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::TCOLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+bool pmake_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64_t outer, int64_t ld, int box_inner,
+                int box_outer) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn enc = nullptr;
+  if (!enc) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<EncodeFn>(p);
+  }
+  const int es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool A_K, bool B_K, int BN, int EPI>
+int pset_attr() {
+  static bool done = false;
+  if (!done) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI>::SMEM);
+    if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "persistent gemm: smem attribute: %s", cudaGetErrorString(e));
+    done = true;
+  }
+  return GPIPE_OK;
+}
+
+template <bool A_K, bool B_K, int BN, int EPI>
+int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
+  using Cfg = PCfg<BN, EPI>;
+  CUtensorMap ta, tb, tc, tc2;
+  bool ok = A_K ? pmake_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, PM) : pmake_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
+  ok = ok && (B_K ? pmake_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, BN)
+                  : pmake_tmap(&tb, g.B, false, g.N, g.K, g.ldb, 64, 64));
+  ok = ok && pmake_tmap(&tc, g.C, Cfg::F32_OUT, g.N, g.M, g.ldc, Cfg::F32_OUT ? 32 : 64, PM);
+  tc2 = tc;
+  if (EPI == EPI_BIAS_GELU) ok = ok && pmake_tmap(&tc2, g.C2, false, g.N, g.M, g.ldc, 64, PM);
+  if (!ok) return set_error(GPIPE_ERR_CUDA, "persistent gemm: cuTensorMapEncodeTiled failed");
+  int rc = pset_attr<A_K, B_K, BN, EPI>();
+  if (rc) return rc;
+  PArgs args{};
+  args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU) ? g.bias : nullptr;
+  args.dbias = EPI == EPI_ACC_F32 ? g.dbias : nullptr;
+  args.xsrc = EPI == EPI_STORE ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : nullptr);
+  args.ldx = EPI == EPI_STORE ? g.ldr : g.ldaux;
+  args.M = g.M;
+  args.N = g.N;
+  args.K = g.K;
+  args.m_tiles = (g.M + PM - 1) / PM;
+  args.n_tiles = (g.N + BN - 1) / BN;
+  const int tiles = args.m_tiles * args.n_tiles;
+  const int grid = ctas < tiles ? ctas : tiles;
+  tc_gemm_persistent<A_K, B_K, BN, EPI><<<grid, P_THREADS, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, args,
+                                                                               device_error_ptr());
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "persistent gemm launch: %s", cudaGetErrorString(e));
+  return GPIPE_OK;
+}
+
+// Output-tile width per epilogue: 256 columns for bf16 stores (a 128 x 256
+// tile halves the A traffic per flop), 128 where the staging or the
+// bias-gradient accumulator needs the room.
+template <int EPI>
+constexpr int pbn() {
+  return (EPI == EPI_STORE || EPI == EPI_GELU_BWD) ? 256 : 128;
+}
+
+}  // namespace
+
+int64_t persistent_tiles(const GemmDesc& g) {
+  int bn = 128;
+  if (g.epi == EPI_STORE || g.epi == EPI_GELU_BWD) bn = 256;
+  return static_cast<int64_t>((g.M + PM - 1) / PM) * ((g.N + bn - 1) / bn);
+}
+
+int launch_gemm_persistent(const GemmDesc& g, cudaStream_t s, int ctas) {
+  if (g.a_kmajor && g.b_kmajor) {
+    switch (g.epi) {
+      case EPI_STORE: return prun<true, true, pbn<EPI_STORE>(), EPI_STORE>(g, s, ctas);
+      case EPI_BIAS_GELU: return prun<true, true, pbn<EPI_BIAS_GELU>(), EPI_BIAS_GELU>(g, s, ctas);
+      case EPI_STORE_F32: return prun<true, true, pbn<EPI_STORE_F32>(), EPI_STORE_F32>(g, s, ctas);
+      case EPI_ACC_F32: return prun<true, true, pbn<EPI_ACC_F32>(), EPI_ACC_F32>(g, s, ctas);
+    }
+  } else if (g.a_kmajor && !g.b_kmajor) {
+    switch (g.epi) {
+      case EPI_STORE: return prun<true, false, pbn<EPI_STORE>(), EPI_STORE>(g, s, ctas);
+      case EPI_GELU_BWD: return prun<true, false, pbn<EPI_GELU_BWD>(), EPI_GELU_BWD>(g, s, ctas);
+      case EPI_ACC_F32: return prun<true, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>(g, s, ctas);
+    }
+  } else if (!g.a_kmajor && !g.b_kmajor) {
+    switch (g.epi) {
+      case EPI_STORE: return prun<false, false, pbn<EPI_STORE>(), EPI_STORE>(g, s, ctas);
+      case EPI_ACC_F32: return prun<false, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>(g, s, ctas);
+    }
+  }
+  return set_error(GPIPE_ERR_UNSUPPORTED, "persistent gemm: layout/epilogue not built");
+}
+
+int prepare_gemm_persistent() {
+  int rc = GPIPE_OK;
+  rc = rc ? rc : pset_attr<true, true, pbn<EPI_STORE>(), EPI_STORE>();
+  rc = rc ? rc : pset_attr<true, true, pbn<EPI_BIAS_GELU>(), EPI_BIAS_GELU>();
+  rc = rc ? rc : pset_attr<true, true, pbn<EPI_STORE_F32>(), EPI_STORE_F32>();
+  rc = rc ? rc : pset_attr<true, true, pbn<EPI_ACC_F32>(), EPI_ACC_F32>();
+  rc = rc ? rc : pset_attr<true, false, pbn<EPI_STORE>(), EPI_STORE>();
+  rc = rc ? rc : pset_attr<true, false, pbn<EPI_GELU_BWD>(), EPI_GELU_BWD>();
+  rc = rc ? rc : pset_attr<true, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>();
+  rc = rc ? rc : pset_attr<false, false, pbn<EPI_STORE>(), EPI_STORE>();
+  rc = rc ? rc : pset_attr<false, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>();
+  return rc;
+}
+
+}  // namespace gp

@@ -514,10 +514,13 @@ int run_epi_bn(const GemmDesc& g, cudaStream_t s) {
 // 128 columns when that already gives at least one CTA per SM, else 64
 // (twice the CTAs, each with half the operand traffic and epilogue work).
 int run_epi(const GemmDesc& g, cudaStream_t s) {
-  // Tile width: 128 columns when that gives at least one CTA per SM of this
-  // GEMM's share of the machine, else 64 (twice the CTAs, each with half the
-  // operand traffic and epilogue work).
+  // More tiles than this GEMM's share of the machine (at 128 x 256 / 128 x 128
+  // tiles): the persistent kernel, one CTA per SM of the share, overlapping
+  // each tile's epilogue with the next tile's MMAs.  Otherwise one tile per
+  // CTA, 128 columns when that gives at least one CTA per SM of the share,
+  // else 64 (twice the CTAs, each with half the operand traffic and epilogue).
   const int budget = g.sm_budget > 0 ? g.sm_budget : num_sms();
+  if (persistent_tiles(g) > budget) return launch_gemm_persistent(g, s, budget);
   const int64_t tiles128 = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 127) / 128);
   if (tiles128 >= budget) return run_epi_bn<128>(g, s);
   return run_epi_bn<64>(g, s);
@@ -548,7 +551,8 @@ int prepare_bn() {
 int prepare_gemm_tc() {
   if (!encode_fn()) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled entry point not found");
   int rc = prepare_bn<128>();
-  return rc ? rc : prepare_bn<64>();
+  rc = rc ? rc : prepare_bn<64>();
+  return rc ? rc : prepare_gemm_persistent();
 }
 
 int launch_gemm_tc(const GemmDesc& g, cudaStream_t stream) {

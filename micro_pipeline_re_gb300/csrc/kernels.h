@@ -49,6 +49,11 @@ struct GemmDesc {
 int launch_gemm(const GemmDesc& g, cudaStream_t stream);       // dispatch by dtype
 int launch_gemm_tc(const GemmDesc& g, cudaStream_t stream);    // bf16, tcgen05 + TMA
 int launch_gemm_simt(const GemmDesc& g, cudaStream_t stream);  // fp32 or bf16, FFMA
+// Persistent tcgen05 GEMM (one CTA per SM over many tiles, two TMEM
+// accumulators); `ctas` caps the grid.  persistent_tiles: its tile count.
+int launch_gemm_persistent(const GemmDesc& g, cudaStream_t stream, int ctas);
+int64_t persistent_tiles(const GemmDesc& g);
+int prepare_gemm_persistent();
 
 size_t colred_scratch_floats(int rows, int cols);
 

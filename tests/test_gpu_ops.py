@@ -31,10 +31,12 @@ def _gemm_ref(A, B, ak, bk):
 # (M, N, K): several tiles with ragged tails in every dimension
 # (the last one has enough 128-wide tiles to take the 128-column variant;
 # the others take the 64-column one)
-# (1704^2 has enough 128-wide tiles for the 128-column variant; the others
-# take the 64-column one; the two long-K shapes split K across a cluster)
+# (1704^2 has enough 128-wide tiles for the 128-column variant or, for the
+# 128-wide epilogues, the persistent kernel; the others take the 64-column one;
+# the two long-K shapes split K across a cluster; 2056 x 2568 takes the
+# persistent kernel for every epilogue, ragged in M, N and K)
 SHAPES = [(384, 640, 512), (200, 136, 200), (128, 128, 64), (1000, 96, 72), (1704, 1704, 200),
-          (200, 256, 16384), (256, 136, 4096)]
+          (200, 256, 16384), (256, 136, 4096), (2056, 2568, 264)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
