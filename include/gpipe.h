@@ -163,11 +163,14 @@ enum {
   GPIPE_OPT_CONCURRENT = 6,  /* [1] run weight-gradient GEMMs and the loss-only head
                                 forward on a second stream per lane (ordered by
                                 events); 0: in program order.  Results are identical. */
-  GPIPE_OPT_PIPELINE = 7     /* [1] run the K cells as K concurrent lanes, each with its
+  GPIPE_OPT_PIPELINE = 7,    /* [1] run the K cells as K concurrent lanes, each with its
                                 own cell workspace: cell k works on micro-batch m while
                                 cell k+1 works on m-1, as the review's K accelerators
                                 do; 0: one lane, cells in turn (least memory).  Results
                                 are identical.  Set before gpipe_sizes. */
+  GPIPE_OPT_PDL = 8          /* [1] launch each kernel with programmatic dependent
+                                launch (it waits for its predecessor on the GPU before
+                                reading memory, so only the launch overlaps); 0: off */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

@@ -20,8 +20,8 @@ OK = 0
 ERR = {-1: "INVALID_ARG", -2: "NOT_PARTITIONED", -3: "CUDA", -4: "DEVICE_TIMEOUT", -5: "NONFINITE_LOSS",
        -6: "UNSUPPORTED"}
 
-OPT_KEEP_GRADS, OPT_GRAPH, OPT_NO_REMAT, OPT_REMAT_CHECK, OPT_SKIP_UPDATE, OPT_CONCURRENT, OPT_PIPELINE = \
-    1, 2, 3, 4, 5, 6, 7
+OPT_KEEP_GRADS, OPT_GRAPH, OPT_NO_REMAT, OPT_REMAT_CHECK, OPT_SKIP_UPDATE, OPT_CONCURRENT, OPT_PIPELINE, OPT_PDL = \
+    1, 2, 3, 4, 5, 6, 7, 8
 EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
 
 

@@ -16,6 +16,7 @@
 #include "../../include/gpipe.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "launch_util.cuh"
 
 namespace gp {
 namespace {
@@ -131,6 +132,8 @@ __device__ __forceinline__ void store_frag(__nv_bfloat16* dst, int64_t ld, const
 __global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __restrict__ qkv,
                                                        __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                                                        int seq, int heads) {
+  griddep_wait();
+  griddep_launch();
   __shared__ __align__(16) __nv_bfloat16 Qs[BQ][LDS];
   __shared__ __align__(16) __nv_bfloat16 Ks[2][BQ][LDS];
   __shared__ __align__(16) __nv_bfloat16 Vs[2][BQ][LDS];
@@ -257,6 +260,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
                                                           const __nv_bfloat16* __restrict__ dout,
                                                           const float* __restrict__ lse, float* __restrict__ dvec,
                                                           __nv_bfloat16* __restrict__ dqkv, int seq, int heads) {
+  griddep_wait();
+  griddep_launch();
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   DqSmem& S = *reinterpret_cast<DqSmem*>(dyn_smem);
   auto& Qs = S.Qs;
@@ -353,6 +358,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const __nv_bfloat16* 
                                                            const float* __restrict__ lse,
                                                            const float* __restrict__ dvec,
                                                            __nv_bfloat16* __restrict__ dqkv, int seq, int heads) {
+  griddep_wait();
+  griddep_launch();
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   DkvSmem& S = *reinterpret_cast<DkvSmem*>(dyn_smem);
   auto& Ks = S.Ks;
@@ -455,7 +462,7 @@ int launch_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o,
     return set_error(GPIPE_ERR_INVALID_ARG, "attention: need nseq >= 1, seq %% 64 == 0, heads >= 1");
   if (!al16(qkv) || !al16(o)) return set_error(GPIPE_ERR_INVALID_ARG, "attention: pointers must be 16-B aligned");
   dim3 grid(seq / BQ, heads, nseq);
-  attn_fwd_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), lse,
+  (void)launch_k(attn_fwd_kernel, grid, 128, 0, s, static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), lse,
                                        seq, heads);
   count_launch();
   cudaError_t e = cudaGetLastError();
@@ -472,12 +479,12 @@ int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const vo
   int rc = prepare_attention();
   if (rc) return rc;
   dim3 grid(seq / BQ, heads, nseq);
-  attn_bwd_dq_kernel<<<grid, 128, sizeof(DqSmem), s>>>(static_cast<const __nv_bfloat16*>(qkv),
+  (void)launch_k(attn_bwd_dq_kernel, grid, 128, sizeof(DqSmem), s, static_cast<const __nv_bfloat16*>(qkv),
                                           static_cast<const __nv_bfloat16*>(o),
                                           static_cast<const __nv_bfloat16*>(dout), lse, dvec,
                                           static_cast<__nv_bfloat16*>(dqkv), seq, heads);
   count_launch();
-  attn_bwd_dkv_kernel<<<grid, 128, sizeof(DkvSmem), s>>>(static_cast<const __nv_bfloat16*>(qkv),
+  (void)launch_k(attn_bwd_dkv_kernel, grid, 128, sizeof(DkvSmem), s, static_cast<const __nv_bfloat16*>(qkv),
                                            static_cast<const __nv_bfloat16*>(dout), lse, dvec,
                                            static_cast<__nv_bfloat16*>(dqkv), seq, heads);
   count_launch();

@@ -9,6 +9,7 @@
 #include "../../include/gpipe.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "launch_util.cuh"
 
 namespace gp {
 namespace {
@@ -37,6 +38,8 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, co
                                                      const float* __restrict__ b, T* __restrict__ y,
                                                      float* __restrict__ mean, float* __restrict__ rstd, int rows,
                                                      int d) {
+  griddep_wait();
+  griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
   if (row >= rows) return;
@@ -99,6 +102,8 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, c
                                                      const float* __restrict__ g, const T* __restrict__ dres,
                                                      T* __restrict__ dx, float* __restrict__ partial, int rows,
                                                      int d) {
+  griddep_wait();
+  griddep_launch();
   __shared__ __align__(16) float acc_s[2 * 32 * 8 * kMaxChunks];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kLnRowsPerWarp + warp;
@@ -180,6 +185,8 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, c
 // the rest to out_b.
 __global__ void col_reduce_kernel(const float* __restrict__ partial, int nparts, int ncols, float* out_a,
                                   int split, float* out_b) {
+  griddep_wait();
+  griddep_launch();
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= ncols) return;
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -201,6 +208,8 @@ __global__ void col_reduce_kernel(const float* __restrict__ partial, int nparts,
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict__ y, int64_t ldy, int rows,
                                                              int cols, float* __restrict__ partial) {
+  griddep_wait();
+  griddep_launch();
   const int col = (blockIdx.x * 256 + threadIdx.x) * 8;
   if (col >= cols) return;
   const int r0 = blockIdx.y * kColRowsPerChunk;
@@ -224,6 +233,8 @@ __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logi
                                                         const int32_t* __restrict__ tokens, int row0,
                                                         float inv_count, float* __restrict__ loss_rows,
                                                         int want_grad, int* err) {
+  griddep_wait();
+  griddep_launch();
   __shared__ float sm_m[kCeThreads / 32], sm_s[kCeThreads / 32];
   __shared__ float sh_lse;
   const int r = blockIdx.x;
@@ -304,6 +315,8 @@ __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logi
 // MSE: one warp per row.
 __global__ void mse_kernel(const float* __restrict__ y, const float* __restrict__ t, int rows, int d,
                            float inv_count, float* __restrict__ loss_rows, float* __restrict__ dy) {
+  griddep_wait();
+  griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
   if (r >= rows) return;
@@ -322,6 +335,8 @@ __global__ void mse_kernel(const float* __restrict__ y, const float* __restrict_
 // ---------------------------------------------------------------------------
 __global__ void embed_fwd_kernel(int rows, int d, int vocab, const int32_t* __restrict__ tokens,
                                  const __nv_bfloat16* __restrict__ emb, __nv_bfloat16* __restrict__ x, int* err) {
+  griddep_wait();
+  griddep_launch();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element group
   const int groups = d / 8;
   if (i >= (int64_t)rows * groups) return;
@@ -343,6 +358,8 @@ __global__ void __launch_bounds__(256) embed_bwd_kernel(int rows, int d, int voc
                                                         const int32_t* __restrict__ tokens,
                                                         const __nv_bfloat16* __restrict__ dx,
                                                         float* __restrict__ demb) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int list[256];
   __shared__ int wcount[8];
   const int v0 = blockIdx.x * vpc, v1 = min(v0 + vpc, vocab);
@@ -388,6 +405,8 @@ __device__ __forceinline__ void rms_one(float& w, float& g, float& v, float lr, 
 __global__ void rmsprop_kernel(float* __restrict__ w, float* __restrict__ g, float* __restrict__ v,
                                __nv_bfloat16* __restrict__ wb, size_t n, float lr, float decay, float eps,
                                int zero_grad) {
+  griddep_wait();
+  griddep_launch();
   const float omd = 1.0f - decay;
   const size_t n4 = n / 4;
   float4* w4 = reinterpret_cast<float4*>(w);
@@ -423,12 +442,16 @@ __global__ void rmsprop_kernel(float* __restrict__ w, float* __restrict__ g, flo
 }
 
 __global__ void cast_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, size_t n) {
+  griddep_wait();
+  griddep_launch();
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = f2bf(src[i]);
 }
 
 // One block of 1024 threads: fixed-order fp64 partial sums, fixed tree.
 __global__ void __launch_bounds__(1024) sum_kernel(const float* __restrict__ x, size_t n, float* out) {
+  griddep_wait();
+  griddep_launch();
   __shared__ double sm[1024];
   double s = 0.0;
   for (size_t i = threadIdx.x; i < n; i += 1024) s += static_cast<double>(x[i]);
@@ -442,12 +465,16 @@ __global__ void __launch_bounds__(1024) sum_kernel(const float* __restrict__ x, 
 }
 
 __global__ void copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, size_t n16) {
+  griddep_wait();
+  griddep_launch();
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) dst[i] = src[i];
 }
 
 __global__ void count_diff_kernel(const uint32_t* __restrict__ a, const uint32_t* __restrict__ b, size_t n4,
                                   unsigned long long* counter) {
+  griddep_wait();
+  griddep_launch();
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   unsigned int c = 0;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -476,10 +503,10 @@ int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float*
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm: pointers must be 16-B aligned");
   const int grid = blocks_for(rows, 8);
   if (dtype == DT_F32)
-    ln_fwd_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), g, b, static_cast<float*>(y), mean,
+    (void)launch_k(ln_fwd_kernel<float>, grid, 256, 0, s, static_cast<const float*>(x), g, b, static_cast<float*>(y), mean,
                                               rstd, rows, d);
   else
-    ln_fwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), g, b,
+    (void)launch_k(ln_fwd_kernel<__nv_bfloat16>, grid, 256, 0, s, static_cast<const __nv_bfloat16*>(x), g, b,
                                                       static_cast<__nv_bfloat16*>(y), mean, rstd, rows, d);
   return check_launch("layernorm_fwd");
 }
@@ -494,16 +521,16 @@ int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void*
   const int parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
   const int grid = parts;
   if (dtype == DT_F32)
-    ln_bwd_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(dy), static_cast<const float*>(x), mean,
+    (void)launch_k(ln_bwd_kernel<float>, grid, 256, 0, s, static_cast<const float*>(dy), static_cast<const float*>(x), mean,
                                               rstd, g, static_cast<const float*>(dres), static_cast<float*>(dx),
                                               scratch, rows, d);
   else
-    ln_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+    (void)launch_k(ln_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, 
         static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean, rstd, g,
         static_cast<const __nv_bfloat16*>(dres), static_cast<__nv_bfloat16*>(dx), scratch, rows, d);
   int rc = check_launch("layernorm_bwd");
   if (rc) return rc;
-  col_reduce_kernel<<<blocks_for(2 * d, 256), 256, 0, s>>>(scratch, parts, 2 * d, dg_acc, d, db_acc);
+  (void)launch_k(col_reduce_kernel, blocks_for(2 * d, 256), 256, 0, s, scratch, parts, 2 * d, dg_acc, d, db_acc);
   return check_launch("layernorm_bwd reduce");
 }
 
@@ -515,13 +542,13 @@ int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, flo
   const int chunks = (rows + kColRowsPerChunk - 1) / kColRowsPerChunk;
   dim3 grid(blocks_for(cols, 256 * 8), chunks);
   if (dtype == DT_F32)
-    colsum_partial_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(y), ldy, rows, cols, scratch);
+    (void)launch_k(colsum_partial_kernel<float>, grid, 256, 0, s, static_cast<const float*>(y), ldy, rows, cols, scratch);
   else
-    colsum_partial_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(y), ldy, rows,
+    (void)launch_k(colsum_partial_kernel<__nv_bfloat16>, grid, 256, 0, s, static_cast<const __nv_bfloat16*>(y), ldy, rows,
                                                               cols, scratch);
   int rc = check_launch("colsum");
   if (rc) return rc;
-  col_reduce_kernel<<<blocks_for(cols, 256), 256, 0, s>>>(scratch, chunks, cols, out_acc, cols, nullptr);
+  (void)launch_k(col_reduce_kernel, blocks_for(cols, 256), 256, 0, s, scratch, chunks, cols, out_acc, cols, nullptr);
   return check_launch("colsum reduce");
 }
 
@@ -530,7 +557,7 @@ int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, in
   if (rows < 1 || vocab < 4 || vocab % 4 || seq < 1 || row0 < 0)
     return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: need rows >= 1, vocab %% 4 == 0, seq >= 1");
   if (!al16(logits)) return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: logits must be 16-B aligned");
-  ce_kernel<<<rows, kCeThreads, 0, s>>>(logits, vocab, seq, tokens, row0, inv_count, loss_rows, want_grad,
+  (void)launch_k(ce_kernel, rows, kCeThreads, 0, s, logits, vocab, seq, tokens, row0, inv_count, loss_rows, want_grad,
                                         device_error_ptr());
   return check_launch("cross_entropy");
 }
@@ -538,7 +565,7 @@ int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, in
 int launch_mse(int rows, int d, const float* y, const float* t, float inv_count, float* loss_rows, float* dy,
                cudaStream_t s) {
   if (rows < 1 || d < 1) return set_error(GPIPE_ERR_INVALID_ARG, "mse: need rows, d >= 1");
-  mse_kernel<<<blocks_for(rows, 8), 256, 0, s>>>(y, t, rows, d, inv_count, loss_rows, dy);
+  (void)launch_k(mse_kernel, blocks_for(rows, 8), 256, 0, s, y, t, rows, d, inv_count, loss_rows, dy);
   return check_launch("mse");
 }
 
@@ -547,7 +574,7 @@ int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, cons
   if (rows < 1 || d < 8 || d % 8 || !al16(emb) || !al16(x))
     return set_error(GPIPE_ERR_INVALID_ARG, "embedding_fwd: need d %% 8 == 0 and 16-B aligned rows");
   const int64_t n = (int64_t)rows * (d / 8);
-  embed_fwd_kernel<<<blocks_for(n, 256), 256, 0, s>>>(rows, d, vocab, tokens,
+  (void)launch_k(embed_fwd_kernel, blocks_for(n, 256), 256, 0, s, rows, d, vocab, tokens,
                                                       static_cast<const __nv_bfloat16*>(emb),
                                                       static_cast<__nv_bfloat16*>(x), device_error_ptr());
   return check_launch("embedding_fwd");
@@ -560,7 +587,7 @@ int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, cons
   int ctas = 4 * num_sms();
   const int vpc = (vocab + ctas - 1) / ctas;
   ctas = (vocab + vpc - 1) / vpc;
-  embed_bwd_kernel<<<ctas, 256, 0, s>>>(rows, d, vocab, vpc, tokens, static_cast<const __nv_bfloat16*>(dx), demb);
+  (void)launch_k(embed_bwd_kernel, ctas, 256, 0, s, rows, d, vocab, vpc, tokens, static_cast<const __nv_bfloat16*>(dx), demb);
   return check_launch("embedding_bwd");
 }
 
@@ -570,19 +597,19 @@ int launch_rmsprop(size_t n, float* w, float* g, float* v, void* wb, float lr, f
   if (!al16(w) || !al16(g) || !al16(v) || (wb && (reinterpret_cast<uintptr_t>(wb) & 7u)))
     return set_error(GPIPE_ERR_INVALID_ARG, "rmsprop: w, g, v must be 16-B aligned, w_bf16 8-B aligned");
   const int grid = std::min<int64_t>(blocks_for(n / 4 + 1, 256), (int64_t)num_sms() * 8);
-  rmsprop_kernel<<<grid, 256, 0, s>>>(w, g, v, static_cast<__nv_bfloat16*>(wb), n, lr, decay, eps, zero_grad);
+  (void)launch_k(rmsprop_kernel, grid, 256, 0, s, w, g, v, static_cast<__nv_bfloat16*>(wb), n, lr, decay, eps, zero_grad);
   return check_launch("rmsprop");
 }
 
 int launch_cast_bf16(size_t n, const float* src, void* dst, cudaStream_t s) {
   if (n == 0) return GPIPE_OK;
   const int grid = std::min<int64_t>(blocks_for(n, 256), (int64_t)num_sms() * 8);
-  cast_bf16_kernel<<<grid, 256, 0, s>>>(src, static_cast<__nv_bfloat16*>(dst), n);
+  (void)launch_k(cast_bf16_kernel, grid, 256, 0, s, src, static_cast<__nv_bfloat16*>(dst), n);
   return check_launch("cast_bf16");
 }
 
 int launch_sum(const float* x, size_t n, float* out, cudaStream_t s) {
-  sum_kernel<<<1, 1024, 0, s>>>(x, n, out);
+  (void)launch_k(sum_kernel, 1, 1024, 0, s, x, n, out);
   return check_launch("sum");
 }
 
@@ -591,7 +618,7 @@ int launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
     return set_error(GPIPE_ERR_INVALID_ARG, "copy: 16-B aligned buffers and sizes required");
   if (bytes == 0) return GPIPE_OK;
   const int grid = std::min<int64_t>(blocks_for(bytes / 16, 256), (int64_t)num_sms() * 8);
-  copy_kernel<<<grid, 256, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), bytes / 16);
+  (void)launch_k(copy_kernel, grid, 256, 0, s, static_cast<uint4*>(dst), static_cast<const uint4*>(src), bytes / 16);
   return check_launch("copy");
 }
 
@@ -599,7 +626,7 @@ int launch_count_diff(const void* a, const void* b, size_t bytes, unsigned long 
   if (bytes % 4) return set_error(GPIPE_ERR_INVALID_ARG, "count_diff: size must be a multiple of 4");
   if (bytes == 0) return GPIPE_OK;
   const int grid = std::min<int64_t>(blocks_for(bytes / 4, 256), (int64_t)num_sms() * 8);
-  count_diff_kernel<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(a), static_cast<const uint32_t*>(b),
+  (void)launch_k(count_diff_kernel, grid, 256, 0, s, static_cast<const uint32_t*>(a), static_cast<const uint32_t*>(b),
                                          bytes / 4, counter);
   return check_launch("count_diff");
 }

@@ -19,6 +19,7 @@
 #include "../../include/gpipe.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "launch_util.cuh"
 
 namespace gp {
 namespace {
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  griddep_wait();  // the previous kernel in the stream has completed; global reads from here on
 
   if (warp == 0) {
     if (lane == 0) {
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
         mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, err, DERR_DRAIN_WAIT);
     }
+    griddep_launch();
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = mma_idesc_bf16(PM, BN, !A_K, !B_K);
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         tc_commit(&accf[b]);  // fires once this tile's MMAs have completed
       }
     }
+    griddep_launch();
   } else {
     // ---- epilogue warps 2..9: TMEM lane quarter q, column half h of each 64-column step ----
     const int q = warp & 3;
@@ -294,6 +298,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[b]);  // this warp has drained accumulator b
     }
+    griddep_launch();
     if (etid == 0) bulk_wait_all();
   }
   tc_fence_before();
@@ -369,7 +374,7 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   args.n_tiles = (g.N + BN - 1) / BN;
   const int tiles = args.m_tiles * args.n_tiles;
   const int grid = ctas < tiles ? ctas : tiles;
-  tc_gemm_persistent<A_K, B_K, BN, EPI><<<grid, P_THREADS, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, args,
+  (void)launch_k(tc_gemm_persistent<A_K, B_K, BN, EPI>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
                                                                                device_error_ptr());
   count_launch();
   cudaError_t e = cudaGetLastError();

@@ -9,6 +9,7 @@
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "launch_util.cuh"
 
 namespace gp {
 namespace {
@@ -19,6 +20,8 @@ template <typename T, int EPI>
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const T* __restrict__ A, int64_t lda, int a_k,
                                                         const T* __restrict__ B, int64_t ldb, int b_k, int M, int N,
                                                         int K, EpiArgs ep, float* __restrict__ dbias) {
+  griddep_wait();
+  griddep_launch();
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   const int tid = threadIdx.x;
@@ -93,11 +96,11 @@ int run_simt(const GemmDesc& g, cudaStream_t s) {
   int ak = g.a_kmajor ? 1 : 0, bk = g.b_kmajor ? 1 : 0;
   float* db = g.epi == EPI_ACC_F32 ? g.dbias : nullptr;
   switch (g.epi) {
-    case EPI_STORE: simt_gemm_kernel<T, EPI_STORE><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
-    case EPI_BIAS_GELU: simt_gemm_kernel<T, EPI_BIAS_GELU><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
-    case EPI_GELU_BWD: simt_gemm_kernel<T, EPI_GELU_BWD><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
-    case EPI_ACC_F32: simt_gemm_kernel<T, EPI_ACC_F32><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
-    case EPI_STORE_F32: simt_gemm_kernel<T, EPI_STORE_F32><<<grid, 256, 0, s>>>(A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_STORE: (void)launch_k(simt_gemm_kernel<T, EPI_STORE>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_BIAS_GELU: (void)launch_k(simt_gemm_kernel<T, EPI_BIAS_GELU>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_GELU_BWD: (void)launch_k(simt_gemm_kernel<T, EPI_GELU_BWD>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_ACC_F32: (void)launch_k(simt_gemm_kernel<T, EPI_ACC_F32>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_STORE_F32: (void)launch_k(simt_gemm_kernel<T, EPI_STORE_F32>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
     default: return set_error(GPIPE_ERR_INVALID_ARG, "gemm: unknown epilogue %d", g.epi);
   }
   count_launch();

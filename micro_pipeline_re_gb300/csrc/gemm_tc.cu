@@ -37,6 +37,7 @@
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "launch_util.cuh"
 
 namespace gp {
 namespace {
@@ -128,6 +129,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(epib, 1);
     fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc(tslot, tcols);
+    tmem_relinquish();
+  }
+  griddep_wait();  // the previous kernel in the stream has completed; global reads from here on
   if (EPI != EPI_ACC_F32 && EPI != EPI_STORE_F32 && EPI != EPI_GELU_BWD) {
     if (threadIdx.x < BN) {
       const int n = n0 + threadIdx.x;
@@ -137,10 +143,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (do_db && threadIdx.x < 128) {  // 16 rows x 64 bf16 of 1.0
     reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_proxy_async_smem();
-  }
-  if (warp == 1) {
-    tmem_alloc(tslot, tcols);
-    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_commit(accb);  // fires once every MMA issued above has completed
   }
   __syncwarp();
+  griddep_launch();  // main loop issued: the next kernel may start its prologue
 
   // ---- epilogue: warp w reads TMEM lanes 32(w%4).. (tile rows 32(w%4) + lane);
   //      warps w and w+4 split the tile's 32-column chunks ----
@@ -441,17 +444,19 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = Cfg::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = S;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>, ta, tb, tc, tc2, tx, args,
                            device_error_ptr());
   } else {
-    tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT><<<grid, THREADS, Cfg::SMEM, stream>>>(ta, tb, tc, tc2, tx, args,
+    (void)launch_k(tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>, grid, THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, tx, args,
                                                                                   device_error_ptr());
     e = cudaGetLastError();
   }

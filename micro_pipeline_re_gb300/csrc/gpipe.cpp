@@ -25,6 +25,7 @@
 
 #include "../../include/gpipe.h"
 #include "kernels.h"
+#include "launch_util.cuh"
 #include "planner.h"
 
 namespace {
@@ -66,6 +67,7 @@ struct gpipe_ctx {
   cudaStream_t cap_stream = nullptr;
   bool concurrent = true;  // weight gradients and the loss-only head on each lane's side stream
   bool pipelined = true;   // cells run as concurrent lanes (the review's pipeline on one GPU)
+  bool pdl = true;         // kernels may launch while their predecessor drains
   static constexpr int kMaxLanes = 64;
   static constexpr int kLaneEvents = 9;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
@@ -158,6 +160,7 @@ class Executor {
   int run_step() {
     const Workspace& w = c_->ws;
     const int M = c_->M, K = c_->K;
+    set_pdl_enabled(c_->pdl);
     // zero the loss scalar and the debug counter, then start every lane
     if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, origin_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
@@ -673,6 +676,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[3] = c->remat_check_m;
     key.opts[4] = c->concurrent;
     key.opts[5] = c->pipelined;
+    key.opts[6] = c->pdl;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -764,6 +768,7 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_SKIP_UPDATE: c->skip_update = value != 0; break;
     case GPIPE_OPT_CONCURRENT: c->concurrent = value != 0; break;
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
+    case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     default: return c->fail(GPIPE_ERR_INVALID_ARG, "unknown option");
   }
   c->drop_graph();

@@ -8,6 +8,7 @@
 #include "../../include/gpipe_ops.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "launch_util.cuh"
 
 namespace gp {
 
@@ -30,6 +31,12 @@ int set_error(int code, const char* fmt, ...) {
 const char* last_error_message() { return g_last_error.c_str(); }
 
 void count_launch(int n) { g_launches += n; }
+
+namespace {
+thread_local bool g_pdl = true;
+}
+bool pdl_enabled() { return g_pdl; }
+void set_pdl_enabled(bool on) { g_pdl = on; }
 int64_t launch_count() { return g_launches; }
 
 int* device_error_ptr() {

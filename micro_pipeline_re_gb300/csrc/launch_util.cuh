@@ -1,0 +1,40 @@
+// Kernel launch with programmatic dependent launch (PDL).
+//
+// Every kernel of the library starts with griddep_wait() before it touches
+// global memory, which blocks until the preceding kernel in the stream has
+// completed and its writes are visible; so letting the next kernel launch
+// early (PDL) only overlaps its launch and prologue with the predecessor's
+// tail, and never changes a result.  Kernels call griddep_launch() once their
+// remaining work no longer needs the SM resources a waiting successor would
+// take.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <utility>
+
+namespace gp {
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Whether launches made by this thread may overlap their predecessor (set by
+// the step executor; default on).
+bool pdl_enabled();
+void set_pdl_enabled(bool on);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+}  // namespace gp

@@ -163,9 +163,10 @@ def test_schedules_are_bit_identical(b, wname):
     w = SMALL_LM if wname == "small_lm" else WORKLOADS[wname]
     inp = make_inputs(w)
     outs = []
-    for pipe, conc, graph in ((0, 0, 1), (1, 1, 1), (1, 0, 1), (0, 1, 1), (1, 1, 0)):
+    for pipe, conc, graph, pdl in ((0, 0, 1, 0), (1, 1, 1, 1), (1, 0, 1, 1), (0, 1, 1, 1), (1, 1, 0, 1),
+                                   (1, 1, 1, 0)):
         _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_PIPELINE, pipe), (b.OPT_CONCURRENT, conc),
-                                                     (b.OPT_GRAPH, graph)])
+                                                     (b.OPT_GRAPH, graph), (b.OPT_PDL, pdl)])
         outs.append((loss, st.g32.cpu().numpy().copy(), st.p32.cpu().numpy().copy()))
     for o in outs[1:]:
         assert o[0] == outs[0][0]
