@@ -168,9 +168,11 @@ enum {
                                 cell k+1 works on m-1, as the review's K accelerators
                                 do; 0: one lane, cells in turn (least memory).  Results
                                 are identical.  Set before gpipe_sizes. */
-  GPIPE_OPT_PDL = 8          /* [1] launch each kernel with programmatic dependent
+  GPIPE_OPT_PDL = 8          /* [0] 1: launch each kernel with programmatic dependent
                                 launch (it waits for its predecessor on the GPU before
-                                reading memory, so only the launch overlaps); 0: off */
+                                reading memory, so only the launch overlaps).  Off by
+                                default: with concurrent lanes the early-launched
+                                kernels hold SM resources other lanes need.          */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

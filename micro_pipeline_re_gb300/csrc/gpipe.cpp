@@ -67,7 +67,7 @@ struct gpipe_ctx {
   cudaStream_t cap_stream = nullptr;
   bool concurrent = true;  // weight gradients and the loss-only head on each lane's side stream
   bool pipelined = true;   // cells run as concurrent lanes (the review's pipeline on one GPU)
-  bool pdl = true;         // kernels may launch while their predecessor drains
+  bool pdl = false;        // kernels may launch while their predecessor drains (measured slower with lanes)
   static constexpr int kMaxLanes = 64;
   static constexpr int kLaneEvents = 9;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
