@@ -74,6 +74,9 @@ struct gpipe_ctx {
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
   cudaEvent_t ev_origin = nullptr, ev_fwd[kMaxLanes] = {}, ev_bdone[kMaxLanes][2] = {}, ev_bfree[kMaxLanes][2] = {},
               ev_lane_end[kMaxLanes] = {};
+  std::vector<cudaEvent_t> ev_hdone;  // per micro-batch: the head has written the last cell's output gradient
+  // streams in use: one pair per lane, plus the head's pair when the cells are pipelined
+  int nstreams() const { return ws.nlanes > 1 ? ws.nlanes + 1 : 1; }
   cudaGraphExec_t gexec = nullptr;
   cudaGraph_t graph = nullptr;
   GraphKey key{};
@@ -94,7 +97,7 @@ struct gpipe_ctx {
   void refresh_ws() {
     if (ws_stale) {
       ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat,
-                          pipelined && K <= kMaxLanes);
+                          pipelined && K < kMaxLanes);
       ws_stale = false;
     }
   }
@@ -107,7 +110,9 @@ struct gpipe_ctx {
       return st || cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
     };
     bool ok = mk_ev(ev_origin);
-    for (int i = 0; i < ws.nlanes && ok; ++i) {
+    if (static_cast<int>(ev_hdone.size()) < M) ev_hdone.resize(M, nullptr);
+    for (int m = 0; m < M && ok; ++m) ok = mk_ev(ev_hdone[m]);
+    for (int i = 0; i < nstreams() && ok; ++i) {
       ok = mk_st(lane_main[i]) && mk_st(lane_side[i]) && mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
       for (int e = 0; e < kLaneEvents && ok; ++e) ok = mk_ev(lane_ev[i][e]);
     }
@@ -165,24 +170,24 @@ class Executor {
     if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, origin_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
     TRY(cuda_ok(cudaEventRecord(c_->ev_origin, origin_), "event record"));
-    for (int i = 0; i < w.nlanes; ++i)
+    for (int i = 0; i < c_->nstreams(); ++i)
       TRY(cuda_ok(cudaStreamWaitEvent(c_->lane_main[i], c_->ev_origin, 0), "stream wait"));
 
-    // phase 1: forward of every micro-batch through every cell
+    // phase 1: forward of every micro-batch through every cell; then the head
+    // (final LN, logits, loss and its gradient) of that micro-batch, once, on
+    // its own lane, which hands the last cell the gradient of its output
+    const int hl = head_lane();
     for (int m = 0; m < M; ++m) {
       TRY(cell0_input(m));
       for (int k = 0; k < K; ++k) {
         if (k > 0) TRY(cross_wait(k, c_->ev_fwd[k - 1], fwd_rec_[k - 1], k - 1));
         TRY(cell_forward(k, m, /*recompute=*/false));
-        if (k < K - 1) TRY(cross_record(k, c_->ev_fwd[k], fwd_rec_[k]));
+        TRY(cross_record(k, c_->ev_fwd[k], fwd_rec_[k]));
       }
-      // loss-only head forward on the last lane's side stream
-      const int lk = lane_of(K - 1);
-      TRY(fork(lk));
-      cur_ = side(lk);
-      TRY(head(m, /*backward=*/false, nullptr));
-      cur_ = nullptr;
-      TRY(mark(lk, EV_HEADF));
+      if (hl != lane_of(K - 1))
+        TRY(cuda_ok(cudaStreamWaitEvent(main_s(hl), c_->ev_fwd[K - 1], 0), "stream wait"));
+      TRY(head(m));
+      if (hl != lane_of(K - 1)) TRY(cuda_ok(cudaEventRecord(c_->ev_hdone[m], main_s(hl)), "event record"));
     }
     // phase 2: backward with re-computation
     for (int m = 0; m < M; ++m) {
@@ -190,20 +195,19 @@ class Executor {
       for (int k = K - 1; k >= 0; --k) {
         const int lk = lane_of(k);
         cur_lane_ = lk;
-        TRY(join_all(lk));  // side work still reading this lane's slots / head buffers
+        TRY(join_all(lk));  // side work still reading this lane's slots
         if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
         // gradient of the cell's output
         char* dy;
-        int dy_buf;
+        const int dy_buf = BUF_EXT;
         if (k == K - 1) {
-          dy = lbuf(lk, 0);
-          dy_buf = 0;
-          TRY(head(m, /*backward=*/true, dy));
+          if (hl != lk) TRY(cuda_ok(cudaStreamWaitEvent(main_s(lk), c_->ev_hdone[m], 0), "stream wait"));
+          dy = hdy(m);
         } else {
           TRY(cross_wait(k, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
           dy = bgrad(k + 1, p);
-          dy_buf = BUF_EXT;
         }
+        int cur_buf = dy_buf;
         const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
         for (int j = n - 1; j >= 0; --j) {
           const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
@@ -218,12 +222,12 @@ class Executor {
             dx = dx0(m);  // the embedding's input gradient, scattered once at the end
             dx_buf = BUF_EXT;
           } else {
-            dx_buf = dy_buf == 0 ? 1 : 0;
+            dx_buf = cur_buf == 0 ? 1 : 0;
             dx = lbuf(lk, dx_buf);
           }
-          TRY(layer_backward(first + j, x, slot(k, m, j), dy, dy_buf, dx, dx_buf));
+          TRY(layer_backward(first + j, x, slot(k, m, j), dy, cur_buf, dx, dx_buf));
           dy = dx;
-          dy_buf = dx_buf;
+          cur_buf = dx_buf;
         }
         if (k > 0) TRY(cross_record(k, c_->ev_bdone[k][p], bdone_rec_[k][p]));
         if (k < K - 1) {  // this cell has finished reading the ring slot of cell k+1
@@ -233,7 +237,7 @@ class Executor {
       }
     }
     // every lane (and its side stream) back into the origin stream
-    for (int i = 0; i < w.nlanes; ++i) {
+    for (int i = 0; i < c_->nstreams(); ++i) {
       TRY(join_all(i));
       TRY(cuda_ok(cudaEventRecord(c_->ev_lane_end[i], c_->lane_main[i]), "event record"));
       TRY(cuda_ok(cudaStreamWaitEvent(origin_, c_->ev_lane_end[i], 0), "stream wait"));
@@ -263,6 +267,8 @@ class Executor {
   bool bfree_rec_[64][2] = {};
 
   int lane_of(int k) const { return c_->ws.nlanes > 1 ? k : 0; }
+  int head_lane() const { return c_->ws.nlanes > 1 ? c_->K : 0; }
+  char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
   cudaStream_t side(int lane) const { return c_->concurrent ? c_->lane_side[lane] : c_->lane_main[lane]; }
   cudaStream_t st() const { return cur_ ? cur_ : c_->lane_main[cur_lane_]; }
@@ -380,7 +386,7 @@ class Executor {
     g.C2 = C2;
     g.aux = aux;
     g.ldaux = ldaux;
-    g.sm_budget = num_sms() / c_->ws.nlanes;  // lanes share the machine
+    g.sm_budget = num_sms() / c_->nstreams();  // lanes share the machine
     return launch_gemm(g, st());
   }
 
@@ -506,40 +512,42 @@ class Executor {
                                 grad(o.ln1_b), scratch, st());
   }
 
-  // Loss of micro-batch m from the last cell's output stash[K][m]; with
-  // backward, also writes the gradient of that output into dy (lane buffer 0).
-  int head(int m, bool backward, char* dy) {
+  // The head of micro-batch m, once: loss rows from the last cell's output
+  // stash[K][m] and the gradient of that output into hdy[m] (final LN, tied
+  // logits, cross-entropy and their backward; MSE for the FFN model).
+  int head(int m) {
     const Dims& dm = c_->dm;
     const Workspace& w = c_->ws;
-    cur_lane_ = lane_of(c_->K - 1);
+    cur_lane_ = head_lane();
     const int T = static_cast<int>(c_->Tmb()), d = dm.d;
     float* loss_rows = reinterpret_cast<float*>(ws(w.loss_rows)) + static_cast<size_t>(m) * T;
     const char* xf = stash(c_->K, m);
+    char* dy = hdy(m);
     if (dm.kind == 0) {
       const float inv = 1.0f / (static_cast<float>(dm.n) * d);
       const float* t = static_cast<const float*>(p_.targets) + static_cast<size_t>(m) * T * d;
-      float* dyp = backward ? reinterpret_cast<float*>(dy) : reinterpret_cast<float*>(lbuf(cur_lane_, 1));
-      return launch_mse(T, d, reinterpret_cast<const float*>(xf), t, inv, loss_rows, dyp, st());
+      return launch_mse(T, d, reinterpret_cast<const float*>(xf), t, inv, loss_rows, reinterpret_cast<float*>(dy),
+                        st());
     }
+    TRY(join(cur_lane_, EV_HEAD));  // the previous micro-batch's dE GEMM has read the logits and hf
     const float inv = 1.0f / (static_cast<float>(dm.n) * (dm.seq - 1));
     float* logits = reinterpret_cast<float*>(ws(w.logits));
     TRY(launch_layernorm_fwd(DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(w.hf),
                              reinterpret_cast<float*>(ws(w.meanf)), reinterpret_cast<float*>(ws(w.rstdf)), st()));
     TRY(gemm(T, dm.vocab, d, ws(w.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
     TRY(launch_cross_entropy(T, dm.vocab, dm.seq, static_cast<const int32_t*>(p_.batch), m * T, inv, logits,
-                             loss_rows, backward ? 1 : 0, st()));
-    if (!backward) return GPIPE_OK;
+                             loss_rows, 1, st()));
     // dz (bf16, in place over the logits, leading dimension 2*vocab)
     const int64_t ldz = 2 * static_cast<int64_t>(dm.vocab);
-    char* gt = lane_base(cur_lane_) + w.lane.gt;
+    char* gt = ws(w.hgt);
     TRY(gemm(T, d, dm.vocab, logits, ldz, true, wgt(c_->pl.emb), d, false, EPI_STORE, gt, d));
     TRY(on_side(EV_HEAD, [&] {
       return gemm(dm.vocab, d, T, logits, ldz, false, ws(w.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d);
     }));
     return launch_layernorm_bwd(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(w.meanf)),
                                 reinterpret_cast<float*>(ws(w.rstdf)), p32(c_->pl.lnf_g), nullptr, dy,
-                                grad(c_->pl.lnf_g), grad(c_->pl.lnf_b),
-                                reinterpret_cast<float*>(lane_base(cur_lane_) + w.lane.scratch), st());
+                                grad(c_->pl.lnf_g), grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(w.hscratch)),
+                                st());
   }
 };
 
@@ -823,6 +831,8 @@ void gpipe_destroy(gpipe_ctx* c) {
       if (e) cudaEventDestroy(e);
   }
   if (c->ev_origin) cudaEventDestroy(c->ev_origin);
+  for (cudaEvent_t e : c->ev_hdone)
+    if (e) cudaEventDestroy(e);
   delete c;
 }
 

@@ -202,11 +202,14 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.lanes = take(static_cast<size_t>(w.nlanes) * ln.bytes);
   w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
   w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
+  w.hdy = take(static_cast<size_t>(M) * w.stash_bytes);
   if (dm.kind == 1) {
     w.hf = take(Tmb * d * es);
     w.meanf = take(Tmb * 4);
     w.rstdf = take(Tmb * 4);
     w.logits = take(Tmb * static_cast<size_t>(dm.vocab) * 4);
+    w.hgt = take(Tmb * d * es);
+    w.hscratch = take(w.scratch_bytes);
   }
   w.loss_rows = take(T * 4);
   w.act_bytes = off;
@@ -222,9 +225,10 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   // per lane one cell of Lc layers of kept internals for one micro-batch plus
   // that lane's gradient buffers (proportional to (L/K)(N/M)); the head's
   // logits and the per-row losses.
-  const size_t boundary = static_cast<size_t>(K + 2) * T * d * es + static_cast<size_t>(K) * 2 * Tmb * d * es;
+  const size_t boundary = static_cast<size_t>(K + 3) * T * d * es + static_cast<size_t>(K) * 2 * Tmb * d * es;
   const size_t per_lane = ln.bytes + 4096;
-  const size_t head = dm.kind == 1 ? Tmb * (d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + 4096 : 0;
+  const size_t head =
+      dm.kind == 1 ? Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + w.scratch_bytes + 8192 : 0;
   const size_t cell_all = remat ? 0 : static_cast<size_t>(L) * M * w.slot_bytes;
   w.bound_bytes = boundary + static_cast<size_t>(w.nlanes) * per_lane + cell_all + head + T * 4 + 8192;
   return w;

@@ -64,6 +64,8 @@ struct Workspace {
   SlotLayout slot{};
   size_t noremat_slots = 0, nslots_noremat = 0;  // L x M slots when re-materialisation is off
   size_t hf = 0, meanf = 0, rstdf = 0, logits = 0;  // head (kind 1)
+  size_t hgt = 0, hscratch = 0;             // head's gradient temporary and reduction scratch
+  size_t hdy = 0;                           // M x [Tmb, d]: gradient of the last cell's output per micro-batch
   size_t scratch_bytes = 0;
   size_t loss_rows = 0, misc = 0;            // misc: loss (float) at +0, remat counter (u64) at +8
   size_t check = 0, check_bytes = 0;         // re-materialisation check copies (debug)
