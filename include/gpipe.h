@@ -168,11 +168,14 @@ enum {
                                 cell k+1 works on m-1, as the review's K accelerators
                                 do; 0: one lane, cells in turn (least memory).  Results
                                 are identical.  Set before gpipe_sizes. */
-  GPIPE_OPT_PDL = 8          /* [0] 1: launch each kernel with programmatic dependent
+  GPIPE_OPT_PDL = 8,         /* [0] 1: launch each kernel with programmatic dependent
                                 launch (it waits for its predecessor on the GPU before
                                 reading memory, so only the launch overlaps).  Off by
                                 default: with concurrent lanes the early-launched
                                 kernels hold SM resources other lanes need.          */
+  GPIPE_OPT_TRACE = 9        /* [0] 1: write the GPU clock (ns) when every cell (and
+                                the head) finishes each micro-batch's forward and
+                                backward; read with gpipe_trace                      */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 
@@ -188,6 +191,13 @@ int gpipe_debug_counters(gpipe_ctx* ctx, void* workspace, void* stream,
  * sequence n, 0 for t = seq-1), already divided by N(seq-1); kind 0: rows [N]
  * (sum over the row of (y-t)^2 / (N d)).  host_out holds `count` floats. */
 int gpipe_loss_rows(gpipe_ctx* ctx, void* workspace, void* stream, float* host_out, size_t count);
+
+/* Timestamps of the last step taken with GPIPE_OPT_TRACE (synchronises
+ * `stream`): host_out[0] = step start, [1] = step end, then for c = 0..K (c = K is
+ * the head) and m = 0..M-1: [2 + (c*M + m)*2] = end of c's forward of m (the head:
+ * end of its loss and gradient for m), [2 + (c*M + m)*2 + 1] = end of cell c's
+ * backward of m.  Nanoseconds of the GPU clock; count <= 2 + 2(K+1)M. */
+int gpipe_trace(gpipe_ctx* ctx, void* workspace, void* stream, uint64_t* host_out, size_t count);
 
 /* Number of kernels one step launches. */
 int64_t gpipe_launches_per_step(const gpipe_ctx* ctx);

@@ -22,6 +22,7 @@ ERR = {-1: "INVALID_ARG", -2: "NOT_PARTITIONED", -3: "CUDA", -4: "DEVICE_TIMEOUT
 
 OPT_KEEP_GRADS, OPT_GRAPH, OPT_NO_REMAT, OPT_REMAT_CHECK, OPT_SKIP_UPDATE, OPT_CONCURRENT, OPT_PIPELINE, OPT_PDL = \
     1, 2, 3, 4, 5, 6, 7, 8
+OPT_TRACE = 9
 EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
 
 
@@ -55,6 +56,7 @@ _SIGS = {
     "gpipe_debug_counters": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_uint64), POINTER(c_int)]),
     "gpipe_loss_rows": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float), c_size_t]),
     "gpipe_launches_per_step": (c_int64, [c_void_p]),
+    "gpipe_trace": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_uint64), c_size_t]),
     "gpipe_last_error": (ctypes.c_char_p, [c_void_p]),
     "gpipe_destroy": (None, [c_void_p]),
     "gpipe_op_gemm": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_int64, c_int, c_void_p, c_int64, c_int, c_int,
@@ -203,6 +205,15 @@ class GPipe:
         out = (c_float * count)()
         _check(lib().gpipe_loss_rows(self.h, _ptr(workspace), stream, out, count), self.h)
         return np.frombuffer(out, dtype=np.float32).copy()
+
+    def trace(self, workspace, stream=None):
+        """(start, end, fwd[c][m], bwd[c][m]) in ns; c = 0..K (K: the head)."""
+        n = 2 + 2 * (self.K + 1) * self.M
+        out = (c_uint64 * n)()
+        _check(lib().gpipe_trace(self.h, _ptr(workspace), stream, out, n), self.h)
+        a = np.frombuffer(out, dtype=np.uint64).astype(np.int64)
+        per = a[2:].reshape(self.K + 1, self.M, 2)
+        return int(a[0]), int(a[1]), per[:, :, 0], per[:, :, 1]
 
     def launches_per_step(self):
         return lib().gpipe_launches_per_step(self.h)

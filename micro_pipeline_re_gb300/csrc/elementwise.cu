@@ -464,6 +464,13 @@ __global__ void __launch_bounds__(1024) sum_kernel(const float* __restrict__ x, 
   if (threadIdx.x == 0) *out = static_cast<float>(sm[0]);
 }
 
+// One thread writes the GPU's nanosecond clock (tracing of the step's phases).
+__global__ void stamp_kernel(unsigned long long* out) {
+  griddep_wait();
+  griddep_launch();
+  *out = globaltimer_ns();
+}
+
 __global__ void copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, size_t n16) {
   griddep_wait();
   griddep_launch();
@@ -611,6 +618,11 @@ int launch_cast_bf16(size_t n, const float* src, void* dst, cudaStream_t s) {
 int launch_sum(const float* x, size_t n, float* out, cudaStream_t s) {
   (void)launch_k(sum_kernel, 1, 1024, 0, s, x, n, out);
   return check_launch("sum");
+}
+
+int launch_stamp(unsigned long long* out, cudaStream_t s) {
+  (void)launch_k(stamp_kernel, 1, 1, 0, s, out);
+  return check_launch("stamp");
 }
 
 int launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {

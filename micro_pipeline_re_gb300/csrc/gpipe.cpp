@@ -68,6 +68,7 @@ struct gpipe_ctx {
   bool concurrent = true;  // weight gradients and the loss-only head on each lane's side stream
   bool pipelined = true;   // cells run as concurrent lanes (the review's pipeline on one GPU)
   bool pdl = false;        // kernels may launch while their predecessor drains (measured slower with lanes)
+  bool trace = false;      // stamp the GPU clock at the end of every (cell, micro-batch, phase)
   static constexpr int kMaxLanes = 64;
   static constexpr int kLaneEvents = 9;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
@@ -169,6 +170,7 @@ class Executor {
     // zero the loss scalar and the debug counter, then start every lane
     if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, origin_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
+    if (c_->trace) TRY(launch_stamp(stamp(0), origin_));
     TRY(cuda_ok(cudaEventRecord(c_->ev_origin, origin_), "event record"));
     for (int i = 0; i < c_->nstreams(); ++i)
       TRY(cuda_ok(cudaStreamWaitEvent(c_->lane_main[i], c_->ev_origin, 0), "stream wait"));
@@ -182,11 +184,13 @@ class Executor {
       for (int k = 0; k < K; ++k) {
         if (k > 0) TRY(cross_wait(k, c_->ev_fwd[k - 1], fwd_rec_[k - 1], k - 1));
         TRY(cell_forward(k, m, /*recompute=*/false));
+        if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2), st()));
         TRY(cross_record(k, c_->ev_fwd[k], fwd_rec_[k]));
       }
       if (hl != lane_of(K - 1))
         TRY(cuda_ok(cudaStreamWaitEvent(main_s(hl), c_->ev_fwd[K - 1], 0), "stream wait"));
       TRY(head(m));
+      if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(K) * M + m) * 2), st()));
       if (hl != lane_of(K - 1)) TRY(cuda_ok(cudaEventRecord(c_->ev_hdone[m], main_s(hl)), "event record"));
     }
     // phase 2: backward with re-computation
@@ -229,6 +233,7 @@ class Executor {
           dy = dx;
           cur_buf = dx_buf;
         }
+        if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2 + 1), st()));
         if (k > 0) TRY(cross_record(k, c_->ev_bdone[k][p], bdone_rec_[k][p]));
         if (k < K - 1) {  // this cell has finished reading the ring slot of cell k+1
           TRY(join(lk, EV_DYB));
@@ -252,6 +257,7 @@ class Executor {
                          c_->dm.decay, c_->dm.eps, c_->keep_grads ? 0 : 1, origin_));
     TRY(launch_sum(reinterpret_cast<float*>(ws(w.loss_rows)), c_->T(), reinterpret_cast<float*>(ws(w.misc)),
                    origin_));
+    if (c_->trace) TRY(launch_stamp(stamp(1), origin_));
     return GPIPE_OK;
   }
 
@@ -316,6 +322,9 @@ class Executor {
   }
 
   char* ws(size_t off) const { return p_.ws + off; }
+  unsigned long long* stamp(size_t i) const {
+    return reinterpret_cast<unsigned long long*>(ws(c_->ws.trace)) + i;
+  }
   const float* p32(size_t off) const { return p_.p32 + off; }
   float* grad(size_t off) const { return p_.g32 + off; }
   // GEMM operand weights: the bf16 compute copy, or the fp32 master for dtype 0
@@ -685,6 +694,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[4] = c->concurrent;
     key.opts[5] = c->pipelined;
     key.opts[6] = c->pdl;
+    key.opts[7] = c->trace;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -777,6 +787,7 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_CONCURRENT: c->concurrent = value != 0; break;
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
+    case GPIPE_OPT_TRACE: c->trace = value != 0; break;
     default: return c->fail(GPIPE_ERR_INVALID_ARG, "unknown option");
   }
   c->drop_graph();
@@ -804,6 +815,18 @@ int gpipe_loss_rows(gpipe_ctx* c, void* workspace, void* stream, float* host_out
   if (count > c->T()) return c->fail(GPIPE_ERR_INVALID_ARG, "count exceeds the number of loss rows");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t ce = cudaMemcpyAsync(host_out, static_cast<char*>(workspace) + c->ws.loss_rows, count * 4,
+                                   cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, cudaGetErrorString(ce));
+  return GPIPE_OK;
+}
+
+int gpipe_trace(gpipe_ctx* c, void* workspace, void* stream, uint64_t* host_out, size_t count) {
+  if (!c || !workspace || !host_out) return GPIPE_ERR_INVALID_ARG;
+  c->refresh_ws();
+  if (count > c->ws.trace_count) return c->fail(GPIPE_ERR_INVALID_ARG, "count exceeds the trace length");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaMemcpyAsync(host_out, static_cast<char*>(workspace) + c->ws.trace, count * 8,
                                    cudaMemcpyDeviceToHost, s);
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
   if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, cudaGetErrorString(ce));

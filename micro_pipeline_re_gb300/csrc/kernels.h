@@ -91,6 +91,8 @@ int launch_cast_bf16(size_t n, const float* src, void* dst, cudaStream_t stream)
 
 // Deterministic sum of n floats into *out (one block, fixed order, fp64 partials).
 int launch_sum(const float* x, size_t n, float* out, cudaStream_t stream);
+// *out = the GPU's nanosecond clock (one thread), for tracing.
+int launch_stamp(unsigned long long* out, cudaStream_t stream);
 // Copy n bytes (device to device) with a kernel.
 int launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 // counter[0] += number of bytes that differ between a and b.

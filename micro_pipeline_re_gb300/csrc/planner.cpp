@@ -214,6 +214,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.loss_rows = take(T * 4);
   w.act_bytes = off;
   w.misc = take(256);
+  w.trace_count = 2 + static_cast<size_t>(K + 1) * M * 2;
+  w.trace = take(w.trace_count * 8);
   if (remat && remat_check) {
     w.check_bytes = static_cast<size_t>(K) * max_cell_layers * w.slot_bytes;
     w.check = take(w.check_bytes);

@@ -68,6 +68,7 @@ struct Workspace {
   size_t hdy = 0;                           // M x [Tmb, d]: gradient of the last cell's output per micro-batch
   size_t scratch_bytes = 0;
   size_t loss_rows = 0, misc = 0;            // misc: loss (float) at +0, remat counter (u64) at +8
+  size_t trace = 0, trace_count = 0;         // phase timestamps (u64): start, end, then per (cell/head, m, phase)
   size_t check = 0, check_bytes = 0;         // re-materialisation check copies (debug)
   size_t act_bytes = 0;                      // activation bytes (everything but misc/check)
   size_t total = 0;

@@ -222,3 +222,23 @@ def test_loss_near_log_vocab_and_update_from_zero_state(b):
     expect = w.lr / math.sqrt(1 - w.decay)
     assert np.allclose(np.abs(dw[big]), expect, rtol=2e-3)
     assert np.all(np.sign(dw[big]) == -np.sign(g[big]))
+
+
+def test_trace_follows_the_pipeline_dependencies(b):
+    """With cells as concurrent lanes, GPU timestamps obey the review's pipeline:
+    cell k finishes forwarding micro-batch m after cell k-1, the head after the
+    last cell, the last cell's backward after the head, cell k-1's backward
+    after cell k's, and every lane takes micro-batches in order."""
+    w = WORKLOADS["lm_small"]
+    gp, st, _, _ = _run(b, w, make_inputs(w), options=[(b.OPT_TRACE, 1)])
+    t0, t1, fwd, bwd = gp.trace(st.ws, st.stream)
+    K, M = w.K, w.M
+    assert t0 <= fwd.min() and max(fwd.max(), bwd[:K].max()) <= t1
+    for m in range(M):
+        for k in range(1, K + 1):
+            assert fwd[k, m] >= fwd[k - 1, m]
+        assert bwd[K - 1, m] >= fwd[K, m]
+        for k in range(K - 1, 0, -1):
+            assert bwd[k - 1, m] >= bwd[k, m]
+    assert np.all(np.diff(fwd, axis=1) >= 0)
+    assert np.all(np.diff(bwd[:K], axis=1) >= 0)
