@@ -374,7 +374,7 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   args.n_tiles = (g.N + BN - 1) / BN;
   const int tiles = args.m_tiles * args.n_tiles;
   const int grid = ctas < tiles ? ctas : tiles;
-  (void)launch_k(tc_gemm_persistent<A_K, B_K, BN, EPI>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
+  (void)launch_k<true>(tc_gemm_persistent<A_K, B_K, BN, EPI>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
                                                                                device_error_ptr());
   count_launch();
   cudaError_t e = cudaGetLastError();

@@ -450,13 +450,13 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = S;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    attr[1].val.programmaticStreamSerializationAllowed = 0;  // heavy: never launched early
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>, ta, tb, tc, tc2, tx, args,
                            device_error_ptr());
   } else {
-    (void)launch_k(tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>, grid, THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, tx, args,
+    (void)launch_k<true>(tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>, grid, THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, tx, args,
                                                                                   device_error_ptr());
     e = cudaGetLastError();
   }

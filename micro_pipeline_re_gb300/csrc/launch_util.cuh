@@ -22,7 +22,10 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 bool pdl_enabled();
 void set_pdl_enabled(bool on);
 
-template <typename... KArgs, typename... Args>
+// heavy = true: the kernel holds most of an SM's shared memory / tensor
+// memory; it is never launched early, so a waiting copy cannot keep those from
+// kernels of other streams.
+template <bool heavy = false, typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -31,7 +34,7 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = (!heavy && pdl_enabled()) ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
