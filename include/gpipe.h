@@ -16,7 +16,10 @@
  *   - Bubble ("Bubble overhead analysis"): (K-1)/(M+K-1).
  *   - Memory ("Preliminaries 5: re-materialisation"): peak activation memory
  *     O(N + (L/K)(N/M)) instead of O(N L).
- * Here all K cells run on one GPU, in the schedule's order, on one stream.
+ * Here all K cells run on one GPU: each cell is a lane of concurrent CUDA
+ * streams ordered by events with exactly the pipeline's dependencies (cell k
+ * works on micro-batch m while cell k+1 works on m-1), plus a lane for the
+ * head; or, with GPIPE_OPT_PIPELINE = 0, the cells take turns on one lane.
  *
  * Conventions for every function:
  *   - Return value: 0 (GPIPE_OK) or a negative GPIPE_ERR_* code; the message of
@@ -122,7 +125,9 @@ int gpipe_init_params(gpipe_ctx* ctx, const float* params_fp32, void* params_bf1
  *   loss_out    host float* or NULL.  When non-NULL the stream is synchronised,
  *               the device error flag is checked and the mean loss is written.
  * The step is captured into a CUDA graph on first use (per pointer set) and
- * replayed afterwards unless GPIPE_OPT_GRAPH is 0. */
+ * replayed afterwards unless GPIPE_OPT_GRAPH is 0.  The library creates its own
+ * streams and events (host-side objects) on the first call; the caller's
+ * stream waits for all of them before the call's work is complete. */
 int gpipe_step(gpipe_ctx* ctx, float* params_fp32, void* params_bf16, float* grads_fp32,
                float* rms_v_fp32, const void* batch_in, const void* targets,
                void* workspace, void* stream, float* loss_out);

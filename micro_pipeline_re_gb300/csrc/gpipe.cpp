@@ -1,20 +1,31 @@
 // Step executor and the gpipe_* C ABI.
 //
 // One synchronous GPipe step ("GPipe technical review", zzz0906.github.io,
-// "Pipeline flow", phases 1-3) with all K cells on one GPU and one stream:
+// "Pipeline flow", phases 1-3) with all K cells on one GPU:
 //   phase 1  for m in 0..M-1, for k in 0..K-1: cell k forwards micro-batch m
 //            from the stashed cell input stash[k][m] and writes its output to
-//            stash[k+1][m]; internals go to the shared cell slots and are
-//            overwritten by the next cell (re-materialisation keeps only the
-//            boundary activations).  The last cell also computes the loss.
+//            stash[k+1][m]; the cell's internals go to its lane's slots and
+//            are overwritten by the next micro-batch (re-materialisation keeps
+//            only the boundary activations).  Then the head (final LN, tied
+//            logits, cross-entropy; MSE for the FFN model) computes micro-batch
+//            m's loss and the gradient of the last cell's output, once.
 //   phase 2  for m in 0..M-1, for k in K-1..0: re-compute cell k's forward
-//            from stash[k][m] into the slots (the output of its last layer is
-//            not needed and is skipped), then differentiate it layer by layer
-//            in reverse; weight gradients are added into the fp32 gradient
-//            buffer straight from the GEMM epilogue (accumulation across
-//            micro-batches, no update in between).
-//   phase 3  one RMSProp update of every parameter (and the bf16 copy).
-// The whole sequence is captured once into a CUDA graph and replayed.
+//            from stash[k][m] (its last layer's output projection is skipped:
+//            that output is already stashed and not needed to differentiate
+//            the cell), then differentiate it layer by layer in reverse; weight
+//            gradients are added into the fp32 gradient buffer straight from
+//            the GEMM epilogue (accumulation across micro-batches, no update in
+//            between).
+//   phase 3  the tied embedding's scatter-add for all tokens, then one RMSProp
+//            update of every parameter (and the bf16 copy).
+// The review's K accelerators become K concurrent lanes (a main and a side
+// stream each, plus one lane for the head): cell k works on micro-batch m while
+// cell k+1 works on m-1, with events carrying exactly the pipeline's
+// dependencies; weight-gradient GEMMs run on each lane's side stream.  Each
+// cell's gradient accumulation stays in micro-batch order on one stream, so the
+// result is bit-identical to running the cells in turn on one stream
+// (GPIPE_OPT_PIPELINE / GPIPE_OPT_CONCURRENT = 0).  The whole step is captured
+// once into a CUDA graph and replayed.
 #include <cuda_runtime.h>
 
 #include <algorithm>
