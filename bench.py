@@ -309,6 +309,49 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """The micro-batch sweep workload over its (K, M) grid: step throughput,
+    peak activation bytes (the workspace's activation high-water mark, which
+    is what is allocated) against the review's bound, and the modelled bubble
+    (K-1)/(M+K-1).  One JSON line per (K, M); not the throughput line."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    from micro_pipeline_re_gb300 import binding as b
+    from synth import SWEEP_GRID, WORKLOADS, make_inputs
+    peaks = load_peaks()
+    w0 = WORKLOADS[args.workload if args.workload != "lm_small" else "lm_sweep"]
+    inp = make_inputs(w0)
+    for K, M in SWEEP_GRID:
+        w = w0.replace(K=K, M=M)
+        gp = b.GPipe.from_workload(w)
+        free0 = torch.cuda.mem_get_info()[0]
+        st = b.DeviceState(gp, w, inp)
+        free1 = torch.cuda.mem_get_info()[0]
+        for _ in range(max(args.warmup, 2)):
+            st.step(want_loss=False)
+        loss = st.step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            st.step(want_loss=False)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / args.steps
+        peak, bound = gp.memory_report()
+        P, wsb = gp.sizes()
+        print(json.dumps({"sweep": w.name, "K": K, "M": M, "ms_per_step": t * 1e3, "tokens_per_s": w.tokens / t,
+                          "mfu": model_flops(w) / t / (peaks["bf16_sus"] * 1e12), "loss": loss,
+                          "bubble_model": gp.bubble_fraction(), "peak_activation_bytes": peak,
+                          "activation_bound_bytes": bound, "workspace_bytes": wsb,
+                          "device_bytes_taken_by_state": free0 - free1}), flush=True)
+        del st
+        gp.close()
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -321,6 +364,8 @@ def main():
                     help="only run the roofline GEMM (5 eager launches, then a timed graph); for profilers")
     ap.add_argument("--shape", default=None, help="M,N,K for --probe-gemm (default: the workload's FFN1)")
     ap.add_argument("--reps", type=int, default=100)
+    ap.add_argument("--sweep", action="store_true",
+                    help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
     args = ap.parse_args()
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
@@ -331,6 +376,9 @@ def main():
         from micro_pipeline_re_gb300 import binding as b
         shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
         print(json.dumps(gemm_roofline(b, w, load_peaks(), reps=args.reps, shape=shape)), flush=True)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if args.impl == "reference":
         run_reference(args, w)
