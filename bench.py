@@ -224,9 +224,9 @@ def run_ours(args, w):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    import __graft_entry__ as ge
+    from micro_pipeline_re_gb300._build import build as _build
     if rank == 0 or world == 1:
-        ge.build()
+        _build()
     if dist:
         dist.barrier()
     from micro_pipeline_re_gb300 import binding as b
@@ -315,8 +315,8 @@ def run_sweep(args):
     is what is allocated) against the review's bound, and the modelled bubble
     (K-1)/(M+K-1).  One JSON line per (K, M); not the throughput line."""
     import torch
-    import __graft_entry__ as ge
-    ge.build()
+    from micro_pipeline_re_gb300._build import build as _build
+    _build()
     from micro_pipeline_re_gb300 import binding as b
     from synth import SWEEP_GRID, WORKLOADS, make_inputs
     peaks = load_peaks()
@@ -371,8 +371,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.probe_gemm:
         import torch
-        import __graft_entry__ as ge
-        ge.build()
+        from micro_pipeline_re_gb300._build import build as _build
+        _build()
         from micro_pipeline_re_gb300 import binding as b
         shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
         print(json.dumps(gemm_roofline(b, w, load_peaks(), reps=args.reps, shape=shape)), flush=True)
