@@ -178,9 +178,14 @@ enum {
                                 reading memory, so only the launch overlaps).  Off by
                                 default: with concurrent lanes the early-launched
                                 kernels hold SM resources other lanes need.          */
-  GPIPE_OPT_TRACE = 9        /* [0] 1: write the GPU clock (ns) when every cell (and
+  GPIPE_OPT_TRACE = 9,       /* [0] 1: write the GPU clock (ns) when every cell (and
                                 the head) finishes each micro-batch's forward and
                                 backward; read with gpipe_trace                      */
+  GPIPE_OPT_KERNEL_TIMES = 10 /* [0] e+1: bracket every GEMM launch of the step whose
+                                epilogue is e (GPIPE_EPI_* of gpipe_ops.h) with timing
+                                events on the stream it is launched on (recorded as
+                                event nodes of the step's graph); read with
+                                gpipe_kernel_times                                   */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 
@@ -203,6 +208,13 @@ int gpipe_loss_rows(gpipe_ctx* ctx, void* workspace, void* stream, float* host_o
  * end of its loss and gradient for m), [2 + (c*M + m)*2 + 1] = end of cell c's
  * backward of m.  Nanoseconds of the GPU clock; count <= 2 + 2(K+1)M. */
 int gpipe_trace(gpipe_ctx* ctx, void* workspace, void* stream, uint64_t* host_out, size_t count);
+
+/* Durations of the GEMM launches that GPIPE_OPT_KERNEL_TIMES selected, in the
+ * last step taken (waits for that step's events): ms_out[i] = event time of
+ * launch i in issue order, flops_out[i] = its algorithmic work 2*M*N*K.  Writes
+ * min(count, n) entries (either array may be NULL) and returns n, the number of
+ * timed launches per step (0 when the option is off), or a negative error. */
+int gpipe_kernel_times(gpipe_ctx* ctx, float* ms_out, double* flops_out, int count);
 
 /* Number of kernels one step launches. */
 int64_t gpipe_launches_per_step(const gpipe_ctx* ctx);

@@ -23,6 +23,7 @@ ERR = {-1: "INVALID_ARG", -2: "NOT_PARTITIONED", -3: "CUDA", -4: "DEVICE_TIMEOUT
 OPT_KEEP_GRADS, OPT_GRAPH, OPT_NO_REMAT, OPT_REMAT_CHECK, OPT_SKIP_UPDATE, OPT_CONCURRENT, OPT_PIPELINE, OPT_PDL = \
     1, 2, 3, 4, 5, 6, 7, 8
 OPT_TRACE = 9
+OPT_KERNEL_TIMES = 10
 EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
 
 
@@ -57,6 +58,7 @@ _SIGS = {
     "gpipe_loss_rows": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float), c_size_t]),
     "gpipe_launches_per_step": (c_int64, [c_void_p]),
     "gpipe_trace": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_uint64), c_size_t]),
+    "gpipe_kernel_times": (c_int, [c_void_p, POINTER(ctypes.c_float), POINTER(ctypes.c_double), c_int]),
     "gpipe_last_error": (ctypes.c_char_p, [c_void_p]),
     "gpipe_destroy": (None, [c_void_p]),
     "gpipe_op_gemm": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_int64, c_int, c_void_p, c_int64, c_int, c_int,
@@ -205,6 +207,19 @@ class GPipe:
         out = (c_float * count)()
         _check(lib().gpipe_loss_rows(self.h, _ptr(workspace), stream, out, count), self.h)
         return np.frombuffer(out, dtype=np.float32).copy()
+
+    def kernel_times(self):
+        """(ms, flops) arrays of the GEMM launches selected by OPT_KERNEL_TIMES in
+        the last step (waits for its events)."""
+        n = lib().gpipe_kernel_times(self.h, None, None, 0)
+        if n < 0:
+            _check(n, self.h)
+        ms = (ctypes.c_float * max(n, 1))()
+        fl = (ctypes.c_double * max(n, 1))()
+        r = lib().gpipe_kernel_times(self.h, ms, fl, n)
+        if r < 0:
+            _check(r, self.h)
+        return np.frombuffer(ms, dtype=np.float32)[:n].copy(), np.frombuffer(fl, dtype=np.float64)[:n].copy()
 
     def trace(self, workspace, stream=None):
         """(start, end, fwd[c][m], bwd[c][m]) in ns; c = 0..K (K: the head)."""

@@ -1,8 +1,10 @@
 // Persistent bf16 GEMM on tcgen05 for GEMMs with more output tiles than SMs.
 //
-// One CTA per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... (m
-// fastest, so CTAs working at the same time share the B tile and the small A
-// stays in L2).  Each tile is computed by exactly one CTA: deterministic.
+// One CTA per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+// Tiles are numbered in groups of PGROUP row tiles (m fastest within a group,
+// then n), so the tiles in flight at one time read a band of A and a band of B
+// that stay in L2 together.  Each tile is computed by exactly one CTA:
+// deterministic.
 //   warp 0 / lane 0   TMA producer over all (tile, k-block) pairs, through a
 //                     ring of STAGES operand stages
 //   warp 1            allocates TMEM; lane 0 issues tcgen05.mma into one of two
@@ -13,6 +15,8 @@
 //                     128B-swizzled staging box; one thread TMA-stores each
 //                     box (staging is double-buffered, so the store of step s
 //                     overlaps step s+1), or TMA-reduce-adds the fp32 gradient
+//                     (the bias gradient, sum over k of A, is summed by the same
+//                     warps from global memory while the tile's MMAs run)
 // Bounded waits as in the single-tile kernel.
 #include <cuda.h>
 
@@ -40,23 +44,25 @@ struct PCfg {
   // per 64-column step: bf16 -> one box (two for bias+GELU: z and GELU(z)); fp32 -> two boxes
   static constexpr int STEP_BOXES = F32_OUT ? 2 : (EPI == EPI_BIAS_GELU ? 2 : 1);
   static constexpr int STAGING = 2 * STEP_BOXES * PBOX;  // double-buffered
-  static constexpr int ONES_BYTES = EPI == EPI_ACC_F32 ? 2048 : 0;
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - STAGING - ONES_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - STAGING) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
-  static constexpr int OFF_ONES = OFF_STG + STAGING;
-  static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
+  static constexpr int OFF_BAR = OFF_STG + STAGING;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
-  // TMEM: two accumulators of BN columns (+ 2 x 16 bias-gradient columns)
-  static constexpr int TCOLS = (2 * BN + (EPI == EPI_ACC_F32 ? 32 : 0)) <= 256 ? 256 : 512;
-  static_assert(STAGES >= 2, "not enough shared memory for two stages");
+  // TMEM: two accumulators of BN columns
+  static constexpr int TCOLS = 2 * BN <= 256 ? 256 : 512;
+  static_assert(STAGES >= 3, "not enough shared memory for three stages");
   static_assert(SMEM <= 232448, "over the 227 KB per-CTA shared memory limit");
-  static_assert(2 * BN + (EPI == EPI_ACC_F32 ? 32 : 0) <= 512, "accumulators exceed tensor memory");
+  static_assert(2 * BN <= 512, "accumulators exceed tensor memory");
 };
+
+constexpr int PGROUP = 16;  // row tiles per group of the tile order
 
 struct PArgs {
   const float* bias;   // fp32 [N] (store / bias+GELU) or NULL
   float* dbias;        // EPI_ACC_F32: fp32 [M] += sum_k A(m,k), or NULL
+  const void* a;       // A (bf16), for the bias gradient
+  int64_t lda;
   const void* xsrc;    // residual (store) or GELU pre-activation (GELU backward), bf16, or NULL
   int64_t ldx;
   int M, N, K;
@@ -70,6 +76,73 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Origin (row, column) of tile t in the grouped tile order.
+template <int BN>
+__device__ __forceinline__ void tile_origin(int t, const PArgs& a, int& m0, int& n0) {
+  const int per_group = PGROUP * a.n_tiles;
+  const int grp = t / per_group, r = t - grp * per_group;
+  const int first = grp * PGROUP;
+  const int gm = a.m_tiles - first < PGROUP ? a.m_tiles - first : PGROUP;
+  m0 = (first + r % gm) * PM;
+  n0 = (r / gm) * BN;
+}
+
+// Bias gradient of rows m0..m0+127: dbias[m] += sum_k A(m, k), by the 8
+// epilogue warps (warp w owns rows m0 + 16w .. +15) in a fixed order: each
+// lane sums a fixed residue class of k in fp32, then the lanes are folded by
+// xor-shuffles.  One thread adds each row's sum; rows >= M are skipped.
+template <bool A_K>
+__device__ void bias_grad_rows(const PArgs& a, int m0, int ew, int lane) {
+  const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(a.a);
+  const int mb = m0 + 16 * ew;
+  if (A_K) {
+    // row-major rows of K: lane = (row r = lane >> 1, half h = lane & 1); h sums chunks 2j + h of 8
+    const int m = mb + (lane >> 1), h = lane & 1;
+    float s = 0.f;
+    if (m < a.M) {
+      const __nv_bfloat16* row = A + static_cast<int64_t>(m) * a.lda;
+      const int full = a.K / 8;
+      for (int j = h; j < full; j += 2) {
+        float v[8];
+        load8(row + 8 * j, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += v[e];
+      }
+      if (h == 0)
+        for (int k = 8 * full; k < a.K; ++k) s += bf2f(row[k]);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (h == 0 && m < a.M) a.dbias[m] += s;
+  } else {
+    // rows of A are k: lane = (row class g = lane >> 1, 8-column chunk c = lane & 1)
+    const int g = lane >> 1, c = lane & 1;
+    const int mc = mb + 8 * c;
+    float s[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[e] = 0.f;
+    const bool vec = mc + 8 <= a.M;
+    for (int k = g; k < a.K; k += 16) {
+      const __nv_bfloat16* p = A + static_cast<int64_t>(k) * a.lda + mc;
+      if (vec) {
+        float v[8];
+        load8(p, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[e] += v[e];
+      } else {
+        for (int e = 0; e < 8; ++e)
+          if (mc + e < a.M) s[e] += bf2f(p[e]);
+      }
+    }
+#pragma unroll
+    for (int o = 2; o < 32; o <<= 1)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s[e] += __shfl_xor_sync(0xffffffffu, s[e], o);
+    if (g == 0)
+      for (int e = 0; e < 8; ++e)
+        if (mc + e < a.M) a.dbias[mc + e] += s[e];
+  }
 }
 
 // Bounded wait that gives up at once after any earlier give-up in the CTA.
@@ -90,7 +163,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sStg = smem + Cfg::OFF_STG;
-  uint8_t* sOnes = smem + Cfg::OFF_ONES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* accf = empty + STAGES;  // accumulator b holds a finished tile
@@ -117,10 +189,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     *abort = 0;
     fence_barrier_init();
   }
-  if (EPI == EPI_ACC_F32 && threadIdx.x < 128) {  // 16 rows x 64 bf16 of 1.0
-    reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    fence_proxy_async_smem();
-  }
   if (warp == 1) {
     tmem_alloc(tslot, Cfg::TCOLS);
     tmem_relinquish();
@@ -135,7 +203,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     if (lane == 0) {
       int it = 0;
       for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
-        const int m0 = (t % args.m_tiles) * PM, n0 = (t / args.m_tiles) * BN;
+        int m0, n0;
+        tile_origin<BN>(t, args, m0, n0);
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           if (!pwait(&empty[s], ((it / STAGES) & 1) ^ 1, err, DERR_TMA_WAIT, abort)) break;
@@ -165,14 +234,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = mma_idesc_bf16(PM, BN, !A_K, !B_K);
-      constexpr uint32_t idesc_db = mma_idesc_bf16(PM, 16, !A_K, false);
-      const uint32_t ones = smem_u32(sOnes);
       int it = 0, i = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
         const int b = i & 1;
         if (!pwait(&acce[b], ((i >> 1) & 1) ^ 1, err, DERR_MMA_WAIT, abort)) break;
         tc_fence_after();
-        const bool do_db = EPI == EPI_ACC_F32 && args.dbias != nullptr && t / args.m_tiles == 0;
         const uint32_t dacc = tmem + b * BN;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
@@ -186,7 +252,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             const uint64_t bd = B_K ? sw128_desc(bb + kk * 32, 16, 1024) : sw128_desc(bb + kk * 2048, 8192, 1024);
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
             tc_mma_f16(dacc, ad, bd, idesc, acc);
-            if (do_db) tc_mma_f16(tmem + 2 * BN + 16 * b, ad, sw128_desc(ones + kk * 32, 16, 1024), idesc_db, acc);
           }
           tc_commit(&empty[s]);
         }
@@ -203,8 +268,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     int step = 0, i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
       const int b = i & 1;
-      const int m0 = (t % args.m_tiles) * PM, n0 = (t / args.m_tiles) * BN;
+      int m0, n0;
+      tile_origin<BN>(t, args, m0, n0);
       const int m = m0 + r;
+      if (EPI == EPI_ACC_F32 && args.dbias != nullptr && n0 == 0 && !*abort)
+        bias_grad_rows<A_K>(args, m0, warp - 2, lane);  // overlaps this tile's MMAs
       pwait(&accf[b], (i >> 1) & 1, err, DERR_ACC_WAIT, abort);
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
@@ -288,12 +356,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           bulk_commit();
         }
       }
-      if (EPI == EPI_ACC_F32 && args.dbias != nullptr && n0 == 0 && h == 0) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * BN + 16 * b, rr);
-        tmem_ld_wait();
-        if (m < args.M && !*abort) args.dbias[m] += __uint_as_float(rr[0]);
-      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[b]);  // this warp has drained accumulator b
@@ -365,6 +427,8 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   PArgs args{};
   args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU) ? g.bias : nullptr;
   args.dbias = EPI == EPI_ACC_F32 ? g.dbias : nullptr;
+  args.a = g.A;
+  args.lda = g.lda;
   args.xsrc = EPI == EPI_STORE ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : nullptr);
   args.ldx = EPI == EPI_STORE ? g.ldr : g.ldaux;
   args.M = g.M;
@@ -382,57 +446,70 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   return GPIPE_OK;
 }
 
-// Output-tile width per epilogue: 256 columns for bf16 stores (a 128 x 256
-// tile halves the A traffic per flop), 128 where the staging or the
-// bias-gradient accumulator needs the room.
-template <int EPI>
-constexpr int pbn() {
-  return (EPI == EPI_STORE || EPI == EPI_GELU_BWD) ? 256 : 128;
+// Output-tile width: 128 x 256 tiles read 96 B of operands per 128 clocks of
+// MMA against 128 B per 64 clocks for 128 x 128 tiles, so they win unless
+// the coarser tiles leave CTAs idle: take 256 when the rounds of tiles per CTA
+// times the wider tile's relative time (1.5) is below the narrow tiles' rounds.
+bool wide_tiles(const GemmDesc& g, int ctas) {
+  const int64_t mt = (g.M + PM - 1) / PM;
+  const int64_t r128 = (mt * ((g.N + 127) / 128) + ctas - 1) / ctas;
+  const int64_t r256 = (mt * ((g.N + 255) / 256) + ctas - 1) / ctas;
+  return 3 * r256 < 2 * r128;
 }
 
-}  // namespace
-
-int64_t persistent_tiles(const GemmDesc& g) {
-  int bn = 128;
-  if (g.epi == EPI_STORE || g.epi == EPI_GELU_BWD) bn = 256;
-  return static_cast<int64_t>((g.M + PM - 1) / PM) * ((g.N + bn - 1) / bn);
-}
-
-int launch_gemm_persistent(const GemmDesc& g, cudaStream_t s, int ctas) {
+template <int BN>
+int dispatch(const GemmDesc& g, cudaStream_t s, int ctas) {
   if (g.a_kmajor && g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return prun<true, true, pbn<EPI_STORE>(), EPI_STORE>(g, s, ctas);
-      case EPI_BIAS_GELU: return prun<true, true, pbn<EPI_BIAS_GELU>(), EPI_BIAS_GELU>(g, s, ctas);
-      case EPI_STORE_F32: return prun<true, true, pbn<EPI_STORE_F32>(), EPI_STORE_F32>(g, s, ctas);
-      case EPI_ACC_F32: return prun<true, true, pbn<EPI_ACC_F32>(), EPI_ACC_F32>(g, s, ctas);
+      case EPI_STORE: return prun<true, true, BN, EPI_STORE>(g, s, ctas);
+      case EPI_BIAS_GELU: return prun<true, true, BN, EPI_BIAS_GELU>(g, s, ctas);
+      case EPI_STORE_F32: return prun<true, true, BN, EPI_STORE_F32>(g, s, ctas);
+      case EPI_ACC_F32: return prun<true, true, BN, EPI_ACC_F32>(g, s, ctas);
     }
   } else if (g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return prun<true, false, pbn<EPI_STORE>(), EPI_STORE>(g, s, ctas);
-      case EPI_GELU_BWD: return prun<true, false, pbn<EPI_GELU_BWD>(), EPI_GELU_BWD>(g, s, ctas);
-      case EPI_ACC_F32: return prun<true, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>(g, s, ctas);
+      case EPI_STORE: return prun<true, false, BN, EPI_STORE>(g, s, ctas);
+      case EPI_GELU_BWD: return prun<true, false, BN, EPI_GELU_BWD>(g, s, ctas);
+      case EPI_ACC_F32: return prun<true, false, BN, EPI_ACC_F32>(g, s, ctas);
     }
   } else if (!g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return prun<false, false, pbn<EPI_STORE>(), EPI_STORE>(g, s, ctas);
-      case EPI_ACC_F32: return prun<false, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>(g, s, ctas);
+      case EPI_STORE: return prun<false, false, BN, EPI_STORE>(g, s, ctas);
+      case EPI_ACC_F32: return prun<false, false, BN, EPI_ACC_F32>(g, s, ctas);
     }
   }
   return set_error(GPIPE_ERR_UNSUPPORTED, "persistent gemm: layout/epilogue not built");
 }
 
-int prepare_gemm_persistent() {
+template <int BN>
+int prepare_bn() {
   int rc = GPIPE_OK;
-  rc = rc ? rc : pset_attr<true, true, pbn<EPI_STORE>(), EPI_STORE>();
-  rc = rc ? rc : pset_attr<true, true, pbn<EPI_BIAS_GELU>(), EPI_BIAS_GELU>();
-  rc = rc ? rc : pset_attr<true, true, pbn<EPI_STORE_F32>(), EPI_STORE_F32>();
-  rc = rc ? rc : pset_attr<true, true, pbn<EPI_ACC_F32>(), EPI_ACC_F32>();
-  rc = rc ? rc : pset_attr<true, false, pbn<EPI_STORE>(), EPI_STORE>();
-  rc = rc ? rc : pset_attr<true, false, pbn<EPI_GELU_BWD>(), EPI_GELU_BWD>();
-  rc = rc ? rc : pset_attr<true, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>();
-  rc = rc ? rc : pset_attr<false, false, pbn<EPI_STORE>(), EPI_STORE>();
-  rc = rc ? rc : pset_attr<false, false, pbn<EPI_ACC_F32>(), EPI_ACC_F32>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE_F32>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_ACC_F32>();
+  rc = rc ? rc : pset_attr<true, false, BN, EPI_STORE>();
+  rc = rc ? rc : pset_attr<true, false, BN, EPI_GELU_BWD>();
+  rc = rc ? rc : pset_attr<true, false, BN, EPI_ACC_F32>();
+  rc = rc ? rc : pset_attr<false, false, BN, EPI_STORE>();
+  rc = rc ? rc : pset_attr<false, false, BN, EPI_ACC_F32>();
   return rc;
+}
+
+}  // namespace
+
+// Output tiles at the finest persistent tiling (128 x 128).
+int64_t persistent_tiles(const GemmDesc& g) {
+  return static_cast<int64_t>((g.M + PM - 1) / PM) * ((g.N + 127) / 128);
+}
+
+int launch_gemm_persistent(const GemmDesc& g, cudaStream_t s, int ctas) {
+  return wide_tiles(g, ctas) ? dispatch<256>(g, s, ctas) : dispatch<128>(g, s, ctas);
+}
+
+int prepare_gemm_persistent() {
+  const int rc = prepare_bn<128>();
+  return rc ? rc : prepare_bn<256>();
 }
 
 }  // namespace gp

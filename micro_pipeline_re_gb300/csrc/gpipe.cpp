@@ -55,7 +55,7 @@ struct StepPtrs {
 
 struct GraphKey {
   StepPtrs p;
-  int64_t opts[8];
+  int64_t opts[9];
   bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
 };
 
@@ -80,6 +80,10 @@ struct gpipe_ctx {
   bool pipelined = true;   // cells run as concurrent lanes (the review's pipeline on one GPU)
   bool pdl = false;        // kernels may launch while their predecessor drains (measured slower with lanes)
   bool trace = false;      // stamp the GPU clock at the end of every (cell, micro-batch, phase)
+  int ktime = 0;           // e+1: time every GEMM launch with epilogue e (event pairs)
+  std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
+  std::vector<double> kt_flops;
+  int kt_n = 0;  // timed launches issued by the last issued (or captured) step
   static constexpr int kMaxLanes = 64;
   static constexpr int kLaneEvents = 9;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
@@ -133,6 +137,20 @@ struct gpipe_ctx {
            mk_ev(ev_fwd[k]);
     return ok ? GPIPE_OK : fail(GPIPE_ERR_CUDA, "cannot create the lane streams/events");
   }
+  // The event pair of the next timed launch (created on first use).
+  int kt_next(double flops, cudaEvent_t* e0, cudaEvent_t* e1) {
+    while (kt_ev.size() < static_cast<size_t>(2 * kt_n + 2)) {
+      cudaEvent_t e = nullptr;
+      if (cudaEventCreate(&e) != cudaSuccess) return fail(GPIPE_ERR_CUDA, "cannot create a timing event");
+      kt_ev.push_back(e);
+    }
+    if (kt_flops.size() <= static_cast<size_t>(kt_n)) kt_flops.resize(kt_n + 1);
+    kt_flops[kt_n] = flops;
+    *e0 = kt_ev[2 * kt_n];
+    *e1 = kt_ev[2 * kt_n + 1];
+    ++kt_n;
+    return GPIPE_OK;
+  }
   void drop_graph() {
     if (gexec) cudaGraphExecDestroy(gexec);
     if (graph) cudaGraphDestroy(graph);
@@ -178,6 +196,7 @@ class Executor {
     const Workspace& w = c_->ws;
     const int M = c_->M, K = c_->K;
     set_pdl_enabled(c_->pdl);
+    c_->kt_n = 0;
     // zero the loss scalar and the debug counter, then start every lane
     if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, origin_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
@@ -407,7 +426,22 @@ class Executor {
     g.aux = aux;
     g.ldaux = ldaux;
     g.sm_budget = num_sms() / c_->nstreams();  // lanes share the machine
-    return launch_gemm(g, st());
+    if (c_->ktime != epi + 1) return launch_gemm(g, st());
+    cudaEvent_t e0, e1;
+    TRY(c_->kt_next(2.0 * M * N * K, &e0, &e1));
+    TRY(record_timed(e0));
+    TRY(launch_gemm(g, st()));
+    return record_timed(e1);
+  }
+
+  // A timing event on the current stream; under capture it becomes an event
+  // node of the graph, so it is recorded at every replay.
+  int record_timed(cudaEvent_t e) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st(), &cs) != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "cudaStreamIsCapturing failed");
+    const cudaError_t ce = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(e, st(), cudaEventRecordExternal)
+                                                               : cudaEventRecord(e, st());
+    return cuda_ok(ce, "timing event record");
   }
 
   int cell0_input(int m) {
@@ -706,6 +740,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[5] = c->pipelined;
     key.opts[6] = c->pdl;
     key.opts[7] = c->trace;
+    key.opts[8] = c->ktime;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -799,10 +834,28 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_KERNEL_TIMES:
+      if (value < 0 || value > 5) return c->fail(GPIPE_ERR_INVALID_ARG, "kernel-times selector out of range");
+      c->ktime = static_cast<int>(value);
+      break;
     default: return c->fail(GPIPE_ERR_INVALID_ARG, "unknown option");
   }
   c->drop_graph();
   return GPIPE_OK;
+}
+
+int gpipe_kernel_times(gpipe_ctx* c, float* ms_out, double* flops_out, int count) {
+  if (!c || count < 0) return GPIPE_ERR_INVALID_ARG;
+  const int n = c->ktime ? c->kt_n : 0;
+  for (int i = 0; i < n && i < count; ++i) {
+    float t = 0.f;
+    cudaError_t ce = cudaEventSynchronize(c->kt_ev[2 * i + 1]);
+    if (ce == cudaSuccess) ce = cudaEventElapsedTime(&t, c->kt_ev[2 * i], c->kt_ev[2 * i + 1]);
+    if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, std::string("kernel times: ") + cudaGetErrorString(ce));
+    if (ms_out) ms_out[i] = t;
+    if (flops_out) flops_out[i] = c->kt_flops[i];
+  }
+  return n;
 }
 
 int gpipe_debug_counters(gpipe_ctx* c, void* workspace, void* stream, uint64_t* remat_mismatch, int* error_flag) {
@@ -866,6 +919,8 @@ void gpipe_destroy(gpipe_ctx* c) {
   }
   if (c->ev_origin) cudaEventDestroy(c->ev_origin);
   for (cudaEvent_t e : c->ev_hdone)
+    if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->kt_ev)
     if (e) cudaEventDestroy(e);
   delete c;
 }

@@ -242,3 +242,22 @@ def test_trace_follows_the_pipeline_dependencies(b):
             assert bwd[k - 1, m] >= bwd[k, m]
     assert np.all(np.diff(fwd, axis=1) >= 0)
     assert np.all(np.diff(bwd[:K], axis=1) >= 0)
+
+
+@pytest.mark.parametrize("graph", [1, 0])
+def test_kernel_times_bracket_the_selected_gemms(b, graph):
+    """GPIPE_OPT_KERNEL_TIMES times every FFN first-projection launch (forward
+    and re-computation: 2 L M per step) on its own stream, inside the step's
+    graph too, and changes no result."""
+    w = SMALL_LM
+    inp = make_inputs(w)
+    opts = [(b.OPT_GRAPH, graph)]
+    gp0, st0, _, _ = _run(b, w, inp, steps=2, options=opts)
+    gp1, st1, _, _ = _run(b, w, inp, steps=2, options=opts + [(b.OPT_KERNEL_TIMES, b.EPI_BIAS_GELU + 1)])
+    ms, fl = gp1.kernel_times()
+    T = w.n * w.seq // w.M
+    assert len(ms) == 2 * w.L * w.M
+    assert np.all(ms > 0) and np.all(ms < 100)
+    assert np.all(fl == 2.0 * T * w.ffn * w.d)
+    assert np.array_equal(st0.host(st0.p32), st1.host(st1.p32))
+    assert gp0.kernel_times()[0].size == 0

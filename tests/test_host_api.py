@@ -190,3 +190,18 @@ def test_last_error_without_context_reports_any_failed_call(binding):
     with pytest.raises(binding.GpipeError):
         binding.GPipe(4, 5, 1, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=4, dtype=0)
     assert b"K <= L" in lib.gpipe_last_error(None)
+
+
+def test_options_are_validated_and_kernel_times_start_empty(binding):
+    from synth import WORKLOADS
+    g = binding.GPipe.from_workload(WORKLOADS["lm_small"])
+    with pytest.raises(binding.GpipeError) as e:
+        g.set_option(999, 1)
+    assert e.value.code == -1   # GPIPE_ERR_INVALID_ARG
+    for bad in (-1, 6):
+        with pytest.raises(binding.GpipeError):
+            g.set_option(binding.OPT_KERNEL_TIMES, bad)
+    g.set_option(binding.OPT_KERNEL_TIMES, binding.EPI_BIAS_GELU + 1)
+    ms, fl = g.kernel_times()   # no step taken yet: nothing timed, no CUDA call made
+    assert ms.size == 0 and fl.size == 0
+    g.close()
