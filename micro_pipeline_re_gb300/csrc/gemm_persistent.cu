@@ -21,6 +21,7 @@
 #include <cuda.h>
 
 #include "../../include/gpipe.h"
+#include "bias_grad.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "launch_util.cuh"
@@ -87,62 +88,6 @@ __device__ __forceinline__ void tile_origin(int t, const PArgs& a, int& m0, int&
   const int gm = a.m_tiles - first < PGROUP ? a.m_tiles - first : PGROUP;
   m0 = (first + r % gm) * PM;
   n0 = (r / gm) * BN;
-}
-
-// Bias gradient of rows m0..m0+127: dbias[m] += sum_k A(m, k), by the 8
-// epilogue warps (warp w owns rows m0 + 16w .. +15) in a fixed order: each
-// lane sums a fixed residue class of k in fp32, then the lanes are folded by
-// xor-shuffles.  One thread adds each row's sum; rows >= M are skipped.
-template <bool A_K>
-__device__ void bias_grad_rows(const PArgs& a, int m0, int ew, int lane) {
-  const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(a.a);
-  const int mb = m0 + 16 * ew;
-  if (A_K) {
-    // row-major rows of K: lane = (row r = lane >> 1, half h = lane & 1); h sums chunks 2j + h of 8
-    const int m = mb + (lane >> 1), h = lane & 1;
-    float s = 0.f;
-    if (m < a.M) {
-      const __nv_bfloat16* row = A + static_cast<int64_t>(m) * a.lda;
-      const int full = a.K / 8;
-      for (int j = h; j < full; j += 2) {
-        float v[8];
-        load8(row + 8 * j, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s += v[e];
-      }
-      if (h == 0)
-        for (int k = 8 * full; k < a.K; ++k) s += bf2f(row[k]);
-    }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    if (h == 0 && m < a.M) a.dbias[m] += s;
-  } else {
-    // rows of A are k: lane = (row class g = lane >> 1, 8-column chunk c = lane & 1)
-    const int g = lane >> 1, c = lane & 1;
-    const int mc = mb + 8 * c;
-    float s[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s[e] = 0.f;
-    const bool vec = mc + 8 <= a.M;
-    for (int k = g; k < a.K; k += 16) {
-      const __nv_bfloat16* p = A + static_cast<int64_t>(k) * a.lda + mc;
-      if (vec) {
-        float v[8];
-        load8(p, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s[e] += v[e];
-      } else {
-        for (int e = 0; e < 8; ++e)
-          if (mc + e < a.M) s[e] += bf2f(p[e]);
-      }
-    }
-#pragma unroll
-    for (int o = 2; o < 32; o <<= 1)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) s[e] += __shfl_xor_sync(0xffffffffu, s[e], o);
-    if (g == 0)
-      for (int e = 0; e < 8; ++e)
-        if (mc + e < a.M) a.dbias[mc + e] += s[e];
-  }
 }
 
 // Bounded wait that gives up at once after any earlier give-up in the CTA.
@@ -272,7 +217,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       tile_origin<BN>(t, args, m0, n0);
       const int m = m0 + r;
       if (EPI == EPI_ACC_F32 && args.dbias != nullptr && n0 == 0 && !*abort)
-        bias_grad_rows<A_K>(args, m0, warp - 2, lane);  // overlaps this tile's MMAs
+        bias_grad_rows<A_K>(static_cast<const __nv_bfloat16*>(args.a), args.lda, args.M, args.K, args.dbias, m0,
+                            warp - 2, lane);  // overlaps this tile's MMAs
       pwait(&accf[b], (i >> 1) & 1, err, DERR_ACC_WAIT, abort);
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
