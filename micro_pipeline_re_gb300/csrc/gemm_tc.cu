@@ -466,28 +466,24 @@ int split_factor(const GemmDesc& g, int BN) {
   return S;
 }
 
+// S: K split across a cluster of S CTAs (1: none), for the bf16-output
+// epilogues that have a split variant.
 template <int BN>
-int run_epi_bn(const GemmDesc& g, cudaStream_t s) {
+int run_epi_bn(const GemmDesc& g, cudaStream_t s, int S) {
   if (g.a_kmajor && g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: {
-        const int S = split_factor(g, BN);
+      case EPI_STORE:
         return S > 1 ? run<true, true, BN, EPI_STORE, true>(g, s, S) : run<true, true, BN, EPI_STORE>(g, s);
-      }
       case EPI_BIAS_GELU: return run<true, true, BN, EPI_BIAS_GELU>(g, s);
       case EPI_STORE_F32: return run<true, true, BN, EPI_STORE_F32>(g, s);
       case EPI_ACC_F32: return run<true, true, BN, EPI_ACC_F32>(g, s);
     }
   } else if (g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: {
-        const int S = split_factor(g, BN);
+      case EPI_STORE:
         return S > 1 ? run<true, false, BN, EPI_STORE, true>(g, s, S) : run<true, false, BN, EPI_STORE>(g, s);
-      }
-      case EPI_GELU_BWD: {
-        const int S = split_factor(g, BN);
+      case EPI_GELU_BWD:
         return S > 1 ? run<true, false, BN, EPI_GELU_BWD, true>(g, s, S) : run<true, false, BN, EPI_GELU_BWD>(g, s);
-      }
       case EPI_ACC_F32: return run<true, false, BN, EPI_ACC_F32>(g, s);
     }
   } else if (!g.a_kmajor && !g.b_kmajor) {
@@ -513,11 +509,16 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
   // each tile's epilogue with the next tile's MMAs.  Otherwise one tile per
   // CTA, 128 columns when that gives at least one CTA per SM of the share,
   // else 64 (twice the CTAs, each with half the operand traffic and epilogue).
+  // The split-K choice depends on the shape alone (never on the SM share), so
+  // that a GEMM sums in the same order whatever the schedule around it.
+  const bool has_split = g.a_kmajor && (g.epi == EPI_STORE || (!g.b_kmajor && g.epi == EPI_GELU_BWD));
+  const int S = has_split ? split_factor(g, 64) : 1;
+  if (S > 1) return run_epi_bn<64>(g, s, S);
   const int budget = g.sm_budget > 0 ? g.sm_budget : num_sms();
   if (persistent_tiles(g) > budget) return launch_gemm_persistent(g, s, budget);
   const int64_t tiles128 = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 127) / 128);
-  if (tiles128 >= budget) return run_epi_bn<128>(g, s);
-  return run_epi_bn<64>(g, s);
+  if (tiles128 >= budget) return run_epi_bn<128>(g, s, 1);
+  return run_epi_bn<64>(g, s, 1);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -192,6 +192,14 @@ class Executor {
  public:
   Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t origin) : c_(c), p_(p), origin_(origin) {}
 
+  // Cells busy at clock tick t of the review's schedule (cell k works on
+  // micro-batch t - k in the forward, on micro-batch t - (K-1-k) in the backward).
+  int busy_at(int t) const {
+    const int lo = t - (c_->M - 1) > 0 ? t - (c_->M - 1) : 0;
+    const int hi = t < c_->K - 1 ? t : c_->K - 1;
+    return hi >= lo ? hi - lo + 1 : 1;
+  }
+
   int run_step() {
     const Workspace& w = c_->ws;
     const int M = c_->M, K = c_->K;
@@ -210,8 +218,10 @@ class Executor {
     // its own lane, which hands the last cell the gradient of its output
     const int hl = head_lane();
     for (int m = 0; m < M; ++m) {
+      busy_ = busy_at(m);
       TRY(cell0_input(m));
       for (int k = 0; k < K; ++k) {
+        busy_ = busy_at(k + m);
         if (k > 0) TRY(cross_wait(k, c_->ev_fwd[k - 1], fwd_rec_[k - 1], k - 1));
         TRY(cell_forward(k, m, /*recompute=*/false));
         if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2), st()));
@@ -219,6 +229,7 @@ class Executor {
       }
       if (hl != lane_of(K - 1))
         TRY(cuda_ok(cudaStreamWaitEvent(main_s(hl), c_->ev_fwd[K - 1], 0), "stream wait"));
+      busy_ = busy_at(K - 1 + m);
       TRY(head(m));
       if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(K) * M + m) * 2), st()));
       if (hl != lane_of(K - 1)) TRY(cuda_ok(cudaEventRecord(c_->ev_hdone[m], main_s(hl)), "event record"));
@@ -229,6 +240,7 @@ class Executor {
       for (int k = K - 1; k >= 0; --k) {
         const int lk = lane_of(k);
         cur_lane_ = lk;
+        busy_ = busy_at(K - 1 - k + m);
         TRY(join_all(lk));  // side work still reading this lane's slots
         if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
         // gradient of the cell's output
@@ -297,6 +309,7 @@ class Executor {
   cudaStream_t origin_;
   cudaStream_t cur_ = nullptr;  // stream override for gemm()/launch helpers (nullptr: the lane's main stream)
   int cur_lane_ = 0;            // lane whose main stream receives the current cell's work
+  int busy_ = 1;                // cells busy at the current op's tick of the schedule
   bool rec_[64][EV_COUNT] = {};
   bool fwd_rec_[64] = {};
   bool bdone_rec_[64][2] = {};
@@ -425,7 +438,9 @@ class Executor {
     g.C2 = C2;
     g.aux = aux;
     g.ldaux = ldaux;
-    g.sm_budget = num_sms() / c_->nstreams();  // lanes share the machine
+    // lanes share the machine: a GEMM gets the SMs of one lane among the cells
+    // that the review's schedule has busy at this clock tick (plus the head)
+    g.sm_budget = c_->nstreams() > 1 ? num_sms() / (busy_ + 1) : num_sms();
     if (c_->ktime != epi + 1) return launch_gemm(g, st());
     cudaEvent_t e0, e1;
     TRY(c_->kt_next(2.0 * M * N * K, &e0, &e1));
