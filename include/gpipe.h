@@ -181,11 +181,15 @@ enum {
   GPIPE_OPT_TRACE = 9,       /* [0] 1: write the GPU clock (ns) when every cell (and
                                 the head) finishes each micro-batch's forward and
                                 backward; read with gpipe_trace                      */
-  GPIPE_OPT_KERNEL_TIMES = 10 /* [0] e+1: bracket every GEMM launch of the step whose
+  GPIPE_OPT_KERNEL_TIMES = 10, /* [0] e+1: bracket every GEMM launch of the step whose
                                 epilogue is e (GPIPE_EPI_* of gpipe_ops.h) with timing
                                 events on the stream it is launched on (recorded as
                                 event nodes of the step's graph); read with
                                 gpipe_kernel_times                                   */
+  GPIPE_OPT_SM_SHARE = 11    /* [100] with lanes, a GEMM's grid is this percentage of
+                                its fair share of the SMs (SMs / (cells busy at its
+                                tick of the schedule + 1)), 25..800; the tile
+                                choice follows the grid, results stay identical    */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

@@ -55,7 +55,7 @@ struct StepPtrs {
 
 struct GraphKey {
   StepPtrs p;
-  int64_t opts[9];
+  int64_t opts[10];
   bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
 };
 
@@ -81,6 +81,7 @@ struct gpipe_ctx {
   bool pdl = false;        // kernels may launch while their predecessor drains (measured slower with lanes)
   bool trace = false;      // stamp the GPU clock at the end of every (cell, micro-batch, phase)
   int ktime = 0;           // e+1: time every GEMM launch with epilogue e (event pairs)
+  int sm_share = 100;      // percent of a GEMM's fair share of the SMs (with lanes)
   std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
   std::vector<double> kt_flops;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
@@ -440,7 +441,12 @@ class Executor {
     g.ldaux = ldaux;
     // lanes share the machine: a GEMM gets the SMs of one lane among the cells
     // that the review's schedule has busy at this clock tick (plus the head)
-    g.sm_budget = c_->nstreams() > 1 ? num_sms() / (busy_ + 1) : num_sms();
+    if (c_->nstreams() > 1) {
+      const int share = num_sms() * c_->sm_share / (100 * (busy_ + 1));
+      g.sm_budget = share < 1 ? 1 : (share > num_sms() ? num_sms() : share);
+    } else {
+      g.sm_budget = num_sms();
+    }
     if (c_->ktime != epi + 1) return launch_gemm(g, st());
     cudaEvent_t e0, e1;
     TRY(c_->kt_next(2.0 * M * N * K, &e0, &e1));
@@ -756,6 +762,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[6] = c->pdl;
     key.opts[7] = c->trace;
     key.opts[8] = c->ktime;
+    key.opts[9] = c->sm_share;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -849,6 +856,10 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_SM_SHARE:
+      if (value < 25 || value > 800) return c->fail(GPIPE_ERR_INVALID_ARG, "SM share must be 25..800 percent");
+      c->sm_share = static_cast<int>(value);
+      break;
     case GPIPE_OPT_KERNEL_TIMES:
       if (value < 0 || value > 5) return c->fail(GPIPE_ERR_INVALID_ARG, "kernel-times selector out of range");
       c->ktime = static_cast<int>(value);

@@ -201,6 +201,10 @@ def test_options_are_validated_and_kernel_times_start_empty(binding):
     for bad in (-1, 6):
         with pytest.raises(binding.GpipeError):
             g.set_option(binding.OPT_KERNEL_TIMES, bad)
+    for bad in (24, 801):
+        with pytest.raises(binding.GpipeError):
+            g.set_option(binding.OPT_SM_SHARE, bad)
+    g.set_option(binding.OPT_SM_SHARE, 200)
     g.set_option(binding.OPT_KERNEL_TIMES, binding.EPI_BIAS_GELU + 1)
     ms, fl = g.kernel_times()   # no step taken yet: nothing timed, no CUDA call made
     assert ms.size == 0 and fl.size == 0
