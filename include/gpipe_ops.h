@@ -106,8 +106,10 @@ int gpipe_op_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* 
                            float* lse, void* stream);
 
 /* Backward: dqkv [nseq*seq, 3*heads*64] gets dQ | dK | dV.  dvec is fp32
- * scratch [nseq*seq, heads] (rowsum(dO o O)).  No atomics: dQ and dK/dV are
- * produced by separate kernels, so results are bit-reproducible. */
+ * [nseq*seq, heads] output of rowsum(dO o O).  One launch: its dQ blocks and
+ * its dK/dV blocks each compute what they need of rowsum(dO o O) themselves
+ * (same arithmetic), so they run side by side; no atomics, so results are
+ * bit-reproducible.  nseq <= 32767. */
 int gpipe_op_attention_bwd(int nseq, int seq, int heads, const void* qkv, const void* o,
                            const void* dout, const float* lse, float* dvec, void* dqkv,
                            void* stream);

@@ -252,17 +252,34 @@ struct DkvSmem {
   float Ls[2][BQ], Ds[2][BQ];
 };
 
+// D = rowsum(dO o O) of head h for the 64 rows row0..row0+63, by the block's
+// 128 threads (two per row, 32 columns each, then one shuffle): the same
+// arithmetic wherever it runs, so the dQ and dK/dV blocks agree bit for bit.
+__device__ __forceinline__ float row_dot_o_do(const __nv_bfloat16* __restrict__ out,
+                                              const __nv_bfloat16* __restrict__ dout, int64_t row0, int h, int D) {
+  const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 32;
+  const __nv_bfloat16* orow = out + (row0 + r) * D + h * HD + c0;
+  const __nv_bfloat16* drow = dout + (row0 + r) * D + h * HD + c0;
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < 32; c += 8) {
+    float ov[8], dv[8];
+    load8(orow + c, ov);
+    load8(drow + c, dv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc = fmaf(ov[j], dv[j], acc);
+  }
+  return acc + __shfl_xor_sync(0xffffffffu, acc, 1);
+}
+
 // ---------------------------------------------------------------------------
-// Backward: dQ (and D = rowsum(dO o O))
+// Backward: dQ (and D = rowsum(dO o O)) for sequence b
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* __restrict__ qkv,
-                                                          const __nv_bfloat16* __restrict__ out,
-                                                          const __nv_bfloat16* __restrict__ dout,
-                                                          const float* __restrict__ lse, float* __restrict__ dvec,
-                                                          __nv_bfloat16* __restrict__ dqkv, int seq, int heads) {
-  griddep_wait();
-  griddep_launch();
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
+__device__ __forceinline__ void attn_bwd_dq(const __nv_bfloat16* __restrict__ qkv,
+                                            const __nv_bfloat16* __restrict__ out,
+                                            const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+                                            float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv, int seq,
+                                            int heads, int b, uint8_t* dyn_smem) {
   DqSmem& S = *reinterpret_cast<DqSmem*>(dyn_smem);
   auto& Qs = S.Qs;
   auto& dOs = S.dOs;
@@ -270,7 +287,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
   auto& Vs = S.Vs;
   auto& Ls = S.Ls;
   auto& Ds = S.Ds;
-  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qb = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int D = heads * HD;
   const int64_t ld = 3 * (int64_t)D;
@@ -285,21 +302,10 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
   load_tile(Vs[0], Vg, ld);
   cp_async_commit();
 
-  // D for the block's rows: two threads per row, 32 columns each.
+  // D for the block's rows
   {
-    const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 32;
-    const __nv_bfloat16* orow = out + (row0 + r) * D + h * HD + c0;
-    const __nv_bfloat16* drow = dout + (row0 + r) * D + h * HD + c0;
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 32; c += 8) {
-      float ov[8], dv[8];
-      load8(orow + c, ov);
-      load8(drow + c, dv);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc += ov[j] * dv[j];
-    }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    const int r = threadIdx.x >> 1;
+    const float acc = row_dot_o_do(out, dout, row0, h, D);
     if ((threadIdx.x & 1) == 0) {
       Ds[r] = acc;
       dvec[(row0 + r) * heads + h] = acc;
@@ -353,14 +359,12 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
 // ---------------------------------------------------------------------------
 // Backward: dK, dV
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const __nv_bfloat16* __restrict__ qkv,
-                                                           const __nv_bfloat16* __restrict__ dout,
-                                                           const float* __restrict__ lse,
-                                                           const float* __restrict__ dvec,
-                                                           __nv_bfloat16* __restrict__ dqkv, int seq, int heads) {
-  griddep_wait();
-  griddep_launch();
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
+// (D of the query rows recomputed here, so this part does not wait for the dQ part)
+__device__ __forceinline__ void attn_bwd_dkv(const __nv_bfloat16* __restrict__ qkv,
+                                             const __nv_bfloat16* __restrict__ out,
+                                             const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+                                             __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int b,
+                                             uint8_t* dyn_smem) {
   DkvSmem& S = *reinterpret_cast<DkvSmem*>(dyn_smem);
   auto& Ks = S.Ks;
   auto& Vs = S.Vs;
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const __nv_bfloat16* 
   auto& dOs = S.dOs;
   auto& Ls = S.Ls;
   auto& Ds = S.Ds;
-  const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int kb = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int D = heads * HD;
   const int64_t ld = 3 * (int64_t)D;
@@ -382,10 +386,13 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const __nv_bfloat16* 
   load_tile(Qs[0], Qg + (int64_t)kb * BQ * ld, ld);
   load_tile(dOs[0], dOg + (int64_t)kb * BQ * D, D);
   cp_async_commit();
+  {
+    const float dd = row_dot_o_do(out, dout, srow + kb * BQ, h, D);
+    if ((threadIdx.x & 1) == 0) Ds[0][threadIdx.x >> 1] = dd;
+  }
   if (threadIdx.x < BQ) {
     const int64_t r = srow + kb * BQ + threadIdx.x;
     Ls[0][threadIdx.x] = lse[r * heads + h] * 1.4426950408889634f;
-    Ds[0][threadIdx.x] = dvec[r * heads + h];
   }
 
   uint32_t kf[4][4], vf[4][4];
@@ -400,10 +407,13 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const __nv_bfloat16* 
       load_tile(Qs[nb], Qg + (int64_t)(qb + 1) * BQ * ld, ld);
       load_tile(dOs[nb], dOg + (int64_t)(qb + 1) * BQ * D, D);
       cp_async_commit();
+      {
+        const float dd = row_dot_o_do(out, dout, srow + (qb + 1) * BQ, h, D);
+        if ((threadIdx.x & 1) == 0) Ds[nb][threadIdx.x >> 1] = dd;
+      }
       if (threadIdx.x < BQ) {
         const int64_t r = srow + (qb + 1) * BQ + threadIdx.x;
         Ls[nb][threadIdx.x] = lse[r * heads + h] * 1.4426950408889634f;
-        Ds[nb][threadIdx.x] = dvec[r * heads + h];
       }
       cp_async_wait<1>();
     } else {
@@ -439,6 +449,24 @@ __global__ void __launch_bounds__(128) attn_bwd_dkv_kernel(const __nv_bfloat16* 
   store_frag(dqkv + row * ld + 2 * D + h * HD, ld, dv, 1.0f);
 }
 
+// One launch for both parts: blocks with z < nseq compute dQ of sequence z,
+// the others dK/dV of sequence z - nseq; the two parts share no data.
+constexpr size_t kBwdSmem = sizeof(DqSmem) > sizeof(DkvSmem) ? sizeof(DqSmem) : sizeof(DkvSmem);
+__global__ void __launch_bounds__(128) attn_bwd_kernel(const __nv_bfloat16* __restrict__ qkv,
+                                                       const __nv_bfloat16* __restrict__ out,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       const float* __restrict__ lse, float* __restrict__ dvec,
+                                                       __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int nseq) {
+  griddep_wait();
+  griddep_launch();
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  const int z = blockIdx.z;
+  if (z < nseq)
+    attn_bwd_dq(qkv, out, dout, lse, dvec, dqkv, seq, heads, z, dyn_smem);
+  else
+    attn_bwd_dkv(qkv, out, dout, lse, dqkv, seq, heads, z - nseq, dyn_smem);
+}
+
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -446,11 +474,9 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int prepare_attention() {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e1 = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(DqSmem));
-    cudaError_t e2 = cudaFuncSetAttribute(attn_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(DkvSmem));
-    if (e1 != cudaSuccess || e2 != cudaSuccess)
+    cudaError_t e1 = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kBwdSmem);
+    if (e1 != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "attention_bwd: shared-memory attribute failed");
     attr_set = true;
   }
@@ -478,15 +504,11 @@ int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const vo
     return set_error(GPIPE_ERR_INVALID_ARG, "attention: pointers must be 16-B aligned");
   int rc = prepare_attention();
   if (rc) return rc;
-  dim3 grid(seq / BQ, heads, nseq);
-  (void)launch_k(attn_bwd_dq_kernel, grid, 128, sizeof(DqSmem), s, static_cast<const __nv_bfloat16*>(qkv),
-                                          static_cast<const __nv_bfloat16*>(o),
-                                          static_cast<const __nv_bfloat16*>(dout), lse, dvec,
-                                          static_cast<__nv_bfloat16*>(dqkv), seq, heads);
-  count_launch();
-  (void)launch_k(attn_bwd_dkv_kernel, grid, 128, sizeof(DkvSmem), s, static_cast<const __nv_bfloat16*>(qkv),
-                                           static_cast<const __nv_bfloat16*>(dout), lse, dvec,
-                                           static_cast<__nv_bfloat16*>(dqkv), seq, heads);
+  if (nseq > 32767) return set_error(GPIPE_ERR_INVALID_ARG, "attention: nseq must be <= 32767");
+  dim3 grid(seq / BQ, heads, 2 * nseq);
+  (void)launch_k(attn_bwd_kernel, grid, 128, kBwdSmem, s, static_cast<const __nv_bfloat16*>(qkv),
+                 static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, dvec,
+                 static_cast<__nv_bfloat16*>(dqkv), seq, heads, nseq);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention_bwd launch: %s", cudaGetErrorString(e));

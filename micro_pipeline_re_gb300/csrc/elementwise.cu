@@ -518,15 +518,14 @@ int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float*
   return check_launch("layernorm_fwd");
 }
 
-int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
-                         const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
-                         float* db_acc, float* scratch, cudaStream_t s) {
+int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                              const float* rstd, const float* g, const void* dres, void* dx, float* scratch,
+                              cudaStream_t s) {
   if (rows < 1 || d < 8 || d % 8 || d > 32 * 8 * kMaxChunks)
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: need rows >= 1, d %% 8 == 0, 8 <= d <= 1024");
   if (!al16(dy) || !al16(x) || !al16(dx) || !al16(g) || (dres && !al16(dres)) || !al16(scratch))
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: pointers must be 16-B aligned");
-  const int parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
-  const int grid = parts;
+  const int grid = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
   if (dtype == DT_F32)
     (void)launch_k(ln_bwd_kernel<float>, grid, 256, 0, s, static_cast<const float*>(dy), static_cast<const float*>(x), mean,
                                               rstd, g, static_cast<const float*>(dres), static_cast<float*>(dx),
@@ -535,10 +534,20 @@ int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void*
     (void)launch_k(ln_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, 
         static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean, rstd, g,
         static_cast<const __nv_bfloat16*>(dres), static_cast<__nv_bfloat16*>(dx), scratch, rows, d);
-  int rc = check_launch("layernorm_bwd");
-  if (rc) return rc;
+  return check_launch("layernorm_bwd");
+}
+
+int launch_layernorm_bwd_reduce(int rows, int d, const float* scratch, float* dg_acc, float* db_acc, cudaStream_t s) {
+  const int parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
   (void)launch_k(col_reduce_kernel, blocks_for(2 * d, 256), 256, 0, s, scratch, parts, 2 * d, dg_acc, d, db_acc);
   return check_launch("layernorm_bwd reduce");
+}
+
+int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                         const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
+                         float* db_acc, float* scratch, cudaStream_t s) {
+  const int rc = launch_layernorm_bwd_rows(dtype, rows, d, dy, x, mean, rstd, g, dres, dx, scratch, s);
+  return rc ? rc : launch_layernorm_bwd_reduce(rows, d, scratch, dg_acc, db_acc, s);
 }
 
 int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, float* out_acc, float* scratch,

@@ -86,7 +86,7 @@ struct gpipe_ctx {
   std::vector<double> kt_flops;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
   static constexpr int kMaxLanes = 64;
-  static constexpr int kLaneEvents = 9;
+  static constexpr int kLaneEvents = 11;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
   cudaEvent_t ev_origin = nullptr, ev_fwd[kMaxLanes] = {}, ev_bdone[kMaxLanes][2] = {}, ev_bfree[kMaxLanes][2] = {},
@@ -176,7 +176,7 @@ struct Slot {
 };
 
 // Events that order a lane's side stream against its main stream.
-enum { EV_FORK, EV_GF, EV_GH, EV_GQ, EV_DY0, EV_DY1, EV_DYB, EV_HEAD, EV_HEADF, EV_COUNT };
+enum { EV_FORK, EV_GF, EV_GH, EV_GQ, EV_DY0, EV_DY1, EV_DYB, EV_HEAD, EV_HEADF, EV_LN0, EV_LN1, EV_COUNT };
 constexpr int BUF_EXT = 2;  // "dy lives outside the lane" (boundary ring / head output)
 
 // Issues one step.  Host issue order is the serial GPipe order (phase 1:
@@ -311,6 +311,7 @@ class Executor {
   cudaStream_t cur_ = nullptr;  // stream override for gemm()/launch helpers (nullptr: the lane's main stream)
   int cur_lane_ = 0;            // lane whose main stream receives the current cell's work
   int busy_ = 1;                // cells busy at the current op's tick of the schedule
+  int ln_buf_[64] = {};         // per lane: the LayerNorm-backward partial buffer to use next
   bool rec_[64][EV_COUNT] = {};
   bool fwd_rec_[64] = {};
   bool bdone_rec_[64][2] = {};
@@ -363,6 +364,22 @@ class Executor {
     cur_ = nullptr;
     if (rc) return rc;
     return mark(lane, e);
+  }
+
+  // LayerNorm backward: the rows (dx, on the critical path) on the current
+  // stream; the fixed-order reduction of the gamma/beta partial sums on the
+  // side stream, in issue order like the weight gradients.  The two partial
+  // buffers alternate, so the next LayerNorm backward need not wait for this
+  // reduction, only for the one that read its buffer before.
+  int ln_backward(int dt, int T, int d, const void* dy, const void* x, const float* mean, const float* rstd,
+                  const float* g, const void* dres, void* dx, float* dg, float* db, float* part0, float* part1) {
+    const int lane = cur_lane_;
+    const int b = ln_buf_[lane];
+    ln_buf_[lane] ^= 1;
+    float* part = b ? part1 : part0;
+    TRY(join(lane, EV_LN0 + b));
+    TRY(launch_layernorm_bwd_rows(dt, T, d, dy, x, mean, rstd, g, dres, dx, part, st()));
+    return on_side(EV_LN0 + b, [&] { return launch_layernorm_bwd_reduce(T, d, part, dg, db, st()); });
   }
 
   char* ws(size_t off) const { return p_.ws + off; }
@@ -542,6 +559,8 @@ class Executor {
     const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = dm.ffn;
     const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
     float* scratch = reinterpret_cast<float*>(lb + ll.scratch);
+    float* lnp0 = reinterpret_cast<float*>(lb + ll.lnp[0]);
+    float* lnp1 = reinterpret_cast<float*>(lb + ll.lnp[1]);
     char* gf = lb + ll.gf;
     char* gt = lb + ll.gt;
     const void* ffn_in = dm.kind == 1 ? static_cast<const void*>(s.u2) : static_cast<const void*>(s.u);
@@ -560,15 +579,15 @@ class Executor {
     TRY(gemm(T, d, f, gf, f, true, wgt(o.w1), d, false, EPI_STORE, gt, d));
     if (dm.kind == 0) {
       if (dx_buf != BUF_EXT) TRY(join(lane, dx_buf == 0 ? EV_DY0 : EV_DY1));
-      return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g),
-                                  grad(o.ln1_b), scratch, st());
+      return ln_backward(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g), grad(o.ln1_b),
+                         lnp0, lnp1);
     }
     char* gh = lb + ll.gh;
     char* gq = lb + ll.gq;
     // h1 -> LN2: dh1 = LN2'(du2) + dy
     TRY(join(lane, EV_GH));
-    TRY(launch_layernorm_bwd(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g),
-                             grad(o.ln2_b), scratch, st()));
+    TRY(ln_backward(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g), grad(o.ln2_b),
+                    lnp0, lnp1));
     // attention output projection
     TRY(on_side(EV_GH, [&] {
       return gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d, nullptr, nullptr, 0, nullptr,
@@ -583,8 +602,8 @@ class Executor {
     }));
     TRY(gemm(T, d, 3 * d, gq, 3 * d, true, wgt(o.w_qkv), d, false, EPI_STORE, gt, d));
     if (dx_buf != BUF_EXT) TRY(join(lane, dx_buf == 0 ? EV_DY0 : EV_DY1));
-    return launch_layernorm_bwd(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh, dx, grad(o.ln1_g),
-                                grad(o.ln1_b), scratch, st());
+    return ln_backward(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh, dx, grad(o.ln1_g), grad(o.ln1_b), lnp0,
+                       lnp1);
   }
 
   // The head of micro-batch m, once: loss rows from the last cell's output
@@ -619,10 +638,10 @@ class Executor {
     TRY(on_side(EV_HEAD, [&] {
       return gemm(dm.vocab, d, T, logits, ldz, false, ws(w.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d);
     }));
-    return launch_layernorm_bwd(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(w.meanf)),
-                                reinterpret_cast<float*>(ws(w.rstdf)), p32(c_->pl.lnf_g), nullptr, dy,
-                                grad(c_->pl.lnf_g), grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(w.hscratch)),
-                                st());
+    return ln_backward(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(w.meanf)),
+                       reinterpret_cast<float*>(ws(w.rstdf)), p32(c_->pl.lnf_g), nullptr, dy, grad(c_->pl.lnf_g),
+                       grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(w.hlnp[0])),
+                       reinterpret_cast<float*>(ws(w.hlnp[1])));
   }
 };
 

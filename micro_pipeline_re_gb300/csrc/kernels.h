@@ -59,6 +59,13 @@ size_t colred_scratch_floats(int rows, int cols);
 
 int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
                          float* mean, float* rstd, cudaStream_t stream);
+// LayerNorm backward in two launches: the rows (dx, and one partial row of the
+// gamma/beta column sums per 8 rows into scratch), then the fixed-order
+// reduction of the partials into dg_acc / db_acc (+=).
+int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
+                              const float* rstd, const float* g, const void* dres, void* dx, float* scratch,
+                              cudaStream_t s);
+int launch_layernorm_bwd_reduce(int rows, int d, const float* scratch, float* dg_acc, float* db_acc, cudaStream_t s);
 int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
                          const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,
                          float* db_acc, float* scratch, cudaStream_t stream);

@@ -185,6 +185,9 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   const size_t parts = (Tmb + 7) / 8;
   w.scratch_bytes = std::max(parts * cols * 4, Tmb * std::max<size_t>(H, 1) * 4);
   ln.scratch = ltake(w.scratch_bytes);
+  w.lnp_bytes = parts * 2 * d * 4;
+  ln.lnp[0] = ltake(w.lnp_bytes);
+  ln.lnp[1] = ltake(w.lnp_bytes);
   ln.bytes = lo;
   w.lane = ln;
   w.nlanes = pipelined ? K : 1;
@@ -210,6 +213,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     w.logits = take(Tmb * static_cast<size_t>(dm.vocab) * 4);
     w.hgt = take(Tmb * d * es);
     w.hscratch = take(w.scratch_bytes);
+    w.hlnp[0] = take(w.lnp_bytes);
+    w.hlnp[1] = take(w.lnp_bytes);
   }
   w.loss_rows = take(T * 4);
   w.act_bytes = off;
@@ -230,7 +235,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   const size_t boundary = static_cast<size_t>(K + 3) * T * d * es + static_cast<size_t>(K) * 2 * Tmb * d * es;
   const size_t per_lane = ln.bytes + 4096;
   const size_t head =
-      dm.kind == 1 ? Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + w.scratch_bytes + 8192 : 0;
+      dm.kind == 1 ? Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + w.scratch_bytes + 2 * w.lnp_bytes + 8192
+                   : 0;
   const size_t cell_all = remat ? 0 : static_cast<size_t>(L) * M * w.slot_bytes;
   w.bound_bytes = boundary + static_cast<size_t>(w.nlanes) * per_lane + cell_all + head + T * 4 + 8192;
   return w;

@@ -50,6 +50,7 @@ struct LaneLayout {
   size_t slots = 0;                             // re-materialised internals of one cell (Lc slots)
   size_t g0 = 0, g1 = 0, gt = 0, gf = 0, gh = 0, gq = 0;  // gradients in flight
   size_t scratch = 0;                           // reduction partials / attention row sums
+  size_t lnp[2] = {0, 0};                       // LayerNorm-backward gamma/beta partials, alternating
   size_t bytes = 0;
 };
 
@@ -65,6 +66,8 @@ struct Workspace {
   size_t noremat_slots = 0, nslots_noremat = 0;  // L x M slots when re-materialisation is off
   size_t hf = 0, meanf = 0, rstdf = 0, logits = 0;  // head (kind 1)
   size_t hgt = 0, hscratch = 0;             // head's gradient temporary and reduction scratch
+  size_t hlnp[2] = {0, 0};                  // head's LayerNorm-backward partials, alternating
+  size_t lnp_bytes = 0;                     // ceil(Tmb / 8) x 2d fp32
   size_t hdy = 0;                           // M x [Tmb, d]: gradient of the last cell's output per micro-batch
   size_t scratch_bytes = 0;
   size_t loss_rows = 0, misc = 0;            // misc: loss (float) at +0, remat counter (u64) at +8
