@@ -459,7 +459,11 @@ class Executor {
     // lanes share the machine: a GEMM gets the SMs of one lane among the cells
     // that the review's schedule has busy at this clock tick (plus the head)
     if (c_->nstreams() > 1) {
-      const int share = num_sms() * c_->sm_share / (100 * (busy_ + 1));
+      // a GEMM of few output tiles is bound by latency, not by its share of
+      // the tensor cores: let it spread over twice the share
+      int share = num_sms() * c_->sm_share / (100 * (busy_ + 1));
+      const int64_t tiles = static_cast<int64_t>((M + 127) / 128) * ((N + 127) / 128);
+      if (tiles <= 4 * static_cast<int64_t>(share)) share *= 2;
       g.sm_budget = share < 1 ? 1 : (share > num_sms() ? num_sms() : share);
     } else {
       g.sm_budget = num_sms();
