@@ -433,15 +433,16 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = Cfg::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = S;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 0;  // heavy: never launched early
+    set_priority_attr(attr[2], stream);
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 3;
     e = cudaLaunchKernelEx(&cfg, tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>, ta, tb, tc, tc2, tx, args,
                            device_error_ptr());
   } else {

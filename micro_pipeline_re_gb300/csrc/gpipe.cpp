@@ -123,14 +123,21 @@ struct gpipe_ctx {
     auto mk_ev = [&](cudaEvent_t& e) {
       return e || cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
     };
-    auto mk_st = [&](cudaStream_t& st) {
-      return st || cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
+    // Priorities: the cells' main streams (the critical path) highest, the
+    // head's main stream next, the side streams (weight gradients and
+    // gamma/beta reductions, off the critical path) lowest.
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) least = greatest = 0;
+    auto mk_st = [&](cudaStream_t& st, int prio) {
+      return st || cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, prio) == cudaSuccess;
     };
     bool ok = mk_ev(ev_origin);
     if (static_cast<int>(ev_hdone.size()) < M) ev_hdone.resize(M, nullptr);
     for (int m = 0; m < M && ok; ++m) ok = mk_ev(ev_hdone[m]);
     for (int i = 0; i < nstreams() && ok; ++i) {
-      ok = mk_st(lane_main[i]) && mk_st(lane_side[i]) && mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
+      const bool head = nstreams() > 1 && i == nstreams() - 1;
+      ok = mk_st(lane_main[i], head ? (least + greatest) / 2 : greatest) && mk_st(lane_side[i], least) &&
+           mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
       for (int e = 0; e < kLaneEvents && ok; ++e) ok = mk_ev(lane_ev[i][e]);
     }
     for (int k = 0; k < K && k < kMaxLanes && ok; ++k)
@@ -807,7 +814,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
         return c->fail(GPIPE_ERR_CUDA, std::string("graph capture failed: ") + cudaGetErrorString(ce));
       c->launches_per_step = launch_count() - before;
       c->graph = g;
-      ce = cudaGraphInstantiate(&c->gexec, g, 0);
+      ce = cudaGraphInstantiate(&c->gexec, g, cudaGraphInstantiateFlagUseNodePriority);
       if (ce != cudaSuccess) {
         c->drop_graph();
         return c->fail(GPIPE_ERR_CUDA, std::string("graph instantiate failed: ") + cudaGetErrorString(ce));

@@ -25,6 +25,17 @@ void set_pdl_enabled(bool on);
 // heavy = true: the kernel holds most of an SM's shared memory / tensor
 // memory; it is never launched early, so a waiting copy cannot keep those from
 // kernels of other streams.
+// Every launch carries its stream's priority as a launch attribute, so that a
+// kernel captured into a graph (instantiated with node priorities) keeps the
+// priority of the stream it was issued to: the step's critical-path streams
+// get SMs before its weight-gradient streams.
+inline void set_priority_attr(cudaLaunchAttribute& a, cudaStream_t s) {
+  int prio = 0;
+  if (cudaStreamGetPriority(s, &prio) != cudaSuccess) prio = 0;
+  a.id = cudaLaunchAttributePriority;
+  a.val.priority = prio;
+}
+
 template <bool heavy = false, typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
@@ -32,11 +43,12 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = (!heavy && pdl_enabled()) ? 1 : 0;
+  set_priority_attr(attr[1], s);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
