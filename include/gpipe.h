@@ -186,10 +186,16 @@ enum {
                                 events on the stream it is launched on (recorded as
                                 event nodes of the step's graph); read with
                                 gpipe_kernel_times                                   */
-  GPIPE_OPT_SM_SHARE = 11    /* [100] with lanes, a GEMM's grid is this percentage of
-                                its fair share of the SMs (SMs / (cells busy at its
+  GPIPE_OPT_SM_SHARE = 11,   /* [100] with lanes, a GEMM's grid is this percentage of
+                                its fair share of the SMs (SMs / (lanes busy at its
                                 tick of the schedule + 1)), 25..800; the tile
                                 choice follows the grid, results stay identical    */
+  GPIPE_OPT_INFLIGHT = 12    /* [1] with lanes: micro-batches each cell works on at
+                                once (1 or 2).  2 gives each cell two lanes that take
+                                its micro-batches in turn (one more cell workspace per
+                                cell) and share one side stream, so every weight
+                                gradient still accumulates in micro-batch order and
+                                results are identical.  Set before gpipe_sizes.      */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

@@ -80,12 +80,13 @@ struct gpipe_ctx {
   bool pipelined = true;   // cells run as concurrent lanes (the review's pipeline on one GPU)
   bool pdl = false;        // kernels may launch while their predecessor drains (measured slower with lanes)
   bool trace = false;      // stamp the GPU clock at the end of every (cell, micro-batch, phase)
+  int inflight = 1;        // with lanes: micro-batches each cell works on at once (1 or 2)
   int ktime = 0;           // e+1: time every GEMM launch with epilogue e (event pairs)
   int sm_share = 100;      // percent of a GEMM's fair share of the SMs (with lanes)
   std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
   std::vector<double> kt_flops;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
-  static constexpr int kMaxLanes = 64;
+  static constexpr int kMaxLanes = 128;
   static constexpr int kLaneEvents = 11;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
@@ -113,8 +114,9 @@ struct gpipe_ctx {
   }
   void refresh_ws() {
     if (ws_stale) {
-      ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat,
-                          pipelined && K < kMaxLanes);
+      const bool lanes = pipelined && K * inflight < kMaxLanes;
+      ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat, lanes,
+                          lanes ? inflight : 1);
       ws_stale = false;
     }
   }
@@ -230,23 +232,23 @@ class Executor {
       TRY(cell0_input(m));
       for (int k = 0; k < K; ++k) {
         busy_ = busy_at(k + m);
-        if (k > 0) TRY(cross_wait(k, c_->ev_fwd[k - 1], fwd_rec_[k - 1], k - 1));
+        if (k > 0) TRY(cross_wait(k, m, c_->ev_fwd[k - 1], fwd_rec_[k - 1], k - 1));
         TRY(cell_forward(k, m, /*recompute=*/false));
         if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2), st()));
-        TRY(cross_record(k, c_->ev_fwd[k], fwd_rec_[k]));
+        TRY(cross_record(k, m, c_->ev_fwd[k], fwd_rec_[k]));
       }
-      if (hl != lane_of(K - 1))
+      if (hl != lane_of(K - 1, m))
         TRY(cuda_ok(cudaStreamWaitEvent(main_s(hl), c_->ev_fwd[K - 1], 0), "stream wait"));
       busy_ = busy_at(K - 1 + m);
       TRY(head(m));
       if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(K) * M + m) * 2), st()));
-      if (hl != lane_of(K - 1)) TRY(cuda_ok(cudaEventRecord(c_->ev_hdone[m], main_s(hl)), "event record"));
+      if (hl != lane_of(K - 1, m)) TRY(cuda_ok(cudaEventRecord(c_->ev_hdone[m], main_s(hl)), "event record"));
     }
     // phase 2: backward with re-computation
     for (int m = 0; m < M; ++m) {
       const int p = m & 1;
       for (int k = K - 1; k >= 0; --k) {
-        const int lk = lane_of(k);
+        const int lk = lane_of(k, m);
         cur_lane_ = lk;
         busy_ = busy_at(K - 1 - k + m);
         TRY(join_all(lk));  // side work still reading this lane's slots
@@ -258,7 +260,7 @@ class Executor {
           if (hl != lk) TRY(cuda_ok(cudaStreamWaitEvent(main_s(lk), c_->ev_hdone[m], 0), "stream wait"));
           dy = hdy(m);
         } else {
-          TRY(cross_wait(k, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
+          TRY(cross_wait(k, m, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
           dy = bgrad(k + 1, p);
         }
         int cur_buf = dy_buf;
@@ -269,7 +271,7 @@ class Executor {
           int dx_buf;
           if (j == 0 && k > 0) {
             // hand the input gradient to cell k-1 through the ring
-            if (bfree_rec_[k][p]) TRY(cross_wait(k, c_->ev_bfree[k][p], bfree_rec_[k][p], k - 1));
+            if (bfree_rec_[k][p]) TRY(cross_wait(k, m, c_->ev_bfree[k][p], bfree_rec_[k][p], k - 1));
             dx = bgrad(k, p);
             dx_buf = BUF_EXT;
           } else if (j == 0 && c_->dm.kind == 1) {
@@ -284,10 +286,10 @@ class Executor {
           cur_buf = dx_buf;
         }
         if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2 + 1), st()));
-        if (k > 0) TRY(cross_record(k, c_->ev_bdone[k][p], bdone_rec_[k][p]));
+        if (k > 0) TRY(cross_record(k, m, c_->ev_bdone[k][p], bdone_rec_[k][p]));
         if (k < K - 1) {  // this cell has finished reading the ring slot of cell k+1
           TRY(join(lk, EV_DYB));
-          TRY(cross_record(k, c_->ev_bfree[k + 1][p], bfree_rec_[k + 1][p]));
+          TRY(cross_record(k, m, c_->ev_bfree[k + 1][p], bfree_rec_[k + 1][p]));
         }
       }
     }
@@ -318,41 +320,46 @@ class Executor {
   cudaStream_t cur_ = nullptr;  // stream override for gemm()/launch helpers (nullptr: the lane's main stream)
   int cur_lane_ = 0;            // lane whose main stream receives the current cell's work
   int busy_ = 1;                // cells busy at the current op's tick of the schedule
-  int ln_buf_[64] = {};         // per lane: the LayerNorm-backward partial buffer to use next
-  bool rec_[64][EV_COUNT] = {};
-  bool fwd_rec_[64] = {};
-  bool bdone_rec_[64][2] = {};
-  bool bfree_rec_[64][2] = {};
+  int ln_buf_[gpipe_ctx::kMaxLanes] = {};  // per lane: the LayerNorm-backward partial buffer to use next
+  bool rec_[gpipe_ctx::kMaxLanes][EV_COUNT] = {};
+  bool fwd_rec_[gpipe_ctx::kMaxLanes] = {};
+  bool bdone_rec_[gpipe_ctx::kMaxLanes][2] = {};
+  bool bfree_rec_[gpipe_ctx::kMaxLanes][2] = {};
 
-  int lane_of(int k) const { return c_->ws.nlanes > 1 ? k : 0; }
-  int head_lane() const { return c_->ws.nlanes > 1 ? c_->K : 0; }
+  // Lane of cell k for micro-batch m: with lanes, cell k owns lanes
+  // k*inflight .. k*inflight + inflight-1 and takes its micro-batches in turn.
+  int lane_of(int k, int m) const { return c_->ws.nlanes > 1 ? k * c_->ws.inflight + m % c_->ws.inflight : 0; }
+  int head_lane() const { return c_->ws.nlanes > 1 ? c_->ws.nlanes : 0; }
+  // A cell's lanes share one side stream (its first lane's), which receives the
+  // cell's weight-gradient work in micro-batch order.
+  int side_of(int lane) const { return lane < c_->ws.nlanes ? lane - lane % c_->ws.inflight : lane; }
   char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
-  cudaStream_t side(int lane) const { return c_->concurrent ? c_->lane_side[lane] : c_->lane_main[lane]; }
+  cudaStream_t side(int lane) const { return c_->concurrent ? c_->lane_side[side_of(lane)] : c_->lane_main[lane]; }
   cudaStream_t st() const { return cur_ ? cur_ : c_->lane_main[cur_lane_]; }
   int cuda_ok(cudaError_t e, const char* what) {
     return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   }
   // cross-lane handshakes (no-ops when both cells share a lane)
-  int cross_record(int k, cudaEvent_t e, bool& rec) {
+  int cross_record(int k, int m, cudaEvent_t e, bool& rec) {
     if (c_->ws.nlanes == 1) return GPIPE_OK;
     rec = true;
-    return cuda_ok(cudaEventRecord(e, main_s(lane_of(k))), "event record");
+    return cuda_ok(cudaEventRecord(e, main_s(lane_of(k, m))), "event record");
   }
-  int cross_wait(int k, cudaEvent_t e, bool rec, int from_k) {
-    if (c_->ws.nlanes == 1 || !rec || lane_of(k) == lane_of(from_k)) return GPIPE_OK;
-    return cuda_ok(cudaStreamWaitEvent(main_s(lane_of(k)), e, 0), "stream wait");
+  int cross_wait(int k, int m, cudaEvent_t e, bool rec, int from_k) {
+    if (c_->ws.nlanes == 1 || !rec || lane_of(k, m) == lane_of(from_k, m)) return GPIPE_OK;
+    return cuda_ok(cudaStreamWaitEvent(main_s(lane_of(k, m)), e, 0), "stream wait");
   }
   // a lane's side stream starts after everything issued so far on its main stream
   int fork(int lane) {
     if (!c_->concurrent) return GPIPE_OK;
     TRY(cuda_ok(cudaEventRecord(c_->lane_ev[lane][EV_FORK], main_s(lane)), "event record"));
-    return cuda_ok(cudaStreamWaitEvent(c_->lane_side[lane], c_->lane_ev[lane][EV_FORK], 0), "stream wait");
+    return cuda_ok(cudaStreamWaitEvent(side(lane), c_->lane_ev[lane][EV_FORK], 0), "stream wait");
   }
   int mark(int lane, int e) {
     if (!c_->concurrent) return GPIPE_OK;
     rec_[lane][e] = true;
-    return cuda_ok(cudaEventRecord(c_->lane_ev[lane][e], c_->lane_side[lane]), "event record");
+    return cuda_ok(cudaEventRecord(c_->lane_ev[lane][e], side(lane)), "event record");
   }
   int join(int lane, int e) {
     if (!c_->concurrent || !rec_[lane][e]) return GPIPE_OK;
@@ -420,7 +427,7 @@ class Executor {
     if (c_->no_remat)
       b = ws(c_->ws.noremat_slots) + (static_cast<size_t>(m) * c_->L + c_->bounds[k] + j) * c_->ws.slot_bytes;
     else
-      b = lane_base(lane_of(k)) + c_->ws.lane.slots + static_cast<size_t>(j) * c_->ws.slot_bytes;
+      b = lane_base(lane_of(k, m)) + c_->ws.lane.slots + static_cast<size_t>(j) * c_->ws.slot_bytes;
     const SlotLayout& s = c_->ws.slot;
     Slot r;
     r.u = b + s.u;
@@ -468,7 +475,7 @@ class Executor {
     if (c_->nstreams() > 1) {
       // a GEMM of few output tiles is bound by latency, not by its share of
       // the tensor cores: let it spread over twice the share
-      int share = num_sms() * c_->sm_share / (100 * (busy_ + 1));
+      int share = num_sms() * c_->sm_share / (100 * (busy_ * c_->ws.inflight + 1));
       const int64_t tiles = static_cast<int64_t>((M + 127) / 128) * ((N + 127) / 128);
       if (tiles <= 4 * static_cast<int64_t>(share)) share *= 2;
       g.sm_budget = share < 1 ? 1 : (share > num_sms() ? num_sms() : share);
@@ -495,7 +502,7 @@ class Executor {
 
   int cell0_input(int m) {
     if (c_->dm.kind != 1) return GPIPE_OK;  // kind 0 reads the caller's x directly
-    cur_lane_ = lane_of(0);
+    cur_lane_ = lane_of(0, m);
     return launch_embedding_fwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), wgt(c_->pl.emb),
                                 stash(0, m), st());
   }
@@ -505,23 +512,23 @@ class Executor {
   // result, the cell output, is already stashed and not needed to
   // differentiate the cell).
   int cell_forward(int k, int m, bool recompute) {
-    cur_lane_ = lane_of(k);
+    cur_lane_ = lane_of(k, m);
     const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
     for (int j = 0; j < n; ++j) {
       const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
       void* out = j == n - 1 ? static_cast<void*>(stash(k + 1, m)) : static_cast<void*>(slot(k, m, j).y);
       TRY(layer_forward(first + j, x, slot(k, m, j), out, recompute && j == n - 1));
     }
-    if (c_->remat_check_m == m && !c_->no_remat) TRY(remat_check(k, n, recompute));
+    if (c_->remat_check_m == m && !c_->no_remat) TRY(remat_check(k, m, n, recompute));
     return GPIPE_OK;
   }
 
   // Debug: keep the first forward's internals of micro-batch m and count the
   // bytes that the re-computation reproduces differently.
-  int remat_check(int k, int n, bool recompute) {
+  int remat_check(int k, int m, int n, bool recompute) {
     const Workspace& w = c_->ws;
     char* saved = ws(w.check) + static_cast<size_t>(k) * c_->max_cell * w.slot_bytes;
-    char* slots = lane_base(lane_of(k)) + w.lane.slots;
+    char* slots = lane_base(lane_of(k, m)) + w.lane.slots;
     for (int j = 0; j < n; ++j) {
       char* sl = slots + static_cast<size_t>(j) * w.slot_bytes;
       const size_t bytes = j == n - 1 ? w.slot.compare_bytes_last : w.slot_bytes;
@@ -886,6 +893,11 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_INFLIGHT:
+      if (value < 1 || value > 2) return c->fail(GPIPE_ERR_INVALID_ARG, "in-flight micro-batches per cell must be 1 or 2");
+      c->inflight = static_cast<int>(value);
+      c->ws_stale = true;
+      break;
     case GPIPE_OPT_SM_SHARE:
       if (value < 25 || value > 800) return c->fail(GPIPE_ERR_INVALID_ARG, "SM share must be 25..800 percent");
       c->sm_share = static_cast<int>(value);

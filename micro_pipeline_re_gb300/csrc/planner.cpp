@@ -127,7 +127,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check,
-                         bool pipelined) {
+                         bool pipelined, int inflight) {
   Workspace w;
   const size_t es = dm.dtype == 0 ? 4 : 2;
   const size_t T = static_cast<size_t>(dm.n) * (dm.kind == 1 ? dm.seq : 1);
@@ -190,7 +190,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   ln.lnp[1] = ltake(w.lnp_bytes);
   ln.bytes = lo;
   w.lane = ln;
-  w.nlanes = pipelined ? K : 1;
+  w.inflight = pipelined ? inflight : 1;
+  w.nlanes = pipelined ? K * w.inflight : 1;
 
   size_t off = 0;
   auto take = [&](size_t bytes) {

@@ -59,7 +59,8 @@ struct Workspace {
   size_t dx0 = 0;                           // M x [Tmb, d]: gradient w.r.t. the embedding output (kind 1)
   size_t bgrad = 0;                         // K x 2 x [Tmb, d]: gradient w.r.t. cell k's input, 2-deep ring
   size_t lanes = 0;                         // nlanes x lane
-  int nlanes = 1;
+  int nlanes = 1;                           // K x inflight when the cells are pipelined, else 1
+  int inflight = 1;                         // micro-batches a cell works on at once (its lanes)
   LaneLayout lane{};
   size_t slot_bytes = 0;
   SlotLayout slot{};
@@ -80,6 +81,6 @@ struct Workspace {
 };
 
 Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check,
-                         bool pipelined);
+                         bool pipelined, int inflight = 1);
 
 }  // namespace gp

@@ -163,10 +163,11 @@ def test_schedules_are_bit_identical(b, wname):
     w = SMALL_LM if wname == "small_lm" else WORKLOADS[wname]
     inp = make_inputs(w)
     outs = []
-    for pipe, conc, graph, pdl in ((0, 0, 1, 0), (1, 1, 1, 1), (1, 0, 1, 1), (0, 1, 1, 1), (1, 1, 0, 1),
-                                   (1, 1, 1, 0)):
-        _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_PIPELINE, pipe), (b.OPT_CONCURRENT, conc),
-                                                     (b.OPT_GRAPH, graph), (b.OPT_PDL, pdl)])
+    for pipe, conc, graph, pdl, inflight in ((0, 0, 1, 0, 1), (1, 1, 1, 1, 1), (1, 0, 1, 1, 1), (0, 1, 1, 1, 1),
+                                             (1, 1, 0, 1, 1), (1, 1, 1, 0, 1), (1, 1, 1, 0, 2), (1, 0, 0, 0, 2)):
+        _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_INFLIGHT, inflight), (b.OPT_PIPELINE, pipe),
+                                                     (b.OPT_CONCURRENT, conc), (b.OPT_GRAPH, graph),
+                                                     (b.OPT_PDL, pdl)])
         outs.append((loss, st.g32.cpu().numpy().copy(), st.p32.cpu().numpy().copy()))
     for o in outs[1:]:
         assert o[0] == outs[0][0]
@@ -224,13 +225,15 @@ def test_loss_near_log_vocab_and_update_from_zero_state(b):
     assert np.all(np.sign(dw[big]) == -np.sign(g[big]))
 
 
-def test_trace_follows_the_pipeline_dependencies(b):
+@pytest.mark.parametrize("inflight", [1, 2])
+def test_trace_follows_the_pipeline_dependencies(b, inflight):
     """With cells as concurrent lanes, GPU timestamps obey the review's pipeline:
     cell k finishes forwarding micro-batch m after cell k-1, the head after the
     last cell, the last cell's backward after the head, cell k-1's backward
-    after cell k's, and every lane takes micro-batches in order."""
+    after cell k's, and every lane takes its micro-batches in order (with two
+    in flight per cell, a cell's lanes take alternate micro-batches)."""
     w = WORKLOADS["lm_small"]
-    gp, st, _, _ = _run(b, w, make_inputs(w), options=[(b.OPT_TRACE, 1)])
+    gp, st, _, _ = _run(b, w, make_inputs(w), options=[(b.OPT_INFLIGHT, inflight), (b.OPT_TRACE, 1)])
     t0, t1, fwd, bwd = gp.trace(st.ws, st.stream)
     K, M = w.K, w.M
     assert t0 <= fwd.min() and max(fwd.max(), bwd[:K].max()) <= t1
@@ -240,8 +243,10 @@ def test_trace_follows_the_pipeline_dependencies(b):
         assert bwd[K - 1, m] >= fwd[K, m]
         for k in range(K - 1, 0, -1):
             assert bwd[k - 1, m] >= bwd[k, m]
-    assert np.all(np.diff(fwd, axis=1) >= 0)
-    assert np.all(np.diff(bwd[:K], axis=1) >= 0)
+    for r in range(inflight):
+        assert np.all(np.diff(fwd[:K, r::inflight], axis=1) >= 0)
+        assert np.all(np.diff(bwd[:K, r::inflight], axis=1) >= 0)
+    assert np.all(np.diff(fwd[K]) >= 0)  # the head lane takes every micro-batch in order
 
 
 @pytest.mark.parametrize("graph", [1, 0])

@@ -122,8 +122,10 @@ def test_clock_model_unequal_cells(binding):
         assert bub == pytest.approx(float(sim["bubble"]), abs=1e-12)
 
 
-def _report(binding, w, K, M, no_remat=False, pipelined=True):
+def _report(binding, w, K, M, no_remat=False, pipelined=True, inflight=1):
     g = binding.GPipe.from_workload(w, K=K, M=M)
+    if inflight != 1:
+        g.set_option(binding.OPT_INFLIGHT, inflight)
     if no_remat:
         g.set_option(binding.OPT_NO_REMAT, 1)
     if not pipelined:
@@ -135,10 +137,23 @@ def _report(binding, w, K, M, no_remat=False, pipelined=True):
 
 def test_memory_within_bound_and_workspace(binding):
     for name, w in WORKLOADS.items():
-        for pipelined in (True, False):
-            peak, bound, ws = _report(binding, w, w.K, w.M, pipelined=pipelined)
+        for pipelined, inflight in ((True, 1), (True, 2), (False, 1)):
+            peak, bound, ws = _report(binding, w, w.K, w.M, pipelined=pipelined, inflight=inflight)
             assert peak <= bound, name
             assert ws >= peak
+
+
+def test_two_in_flight_cost_one_more_cell_workspace_per_cell(binding):
+    """Two micro-batches in flight per cell double the per-lane term of the
+    activation memory (one more cell workspace per cell), nothing else."""
+    w = WORKLOADS["lm_wide"]
+    one, _, _ = _report(binding, w, w.K, w.M)
+    two, _, _ = _report(binding, w, w.K, w.M, inflight=2)
+    serial, _, _ = _report(binding, w, w.K, w.M, pipelined=False)
+    lane = (one - serial) / (w.K - 1)  # one lane's workspace
+    assert two - one == pytest.approx(w.K * lane, rel=1e-6)
+    with pytest.raises(binding.GpipeError):
+        binding.GPipe.from_workload(w).set_option(binding.OPT_INFLIGHT, 3)
 
 
 @pytest.mark.parametrize("pipelined", [False, True])
