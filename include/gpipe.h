@@ -193,9 +193,10 @@ enum {
   GPIPE_OPT_INFLIGHT = 12    /* [1] with lanes: micro-batches each cell works on at
                                 once (1 or 2).  2 gives each cell two lanes that take
                                 its micro-batches in turn (one more cell workspace per
-                                cell) and share one side stream, so every weight
-                                gradient still accumulates in micro-batch order and
-                                results are identical.  Set before gpipe_sizes.      */
+                                cell) and share one side stream (used whatever
+                                GPIPE_OPT_CONCURRENT says), so every weight gradient
+                                still accumulates in micro-batch order and results
+                                are identical.  Set before gpipe_sizes.              */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

@@ -335,7 +335,11 @@ class Executor {
   int side_of(int lane) const { return lane < c_->ws.nlanes ? lane - lane % c_->ws.inflight : lane; }
   char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
-  cudaStream_t side(int lane) const { return c_->concurrent ? c_->lane_side[side_of(lane)] : c_->lane_main[lane]; }
+  // Weight-gradient work goes to a side stream when CONCURRENT is on, and
+  // always with two micro-batches in flight (the cell's two lanes must not
+  // accumulate into the same gradients from two streams).
+  bool use_side() const { return c_->concurrent || c_->ws.inflight > 1; }
+  cudaStream_t side(int lane) const { return use_side() ? c_->lane_side[side_of(lane)] : c_->lane_main[lane]; }
   cudaStream_t st() const { return cur_ ? cur_ : c_->lane_main[cur_lane_]; }
   int cuda_ok(cudaError_t e, const char* what) {
     return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -352,17 +356,17 @@ class Executor {
   }
   // a lane's side stream starts after everything issued so far on its main stream
   int fork(int lane) {
-    if (!c_->concurrent) return GPIPE_OK;
+    if (!use_side()) return GPIPE_OK;
     TRY(cuda_ok(cudaEventRecord(c_->lane_ev[lane][EV_FORK], main_s(lane)), "event record"));
     return cuda_ok(cudaStreamWaitEvent(side(lane), c_->lane_ev[lane][EV_FORK], 0), "stream wait");
   }
   int mark(int lane, int e) {
-    if (!c_->concurrent) return GPIPE_OK;
+    if (!use_side()) return GPIPE_OK;
     rec_[lane][e] = true;
     return cuda_ok(cudaEventRecord(c_->lane_ev[lane][e], side(lane)), "event record");
   }
   int join(int lane, int e) {
-    if (!c_->concurrent || !rec_[lane][e]) return GPIPE_OK;
+    if (!use_side() || !rec_[lane][e]) return GPIPE_OK;
     return cuda_ok(cudaStreamWaitEvent(main_s(lane), c_->lane_ev[lane][e], 0), "stream wait");
   }
   int join_all(int lane) {

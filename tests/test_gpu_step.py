@@ -149,10 +149,10 @@ def test_steps_are_bit_reproducible_and_graph_equals_direct(b):
     for graph in (1, 1, 0):
         gp, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_GRAPH, graph)])
         outs.append((loss, st.g32.cpu().numpy().copy(), st.p32.cpu().numpy().copy()))
-    for o in outs[1:]:
-        assert o[0] == outs[0][0]
-        assert np.array_equal(o[1], outs[0][1])
-        assert np.array_equal(o[2], outs[0][2])
+    for i, o in enumerate(outs[1:], 1):
+        assert o[0] == outs[0][0], i
+        assert np.array_equal(o[1], outs[0][1]), i
+        assert np.array_equal(o[2], outs[0][2]), i
 
 
 @pytest.mark.parametrize("wname", ["small_lm", "tiny_ffn", "lm_small"])
@@ -169,10 +169,10 @@ def test_schedules_are_bit_identical(b, wname):
                                                      (b.OPT_CONCURRENT, conc), (b.OPT_GRAPH, graph),
                                                      (b.OPT_PDL, pdl)])
         outs.append((loss, st.g32.cpu().numpy().copy(), st.p32.cpu().numpy().copy()))
-    for o in outs[1:]:
-        assert o[0] == outs[0][0]
-        assert np.array_equal(o[1], outs[0][1])
-        assert np.array_equal(o[2], outs[0][2])
+    for i, o in enumerate(outs[1:], 1):
+        assert o[0] == outs[0][0], i
+        assert np.array_equal(o[1], outs[0][1]), i
+        assert np.array_equal(o[2], outs[0][2]), i
 
 
 def test_no_rematerialisation_mode_is_identical(b):
