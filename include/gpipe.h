@@ -187,11 +187,14 @@ enum {
                                 event nodes of the step's graph); read with
                                 gpipe_kernel_times                                   */
   GPIPE_OPT_SM_SHARE = 11,   /* [100] with lanes, a GEMM's grid is this percentage of
-                                its fair share of the SMs (SMs / (lanes busy at its
-                                tick of the schedule + 1)), 25..800; the tile
+                                its fair share of the SMs (SMs / (cells busy at its
+                                tick of the schedule + 1), doubled for GEMMs of at
+                                most 4 x that many 128 x 128 tiles), 25..800; the tile
                                 choice follows the grid, results stay identical    */
-  GPIPE_OPT_INFLIGHT = 12    /* [1] with lanes: micro-batches each cell works on at
-                                once (1 or 2).  2 gives each cell two lanes that take
+  GPIPE_OPT_INFLIGHT = 12    /* [0] with lanes: micro-batches each cell works on at
+                                once: 1, 2, or 0 = 2 when a micro-batch's FFN GEMM
+                                (tokens x d x ffn) is at most 2^30 multiply-adds,
+                                else 1.  2 gives each cell two lanes that take
                                 its micro-batches in turn (one more cell workspace per
                                 cell) and share one side stream (used whatever
                                 GPIPE_OPT_CONCURRENT says), so every weight gradient

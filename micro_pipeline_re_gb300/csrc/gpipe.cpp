@@ -80,7 +80,14 @@ struct gpipe_ctx {
   bool pipelined = true;   // cells run as concurrent lanes (the review's pipeline on one GPU)
   bool pdl = false;        // kernels may launch while their predecessor drains (measured slower with lanes)
   bool trace = false;      // stamp the GPU clock at the end of every (cell, micro-batch, phase)
-  int inflight = 1;        // with lanes: micro-batches each cell works on at once (1 or 2)
+  int inflight = 0;        // with lanes: micro-batches each cell works on at once (1, 2; 0: by size)
+  // Two in flight when a micro-batch's FFN GEMM is small enough (tokens x d x
+  // ffn <= 2^30) that its kernels are bound by latency rather than throughput.
+  int inflight_eff() const {
+    if (inflight) return inflight;
+    const double work = static_cast<double>(Tmb()) * dm.d * (dm.ffn > 0 ? dm.ffn : dm.d);
+    return work <= 1073741824.0 ? 2 : 1;
+  }
   int ktime = 0;           // e+1: time every GEMM launch with epilogue e (event pairs)
   int sm_share = 100;      // percent of a GEMM's fair share of the SMs (with lanes)
   std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
@@ -114,9 +121,10 @@ struct gpipe_ctx {
   }
   void refresh_ws() {
     if (ws_stale) {
-      const bool lanes = pipelined && K * inflight < kMaxLanes;
+      const int nin = inflight_eff();
+      const bool lanes = pipelined && K * nin < kMaxLanes;
       ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat, lanes,
-                          lanes ? inflight : 1);
+                          lanes ? nin : 1);
       ws_stale = false;
     }
   }
@@ -479,7 +487,7 @@ class Executor {
     if (c_->nstreams() > 1) {
       // a GEMM of few output tiles is bound by latency, not by its share of
       // the tensor cores: let it spread over twice the share
-      int share = num_sms() * c_->sm_share / (100 * (busy_ * c_->ws.inflight + 1));
+      int share = num_sms() * c_->sm_share / (100 * (busy_ + 1));
       const int64_t tiles = static_cast<int64_t>((M + 127) / 128) * ((N + 127) / 128);
       if (tiles <= 4 * static_cast<int64_t>(share)) share *= 2;
       g.sm_budget = share < 1 ? 1 : (share > num_sms() ? num_sms() : share);
@@ -898,7 +906,8 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
     case GPIPE_OPT_INFLIGHT:
-      if (value < 1 || value > 2) return c->fail(GPIPE_ERR_INVALID_ARG, "in-flight micro-batches per cell must be 1 or 2");
+      if (value < 0 || value > 2)
+        return c->fail(GPIPE_ERR_INVALID_ARG, "in-flight micro-batches per cell must be 0 (by size), 1 or 2");
       c->inflight = static_cast<int>(value);
       c->ws_stale = true;
       break;

@@ -124,8 +124,7 @@ def test_clock_model_unequal_cells(binding):
 
 def _report(binding, w, K, M, no_remat=False, pipelined=True, inflight=1):
     g = binding.GPipe.from_workload(w, K=K, M=M)
-    if inflight != 1:
-        g.set_option(binding.OPT_INFLIGHT, inflight)
+    g.set_option(binding.OPT_INFLIGHT, inflight)
     if no_remat:
         g.set_option(binding.OPT_NO_REMAT, 1)
     if not pipelined:
@@ -154,6 +153,12 @@ def test_two_in_flight_cost_one_more_cell_workspace_per_cell(binding):
     assert two - one == pytest.approx(w.K * lane, rel=1e-6)
     with pytest.raises(binding.GpipeError):
         binding.GPipe.from_workload(w).set_option(binding.OPT_INFLIGHT, 3)
+    # by size (the default): two in flight for the small LM, one for the wide one
+    small = WORKLOADS["lm_small"]
+    auto_small, _, _ = _report(binding, small, small.K, small.M, inflight=0)
+    two_small, _, _ = _report(binding, small, small.K, small.M, inflight=2)
+    auto_wide, _, _ = _report(binding, w, w.K, w.M, inflight=0)
+    assert auto_small == two_small and auto_wide == one
 
 
 @pytest.mark.parametrize("pipelined", [False, True])
