@@ -192,11 +192,12 @@ enum {
                                 most 4 x that many 128 x 128 tiles), 25..800; the tile
                                 choice follows the grid, results stay identical    */
   GPIPE_OPT_INFLIGHT = 12    /* [0] with lanes: micro-batches each cell works on at
-                                once: 1, 2, or 0 = 2 when a micro-batch's FFN GEMM
+                                once: 1..4, or 0 = 2 when a micro-batch's FFN GEMM
                                 (tokens x d x ffn) is at most 2^30 multiply-adds,
-                                else 1.  2 gives each cell two lanes that take
-                                its micro-batches in turn (one more cell workspace per
-                                cell) and share one side stream (used whatever
+                                else 1.  S > 1 gives each cell S lanes that take
+                                its micro-batches in turn (S-1 more cell workspaces
+                                per cell, and a gradient ring S deep between
+                                neighbouring cells) and share one side stream (used whatever
                                 GPIPE_OPT_CONCURRENT says), so every weight gradient
                                 still accumulates in micro-batch order and results
                                 are identical.  Set before gpipe_sizes.              */

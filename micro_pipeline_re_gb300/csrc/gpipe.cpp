@@ -97,7 +97,9 @@ struct gpipe_ctx {
   static constexpr int kLaneEvents = 11;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
-  cudaEvent_t ev_origin = nullptr, ev_fwd[kMaxLanes] = {}, ev_bdone[kMaxLanes][2] = {}, ev_bfree[kMaxLanes][2] = {},
+  static constexpr int kRing = 4;  // deepest gradient ring between neighbouring cells (= most in flight)
+  cudaEvent_t ev_origin = nullptr, ev_fwd[kMaxLanes] = {}, ev_bdone[kMaxLanes][kRing] = {},
+              ev_bfree[kMaxLanes][kRing] = {},
               ev_lane_end[kMaxLanes] = {};
   std::vector<cudaEvent_t> ev_hdone;  // per micro-batch: the head has written the last cell's output gradient
   // streams in use: one pair per lane, plus the head's pair when the cells are pipelined
@@ -150,9 +152,10 @@ struct gpipe_ctx {
            mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
       for (int e = 0; e < kLaneEvents && ok; ++e) ok = mk_ev(lane_ev[i][e]);
     }
-    for (int k = 0; k < K && k < kMaxLanes && ok; ++k)
-      ok = mk_ev(ev_bdone[k][0]) && mk_ev(ev_bdone[k][1]) && mk_ev(ev_bfree[k][0]) && mk_ev(ev_bfree[k][1]) &&
-           mk_ev(ev_fwd[k]);
+    for (int k = 0; k < K && k < kMaxLanes && ok; ++k) {
+      for (int r = 0; r < kRing && ok; ++r) ok = mk_ev(ev_bdone[k][r]) && mk_ev(ev_bfree[k][r]);
+      ok = ok && mk_ev(ev_fwd[k]);
+    }
     return ok ? GPIPE_OK : fail(GPIPE_ERR_CUDA, "cannot create the lane streams/events");
   }
   // The event pair of the next timed launch (created on first use).
@@ -254,7 +257,7 @@ class Executor {
     }
     // phase 2: backward with re-computation
     for (int m = 0; m < M; ++m) {
-      const int p = m & 1;
+      const int p = m % c_->ws.ring;
       for (int k = K - 1; k >= 0; --k) {
         const int lk = lane_of(k, m);
         cur_lane_ = lk;
@@ -331,8 +334,8 @@ class Executor {
   int ln_buf_[gpipe_ctx::kMaxLanes] = {};  // per lane: the LayerNorm-backward partial buffer to use next
   bool rec_[gpipe_ctx::kMaxLanes][EV_COUNT] = {};
   bool fwd_rec_[gpipe_ctx::kMaxLanes] = {};
-  bool bdone_rec_[gpipe_ctx::kMaxLanes][2] = {};
-  bool bfree_rec_[gpipe_ctx::kMaxLanes][2] = {};
+  bool bdone_rec_[gpipe_ctx::kMaxLanes][gpipe_ctx::kRing] = {};
+  bool bfree_rec_[gpipe_ctx::kMaxLanes][gpipe_ctx::kRing] = {};
 
   // Lane of cell k for micro-batch m: with lanes, cell k owns lanes
   // k*inflight .. k*inflight + inflight-1 and takes its micro-batches in turn.
@@ -426,7 +429,9 @@ class Executor {
     return ws(c_->ws.stash) + (static_cast<size_t>(k) * c_->M + m) * c_->ws.stash_bytes;
   }
   char* dx0(int m) const { return ws(c_->ws.dx0) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
-  char* bgrad(int k, int p) const { return ws(c_->ws.bgrad) + (static_cast<size_t>(k) * 2 + p) * c_->ws.stash_bytes; }
+  char* bgrad(int k, int p) const {
+    return ws(c_->ws.bgrad) + (static_cast<size_t>(k) * c_->ws.ring + p) * c_->ws.stash_bytes;
+  }
   char* lane_base(int lane) const { return ws(c_->ws.lanes) + static_cast<size_t>(lane) * c_->ws.lane.bytes; }
   char* lbuf(int lane, int i) const { return lane_base(lane) + (i == 0 ? c_->ws.lane.g0 : c_->ws.lane.g1); }
   const void* cell_input(int k, int m) const {
@@ -906,8 +911,8 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
     case GPIPE_OPT_INFLIGHT:
-      if (value < 0 || value > 2)
-        return c->fail(GPIPE_ERR_INVALID_ARG, "in-flight micro-batches per cell must be 0 (by size), 1 or 2");
+      if (value < 0 || value > gpipe_ctx::kRing)
+        return c->fail(GPIPE_ERR_INVALID_ARG, "in-flight micro-batches per cell must be 0 (by size) or 1..4");
       c->inflight = static_cast<int>(value);
       c->ws_stale = true;
       break;
@@ -994,8 +999,11 @@ void gpipe_destroy(gpipe_ctx* c) {
     if (c->lane_side[i]) cudaStreamDestroy(c->lane_side[i]);
     for (auto& e : c->lane_ev[i])
       if (e) cudaEventDestroy(e);
-    for (cudaEvent_t e : {c->ev_fwd[i], c->ev_bdone[i][0], c->ev_bdone[i][1], c->ev_bfree[i][0], c->ev_bfree[i][1],
-                          c->ev_lane_end[i]})
+    for (int r = 0; r < gpipe_ctx::kRing; ++r) {
+      if (c->ev_bdone[i][r]) cudaEventDestroy(c->ev_bdone[i][r]);
+      if (c->ev_bfree[i][r]) cudaEventDestroy(c->ev_bfree[i][r]);
+    }
+    for (cudaEvent_t e : {c->ev_fwd[i], c->ev_lane_end[i]})
       if (e) cudaEventDestroy(e);
   }
   if (c->ev_origin) cudaEventDestroy(c->ev_origin);

@@ -202,7 +202,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.stash_bytes = Tmb * d * es;
   w.stash = take(static_cast<size_t>(K + 1) * M * w.stash_bytes);
   w.dx0 = take(dm.kind == 1 ? static_cast<size_t>(M) * w.stash_bytes : 0);
-  w.bgrad = take(static_cast<size_t>(K) * 2 * w.stash_bytes);
+  w.ring = w.inflight > 2 ? w.inflight : 2;
+  w.bgrad = take(static_cast<size_t>(K) * w.ring * w.stash_bytes);
   w.lanes = take(static_cast<size_t>(w.nlanes) * ln.bytes);
   w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
   w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
@@ -233,7 +234,7 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   // per lane one cell of Lc layers of kept internals for one micro-batch plus
   // that lane's gradient buffers (proportional to (L/K)(N/M)); the head's
   // logits and the per-row losses.
-  const size_t boundary = static_cast<size_t>(K + 3) * T * d * es + static_cast<size_t>(K) * 2 * Tmb * d * es;
+  const size_t boundary = static_cast<size_t>(K + 3) * T * d * es + static_cast<size_t>(K) * w.ring * Tmb * d * es;
   const size_t per_lane = ln.bytes + 4096;
   const size_t head =
       dm.kind == 1 ? Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + w.scratch_bytes + 2 * w.lnp_bytes + 8192

@@ -57,7 +57,8 @@ struct LaneLayout {
 struct Workspace {
   size_t stash = 0, stash_bytes = 0;        // (K+1) x M boundary tensors [Tmb, d]
   size_t dx0 = 0;                           // M x [Tmb, d]: gradient w.r.t. the embedding output (kind 1)
-  size_t bgrad = 0;                         // K x 2 x [Tmb, d]: gradient w.r.t. cell k's input, 2-deep ring
+  size_t bgrad = 0;                         // K x ring x [Tmb, d]: gradient w.r.t. cell k's input
+  int ring = 2;                             // depth of that ring: max(2, micro-batches in flight per cell)
   size_t lanes = 0;                         // nlanes x lane
   int nlanes = 1;                           // K x inflight when the cells are pipelined, else 1
   int inflight = 1;                         // micro-batches a cell works on at once (its lanes)

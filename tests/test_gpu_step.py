@@ -164,7 +164,8 @@ def test_schedules_are_bit_identical(b, wname):
     inp = make_inputs(w)
     outs = []
     for pipe, conc, graph, pdl, inflight in ((0, 0, 1, 0, 1), (1, 1, 1, 1, 1), (1, 0, 1, 1, 1), (0, 1, 1, 1, 1),
-                                             (1, 1, 0, 1, 1), (1, 1, 1, 0, 1), (1, 1, 1, 0, 2), (1, 0, 0, 0, 2)):
+                                             (1, 1, 0, 1, 1), (1, 1, 1, 0, 1), (1, 1, 1, 0, 2), (1, 0, 0, 0, 2),
+                                             (1, 1, 1, 0, 3), (1, 1, 1, 0, 4)):
         _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_INFLIGHT, inflight), (b.OPT_PIPELINE, pipe),
                                                      (b.OPT_CONCURRENT, conc), (b.OPT_GRAPH, graph),
                                                      (b.OPT_PDL, pdl)])
@@ -225,7 +226,7 @@ def test_loss_near_log_vocab_and_update_from_zero_state(b):
     assert np.all(np.sign(dw[big]) == -np.sign(g[big]))
 
 
-@pytest.mark.parametrize("inflight", [1, 2])
+@pytest.mark.parametrize("inflight", [1, 2, 4])
 def test_trace_follows_the_pipeline_dependencies(b, inflight):
     """With cells as concurrent lanes, GPU timestamps obey the review's pipeline:
     cell k finishes forwarding micro-batch m after cell k-1, the head after the

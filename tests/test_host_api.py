@@ -152,13 +152,17 @@ def test_two_in_flight_cost_one_more_cell_workspace_per_cell(binding):
     lane = (one - serial) / (w.K - 1)  # one lane's workspace
     assert two - one == pytest.approx(w.K * lane, rel=1e-6)
     with pytest.raises(binding.GpipeError):
-        binding.GPipe.from_workload(w).set_option(binding.OPT_INFLIGHT, 3)
+        binding.GPipe.from_workload(w).set_option(binding.OPT_INFLIGHT, 5)
     # by size (the default): two in flight for the small LM, one for the wide one
     small = WORKLOADS["lm_small"]
     auto_small, _, _ = _report(binding, small, small.K, small.M, inflight=0)
     two_small, _, _ = _report(binding, small, small.K, small.M, inflight=2)
     auto_wide, _, _ = _report(binding, w, w.K, w.M, inflight=0)
     assert auto_small == two_small and auto_wide == one
+    # S in flight: S-1 more lane workspaces per cell, and the gradient ring S deep
+    four, _, _ = _report(binding, w, w.K, w.M, inflight=4)
+    stash = w.tokens // w.M * w.d * 2
+    assert four - one == pytest.approx(3 * w.K * lane + 2 * w.K * stash, rel=1e-6)
 
 
 @pytest.mark.parametrize("pipelined", [False, True])
