@@ -167,26 +167,36 @@ def cfg(w, args):
             "l2": "working set larger than L2 (parameters, gradients and RMSProp state alone exceed 129 MB)"}
 
 
-def gemm_roofline(b, w, peaks, eager_launches=5, reps=100, shape=None):
-    """Time the dominant kernel class (tcgen05 GEMM, FFN first projection with
-    bias+GELU at the step's micro-batch shape) with CUDA events around a CUDA
-    graph of `reps` launches on the launching stream (host launch cost is not
-    in the number)."""
+def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
+    """Time one GEMM of the library alone: CUDA events around a CUDA graph of
+    `reps` back-to-back launches on the launching stream (host launch cost is
+    not in the number; operands stay in L2 where they fit).  epi 1: the FFN
+    first projection (K-major operands, bias + GELU, two bf16 outputs); epi 3: a
+    weight gradient (MN-major operands, fp32 TMA reduce-add, bias gradient)."""
     import torch
-    T, d, f = w.tokens // w.M, w.d, w.ffn
-    if shape is not None:
-        T, f, d = shape  # M, N, K
-    A = torch.randn(T, d, device="cuda").to(torch.bfloat16)
-    Bw = torch.randn(f, d, device="cuda").to(torch.bfloat16)
-    bias = torch.zeros(f, device="cuda")
-    Z = torch.empty(T, f, device="cuda", dtype=torch.bfloat16)
-    G = torch.empty(T, f, device="cuda", dtype=torch.bfloat16)
+    M, N, K = shape
+    bf = torch.bfloat16
+    if epi == 3:
+        A = torch.randn(K, M, device="cuda").to(bf)
+        Bw = torch.randn(K, N, device="cuda").to(bf)
+        C = torch.zeros(M, N, device="cuda")
+        vec = torch.zeros(M, device="cuda")
+        args = (1, M, N, K, A.data_ptr(), M, 0, Bw.data_ptr(), N, 0, 3, C.data_ptr(), N, vec.data_ptr(), None, 0,
+                None, None, 0)
+        name = f"weight-gradient GEMM (fp32 reduce-add + bias gradient) {M}x{N}x{K}"
+    else:
+        A = torch.randn(M, K, device="cuda").to(bf)
+        Bw = torch.randn(N, K, device="cuda").to(bf)
+        vec = torch.zeros(N, device="cuda")
+        Z = torch.empty(M, N, device="cuda", dtype=bf)
+        G = torch.empty(M, N, device="cuda", dtype=bf)
+        args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), K, 1, 1, Z.data_ptr(), N, vec.data_ptr(), None, 0,
+                G.data_ptr(), None, 0)
+        name = f"FFN first projection GEMM (bias + GELU) {M}x{N}x{K}"
     lib = b.lib()
 
     def launch():
-        rc = lib.gpipe_op_gemm(1, T, f, d, A.data_ptr(), d, 1, Bw.data_ptr(), d, 1, 1, Z.data_ptr(), f,
-                               bias.data_ptr(), None, 0, G.data_ptr(), None, 0,
-                               torch.cuda.current_stream().cuda_stream)
+        rc = lib.gpipe_op_gemm(*args, torch.cuda.current_stream().cuda_stream)
         assert rc == 0
     for _ in range(eager_launches):
         launch()
@@ -206,12 +216,10 @@ def gemm_roofline(b, w, peaks, eager_launches=5, reps=100, shape=None):
     e.record()
     torch.cuda.synchronize()
     dt = s.elapsed_time(e) / 1e3 / reps
-    flops = 2.0 * T * f * d
-    ach = flops / dt / 1e12
-    return {"bound": "tensor", "kernel": f"tc_gemm bias+GELU {T}x{f}x{d}", "achieved": ach, "peak": peaks["bf16"],
-            "unit": "TFLOP/s", "frac": ach / peaks["bf16"], "traffic": None,
+    ach = 2.0 * M * N * K / dt / 1e12
+    return {"kernel": name, "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": ach / peaks["bf16"],
             "peak_source": peaks["source"] + " (burst)", "avg_launch_us": dt * 1e6,
-            "timing": f"CUDA events around a graph of {reps} back-to-back launches"}
+            "timing": f"CUDA events around a graph of {reps} back-to-back launches of this GEMM alone"}
 
 
 # The kernel class the roofline reports: the fp32 weight-gradient GEMMs
@@ -220,22 +228,41 @@ def gemm_roofline(b, w, peaks, eager_launches=5, reps=100, shape=None):
 ROOF_EPI = 3
 
 
-def live_roofline(kt, peaks, iso):
-    """Roofline of the dominant kernel class from its launches in one step:
-    events bracket each launch on the stream it runs on (event nodes of the
-    step's graph), so durations include the concurrency of the real step."""
-    ms, fl = kt
+# Per-launch DRAM traffic of the roofline GEMM, from one ncu capture of the
+# same shape and epilogue alone (`--probe-gemm`; cold L2, so an upper bound of
+# what the launch reads and writes inside the step): (M, N, K) -> bytes.
+ROOF_TRAFFIC = {}
+
+
+def live_roofline(kt, peaks, b):
+    """Roofline of the dominant kernel: of the launches of the roofline class in
+    one step (events bracket each launch on the stream it runs on, as event
+    nodes of the step's graph, so durations include the concurrency of the real
+    step), the GEMM shape with the largest total time."""
+    ms, fl, mnk = kt
     if ms.size == 0:
         return None
-    ach = float(fl.sum()) / (float(ms.sum()) / 1e3) / 1e12
-    return {"bound": "tensor", "kernel": "tcgen05 GEMM, fp32 weight-gradient accumulation (TMA reduce-add)",
+    groups = {}
+    for t, f, s in zip(ms, fl, mnk):
+        g = groups.setdefault(tuple(int(x) for x in s), [0.0, 0.0, 0])
+        g[0] += float(t)
+        g[1] += float(f)
+        g[2] += 1
+    shape, (tot_ms, tot_fl, n) = max(groups.items(), key=lambda kv: kv[1][0])
+    ach = tot_fl / (tot_ms / 1e3) / 1e12
+    cls = float(fl.sum()) / (float(ms.sum()) / 1e3) / 1e12
+    return {"bound": "tensor",
+            "kernel": f"tcgen05 weight-gradient GEMM {shape[0]}x{shape[1]}x{shape[2]} (MN-major operands, fp32 "
+                      f"TMA reduce-add, bias gradient)",
             "achieved": ach, "peak": peaks["bf16_sus"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_sus"],
-            "traffic": None, "peak_source": peaks["source"] + " (sustained: the kernel runs inside a long step)",
-            "launches_per_step": int(ms.size), "avg_launch_us": float(ms.mean()) * 1e3,
-            "algorithmic_flop_per_launch": float(fl.mean()),
-            "timing": "CUDA events around every launch of the class in one step (a pass after the timed region, "
-                      "same graph plus the event nodes), on the stream it runs on",
-            "isolated": iso}
+            "traffic": ROOF_TRAFFIC.get(shape), "peak_source": peaks["source"] + " (sustained: the kernel runs "
+                                                                              "inside a long step)",
+            "algorithmic_flop_per_launch": tot_fl / n, "launches_per_step": n, "avg_launch_us": tot_ms / n * 1e3,
+            "timing": "CUDA events around every launch of the class in one step (a pass after the timed region: "
+                      "the same graph plus the event nodes), on the stream it runs on",
+            "class": {"launches_per_step": int(ms.size), "achieved": cls, "frac": cls / peaks["bf16_sus"],
+                      "shapes": len(groups)},
+            "isolated": gemm_roofline(b, peaks, shape, ROOF_EPI)}
 
 
 def run_ours(args, w):
@@ -310,10 +337,9 @@ def run_ours(args, w):
         st.step(want_loss=False)
     for _ in range(min(args.steps, 5)):
         st.step(want_loss=False)
-    kt = gp.kernel_times()  # the launches of the last of these steps
+    kt = gp.kernel_times(with_shapes=True)  # the launches of the last of these steps
     gp.set_option(b.OPT_KERNEL_TIMES, 0)
-    iso = gemm_roofline(b, w, peaks)
-    roof = live_roofline(kt, peaks, iso)
+    roof = live_roofline(kt, peaks, b)
     peak_act, bound = gp.memory_report()
     if rank == 0:
         cpu = None
@@ -397,6 +423,7 @@ def main():
     ap.add_argument("--probe-gemm", action="store_true",
                     help="only run the roofline GEMM (5 eager launches, then a timed graph); for profilers")
     ap.add_argument("--shape", default=None, help="M,N,K for --probe-gemm (default: the workload's FFN1)")
+    ap.add_argument("--epi", type=int, default=1, help="--probe-gemm epilogue: 1 bias+GELU, 3 weight gradient")
     ap.add_argument("--reps", type=int, default=100)
     ap.add_argument("--sweep", action="store_true",
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
@@ -408,8 +435,8 @@ def main():
         from micro_pipeline_re_gb300._build import build as _build
         _build()
         from micro_pipeline_re_gb300 import binding as b
-        shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else None
-        print(json.dumps(gemm_roofline(b, w, load_peaks(), reps=args.reps, shape=shape)), flush=True)
+        shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else (w.tokens // w.M, w.ffn, w.d)
+        print(json.dumps(gemm_roofline(b, load_peaks(), shape, args.epi, reps=args.reps)), flush=True)
         return
     if args.sweep:
         run_sweep(args)

@@ -226,10 +226,11 @@ int gpipe_trace(gpipe_ctx* ctx, void* workspace, void* stream, uint64_t* host_ou
 
 /* Durations of the GEMM launches that GPIPE_OPT_KERNEL_TIMES selected, in the
  * last step taken (waits for that step's events): ms_out[i] = event time of
- * launch i in issue order, flops_out[i] = its algorithmic work 2*M*N*K.  Writes
- * min(count, n) entries (either array may be NULL) and returns n, the number of
- * timed launches per step (0 when the option is off), or a negative error. */
-int gpipe_kernel_times(gpipe_ctx* ctx, float* ms_out, double* flops_out, int count);
+ * launch i in issue order, flops_out[i] = its algorithmic work 2*M*N*K,
+ * mnk_out[3i..3i+2] = its M, N, K.  Writes min(count, n) entries (any array may
+ * be NULL) and returns n, the number of timed launches per step (0 when the
+ * option is off), or a negative error. */
+int gpipe_kernel_times(gpipe_ctx* ctx, float* ms_out, double* flops_out, int32_t* mnk_out, int count);
 
 /* Number of kernels one step launches. */
 int64_t gpipe_launches_per_step(const gpipe_ctx* ctx);

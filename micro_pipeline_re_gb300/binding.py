@@ -60,7 +60,8 @@ _SIGS = {
     "gpipe_loss_rows": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float), c_size_t]),
     "gpipe_launches_per_step": (c_int64, [c_void_p]),
     "gpipe_trace": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_uint64), c_size_t]),
-    "gpipe_kernel_times": (c_int, [c_void_p, POINTER(ctypes.c_float), POINTER(ctypes.c_double), c_int]),
+    "gpipe_kernel_times": (c_int, [c_void_p, POINTER(ctypes.c_float), POINTER(ctypes.c_double),
+                                   POINTER(ctypes.c_int32), c_int]),
     "gpipe_last_error": (ctypes.c_char_p, [c_void_p]),
     "gpipe_destroy": (None, [c_void_p]),
     "gpipe_op_gemm": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_int64, c_int, c_void_p, c_int64, c_int, c_int,
@@ -210,18 +211,22 @@ class GPipe:
         _check(lib().gpipe_loss_rows(self.h, _ptr(workspace), stream, out, count), self.h)
         return np.frombuffer(out, dtype=np.float32).copy()
 
-    def kernel_times(self):
-        """(ms, flops) arrays of the GEMM launches selected by OPT_KERNEL_TIMES in
-        the last step (waits for its events)."""
-        n = lib().gpipe_kernel_times(self.h, None, None, 0)
+    def kernel_times(self, with_shapes=False):
+        """(ms, flops[, mnk]) arrays of the GEMM launches selected by
+        OPT_KERNEL_TIMES in the last step (waits for its events)."""
+        n = lib().gpipe_kernel_times(self.h, None, None, None, 0)
         if n < 0:
             _check(n, self.h)
         ms = (ctypes.c_float * max(n, 1))()
         fl = (ctypes.c_double * max(n, 1))()
-        r = lib().gpipe_kernel_times(self.h, ms, fl, n)
+        mnk = (ctypes.c_int32 * max(3 * n, 1))()
+        r = lib().gpipe_kernel_times(self.h, ms, fl, mnk, n)
         if r < 0:
             _check(r, self.h)
-        return np.frombuffer(ms, dtype=np.float32)[:n].copy(), np.frombuffer(fl, dtype=np.float64)[:n].copy()
+        out = (np.frombuffer(ms, dtype=np.float32)[:n].copy(), np.frombuffer(fl, dtype=np.float64)[:n].copy())
+        if with_shapes:
+            out += (np.frombuffer(mnk, dtype=np.int32)[:3 * n].reshape(n, 3).copy(),)
+        return out
 
     def trace(self, workspace, stream=None):
         """(start, end, fwd[c][m], bwd[c][m]) in ns; c = 0..K (K: the head)."""

@@ -92,6 +92,7 @@ struct gpipe_ctx {
   int sm_share = 100;      // percent of a GEMM's fair share of the SMs (with lanes)
   std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
   std::vector<double> kt_flops;
+  std::vector<int32_t> kt_mnk;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
   static constexpr int kMaxLanes = 128;
   static constexpr int kLaneEvents = 11;
@@ -159,14 +160,20 @@ struct gpipe_ctx {
     return ok ? GPIPE_OK : fail(GPIPE_ERR_CUDA, "cannot create the lane streams/events");
   }
   // The event pair of the next timed launch (created on first use).
-  int kt_next(double flops, cudaEvent_t* e0, cudaEvent_t* e1) {
+  int kt_next(int M, int N, int K, cudaEvent_t* e0, cudaEvent_t* e1) {
     while (kt_ev.size() < static_cast<size_t>(2 * kt_n + 2)) {
       cudaEvent_t e = nullptr;
       if (cudaEventCreate(&e) != cudaSuccess) return fail(GPIPE_ERR_CUDA, "cannot create a timing event");
       kt_ev.push_back(e);
     }
-    if (kt_flops.size() <= static_cast<size_t>(kt_n)) kt_flops.resize(kt_n + 1);
-    kt_flops[kt_n] = flops;
+    if (kt_flops.size() <= static_cast<size_t>(kt_n)) {
+      kt_flops.resize(kt_n + 1);
+      kt_mnk.resize(3 * (kt_n + 1));
+    }
+    kt_flops[kt_n] = 2.0 * M * N * K;
+    kt_mnk[3 * kt_n] = M;
+    kt_mnk[3 * kt_n + 1] = N;
+    kt_mnk[3 * kt_n + 2] = K;
     *e0 = kt_ev[2 * kt_n];
     *e1 = kt_ev[2 * kt_n + 1];
     ++kt_n;
@@ -501,7 +508,7 @@ class Executor {
     }
     if (c_->ktime != epi + 1) return launch_gemm(g, st());
     cudaEvent_t e0, e1;
-    TRY(c_->kt_next(2.0 * M * N * K, &e0, &e1));
+    TRY(c_->kt_next(M, N, K, &e0, &e1));
     TRY(record_timed(e0));
     TRY(launch_gemm(g, st()));
     return record_timed(e1);
@@ -930,7 +937,7 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
   return GPIPE_OK;
 }
 
-int gpipe_kernel_times(gpipe_ctx* c, float* ms_out, double* flops_out, int count) {
+int gpipe_kernel_times(gpipe_ctx* c, float* ms_out, double* flops_out, int32_t* mnk_out, int count) {
   if (!c || count < 0) return GPIPE_ERR_INVALID_ARG;
   const int n = c->ktime ? c->kt_n : 0;
   for (int i = 0; i < n && i < count; ++i) {
@@ -940,6 +947,8 @@ int gpipe_kernel_times(gpipe_ctx* c, float* ms_out, double* flops_out, int count
     if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, std::string("kernel times: ") + cudaGetErrorString(ce));
     if (ms_out) ms_out[i] = t;
     if (flops_out) flops_out[i] = c->kt_flops[i];
+    if (mnk_out)
+      for (int j = 0; j < 3; ++j) mnk_out[3 * i + j] = c->kt_mnk[3 * i + j];
   }
   return n;
 }

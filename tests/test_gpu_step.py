@@ -260,9 +260,10 @@ def test_kernel_times_bracket_the_selected_gemms(b, graph):
     opts = [(b.OPT_GRAPH, graph)]
     gp0, st0, _, _ = _run(b, w, inp, steps=2, options=opts)
     gp1, st1, _, _ = _run(b, w, inp, steps=2, options=opts + [(b.OPT_KERNEL_TIMES, b.EPI_BIAS_GELU + 1)])
-    ms, fl = gp1.kernel_times()
+    ms, fl, mnk = gp1.kernel_times(with_shapes=True)
     T = w.n * w.seq // w.M
     assert len(ms) == 2 * w.L * w.M
+    assert np.all(mnk == np.array([T, w.ffn, w.d]))
     assert np.all(ms > 0) and np.all(ms < 100)
     assert np.all(fl == 2.0 * T * w.ffn * w.d)
     assert np.array_equal(st0.host(st0.p32), st1.host(st1.p32))
