@@ -15,8 +15,11 @@
 //                     128B-swizzled staging box; one thread TMA-stores each
 //                     box (staging is double-buffered, so the store of step s
 //                     overlaps step s+1), or TMA-reduce-adds the fp32 gradient
-//                     (the bias gradient, sum over k of A, is summed by the same
-//                     warps from global memory while the tile's MMAs run)
+//                     (the bias gradient, sum over k of A: with 128-wide tiles an
+//                     M=128, N=16 MMA against a tile of ones into TMEM beside
+//                     the accumulators; with 256-wide tiles, which fill TMEM,
+//                     summed by the epilogue warps from global memory while the
+//                     tile's MMAs run)
 // Bounded waits as in the single-tile kernel.
 #include <cuda.h>
 
@@ -45,16 +48,20 @@ struct PCfg {
   // per 64-column step: bf16 -> one box (two for bias+GELU: z and GELU(z)); fp32 -> two boxes
   static constexpr int STEP_BOXES = F32_OUT ? 2 : (EPI == EPI_BIAS_GELU ? 2 : 1);
   static constexpr int STAGING = 2 * STEP_BOXES * PBOX;  // double-buffered
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - STAGING) / STAGE_BYTES;
+  // bias gradient by MMA against ones (2 x 16 TMEM columns beside the accumulators) when they fit
+  static constexpr bool DB_MMA = EPI == EPI_ACC_F32 && 2 * BN + 32 <= 512;
+  static constexpr int ONES_BYTES = DB_MMA ? 2048 : 0;
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - STAGING - ONES_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_STG + STAGING;
+  static constexpr int OFF_ONES = OFF_STG + STAGING;
+  static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
-  // TMEM: two accumulators of BN columns
-  static constexpr int TCOLS = 2 * BN <= 256 ? 256 : 512;
+  // TMEM: two accumulators of BN columns (+ 2 x 16 bias-gradient columns)
+  static constexpr int TCOLS = (2 * BN + (DB_MMA ? 32 : 0)) <= 256 ? 256 : 512;
   static_assert(STAGES >= 3, "not enough shared memory for three stages");
   static_assert(SMEM <= 232448, "over the 227 KB per-CTA shared memory limit");
-  static_assert(2 * BN <= 512, "accumulators exceed tensor memory");
+  static_assert(2 * BN + (DB_MMA ? 32 : 0) <= 512, "accumulators exceed tensor memory");
 };
 
 constexpr int PGROUP = 16;  // row tiles per group of the tile order
@@ -108,6 +115,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sStg = smem + Cfg::OFF_STG;
+  uint8_t* sOnes = smem + Cfg::OFF_ONES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* accf = empty + STAGES;  // accumulator b holds a finished tile
@@ -133,6 +141,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     *abort = 0;
     fence_barrier_init();
+  }
+  if (Cfg::DB_MMA && threadIdx.x < 128) {  // 16 rows x 64 bf16 of 1.0
+    reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   if (warp == 1) {
     tmem_alloc(tslot, Cfg::TCOLS);
@@ -179,11 +191,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = mma_idesc_bf16(PM, BN, !A_K, !B_K);
+      constexpr uint32_t idesc_db = mma_idesc_bf16(PM, 16, !A_K, false);
+      const uint32_t ones = smem_u32(sOnes);
       int it = 0, i = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
         const int b = i & 1;
         if (!pwait(&acce[b], ((i >> 1) & 1) ^ 1, err, DERR_MMA_WAIT, abort)) break;
         tc_fence_after();
+        int tm0, tn0;
+        tile_origin<BN>(t, args, tm0, tn0);
+        const bool do_db = Cfg::DB_MMA && args.dbias != nullptr && tn0 == 0;
         const uint32_t dacc = tmem + b * BN;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
@@ -197,6 +214,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             const uint64_t bd = B_K ? sw128_desc(bb + kk * 32, 16, 1024) : sw128_desc(bb + kk * 2048, 8192, 1024);
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
             tc_mma_f16(dacc, ad, bd, idesc, acc);
+            if (do_db) tc_mma_f16(tmem + 2 * BN + 16 * b, ad, sw128_desc(ones + kk * 32, 16, 1024), idesc_db, acc);
           }
           tc_commit(&empty[s]);
         }
@@ -216,7 +234,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int m0, n0;
       tile_origin<BN>(t, args, m0, n0);
       const int m = m0 + r;
-      if (EPI == EPI_ACC_F32 && args.dbias != nullptr && n0 == 0 && !*abort)
+      if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && args.dbias != nullptr && n0 == 0 && !*abort)
         bias_grad_rows<A_K>(static_cast<const __nv_bfloat16*>(args.a), args.lda, args.M, args.K, args.dbias, m0,
                             warp - 2, lane);  // overlaps this tile's MMAs
       pwait(&accf[b], (i >> 1) & 1, err, DERR_ACC_WAIT, abort);
@@ -301,6 +319,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
           bulk_commit();
         }
+      }
+      if (Cfg::DB_MMA && args.dbias != nullptr && n0 == 0 && h == 0) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * BN + 16 * b, rr);
+        tmem_ld_wait();
+        if (m < args.M && !*abort) args.dbias[m] += __uint_as_float(rr[0]);
       }
       tc_fence_before();
       __syncwarp();
@@ -449,7 +473,15 @@ int64_t persistent_tiles(const GemmDesc& g) {
   return static_cast<int64_t>((g.M + PM - 1) / PM) * ((g.N + 127) / 128);
 }
 
+// A weight-gradient GEMM with a bias gradient sums that gradient by MMA with
+// 128-wide tiles and in SIMT with 256-wide ones (different rounding), so its
+// tile width must not depend on the SM share: 256 exactly when
+// wide_bias_grad_gemm(g) (then always the persistent kernel), else 128.
+bool wide_bias_grad_gemm(const GemmDesc& g) { return g.epi == EPI_ACC_F32 && g.dbias && g.M >= 1024 && g.N >= 1024; }
+
 int launch_gemm_persistent(const GemmDesc& g, cudaStream_t s, int ctas) {
+  if (g.epi == EPI_ACC_F32 && g.dbias)
+    return wide_bias_grad_gemm(g) ? dispatch<256>(g, s, ctas) : dispatch<128>(g, s, ctas);
   return wide_tiles(g, ctas) ? dispatch<256>(g, s, ctas) : dispatch<128>(g, s, ctas);
 }
 

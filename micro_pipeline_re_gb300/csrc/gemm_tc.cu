@@ -8,10 +8,10 @@
 //                     GELU pre-activation) so it lands during the main loop
 //   warp 1 / lane 0   MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16,
 //                     fp32 accumulator in tensor memory; tcgen05.commit frees
-//                     each stage and finally signals the epilogue
-//   all 8 warps       for the weight-gradient GEMM of the first N tile, the
-//                     bias gradient sum_k A(m,k) from global memory while the
-//                     MMAs run (bias_grad.cuh)
+//                     each stage and finally signals the epilogue.  For the
+//                     weight-gradient GEMM of the first N tile it also issues
+//                     an M=128, N=16 MMA against a tile of ones, which leaves
+//                     sum_k A(m,k) (the bias gradient) in TMEM column BN
 //   warps 0..3        epilogue: tcgen05.ld of their 32 TMEM lanes (= rows),
 //                     fused bias / residual / GELU, written into a 128B-swizzled
 //                     shared tile that one thread sends out with TMA stores
@@ -34,7 +34,6 @@
 #include <cuda.h>
 
 #include "../../include/gpipe.h"
-#include "bias_grad.cuh"
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -55,9 +54,11 @@ struct TcCfg {
   static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
   static constexpr int OUT_BOXES = F32_OUT ? BN / 32 : BN / 64;            // boxes of one output tile
   static constexpr int EPI_BYTES = (EPI == EPI_BIAS_GELU ? 2 : 1) * OUT_BOXES * BOX;
+  static constexpr int ONES_BYTES = (EPI == EPI_ACC_F32) ? 2048 : 0;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BIAS = OFF_EPI + EPI_BYTES;
+  static constexpr int OFF_ONES = OFF_EPI + EPI_BYTES;
+  static constexpr int OFF_BIAS = OFF_ONES + ONES_BYTES;
   static constexpr int OFF_BAR = OFF_BIAS + BN * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
 };
@@ -65,8 +66,6 @@ struct TcCfg {
 struct TcArgs {
   const float* bias;  // forward epilogues: fp32 [N] or NULL
   float* dbias;       // EPI_ACC_F32: fp32 [M] accumulator of sum_k A(m,k), or NULL
-  const void* a;      // A (bf16) and its leading dimension, for the bias gradient
-  int64_t lda;
   int M, N, K;
   int has_x;          // the epilogue input tile (residual / GELU pre-activation) is used
   // split-K epilogue (plain global accesses): output, its leading dimension,
@@ -100,6 +99,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + Cfg::OFF_B;
   uint8_t* sE = smem + Cfg::OFF_EPI;
+  uint8_t* sOnes = smem + Cfg::OFF_ONES;
   float* sBias = reinterpret_cast<float*>(smem + Cfg::OFF_BIAS);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + STAGES;
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int kb_begin = SPLIT ? static_cast<int>(blockIdx.z) * nk_all / S : 0;
   const int nk = (SPLIT ? (static_cast<int>(blockIdx.z) + 1) * nk_all / S : nk_all) - kb_begin;
   const bool do_db = (EPI == EPI_ACC_F32) && args.dbias != nullptr && blockIdx.x == 0;
-  constexpr uint32_t tcols = BN;
+  const uint32_t tcols = do_db ? static_cast<uint32_t>(BN == 64 ? 128 : 256) : static_cast<uint32_t>(BN);
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -139,6 +139,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int n = n0 + threadIdx.x;
       sBias[threadIdx.x] = (args.bias != nullptr && n < args.N) ? args.bias[n] : 0.f;
     }
+  }
+  if (do_db && threadIdx.x < 128) {  // 16 rows x 64 bf16 of 1.0
+    reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -180,6 +184,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (args.has_x) mbar_wait_bounded(epib, 0, err, DERR_DRAIN_WAIT);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = mma_idesc_bf16(BM, BN, !A_K, !B_K);
+    constexpr uint32_t idesc_db = mma_idesc_bf16(BM, 16, !A_K, false);
+    const uint32_t ones = smem_u32(sOnes);
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
@@ -193,6 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t bd = B_K ? sw128_desc(b + kk * 32, 16, 1024) : sw128_desc(b + kk * 2048, 8192, 1024);
         const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
         tc_mma_f16(tmem, ad, bd, idesc, acc);
+        if (do_db) tc_mma_f16(tmem + BN, ad, sw128_desc(ones + kk * 32, 16, 1024), idesc_db, acc);
       }
       tc_commit(&empty[s]);
     }
@@ -200,9 +207,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncwarp();
   griddep_launch();  // main loop issued: the next kernel may start its prologue
-  if (do_db)         // overlaps the MMAs still in flight
-    bias_grad_rows<A_K>(static_cast<const __nv_bfloat16*>(args.a), args.lda, args.M, args.K, args.dbias, m0, warp,
-                        lane);
 
   // ---- epilogue: warp w reads TMEM lanes 32(w%4).. (tile rows 32(w%4) + lane);
   //      warps w and w+4 split the tile's 32-column chunks ----
@@ -323,6 +327,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+    if (do_db && warp < 4) {
+      uint32_t rr[32];
+      tmem_ld32(tbase + BN, rr);
+      tmem_ld_wait();
+      const int m = m0 + r;
+      if (m < args.M) args.dbias[m] += __uint_as_float(rr[0]);
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -424,7 +435,7 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
   if (!ok) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed");
   int rc = set_attr<A_K, B_K, BN, EPI, SPLIT>();
   if (rc) return rc;
-  TcArgs args{g.bias, g.dbias, g.A, g.lda, g.M, g.N, g.K, has_x, g.C, g.ldc, xsrc, ldx};
+  TcArgs args{g.bias, g.dbias, g.M, g.N, g.K, has_x, g.C, g.ldc, xsrc, ldx};
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, SPLIT ? S : 1);
   cudaError_t e;
   if (SPLIT) {
@@ -516,7 +527,7 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
   const int S = has_split ? split_factor(g, 64) : 1;
   if (S > 1) return run_epi_bn<64>(g, s, S);
   const int budget = g.sm_budget > 0 ? g.sm_budget : num_sms();
-  if (persistent_tiles(g) > budget) return launch_gemm_persistent(g, s, budget);
+  if (persistent_tiles(g) > budget || wide_bias_grad_gemm(g)) return launch_gemm_persistent(g, s, budget);
   const int64_t tiles128 = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 127) / 128);
   if (tiles128 >= budget) return run_epi_bn<128>(g, s, 1);
   return run_epi_bn<64>(g, s, 1);

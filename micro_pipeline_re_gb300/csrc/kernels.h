@@ -52,6 +52,7 @@ int launch_gemm_simt(const GemmDesc& g, cudaStream_t stream);  // fp32 or bf16, 
 // Persistent tcgen05 GEMM (one CTA per SM over many tiles, two TMEM
 // accumulators); `ctas` caps the grid.  persistent_tiles: its tile count.
 int launch_gemm_persistent(const GemmDesc& g, cudaStream_t stream, int ctas);
+bool wide_bias_grad_gemm(const GemmDesc& g);
 int64_t persistent_tiles(const GemmDesc& g);
 int prepare_gemm_persistent();
 
