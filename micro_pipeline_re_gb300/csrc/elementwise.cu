@@ -91,12 +91,13 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, co
 
 // ---------------------------------------------------------------------------
 // LayerNorm backward.  Block b (8 warps) handles rows 8b .. 8b+7, one row per
-// warp; the warps then add their [dg | db] column sums into shared memory in
-// warp order and the block writes one partial row of scratch; col_reduce adds
-// the partial rows in order.  Both orders are fixed, so results are
-// bit-reproducible.
+// warp, with CH 256-column chunks per row (d <= 256*CH).  The warps then put
+// their dg and db column sums in shared memory and each column is added over
+// the warps in warp order (one barrier per half) into one partial row of
+// scratch; col_reduce adds the partial rows in order.  Both orders are fixed,
+// so results are bit-reproducible.
 // ---------------------------------------------------------------------------
-template <typename T>
+template <typename T, int CH>
 __global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
                                                      const float* __restrict__ mean, const float* __restrict__ rstd,
                                                      const float* __restrict__ g, const T* __restrict__ dres,
@@ -104,20 +105,20 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, c
                                                      int d) {
   griddep_wait();
   griddep_launch();
-  __shared__ __align__(16) float acc_s[2 * 32 * 8 * kMaxChunks];
+  __shared__ __align__(16) float stage[kLnRowsPerWarp][32 * 8 * CH];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kLnRowsPerWarp + warp;
-  float pg[kMaxChunks][8], pb[kMaxChunks][8];
+  float pg[CH][8], pb[CH][8];
 #pragma unroll
-  for (int c = 0; c < kMaxChunks; ++c)
+  for (int c = 0; c < CH; ++c)
 #pragma unroll
     for (int j = 0; j < 8; ++j) pg[c][j] = pb[c][j] = 0.f;
   if (r < rows) {
     const float mu = mean[r], rs = rstd[r];
-    float xh[kMaxChunks][8], gd[kMaxChunks][8];
+    float xh[CH][8], gd[CH][8];
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
+    for (int c = 0; c < CH; ++c) {
       const int col = (c * 32 + lane) * 8;
       if (col < d) {
         float xv[8], dv[8], gg[8];
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, c
     }
     const float m1 = warp_sum(s1) / d, m2 = warp_sum(s2) / d;
 #pragma unroll
-    for (int c = 0; c < kMaxChunks; ++c) {
+    for (int c = 0; c < CH; ++c) {
       const int col = (c * 32 + lane) * 8;
       if (col < d) {
         float o[8];
@@ -153,31 +154,29 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, c
       }
     }
   }
-  // fold the 8 warps' column sums in warp order
-  for (int w = 0; w < 8; ++w) {
-    if (warp == w) {
+  // fold the 8 warps' column sums in warp order: dg into partial[0, d), db into [d, 2d)
+  float* pr = partial + (int64_t)blockIdx.x * 2 * d;
 #pragma unroll
-      for (int c = 0; c < kMaxChunks; ++c) {
-        const int col = (c * 32 + lane) * 8;
-        if (col < d) {
+  for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (w == 0) {
-              acc_s[col + j] = pg[c][j];
-              acc_s[d + col + j] = pb[c][j];
-            } else {
-              acc_s[col + j] += pg[c][j];
-              acc_s[d + col + j] += pb[c][j];
-            }
-          }
-        }
+    for (int c = 0; c < CH; ++c) {
+      const int col = (c * 32 + lane) * 8;
+      if (col < d) {
+        float* dst = &stage[warp][col];
+        const float* src = half == 0 ? pg[c] : pb[c];
+        *reinterpret_cast<float4*>(dst) = make_float4(src[0], src[1], src[2], src[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(src[4], src[5], src[6], src[7]);
       }
     }
     __syncthreads();
+    for (int col = threadIdx.x; col < d; col += 256) {
+      float a = stage[0][col];
+#pragma unroll
+      for (int w = 1; w < kLnRowsPerWarp; ++w) a += stage[w][col];
+      pr[half * d + col] = a;
+    }
+    __syncthreads();
   }
-  float* pr = partial + (int64_t)blockIdx.x * 2 * d;
-  for (int i = threadIdx.x * 4; i < 2 * d; i += 256 * 4)
-    *reinterpret_cast<float4*>(pr + i) = *reinterpret_cast<const float4*>(acc_s + i);
 }
 
 // out[c] += sum_{p < nparts} partial[p*ncols + c], fixed order (4 interleaved
@@ -526,14 +525,27 @@ int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const 
   if (!al16(dy) || !al16(x) || !al16(dx) || !al16(g) || (dres && !al16(dres)) || !al16(scratch))
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: pointers must be 16-B aligned");
   const int grid = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
-  if (dtype == DT_F32)
-    (void)launch_k(ln_bwd_kernel<float>, grid, 256, 0, s, static_cast<const float*>(dy), static_cast<const float*>(x), mean,
-                                              rstd, g, static_cast<const float*>(dres), static_cast<float*>(dx),
-                                              scratch, rows, d);
-  else
-    (void)launch_k(ln_bwd_kernel<__nv_bfloat16>, grid, 256, 0, s, 
-        static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(x), mean, rstd, g,
-        static_cast<const __nv_bfloat16*>(dres), static_cast<__nv_bfloat16*>(dx), scratch, rows, d);
+  if (dtype == DT_F32) {
+    const float *dyp = static_cast<const float*>(dy), *xp = static_cast<const float*>(x),
+                *rp = static_cast<const float*>(dres);
+    float* dxp = static_cast<float*>(dx);
+    if (d <= 256)
+      (void)launch_k(ln_bwd_kernel<float, 1>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
+    else if (d <= 512)
+      (void)launch_k(ln_bwd_kernel<float, 2>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
+    else
+      (void)launch_k(ln_bwd_kernel<float, 4>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
+  } else {
+    const __nv_bfloat16 *dyp = static_cast<const __nv_bfloat16*>(dy), *xp = static_cast<const __nv_bfloat16*>(x),
+                        *rp = static_cast<const __nv_bfloat16*>(dres);
+    __nv_bfloat16* dxp = static_cast<__nv_bfloat16*>(dx);
+    if (d <= 256)
+      (void)launch_k(ln_bwd_kernel<__nv_bfloat16, 1>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
+    else if (d <= 512)
+      (void)launch_k(ln_bwd_kernel<__nv_bfloat16, 2>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
+    else
+      (void)launch_k(ln_bwd_kernel<__nv_bfloat16, 4>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
+  }
   return check_launch("layernorm_bwd");
 }
 
