@@ -245,20 +245,33 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         uint8_t* stg = sStg + (step & 1) * Cfg::STEP_BOXES * PBOX;
         if (etid == 0) bulk_wait_read_1();  // the store that last used this buffer has read it
         epi_bar();
+        const int ncol0 = n0 + c * 64 + h * 32;
+        const bool full_cols = ncol0 + 32 <= args.N;
+        // the epilogue input (residual / GELU pre-activation) is read from global
+        // memory first, so its latency overlaps the tensor-memory read below
+        float xv[32];
+        const bool has_x = !Cfg::F32_OUT && args.xsrc && m < args.M;
+        if (has_x) {
+          const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx;
+          if (full_cols) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) load8(xr + ncol0 + j, xv + j);
+          } else {
+            for (int j = 0; j < 32; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xr[ncol0 + j]) : 0.f;
+          }
+        }
         uint32_t rr[32];
         tmem_ld32(tb + c * 64 + h * 32, rr);
         tmem_ld_wait();
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
-        const int ncol0 = n0 + c * 64 + h * 32;
         if (Cfg::F32_OUT) {
           uint8_t* box = stg + h * PBOX;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<float4*>(box + pswz(r, u)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         } else {
-          const bool full_cols = ncol0 + 32 <= args.N;
           if ((EPI == EPI_STORE || EPI == EPI_BIAS_GELU) && args.bias) {
             if (full_cols) {
 #pragma unroll
@@ -273,15 +286,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 if (ncol0 + j < args.N) v[j] += args.bias[ncol0 + j];
             }
           }
-          if (args.xsrc && m < args.M) {
-            const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx;
-            float xv[32];
-            if (full_cols) {
-#pragma unroll
-              for (int j = 0; j < 32; j += 8) load8(xr + ncol0 + j, xv + j);
-            } else {
-              for (int j = 0; j < 32; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xr[ncol0 + j]) : 0.f;
-            }
+          if (has_x) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               if (EPI == EPI_GELU_BWD) v[j] *= gelu_grad_f(xv[j]);
