@@ -176,7 +176,15 @@ def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
     import torch
     M, N, K = shape
     bf = torch.bfloat16
-    if epi == 3:
+    if epi == 0:
+        A = torch.randn(M, K, device="cuda").to(bf)
+        Bw = torch.randn(N, K, device="cuda").to(bf)
+        vec = torch.zeros(N, device="cuda")
+        Z = torch.empty(M, N, device="cuda", dtype=bf)
+        args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), K, 1, 0, Z.data_ptr(), N, vec.data_ptr(), None, 0,
+                None, None, 0)
+        name = f"projection GEMM (bias, bf16 store) {M}x{N}x{K}"
+    elif epi == 3:
         A = torch.randn(K, M, device="cuda").to(bf)
         Bw = torch.randn(K, N, device="cuda").to(bf)
         C = torch.zeros(M, N, device="cuda")
@@ -222,16 +230,20 @@ def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
             "timing": f"CUDA events around a graph of {reps} back-to-back launches of this GEMM alone"}
 
 
-# The kernel class the roofline reports: the fp32 weight-gradient GEMMs
-# (epilogue 3, TMA reduce-add into the gradient buffer) take the largest share
-# of kernel time in the step's launch list.
-ROOF_EPI = 3
+# The kernel class the roofline reports: the GEMMs with the bf16 store
+# epilogue (epilogue 0: the forward projections and the input gradients) take
+# the largest share of kernel time in the step's launch list.
+ROOF_EPI = 0
+EPI_NAMES = {0: "bf16 store epilogue (bias / residual)", 1: "bias + GELU epilogue", 2: "GELU-backward epilogue",
+             3: "fp32 TMA reduce-add epilogue (weight gradient, bias gradient)", 4: "fp32 store epilogue"}
 
 
-# Per-launch DRAM traffic of the roofline GEMM, from one ncu capture of the
-# same shape and epilogue alone (`--probe-gemm`; cold L2, so an upper bound of
-# what the launch reads and writes inside the step): (M, N, K) -> bytes.
-ROOF_TRAFFIC = {}
+# Per-launch DRAM traffic (read + write bytes) of GEMMs of the step's shapes,
+# each from one ncu capture of that shape and epilogue alone (`--probe-gemm`,
+# cold L2): (epilogue, M, N, K) -> bytes.  Inside the step the operands are
+# often still in L2, so this is an upper bound of a launch's DRAM traffic.
+ROOF_TRAFFIC = {(3, 512, 2048, 512): 6832896, (3, 2048, 512, 512): 6839040, (3, 1536, 512, 512): 5264128,
+                (3, 512, 512, 512): 2114304}
 
 
 def live_roofline(kt, peaks, b):
@@ -252,11 +264,10 @@ def live_roofline(kt, peaks, b):
     ach = tot_fl / (tot_ms / 1e3) / 1e12
     cls = float(fl.sum()) / (float(ms.sum()) / 1e3) / 1e12
     return {"bound": "tensor",
-            "kernel": f"tcgen05 weight-gradient GEMM {shape[0]}x{shape[1]}x{shape[2]} (MN-major operands, fp32 "
-                      f"TMA reduce-add, bias gradient)",
+            "kernel": f"tcgen05 GEMM {shape[0]}x{shape[1]}x{shape[2]}, {EPI_NAMES[ROOF_EPI]}",
             "achieved": ach, "peak": peaks["bf16_sus"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_sus"],
-            "traffic": ROOF_TRAFFIC.get(shape), "peak_source": peaks["source"] + " (sustained: the kernel runs "
-                                                                              "inside a long step)",
+            "traffic": ROOF_TRAFFIC.get((ROOF_EPI,) + shape),
+            "peak_source": peaks["source"] + " (sustained: the kernel runs inside a long step)",
             "algorithmic_flop_per_launch": tot_fl / n, "launches_per_step": n, "avg_launch_us": tot_ms / n * 1e3,
             "timing": "CUDA events around every launch of the class in one step (a pass after the timed region: "
                       "the same graph plus the event nodes), on the stream it runs on",
@@ -423,7 +434,8 @@ def main():
     ap.add_argument("--probe-gemm", action="store_true",
                     help="only run the roofline GEMM (5 eager launches, then a timed graph); for profilers")
     ap.add_argument("--shape", default=None, help="M,N,K for --probe-gemm (default: the workload's FFN1)")
-    ap.add_argument("--epi", type=int, default=1, help="--probe-gemm epilogue: 1 bias+GELU, 3 weight gradient")
+    ap.add_argument("--epi", type=int, default=1,
+                    help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 3 weight gradient")
     ap.add_argument("--reps", type=int, default=100)
     ap.add_argument("--sweep", action="store_true",
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
