@@ -470,11 +470,17 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
 // Split-K factor for a bf16-output GEMM: only K long enough that every split
 // keeps at least 32 k-blocks (so the per-CTA set-up stays small against its
 // work), up to 8 (a portable cluster) and never more CTAs than two per SM.
+// Split K across S (<= 8) CTAs of a cluster while each split keeps at least
+// kMinSplitBlocks k-blocks and the tiles x S stay within two waves: a long-K
+// GEMM with few output tiles (512 x 512 x 2048) otherwise streams all of K
+// through a few SMs.
+constexpr int kMinSplitBlocks = 8;
+
 int split_factor(const GemmDesc& g, int BN) {
   const int64_t tiles = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int nk = (g.K + BK - 1) / BK;
   int S = 1;
-  while (S < 8 && nk / (S * 2) >= 32 && tiles * S * 2 <= 2 * static_cast<int64_t>(num_sms())) S *= 2;
+  while (S < 8 && nk / (S * 2) >= kMinSplitBlocks && tiles * S * 2 <= 2 * static_cast<int64_t>(num_sms())) S *= 2;
   return S;
 }
 
