@@ -471,10 +471,11 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
 // keeps at least 32 k-blocks (so the per-CTA set-up stays small against its
 // work), up to 8 (a portable cluster) and never more CTAs than two per SM.
 // Split K across S (<= 8) CTAs of a cluster while each split keeps at least
-// kMinSplitBlocks k-blocks and the tiles x S stay within two waves: a long-K
-// GEMM with few output tiles (512 x 512 x 2048) otherwise streams all of K
-// through a few SMs.
-constexpr int kMinSplitBlocks = 8;
+// kMinSplitBlocks k-blocks and the tiles x S stay within two waves.  Only very
+// long K qualifies (the head's dh = dz E, K = vocab): splitting mid-length K
+// (2048) made single GEMMs faster but the concurrent step slower, as cluster
+// launches wait for co-resident SMs that other lanes hold.
+constexpr int kMinSplitBlocks = 32;
 
 int split_factor(const GemmDesc& g, int BN) {
   const int64_t tiles = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
