@@ -133,6 +133,21 @@ def test_lm_wide_layers_sub_batch(b):
     _lm_parity(b, w, make_inputs(w))
 
 
+def test_sweep_layers_single_micro_batch(b):
+    """The sweep workload's layer (d=1024, ffn=8192, seq=256) with K=8 cells and
+    the degenerate M=1 (no micro-batching), 16 layers on one sequence (the fp64
+    oracle's time grows with layers x tokens)."""
+    w = WORKLOADS["lm_sweep"].replace(L=16, n=1, M=1, K=8)
+    _lm_parity(b, w, make_inputs(w))
+
+
+def test_memory_scaling_layers_sub_batch(b):
+    """The memory-scaling workload's layer at seq 512 with K=16 cells (one layer
+    each) on one sequence, M=1."""
+    w = WORKLOADS["lm_deep"].replace(L=16, n=1, M=1)
+    _lm_parity(b, w, make_inputs(w))
+
+
 @pytest.mark.parametrize("m_check", [0, 1])
 def test_rematerialised_internals_bit_identical(b, m_check):
     w = SMALL_LM

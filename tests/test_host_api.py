@@ -198,11 +198,15 @@ def test_pipelined_lanes_cost_memory_only_per_cell(binding):
     assert serial < piped < noremat / 4
 
 
-def test_rematerialisation_saves_memory(binding):
-    w = WORKLOADS["lm_wide"]
-    peak, _, _ = _report(binding, w, w.K, w.M)
-    peak_nr, _, _ = _report(binding, w, w.K, w.M, no_remat=True)
-    # without re-materialisation every layer keeps its internals for every micro-batch
+@pytest.mark.parametrize("name", ["lm_wide", "lm_deep"])
+def test_rematerialisation_saves_memory(binding, name):
+    """The memory-scaling comparison: peak activation bytes with and without
+    re-materialisation, each within its bound; without it every layer keeps its
+    internals for every micro-batch."""
+    w = WORKLOADS[name]
+    peak, bound, _ = _report(binding, w, w.K, w.M)
+    peak_nr, bound_nr, _ = _report(binding, w, w.K, w.M, no_remat=True)
+    assert peak <= bound and peak_nr <= bound_nr
     assert peak_nr > 10 * peak
 
 
