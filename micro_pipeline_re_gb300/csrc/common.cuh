@@ -190,6 +190,10 @@ __device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait only until every committed bulk copy has finished reading its shared
+// memory source (enough before a CTA exits: the grid's completion makes the
+// global writes visible to later kernels).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       if (lane == 0) mbar_arrive(&acce[b]);  // this warp has drained accumulator b
     }
     griddep_launch();
-    if (etid == 0) bulk_wait_all();
+    if (etid == 0) bulk_wait_read_all();
   }
   tc_fence_before();
   __syncthreads();

@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (EPI == EPI_BIAS_GELU) tma_store_2d(&tmC2, x, m0, sE + (Cfg::OUT_BOXES + b) * BOX);
     }
     bulk_commit();
-    bulk_wait_all();
+    bulk_wait_read_all();
   }
   __syncthreads();
   if (warp == 1) {
