@@ -191,7 +191,7 @@ enum {
                                 tick of the schedule + 1), doubled for GEMMs of at
                                 most 4 x that many 128 x 128 tiles), 25..800; the tile
                                 choice follows the grid, results stay identical    */
-  GPIPE_OPT_INFLIGHT = 12    /* [0] with lanes: micro-batches each cell works on at
+  GPIPE_OPT_INFLIGHT = 12,   /* [0] with lanes: micro-batches each cell works on at
                                 once: 1..4, or 0 = 2 when a micro-batch's FFN GEMM
                                 (tokens x d x ffn) is at most 2^30 multiply-adds,
                                 else 1.  S > 1 gives each cell S lanes that take
@@ -201,6 +201,11 @@ enum {
                                 GPIPE_OPT_CONCURRENT says), so every weight gradient
                                 still accumulates in micro-batch order and results
                                 are identical.  Set before gpipe_sizes.              */
+  GPIPE_OPT_SIDE_SHARE = 13  /* [100] with lanes, GEMMs on the side streams (weight
+                                gradients, off the critical path) get this percentage
+                                of the SM share, 5..800: a smaller grid does the same
+                                tiles with fewer CTAs, so less SM time; results stay
+                                identical                                            */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

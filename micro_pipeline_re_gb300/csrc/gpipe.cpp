@@ -55,7 +55,7 @@ struct StepPtrs {
 
 struct GraphKey {
   StepPtrs p;
-  int64_t opts[10];
+  int64_t opts[11];
   bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
 };
 
@@ -90,6 +90,7 @@ struct gpipe_ctx {
   }
   int ktime = 0;           // e+1: time every GEMM launch with epilogue e (event pairs)
   int sm_share = 100;      // percent of a GEMM's fair share of the SMs (with lanes)
+  int side_share = 100;    // percent of that share for GEMMs on the side streams
   std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
   std::vector<double> kt_flops;
   std::vector<int32_t> kt_mnk;
@@ -501,7 +502,13 @@ class Executor {
       // the tensor cores: let it spread over twice the share
       int share = num_sms() * c_->sm_share / (100 * (busy_ + 1));
       const int64_t tiles = static_cast<int64_t>((M + 127) / 128) * ((N + 127) / 128);
-      if (tiles <= 4 * static_cast<int64_t>(share)) share *= 2;
+      if (cur_) {
+        // side stream (weight gradients, off the critical path): a small grid
+        // whose CTAs each take many tiles spends the least SM time
+        share = share * c_->side_share / 100;
+      } else if (tiles <= 4 * static_cast<int64_t>(share)) {
+        share *= 2;
+      }
       g.sm_budget = share < 1 ? 1 : (share > num_sms() ? num_sms() : share);
     } else {
       g.sm_budget = num_sms();
@@ -824,6 +831,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[7] = c->trace;
     key.opts[8] = c->ktime;
     key.opts[9] = c->sm_share;
+    key.opts[10] = c->side_share;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -917,6 +925,10 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_SIDE_SHARE:
+      if (value < 5 || value > 800) return c->fail(GPIPE_ERR_INVALID_ARG, "side SM share must be 5..800 percent");
+      c->side_share = static_cast<int>(value);
+      break;
     case GPIPE_OPT_INFLIGHT:
       if (value < 0 || value > gpipe_ctx::kRing)
         return c->fail(GPIPE_ERR_INVALID_ARG, "in-flight micro-batches per cell must be 0 (by size) or 1..4");
