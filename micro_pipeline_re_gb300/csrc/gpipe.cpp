@@ -96,7 +96,7 @@ struct gpipe_ctx {
   std::vector<int32_t> kt_mnk;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
   static constexpr int kMaxLanes = 128;
-  static constexpr int kLaneEvents = 11;
+  static constexpr int kLaneEvents = 14;
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
   static constexpr int kRing = 4;  // deepest gradient ring between neighbouring cells (= most in flight)
@@ -204,7 +204,23 @@ struct Slot {
 };
 
 // Events that order a lane's side stream against its main stream.
-enum { EV_FORK, EV_GF, EV_GH, EV_GQ, EV_DY0, EV_DY1, EV_DYB, EV_HEAD, EV_HEADF, EV_LN0, EV_LN1, EV_COUNT };
+enum {
+  EV_FORK,
+  EV_GF,  // EV_GF + b: side work has read gf[b] (likewise gh[b], gq[b])
+  EV_GF1,
+  EV_GH,
+  EV_GH1,
+  EV_GQ,
+  EV_GQ1,
+  EV_DY0,
+  EV_DY1,
+  EV_DYB,
+  EV_HEAD,
+  EV_HEADF,
+  EV_LN0,
+  EV_LN1,
+  EV_COUNT
+};
 constexpr int BUF_EXT = 2;  // "dy lives outside the lane" (boundary ring / head output)
 
 // Issues one step.  Host issue order is the serial GPipe order (phase 1:
@@ -340,6 +356,7 @@ class Executor {
   int cur_lane_ = 0;            // lane whose main stream receives the current cell's work
   int busy_ = 1;                // cells busy at the current op's tick of the schedule
   int ln_buf_[gpipe_ctx::kMaxLanes] = {};  // per lane: the LayerNorm-backward partial buffer to use next
+  int gbuf_[gpipe_ctx::kMaxLanes] = {};    // per lane: the gf/gh/gq set the next layer backward uses
   bool rec_[gpipe_ctx::kMaxLanes][EV_COUNT] = {};
   bool fwd_rec_[gpipe_ctx::kMaxLanes] = {};
   bool bdone_rec_[gpipe_ctx::kMaxLanes][gpipe_ctx::kRing] = {};
@@ -610,7 +627,11 @@ class Executor {
     float* scratch = reinterpret_cast<float*>(lb + ll.scratch);
     float* lnp0 = reinterpret_cast<float*>(lb + ll.lnp[0]);
     float* lnp1 = reinterpret_cast<float*>(lb + ll.lnp[1]);
-    char* gf = lb + ll.gf;
+    // the weight-gradient operands alternate between two sets by layer, so the
+    // main stream waits only for side work of two layers back before reuse
+    const int gb = gbuf_[lane];
+    gbuf_[lane] ^= 1;
+    char* gf = lb + ll.gf[gb];
     char* gt = lb + ll.gt;
     const void* ffn_in = dm.kind == 1 ? static_cast<const void*>(s.u2) : static_cast<const void*>(s.u);
     const int ev_dy = dy_buf == 0 ? EV_DY0 : (dy_buf == 1 ? EV_DY1 : EV_DYB);
@@ -619,9 +640,9 @@ class Executor {
       return gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f, nullptr, nullptr, 0, nullptr,
                   nullptr, 0, grad(o.b2));
     }));
-    TRY(join(lane, EV_GF));
+    TRY(join(lane, EV_GF + gb));
     TRY(gemm(T, f, d, dy, d, true, wgt(o.w2), f, false, EPI_GELU_BWD, gf, f, nullptr, nullptr, 0, nullptr, s.z1, f));
-    TRY(on_side(EV_GF, [&] {
+    TRY(on_side(EV_GF + gb, [&] {
       return gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d, nullptr, nullptr, 0, nullptr,
                   nullptr, 0, grad(o.b1));
     }));
@@ -631,21 +652,21 @@ class Executor {
       return ln_backward(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g), grad(o.ln1_b),
                          lnp0, lnp1);
     }
-    char* gh = lb + ll.gh;
-    char* gq = lb + ll.gq;
+    char* gh = lb + ll.gh[gb];
+    char* gq = lb + ll.gq[gb];
     // h1 -> LN2: dh1 = LN2'(du2) + dy
-    TRY(join(lane, EV_GH));
+    TRY(join(lane, EV_GH + gb));
     TRY(ln_backward(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g), grad(o.ln2_b),
                     lnp0, lnp1));
     // attention output projection
-    TRY(on_side(EV_GH, [&] {
+    TRY(on_side(EV_GH + gb, [&] {
       return gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d, nullptr, nullptr, 0, nullptr,
                   nullptr, 0, grad(o.b_o));
     }));
     TRY(gemm(T, d, d, gh, d, true, wgt(o.w_o), d, false, EPI_STORE, gt, d));
-    TRY(join(lane, EV_GQ));
+    TRY(join(lane, EV_GQ + gb));
     TRY(launch_attention_bwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, gt, s.lse, scratch, gq, st()));
-    TRY(on_side(EV_GQ, [&] {
+    TRY(on_side(EV_GQ + gb, [&] {
       return gemm(3 * d, d, T, gq, 3 * d, false, s.u, d, false, EPI_ACC_F32, grad(o.w_qkv), d, nullptr, nullptr, 0,
                   nullptr, nullptr, 0, grad(o.b_qkv));
     }));

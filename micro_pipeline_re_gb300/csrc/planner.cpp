@@ -175,10 +175,12 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   ln.g0 = ltake(Tmb * d * es);
   ln.g1 = ltake(Tmb * d * es);
   ln.gt = ltake(Tmb * d * es);
-  ln.gf = ltake(Tmb * f * es);
-  if (dm.kind == 1) {
-    ln.gh = ltake(Tmb * d * es);
-    ln.gq = ltake(Tmb * 3 * d * es);
+  for (int i = 0; i < 2; ++i) {
+    ln.gf[i] = ltake(Tmb * f * es);
+    if (dm.kind == 1) {
+      ln.gh[i] = ltake(Tmb * d * es);
+      ln.gq[i] = ltake(Tmb * 3 * d * es);
+    }
   }
   size_t cols = std::max<size_t>(2 * d, f);
   if (dm.kind == 1) cols = std::max<size_t>(cols, 3 * d);
