@@ -48,24 +48,19 @@ constexpr int BOX = 16384;  // one epilogue box: 128 rows x 128 B
 
 template <int BN, int EPI>
 struct TcCfg {
+  static constexpr int STAGES = BN == 64 ? 3 : 4;  // BN=64: two CTAs fit on one SM
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
   static constexpr int OUT_BOXES = F32_OUT ? BN / 32 : BN / 64;            // boxes of one output tile
   static constexpr int EPI_BYTES = (EPI == EPI_BIAS_GELU ? 2 : 1) * OUT_BOXES * BOX;
   static constexpr int ONES_BYTES = (EPI == EPI_ACC_F32) ? 2048 : 0;
-  // As many operand stages as shared memory holds, up to 8 (K = 512 in flight at
-  // once: these GEMMs are short, so the TMA round trips, not the MMAs, set the time)
-  static constexpr int STAGES_FIT = (232448 - 1024 - 256 - BN * 4 - ONES_BYTES - EPI_BYTES) / (A_BYTES + B_BYTES);
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_ONES = OFF_EPI + EPI_BYTES;
   static constexpr int OFF_BIAS = OFF_ONES + ONES_BYTES;
   static constexpr int OFF_BAR = OFF_BIAS + BN * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static_assert(STAGES >= 3, "fewer than three operand stages fit");
-  static_assert(SMEM <= 232448, "over the 227 KB per-CTA shared memory limit");
 };
 
 struct TcArgs {
