@@ -201,10 +201,16 @@ enum {
                                 GPIPE_OPT_CONCURRENT says), so every weight gradient
                                 still accumulates in micro-batch order and results
                                 are identical.  Set before gpipe_sizes.              */
-  GPIPE_OPT_SIDE_SHARE = 13  /* [100] with lanes, GEMMs on the side streams (weight
+  GPIPE_OPT_SIDE_SHARE = 13, /* [100] with lanes, GEMMs on the side streams (weight
                                 gradients, off the critical path) get this percentage
                                 of the SM share, 5..800: a smaller grid does the same
                                 tiles with fewer CTAs, so less SM time; results stay
+                                identical                                            */
+  GPIPE_OPT_SIDE_STREAMS = 14 /* [1] side streams per lane, 1..4: the weight-gradient
+                                work of W2, W1, W_o, W_qkv and the LayerNorm
+                                reductions go to stream (group mod this); a group
+                                always uses the same stream, so every gradient still
+                                accumulates in micro-batch order and results are
                                 identical                                            */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);

@@ -27,6 +27,7 @@ OPT_KERNEL_TIMES = 10
 OPT_SM_SHARE = 11
 OPT_INFLIGHT = 12
 OPT_SIDE_SHARE = 13
+OPT_SIDE_STREAMS = 14
 EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
 
 

@@ -55,7 +55,7 @@ struct StepPtrs {
 
 struct GraphKey {
   StepPtrs p;
-  int64_t opts[11];
+  int64_t opts[12];
   bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
 };
 
@@ -91,13 +91,15 @@ struct gpipe_ctx {
   int ktime = 0;           // e+1: time every GEMM launch with epilogue e (event pairs)
   int sm_share = 100;      // percent of a GEMM's fair share of the SMs (with lanes)
   int side_share = 100;    // percent of that share for GEMMs on the side streams
+  int nside = 1;           // side streams per lane (parameter groups spread over them)
   std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
   std::vector<double> kt_flops;
   std::vector<int32_t> kt_mnk;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
   static constexpr int kMaxLanes = 128;
   static constexpr int kLaneEvents = 14;
-  cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes] = {};
+  static constexpr int kSides = 4;  // most side streams per lane
+  cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes][kSides] = {};
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
   static constexpr int kRing = 4;  // deepest gradient ring between neighbouring cells (= most in flight)
   cudaEvent_t ev_origin = nullptr, ev_fwd[kMaxLanes] = {}, ev_bdone[kMaxLanes][kRing] = {},
@@ -150,7 +152,9 @@ struct gpipe_ctx {
     for (int m = 0; m < M && ok; ++m) ok = mk_ev(ev_hdone[m]);
     for (int i = 0; i < nstreams() && ok; ++i) {
       const bool head = nstreams() > 1 && i == nstreams() - 1;
-      ok = mk_st(lane_main[i], head ? (least + greatest) / 2 : greatest) && mk_st(lane_side[i], least) &&
+      ok = mk_st(lane_main[i], head ? (least + greatest) / 2 : greatest);
+      for (int j = 0; j < nside && ok; ++j) ok = mk_st(lane_side[i][j], least);
+      ok = ok &&
            mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
       for (int e = 0; e < kLaneEvents && ok; ++e) ok = mk_ev(lane_ev[i][e]);
     }
@@ -375,7 +379,22 @@ class Executor {
   // always with two micro-batches in flight (the cell's two lanes must not
   // accumulate into the same gradients from two streams).
   bool use_side() const { return c_->concurrent || c_->ws.inflight > 1; }
-  cudaStream_t side(int lane) const { return use_side() ? c_->lane_side[side_of(lane)] : c_->lane_main[lane]; }
+  // The side stream of a parameter group: the group of the event that marks
+  // its work (W2, W1, W_o, W_qkv weight gradients, LayerNorm reductions; the
+  // head's dE with W2).  A group always goes to the same stream, so each
+  // parameter's gradient still accumulates in micro-batch order.
+  static int group_of(int e) {
+    switch (e) {
+      case EV_GF: case EV_GF1: return 1;
+      case EV_GH: case EV_GH1: return 2;
+      case EV_GQ: case EV_GQ1: return 3;
+      case EV_LN0: case EV_LN1: return 4;
+      default: return 0;
+    }
+  }
+  cudaStream_t side(int lane, int e) const {
+    return use_side() ? c_->lane_side[side_of(lane)][group_of(e) % c_->nside] : c_->lane_main[lane];
+  }
   cudaStream_t st() const { return cur_ ? cur_ : c_->lane_main[cur_lane_]; }
   int cuda_ok(cudaError_t e, const char* what) {
     return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -391,15 +410,15 @@ class Executor {
     return cuda_ok(cudaStreamWaitEvent(main_s(lane_of(k, m)), e, 0), "stream wait");
   }
   // a lane's side stream starts after everything issued so far on its main stream
-  int fork(int lane) {
+  int fork(int lane, int e) {
     if (!use_side()) return GPIPE_OK;
     TRY(cuda_ok(cudaEventRecord(c_->lane_ev[lane][EV_FORK], main_s(lane)), "event record"));
-    return cuda_ok(cudaStreamWaitEvent(side(lane), c_->lane_ev[lane][EV_FORK], 0), "stream wait");
+    return cuda_ok(cudaStreamWaitEvent(side(lane, e), c_->lane_ev[lane][EV_FORK], 0), "stream wait");
   }
   int mark(int lane, int e) {
     if (!use_side()) return GPIPE_OK;
     rec_[lane][e] = true;
-    return cuda_ok(cudaEventRecord(c_->lane_ev[lane][e], side(lane)), "event record");
+    return cuda_ok(cudaEventRecord(c_->lane_ev[lane][e], side(lane, e)), "event record");
   }
   int join(int lane, int e) {
     if (!use_side() || !rec_[lane][e]) return GPIPE_OK;
@@ -412,8 +431,8 @@ class Executor {
   template <typename F>
   int on_side(int e, F&& f) {
     const int lane = cur_lane_;
-    TRY(fork(lane));
-    cur_ = side(lane);
+    TRY(fork(lane, e));
+    cur_ = side(lane, e);
     int rc = f();
     cur_ = nullptr;
     if (rc) return rc;
@@ -853,6 +872,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[8] = c->ktime;
     key.opts[9] = c->sm_share;
     key.opts[10] = c->side_share;
+    key.opts[11] = c->nside;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -946,6 +966,11 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_SIDE_STREAMS:
+      if (value < 1 || value > gpipe_ctx::kSides)
+        return c->fail(GPIPE_ERR_INVALID_ARG, "side streams per lane must be 1..4");
+      c->nside = static_cast<int>(value);
+      break;
     case GPIPE_OPT_SIDE_SHARE:
       if (value < 5 || value > 800) return c->fail(GPIPE_ERR_INVALID_ARG, "side SM share must be 5..800 percent");
       c->side_share = static_cast<int>(value);
@@ -1038,7 +1063,8 @@ void gpipe_destroy(gpipe_ctx* c) {
   if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
   for (int i = 0; i < gpipe_ctx::kMaxLanes; ++i) {
     if (c->lane_main[i]) cudaStreamDestroy(c->lane_main[i]);
-    if (c->lane_side[i]) cudaStreamDestroy(c->lane_side[i]);
+    for (cudaStream_t st : c->lane_side[i])
+      if (st) cudaStreamDestroy(st);
     for (auto& e : c->lane_ev[i])
       if (e) cudaEventDestroy(e);
     for (int r = 0; r < gpipe_ctx::kRing; ++r) {

@@ -178,12 +178,13 @@ def test_schedules_are_bit_identical(b, wname):
     w = SMALL_LM if wname == "small_lm" else WORKLOADS[wname]
     inp = make_inputs(w)
     outs = []
-    for pipe, conc, graph, pdl, inflight in ((0, 0, 1, 0, 1), (1, 1, 1, 1, 1), (1, 0, 1, 1, 1), (0, 1, 1, 1, 1),
-                                             (1, 1, 0, 1, 1), (1, 1, 1, 0, 1), (1, 1, 1, 0, 2), (1, 0, 0, 0, 2),
-                                             (1, 1, 1, 0, 3), (1, 1, 1, 0, 4)):
+    for pipe, conc, graph, pdl, inflight, nside in (
+            (0, 0, 1, 0, 1, 1), (1, 1, 1, 1, 1, 1), (1, 0, 1, 1, 1, 1), (0, 1, 1, 1, 1, 1), (1, 1, 0, 1, 1, 1),
+            (1, 1, 1, 0, 1, 1), (1, 1, 1, 0, 2, 1), (1, 0, 0, 0, 2, 1), (1, 1, 1, 0, 3, 1), (1, 1, 1, 0, 4, 1),
+            (1, 1, 1, 0, 2, 4), (1, 1, 1, 0, 1, 3), (0, 1, 0, 0, 1, 2)):
         _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_INFLIGHT, inflight), (b.OPT_PIPELINE, pipe),
                                                      (b.OPT_CONCURRENT, conc), (b.OPT_GRAPH, graph),
-                                                     (b.OPT_PDL, pdl)])
+                                                     (b.OPT_PDL, pdl), (b.OPT_SIDE_STREAMS, nside)])
         outs.append((loss, st.g32.cpu().numpy().copy(), st.p32.cpu().numpy().copy()))
     for i, o in enumerate(outs[1:], 1):
         assert o[0] == outs[0][0], i
