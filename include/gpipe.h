@@ -206,7 +206,7 @@ enum {
                                 of the SM share, 5..800: a smaller grid does the same
                                 tiles with fewer CTAs, so less SM time; results stay
                                 identical                                            */
-  GPIPE_OPT_SIDE_STREAMS = 14 /* [1] side streams per lane, 1..4: the weight-gradient
+  GPIPE_OPT_SIDE_STREAMS = 14 /* [2] side streams per lane, 1..4: the weight-gradient
                                 work of W2, W1, W_o, W_qkv and the LayerNorm
                                 reductions go to stream (group mod this); a group
                                 always uses the same stream, so every gradient still

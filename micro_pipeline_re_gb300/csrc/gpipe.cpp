@@ -91,7 +91,7 @@ struct gpipe_ctx {
   int ktime = 0;           // e+1: time every GEMM launch with epilogue e (event pairs)
   int sm_share = 100;      // percent of a GEMM's fair share of the SMs (with lanes)
   int side_share = 100;    // percent of that share for GEMMs on the side streams
-  int nside = 1;           // side streams per lane (parameter groups spread over them)
+  int nside = 2;           // side streams per lane (parameter groups spread over them)
   std::vector<cudaEvent_t> kt_ev;  // 2 per timed launch, reused step to step
   std::vector<double> kt_flops;
   std::vector<int32_t> kt_mnk;
