@@ -47,7 +47,11 @@ struct PCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // per 64-column step: bf16 -> one box (two for bias+GELU: z and GELU(z)); fp32 -> two boxes
   static constexpr int STEP_BOXES = F32_OUT ? 2 : (EPI == EPI_BIAS_GELU ? 2 : 1);
-  static constexpr int STAGING = 2 * STEP_BOXES * PBOX;  // double-buffered
+  // one-box steps are double-buffered (a step's store overlaps the next step);
+  // two-box steps single-buffered, which leaves room for a fourth operand stage
+  // at 256 columns (measured faster than the overlap)
+  static constexpr int NBUF = STEP_BOXES == 1 ? 2 : 1;
+  static constexpr int STAGING = NBUF * STEP_BOXES * PBOX;
   // bias gradient by MMA against ones (2 x 16 TMEM columns beside the accumulators) when they fit
   static constexpr bool DB_MMA = EPI == EPI_ACC_F32 && 2 * BN + 32 <= 512;
   static constexpr int ONES_BYTES = DB_MMA ? 2048 : 0;
@@ -242,8 +246,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 64; ++c, ++step) {
-        uint8_t* stg = sStg + (step & 1) * Cfg::STEP_BOXES * PBOX;
-        if (etid == 0) bulk_wait_read_1();  // the store that last used this buffer has read it
+        uint8_t* stg = sStg + (Cfg::NBUF == 2 ? (step & 1) : 0) * Cfg::STEP_BOXES * PBOX;
+        if (etid == 0) {  // the store that last used this buffer has read it
+          if (Cfg::NBUF == 2) bulk_wait_read_1();
+          else bulk_wait_read_all();
+        }
         epi_bar();
         const int ncol0 = n0 + c * 64 + h * 32;
         const bool full_cols = ncol0 + 32 <= args.N;
