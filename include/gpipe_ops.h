@@ -150,6 +150,12 @@ int gpipe_op_rmsprop(size_t n, float* w, float* g, float* v, void* w_bf16, float
 /* dst[i] = bf16(src[i]) (round to nearest even). */
 int gpipe_op_cast_bf16(size_t n, const float* src, void* dst, void* stream);
 
+/* The GELU arithmetic of the GEMM epilogues, in fp32 (for checking it):
+ * gelu[i] = z Phi(z) and dgelu[i] = Phi(z) + z phi(z) for z = z_in[i] (exact-erf
+ * GELU as the review's Transformer uses it; erf evaluated to within 1.5e-7, see
+ * the kernels).  Either output may be NULL. */
+int gpipe_op_gelu(size_t n, const float* z_in, float* gelu, float* dgelu, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -88,6 +88,7 @@ _SIGS = {
     "gpipe_op_rmsprop": (c_int, [c_size_t, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_float, c_float,
                                  c_int, c_void_p]),
     "gpipe_op_cast_bf16": (c_int, [c_size_t, c_void_p, c_void_p, c_void_p]),
+    "gpipe_op_gelu": (c_int, [c_size_t, c_void_p, c_void_p, c_void_p, c_void_p]),
 }
 
 

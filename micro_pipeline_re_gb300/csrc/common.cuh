@@ -90,13 +90,30 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Exact-erf GELU and its derivative, calling CUDA's erff/expf.
+// Exact-erf GELU, GELU(z) = z Phi(z), and its derivative Phi(z) + z phi(z),
+// with Phi(z) = 1 - erfc(z / sqrt 2) / 2 and phi(z) = e^{-z^2/2} / sqrt(2 pi).
+// erfc(a), a >= 0, by Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26: erfc(a) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^{-a^2},
+// t = 1 / (1 + p a), |error| <= 1.5e-7.  In this erfc form the negative side
+// has no cancellation and the derivative reuses e^{-a^2} (= e^{-z^2/2}).
+// Cheaper than a general erf: one reciprocal and one exponential on the SFU.
+__device__ __forceinline__ float gelu_cdf(float z, float& e) {
+  const float a = fabsf(z) * 0.70710678118654752f;
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, a, 1.0f));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+  e = __expf(-a * a);
+  const float half_erfc = 0.5f * poly * e;
+  return z >= 0.f ? 1.0f - half_erfc : half_erfc;
+}
 __device__ __forceinline__ float gelu_f(float z) {
-  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+  float e;
+  return z * gelu_cdf(z, e);
 }
 __device__ __forceinline__ float gelu_grad_f(float z) {
-  return 0.5f * (1.0f + erff(z * 0.70710678118654752f)) +
-         z * 0.39894228040143268f * expf(-0.5f * z * z);
+  float e;
+  const float cdf = gelu_cdf(z, e);
+  return fmaf(z * 0.39894228040143268f, e, cdf);
 }
 
 // ---------------------------------------------------------------------------

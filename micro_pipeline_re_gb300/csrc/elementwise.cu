@@ -494,7 +494,26 @@ __global__ void count_diff_kernel(const uint32_t* __restrict__ a, const uint32_t
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// GELU and its derivative in fp32 (the epilogues' arithmetic, for checking it).
+__global__ void gelu_kernel(size_t n, const float* __restrict__ z, float* __restrict__ y, float* __restrict__ dy) {
+  griddep_wait();
+  griddep_launch();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    if (y) y[i] = gelu_f(z[i]);
+    if (dy) dy[i] = gelu_grad_f(z[i]);
+  }
+}
+
 }  // namespace
+
+int launch_gelu(size_t n, const float* z, float* y, float* dy, cudaStream_t s) {
+  if (n == 0) return GPIPE_OK;
+  if (!z) return set_error(GPIPE_ERR_INVALID_ARG, "gelu: NULL input");
+  const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 65536));
+  (void)launch_k(gelu_kernel, grid, 256, 0, s, n, z, y, dy);
+  return check_launch("gelu");
+}
 
 size_t colred_scratch_floats(int rows, int cols) {
   const size_t parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;

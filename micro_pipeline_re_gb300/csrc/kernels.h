@@ -66,6 +66,7 @@ int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float*
 int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
                               const float* rstd, const float* g, const void* dres, void* dx, float* scratch,
                               cudaStream_t s);
+int launch_gelu(size_t n, const float* z, float* y, float* dy, cudaStream_t s);
 int launch_layernorm_bwd_reduce(int rows, int d, const float* scratch, float* dg_acc, float* db_acc, cudaStream_t s);
 int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
                          const float* rstd, const float* g, const void* dres, void* dx, float* dg_acc,

@@ -179,4 +179,8 @@ int gpipe_op_cast_bf16(size_t n, const float* src, void* dst, void* stream) {
   return gp::launch_cast_bf16(n, src, dst, static_cast<cudaStream_t>(stream));
 }
 
+int gpipe_op_gelu(size_t n, const float* z_in, float* gelu, float* dgelu, void* stream) {
+  return gp::launch_gelu(n, z_in, gelu, dgelu, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -373,3 +373,29 @@ def test_cast_bf16(b):
     assert b.lib().gpipe_op_cast_bf16(4099, dev(x).data_ptr(), out.data_ptr(), stream()) == 0
     sync()
     assert np.array_equal(out.float().cpu().numpy(), bf16_round(x).astype(np.float32))
+
+
+def test_gelu_arithmetic_within_its_error_bound(b):
+    """The epilogues' GELU and GELU' (erf by Abramowitz & Stegun 7.1.26, whose
+    |error| <= 1.5e-7) against the exact-erf definitions in fp64: the error is
+    at most that bound scaled through GELU, plus fp32 rounding."""
+    from scipy.special import erf
+    t = __import__("torch")
+    rng = np.random.default_rng(11)
+    z = np.concatenate([np.linspace(-12, 12, 200001), rng.standard_normal(100000) * 3]).astype(np.float32)
+    zd = dev(z)
+    y = t.empty_like(zd)
+    dy = t.empty_like(zd)
+    assert b.lib().gpipe_op_gelu(z.size, zd.data_ptr(), y.data_ptr(), dy.data_ptr(), stream()) == 0
+    sync()
+    z64 = z.astype(np.float64)
+    cdf = 0.5 * (1 + erf(z64 / np.sqrt(2)))
+    ref = z64 * cdf
+    dref = cdf + z64 * np.exp(-0.5 * z64 * z64) / np.sqrt(2 * np.pi)
+    err = np.abs(host(y) - ref)
+    derr = np.abs(host(dy) - dref)
+    assert np.all(err <= 1e-7 * np.abs(z64) + 2e-7 * np.abs(ref) + 1e-30), err.max()
+    assert np.all(derr <= 2e-7 + 2e-7 * np.abs(z64) * np.exp(-0.25 * z64 * z64) + 2e-7 * np.abs(dref)), derr.max()
+    # the sign of the tiny negative tail is kept (no cancellation in 1 + erf)
+    neg = z64 < -3
+    assert np.all(host(y)[neg] <= 0)
