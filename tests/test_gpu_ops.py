@@ -377,8 +377,10 @@ def test_cast_bf16(b):
 
 def test_gelu_arithmetic_within_its_error_bound(b):
     """The epilogues' GELU and GELU' (erf by Abramowitz & Stegun 7.1.26, whose
-    |error| <= 1.5e-7) against the exact-erf definitions in fp64: the error is
-    at most that bound scaled through GELU, plus fp32 rounding."""
+    |error| <= 1.5e-7) against the exact-erf definitions in fp64: Phi is off by
+    at most 0.75e-7 from the formula plus ~2e-7 from evaluating it in fp32, so
+    |GELU error| <= 3e-7 |z| (+ rounding of the result) and |GELU' error| <=
+    4e-7 (+ rounding).  CUDA's erff is itself ~2 ulp (~2.4e-7 near 1)."""
     from scipy.special import erf
     t = __import__("torch")
     rng = np.random.default_rng(11)
@@ -394,8 +396,8 @@ def test_gelu_arithmetic_within_its_error_bound(b):
     dref = cdf + z64 * np.exp(-0.5 * z64 * z64) / np.sqrt(2 * np.pi)
     err = np.abs(host(y) - ref)
     derr = np.abs(host(dy) - dref)
-    assert np.all(err <= 1e-7 * np.abs(z64) + 2e-7 * np.abs(ref) + 1e-30), err.max()
-    assert np.all(derr <= 2e-7 + 2e-7 * np.abs(z64) * np.exp(-0.25 * z64 * z64) + 2e-7 * np.abs(dref)), derr.max()
+    assert np.all(err <= 3e-7 * np.abs(z64) + 2e-7 * np.abs(ref)), err.max()
+    assert np.all(derr <= 4e-7 + 2e-7 * np.abs(dref)), derr.max()
     # the sign of the tiny negative tail is kept (no cancellation in 1 + erf)
     neg = z64 < -3
     assert np.all(host(y)[neg] <= 0)
