@@ -34,10 +34,8 @@ namespace {
 
 constexpr int PM = 128;
 constexpr int PK = 64;
-constexpr int P_EPI_WARPS = 16;                 // four per TMEM lane quarter
-constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;  // warp 0 TMA, warp 1 MMA, then the epilogue
-constexpr int P_EPI_THREADS = 32 * P_EPI_WARPS;
-constexpr int P_CW = 64 / (P_EPI_WARPS / 4);     // columns of a 64-column step per epilogue warp
+constexpr int P_THREADS = 320;      // 10 warps
+constexpr int P_EPI_THREADS = 256;  // warps 2..9
 constexpr int PBOX = 16384;         // staging box: 128 rows x 128 B
 constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
 
@@ -143,7 +141,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], P_EPI_WARPS);  // one arrival per epilogue warp
+      mbar_init(&acce[b], 8);  // one arrival per epilogue warp
     }
     *abort = 0;
     fence_barrier_init();
@@ -229,7 +227,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     griddep_launch();
   } else {
-    // ---- epilogue warps: TMEM lane quarter q, column slice h (P_CW wide) of each 64-column step ----
+    // ---- epilogue warps 2..9: TMEM lane quarter q, column half h of each 64-column step ----
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const int r = q * 32 + lane;
@@ -240,7 +238,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int m0, n0;
       tile_origin<BN>(t, args, m0, n0);
       const int m = m0 + r;
-      if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && args.dbias != nullptr && n0 == 0 && warp - 2 < 8 && !*abort)
+      if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && args.dbias != nullptr && n0 == 0 && !*abort)
         bias_grad_rows<A_K>(static_cast<const __nv_bfloat16*>(args.a), args.lda, args.M, args.K, args.dbias, m0,
                             warp - 2, lane);  // overlaps this tile's MMAs
       pwait(&accf[b], (i >> 1) & 1, err, DERR_ACC_WAIT, abort);
@@ -254,70 +252,63 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           else bulk_wait_read_all();
         }
         epi_bar();
-        const int ncol0 = n0 + c * 64 + h * P_CW;
-        const bool full_cols = ncol0 + P_CW <= args.N;
+        const int ncol0 = n0 + c * 64 + h * 32;
+        const bool full_cols = ncol0 + 32 <= args.N;
         // the epilogue input (residual / GELU pre-activation) is read from global
         // memory first, so its latency overlaps the tensor-memory read below
-        float xv[P_CW];
+        float xv[32];
         const bool has_x = !Cfg::F32_OUT && args.xsrc && m < args.M;
         if (has_x) {
           const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx;
           if (full_cols) {
 #pragma unroll
-            for (int j = 0; j < P_CW; j += 8) load8(xr + ncol0 + j, xv + j);
+            for (int j = 0; j < 32; j += 8) load8(xr + ncol0 + j, xv + j);
           } else {
-            for (int j = 0; j < P_CW; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xr[ncol0 + j]) : 0.f;
+            for (int j = 0; j < 32; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xr[ncol0 + j]) : 0.f;
           }
         }
-        uint32_t rr[P_CW];
-        if (P_CW == 32) tmem_ld32(tb + c * 64 + h * P_CW, rr);
-        else tmem_ld16(tb + c * 64 + h * P_CW, rr);
+        uint32_t rr[32];
+        tmem_ld32(tb + c * 64 + h * 32, rr);
         tmem_ld_wait();
-        float v[P_CW];
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < P_CW; ++j) v[j] = __uint_as_float(rr[j]);
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         if (Cfg::F32_OUT) {
-          // fp32: a box holds 32 columns (8 16-B units); this slice starts at unit (h*P_CW % 32) / 4
-          uint8_t* box = stg + (h * P_CW / 32) * PBOX;
-          const int u0 = (h * P_CW % 32) / 4;
+          uint8_t* box = stg + h * PBOX;
 #pragma unroll
-          for (int u = 0; u < P_CW / 4; ++u)
-            *reinterpret_cast<float4*>(box + pswz(r, u0 + u)) =
-                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(box + pswz(r, u)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         } else {
           if ((EPI == EPI_STORE || EPI == EPI_BIAS_GELU) && args.bias) {
             if (full_cols) {
 #pragma unroll
-              for (int j = 0; j < P_CW; j += 8) {
+              for (int j = 0; j < 32; j += 8) {
                 float bb8[8];
                 load8(args.bias + ncol0 + j, bb8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[j + e] += bb8[e];
               }
             } else {
-              for (int j = 0; j < P_CW; ++j)
+              for (int j = 0; j < 32; ++j)
                 if (ncol0 + j < args.N) v[j] += args.bias[ncol0 + j];
             }
           }
           if (has_x) {
 #pragma unroll
-            for (int j = 0; j < P_CW; ++j) {
+            for (int j = 0; j < 32; ++j) {
               if (EPI == EPI_GELU_BWD) v[j] *= gelu_grad_f(xv[j]);
               else v[j] += xv[j];
             }
           }
-          // bf16: a box holds the step's 64 columns (8 16-B units); this slice is units h*P_CW/8 ..
-          constexpr int UPS = P_CW / 8;
 #pragma unroll
-          for (int u = 0; u < UPS; ++u)
-            store8(reinterpret_cast<__nv_bfloat16*>(stg + pswz(r, h * UPS + u)), v + 8 * u);
+          for (int u = 0; u < 4; ++u) store8(reinterpret_cast<__nv_bfloat16*>(stg + pswz(r, h * 4 + u)), v + 8 * u);
           if (EPI == EPI_BIAS_GELU) {
 #pragma unroll
-            for (int u = 0; u < UPS; ++u) {
+            for (int u = 0; u < 4; ++u) {
               float gv[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) gv[e] = gelu_f(v[8 * u + e]);
-              store8(reinterpret_cast<__nv_bfloat16*>(stg + PBOX + pswz(r, h * UPS + u)), gv);
+              store8(reinterpret_cast<__nv_bfloat16*>(stg + PBOX + pswz(r, h * 4 + u)), gv);
             }
           }
         }
