@@ -184,6 +184,13 @@ def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
         args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), K, 1, 0, Z.data_ptr(), N, vec.data_ptr(), None, 0,
                 None, None, 0)
         name = f"projection GEMM (bias, bf16 store) {M}x{N}x{K}"
+    elif epi == 4:
+        A = torch.randn(M, K, device="cuda").to(bf)
+        Bw = torch.randn(N, K, device="cuda").to(bf)
+        C = torch.empty(M, N, device="cuda")
+        args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), K, 1, 4, C.data_ptr(), N, None, None, 0,
+                None, None, 0)
+        name = f"logits GEMM (fp32 store) {M}x{N}x{K}"
     elif epi == 3:
         A = torch.randn(K, M, device="cuda").to(bf)
         Bw = torch.randn(K, N, device="cuda").to(bf)
@@ -437,7 +444,7 @@ def main():
                     help="only run the roofline GEMM (5 eager launches, then a timed graph); for profilers")
     ap.add_argument("--shape", default=None, help="M,N,K for --probe-gemm (default: the workload's FFN1)")
     ap.add_argument("--epi", type=int, default=1,
-                    help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 3 weight gradient")
+                    help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 3 weight gradient, 4 fp32 store")
     ap.add_argument("--reps", type=int, default=100)
     ap.add_argument("--sweep", action="store_true",
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
