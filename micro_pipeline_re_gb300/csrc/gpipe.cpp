@@ -139,9 +139,11 @@ struct gpipe_ctx {
     auto mk_ev = [&](cudaEvent_t& e) {
       return e || cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
     };
-    // Priorities: the cells' main streams (the critical path) highest, the
-    // head's main stream next, the side streams (weight gradients and
-    // gamma/beta reductions, off the critical path) lowest.
+    // Priorities: the head's main stream highest (with three vocabulary-sized
+    // GEMMs per micro-batch it is the heaviest pipeline stage, and the last
+    // cell's backward of each micro-batch waits for it), the cells' main
+    // streams next, the side streams (weight gradients and gamma/beta
+    // reductions, off the critical path) lowest.
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) least = greatest = 0;
     auto mk_st = [&](cudaStream_t& st, int prio) {
@@ -152,7 +154,7 @@ struct gpipe_ctx {
     for (int m = 0; m < M && ok; ++m) ok = mk_ev(ev_hdone[m]);
     for (int i = 0; i < nstreams() && ok; ++i) {
       const bool head = nstreams() > 1 && i == nstreams() - 1;
-      ok = mk_st(lane_main[i], head ? (least + greatest) / 2 : greatest);
+      ok = mk_st(lane_main[i], head || greatest == least ? greatest : greatest + 1);
       for (int j = 0; j < nside && ok; ++j) ok = mk_st(lane_side[i][j], least);
       ok = ok &&
            mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
@@ -542,6 +544,8 @@ class Executor {
         // side stream (weight gradients, off the critical path): a small grid
         // whose CTAs each take many tiles spends the least SM time
         share = share * c_->side_share / 100;
+      } else if (cur_lane_ == head_lane()) {
+        share = num_sms() * c_->sm_share / 200;  // the head's GEMMs: half the machine
       } else if (tiles <= 4 * static_cast<int64_t>(share)) {
         share *= 2;
       }
