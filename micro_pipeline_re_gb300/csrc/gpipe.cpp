@@ -107,7 +107,7 @@ struct gpipe_ctx {
               ev_lane_end[kMaxLanes] = {};
   std::vector<cudaEvent_t> ev_hdone;  // per micro-batch: the head has written the last cell's output gradient
   // streams in use: one pair per lane, plus the head's pair when the cells are pipelined
-  int nstreams() const { return ws.nlanes > 1 ? ws.nlanes + 1 : 1; }
+  int nstreams() const { return ws.nlanes > 1 ? ws.nlanes + ws.nheads : 1; }
   cudaGraphExec_t gexec = nullptr;
   cudaGraph_t graph = nullptr;
   GraphKey key{};
@@ -128,7 +128,7 @@ struct gpipe_ctx {
   void refresh_ws() {
     if (ws_stale) {
       const int nin = inflight_eff();
-      const bool lanes = pipelined && K * nin < kMaxLanes;
+      const bool lanes = pipelined && K * nin + 2 <= kMaxLanes;  // + the head lanes
       ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat, lanes,
                           lanes ? nin : 1);
       ws_stale = false;
@@ -153,7 +153,7 @@ struct gpipe_ctx {
     if (static_cast<int>(ev_hdone.size()) < M) ev_hdone.resize(M, nullptr);
     for (int m = 0; m < M && ok; ++m) ok = mk_ev(ev_hdone[m]);
     for (int i = 0; i < nstreams() && ok; ++i) {
-      const bool head = nstreams() > 1 && i == nstreams() - 1;
+      const bool head = nstreams() > 1 && i >= ws.nlanes;
       ok = mk_st(lane_main[i], head || greatest == least ? greatest : greatest + 1);
       for (int j = 0; j < nside && ok; ++j) ok = mk_st(lane_side[i][j], least);
       ok = ok &&
@@ -267,8 +267,8 @@ class Executor {
     // phase 1: forward of every micro-batch through every cell; then the head
     // (final LN, logits, loss and its gradient) of that micro-batch, once, on
     // its own lane, which hands the last cell the gradient of its output
-    const int hl = head_lane();
     for (int m = 0; m < M; ++m) {
+      const int hl = head_lane(m);
       busy_ = busy_at(m);
       TRY(cell0_input(m));
       for (int k = 0; k < K; ++k) {
@@ -298,7 +298,7 @@ class Executor {
         char* dy;
         const int dy_buf = BUF_EXT;
         if (k == K - 1) {
-          if (hl != lk) TRY(cuda_ok(cudaStreamWaitEvent(main_s(lk), c_->ev_hdone[m], 0), "stream wait"));
+          if (head_lane(m) != lk) TRY(cuda_ok(cudaStreamWaitEvent(main_s(lk), c_->ev_hdone[m], 0), "stream wait"));
           dy = hdy(m);
         } else {
           TRY(cross_wait(k, m, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
@@ -371,10 +371,12 @@ class Executor {
   // Lane of cell k for micro-batch m: with lanes, cell k owns lanes
   // k*inflight .. k*inflight + inflight-1 and takes its micro-batches in turn.
   int lane_of(int k, int m) const { return c_->ws.nlanes > 1 ? k * c_->ws.inflight + m % c_->ws.inflight : 0; }
-  int head_lane() const { return c_->ws.nlanes > 1 ? c_->ws.nlanes : 0; }
+  // Head lanes follow the cells' lanes and take the micro-batches in turn.
+  int head_lane(int m) const { return c_->ws.nlanes > 1 ? c_->ws.nlanes + m % c_->ws.nheads : 0; }
+  bool is_head_lane(int lane) const { return c_->ws.nlanes > 1 && lane >= c_->ws.nlanes; }
   // A cell's lanes share one side stream (its first lane's), which receives the
   // cell's weight-gradient work in micro-batch order.
-  int side_of(int lane) const { return lane < c_->ws.nlanes ? lane - lane % c_->ws.inflight : lane; }
+  int side_of(int lane) const { return lane < c_->ws.nlanes ? lane - lane % c_->ws.inflight : c_->ws.nlanes; }
   char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
   // Weight-gradient work goes to a side stream when CONCURRENT is on, and
@@ -544,7 +546,7 @@ class Executor {
         // side stream (weight gradients, off the critical path): a small grid
         // whose CTAs each take many tiles spends the least SM time
         share = share * c_->side_share / 100;
-      } else if (cur_lane_ == head_lane()) {
+      } else if (is_head_lane(cur_lane_)) {
         share = num_sms() * c_->sm_share / 200;  // the head's GEMMs: half the machine
       } else if (tiles <= 4 * static_cast<int64_t>(share)) {
         share *= 2;
@@ -705,7 +707,8 @@ class Executor {
   int head(int m) {
     const Dims& dm = c_->dm;
     const Workspace& w = c_->ws;
-    cur_lane_ = head_lane();
+    cur_lane_ = head_lane(m);
+    const Workspace::Head& hb = w.head[c_->ws.nlanes > 1 ? m % w.nheads : 0];
     const int T = static_cast<int>(c_->Tmb()), d = dm.d;
     float* loss_rows = reinterpret_cast<float*>(ws(w.loss_rows)) + static_cast<size_t>(m) * T;
     const char* xf = stash(c_->K, m);
@@ -718,23 +721,23 @@ class Executor {
     }
     TRY(join(cur_lane_, EV_HEAD));  // the previous micro-batch's dE GEMM has read the logits and hf
     const float inv = 1.0f / (static_cast<float>(dm.n) * (dm.seq - 1));
-    float* logits = reinterpret_cast<float*>(ws(w.logits));
-    TRY(launch_layernorm_fwd(DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(w.hf),
-                             reinterpret_cast<float*>(ws(w.meanf)), reinterpret_cast<float*>(ws(w.rstdf)), st()));
-    TRY(gemm(T, dm.vocab, d, ws(w.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
+    float* logits = reinterpret_cast<float*>(ws(hb.logits));
+    TRY(launch_layernorm_fwd(DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(hb.hf),
+                             reinterpret_cast<float*>(ws(hb.meanf)), reinterpret_cast<float*>(ws(hb.rstdf)), st()));
+    TRY(gemm(T, dm.vocab, d, ws(hb.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
     TRY(launch_cross_entropy(T, dm.vocab, dm.seq, static_cast<const int32_t*>(p_.batch), m * T, inv, logits,
                              loss_rows, 1, st()));
     // dz (bf16, in place over the logits, leading dimension 2*vocab)
     const int64_t ldz = 2 * static_cast<int64_t>(dm.vocab);
-    char* gt = ws(w.hgt);
+    char* gt = ws(hb.hgt);
     TRY(gemm(T, d, dm.vocab, logits, ldz, true, wgt(c_->pl.emb), d, false, EPI_STORE, gt, d));
     TRY(on_side(EV_HEAD, [&] {
-      return gemm(dm.vocab, d, T, logits, ldz, false, ws(w.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d);
+      return gemm(dm.vocab, d, T, logits, ldz, false, ws(hb.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d);
     }));
-    return ln_backward(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(w.meanf)),
-                       reinterpret_cast<float*>(ws(w.rstdf)), p32(c_->pl.lnf_g), nullptr, dy, grad(c_->pl.lnf_g),
-                       grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(w.hlnp[0])),
-                       reinterpret_cast<float*>(ws(w.hlnp[1])));
+    return ln_backward(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(hb.meanf)),
+                       reinterpret_cast<float*>(ws(hb.rstdf)), p32(c_->pl.lnf_g), nullptr, dy, grad(c_->pl.lnf_g),
+                       grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(hb.hlnp[0])),
+                       reinterpret_cast<float*>(ws(hb.hlnp[1])));
   }
 };
 

@@ -210,15 +210,16 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
   w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
   w.hdy = take(static_cast<size_t>(M) * w.stash_bytes);
-  if (dm.kind == 1) {
-    w.hf = take(Tmb * d * es);
-    w.meanf = take(Tmb * 4);
-    w.rstdf = take(Tmb * 4);
-    w.logits = take(Tmb * static_cast<size_t>(dm.vocab) * 4);
-    w.hgt = take(Tmb * d * es);
-    w.hscratch = take(w.scratch_bytes);
-    w.hlnp[0] = take(w.lnp_bytes);
-    w.hlnp[1] = take(w.lnp_bytes);
+  w.nheads = dm.kind == 1 && w.nlanes > 1 ? 2 : 1;
+  for (int h = 0; h < w.nheads && dm.kind == 1; ++h) {
+    Workspace::Head& hb = w.head[h];
+    hb.hf = take(Tmb * d * es);
+    hb.meanf = take(Tmb * 4);
+    hb.rstdf = take(Tmb * 4);
+    hb.logits = take(Tmb * static_cast<size_t>(dm.vocab) * 4);
+    hb.hgt = take(Tmb * d * es);
+    hb.hlnp[0] = take(w.lnp_bytes);
+    hb.hlnp[1] = take(w.lnp_bytes);
   }
   w.loss_rows = take(T * 4);
   w.act_bytes = off;
@@ -234,13 +235,14 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   // constants, summed over the lanes: the boundary tensors (stash, the
   // embedding's input gradient and the gradient ring; proportional to N), and
   // per lane one cell of Lc layers of kept internals for one micro-batch plus
-  // that lane's gradient buffers (proportional to (L/K)(N/M)); the head's
-  // logits and the per-row losses.
+  // that lane's gradient buffers (proportional to (L/K)(N/M)); per head lane
+  // the logits of one micro-batch and its temporaries; the per-row losses.
   const size_t boundary = static_cast<size_t>(K + 3) * T * d * es + static_cast<size_t>(K) * w.ring * Tmb * d * es;
   const size_t per_lane = ln.bytes + 4096;
   const size_t head =
-      dm.kind == 1 ? Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + w.scratch_bytes + 2 * w.lnp_bytes + 8192
-                   : 0;
+      dm.kind == 1
+          ? w.nheads * (Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + 2 * w.lnp_bytes + 8192)
+          : 0;
   const size_t cell_all = remat ? 0 : static_cast<size_t>(L) * M * w.slot_bytes;
   w.bound_bytes = boundary + static_cast<size_t>(w.nlanes) * per_lane + cell_all + head + T * 4 + 8192;
   return w;

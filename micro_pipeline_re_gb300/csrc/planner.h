@@ -67,9 +67,13 @@ struct Workspace {
   size_t slot_bytes = 0;
   SlotLayout slot{};
   size_t noremat_slots = 0, nslots_noremat = 0;  // L x M slots when re-materialisation is off
-  size_t hf = 0, meanf = 0, rstdf = 0, logits = 0;  // head (kind 1)
-  size_t hgt = 0, hscratch = 0;             // head's gradient temporary and reduction scratch
-  size_t hlnp[2] = {0, 0};                  // head's LayerNorm-backward partials, alternating
+  struct Head {                             // one head lane's buffers (kind 1)
+    size_t hf = 0, meanf = 0, rstdf = 0, logits = 0;
+    size_t hgt = 0;                         // gradient temporary
+    size_t hlnp[2] = {0, 0};                // LayerNorm-backward partials, alternating
+  };
+  Head head[2]{};
+  int nheads = 1;                           // head lanes: 2 (alternate micro-batches) when pipelined
   size_t lnp_bytes = 0;                     // ceil(Tmb / 8) x 2d fp32
   size_t hdy = 0;                           // M x [Tmb, d]: gradient of the last cell's output per micro-batch
   size_t scratch_bytes = 0;
