@@ -139,11 +139,10 @@ struct gpipe_ctx {
     auto mk_ev = [&](cudaEvent_t& e) {
       return e || cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
     };
-    // Priorities: the head's main stream highest (with three vocabulary-sized
-    // GEMMs per micro-batch it is the heaviest pipeline stage, and the last
-    // cell's backward of each micro-batch waits for it), the cells' main
-    // streams next, the side streams (weight gradients and gamma/beta
-    // reductions, off the critical path) lowest.
+    // Priorities: the cells' main streams (the critical path) highest, the
+    // head lanes next (two of them keep ahead of the last cell's backward),
+    // the side streams (weight gradients and gamma/beta reductions, off the
+    // critical path) lowest.
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) least = greatest = 0;
     auto mk_st = [&](cudaStream_t& st, int prio) {
@@ -154,7 +153,7 @@ struct gpipe_ctx {
     for (int m = 0; m < M && ok; ++m) ok = mk_ev(ev_hdone[m]);
     for (int i = 0; i < nstreams() && ok; ++i) {
       const bool head = nstreams() > 1 && i >= ws.nlanes;
-      ok = mk_st(lane_main[i], head || greatest == least ? greatest : greatest + 1);
+      ok = mk_st(lane_main[i], head ? (least + greatest) / 2 : greatest);
       for (int j = 0; j < nside && ok; ++j) ok = mk_st(lane_side[i][j], least);
       ok = ok &&
            mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
