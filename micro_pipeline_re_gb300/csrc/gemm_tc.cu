@@ -74,10 +74,6 @@ struct TcArgs {
   int64_t ldc;
   const void* xsrc;
   int64_t ldx;
-  // split-K through global memory (SPLIT without a cluster): fp32 partial tiles
-  // [tile][split][BM][BN] and a per-tile arrival counter (zero between launches)
-  float* gpart;
-  unsigned* gcnt;
 };
 
 __device__ __forceinline__ uint32_t swz(int r, int unit) {
@@ -215,78 +211,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- epilogue: warp w reads TMEM lanes 32(w%4).. (tile rows 32(w%4) + lane);
   //      warps w and w+4 split the tile's 32-column chunks ----
   const int r = (warp & 3) * 32 + lane;
-  if (SPLIT && args.gpart) {
-    // Split-K through global memory: every CTA stores its fp32 partial tile; the
-    // CTA that arrives last at the tile's counter adds the S partials in split
-    // order (so the result does not depend on arrival order), applies the
-    // epilogue, stores, and resets the counter.  No CTA waits for another.
-    __shared__ int s_last;
-    const int tile = blockIdx.y * gridDim.x + blockIdx.x;
-    float* part = args.gpart + (static_cast<int64_t>(tile) * S + blockIdx.z) * (BM * BN);
-    const bool okp = mbar_wait_bounded(accb, 0, err, DERR_ACC_WAIT);
-    tc_fence_after();
-    if (okp) {
-      const uint32_t tb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-#pragma unroll 1
-      for (int c = warp >> 2; c < BN / 32; c += 2) {
-        uint32_t rr[32];
-        tmem_ld32(tb + c * 32, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          __stcg(reinterpret_cast<float4*>(part + r * BN + c * 32 + 4 * u),
-                 make_float4(__uint_as_float(rr[4 * u]), __uint_as_float(rr[4 * u + 1]),
-                             __uint_as_float(rr[4 * u + 2]), __uint_as_float(rr[4 * u + 3])));
-      }
-    }
-    __threadfence();
-    tc_fence_before();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&args.gcnt[tile], 1u) == static_cast<unsigned>(S - 1);
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      const float* tp = args.gpart + static_cast<int64_t>(tile) * S * (BM * BN);
-      constexpr int groups = BM * (BN / 8);
-      for (int gi = threadIdx.x; gi < groups; gi += THREADS) {
-        const int rr = gi / (BN / 8);
-        const int cc = (gi % (BN / 8)) * 8;
-        const int m = m0 + rr, n = n0 + cc;
-        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int q = 0; q < S; ++q) {
-          const float4* src = reinterpret_cast<const float4*>(tp + static_cast<int64_t>(q) * (BM * BN) + rr * BN + cc);
-          const float4 a = __ldcg(src), b = __ldcg(src + 1);
-          v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
-          v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
-        }
-        if (m < args.M && n < args.N) {
-          if (EPI == EPI_STORE && args.bias) {
-            float bb[8];
-            load8(args.bias + n, bb);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] += bb[j];
-          }
-          if (args.xsrc) {  // residual (store) or GELU pre-activation (GELU backward)
-            float t[8];
-            load8(static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx + n, t);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (EPI == EPI_GELU_BWD) v[j] *= gelu_grad_f(t[j]);
-              else v[j] += t[j];
-            }
-          }
-          store8(static_cast<__nv_bfloat16*>(args.C) + static_cast<int64_t>(m) * args.ldc + n, v);
-        }
-      }
-      if (threadIdx.x == 0) args.gcnt[tile] = 0u;  // ready for the next launch that uses it
-    }
-    __syncthreads();
-    if (warp == 1) {
-      tc_fence_after();
-      tmem_dealloc(tmem, tcols);
-    }
-    return;
-  }
   if (SPLIT) {
     constexpr int PLD = BN + 4;  // padded fp32 row of the partial tile (in the now idle stage buffers)
     float* P = reinterpret_cast<float*>(sA);
@@ -511,18 +435,10 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
   if (!ok) return set_error(GPIPE_ERR_CUDA, "gemm: cuTensorMapEncodeTiled failed");
   int rc = set_attr<A_K, B_K, BN, EPI, SPLIT>();
   if (rc) return rc;
-  TcArgs args{g.bias, g.dbias, g.M, g.N, g.K, has_x, g.C, g.ldc, xsrc, ldx, nullptr, nullptr};
+  TcArgs args{g.bias, g.dbias, g.M, g.N, g.K, has_x, g.C, g.ldc, xsrc, ldx};
   dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, SPLIT ? S : 1);
-  const bool global_split = SPLIT && g.split_ws != nullptr;
-  if (global_split) {
-    const size_t need = static_cast<size_t>(grid.x) * grid.y * S * BM * BN * sizeof(float);
-    if (need > g.split_ws_bytes || static_cast<size_t>(grid.x) * grid.y > g.split_cnt_n)
-      return set_error(GPIPE_ERR_INVALID_ARG, "gemm: split-K workspace too small (%zu bytes needed)", need);
-    args.gpart = g.split_ws;
-    args.gcnt = g.split_cnt;
-  }
   cudaError_t e;
-  if (SPLIT && !global_split) {
+  if (SPLIT) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(THREADS);
@@ -571,17 +487,6 @@ int split_factor(const GemmDesc& g, int BN) {
 
 // S: K split across a cluster of S CTAs (1: none), for the bf16-output
 // epilogues that have a split variant.
-// Split-K through global memory for GEMMs of at most 64 tiles of 128 x 64 and
-// at least 16 k-blocks: S = k-blocks / 8 (each split keeps >= 8), at most 8.
-// These (e.g. 512 x 512 x 2048) otherwise stream all of K through few SMs.
-int split_global_factor(const GemmDesc& g) {
-  const int64_t tiles = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 63) / 64);
-  const int nk = (g.K + BK - 1) / BK;
-  if (tiles > 64 || nk < 16) return 1;
-  const int S = nk / 8;
-  return S > 8 ? 8 : S;
-}
-
 template <int BN>
 int run_epi_bn(const GemmDesc& g, cudaStream_t s, int S) {
   if (g.a_kmajor && g.b_kmajor) {
@@ -624,12 +529,9 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
   // CTA, 128 columns when that gives at least one CTA per SM of the share,
   // else 64 (twice the CTAs, each with half the operand traffic and epilogue).
   // The split-K choice depends on the shape alone (never on the SM share), so
-  // that a GEMM sums in the same order whatever the schedule around it.  With
-  // a split workspace (the step provides one per lane) GEMMs of few tiles and
-  // long K split through global memory; without one, only very long K splits
-  // over a cluster.
+  // that a GEMM sums in the same order whatever the schedule around it.
   const bool has_split = g.a_kmajor && (g.epi == EPI_STORE || (!g.b_kmajor && g.epi == EPI_GELU_BWD));
-  const int S = !has_split ? 1 : (g.split_ws ? split_global_factor(g) : split_factor(g, 64));
+  const int S = has_split ? split_factor(g, 64) : 1;
   if (S > 1) return run_epi_bn<64>(g, s, S);
   const int budget = g.sm_budget > 0 ? g.sm_budget : num_sms();
   if (persistent_tiles(g) > budget || wide_bias_grad_gemm(g)) return launch_gemm_persistent(g, s, budget);

@@ -258,9 +258,6 @@ class Executor {
     // zero the loss scalar and the debug counter, then start every lane
     if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, origin_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
-    if (cudaMemsetAsync(p_.ws + w.splitcnt, 0, static_cast<size_t>(w.nlanes + w.nheads) * Workspace::kSplitCnt * 4,
-                        origin_) != cudaSuccess)
-      return set_error(GPIPE_ERR_CUDA, "memset of the split-K counters failed");
     if (c_->trace) TRY(launch_stamp(stamp(0), origin_));
     TRY(cuda_ok(cudaEventRecord(c_->ev_origin, origin_), "event record"));
     for (int i = 0; i < c_->nstreams(); ++i)
@@ -556,14 +553,6 @@ class Executor {
       g.sm_budget = share < 1 ? 1 : (share > num_sms() ? num_sms() : share);
     } else {
       g.sm_budget = num_sms();
-    }
-    if (c_->ws.split_bytes) {  // this lane's split-K workspace and counters
-      const int lane = cur_lane_;
-      g.split_ws = reinterpret_cast<float*>(
-          is_head_lane(lane) ? ws(c_->ws.head[lane - c_->ws.nlanes].split) : lane_base(lane) + c_->ws.lane.split);
-      g.split_ws_bytes = c_->ws.split_bytes;
-      g.split_cnt = reinterpret_cast<unsigned*>(ws(c_->ws.splitcnt)) + static_cast<size_t>(lane) * Workspace::kSplitCnt;
-      g.split_cnt_n = Workspace::kSplitCnt;
     }
     if (c_->ktime != epi + 1) return launch_gemm(g, st());
     cudaEvent_t e0, e1;

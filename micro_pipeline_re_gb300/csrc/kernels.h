@@ -44,12 +44,6 @@ struct GemmDesc {
   const void* aux = nullptr;
   int64_t ldaux = 0;
   int sm_budget = 0;  // SMs this GEMM may expect to itself (0: all); picks tile width and split-K
-  // optional split-K workspace (fp32 partial tiles) and per-tile counters that
-  // are zero between launches; with it, few-tile long-K GEMMs split K
-  float* split_ws = nullptr;
-  size_t split_ws_bytes = 0;
-  unsigned* split_cnt = nullptr;
-  size_t split_cnt_n = 0;
 };
 
 int launch_gemm(const GemmDesc& g, cudaStream_t stream);       // dispatch by dtype

@@ -190,13 +190,6 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.lnp_bytes = parts * 2 * d * 4;
   ln.lnp[0] = ltake(w.lnp_bytes);
   ln.lnp[1] = ltake(w.lnp_bytes);
-  // The GEMMs with a [Tmb, d] output and long K (FFN output projection, input
-  // gradients of the FFN and QKV projections, the head's dz E) split K through
-  // global memory when they have at most 64 tiles of 128 x 64: up to 8 fp32
-  // partial tiles each.
-  const size_t split_tiles = ((Tmb + 127) / 128) * ((static_cast<size_t>(d) + 63) / 64);
-  w.split_bytes = dm.dtype == 1 && split_tiles <= Workspace::kSplitCnt ? 8 * split_tiles * 128 * 64 * 4 : 0;
-  ln.split = ltake(w.split_bytes);
   ln.bytes = lo;
   w.lane = ln;
   w.inflight = pipelined ? inflight : 1;
@@ -227,10 +220,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     hb.hgt = take(Tmb * d * es);
     hb.hlnp[0] = take(w.lnp_bytes);
     hb.hlnp[1] = take(w.lnp_bytes);
-    hb.split = take(w.split_bytes);
   }
   w.loss_rows = take(T * 4);
-  w.splitcnt = take(static_cast<size_t>(w.nlanes + w.nheads) * Workspace::kSplitCnt * 4);
   w.act_bytes = off;
   w.misc = take(256);
   w.trace_count = 2 + static_cast<size_t>(K + 1) * M * 2;
@@ -250,12 +241,10 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   const size_t per_lane = ln.bytes + 4096;
   const size_t head =
       dm.kind == 1
-          ? w.nheads * (Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + 2 * w.lnp_bytes +
-                        w.split_bytes + 8192)
+          ? w.nheads * (Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + 2 * w.lnp_bytes + 8192)
           : 0;
   const size_t cell_all = remat ? 0 : static_cast<size_t>(L) * M * w.slot_bytes;
-  w.bound_bytes = boundary + static_cast<size_t>(w.nlanes) * per_lane + cell_all + head + T * 4 + 8192 +
-                  static_cast<size_t>(w.nlanes + w.nheads) * Workspace::kSplitCnt * 4;
+  w.bound_bytes = boundary + static_cast<size_t>(w.nlanes) * per_lane + cell_all + head + T * 4 + 8192;
   return w;
 }
 

@@ -52,7 +52,6 @@ struct LaneLayout {
   size_t gf[2] = {0, 0}, gh[2] = {0, 0}, gq[2] = {0, 0};  // weight-gradient operands, alternating by layer
   size_t scratch = 0;                           // reduction partials / attention row sums
   size_t lnp[2] = {0, 0};                       // LayerNorm-backward gamma/beta partials, alternating
-  size_t split = 0;                             // split-K partial tiles (0 bytes when no GEMM splits)
   size_t bytes = 0;
 };
 
@@ -72,13 +71,9 @@ struct Workspace {
     size_t hf = 0, meanf = 0, rstdf = 0, logits = 0;
     size_t hgt = 0;                         // gradient temporary
     size_t hlnp[2] = {0, 0};                // LayerNorm-backward partials, alternating
-    size_t split = 0;                       // split-K partial tiles
   };
   Head head[2]{};
   int nheads = 1;                           // head lanes: 2 (alternate micro-batches) when pipelined
-  size_t split_bytes = 0;                   // per lane: split-K partial tiles of the [Tmb, d] GEMMs
-  size_t splitcnt = 0;                      // (lanes + head lanes) x kSplitCnt zeroed counters
-  static constexpr size_t kSplitCnt = 64;
   size_t lnp_bytes = 0;                     // ceil(Tmb / 8) x 2d fp32
   size_t hdy = 0;                           // M x [Tmb, d]: gradient of the last cell's output per micro-batch
   size_t scratch_bytes = 0;
