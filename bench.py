@@ -249,7 +249,7 @@ EPI_NAMES = {0: "bf16 store epilogue (bias / residual)", 1: "bias + GELU epilogu
 # each from one ncu capture of that shape and epilogue alone (`--probe-gemm`,
 # cold L2): (epilogue, M, N, K) -> bytes.  Inside the step the operands are
 # often still in L2, so this is an upper bound of a launch's DRAM traffic.
-ROOF_TRAFFIC = {(0, 512, 512, 2048): 4212224, (0, 512, 1536, 512): 2119168, (0, 512, 512, 512): 1066496,
+ROOF_TRAFFIC = {(0, 1024, 1024, 8192): 33594368, (0, 512, 512, 2048): 4212224, (0, 512, 1536, 512): 2119168, (0, 512, 512, 512): 1066496,
                 (0, 512, 512, 1536): 3163392,
                 (3, 512, 2048, 512): 6832896, (3, 2048, 512, 512): 6839040, (3, 1536, 512, 512): 5264128,
                 (3, 512, 512, 512): 2114304}
