@@ -16,10 +16,13 @@
  *   - Bubble ("Bubble overhead analysis"): (K-1)/(M+K-1).
  *   - Memory ("Preliminaries 5: re-materialisation"): peak activation memory
  *     O(N + (L/K)(N/M)) instead of O(N L).
- * Here all K cells run on one GPU: each cell is a lane of concurrent CUDA
- * streams ordered by events with exactly the pipeline's dependencies (cell k
- * works on micro-batch m while cell k+1 works on m-1), plus a lane for the
- * head; or, with GPIPE_OPT_PIPELINE = 0, the cells take turns on one lane.
+ * Here all K cells run on one GPU: each cell owns one or more lanes of
+ * concurrent CUDA streams ordered by events with exactly the pipeline's
+ * dependencies (cell k works on micro-batch m while cell k+1 works on m-1;
+ * with two lanes per cell, GPIPE_OPT_INFLIGHT, a cell also overlaps two of its
+ * micro-batches), plus lanes for the head; or, with GPIPE_OPT_PIPELINE = 0,
+ * the cells take turns on one lane.  Every parameter's gradient accumulates
+ * on one stream in micro-batch order, so all schedules give identical bits.
  *
  * Conventions for every function:
  *   - Return value: 0 (GPIPE_OK) or a negative GPIPE_ERR_* code; the message of
@@ -120,8 +123,9 @@ int gpipe_init_params(gpipe_ctx* ctx, const float* params_fp32, void* params_bf1
  *   targets     kind 1: NULL (next-token targets come from batch_in);
  *               kind 0: fp32 targets [N, d]
  *   workspace   device buffer of gpipe_sizes' workspace_bytes, 256-B aligned;
- *               holds the boundary stash, one cell's re-computed internals and
- *               all scratch.  Its contents need no initialisation.
+ *               holds the boundary stash, each lane's re-computed cell
+ *               internals and all scratch.  Its contents need no
+ *               initialisation.
  *   loss_out    host float* or NULL.  When non-NULL the stream is synchronised,
  *               the device error flag is checked and the mean loss is written.
  * The step is captured into a CUDA graph on first use (per pointer set) and
@@ -147,10 +151,13 @@ int gpipe_schedule_model(const gpipe_ctx* ctx, const double* t_f, const double* 
  *                     stash + the re-computed cell's internals + head + the
  *                     gradients in flight); all of it is live at the peak;
  *   model_bound_bytes the review's bound O(N + (L/K)(N/M)) with explicit
- *                     constants: (K+1) T d e  +  Lc (T/M) a  +  (T/M) h,
- *                     T = tokens per step, e = activation element bytes,
- *                     Lc = largest cell's layer count, a = bytes one layer
- *                     keeps per token, h = per-token head/gradient bytes.
+ *                     constants: (K+3) T d e + K R (T/M) d e  +  lanes
+ *                     (Lc (T/M) a + (T/M) g)  +  heads (T/M) h, T = tokens per
+ *                     step, e = activation element bytes, R = gradient-ring
+ *                     depth, lanes = K x micro-batches in flight (1 without
+ *                     lanes), Lc = largest cell's layer count, a = bytes one
+ *                     layer keeps per token, g = per-token gradient bytes of a
+ *                     lane, h = per-token head bytes (logits included).
  * Either output may be NULL. */
 int gpipe_memory_report(const gpipe_ctx* ctx, size_t* peak_act_bytes, size_t* model_bound_bytes);
 
