@@ -443,6 +443,8 @@ def main():
     ap.add_argument("--probe-gemm", action="store_true",
                     help="only run the roofline GEMM (5 eager launches, then a timed graph); for profilers")
     ap.add_argument("--shape", default=None, help="M,N,K for --probe-gemm (default: the workload's FFN1)")
+    ap.add_argument("--sms", type=int, default=0,
+                    help="--probe-gemm: the GEMM's SM share (its grid as the step would size it); 0: all SMs")
     ap.add_argument("--epi", type=int, default=1,
                     help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 3 weight gradient, 4 fp32 store")
     ap.add_argument("--reps", type=int, default=100)
@@ -457,6 +459,8 @@ def main():
         _build()
         from micro_pipeline_re_gb300 import binding as b
         shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else (w.tokens // w.M, w.ffn, w.d)
+        if args.sms:
+            assert b.lib().gpipe_op_gemm_set_sm_share(args.sms) == 0
         print(json.dumps(gemm_roofline(b, load_peaks(), shape, args.epi, reps=args.reps)), flush=True)
         return
     if args.sweep:

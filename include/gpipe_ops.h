@@ -56,6 +56,12 @@ int gpipe_op_gemm(int dtype, int M, int N, int K,
                   float* bias, const void* resid, int64_t ldr,
                   void* C2, const void* aux, int64_t ldaux, void* stream);
 
+/* SM share of the GEMMs this host thread launches through gpipe_op_gemm from
+ * now on: sms > 0 sizes their grids (and so the tile width and kernel) as the
+ * step does for a GEMM given that many SMs; 0 (the default) gives each the
+ * whole GPU.  Returns 0, or GPIPE_ERR_INVALID_ARG for sms < 0. */
+int gpipe_op_gemm_set_sm_share(int sms);
+
 /* Bytes of fp32 scratch the two-stage column reductions below need. */
 size_t gpipe_op_scratch_bytes(int rows, int cols);
 

@@ -83,6 +83,16 @@ using gp::set_error;
 
 extern "C" {
 
+namespace {
+thread_local int g_op_sm_share = 0;
+}
+
+int gpipe_op_gemm_set_sm_share(int sms) {
+  if (sms < 0) return gp::set_error(GPIPE_ERR_INVALID_ARG, "gemm SM share must be >= 0");
+  g_op_sm_share = sms;
+  return GPIPE_OK;
+}
+
 int gpipe_op_gemm(int dtype, int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
                   int64_t ldb, int b_kmajor, int epi, void* C, int64_t ldc, float* bias, const void* resid,
                   int64_t ldr, void* C2, const void* aux, int64_t ldaux, void* stream) {
@@ -107,6 +117,7 @@ int gpipe_op_gemm(int dtype, int M, int N, int K, const void* A, int64_t lda, in
   g.C2 = C2;
   g.aux = aux;
   g.ldaux = ldaux;
+  g.sm_budget = g_op_sm_share;
   return gp::launch_gemm(g, static_cast<cudaStream_t>(stream));
 }
 

@@ -401,3 +401,37 @@ def test_gelu_arithmetic_within_its_error_bound(b):
     # the sign of the tiny negative tail is kept (no cancellation in 1 + erf)
     neg = z64 < -3
     assert np.all(host(y)[neg] <= 0)
+
+
+@pytest.mark.parametrize("ak,bk,epi,shape", [(1, 1, 1, (1024, 2048, 512)), (1, 1, 0, (512, 1536, 512)),
+                                             (1, 0, 2, (512, 2048, 512)), (0, 0, 3, (2048, 512, 512)),
+                                             (0, 0, 3, (1152, 1088, 256))])
+def test_gemm_bits_do_not_depend_on_sm_share(b, ak, bk, epi, shape):
+    """The step sizes each GEMM's grid by its share of the SMs, which changes
+    the kernel (one tile per CTA, 64/128 wide, or persistent 128/256 wide) but
+    must not change a bit of the result."""
+    t = __import__("torch")
+    M, N, K = shape
+    rng = np.random.default_rng(M + N + K + epi)
+    A = dev(bf16_round(rng.standard_normal((M, K) if ak else (K, M))), "bf16")
+    B = dev(bf16_round(rng.standard_normal((N, K) if bk else (K, N)) / np.sqrt(K)), "bf16")
+    bias = dev(rng.standard_normal(N if epi != 3 else M).astype(np.float32))
+    aux = dev(bf16_round(rng.standard_normal((M, N))), "bf16") if epi == 2 else None
+    outs = []
+    for share in (0, 16, 40, 7):
+        assert b.lib().gpipe_op_gemm_set_sm_share(share) == 0
+        C = t.zeros((M, N), device="cuda", dtype=t.float32 if epi == 3 else t.bfloat16)
+        C2 = t.zeros((M, N), device="cuda", dtype=t.bfloat16) if epi == 1 else None
+        db = bias.clone() if epi == 3 else bias
+        rc = b.lib().gpipe_op_gemm(1, M, N, K, A.data_ptr(), K if ak else M, ak, B.data_ptr(), K if bk else N, bk,
+                                   epi, C.data_ptr(), N, db.data_ptr(), None, 0,
+                                   C2.data_ptr() if C2 is not None else None,
+                                   aux.data_ptr() if aux is not None else None, N if aux is not None else 0,
+                                   stream())
+        assert rc == 0, b.lib().gpipe_last_error(None)
+        sync()
+        outs.append([C.cpu(), C2.cpu() if C2 is not None else None, db.cpu() if epi == 3 else None])
+    assert b.lib().gpipe_op_gemm_set_sm_share(0) == 0
+    for o in outs[1:]:
+        for x, y in zip(o, outs[0]):
+            assert (x is None and y is None) or t.equal(x, y)
