@@ -471,16 +471,20 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
 // keeps at least 32 k-blocks (so the per-CTA set-up stays small against its
 // work), up to 8 (a portable cluster) and never more CTAs than two per SM.
 // Split K across S (<= 8) CTAs of a cluster while each split keeps at least
-// kMinSplitBlocks k-blocks and the tiles x S stay within two waves.  Only very
-// long K qualifies (the head's dh = dz E, K = vocab): splitting mid-length K
-// (2048) made single GEMMs faster but the concurrent step slower, as cluster
-// launches wait for co-resident SMs that other lanes hold.
+// kMinSplitBlocks k-blocks and the tiles x S stay within two waves, and only
+// for GEMMs of at most 64 tiles of 128 x 64: in the concurrent step cluster
+// launches wait for co-resident SMs that other lanes hold, so only very long
+// K with few tiles (the head's dh = dz E, K = vocab) gains.  (Measured: splits
+// of mid-length K (2048) slowed the small LM's step, and splitting the wide
+// LM's 128-tile 1024 x 1024 x 8192 GEMMs cost it 16%.)
 constexpr int kMinSplitBlocks = 32;
+constexpr int64_t kMaxSplitTiles = 64;
 
 int split_factor(const GemmDesc& g, int BN) {
   const int64_t tiles = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int nk = (g.K + BK - 1) / BK;
   int S = 1;
+  if (tiles > kMaxSplitTiles) return 1;
   while (S < 8 && nk / (S * 2) >= kMinSplitBlocks && tiles * S * 2 <= 2 * static_cast<int64_t>(num_sms())) S *= 2;
   return S;
 }
