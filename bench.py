@@ -184,6 +184,14 @@ def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
         args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), K, 1, 0, Z.data_ptr(), N, vec.data_ptr(), None, 0,
                 None, None, 0)
         name = f"projection GEMM (bias, bf16 store) {M}x{N}x{K}"
+    elif epi == 2:
+        A = torch.randn(M, K, device="cuda").to(bf)
+        Bw = torch.randn(K, N, device="cuda").to(bf)
+        X = torch.randn(M, N, device="cuda").to(bf)
+        C = torch.empty(M, N, device="cuda", dtype=bf)
+        args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), N, 0, 2, C.data_ptr(), N, None, None, 0,
+                None, X.data_ptr(), N)
+        name = f"GELU-backward GEMM (input gradient x GELU'(z)) {M}x{N}x{K}"
     elif epi == 4:
         A = torch.randn(M, K, device="cuda").to(bf)
         Bw = torch.randn(N, K, device="cuda").to(bf)
@@ -446,7 +454,8 @@ def main():
     ap.add_argument("--sms", type=int, default=0,
                     help="--probe-gemm: the GEMM's SM share (its grid as the step would size it); 0: all SMs")
     ap.add_argument("--epi", type=int, default=1,
-                    help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 3 weight gradient, 4 fp32 store")
+                    help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 2 GELU backward, 3 weight gradient, "
+                         "4 fp32 store")
     ap.add_argument("--reps", type=int, default=100)
     ap.add_argument("--sweep", action="store_true",
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")

@@ -39,7 +39,10 @@ constexpr int P_EPI_THREADS = 256;  // warps 2..9
 constexpr int PBOX = 16384;         // staging box: 128 rows x 128 B
 constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
 
-template <int BN, int EPI>
+// SK (short K): two-box epilogue steps double-buffered too.  With few k-blocks
+// per tile the epilogue bounds the tile rate and the overlap pays; with many,
+// the fourth operand stage that single buffering leaves room for pays more.
+template <int BN, int EPI, bool SK = false>
 struct PCfg {
   static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
   static constexpr int A_BYTES = PM * PK * 2;
@@ -50,7 +53,7 @@ struct PCfg {
   // one-box steps are double-buffered (a step's store overlaps the next step);
   // two-box steps single-buffered, which leaves room for a fourth operand stage
   // at 256 columns (measured faster than the overlap)
-  static constexpr int NBUF = STEP_BOXES == 1 ? 2 : 1;
+  static constexpr int NBUF = (STEP_BOXES == 1 || SK) ? 2 : 1;
   static constexpr int STAGING = NBUF * STEP_BOXES * PBOX;
   // bias gradient by MMA against ones (2 x 16 TMEM columns beside the accumulators) when they fit
   static constexpr bool DB_MMA = EPI == EPI_ACC_F32 && 2 * BN + 32 <= 512;
@@ -109,12 +112,12 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, int* err, 
   return false;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
+template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>
 __global__ void __launch_bounds__(P_THREADS, 1)
     tc_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                        PArgs args, int* err) {
-  using Cfg = PCfg<BN, EPI>;
+  using Cfg = PCfg<BN, EPI, SK>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -381,21 +384,21 @@ bool pmake_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
+template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>
 int pset_attr() {
   static bool done = false;
   if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI, SK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI, SK>::SMEM);
     if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "persistent gemm: smem attribute: %s", cudaGetErrorString(e));
     done = true;
   }
   return GPIPE_OK;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
+template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>
 int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
-  using Cfg = PCfg<BN, EPI>;
+  using Cfg = PCfg<BN, EPI, SK>;
   CUtensorMap ta, tb, tc, tc2;
   bool ok = A_K ? pmake_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, PM) : pmake_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
   ok = ok && (B_K ? pmake_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, BN)
@@ -404,7 +407,7 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   tc2 = tc;
   if (EPI == EPI_BIAS_GELU) ok = ok && pmake_tmap(&tc2, g.C2, false, g.N, g.M, g.ldc, 64, PM);
   if (!ok) return set_error(GPIPE_ERR_CUDA, "persistent gemm: cuTensorMapEncodeTiled failed");
-  int rc = pset_attr<A_K, B_K, BN, EPI>();
+  int rc = pset_attr<A_K, B_K, BN, EPI, SK>();
   if (rc) return rc;
   PArgs args{};
   args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU) ? g.bias : nullptr;
@@ -420,7 +423,7 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   args.n_tiles = (g.N + BN - 1) / BN;
   const int tiles = args.m_tiles * args.n_tiles;
   const int grid = ctas < tiles ? ctas : tiles;
-  (void)launch_k<true>(tc_gemm_persistent<A_K, B_K, BN, EPI>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
+  (void)launch_k<true>(tc_gemm_persistent<A_K, B_K, BN, EPI, SK>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
                                                                                device_error_ptr());
   count_launch();
   cudaError_t e = cudaGetLastError();
@@ -444,7 +447,9 @@ int dispatch(const GemmDesc& g, cudaStream_t s, int ctas) {
   if (g.a_kmajor && g.b_kmajor) {
     switch (g.epi) {
       case EPI_STORE: return prun<true, true, BN, EPI_STORE>(g, s, ctas);
-      case EPI_BIAS_GELU: return prun<true, true, BN, EPI_BIAS_GELU>(g, s, ctas);
+      case EPI_BIAS_GELU:
+        return (g.K + PK - 1) / PK < 32 ? prun<true, true, BN, EPI_BIAS_GELU, true>(g, s, ctas)
+                                        : prun<true, true, BN, EPI_BIAS_GELU>(g, s, ctas);
       case EPI_STORE_F32: return prun<true, true, BN, EPI_STORE_F32>(g, s, ctas);
       case EPI_ACC_F32: return prun<true, true, BN, EPI_ACC_F32>(g, s, ctas);
     }
@@ -468,6 +473,7 @@ int prepare_bn() {
   int rc = GPIPE_OK;
   rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU, true>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE_F32>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_ACC_F32>();
   rc = rc ? rc : pset_attr<true, false, BN, EPI_STORE>();
