@@ -244,11 +244,31 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && args.dbias != nullptr && n0 == 0 && !*abort)
         bias_grad_rows<A_K>(static_cast<const __nv_bfloat16*>(args.a), args.lda, args.M, args.K, args.dbias, m0,
                             warp - 2, lane);  // overlaps this tile's MMAs
+      // The epilogue input (residual / GELU pre-activation) of this thread's row
+      // is read one 64-column step ahead: step 0 before waiting for the
+      // accumulator, step c+1 while step c is processed.
+      const bool has_x = !Cfg::F32_OUT && args.xsrc != nullptr && m < args.M;
+      const __nv_bfloat16* xrow =
+          has_x ? static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx : nullptr;
+      uint4 xnext[4];
+      auto load_x = [&](int cc, uint4* dst) {
+        const int col = n0 + cc * 64 + h * 32;
+        if (has_x && col + 32 <= args.N) {
+          const uint4* src = reinterpret_cast<const uint4*>(xrow + col);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = src[j];
+        }
+      };
+      load_x(0, xnext);
       pwait(&accf[b], (i >> 1) & 1, err, DERR_ACC_WAIT, abort);
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 64; ++c, ++step) {
+        uint4 xcur[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xcur[j] = xnext[j];
+        if (c + 1 < BN / 64) load_x(c + 1, xnext);
         uint8_t* stg = sStg + (Cfg::NBUF == 2 ? (step & 1) : 0) * Cfg::STEP_BOXES * PBOX;
         if (etid == 0) {  // the store that last used this buffer has read it
           if (Cfg::NBUF == 2) bulk_wait_read_1();
@@ -257,17 +277,21 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         epi_bar();
         const int ncol0 = n0 + c * 64 + h * 32;
         const bool full_cols = ncol0 + 32 <= args.N;
-        // the epilogue input (residual / GELU pre-activation) is read from global
-        // memory first, so its latency overlaps the tensor-memory read below
         float xv[32];
-        const bool has_x = !Cfg::F32_OUT && args.xsrc && m < args.M;
         if (has_x) {
-          const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx;
           if (full_cols) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) load8(xr + ncol0 + j, xv + j);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t w4[4] = {xcur[j].x, xcur[j].y, xcur[j].z, xcur[j].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16x2(w4[e]);
+                xv[8 * j + 2 * e] = f.x;
+                xv[8 * j + 2 * e + 1] = f.y;
+              }
+            }
           } else {
-            for (int j = 0; j < 32; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xr[ncol0 + j]) : 0.f;
+            for (int j = 0; j < 32; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xrow[ncol0 + j]) : 0.f;
           }
         }
         uint32_t rr[32];
