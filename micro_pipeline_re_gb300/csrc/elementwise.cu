@@ -224,6 +224,82 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict
 }
 
 // ---------------------------------------------------------------------------
+// Bias gradient of a weight-gradient GEMM (db[m] += sum_k A(m, k)) in one
+// launch without scratch, fixed order.
+//  - A MN-major (stored [K][M], the step's dY): block b owns the 64 columns
+//    m = 64b .. 64b+63; thread t sums the 8 columns 8(t%8).. over rows
+//    k = t/8, t/8 + 32, ... (16-B loads, a row's 128 B read by 8 threads), then
+//    the 32 row groups are added in order through shared memory.
+//  - A K-major (stored [M][K]): one warp per row m, lanes over k, shuffle fold.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dbias_mn_kernel(const __nv_bfloat16* __restrict__ a, int64_t lda, int M,
+                                                        int K, float* __restrict__ db) {
+  griddep_wait();
+  griddep_launch();
+  __shared__ float part[32][64 + 1];
+  const int c8 = (threadIdx.x & 7) * 8, g = threadIdx.x >> 3;
+  const int m0 = blockIdx.x * 64;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (m0 + c8 + 8 <= M) {
+    int k = g;
+    for (; k + 96 < K; k += 128) {  // four rows in flight
+      float v0[8], v1[8], v2[8], v3[8];
+      load8(a + static_cast<int64_t>(k) * lda + m0 + c8, v0);
+      load8(a + static_cast<int64_t>(k + 32) * lda + m0 + c8, v1);
+      load8(a + static_cast<int64_t>(k + 64) * lda + m0 + c8, v2);
+      load8(a + static_cast<int64_t>(k + 96) * lda + m0 + c8, v3);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += v0[j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += v1[j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += v2[j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += v3[j];
+    }
+    for (; k < K; k += 32) {
+      float v[8];
+      load8(a + static_cast<int64_t>(k) * lda + m0 + c8, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += v[j];
+    }
+  } else {
+    for (int k = g; k < K; k += 32)
+      for (int j = 0; j < 8; ++j)
+        if (m0 + c8 + j < M) acc[j] += bf2f(a[static_cast<int64_t>(k) * lda + m0 + c8 + j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[g][c8 + j] = acc[j];
+  __syncthreads();
+  if (threadIdx.x < 64 && m0 + static_cast<int>(threadIdx.x) < M) {
+    float t = part[0][threadIdx.x];
+    for (int r = 1; r < 32; ++r) t += part[r][threadIdx.x];
+    db[m0 + threadIdx.x] += t;
+  }
+}
+
+__global__ void __launch_bounds__(256) dbias_k_kernel(const __nv_bfloat16* __restrict__ a, int64_t lda, int M, int K,
+                                                       float* __restrict__ db) {
+  griddep_wait();
+  griddep_launch();
+  const int m = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (m >= M) return;
+  const __nv_bfloat16* row = a + static_cast<int64_t>(m) * lda;
+  float s = 0.f;
+  const int full = K / 8;
+  for (int j = lane; j < full; j += 32) {
+    float v[8];
+    load8(row + 8 * j, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += v[e];
+  }
+  if (lane == 0)
+    for (int k = 8 * full; k < K; ++k) s += bf2f(row[k]);
+  s = warp_sum(s);
+  if (lane == 0) db[m] += s;
+}
+
+// ---------------------------------------------------------------------------
 // Softmax cross-entropy on fp32 logits, one CTA (512 threads) per row.
 // ---------------------------------------------------------------------------
 constexpr int kCeThreads = 512;
@@ -579,6 +655,15 @@ int launch_layernorm_bwd(int dtype, int rows, int d, const void* dy, const void*
                          float* db_acc, float* scratch, cudaStream_t s) {
   const int rc = launch_layernorm_bwd_rows(dtype, rows, d, dy, x, mean, rstd, g, dres, dx, scratch, s);
   return rc ? rc : launch_layernorm_bwd_reduce(rows, d, scratch, dg_acc, db_acc, s);
+}
+
+int launch_dbias(bool a_kmajor, int M, int K, const void* a, int64_t lda, float* db, cudaStream_t s) {
+  const __nv_bfloat16* ap = static_cast<const __nv_bfloat16*>(a);
+  if (a_kmajor)
+    (void)launch_k(dbias_k_kernel, blocks_for(M, 8), 256, 0, s, ap, lda, M, K, db);
+  else
+    (void)launch_k(dbias_mn_kernel, blocks_for(M, 64), 256, 0, s, ap, lda, M, K, db);
+  return check_launch("bias gradient");
 }
 
 int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, float* out_acc, float* scratch,

@@ -17,14 +17,12 @@
 //                     overlaps step s+1), or TMA-reduce-adds the fp32 gradient
 //                     (the bias gradient, sum over k of A: with 128-wide tiles an
 //                     M=128, N=16 MMA against a tile of ones into TMEM beside
-//                     the accumulators; with 256-wide tiles, which fill TMEM,
-//                     summed by the epilogue warps from global memory while the
-//                     tile's MMAs run)
+//                     the accumulators; 256-wide tiles fill TMEM, so callers
+//                     add it with a separate reduction)
 // Bounded waits as in the single-tile kernel.
 #include <cuda.h>
 
 #include "../../include/gpipe.h"
-#include "bias_grad.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "launch_util.cuh"
@@ -76,8 +74,6 @@ constexpr int PGROUP = 16;  // row tiles per group of the tile order
 struct PArgs {
   const float* bias;   // fp32 [N] (store / bias+GELU) or NULL
   float* dbias;        // EPI_ACC_F32: fp32 [M] += sum_k A(m,k), or NULL
-  const void* a;       // A (bf16), for the bias gradient
-  int64_t lda;
   const void* xsrc;    // residual (store) or GELU pre-activation (GELU backward), bf16, or NULL
   int64_t ldx;
   int M, N, K;
@@ -241,9 +237,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int m0, n0;
       tile_origin<BN>(t, args, m0, n0);
       const int m = m0 + r;
-      if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && args.dbias != nullptr && n0 == 0 && !*abort)
-        bias_grad_rows<A_K>(static_cast<const __nv_bfloat16*>(args.a), args.lda, args.M, args.K, args.dbias, m0,
-                            warp - 2, lane);  // overlaps this tile's MMAs
       // The epilogue input (residual / GELU pre-activation) of this thread's row
       // is read one 64-column step ahead: step 0 before waiting for the
       // accumulator, step c+1 while step c is processed.
@@ -436,8 +429,8 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   PArgs args{};
   args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU) ? g.bias : nullptr;
   args.dbias = EPI == EPI_ACC_F32 ? g.dbias : nullptr;
-  args.a = g.A;
-  args.lda = g.lda;
+  if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && g.dbias)
+    return set_error(GPIPE_ERR_UNSUPPORTED, "persistent gemm: no bias gradient with 256-wide tiles");
   args.xsrc = EPI == EPI_STORE ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : nullptr);
   args.ldx = EPI == EPI_STORE ? g.ldr : g.ldaux;
   args.M = g.M;
@@ -515,15 +508,14 @@ int64_t persistent_tiles(const GemmDesc& g) {
   return static_cast<int64_t>((g.M + PM - 1) / PM) * ((g.N + 127) / 128);
 }
 
-// A weight-gradient GEMM with a bias gradient sums that gradient by MMA with
-// 128-wide tiles and in SIMT with 256-wide ones (different rounding), so its
-// tile width must not depend on the SM share: 256 exactly when
-// wide_bias_grad_gemm(g) (then always the persistent kernel), else 128.
+// A weight-gradient GEMM with a bias gradient gets it by an MMA against ones
+// beside 128-wide accumulators; for large ones (wide_bias_grad_gemm: M and N
+// >= 1024, a shape-only rule) the caller runs the GEMM without it, on any
+// tiles, and adds it with a separate reduction.
 bool wide_bias_grad_gemm(const GemmDesc& g) { return g.epi == EPI_ACC_F32 && g.dbias && g.M >= 1024 && g.N >= 1024; }
 
 int launch_gemm_persistent(const GemmDesc& g, cudaStream_t s, int ctas) {
-  if (g.epi == EPI_ACC_F32 && g.dbias)
-    return wide_bias_grad_gemm(g) ? dispatch<256>(g, s, ctas) : dispatch<128>(g, s, ctas);
+  if (g.epi == EPI_ACC_F32 && g.dbias) return dispatch<128>(g, s, ctas);  // bias gradient by ones-MMA
   return wide_tiles(g, ctas) ? dispatch<256>(g, s, ctas) : dispatch<128>(g, s, ctas);
 }
 

@@ -538,7 +538,17 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
   const int S = has_split ? split_factor(g, 64) : 1;
   if (S > 1) return run_epi_bn<64>(g, s, S);
   const int budget = g.sm_budget > 0 ? g.sm_budget : num_sms();
-  if (persistent_tiles(g) > budget || wide_bias_grad_gemm(g)) return launch_gemm_persistent(g, s, budget);
+  if (wide_bias_grad_gemm(g)) {
+    // 256-wide tiles leave no tensor memory for the ones-MMA, and summing A
+    // inside the GEMM's epilogue cost it up to 40%: the GEMM runs without the
+    // bias gradient and one reduction kernel adds it (shape-only choice, so
+    // every schedule sums it the same way)
+    GemmDesc w = g;
+    w.dbias = nullptr;
+    const int rc = launch_gemm_persistent(w, s, budget);
+    return rc ? rc : launch_dbias(g.a_kmajor, g.M, g.K, g.A, g.lda, g.dbias, s);
+  }
+  if (persistent_tiles(g) > budget) return launch_gemm_persistent(g, s, budget);
   const int64_t tiles128 = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 127) / 128);
   if (tiles128 >= budget) return run_epi_bn<128>(g, s, 1);
   return run_epi_bn<64>(g, s, 1);
