@@ -172,9 +172,12 @@ enum {
                                 differ from the re-computed ones
                                 (gpipe_debug_counters); set before gpipe_sizes       */
   GPIPE_OPT_SKIP_UPDATE = 5, /* [0] 1: accumulate gradients but apply no update     */
-  GPIPE_OPT_CONCURRENT = 6,  /* [1] run weight-gradient GEMMs and the loss-only head
-                                forward on a second stream per lane (ordered by
-                                events); 0: in program order.  Results are identical. */
+  GPIPE_OPT_CONCURRENT = 6,  /* [1] run weight-gradient work on side streams of each
+                                lane (ordered by events); 0: in program order on the
+                                lane's stream, which applies to one lane per cell and
+                                one head lane, i.e. GPIPE_OPT_PIPELINE = 0 (lanes that
+                                share a cell or the head always share side streams).
+                                Results are identical.                              */
   GPIPE_OPT_PIPELINE = 7,    /* [1] run the K cells as K concurrent lanes, each with its
                                 own cell workspace: cell k works on micro-batch m while
                                 cell k+1 works on m-1, as the review's K accelerators

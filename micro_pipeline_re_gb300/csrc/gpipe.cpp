@@ -379,9 +379,9 @@ class Executor {
   char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
   // Weight-gradient work goes to a side stream when CONCURRENT is on, and
-  // always with two micro-batches in flight (the cell's two lanes must not
+  // always when a cell or the head has more than one lane (its lanes must not
   // accumulate into the same gradients from two streams).
-  bool use_side() const { return c_->concurrent || c_->ws.inflight > 1; }
+  bool use_side() const { return c_->concurrent || c_->ws.inflight > 1 || c_->ws.nheads > 1; }
   // The side stream of a parameter group: the group of the event that marks
   // its work (W2, W1, W_o, W_qkv weight gradients, LayerNorm reductions; the
   // head's dE with W2).  A group always goes to the same stream, so each
