@@ -293,6 +293,22 @@ def live_roofline(kt, peaks, b):
             "isolated": gemm_roofline(b, peaks, shape, ROOF_EPI)}
 
 
+def max_over_ranks(value, dist, device):
+    """Max of a per-rank float over the process group (the slowest replica sets
+    the job's time); the value itself without a group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, t_step):
+    """Whole-job tokens/s of N independent replicas timed by the slowest."""
+    return tokens_per_rank * world / t_step
+
+
 def run_ours(args, w):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -334,12 +350,9 @@ def run_ours(args, w):
         dist.barrier()
     t_step = ev0.elapsed_time(ev1) / 1e3 / args.steps
     clocks = clk.summary()
-    if dist:
-        tt = torch.tensor([t_step], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = tt.item()
+    t_step = max_over_ranks(t_step, dist, "cuda")
     tokens_all = w.tokens * world
-    value = tokens_all / t_step
+    value = job_throughput(w.tokens, world, t_step)
     mf = model_flops(w)
     bounds = gp.partition()
     hf = mf + recompute_flops(w, bounds)
@@ -354,10 +367,7 @@ def run_ours(args, w):
         st.batch.copy_(host_tok, non_blocking=True)
         st.step(want_loss=True)
     t_e2e = (time.perf_counter() - t0) / e2e_steps
-    if dist:
-        tt = torch.tensor([t_e2e], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = tt.item()
+    t_e2e = max_over_ranks(t_e2e, dist, "cuda")
     # roofline pass: the same step again with timing events around every launch
     # of the roofline class (the event nodes slow the step, so not in the region above)
     gp.set_option(b.OPT_KERNEL_TIMES, ROOF_EPI + 1)
