@@ -97,7 +97,7 @@ struct gpipe_ctx {
   std::vector<int32_t> kt_mnk;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
   static constexpr int kMaxLanes = 128;
-  static constexpr int kLaneEvents = 14;
+  static constexpr int kLaneEvents = 13;
   static constexpr int kSides = 4;  // most side streams per lane
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes][kSides] = {};
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
@@ -221,7 +221,6 @@ enum {
   EV_DY1,
   EV_DYB,
   EV_HEAD,
-  EV_HEADF,
   EV_LN0,
   EV_LN1,
   EV_COUNT

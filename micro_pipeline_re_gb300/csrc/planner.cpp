@@ -182,10 +182,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
       ln.gq[i] = ltake(Tmb * 3 * d * es);
     }
   }
-  size_t cols = std::max<size_t>(2 * d, f);
-  if (dm.kind == 1) cols = std::max<size_t>(cols, 3 * d);
   const size_t parts = (Tmb + 7) / 8;
-  w.scratch_bytes = std::max(parts * cols * 4, Tmb * std::max<size_t>(H, 1) * 4);
+  w.scratch_bytes = Tmb * std::max<size_t>(H, 1) * 4;  // attention row sums rowsum(dO o O)
   ln.scratch = ltake(w.scratch_bytes);
   w.lnp_bytes = parts * 2 * d * 4;
   ln.lnp[0] = ltake(w.lnp_bytes);

@@ -50,7 +50,7 @@ struct LaneLayout {
   size_t slots = 0;                             // re-materialised internals of one cell (Lc slots)
   size_t g0 = 0, g1 = 0, gt = 0;                // gradients in flight
   size_t gf[2] = {0, 0}, gh[2] = {0, 0}, gq[2] = {0, 0};  // weight-gradient operands, alternating by layer
-  size_t scratch = 0;                           // reduction partials / attention row sums
+  size_t scratch = 0;                           // attention row sums
   size_t lnp[2] = {0, 0};                       // LayerNorm-backward gamma/beta partials, alternating
   size_t bytes = 0;
 };
