@@ -36,10 +36,6 @@ constexpr int P_THREADS = 320;      // 10 warps
 constexpr int P_EPI_THREADS = 256;  // warps 2..9
 constexpr int PBOX = 16384;         // staging box: 128 rows x 128 B
 constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
-// Epilogue stores: each thread writes its row's columns straight to global
-// memory (fp32 gradients with a vector reduction), no shared-memory staging,
-// no barriers between the epilogue warps; false: staging + TMA store.
-constexpr bool P_DIRECT = true;
 
 // SK (short K): two-box epilogue steps double-buffered too.  With few k-blocks
 // per tile the epilogue bounds the tile rate and the overlap pays; with many,
@@ -56,7 +52,7 @@ struct PCfg {
   // two-box steps single-buffered, which leaves room for a fourth operand stage
   // at 256 columns (measured faster than the overlap)
   static constexpr int NBUF = (STEP_BOXES == 1 || SK) ? 2 : 1;
-  static constexpr int STAGING = P_DIRECT ? 0 : NBUF * STEP_BOXES * PBOX;
+  static constexpr int STAGING = NBUF * STEP_BOXES * PBOX;
   // bias gradient by MMA against ones (2 x 16 TMEM columns beside the accumulators) when they fit
   static constexpr bool DB_MMA = EPI == EPI_ACC_F32 && 2 * BN + 32 <= 512;
   static constexpr int ONES_BYTES = DB_MMA ? 2048 : 0;
@@ -80,20 +76,12 @@ struct PArgs {
   float* dbias;        // EPI_ACC_F32: fp32 [M] += sum_k A(m,k), or NULL
   const void* xsrc;    // residual (store) or GELU pre-activation (GELU backward), bf16, or NULL
   int64_t ldx;
-  void* c;             // output (bf16, or fp32 for the fp32 epilogues) and, for bias + GELU, GELU(z)
-  void* c2;
-  int64_t ldc;
   int M, N, K;
   int m_tiles, n_tiles;
 };
 
 __device__ __forceinline__ uint32_t pswz(int r, int unit) {
   return static_cast<uint32_t>(r * 128 + ((unit ^ (r & 7)) << 4));
-}
-// fp32 v4 reduction into global memory (one add per element per launch, so the
-// order of additions to an element is the launch order)
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(P_EPI_THREADS) : "memory"); }
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
@@ -275,13 +263,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         for (int j = 0; j < 4; ++j) xcur[j] = xnext[j];
         if (c + 1 < BN / 64) load_x(c + 1, xnext);
         uint8_t* stg = sStg + (Cfg::NBUF == 2 ? (step & 1) : 0) * Cfg::STEP_BOXES * PBOX;
-        if (!P_DIRECT) {
-          if (etid == 0) {  // the store that last used this buffer has read it
-            if (Cfg::NBUF == 2) bulk_wait_read_1();
-            else bulk_wait_read_all();
-          }
-          epi_bar();
+        if (etid == 0) {  // the store that last used this buffer has read it
+          if (Cfg::NBUF == 2) bulk_wait_read_1();
+          else bulk_wait_read_all();
         }
+        epi_bar();
         const int ncol0 = n0 + c * 64 + h * 32;
         const bool full_cols = ncol0 + 32 <= args.N;
         float xv[32];
@@ -307,27 +293,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
-        if (Cfg::F32_OUT && P_DIRECT) {
-          if (m < args.M && !*abort) {
-            float* crow = static_cast<float*>(args.c) + static_cast<int64_t>(m) * args.ldc + ncol0;
-            if (full_cols) {
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                if (EPI == EPI_ACC_F32) red_add_v4(crow + 4 * u, v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-                else
-                  *reinterpret_cast<float4*>(crow + 4 * u) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                if (ncol0 + j < args.N) {
-                  if (EPI == EPI_ACC_F32) atomicAdd(crow + j, v[j]);
-                  else crow[j] = v[j];
-                }
-              }
-            }
-          }
-        } else if (Cfg::F32_OUT) {
+        if (Cfg::F32_OUT) {
           uint8_t* box = stg + h * PBOX;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -354,48 +320,18 @@ __global__ void __launch_bounds__(P_THREADS, 1)
               else v[j] += xv[j];
             }
           }
-          if (P_DIRECT) {
-            if (m < args.M && !*abort) {
-              __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.c) + static_cast<int64_t>(m) * args.ldc + ncol0;
-              __nv_bfloat16* grow = EPI == EPI_BIAS_GELU
-                                        ? static_cast<__nv_bfloat16*>(args.c2) + static_cast<int64_t>(m) * args.ldc + ncol0
-                                        : nullptr;
-              if (full_cols) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  store8(crow + 8 * u, v + 8 * u);
-                  if (EPI == EPI_BIAS_GELU) {
-                    float gv[8];
+          for (int u = 0; u < 4; ++u) store8(reinterpret_cast<__nv_bfloat16*>(stg + pswz(r, h * 4 + u)), v + 8 * u);
+          if (EPI == EPI_BIAS_GELU) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gv[e] = gelu_f(v[8 * u + e]);
-                    store8(grow + 8 * u, gv);
-                  }
-                }
-              } else {
+            for (int u = 0; u < 4; ++u) {
+              float gv[8];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  if (ncol0 + j < args.N) {
-                    crow[j] = __float2bfloat16_rn(v[j]);
-                    if (EPI == EPI_BIAS_GELU) grow[j] = __float2bfloat16_rn(gelu_f(v[j]));
-                  }
-                }
-              }
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) store8(reinterpret_cast<__nv_bfloat16*>(stg + pswz(r, h * 4 + u)), v + 8 * u);
-            if (EPI == EPI_BIAS_GELU) {
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                float gv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) gv[e] = gelu_f(v[8 * u + e]);
-                store8(reinterpret_cast<__nv_bfloat16*>(stg + PBOX + pswz(r, h * 4 + u)), gv);
-              }
+              for (int e = 0; e < 8; ++e) gv[e] = gelu_f(v[8 * u + e]);
+              store8(reinterpret_cast<__nv_bfloat16*>(stg + PBOX + pswz(r, h * 4 + u)), gv);
             }
           }
         }
-        if (P_DIRECT) continue;
         fence_proxy_async_smem();
         epi_bar();
         if (etid == 0 && !*abort) {
@@ -495,9 +431,6 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   args.dbias = EPI == EPI_ACC_F32 ? g.dbias : nullptr;
   if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && g.dbias)
     return set_error(GPIPE_ERR_UNSUPPORTED, "persistent gemm: no bias gradient with 256-wide tiles");
-  args.c = g.C;
-  args.c2 = g.C2;
-  args.ldc = g.ldc;
   args.xsrc = EPI == EPI_STORE ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : nullptr);
   args.ldx = EPI == EPI_STORE ? g.ldr : g.ldaux;
   args.M = g.M;
