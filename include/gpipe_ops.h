@@ -156,6 +156,19 @@ int gpipe_op_rmsprop(size_t n, float* w, float* g, float* v, void* w_bf16, float
 /* dst[i] = bf16(src[i]) (round to nearest even). */
 int gpipe_op_cast_bf16(size_t n, const float* src, void* dst, void* stream);
 
+/* Failure detection.  Every wait of the library's kernels on another part of
+ * the GPU is bounded (2 s); one that gives up, or a kernel that meets an
+ * invalid input it skips (a token id outside [0, vocab)), sets the device error
+ * word of the current device: 1-4 a bounded wait (TMA producer, MMA issuer,
+ * epilogue, exit drain), 5 an invalid token id, 6 this probe.
+ *   gpipe_op_wait_probe: launches one CTA whose bounded wait on an mbarrier
+ *     that nothing completes gives up after the limit and sets code 6; the
+ *     kernel returns normally and the context stays usable.
+ *   gpipe_op_device_error: copies the word to *flag_out (synchronises
+ *     `stream`); clear != 0 resets it to 0 afterwards. */
+int gpipe_op_wait_probe(void* stream);
+int gpipe_op_device_error(int* flag_out, int clear, void* stream);
+
 /* The GELU arithmetic of the GEMM epilogues, in fp32 (for checking it):
  * gelu[i] = z Phi(z) and dgelu[i] = Phi(z) + z phi(z) for z = z_in[i] (exact-erf
  * GELU as the review's Transformer uses it; erf evaluated to within 1.5e-7, see

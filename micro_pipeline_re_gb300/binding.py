@@ -90,6 +90,8 @@ _SIGS = {
     "gpipe_op_cast_bf16": (c_int, [c_size_t, c_void_p, c_void_p, c_void_p]),
     "gpipe_op_gelu": (c_int, [c_size_t, c_void_p, c_void_p, c_void_p, c_void_p]),
     "gpipe_op_gemm_set_sm_share": (c_int, [c_int]),
+    "gpipe_op_wait_probe": (c_int, [c_void_p]),
+    "gpipe_op_device_error": (c_int, [POINTER(c_int), c_int, c_void_p]),
 }
 
 

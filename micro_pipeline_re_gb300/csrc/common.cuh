@@ -19,7 +19,8 @@ enum DeviceError : int {
   DERR_MMA_WAIT = 2,   // MMA issuer waited too long for a filled stage
   DERR_ACC_WAIT = 3,   // epilogue waited too long for the accumulator
   DERR_DRAIN_WAIT = 4, // exit-time wait for in-flight copies gave up
-  DERR_BAD_TOKEN = 5   // a token id outside [0, vocab) (the read is skipped)
+  DERR_BAD_TOKEN = 5,  // a token id outside [0, vocab) (the read is skipped)
+  DERR_PROBE = 6       // the failure-detection probe's wait gave up (as it must)
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait

@@ -581,7 +581,26 @@ __global__ void gelu_kernel(size_t n, const float* __restrict__ z, float* __rest
   }
 }
 
+// Failure-detection probe: one thread waits, with the library's bounded wait,
+// on an mbarrier that nothing will complete; the wait gives up after its limit
+// and sets the device error word, and the kernel returns.
+__global__ void wait_probe_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait_bounded(&bar, 0, err, DERR_PROBE);
+  __syncthreads();
+}
+
 }  // namespace
+
+int launch_wait_probe(cudaStream_t s) {
+  (void)launch_k(wait_probe_kernel, 1, 32, 0, s, device_error_ptr());
+  return check_launch("wait probe");
+}
 
 int launch_gelu(size_t n, const float* z, float* y, float* dy, cudaStream_t s) {
   if (n == 0) return GPIPE_OK;

@@ -67,6 +67,9 @@ int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const 
                               const float* rstd, const float* g, const void* dres, void* dx, float* scratch,
                               cudaStream_t s);
 int launch_gelu(size_t n, const float* z, float* y, float* dy, cudaStream_t s);
+// One CTA whose bounded wait on an mbarrier nothing completes gives up and
+// sets the device error word (code 6): checks the failure path without a fault.
+int launch_wait_probe(cudaStream_t s);
 // db[m] += sum_k A(m, k) for a bf16 A, K-major ([M][K]) or MN-major ([K][M]);
 // one launch, fixed order (the bias gradient of the wide weight-gradient GEMMs).
 int launch_dbias(bool a_kmajor, int M, int K, const void* a, int64_t lda, float* db, cudaStream_t s);

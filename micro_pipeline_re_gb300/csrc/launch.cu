@@ -190,6 +190,20 @@ int gpipe_op_cast_bf16(size_t n, const float* src, void* dst, void* stream) {
   return gp::launch_cast_bf16(n, src, dst, static_cast<cudaStream_t>(stream));
 }
 
+int gpipe_op_wait_probe(void* stream) { return gp::launch_wait_probe(static_cast<cudaStream_t>(stream)); }
+
+int gpipe_op_device_error(int* flag_out, int clear, void* stream) {
+  if (!flag_out) return gp::set_error(GPIPE_ERR_INVALID_ARG, "device_error: NULL output");
+  int* dev = gp::device_error_ptr();
+  if (!dev) return gp::set_error(GPIPE_ERR_CUDA, "device_error: cannot resolve the device error word");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(flag_out, dev, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(dev, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return gp::set_error(GPIPE_ERR_CUDA, "device_error: %s", cudaGetErrorString(e));
+  return GPIPE_OK;
+}
+
 int gpipe_op_gelu(size_t n, const float* z_in, float* gelu, float* dgelu, void* stream) {
   return gp::launch_gelu(n, z_in, gelu, dgelu, static_cast<cudaStream_t>(stream));
 }

@@ -435,3 +435,52 @@ def test_gemm_bits_do_not_depend_on_sm_share(b, ak, bk, epi, shape):
     for o in outs[1:]:
         for x, y in zip(o, outs[0]):
             assert (x is None and y is None) or t.equal(x, y)
+
+
+def _device_error(b, clear=1):
+    import ctypes
+    f = ctypes.c_int(-1)
+    assert b.lib().gpipe_op_device_error(ctypes.byref(f), clear, stream()) == 0
+    return f.value
+
+
+def test_bounded_wait_gives_up_and_reports_without_a_fault(b):
+    """Failure detection without a GPU fault: a kernel's bounded wait on an
+    mbarrier that nothing completes gives up after the limit (2 s), sets the
+    device error word (code 6) and returns; the context keeps working."""
+    import time
+    t = __import__("torch")
+    _device_error(b)  # start clean
+    t0 = time.perf_counter()
+    assert b.lib().gpipe_op_wait_probe(stream()) == 0
+    assert _device_error(b) == 6
+    assert 1.5 < time.perf_counter() - t0 < 60
+    # the same context still computes: a GEMM afterwards is right and flags nothing
+    rng = np.random.default_rng(3)
+    A = bf16_round(rng.standard_normal((256, 128)))
+    B = bf16_round(rng.standard_normal((192, 128)))
+    C = t.zeros((256, 192), dtype=t.bfloat16, device="cuda")
+    assert b.lib().gpipe_op_gemm(1, 256, 192, 128, dev(A, "bf16").data_ptr(), 128, 1, dev(B, "bf16").data_ptr(), 128,
+                                 1, 0, C.data_ptr(), 192, None, None, 0, None, None, 0, stream()) == 0
+    sync()
+    assert rel(host(C), A @ B.T) <= 1e-2
+    assert _device_error(b) == 0
+
+
+def test_invalid_token_is_flagged_not_read(b):
+    """A next-token target outside [0, vocab) is skipped (no out-of-range read)
+    and reported through the device error word (code 5)."""
+    t = __import__("torch")
+    rows, vocab, seq = 64, 1000, 64
+    rng = np.random.default_rng(5)
+    tokens = rng.integers(0, vocab, size=rows).astype(np.int32)
+    tokens[10] = vocab + 3
+    z = dev((rng.standard_normal((rows, vocab)) * 3).astype(np.float32))
+    loss = t.empty(rows, dtype=t.float32, device="cuda")
+    _device_error(b)
+    assert b.lib().gpipe_op_cross_entropy(rows, vocab, seq, dev(tokens).data_ptr(), 0, 1.0, z.data_ptr(),
+                                          loss.data_ptr(), 1, stream()) == 0
+    sync()
+    assert _device_error(b) == 5
+    got = host(loss)
+    assert np.all(np.isfinite(got)) and got[9] == 0.0  # row 9's target was token 10
