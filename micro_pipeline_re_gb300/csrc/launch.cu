@@ -1,7 +1,9 @@
 // Library-wide launch plumbing (error messages, the device error word, the
 // launch counter, SM count) and the gpipe_op_* kernel-level C entry points.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/gpipe.h"
@@ -39,32 +41,44 @@ bool pdl_enabled() { return g_pdl; }
 void set_pdl_enabled(bool on) { g_pdl = on; }
 int64_t launch_count() { return g_launches; }
 
-int* device_error_ptr() {
-  // One address per device; this library drives the current device only.
-  static int dev_cached = -1;
-  static int* ptr = nullptr;
+// Per-device caches (a process may drive several devices from several host
+// threads): resolved once per device under a lock, then read without one.
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_dev_mu;
+std::atomic<int*> g_err_ptr[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];
+int current_device() {
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev != dev_cached) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    ptr = static_cast<int*>(p);
-    dev_cached = dev;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+}  // namespace
+
+int* device_error_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  int* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  p = g_err_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_device_error) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(q);
+    g_err_ptr[dev].store(p, std::memory_order_release);
   }
-  return ptr;
+  return p;
 }
 
 int num_sms() {
-  static int dev_cached = -1;
-  static int sms = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev != dev_cached) {
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-    dev_cached = dev;
-  }
-  return sms;
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  int n = g_sms[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  g_sms[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 int prepare_kernels() {
