@@ -472,15 +472,11 @@ bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace
 
 int prepare_attention() {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e1 = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)kBwdSmem);
-    if (e1 != cudaSuccess)
-      return set_error(GPIPE_ERR_CUDA, "attention_bwd: shared-memory attribute failed");
-    attr_set = true;
-  }
-  return GPIPE_OK;
+  static std::atomic<unsigned long long> done{0};
+  return once_per_device(done, [] {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem);
+    return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "attention_bwd: shared-memory attribute failed");
+  });
 }
 
 int launch_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o, float* lse, cudaStream_t s) {

@@ -403,14 +403,14 @@ bool pmake_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64
 
 template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>
 int pset_attr() {
-  static bool done = false;
-  if (!done) {
+  static std::atomic<unsigned long long> done{0};
+  return once_per_device(done, [] {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI, SK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI, SK>::SMEM);
-    if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "persistent gemm: smem attribute: %s", cudaGetErrorString(e));
-    done = true;
-  }
-  return GPIPE_OK;
+    return e == cudaSuccess
+               ? GPIPE_OK
+               : set_error(GPIPE_ERR_CUDA, "persistent gemm: smem attribute: %s", cudaGetErrorString(e));
+  });
 }
 
 template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>

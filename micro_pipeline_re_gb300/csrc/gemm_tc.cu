@@ -396,14 +396,13 @@ bool make_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64_
 
 template <bool A_K, bool B_K, int BN, int EPI, bool SPLIT = false>
 int set_attr() {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<unsigned long long> done{0};
+  return once_per_device(done, [] {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_K, B_K, BN, EPI, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN, EPI>::SMEM);
-    if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
-    attr_set = true;
-  }
-  return GPIPE_OK;
+    return e == cudaSuccess ? GPIPE_OK
+                            : set_error(GPIPE_ERR_CUDA, "gemm: smem attribute: %s", cudaGetErrorString(e));
+  });
 }
 
 template <bool A_K, bool B_K, int BN, int EPI, bool SPLIT = false>

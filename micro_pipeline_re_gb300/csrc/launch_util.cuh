@@ -10,6 +10,7 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 namespace gp {
@@ -50,6 +51,19 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Run f (a per-device setup such as a kernel attribute, which CUDA keeps per
+// device) once for each device it succeeds on; devices >= 64 run it every time.
+template <typename F>
+int once_per_device(std::atomic<unsigned long long>& done, F&& f) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return f();
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return 0;
+  const int rc = f();
+  if (rc == 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return rc;
 }
 
 }  // namespace gp
