@@ -244,3 +244,6 @@ def test_options_are_validated_and_kernel_times_start_empty(binding):
     ms, fl = g.kernel_times()   # no step taken yet: nothing timed, no CUDA call made
     assert ms.size == 0 and fl.size == 0
     g.close()
+    # the op API's SM share for gpipe_op_gemm: >= 0 (0 = the whole GPU)
+    assert binding.lib().gpipe_op_gemm_set_sm_share(-1) == -1
+    assert binding.lib().gpipe_op_gemm_set_sm_share(0) == 0
