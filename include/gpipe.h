@@ -207,10 +207,11 @@ enum {
                                 else 1.  S > 1 gives each cell S lanes that take
                                 its micro-batches in turn (S-1 more cell workspaces
                                 per cell, and a gradient ring S deep between
-                                neighbouring cells) and share one side stream (used whatever
-                                GPIPE_OPT_CONCURRENT says), so every weight gradient
-                                still accumulates in micro-batch order and results
-                                are identical.  Set before gpipe_sizes.              */
+                                neighbouring cells) and share the cell's side streams
+                                (used whatever GPIPE_OPT_CONCURRENT says), so every
+                                weight gradient still accumulates in micro-batch
+                                order and results are identical.  Set before
+                                gpipe_sizes.                                         */
   GPIPE_OPT_SIDE_SHARE = 13, /* [100] with lanes, GEMMs on the side streams (weight
                                 gradients, off the critical path) get this percentage
                                 of the SM share, 5..800: a smaller grid does the same

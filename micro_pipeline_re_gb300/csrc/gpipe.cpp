@@ -229,14 +229,16 @@ constexpr int BUF_EXT = 2;  // "dy lives outside the lane" (boundary ring / head
 
 // Issues one step.  Host issue order is the serial GPipe order (phase 1:
 // micro-batch-major forward; phase 2: micro-batch-major backward, cells K-1..0;
-// phase 3: update).  When the cells are pipelined, cell k's work goes to lane
-// k's streams, and events carry exactly the dependencies of the review's
-// pipeline: cell k forwards micro-batch m after cell k-1 handed it m; cell k
-// differentiates m after cell k+1 handed it the gradient of m; a lane
-// processes micro-batches in order.  So cell k can work on micro-batch m while
-// cell k+1 works on m-1, as the review's K accelerators do.  Per-cell
-// weight-gradient accumulation stays in micro-batch order on one stream, so
-// the result does not depend on the interleaving.
+// phase 3: update).  When the cells are pipelined, cell k's work for
+// micro-batch m goes to the streams of lane k*S + m mod S (S micro-batches in
+// flight per cell), the head's to head lane m mod 2, and events carry exactly
+// the dependencies of the review's pipeline: cell k forwards micro-batch m
+// after cell k-1 handed it m; cell k differentiates m after cell k+1 handed it
+// the gradient of m; a lane processes its micro-batches in order.  So cell k
+// can work on micro-batch m while cell k+1 works on m-1, as the review's K
+// accelerators do.  Each parameter's gradient accumulation stays in
+// micro-batch order on one stream, so the result does not depend on the
+// interleaving.
 class Executor {
  public:
   Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t origin) : c_(c), p_(p), origin_(origin) {}
@@ -372,8 +374,9 @@ class Executor {
   // Head lanes follow the cells' lanes and take the micro-batches in turn.
   int head_lane(int m) const { return c_->ws.nlanes > 1 ? c_->ws.nlanes + m % c_->ws.nheads : 0; }
   bool is_head_lane(int lane) const { return c_->ws.nlanes > 1 && lane >= c_->ws.nlanes; }
-  // A cell's lanes share one side stream (its first lane's), which receives the
-  // cell's weight-gradient work in micro-batch order.
+  // A cell's lanes share the side streams of its first lane (the head lanes
+  // those of the first head lane), which receive the weight-gradient work in
+  // micro-batch order.
   int side_of(int lane) const { return lane < c_->ws.nlanes ? lane - lane % c_->ws.inflight : c_->ws.nlanes; }
   char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
