@@ -164,7 +164,13 @@ def cfg(w, args):
     return {"workload": w.name, "L": w.L, "K": w.K, "M": w.M, "d": w.d, "heads": w.heads, "ffn": w.ffn,
             "seq_len": w.seq, "vocab": w.vocab, "global_batch": w.n * max(args.gpus, 1),
             "parallelism": "replicas" if args.gpus > 1 else "single-gpu (all K cells on one GPU)",
-            "l2": "working set larger than L2 (parameters, gradients and RMSProp state alone exceed 129 MB)"}
+            "l2": "working set larger than L2 (parameters, gradients and RMSProp state alone exceed 129 MB)",
+            "schedule": getattr(args, "schedule", "gpipe")}
+
+
+# issue orders of the step (GPIPE_OPT_SCHEDULE): the review's GPipe order, or
+# one-forward-one-backward (same results, shorter stash)
+SCHEDULES = {"gpipe": 0, "1f1b": 1}
 
 
 def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
@@ -329,6 +335,7 @@ def run_ours(args, w):
     peaks = load_peaks()
     inp = make_inputs(w)
     gp = b.GPipe.from_workload(w)
+    gp.set_option(b.OPT_SCHEDULE, SCHEDULES[args.schedule])
     st = b.DeviceState(gp, w, inp)
     stream = st.stream
     for _ in range(args.warmup):
@@ -423,6 +430,7 @@ def run_sweep(args):
     for K, M in SWEEP_GRID:
         w = w0.replace(K=K, M=M)
         gp = b.GPipe.from_workload(w)
+        gp.set_option(b.OPT_SCHEDULE, SCHEDULES[args.schedule])
         free0 = torch.cuda.mem_get_info()[0]
         st = b.DeviceState(gp, w, inp)
         free1 = torch.cuda.mem_get_info()[0]
@@ -467,6 +475,8 @@ def main():
                     help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 2 GELU backward, 3 weight gradient, "
                          "4 fp32 store")
     ap.add_argument("--reps", type=int, default=100)
+    ap.add_argument("--schedule", default="gpipe", choices=sorted(SCHEDULES),
+                    help="issue order: gpipe (all forwards, then all backwards) or 1f1b (interleaved, shorter stash)")
     ap.add_argument("--sweep", action="store_true",
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
     args = ap.parse_args()

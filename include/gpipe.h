@@ -23,6 +23,11 @@
  * micro-batches), plus lanes for the head; or, with GPIPE_OPT_PIPELINE = 0,
  * the cells take turns on one lane.  Every parameter's gradient accumulates
  * on one stream in micro-batch order, so all schedules give identical bits.
+ * The issue order is the review's GPipe order by default; GPIPE_OPT_SCHEDULE 1
+ * interleaves each cell's forwards and backwards (one-forward-one-backward, the
+ * order the review's "Historical impact" section credits to PipeDream-2BW for
+ * its lower activation peak), which keeps min(M, K+1) micro-batches per cell
+ * boundary in the stash instead of M.
  *
  * Conventions for every function:
  *   - Return value: 0 (GPIPE_OK) or a negative GPIPE_ERR_* code; the message of
@@ -139,21 +144,32 @@ int gpipe_step(gpipe_ctx* ctx, float* params_fp32, void* params_bf16, float* gra
 /* (K-1)/(M+K-1), the review's bubble fraction for the context's K and M. */
 double gpipe_bubble_fraction(const gpipe_ctx* ctx);
 
-/* Discrete-event model of the GPipe clock on K devices for this context's K,
- * M: t_f[k], t_b[k] are per-cell forward/backward times of one micro-batch
- * (host arrays of K doubles, or NULL for the partition's cell costs with
- * t_b = 2 t_f).  Outputs (any may be NULL): makespan, bubble fraction. */
+/* Discrete-event model of the pipeline clock on K devices for this context's
+ * K, M and issue order (GPIPE_OPT_SCHEDULE): t_f[k], t_b[k] are per-cell
+ * forward/backward times of one micro-batch (host arrays of K doubles, or NULL
+ * for the partition's cell costs with t_b = 2 t_f); the head takes no time.
+ * Outputs (any may be NULL): makespan, bubble fraction. */
 int gpipe_schedule_model(const gpipe_ctx* ctx, const double* t_f, const double* t_b,
                          double* makespan, double* bubble);
+
+/* The order in which gpipe_step issues its operations (host only, no CUDA
+ * call): (2K+1) M operations, written as int32 quadruples (kind, k, m, tick)
+ * into ops_out (room for `count` of them; ops_out may be NULL when count is
+ * 0).  kind 0 = forward of cell k for micro-batch m (the embedding first when
+ * k = 0), 1 = the head of micro-batch m (k = 0), 2 = backward of cell k with
+ * its re-computation.  tick = the round of the list scheduler that issued it.
+ * Returns the number of operations, or a negative GPIPE_ERR_* code. */
+int gpipe_issue_order(const gpipe_ctx* ctx, int32_t* ops_out, int count);
 
 /* Activation memory of the step as laid out in the workspace (bytes):
  *   peak_act_bytes    the workspace's activation high-water mark (boundary
  *                     stash + the re-computed cell's internals + head + the
  *                     gradients in flight); all of it is live at the peak;
  *   model_bound_bytes the review's bound O(N + (L/K)(N/M)) with explicit
- *                     constants: (K+3) T d e + K R (T/M) d e  +  lanes
+ *                     constants: (K+2) D (T/M) d e + T d e + K R (T/M) d e  +  lanes
  *                     (Lc (T/M) a + (T/M) g)  +  heads (T/M) h, T = tokens per
- *                     step, e = activation element bytes, R = gradient-ring
+ *                     step, e = activation element bytes, D = stash-ring depth
+ *                     (M, or min(M, K+1) with GPIPE_OPT_SCHEDULE 1), R = gradient-ring
  *                     depth, lanes = K x micro-batches in flight (1 without
  *                     lanes), Lc = largest cell's layer count, a = bytes one
  *                     layer keeps per token, g = per-token gradient bytes of a
@@ -217,12 +233,23 @@ enum {
                                 of the SM share, 5..800: a smaller grid does the same
                                 tiles with fewer CTAs, so less SM time; results stay
                                 identical                                            */
-  GPIPE_OPT_SIDE_STREAMS = 14 /* [2] side streams per lane, 1..4: the weight-gradient
+  GPIPE_OPT_SIDE_STREAMS = 14, /* [2] side streams per lane, 1..4: the weight-gradient
                                 work of W2, W1, W_o, W_qkv and the LayerNorm
                                 reductions go to stream (group mod this); a group
                                 always uses the same stream, so every gradient still
                                 accumulates in micro-batch order and results are
                                 identical                                            */
+  GPIPE_OPT_SCHEDULE = 15    /* [0] issue order of the step.  0: the review's GPipe
+                                order (every micro-batch forward through all cells,
+                                then every backward), each cell boundary stashed for
+                                all M micro-batches.  1: one-forward-one-backward:
+                                cell k runs min(M, K+1-k) forwards, then alternates
+                                one backward and one forward, so a boundary holds at
+                                most min(M, K+1) micro-batches (a ring of that depth,
+                                also for the head's output gradient).  Each cell
+                                still differentiates its micro-batches in ascending
+                                order, so results are identical.  Set before
+                                gpipe_sizes (it changes the workspace size).          */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

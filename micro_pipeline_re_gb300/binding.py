@@ -28,6 +28,9 @@ OPT_SM_SHARE = 11
 OPT_INFLIGHT = 12
 OPT_SIDE_SHARE = 13
 OPT_SIDE_STREAMS = 14
+OPT_SCHEDULE = 15
+SCHEDULE_GPIPE, SCHEDULE_1F1B = 0, 1
+OP_FWD, OP_HEAD, OP_BWD = 0, 1, 2
 EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
 
 
@@ -57,6 +60,7 @@ _SIGS = {
     "gpipe_schedule_model": (c_int, [c_void_p, POINTER(c_double), POINTER(c_double), POINTER(c_double),
                                      POINTER(c_double)]),
     "gpipe_memory_report": (c_int, [c_void_p, POINTER(c_size_t), POINTER(c_size_t)]),
+    "gpipe_issue_order": (c_int, [c_void_p, POINTER(c_int32), c_int]),
     "gpipe_set_option": (c_int, [c_void_p, c_int, c_int64]),
     "gpipe_debug_counters": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_uint64), POINTER(c_int)]),
     "gpipe_loss_rows": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float), c_size_t]),
@@ -198,6 +202,14 @@ class GPipe:
         tb = (c_double * self.K)(*t_b) if t_b is not None else None
         _check(lib().gpipe_schedule_model(self.h, tf, tb, ctypes.byref(mk), ctypes.byref(bb)), self.h)
         return mk.value, bb.value
+
+    def issue_order(self):
+        """The step's issue order as a list of (kind, k, m, tick)."""
+        n = lib().gpipe_issue_order(self.h, None, 0)
+        _check(min(n, 0), self.h)
+        buf = (c_int32 * (4 * n))()
+        _check(min(lib().gpipe_issue_order(self.h, buf, n), 0), self.h)
+        return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
 
     def memory_report(self):
         a, b = c_size_t(), c_size_t()

@@ -24,8 +24,12 @@
 // dependencies; weight-gradient GEMMs run on each lane's side stream.  Each
 // cell's gradient accumulation stays in micro-batch order on one stream, so the
 // result is bit-identical to running the cells in turn on one stream
-// (GPIPE_OPT_PIPELINE / GPIPE_OPT_CONCURRENT = 0).  The whole step is captured
-// once into a CUDA graph and replayed.
+// (GPIPE_OPT_PIPELINE / GPIPE_OPT_CONCURRENT = 0).  GPIPE_OPT_SCHEDULE 1
+// issues the same operations in the one-forward-one-backward order (each cell
+// alternates forwards and backwards after a short warm-up), so a cell boundary
+// is stashed for at most min(M, K+1) micro-batches: the stash becomes a ring
+// whose slots are rewritten only after their reader released them (events).
+// The whole step is captured once into a CUDA graph and replayed.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -55,7 +59,7 @@ struct StepPtrs {
 
 struct GraphKey {
   StepPtrs p;
-  int64_t opts[12];
+  int64_t opts[13];
   bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
 };
 
@@ -81,6 +85,7 @@ struct gpipe_ctx {
   bool pdl = false;        // kernels may launch while their predecessor drains (measured slower with lanes)
   bool trace = false;      // stamp the GPU clock at the end of every (cell, micro-batch, phase)
   int inflight = 0;        // with lanes: micro-batches each cell works on at once (1, 2; 0: by size)
+  int schedule = 0;        // issue order: 0 GPipe (all forwards, then all backwards), 1 one-forward-one-backward
   // Two in flight when a micro-batch's FFN GEMM is small enough (tokens x d x
   // ffn <= 2^30) that its kernels are bound by latency rather than throughput.
   int inflight_eff() const {
@@ -102,10 +107,12 @@ struct gpipe_ctx {
   cudaStream_t lane_main[kMaxLanes] = {}, lane_side[kMaxLanes][kSides] = {};
   cudaEvent_t lane_ev[kMaxLanes][kLaneEvents] = {};
   static constexpr int kRing = 4;  // deepest gradient ring between neighbouring cells (= most in flight)
-  cudaEvent_t ev_origin = nullptr, ev_fwd[kMaxLanes] = {}, ev_bdone[kMaxLanes][kRing] = {},
-              ev_bfree[kMaxLanes][kRing] = {},
+  cudaEvent_t ev_origin = nullptr, ev_bdone[kMaxLanes][kRing] = {}, ev_bfree[kMaxLanes][kRing] = {},
               ev_lane_end[kMaxLanes] = {};
   std::vector<cudaEvent_t> ev_hdone;  // per micro-batch: the head has written the last cell's output gradient
+  std::vector<cudaEvent_t> ev_fwd;    // per (cell, stash slot): the cell has written its output
+  std::vector<cudaEvent_t> ev_sfree;  // per (stash level, slot): its reader is done (stash ring shorter than M)
+  std::vector<cudaEvent_t> ev_hfree;  // per slot: the last cell has read the head's output gradient (likewise)
   // streams in use: one pair per lane, plus the head's pair when the cells are pipelined
   int nstreams() const { return ws.nlanes > 1 ? ws.nlanes + ws.nheads : 1; }
   cudaGraphExec_t gexec = nullptr;
@@ -130,7 +137,7 @@ struct gpipe_ctx {
       const int nin = inflight_eff();
       const bool lanes = pipelined && K * nin + 2 <= kMaxLanes;  // + the head lanes
       ws = make_workspace(dm, L, K, M, max_cell, !no_remat, remat_check_m >= 0 && !no_remat, lanes,
-                          lanes ? nin : 1);
+                          lanes ? nin : 1, stash_depth(K, M, schedule));
       ws_stale = false;
     }
   }
@@ -149,20 +156,24 @@ struct gpipe_ctx {
       return st || cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, prio) == cudaSuccess;
     };
     bool ok = mk_ev(ev_origin);
-    if (static_cast<int>(ev_hdone.size()) < M) ev_hdone.resize(M, nullptr);
-    for (int m = 0; m < M && ok; ++m) ok = mk_ev(ev_hdone[m]);
+    auto mk_evs = [&](std::vector<cudaEvent_t>& v, size_t n) {
+      if (v.size() < n) v.resize(n, nullptr);
+      bool r = true;
+      for (size_t i = 0; i < n && r; ++i) r = mk_ev(v[i]);
+      return r;
+    };
+    const size_t D = static_cast<size_t>(ws.depth);
+    ok = ok && mk_evs(ev_hdone, M) && mk_evs(ev_fwd, K * D);
+    if (ws.depth < M) ok = ok && mk_evs(ev_sfree, (K + 1) * D) && mk_evs(ev_hfree, D);
     for (int i = 0; i < nstreams() && ok; ++i) {
       const bool head = nstreams() > 1 && i >= ws.nlanes;
       ok = mk_st(lane_main[i], head ? (least + greatest) / 2 : greatest);
       for (int j = 0; j < nside && ok; ++j) ok = mk_st(lane_side[i][j], least);
-      ok = ok &&
-           mk_ev(ev_lane_end[i]) && mk_ev(ev_fwd[i]);
+      ok = ok && mk_ev(ev_lane_end[i]);
       for (int e = 0; e < kLaneEvents && ok; ++e) ok = mk_ev(lane_ev[i][e]);
     }
-    for (int k = 0; k < K && k < kMaxLanes && ok; ++k) {
+    for (int k = 0; k < K && k < kMaxLanes && ok; ++k)
       for (int r = 0; r < kRing && ok; ++r) ok = mk_ev(ev_bdone[k][r]) && mk_ev(ev_bfree[k][r]);
-      ok = ok && mk_ev(ev_fwd[k]);
-    }
     return ok ? GPIPE_OK : fail(GPIPE_ERR_CUDA, "cannot create the lane streams/events");
   }
   // The event pair of the next timed launch (created on first use).
@@ -227,35 +238,41 @@ enum {
 };
 constexpr int BUF_EXT = 2;  // "dy lives outside the lane" (boundary ring / head output)
 
-// Issues one step.  Host issue order is the serial GPipe order (phase 1:
-// micro-batch-major forward; phase 2: micro-batch-major backward, cells K-1..0;
-// phase 3: update).  When the cells are pipelined, cell k's work for
-// micro-batch m goes to the streams of lane k*S + m mod S (S micro-batches in
-// flight per cell), the head's to head lane m mod 2, and events carry exactly
-// the dependencies of the review's pipeline: cell k forwards micro-batch m
-// after cell k-1 handed it m; cell k differentiates m after cell k+1 handed it
-// the gradient of m; a lane processes its micro-batches in order.  So cell k
-// can work on micro-batch m while cell k+1 works on m-1, as the review's K
-// accelerators do.  Each parameter's gradient accumulation stays in
-// micro-batch order on one stream, so the result does not depend on the
-// interleaving.
+// Issues one step.  Host issue order is the step's issue order (the planner's
+// issue_order): the GPipe order of the review's "Pipeline flow" (phase 1:
+// micro-batch-major forward, each micro-batch's head right after its last
+// cell; phase 2: micro-batch-major backward, cells K-1..0) or the
+// one-forward-one-backward order; then phase 3, the update.  When the cells
+// are pipelined, cell k's work for micro-batch m goes to the streams of lane
+// k*S + m mod S (S micro-batches in flight per cell), the head's to head lane
+// m mod 2, and events carry exactly the dependencies of the review's pipeline:
+// cell k forwards micro-batch m after cell k-1 handed it m; cell k
+// differentiates m after cell k+1 handed it the gradient of m; a lane
+// processes its micro-batches in order; a ring slot is rewritten only after
+// its reader released it.  So cell k can work on micro-batch m while cell k+1
+// works on m-1, as the review's K accelerators do.  Each parameter's gradient
+// accumulation stays in micro-batch order on one stream, in either order, so
+// the result does not depend on the interleaving.
 class Executor {
  public:
   Executor(gpipe_ctx* c, const StepPtrs& p, cudaStream_t origin) : c_(c), p_(p), origin_(origin) {}
-
-  // Cells busy at clock tick t of the review's schedule (cell k works on
-  // micro-batch t - k in the forward, on micro-batch t - (K-1-k) in the backward).
-  int busy_at(int t) const {
-    const int lo = t - (c_->M - 1) > 0 ? t - (c_->M - 1) : 0;
-    const int hi = t < c_->K - 1 ? t : c_->K - 1;
-    return hi >= lo ? hi - lo + 1 : 1;
-  }
 
   int run_step() {
     const Workspace& w = c_->ws;
     const int M = c_->M, K = c_->K;
     set_pdl_enabled(c_->pdl);
     c_->kt_n = 0;
+    std::vector<Op> ops;
+    if (!issue_order(K, M, c_->schedule, w.ring, ops)) return set_error(GPIPE_ERR_INVALID_ARG, "no issue order");
+    // cells busy at each tick of the order (ops of one tick can run at once)
+    int ticks = 0;
+    for (const Op& o : ops) ticks = std::max(ticks, o.tick + 1);
+    std::vector<int> busy(ticks, 0);
+    for (const Op& o : ops)
+      if (o.kind != OP_HEAD) ++busy[o.tick];
+    fwd_rec_.assign(static_cast<size_t>(K) * w.depth, 0);
+    sfree_rec_.assign(static_cast<size_t>(K + 1) * w.depth, 0);
+    hfree_rec_.assign(w.depth, 0);
     // zero the loss scalar and the debug counter, then start every lane
     if (cudaMemsetAsync(p_.ws + w.misc, 0, 16, origin_) != cudaSuccess)
       return set_error(GPIPE_ERR_CUDA, "memset of the step counters failed");
@@ -263,76 +280,14 @@ class Executor {
     TRY(cuda_ok(cudaEventRecord(c_->ev_origin, origin_), "event record"));
     for (int i = 0; i < c_->nstreams(); ++i)
       TRY(cuda_ok(cudaStreamWaitEvent(c_->lane_main[i], c_->ev_origin, 0), "stream wait"));
-
-    // phase 1: forward of every micro-batch through every cell; then the head
-    // (final LN, logits, loss and its gradient) of that micro-batch, once, on
-    // its own lane, which hands the last cell the gradient of its output
-    for (int m = 0; m < M; ++m) {
-      const int hl = head_lane(m);
-      busy_ = busy_at(m);
-      TRY(cell0_input(m));
-      for (int k = 0; k < K; ++k) {
-        busy_ = busy_at(k + m);
-        if (k > 0) TRY(cross_wait(k, m, c_->ev_fwd[k - 1], fwd_rec_[k - 1], k - 1));
-        TRY(cell_forward(k, m, /*recompute=*/false));
-        if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2), st()));
-        TRY(cross_record(k, m, c_->ev_fwd[k], fwd_rec_[k]));
-      }
-      if (hl != lane_of(K - 1, m))
-        TRY(cuda_ok(cudaStreamWaitEvent(main_s(hl), c_->ev_fwd[K - 1], 0), "stream wait"));
-      busy_ = busy_at(K - 1 + m);
-      TRY(head(m));
-      if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(K) * M + m) * 2), st()));
-      if (hl != lane_of(K - 1, m)) TRY(cuda_ok(cudaEventRecord(c_->ev_hdone[m], main_s(hl)), "event record"));
-    }
-    // phase 2: backward with re-computation
-    for (int m = 0; m < M; ++m) {
-      const int p = m % c_->ws.ring;
-      for (int k = K - 1; k >= 0; --k) {
-        const int lk = lane_of(k, m);
-        cur_lane_ = lk;
-        busy_ = busy_at(K - 1 - k + m);
-        TRY(join_all(lk));  // side work still reading this lane's slots
-        if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
-        // gradient of the cell's output
-        char* dy;
-        const int dy_buf = BUF_EXT;
-        if (k == K - 1) {
-          if (head_lane(m) != lk) TRY(cuda_ok(cudaStreamWaitEvent(main_s(lk), c_->ev_hdone[m], 0), "stream wait"));
-          dy = hdy(m);
-        } else {
-          TRY(cross_wait(k, m, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
-          dy = bgrad(k + 1, p);
-        }
-        int cur_buf = dy_buf;
-        const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
-        for (int j = n - 1; j >= 0; --j) {
-          const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
-          char* dx;
-          int dx_buf;
-          if (j == 0 && k > 0) {
-            // hand the input gradient to cell k-1 through the ring
-            if (bfree_rec_[k][p]) TRY(cross_wait(k, m, c_->ev_bfree[k][p], bfree_rec_[k][p], k - 1));
-            dx = bgrad(k, p);
-            dx_buf = BUF_EXT;
-          } else if (j == 0 && c_->dm.kind == 1) {
-            dx = dx0(m);  // the embedding's input gradient, scattered once at the end
-            dx_buf = BUF_EXT;
-          } else {
-            dx_buf = cur_buf == 0 ? 1 : 0;
-            dx = lbuf(lk, dx_buf);
-          }
-          TRY(layer_backward(first + j, x, slot(k, m, j), dy, cur_buf, dx, dx_buf));
-          dy = dx;
-          cur_buf = dx_buf;
-        }
-        if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2 + 1), st()));
-        if (k > 0) TRY(cross_record(k, m, c_->ev_bdone[k][p], bdone_rec_[k][p]));
-        if (k < K - 1) {  // this cell has finished reading the ring slot of cell k+1
-          TRY(join(lk, EV_DYB));
-          TRY(cross_record(k, m, c_->ev_bfree[k + 1][p], bfree_rec_[k + 1][p]));
-        }
-      }
+    for (const Op& o : ops) {
+      busy_ = std::max(1, busy[o.tick]);
+      if (o.kind == OP_FWD)
+        TRY(forward_op(o.k, o.m));
+      else if (o.kind == OP_HEAD)
+        TRY(head_op(o.m));
+      else
+        TRY(backward_op(o.k, o.m));
     }
     // every lane (and its side stream) back into the origin stream
     for (int i = 0; i < c_->nstreams(); ++i) {
@@ -364,9 +319,131 @@ class Executor {
   int ln_buf_[gpipe_ctx::kMaxLanes] = {};  // per lane: the LayerNorm-backward partial buffer to use next
   int gbuf_[gpipe_ctx::kMaxLanes] = {};    // per lane: the gf/gh/gq set the next layer backward uses
   bool rec_[gpipe_ctx::kMaxLanes][EV_COUNT] = {};
-  bool fwd_rec_[gpipe_ctx::kMaxLanes] = {};
+  std::vector<char> fwd_rec_, sfree_rec_, hfree_rec_;  // per (cell or level, ring slot)
   bool bdone_rec_[gpipe_ctx::kMaxLanes][gpipe_ctx::kRing] = {};
   bool bfree_rec_[gpipe_ctx::kMaxLanes][gpipe_ctx::kRing] = {};
+
+  // Forward of cell k for micro-batch m (the embedding first for k = 0),
+  // handing its output to cell k+1 (or the head) through the stash.
+  int forward_op(int k, int m) {
+    const int M = c_->M;
+    const int lk = lane_of(k, m);
+    // one-forward-one-backward: side work of an earlier backward on this lane
+    // may still read the slots that this forward overwrites (in the GPipe
+    // order every forward comes before the first backward)
+    if (c_->schedule != 0) TRY(join_all(lk));
+    if (k == 0) {
+      if (c_->dm.kind == 1) TRY(slot_free_wait(lk, 0, m));
+      TRY(cell0_input(m));
+    } else {
+      TRY(cross_wait(k, m, fwd_ev(k - 1, m), fwd_rec_[fwd_i(k - 1, m)], k - 1));
+    }
+    TRY(slot_free_wait(lk, k + 1, m));
+    TRY(cell_forward(k, m, /*recompute=*/false));
+    if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2), st()));
+    return cross_record(k, m, fwd_ev(k, m), fwd_rec_[fwd_i(k, m)]);
+  }
+
+  // The head of micro-batch m on its own lane: loss rows and the gradient of
+  // the last cell's output.
+  int head_op(int m) {
+    const int M = c_->M, K = c_->K;
+    const int hl = head_lane(m);
+    if (hl != lane_of(K - 1, m))
+      TRY(cuda_ok(cudaStreamWaitEvent(main_s(hl), fwd_ev(K - 1, m), 0), "stream wait"));
+    const int D = c_->ws.depth;
+    if (m >= D && c_->ws.nlanes > 1) {  // the previous user of this output-gradient slot has read it
+      if (!hfree_rec_[(m - D) % D]) return set_error(GPIPE_ERR_INVALID_ARG, "issue order reuses a head slot early");
+      TRY(cuda_ok(cudaStreamWaitEvent(main_s(hl), c_->ev_hfree[(m - D) % D], 0), "stream wait"));
+    }
+    TRY(head(m));
+    if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(K) * M + m) * 2), st()));
+    if (hl != lane_of(K - 1, m)) TRY(cuda_ok(cudaEventRecord(c_->ev_hdone[m], main_s(hl)), "event record"));
+    return GPIPE_OK;
+  }
+
+  // Backward of cell k for micro-batch m with re-computation, handing the
+  // gradient of its input to cell k-1 through the ring.
+  int backward_op(int k, int m) {
+    const int M = c_->M, K = c_->K;
+    const int p = m % c_->ws.ring;
+    const int lk = lane_of(k, m);
+    cur_lane_ = lk;
+    TRY(join_all(lk));  // side work still reading this lane's slots
+    if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
+    // gradient of the cell's output
+    char* dy;
+    const int dy_buf = BUF_EXT;
+    if (k == K - 1) {
+      if (head_lane(m) != lk) TRY(cuda_ok(cudaStreamWaitEvent(main_s(lk), c_->ev_hdone[m], 0), "stream wait"));
+      dy = hdy(m);
+    } else {
+      TRY(cross_wait(k, m, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
+      dy = bgrad(k + 1, p);
+    }
+    int cur_buf = dy_buf;
+    const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
+    for (int j = n - 1; j >= 0; --j) {
+      const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
+      char* dx;
+      int dx_buf;
+      if (j == 0 && k > 0) {
+        // hand the input gradient to cell k-1 through the ring
+        if (bfree_rec_[k][p]) TRY(cross_wait(k, m, c_->ev_bfree[k][p], bfree_rec_[k][p], k - 1));
+        dx = bgrad(k, p);
+        dx_buf = BUF_EXT;
+      } else if (j == 0 && c_->dm.kind == 1) {
+        dx = dx0(m);  // the embedding's input gradient, scattered once at the end
+        dx_buf = BUF_EXT;
+      } else {
+        dx_buf = cur_buf == 0 ? 1 : 0;
+        dx = lbuf(lk, dx_buf);
+      }
+      TRY(layer_backward(first + j, x, slot(k, m, j), dy, cur_buf, dx, dx_buf));
+      dy = dx;
+      cur_buf = dx_buf;
+    }
+    if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2 + 1), st()));
+    if (k > 0) TRY(cross_record(k, m, c_->ev_bdone[k][p], bdone_rec_[k][p]));
+    if (k < K - 1) {  // this cell has finished reading the ring slot of cell k+1
+      TRY(join(lk, EV_DYB));
+      TRY(cross_record(k, m, c_->ev_bfree[k + 1][p], bfree_rec_[k + 1][p]));
+    }
+    const int D = c_->ws.depth;
+    if (D < M && c_->ws.nlanes > 1) {
+      // with a stash ring shorter than M: release this micro-batch's stash
+      // slot of the cell's input (read by the re-computation and the first
+      // layer's LayerNorm backward, both on the main stream) and, for the last
+      // cell, its slot of the head's output gradient (read on the side too)
+      sfree_rec_[static_cast<size_t>(k) * D + m % D] = 1;
+      TRY(cuda_ok(cudaEventRecord(c_->ev_sfree[static_cast<size_t>(k) * D + m % D], main_s(lk)), "event record"));
+      if (k == K - 1) {
+        TRY(join(lk, EV_DYB));
+        hfree_rec_[m % D] = 1;
+        TRY(cuda_ok(cudaEventRecord(c_->ev_hfree[m % D], main_s(lk)), "event record"));
+      }
+    }
+    return GPIPE_OK;
+  }
+
+  // The stash ring: cell k's output event, and the wait, before a slot of
+  // level lev is rewritten for micro-batch m, for its previous micro-batch's
+  // reader (the backward of cell lev, or the head for lev = K).
+  size_t fwd_i(int k, int m) const { return static_cast<size_t>(k) * c_->ws.depth + m % c_->ws.depth; }
+  cudaEvent_t fwd_ev(int k, int m) const { return c_->ev_fwd[fwd_i(k, m)]; }
+  int slot_free_wait(int lane, int lev, int m) {
+    const int D = c_->ws.depth;
+    if (m < D || c_->ws.nlanes == 1) return GPIPE_OK;
+    cudaEvent_t e;
+    if (lev == c_->K) {
+      e = c_->ev_hdone[m - D];
+    } else {
+      const size_t i = static_cast<size_t>(lev) * D + (m - D) % D;
+      if (!sfree_rec_[i]) return set_error(GPIPE_ERR_INVALID_ARG, "issue order reuses a stash slot early");
+      e = c_->ev_sfree[i];
+    }
+    return cuda_ok(cudaStreamWaitEvent(main_s(lane), e, 0), "stream wait");
+  }
 
   // Lane of cell k for micro-batch m: with lanes, cell k owns lanes
   // k*inflight .. k*inflight + inflight-1 and takes its micro-batches in turn.
@@ -378,7 +455,7 @@ class Executor {
   // those of the first head lane), which receive the weight-gradient work in
   // micro-batch order.
   int side_of(int lane) const { return lane < c_->ws.nlanes ? lane - lane % c_->ws.inflight : c_->ws.nlanes; }
-  char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
+  char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m % c_->ws.depth) * c_->ws.stash_bytes; }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
   // Weight-gradient work goes to a side stream when CONCURRENT is on, and
   // always when a cell or the head has more than one lane (its lanes must not
@@ -405,7 +482,8 @@ class Executor {
     return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   }
   // cross-lane handshakes (no-ops when both cells share a lane)
-  int cross_record(int k, int m, cudaEvent_t e, bool& rec) {
+  template <typename Flag>
+  int cross_record(int k, int m, cudaEvent_t e, Flag& rec) {
     if (c_->ws.nlanes == 1) return GPIPE_OK;
     rec = true;
     return cuda_ok(cudaEventRecord(e, main_s(lane_of(k, m))), "event record");
@@ -475,7 +553,7 @@ class Executor {
     return static_cast<const int32_t*>(p_.batch) + static_cast<size_t>(m) * c_->Tmb();
   }
   char* stash(int k, int m) const {
-    return ws(c_->ws.stash) + (static_cast<size_t>(k) * c_->M + m) * c_->ws.stash_bytes;
+    return ws(c_->ws.stash) + (static_cast<size_t>(k) * c_->ws.depth + m % c_->ws.depth) * c_->ws.stash_bytes;
   }
   char* dx0(int m) const { return ws(c_->ws.dx0) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   char* bgrad(int k, int p) const {
@@ -881,6 +959,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[9] = c->sm_share;
     key.opts[10] = c->side_share;
     key.opts[11] = c->nside;
+    key.opts[12] = c->schedule;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -942,11 +1021,32 @@ int gpipe_schedule_model(const gpipe_ctx* c, const double* t_f, const double* t_
     tf[k] = t_f ? t_f[k] : cellcost;
     tb[k] = t_b ? t_b[k] : 2.0 * cellcost;
   }
-  double b = 0.0;
-  double ms = simulate_gpipe(c->K, c->M, tf.data(), tb.data(), &b);
+  double b = 0.0, ms = 0.0;
+  if (c->schedule == 0) {
+    ms = simulate_gpipe(c->K, c->M, tf.data(), tb.data(), &b);
+  } else {
+    std::vector<Op> ops;
+    if (!issue_order(c->K, c->M, c->schedule, 2, ops)) return GPIPE_ERR_INVALID_ARG;
+    ms = simulate_order(c->K, c->M, ops, tf.data(), tb.data(), &b);
+  }
   if (makespan) *makespan = ms;
   if (bubble) *bubble = b;
   return GPIPE_OK;
+}
+
+int gpipe_issue_order(const gpipe_ctx* cc, int32_t* ops_out, int count) {
+  if (!cc || count < 0 || (count > 0 && !ops_out)) return GPIPE_ERR_INVALID_ARG;
+  gpipe_ctx* c = const_cast<gpipe_ctx*>(cc);
+  c->refresh_ws();
+  std::vector<Op> ops;
+  if (!issue_order(c->K, c->M, c->schedule, c->ws.ring, ops)) return c->fail(GPIPE_ERR_INVALID_ARG, "no issue order");
+  for (int i = 0; i < count && i < static_cast<int>(ops.size()); ++i) {
+    ops_out[4 * i] = ops[i].kind;
+    ops_out[4 * i + 1] = ops[i].k;
+    ops_out[4 * i + 2] = ops[i].m;
+    ops_out[4 * i + 3] = ops[i].tick;
+  }
+  return static_cast<int>(ops.size());
 }
 
 int gpipe_memory_report(const gpipe_ctx* cc, size_t* peak_act_bytes, size_t* model_bound_bytes) {
@@ -974,6 +1074,11 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_SCHEDULE:
+      if (value < 0 || value > 1) return c->fail(GPIPE_ERR_INVALID_ARG, "schedule must be 0 (GPipe) or 1 (1F1B)");
+      c->schedule = static_cast<int>(value);
+      c->ws_stale = true;
+      break;
     case GPIPE_OPT_SIDE_STREAMS:
       if (value < 1 || value > gpipe_ctx::kSides)
         return c->fail(GPIPE_ERR_INVALID_ARG, "side streams per lane must be 1..4");
@@ -1079,12 +1184,12 @@ void gpipe_destroy(gpipe_ctx* c) {
       if (c->ev_bdone[i][r]) cudaEventDestroy(c->ev_bdone[i][r]);
       if (c->ev_bfree[i][r]) cudaEventDestroy(c->ev_bfree[i][r]);
     }
-    for (cudaEvent_t e : {c->ev_fwd[i], c->ev_lane_end[i]})
-      if (e) cudaEventDestroy(e);
+    if (c->ev_lane_end[i]) cudaEventDestroy(c->ev_lane_end[i]);
   }
   if (c->ev_origin) cudaEventDestroy(c->ev_origin);
-  for (cudaEvent_t e : c->ev_hdone)
-    if (e) cudaEventDestroy(e);
+  for (const auto* v : {&c->ev_hdone, &c->ev_fwd, &c->ev_sfree, &c->ev_hfree})
+    for (cudaEvent_t e : *v)
+      if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : c->kt_ev)
     if (e) cudaEventDestroy(e);
   delete c;

@@ -9,6 +9,14 @@
 // Clock model: "Pipeline flow" (phases 1-3) and "Bubble overhead analysis";
 // with equal cells the bubble is (K-1)/(M+K-1).
 //
+// Issue orders: the GPipe order of "Pipeline flow", or the
+// one-forward-one-backward order that the review's "Historical impact" section
+// credits to PipeDream-2BW (forward and backward interleaved to cut the peak
+// memory of accumulated activations); the PipeDream page's citing works
+// describe it as starting backward passes earlier without changing the
+// result.  Both orders differentiate each cell's micro-batches in ascending
+// order, so the gradients accumulate in the same order.
+//
 // Workspace: "Preliminaries 5: re-materialisation" - only the cell-boundary
 // activations of every micro-batch are kept (stash), plus the internals of
 // the one cell being differentiated for one micro-batch, giving the review's
@@ -84,6 +92,111 @@ double simulate_gpipe(int K, int M, const double* t_f, const double* t_b, double
   return makespan;
 }
 
+int stash_depth(int K, int M, int schedule) { return schedule == 1 ? std::min(M, K + 1) : M; }
+
+namespace {
+// Position of op (kind, k, m) in a K x M table per kind (the head uses k = 0).
+inline size_t op_index(int kind, int k, int m, int K, int M) {
+  return (static_cast<size_t>(kind) * (K + 1) + k) * M + m;
+}
+}  // namespace
+
+bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops) {
+  ops.clear();
+  if (K < 1 || M < 1 || ring < 1) return false;
+  if (schedule == 0) {
+    // ticks: forward phase t = k + m; backward phase after it, t = M + K - 1 + (K - 1 - k) + m
+    for (int m = 0; m < M; ++m) {
+      for (int k = 0; k < K; ++k) ops.push_back(Op{OP_FWD, k, m, k + m});
+      ops.push_back(Op{OP_HEAD, 0, m, K - 1 + m});
+    }
+    for (int m = 0; m < M; ++m)
+      for (int k = K - 1; k >= 0; --k) ops.push_back(Op{OP_BWD, k, m, M + K - 1 + (K - 1 - k) + m});
+    return true;
+  }
+  if (schedule != 1) return false;
+  const int D = stash_depth(K, M, schedule);
+  // per-stage sequences: cells 0..K-1, then the head (stage K)
+  std::vector<std::vector<Op>> seq(K + 1);
+  for (int k = 0; k < K; ++k) {
+    const int f0 = std::min(M, K + 1 - k);
+    for (int m = 0; m < f0; ++m) seq[k].push_back(Op{OP_FWD, k, m, 0});
+    for (int i = 0; i < M; ++i) {
+      seq[k].push_back(Op{OP_BWD, k, i, 0});
+      if (f0 + i < M) seq[k].push_back(Op{OP_FWD, k, f0 + i, 0});
+    }
+  }
+  for (int m = 0; m < M; ++m) seq[K].push_back(Op{OP_HEAD, 0, m, 0});
+  std::vector<int> round_of(static_cast<size_t>(3) * (K + 1) * M, -1);
+  auto issued_before = [&](int kind, int k, int m, int r) {
+    const int at = round_of[op_index(kind, k, m, K, M)];
+    return at >= 0 && at < r;
+  };
+  auto ready = [&](const Op& o, int r) {
+    if (o.kind == OP_FWD) {
+      if (o.k > 0 && !issued_before(OP_FWD, o.k - 1, o.m, r)) return false;
+      // the stash slot it writes (cell k's output; the embedding's for k = 0)
+      // was released by the previous micro-batch in it
+      if (o.m >= D) {
+        const int pm = o.m - D;
+        if (o.k + 1 < K ? !issued_before(OP_BWD, o.k + 1, pm, r) : !issued_before(OP_HEAD, 0, pm, r)) return false;
+        if (o.k == 0 && !issued_before(OP_BWD, 0, pm, r)) return false;
+      }
+      return true;
+    }
+    if (o.kind == OP_HEAD) {
+      if (!issued_before(OP_FWD, K - 1, o.m, r)) return false;
+      return o.m < D || issued_before(OP_BWD, K - 1, o.m - D, r);  // its output-gradient slot
+    }
+    if (o.k == K - 1 ? !issued_before(OP_HEAD, 0, o.m, r) : !issued_before(OP_BWD, o.k + 1, o.m, r)) return false;
+    return o.k == 0 || o.m < ring || issued_before(OP_BWD, o.k - 1, o.m - ring, r);  // its ring slot
+  };
+  std::vector<size_t> pos(K + 1, 0);
+  const size_t total = static_cast<size_t>(2 * K + 1) * M;
+  for (int r = 0; ops.size() < total; ++r) {
+    std::vector<Op> batch;
+    for (int s = 0; s <= K; ++s)
+      if (pos[s] < seq[s].size() && ready(seq[s][pos[s]], r)) batch.push_back(seq[s][pos[s]]);
+    if (batch.empty()) return false;
+    for (Op o : batch) {
+      o.tick = r;
+      round_of[op_index(o.kind, o.k, o.m, K, M)] = r;
+      ++pos[o.kind == OP_HEAD ? K : o.k];
+      ops.push_back(o);
+    }
+  }
+  return true;
+}
+
+double simulate_order(int K, int M, const std::vector<Op>& ops, const double* t_f, const double* t_b,
+                      double* bubble) {
+  std::vector<double> fin(static_cast<size_t>(3) * (K + 1) * M, 0.0), stage_free(K + 1, 0.0);
+  double makespan = 0.0;
+  for (const Op& o : ops) {
+    const int s = o.kind == OP_HEAD ? K : o.k;
+    double start = stage_free[s];
+    double dur = 0.0;
+    if (o.kind == OP_FWD) {
+      if (o.k > 0) start = std::max(start, fin[op_index(OP_FWD, o.k - 1, o.m, K, M)]);
+      dur = t_f[o.k];
+    } else if (o.kind == OP_HEAD) {
+      start = std::max(start, fin[op_index(OP_FWD, K - 1, o.m, K, M)]);
+    } else {
+      start = std::max(start, o.k == K - 1 ? fin[op_index(OP_HEAD, 0, o.m, K, M)]
+                                           : fin[op_index(OP_BWD, o.k + 1, o.m, K, M)]);
+      dur = t_b[o.k];
+    }
+    const double end = start + dur;
+    fin[op_index(o.kind, o.k, o.m, K, M)] = end;
+    stage_free[s] = end;
+    makespan = std::max(makespan, end);
+  }
+  double busy = 0.0;
+  for (int k = 0; k < K; ++k) busy += M * (t_f[k] + t_b[k]);
+  if (bubble) *bubble = makespan > 0 ? 1.0 - busy / (K * makespan) : 0.0;
+  return makespan;
+}
+
 ParamLayout make_param_layout(const Dims& dm, int L) {
   ParamLayout p;
   const size_t d = dm.d, f = dm.ffn;
@@ -127,8 +240,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check,
-                         bool pipelined, int inflight) {
+                         bool pipelined, int inflight, int depth) {
   Workspace w;
+  w.depth = depth > 0 && depth < M ? depth : M;
   const size_t es = dm.dtype == 0 ? 4 : 2;
   const size_t T = static_cast<size_t>(dm.n) * (dm.kind == 1 ? dm.seq : 1);
   const size_t Tmb = T / M;
@@ -200,14 +314,14 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     return at;
   };
   w.stash_bytes = Tmb * d * es;
-  w.stash = take(static_cast<size_t>(K + 1) * M * w.stash_bytes);
+  w.stash = take(static_cast<size_t>(K + 1) * w.depth * w.stash_bytes);
   w.dx0 = take(dm.kind == 1 ? static_cast<size_t>(M) * w.stash_bytes : 0);
   w.ring = w.inflight > 2 ? w.inflight : 2;
   w.bgrad = take(static_cast<size_t>(K) * w.ring * w.stash_bytes);
   w.lanes = take(static_cast<size_t>(w.nlanes) * ln.bytes);
   w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
   w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
-  w.hdy = take(static_cast<size_t>(M) * w.stash_bytes);
+  w.hdy = take(static_cast<size_t>(w.depth) * w.stash_bytes);
   w.nheads = dm.kind == 1 && w.nlanes > 1 ? 2 : 1;
   for (int h = 0; h < w.nheads && dm.kind == 1; ++h) {
     Workspace::Head& hb = w.head[h];
@@ -230,12 +344,14 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   }
   w.total = off;
   // The review's bound O(N + (L/K)(N/M)) per accelerator, with explicit
-  // constants, summed over the lanes: the boundary tensors (stash, the
-  // embedding's input gradient and the gradient ring; proportional to N), and
+  // constants, summed over the lanes: the boundary tensors (stash and the
+  // head's output gradient, depth micro-batches each; the embedding's input
+  // gradient; the gradient ring; proportional to N), and
   // per lane one cell of Lc layers of kept internals for one micro-batch plus
   // that lane's gradient buffers (proportional to (L/K)(N/M)); per head lane
   // the logits of one micro-batch and its temporaries; the per-row losses.
-  const size_t boundary = static_cast<size_t>(K + 3) * T * d * es + static_cast<size_t>(K) * w.ring * Tmb * d * es;
+  const size_t boundary = static_cast<size_t>(K + 2) * w.depth * Tmb * d * es + T * d * es +
+                          static_cast<size_t>(K) * w.ring * Tmb * d * es;
   const size_t per_lane = ln.bytes + 4096;
   const size_t head =
       dm.kind == 1

@@ -20,6 +20,38 @@ bool partition_min_variance(const std::vector<int64_t>& costs, int K, std::vecto
 // it the data.  Returns makespan; bubble = 1 - sum busy / (K makespan).
 double simulate_gpipe(int K, int M, const double* t_f, const double* t_b, double* bubble);
 
+// One operation of a step's issue order: the forward of cell k (with the
+// embedding first when k == 0), the head, or the backward (re-computation
+// included) of cell k, for micro-batch m.  tick: the round of the list
+// scheduler that issued it (ops of one tick can run at once).
+enum OpKind { OP_FWD = 0, OP_HEAD = 1, OP_BWD = 2 };
+struct Op {
+  int kind, k, m, tick;
+};
+
+// Depth of the ring that holds each cell boundary (and the head's output
+// gradient): M for the GPipe order (every micro-batch's stash lives until the
+// backward), min(M, K + 1) for the one-forward-one-backward order.
+int stash_depth(int K, int M, int schedule);
+
+// The step's issue order.  schedule 0 (GPipe, the review's "Pipeline flow"):
+// for m, for k: F(k, m), then H(m); then for m, for k = K-1..0: B(k, m).
+// schedule 1 (one-forward-one-backward): cell k runs min(M, K + 1 - k)
+// forwards, then alternates one backward and one forward (backwards in
+// micro-batch order), then its remaining backwards; the head is a stage after
+// the last cell.  The per-stage sequences are merged by a list scheduler that
+// issues, round by round, every stage's next op whose producers were issued in
+// earlier rounds and whose buffer slot (stash ring of depth stash_depth, input-
+// gradient ring of depth ring) its previous user has released.  Returns false
+// on a deadlock (cannot happen for ring >= 2 and depth >= min(M, K + 1)).
+bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops);
+
+// Clock of an issue order: each stage runs its ops in order; an op starts when
+// its stage is free and its producers have finished (forward of cell k: t_f[k],
+// backward: t_b[k], head: 0).  Same quantities as simulate_gpipe.
+double simulate_order(int K, int M, const std::vector<Op>& ops, const double* t_f, const double* t_b,
+                      double* bubble);
+
 struct Dims {
   int kind, d, heads, ffn, seq, vocab, n, dtype;
   float lr, decay, eps;
@@ -56,7 +88,8 @@ struct LaneLayout {
 };
 
 struct Workspace {
-  size_t stash = 0, stash_bytes = 0;        // (K+1) x M boundary tensors [Tmb, d]
+  size_t stash = 0, stash_bytes = 0;        // (K+1) x depth boundary tensors [Tmb, d]
+  int depth = 1;                            // stash ring depth (micro-batch m in slot m mod depth)
   size_t dx0 = 0;                           // M x [Tmb, d]: gradient w.r.t. the embedding output (kind 1)
   size_t bgrad = 0;                         // K x ring x [Tmb, d]: gradient w.r.t. cell k's input
   int ring = 2;                             // depth of that ring: max(2, micro-batches in flight per cell)
@@ -75,7 +108,7 @@ struct Workspace {
   Head head[2]{};
   int nheads = 1;                           // head lanes: 2 (alternate micro-batches) when pipelined
   size_t lnp_bytes = 0;                     // ceil(Tmb / 8) x 2d fp32
-  size_t hdy = 0;                           // M x [Tmb, d]: gradient of the last cell's output per micro-batch
+  size_t hdy = 0;                           // depth x [Tmb, d]: gradient of the last cell's output per micro-batch
   size_t scratch_bytes = 0;
   size_t loss_rows = 0, misc = 0;            // misc: loss (float) at +0, remat counter (u64) at +8
   size_t trace = 0, trace_count = 0;         // phase timestamps (u64): start, end, then per (cell/head, m, phase)
@@ -87,6 +120,6 @@ struct Workspace {
 };
 
 Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check,
-                         bool pipelined, int inflight = 1);
+                         bool pipelined, int inflight = 1, int depth = 0 /* 0: M */);
 
 }  // namespace gp

@@ -172,19 +172,23 @@ def test_steps_are_bit_reproducible_and_graph_equals_direct(b):
 
 @pytest.mark.parametrize("wname", ["small_lm", "tiny_ffn", "lm_small"])
 def test_schedules_are_bit_identical(b, wname):
-    """Cells as concurrent lanes (the review's pipeline on one GPU) and weight
-    gradients on side streams give exactly the one-stream, cells-in-turn
-    result, with and without the CUDA graph."""
+    """Cells as concurrent lanes (the review's pipeline on one GPU), weight
+    gradients on side streams and the one-forward-one-backward issue order
+    (with its shorter stash ring) give exactly the one-stream, cells-in-turn
+    GPipe result, with and without the CUDA graph."""
     w = SMALL_LM if wname == "small_lm" else WORKLOADS[wname]
     inp = make_inputs(w)
     outs = []
-    for pipe, conc, graph, pdl, inflight, nside in (
-            (0, 0, 1, 0, 1, 1), (1, 1, 1, 1, 1, 1), (1, 0, 1, 1, 1, 1), (0, 1, 1, 1, 1, 1), (1, 1, 0, 1, 1, 1),
-            (1, 1, 1, 0, 1, 1), (1, 1, 1, 0, 2, 1), (1, 0, 0, 0, 2, 1), (1, 1, 1, 0, 3, 1), (1, 1, 1, 0, 4, 1),
-            (1, 1, 1, 0, 2, 4), (1, 1, 1, 0, 1, 3), (0, 1, 0, 0, 1, 2)):
+    for pipe, conc, graph, pdl, inflight, nside, sched in (
+            (0, 0, 1, 0, 1, 1, 0), (1, 1, 1, 1, 1, 1, 0), (1, 0, 1, 1, 1, 1, 0), (0, 1, 1, 1, 1, 1, 0),
+            (1, 1, 0, 1, 1, 1, 0), (1, 1, 1, 0, 1, 1, 0), (1, 1, 1, 0, 2, 1, 0), (1, 0, 0, 0, 2, 1, 0),
+            (1, 1, 1, 0, 3, 1, 0), (1, 1, 1, 0, 4, 1, 0), (1, 1, 1, 0, 2, 4, 0), (1, 1, 1, 0, 1, 3, 0),
+            (0, 1, 0, 0, 1, 2, 0), (1, 1, 1, 0, 1, 2, 1), (1, 1, 1, 0, 2, 2, 1), (1, 1, 0, 0, 2, 2, 1),
+            (0, 1, 1, 0, 1, 2, 1), (1, 1, 1, 0, 4, 2, 1)):
         _, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_INFLIGHT, inflight), (b.OPT_PIPELINE, pipe),
                                                      (b.OPT_CONCURRENT, conc), (b.OPT_GRAPH, graph),
-                                                     (b.OPT_PDL, pdl), (b.OPT_SIDE_STREAMS, nside)])
+                                                     (b.OPT_PDL, pdl), (b.OPT_SIDE_STREAMS, nside),
+                                                     (b.OPT_SCHEDULE, sched)])
         outs.append((loss, st.g32.cpu().numpy().copy(), st.p32.cpu().numpy().copy()))
     for i, o in enumerate(outs[1:], 1):
         assert o[0] == outs[0][0], i
@@ -242,16 +246,19 @@ def test_loss_near_log_vocab_and_update_from_zero_state(b):
     assert np.all(np.sign(dw[big]) == -np.sign(g[big]))
 
 
-@pytest.mark.parametrize("inflight", [1, 2, 4])
-def test_trace_follows_the_pipeline_dependencies(b, inflight):
+@pytest.mark.parametrize("inflight,sched", [(1, 0), (2, 0), (4, 0), (1, 1), (2, 1)])
+def test_trace_follows_the_pipeline_dependencies(b, inflight, sched):
     """With cells as concurrent lanes, GPU timestamps obey the review's pipeline:
     cell k finishes forwarding micro-batch m after cell k-1, the head after the
     last cell, the last cell's backward after the head, cell k-1's backward
     after cell k's, and every lane takes its micro-batches in order (with two
     in flight per cell, a cell's lanes take alternate micro-batches; so do the
-    two head lanes)."""
+    two head lanes).  In the one-forward-one-backward order a stash slot is
+    rewritten only after its previous micro-batch's reader finished, and cell
+    0 differentiates micro-batch 0 before it forwards the last one."""
     w = WORKLOADS["lm_small"]
-    gp, st, _, _ = _run(b, w, make_inputs(w), options=[(b.OPT_INFLIGHT, inflight), (b.OPT_TRACE, 1)])
+    gp, st, _, _ = _run(b, w, make_inputs(w), options=[(b.OPT_INFLIGHT, inflight), (b.OPT_TRACE, 1),
+                                                       (b.OPT_SCHEDULE, sched)])
     t0, t1, fwd, bwd = gp.trace(st.ws, st.stream)
     K, M = w.K, w.M
     assert t0 <= fwd.min() and max(fwd.max(), bwd[:K].max()) <= t1
@@ -266,6 +273,16 @@ def test_trace_follows_the_pipeline_dependencies(b, inflight):
         assert np.all(np.diff(bwd[:K, r::inflight], axis=1) >= 0)
     for r in range(2):  # two head lanes take alternate micro-batches, each in order
         assert np.all(np.diff(fwd[K, r::2]) >= 0)
+    if sched == 1:
+        D = min(M, K + 1)
+        assert D < M
+        for m in range(D, M):
+            assert fwd[0, m] >= bwd[0, m - D]          # the embedding's output slot
+            for k in range(K - 1):
+                assert fwd[k, m] >= bwd[k + 1, m - D]  # cell k's output slot
+            assert fwd[K - 1, m] >= fwd[K, m - D]      # the head's input slot
+            assert fwd[K, m] >= bwd[K - 1, m - D]      # the head's output-gradient slot
+        assert bwd[0, 0] <= fwd[0, M - 1]
 
 
 @pytest.mark.parametrize("graph", [1, 0])

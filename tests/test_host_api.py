@@ -247,3 +247,111 @@ def test_options_are_validated_and_kernel_times_start_empty(binding):
     # the op API's SM share for gpipe_op_gemm: >= 0 (0 = the whole GPU)
     assert binding.lib().gpipe_op_gemm_set_sm_share(-1) == -1
     assert binding.lib().gpipe_op_gemm_set_sm_share(0) == 0
+
+
+def _check_issue_order(ops, K, M, schedule, ring, lm=True):
+    """Checks an issue order against the pipeline's dependencies (written out
+    here from the review's "Pipeline flow": cell k forwards m after cell k-1,
+    the head after the last cell, cell k differentiates m after cell k+1 (the
+    last cell after the head)), the micro-batch order of each cell's
+    backwards (the gradient accumulation order), and buffer reuse: a stash
+    slot (depth D) or an input-gradient ring slot (depth R) is rewritten only
+    after its previous reader was issued."""
+    pos = {}
+    for i, (kind, k, m, tick) in enumerate(ops):
+        key = (kind, k, m)
+        assert key not in pos, key
+        pos[key] = i
+    F = lambda k, m: pos[(0, k, m)]
+    H = lambda m: pos[(1, 0, m)]
+    B = lambda k, m: pos[(2, k, m)]
+    assert len(pos) == (2 * K + 1) * M
+    D = min(M, K + 1) if schedule == 1 else M
+    for m in range(M):
+        assert H(m) > F(K - 1, m) and B(K - 1, m) > H(m)
+        if m:
+            assert H(m) > H(m - 1)
+        for k in range(K):
+            assert B(k, m) > F(k, m)
+            if k:
+                assert F(k, m) > F(k - 1, m)
+            if k < K - 1:
+                assert B(k, m) > B(k + 1, m)
+            if m:
+                assert F(k, m) > F(k, m - 1) and B(k, m) > B(k, m - 1)
+            if k and m >= ring:
+                assert B(k, m) > B(k - 1, m - ring)
+        if m >= D:
+            # level 0 (embedding output) and level k+1 (cell k's output)
+            if lm:
+                assert F(0, m) > B(0, m - D)
+            for k in range(K):
+                reader = H(m - D) if k == K - 1 else B(k + 1, m - D)
+                assert F(k, m) > reader
+            assert H(m) > B(K - 1, m - D)
+    # ticks: a producer is issued in an earlier tick than its consumer
+    tick = {(kind, k, m): t for kind, k, m, t in ops}
+    for m in range(M):
+        for k in range(1, K):
+            assert tick[(0, k, m)] > tick[(0, k - 1, m)]
+            assert tick[(2, k - 1, m)] > tick[(2, k, m)]
+    return D
+
+
+@pytest.mark.parametrize("schedule", [0, 1])
+@pytest.mark.parametrize("K,M,inflight", [(1, 1, 1), (1, 5, 2), (2, 1, 1), (3, 7, 1), (4, 16, 2), (4, 4, 1),
+                                          (8, 32, 1), (8, 4, 4), (16, 64, 1), (5, 3, 3)])
+def test_issue_order_respects_dependencies_and_buffer_reuse(binding, schedule, K, M, inflight):
+    g = binding.GPipe(2 * K, K, M, kind=1, d=64, heads=1, ffn=64, seq=64, vocab=64, n=M, dtype=1)
+    g.set_option(binding.OPT_INFLIGHT, inflight)
+    g.set_option(binding.OPT_SCHEDULE, schedule)
+    ops = g.issue_order()
+    ring = max(2, inflight)
+    _check_issue_order(ops, K, M, schedule, ring)
+    if schedule == 0:
+        # the review's figure: every forward (and head) before the first backward
+        first_b = min(i for i, o in enumerate(ops) if o[0] == binding.OP_BWD)
+        assert all(o[0] != binding.OP_BWD for o in ops[:first_b]) and first_b == (K + 1) * M
+    else:
+        # one-forward-one-backward: cell k runs min(M, K+1-k) forwards before its
+        # first backward, then never more than that many ahead of its backwards
+        for k in range(K):
+            seq = [o[0] for o in ops if o[1] == k and o[0] != binding.OP_HEAD]
+            assert seq.index(binding.OP_BWD) == min(M, K + 1 - k)
+            ahead = 0
+            for kind in seq:
+                ahead += 1 if kind == binding.OP_FWD else -1
+                assert 0 <= ahead <= min(M, K + 1 - k)
+
+
+@pytest.mark.parametrize("K,M", [(1, 1), (2, 1), (4, 32), (8, 32), (4, 4), (3, 7), (16, 64)])
+def test_one_f_one_b_clock_equals_gpipe_for_equal_cells(binding, K, M):
+    """With equal cells the interleaved order finishes when the GPipe order
+    does: the same bubble (K-1)/(M+K-1) (backward twice the forward here)."""
+    g = binding.GPipe(K, K, M, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=M, dtype=0)
+    g.set_option(binding.OPT_SCHEDULE, 1)
+    mk, bub = g.schedule_model([1.0] * K, [2.0] * K)
+    sim = osch.simulate(K, M, 1, 2)
+    assert mk == pytest.approx(float(sim["makespan"]), rel=1e-12)
+    assert bub == pytest.approx(float(Fraction(K - 1, M + K - 1)), abs=1e-12)
+
+
+@pytest.mark.parametrize("name", ["lm_small", "lm_wide", "lm_deep"])
+def test_one_f_one_b_keeps_a_shorter_stash(binding, name):
+    """The interleaved order holds min(M, K+1) micro-batches per cell boundary
+    (and of the head's output gradient) instead of M: the workspace shrinks by
+    exactly (K+2)(M - D) boundary tensors, and stays within its bound."""
+    w = WORKLOADS[name]
+    g = binding.GPipe.from_workload(w)
+    peak0, bound0 = g.memory_report()
+    ws0 = g.sizes()[1]
+    g.set_option(binding.OPT_SCHEDULE, 1)
+    peak1, bound1 = g.memory_report()
+    ws1 = g.sizes()[1]
+    D = min(w.M, w.K + 1)
+    stash = w.tokens // w.M * w.d * 2
+    assert peak0 - peak1 == (w.K + 2) * (w.M - D) * stash
+    assert ws0 - ws1 == peak0 - peak1
+    assert peak1 <= bound1 and bound0 - bound1 == peak0 - peak1
+    with pytest.raises(binding.GpipeError):
+        g.set_option(binding.OPT_SCHEDULE, 2)
