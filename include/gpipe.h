@@ -239,7 +239,7 @@ enum {
                                 always uses the same stream, so every gradient still
                                 accumulates in micro-batch order and results are
                                 identical                                            */
-  GPIPE_OPT_SCHEDULE = 15    /* [0] issue order of the step.  0: the review's GPipe
+  GPIPE_OPT_SCHEDULE = 15,   /* [0] issue order of the step.  0: the review's GPipe
                                 order (every micro-batch forward through all cells,
                                 then every backward), each cell boundary stashed for
                                 all M micro-batches.  1: one-forward-one-backward:
@@ -250,6 +250,11 @@ enum {
                                 still differentiates its micro-batches in ascending
                                 order, so results are identical.  Set before
                                 gpipe_sizes (it changes the workspace size).          */
+  GPIPE_OPT_LOGIT_CLIP = 16  /* [0] value v > 0: logit clipping (the review's
+                                "Training stability"): the cross-entropy sees each
+                                logit clamped to [-c, c], c = v / 1000 rounded to
+                                fp32, and its gradient is zero where |z| > c.  0: no
+                                clipping.  0 <= v <= 1e9.  Only the LM (kind 1).     */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 

@@ -132,6 +132,16 @@ int gpipe_op_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, 
                            float inv_count, float* logits, float* loss_rows, int want_grad,
                            void* stream);
 
+/* The same with logit clipping ("GPipe technical review", "Training
+ * stability": logits above a threshold are clipped before the softmax).
+ * clip > 0: the softmax and the target term see min(max(z, -clip), clip), and
+ * dz is zero where |z| > clip (the clamp's derivative; a NaN logit stays NaN in
+ * the loss).  clip = 0: no clipping, exactly gpipe_op_cross_entropy.  A
+ * negative or NaN clip is rejected (GPIPE_ERR_INVALID_ARG). */
+int gpipe_op_cross_entropy_clip(int rows, int vocab, int seq, const int32_t* tokens, int row0,
+                                float inv_count, float clip, float* logits, float* loss_rows,
+                                int want_grad, void* stream);
+
 /* MSE rows: loss_rows[r] = sum_j (y - t)^2 * inv_count; dy = 2 (y - t) inv_count. */
 int gpipe_op_mse(int rows, int d, const float* y, const float* t, float inv_count,
                  float* loss_rows, float* dy, void* stream);

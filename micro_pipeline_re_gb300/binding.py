@@ -29,6 +29,7 @@ OPT_INFLIGHT = 12
 OPT_SIDE_SHARE = 13
 OPT_SIDE_STREAMS = 14
 OPT_SCHEDULE = 15
+OPT_LOGIT_CLIP = 16
 SCHEDULE_GPIPE, SCHEDULE_1F1B = 0, 1
 OP_FWD, OP_HEAD, OP_BWD = 0, 1, 2
 EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
@@ -84,6 +85,8 @@ _SIGS = {
     "gpipe_op_attention_fwd": (c_int, [c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "gpipe_op_attention_bwd": (c_int, [c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_void_p]),
+    "gpipe_op_cross_entropy_clip": (c_int, [c_int, c_int, c_int, c_void_p, c_int, c_float, c_float, c_void_p, c_void_p,
+                                            c_int, c_void_p]),
     "gpipe_op_cross_entropy": (c_int, [c_int, c_int, c_int, c_void_p, c_int, c_float, c_void_p, c_void_p, c_int,
                                        c_void_p]),
     "gpipe_op_mse": (c_int, [c_int, c_int, c_void_p, c_void_p, c_float, c_void_p, c_void_p, c_void_p]),
@@ -157,9 +160,12 @@ class GPipe:
 
     @classmethod
     def from_workload(cls, w, cost=None, K=None, M=None):
-        return cls(w.L, K or w.K, M or w.M, kind=w.kind, d=w.d, heads=w.heads, ffn=w.ffn,
-                   seq=w.seq if w.kind == 1 else 1, vocab=w.vocab, n=w.n, dtype=0 if w.dtype == "f32" else 1,
-                   lr=w.lr, decay=w.decay, eps=w.eps, cost=cost)
+        g = cls(w.L, K or w.K, M or w.M, kind=w.kind, d=w.d, heads=w.heads, ffn=w.ffn,
+                seq=w.seq if w.kind == 1 else 1, vocab=w.vocab, n=w.n, dtype=0 if w.dtype == "f32" else 1,
+                lr=w.lr, decay=w.decay, eps=w.eps, cost=cost)
+        if getattr(w, "logit_clip_milli", 0):
+            g.set_option(OPT_LOGIT_CLIP, w.logit_clip_milli)
+        return g
 
     def close(self):
         if getattr(self, "h", None):

@@ -301,12 +301,18 @@ __global__ void __launch_bounds__(256) dbias_k_kernel(const __nv_bfloat16* __res
 
 // ---------------------------------------------------------------------------
 // Softmax cross-entropy on fp32 logits, one CTA (512 threads) per row.
+// clip > 0: logit clipping ("GPipe technical review", "Training stability"):
+// the softmax sees min(max(z, -clip), clip), and the gradient is zero where a
+// logit lies outside [-clip, clip] (the derivative of the clamp).
 // ---------------------------------------------------------------------------
 constexpr int kCeThreads = 512;
 
+// The clamp keeps a NaN a NaN (so a non-finite loss is still reported).
+__device__ __forceinline__ float clip_logit(float x, float c) { return x < -c ? -c : (x > c ? c : x); }
+
 __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logits, int vocab, int seq,
                                                         const int32_t* __restrict__ tokens, int row0,
-                                                        float inv_count, float* __restrict__ loss_rows,
+                                                        float inv_count, float clip, float* __restrict__ loss_rows,
                                                         int want_grad, int* err) {
   griddep_wait();
   griddep_launch();
@@ -325,10 +331,17 @@ __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logi
   const int n4 = vocab / 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  const bool clipping = clip > 0.f;
   // pass 1: running max and rescaled sum of exp
   float m = -INFINITY, s = 0.f;
   for (int i = tid; i < n4; i += kCeThreads) {
-    const float4 v = z4[i];
+    float4 v = z4[i];
+    if (clipping) {
+      v.x = clip_logit(v.x, clip);
+      v.y = clip_logit(v.y, clip);
+      v.z = clip_logit(v.z, clip);
+      v.w = clip_logit(v.w, clip);
+    }
     const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
     if (mx > m) {
       s *= expf(m - mx);
@@ -359,7 +372,7 @@ __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logi
     }
     const float lse = M + logf(S);
     sh_lse = lse;
-    loss_rows[r] = tgt >= 0 ? (lse - z[tgt]) * inv_count : 0.f;
+    loss_rows[r] = tgt >= 0 ? (lse - (clipping ? clip_logit(z[tgt], clip) : z[tgt])) * inv_count : 0.f;
   }
   __syncthreads();
   if (!want_grad) return;
@@ -375,10 +388,17 @@ __global__ void __launch_bounds__(kCeThreads) ce_kernel(float* __restrict__ logi
     if (i < n4) v = z4[i];
     __syncthreads();
     if (i < n4) {
-      float p[4] = {expf(v.x - lse) * scale, expf(v.y - lse) * scale, expf(v.z - lse) * scale,
-                    expf(v.w - lse) * scale};
+      const float zv[4] = {v.x, v.y, v.z, v.w};
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = expf((clipping ? clip_logit(zv[e], clip) : zv[e]) - lse) * scale;
       const int c0 = 4 * i;
       if (tgt >= c0 && tgt < c0 + 4) p[tgt - c0] -= scale;
+      if (clipping) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (!(fabsf(zv[e]) <= clip)) p[e] = 0.f;
+      }
       uint2 u;
       u.x = pack_bf16x2(p[0], p[1]);
       u.y = pack_bf16x2(p[2], p[3]);
@@ -704,12 +724,13 @@ int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, flo
 }
 
 int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, int row0, float inv_count,
-                         float* logits, float* loss_rows, int want_grad, cudaStream_t s) {
+                         float* logits, float* loss_rows, int want_grad, cudaStream_t s, float clip) {
   if (rows < 1 || vocab < 4 || vocab % 4 || seq < 1 || row0 < 0)
     return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: need rows >= 1, vocab %% 4 == 0, seq >= 1");
   if (!al16(logits)) return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: logits must be 16-B aligned");
-  (void)launch_k(ce_kernel, rows, kCeThreads, 0, s, logits, vocab, seq, tokens, row0, inv_count, loss_rows, want_grad,
-                                        device_error_ptr());
+  if (!(clip >= 0.f)) return set_error(GPIPE_ERR_INVALID_ARG, "cross_entropy: clip must be >= 0 (0: none)");
+  (void)launch_k(ce_kernel, rows, kCeThreads, 0, s, logits, vocab, seq, tokens, row0, inv_count, clip, loss_rows,
+                 want_grad, device_error_ptr());
   return check_launch("cross_entropy");
 }
 

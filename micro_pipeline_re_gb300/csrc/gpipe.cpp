@@ -59,7 +59,7 @@ struct StepPtrs {
 
 struct GraphKey {
   StepPtrs p;
-  int64_t opts[13];
+  int64_t opts[14];
   bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
 };
 
@@ -86,6 +86,7 @@ struct gpipe_ctx {
   bool trace = false;      // stamp the GPU clock at the end of every (cell, micro-batch, phase)
   int inflight = 0;        // with lanes: micro-batches each cell works on at once (1, 2; 0: by size)
   int schedule = 0;        // issue order: 0 GPipe (all forwards, then all backwards), 1 one-forward-one-backward
+  int64_t clip_milli = 0;  // logit clipping threshold in thousandths (0: none)
   // Two in flight when a micro-batch's FFN GEMM is small enough (tokens x d x
   // ffn <= 2^30) that its kernels are bound by latency rather than throughput.
   int inflight_eff() const {
@@ -805,7 +806,7 @@ class Executor {
                              reinterpret_cast<float*>(ws(hb.meanf)), reinterpret_cast<float*>(ws(hb.rstdf)), st()));
     TRY(gemm(T, dm.vocab, d, ws(hb.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
     TRY(launch_cross_entropy(T, dm.vocab, dm.seq, static_cast<const int32_t*>(p_.batch), m * T, inv, logits,
-                             loss_rows, 1, st()));
+                             loss_rows, 1, st(), static_cast<float>(static_cast<double>(c_->clip_milli) / 1000.0)));
     // dz (bf16, in place over the logits, leading dimension 2*vocab)
     const int64_t ldz = 2 * static_cast<int64_t>(dm.vocab);
     char* gt = ws(hb.hgt);
@@ -960,6 +961,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[10] = c->side_share;
     key.opts[11] = c->nside;
     key.opts[12] = c->schedule;
+    key.opts[13] = c->clip_milli;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -1074,6 +1076,11 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_LOGIT_CLIP:
+      if (value < 0 || value > 1000000000)
+        return c->fail(GPIPE_ERR_INVALID_ARG, "logit clip must be 0 (none) or a threshold in thousandths up to 1e9");
+      c->clip_milli = value;
+      break;
     case GPIPE_OPT_SCHEDULE:
       if (value < 0 || value > 1) return c->fail(GPIPE_ERR_INVALID_ARG, "schedule must be 0 (GPipe) or 1 (1F1B)");
       c->schedule = static_cast<int>(value);

@@ -91,7 +91,7 @@ int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const vo
                          const float* lse, float* dvec, void* dqkv, cudaStream_t stream);
 
 int launch_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, int row0, float inv_count,
-                         float* logits, float* loss_rows, int want_grad, cudaStream_t stream);
+                         float* logits, float* loss_rows, int want_grad, cudaStream_t stream, float clip = 0.f);
 int launch_mse(int rows, int d, const float* y, const float* t, float inv_count, float* loss_rows, float* dy,
                cudaStream_t stream);
 

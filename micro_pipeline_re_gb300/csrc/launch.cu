@@ -180,6 +180,12 @@ int gpipe_op_cross_entropy(int rows, int vocab, int seq, const int32_t* tokens, 
                                   static_cast<cudaStream_t>(stream));
 }
 
+int gpipe_op_cross_entropy_clip(int rows, int vocab, int seq, const int32_t* tokens, int row0, float inv_count,
+                                float clip, float* logits, float* loss_rows, int want_grad, void* stream) {
+  return gp::launch_cross_entropy(rows, vocab, seq, tokens, row0, inv_count, logits, loss_rows, want_grad,
+                                  static_cast<cudaStream_t>(stream), clip);
+}
+
 int gpipe_op_mse(int rows, int d, const float* y, const float* t, float inv_count, float* loss_rows, float* dy,
                  void* stream) {
   return gp::launch_mse(rows, d, y, t, inv_count, loss_rows, dy, static_cast<cudaStream_t>(stream));

@@ -24,6 +24,11 @@ What is computed, and where it comes from:
   cross-entropy averaged over all N(seq-1) predicted tokens.
   The FFN-only block (kind 0) is y = x + W_2 GELU(W_1 LN(x) + b_1) + b_2 with
   the MSE loss (1/(N d)) sum (y - t)^2.
+* "Training stability": logit clipping, read as clamping every logit to
+  [-c, c] before the softmax (so the loss sees the clamped logits and the
+  gradient is zero where a logit lies outside the interval).  c is the
+  workload's threshold in thousandths, v / 1000 rounded to fp32 (the value the
+  step is given); v = 0 means no clipping.
 
 All arithmetic is fp64; inputs (fp32 arrays from ``synth``) are promoted.
 """
@@ -207,13 +212,24 @@ def mse_loss(y, t, count):
     return (r * r).sum() / count, 2.0 * r / count
 
 
-def next_token_ce(z, tokens, count):
+def logit_clip_threshold(w):
+    """The clipping threshold c of workload ``w`` (0.0: none)."""
+    v = getattr(w, "logit_clip_milli", 0)
+    return float(np.float32(v / 1000.0)) if v else 0.0
+
+
+def next_token_ce(z, tokens, count, clip=0.0):
     """Next-token softmax cross-entropy over logits z [N, S, V].
 
     Position t predicts tokens[:, t+1]; the last position predicts nothing.
+    clip > 0: the loss is taken over min(max(z, -clip), clip), and dz is the
+    gradient with respect to the unclipped z (zero where |z| > clip).
     Returns (sum of per-token losses / count, dz, per-token losses [N, S-1]).
     """
     n, s, vocab = z.shape
+    raw = z
+    if clip > 0:
+        z = np.clip(z, -clip, clip)
     zp = z[:, :-1, :]
     tgt = tokens[:, 1:]
     m = zp.max(axis=-1, keepdims=True)
@@ -226,6 +242,8 @@ def next_token_ce(z, tokens, count):
     dz[:, :-1, :] = ez / se
     np.put_along_axis(dz[:, :-1, :], tgt[..., None],
                       np.take_along_axis(dz[:, :-1, :], tgt[..., None], axis=-1) - 1.0, axis=-1)
+    if clip > 0:
+        dz = np.where(np.abs(raw) <= clip, dz, 0.0)
     return per_tok.sum() / count, dz / count, per_tok
 
 
@@ -277,7 +295,7 @@ def loss_and_grads(w, params, batch, count=None):
         caches.append(c)
     hf, cf = layer_norm(xs[-1], p["lnf_g"], p["lnf_b"])
     z = hf @ emb.T
-    loss, dz, per_tok = next_token_ce(z, tok, count)
+    loss, dz, per_tok = next_token_ce(z, tok, count, clip=logit_clip_threshold(w))
     extras["per_seq_loss"] = per_tok.sum(axis=1) / (s - 1)
     _acc(grads, "emb", _wgrad(dz, hf))
     dhf = dz @ emb
@@ -317,7 +335,7 @@ def forward_loss(w, params, batch, count=None):
         x, _ = block_forward(1, p, f"l{l}.", x, w.heads)
     hf, _ = layer_norm(x, p["lnf_g"], p["lnf_b"])
     z = hf @ p["emb"].T
-    loss, _, per_tok = next_token_ce(z, tok, count)
+    loss, _, per_tok = next_token_ce(z, tok, count, clip=logit_clip_threshold(w))
     return float(loss), {"per_seq_loss": per_tok.sum(axis=1) / (s - 1)}
 
 

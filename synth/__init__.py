@@ -17,6 +17,13 @@ Random-draw recipe (fixed order, one generator per workload):
   kind 1 (causal LM):        tokens ~ U{0..V-1} [N,seq] int32
   then every parameter in packing order: matrices ~ N(0, 1/d) (variance 1/d,
   d = model width), biases and LN shifts 0 (no draw), LN gains 1 (no draw).
+  With ffn_init_depth_scaled, the FFN matrices W1 and W2 take variance
+  1/(d L) instead (the same draws times 1/sqrt(L)).
+
+Trainability options of the GPipe technical review's "Training stability"
+section (off by default): ffn_init_depth_scaled (the feed-forward layers'
+initialisation shrunk with the depth L) and logit_clip_milli (a logit
+clipping threshold in thousandths, handed to the step, not applied here).
 """
 from __future__ import annotations
 
@@ -47,6 +54,8 @@ class Workload:
     decay: float = 0.9
     eps: float = 1e-8
     seed: int = 0
+    ffn_init_depth_scaled: bool = False
+    logit_clip_milli: int = 0
 
     @property
     def tokens(self) -> int:
@@ -129,10 +138,12 @@ def make_inputs(w: Workload, params: bool = True):
         out["tokens"] = rng.integers(0, w.vocab, size=(w.n, w.seq), dtype=np.int32)
     if params:
         scale = np.float32(1.0 / np.sqrt(w.d))
+        ffn_scale = np.float32(1.0 / np.sqrt(w.d * w.L)) if w.ffn_init_depth_scaled else scale
         ps = {}
         for name, shape, init in param_specs(w):
             if init == "normal":
-                ps[name] = rng.standard_normal(shape, dtype=np.float32) * scale
+                is_ffn = name.endswith(".w1") or name.endswith(".w2")
+                ps[name] = rng.standard_normal(shape, dtype=np.float32) * (ffn_scale if is_ffn else scale)
             elif init == "ones":
                 ps[name] = np.ones(shape, dtype=np.float32)
             else:

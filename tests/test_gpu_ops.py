@@ -302,6 +302,57 @@ def test_cross_entropy(b, rows, vocab, seq, row0):
     assert rel(got_dz, want_dz) <= 8e-3
 
 
+@pytest.mark.parametrize("rows,vocab,seq,row0", [(130, 1000, 64, 0), (64, 32000, 64, 64)])
+def test_cross_entropy_logit_clipping(b, rows, vocab, seq, row0):
+    """Clipped cross-entropy against the oracle's clipped loss on the same fp32
+    logits: the pass/zero decision is taken on identical values, so the
+    zero pattern of dz matches exactly; clip 0 is the unclipped op, bit for
+    bit; a negative clip is rejected."""
+    t = __import__("torch")
+    rng = np.random.default_rng(rows + vocab + 1)
+    n_tok = row0 + rows + seq
+    n_tok += (-n_tok) % seq
+    tokens = rng.integers(0, vocab, size=n_tok).astype(np.int32)
+    z = (rng.standard_normal((rows, vocab)) * 3).astype(np.float32)
+    inv = 1.0 / 1234.0
+    clip_milli = 3000
+    c = float(np.float32(clip_milli / 1000.0))
+    outs = {}
+    for cc in (c, 0.0):
+        dz_buf = dev(z)
+        loss = t.empty(rows, dtype=t.float32, device="cuda")
+        assert b.lib().gpipe_op_cross_entropy_clip(rows, vocab, seq, dev(tokens).data_ptr(), row0, inv, cc,
+                                                   dz_buf.data_ptr(), loss.data_ptr(), 1, stream()) == 0
+        sync()
+        outs[cc] = (host(loss), dz_buf.view(t.bfloat16).view(rows, 2 * vocab)[:, :vocab].float().cpu().numpy())
+    dz_plain = dev(z)
+    loss_plain = t.empty(rows, dtype=t.float32, device="cuda")
+    assert b.lib().gpipe_op_cross_entropy(rows, vocab, seq, dev(tokens).data_ptr(), row0, inv, dz_plain.data_ptr(),
+                                          loss_plain.data_ptr(), 1, stream()) == 0
+    sync()
+    assert np.array_equal(outs[0.0][0], host(loss_plain))
+    assert np.array_equal(outs[0.0][1], dz_plain.view(t.bfloat16).view(rows, 2 * vocab)[:, :vocab].float().cpu().numpy())
+    want_loss = np.zeros(rows)
+    want_dz = np.zeros((rows, vocab))
+    for r in range(rows):
+        gidx = row0 + r
+        if gidx % seq == seq - 1:
+            continue
+        zz = z[r].astype(np.float64)[None, None, :].repeat(2, axis=1)
+        tok = np.array([[0, tokens[gidx + 1]]])
+        _, dz, per = om.next_token_ce(zz, tok, 1.0, clip=c)
+        want_loss[r] = per[0, 0] * inv
+        want_dz[r] = dz[0, 0] * inv
+    got_loss, got_dz = outs[c]
+    assert rel(got_loss, want_loss) <= 1e-5
+    assert rel(got_dz, want_dz) <= 8e-3
+    assert np.array_equal(got_dz == 0, want_dz == 0)
+    assert 0.2 < np.mean(np.abs(z) > c) < 0.5
+    assert b.lib().gpipe_op_cross_entropy_clip(rows, vocab, seq, dev(tokens).data_ptr(), row0, inv, -1.0,
+                                               dev(z).data_ptr(), t.empty(rows, device="cuda").data_ptr(), 1,
+                                               stream()) != 0
+
+
 def test_mse(b):
     t = __import__("torch")
     rng = np.random.default_rng(3)

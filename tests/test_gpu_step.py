@@ -114,6 +114,18 @@ def test_small_lm_bf16_step_matches_oracle(b):
     _lm_parity(b, w, make_inputs(w))
 
 
+def test_small_lm_trainability_options_match_oracle(b):
+    """The review's "Training stability" measures: FFN matrices initialised with
+    variance 1/(d L) and logits clipped to [-1.5, 1.5] in the cross-entropy
+    (about one logit in eight at this initialisation), in the one-forward-
+    one-backward order; the oracle applies the same clip."""
+    w = SMALL_LM.replace(ffn_init_depth_scaled=True, logit_clip_milli=1500)
+    inp = make_inputs(w)
+    ref_plain = om.forward_loss(w.replace(logit_clip_milli=0), inp["params"], inp)[0]
+    _, _, ref = _lm_parity(b, w, inp, options=[(b.OPT_SCHEDULE, 1)])
+    assert abs(ref["loss"] - ref_plain) > 1e-2 * abs(ref_plain)   # the clip is active
+
+
 def test_small_lm_uneven_partition(b):
     """Costs that force unequal cells (3 + 1 layers)."""
     w = SMALL_LM

@@ -240,6 +240,11 @@ def test_options_are_validated_and_kernel_times_start_empty(binding):
     for opt, bad in ((binding.OPT_SIDE_STREAMS, 0), (binding.OPT_SIDE_STREAMS, 5), (binding.OPT_SIDE_SHARE, 4)):
         with pytest.raises(binding.GpipeError):
             g.set_option(opt, bad)
+    for opt, bad in ((binding.OPT_LOGIT_CLIP, -1), (binding.OPT_LOGIT_CLIP, 10**9 + 1), (binding.OPT_SCHEDULE, -1)):
+        with pytest.raises(binding.GpipeError):
+            g.set_option(opt, bad)
+    g.set_option(binding.OPT_LOGIT_CLIP, 2500)
+    g.set_option(binding.OPT_LOGIT_CLIP, 0)
     g.set_option(binding.OPT_KERNEL_TIMES, binding.EPI_BIAS_GELU + 1)
     ms, fl = g.kernel_times()   # no step taken yet: nothing timed, no CUDA call made
     assert ms.size == 0 and fl.size == 0

@@ -84,8 +84,10 @@ def test_finite_differences_input_ffn():
     assert np.linalg.norm(extras["dx0"] - g) / np.linalg.norm(g) <= 1e-6
 
 
-def _torch_loss(w, params_t, batch):
-    """The same model written with torch ops; autograd supplies the gradients."""
+def _torch_loss(w, params_t, batch, want_logits=False):
+    """The same model written with torch ops; autograd supplies the gradients.
+    Logit clipping, when the workload asks for it, is torch.clamp (whose
+    gradient passes where min <= z <= max)."""
     import torch
     import torch.nn.functional as F
     p = params_t
@@ -114,6 +116,11 @@ def _torch_loss(w, params_t, batch):
         x = x + F.linear(F.gelu(F.linear(u2, p[pre + "w1"], p[pre + "b1"])), p[pre + "w2"], p[pre + "b2"])
     hf = F.layer_norm(x, (w.d,), p["lnf_g"], p["lnf_b"], eps=1e-5)
     z = hf @ p["emb"].T
+    if want_logits:
+        return z
+    if w.logit_clip_milli:
+        c = float(np.float32(w.logit_clip_milli / 1000.0))
+        z = torch.clamp(z, -c, c)
     return F.cross_entropy(z[:, :-1].reshape(-1, w.vocab), tok[:, 1:].reshape(-1), reduction="sum") / (n * (s - 1))
 
 
@@ -243,6 +250,88 @@ def test_cross_entropy_special_cases():
             z2[b, t, tok[b, t + 1]] = 20.0
     loss2, _, _ = om.next_token_ce(z2, tok, n * (s - 1))
     assert abs(loss2 - math.log1p((V - 1) * math.exp(-20.0))) < 1e-15
+
+
+def test_clipped_cross_entropy_closed_forms():
+    """Logit clipping ("Training stability"): a threshold above every logit
+    changes nothing; logits beyond it act as +-c and pass no gradient."""
+    V, n, s = 13, 2, 4
+    tok = np.array([[1, 2, 3, 4], [5, 6, 7, 8]])
+    cnt = n * (s - 1)
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((n, s, V))
+    l0, d0, p0 = om.next_token_ce(z, tok, cnt)
+    l1, d1, p1 = om.next_token_ce(z, tok, cnt, clip=float(np.abs(z).max()) + 1e-9)
+    assert l1 == l0 and np.array_equal(d1, d0) and np.array_equal(p1, p0)
+    c = 2.0
+    # every logit far outside: target at +50, the rest at -50
+    zf = np.full((n, s, V), -50.0)
+    for b in range(n):
+        for t in range(s - 1):
+            zf[b, t, tok[b, t + 1]] = 50.0
+    lf, df, _ = om.next_token_ce(zf, tok, cnt, clip=c)
+    assert abs(lf - math.log1p((V - 1) * math.exp(-2 * c))) < 1e-14
+    assert np.all(df == 0.0)
+    # target clipped at +c, the rest (0) inside: only the non-targets carry gradient
+    zm = np.zeros((n, s, V))
+    for b in range(n):
+        for t in range(s - 1):
+            zm[b, t, tok[b, t + 1]] = 50.0
+    lm_, dm_, _ = om.next_token_ce(zm, tok, cnt, clip=c)
+    assert abs(lm_ - (math.log(math.exp(c) + V - 1) - c)) < 1e-14
+    for b in range(n):
+        for t in range(s - 1):
+            row = dm_[b, t]
+            assert row[tok[b, t + 1]] == 0.0
+            others = np.delete(row, tok[b, t + 1])
+            assert np.allclose(others, 1.0 / (math.exp(c) + V - 1) / cnt, rtol=1e-14, atol=0)
+
+
+def _clip_workload(torch):
+    """TINY_LM with a clipping threshold near the median |logit| of its random
+    parameters, at least 1e-4 away from every logit (so +-1e-6 perturbations
+    never cross it)."""
+    params = _random_params(TINY_LM, 6)
+    batch = _batch(TINY_LM, 6)
+    pt = {k: torch.tensor(v, dtype=torch.float64) for k, v in params.items()}
+    z = np.abs(_torch_loss(TINY_LM, pt, batch, want_logits=True)[:, :-1].numpy()).ravel()
+    for milli in range(int(np.median(z) * 1000), int(z.max() * 1000)):
+        c = float(np.float32(milli / 1000.0))
+        if np.min(np.abs(z - c)) > 1e-4:
+            break
+    frac = np.mean(z > c)
+    assert 0.2 <= frac <= 0.6
+    return TINY_LM.replace(logit_clip_milli=milli), params, batch
+
+
+def test_logit_clipping_against_autograd_and_finite_differences():
+    torch = pytest.importorskip("torch")
+    w, params, batch = _clip_workload(torch)
+    loss, grads, _ = om.loss_and_grads(w, params, batch)
+    loss_nc, grads_nc, _ = om.loss_and_grads(TINY_LM, params, batch)
+    assert abs(loss - loss_nc) > 1e-3 * abs(loss_nc)           # the clip is active
+    pt = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in params.items()}
+    lt = _torch_loss(w, pt, batch)
+    lt.backward()
+    assert abs(lt.item() - loss) <= 1e-12 * abs(loss)
+    for k in params:
+        ref = pt[k].grad.numpy()
+        assert np.linalg.norm(grads[k] - ref) <= 1e-11 * max(np.linalg.norm(ref), 1e-300), k
+    # central differences on a few parameter groups
+    h = 1e-6
+    for name in ("emb", "lnf_g", "l1.w2", "l0.b_qkv"):
+        base = params[name]
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            orig = base[idx]
+            base[idx] = orig + h
+            lp, _ = om.forward_loss(w, params, batch)
+            base[idx] = orig - h
+            lm, _ = om.forward_loss(w, params, batch)
+            base[idx] = orig
+            g[idx] = (lp - lm) / (2 * h)
+        assert np.linalg.norm(grads[name] - g) <= 1e-6 * np.linalg.norm(g), name
+        assert np.linalg.norm(grads[name] - grads_nc[name]) > 1e-3 * np.linalg.norm(g), name
 
 
 def test_ffn_zero_weights_reduce_to_residual_and_mse():
