@@ -84,7 +84,8 @@ typedef struct {
 } gpipe_dims;
 
 /* Create a context for L layers cut into K cells and M micro-batches.
- * cost: L per-layer cost estimates c_i (>= 1), or NULL for the layer's FLOPs.
+ * cost: L per-layer cost estimates c_i (>= 1), or NULL for the layer's forward
+ * FLOPs per token: 2(4d^2 + 2d ffn) + 2d(seq+1) (kind 1), 4d ffn (kind 0).
  * Validates 1 <= K <= L, M >= 1, N % M == 0; kind 1: d % 64 == 0,
  * d/heads == 64, seq % 64 == 0, ffn % 64 == 0, vocab % 8 == 0; kind 0: d % 8 == 0,
  * ffn % 8 == 0; then partitions.
@@ -92,6 +93,15 @@ typedef struct {
  * returns this thread's last message. */
 int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims,
                  const int64_t* cost);
+
+/* The same for layers of unequal FFN width (heterogeneous layers; the review's
+ * "Limitations 3: load imbalance"): ffn is a host array of L int32 widths,
+ * each validated like dims->ffn, or NULL for dims->ffn everywhere.  With ffn
+ * given, dims->ffn is ignored.  Layer l's W1 is [ffn[l], d], b1 [ffn[l]] and W2
+ * [d, ffn[l]] in the packing, and its default cost uses ffn[l], so the
+ * partition balances the widths.  The workspace is sized for the widest. */
+int gpipe_create_layers(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims,
+                        const int32_t* ffn, const int64_t* cost);
 
 /* Cell bounds of the variance-minimising partition ("minimal interface"):
  * bounds_out[0] = 0 < bounds_out[1] < ... < bounds_out[K] = L; cell k holds
@@ -250,13 +260,30 @@ enum {
                                 still differentiates its micro-batches in ascending
                                 order, so results are identical.  Set before
                                 gpipe_sizes (it changes the workspace size).          */
-  GPIPE_OPT_LOGIT_CLIP = 16  /* [0] value v > 0: logit clipping (the review's
+  GPIPE_OPT_LOGIT_CLIP = 16, /* [0] value v > 0: logit clipping (the review's
                                 "Training stability"): the cross-entropy sees each
                                 logit clamped to [-c, c], c = v / 1000 rounded to
                                 fp32, and its gradient is zero where |z| > c.  0: no
                                 clipping.  0 <= v <= 1e9.  Only the LM (kind 1).     */
+  GPIPE_OPT_LAYER_TIMES = 17 /* [0] 1: bracket every layer's first forward and its
+                                backward of micro-batch 0 with CUDA events (read by
+                                gpipe_layer_times), to measure per-layer costs for
+                                the partition.  The durations are the layer's own
+                                work only when the step runs on one stream
+                                (GPIPE_OPT_PIPELINE 0 and GPIPE_OPT_CONCURRENT 0);
+                                otherwise they include waits for other lanes and
+                                leave out side-stream work.                          */
 };
 int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
+
+/* Per-layer durations (ms) of the last step taken with GPIPE_OPT_LAYER_TIMES:
+ * fwd_ms[l] = layer l's first forward of micro-batch 0, bwd_ms[l] = its
+ * backward of micro-batch 0 (re-computation excluded), for l < count (either
+ * array may be NULL).  Waits for the step's events.  Returns L, 0 if no such
+ * step was issued since the option was set, or a negative GPIPE_ERR_* code.
+ * Measured costs, e.g. round(1e6 (fwd_ms + bwd_ms)), can be given to
+ * gpipe_create as cost estimates (partitioning on measured times). */
+int gpipe_layer_times(gpipe_ctx* ctx, float* fwd_ms, float* bwd_ms, int count);
 
 /* Debug read-back after a step (synchronises `stream`):
  *   remat_mismatch_bytes: bytes of re-computed internals that differ from the

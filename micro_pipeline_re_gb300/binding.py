@@ -30,6 +30,7 @@ OPT_SIDE_SHARE = 13
 OPT_SIDE_STREAMS = 14
 OPT_SCHEDULE = 15
 OPT_LOGIT_CLIP = 16
+OPT_LAYER_TIMES = 17
 SCHEDULE_GPIPE, SCHEDULE_1F1B = 0, 1
 OP_FWD, OP_HEAD, OP_BWD = 0, 1, 2
 EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
@@ -52,6 +53,8 @@ _lib = None
 # name: (restype, argtypes)
 _SIGS = {
     "gpipe_create": (c_int, [POINTER(c_void_p), c_int, c_int, c_int, POINTER(Dims), POINTER(c_int64)]),
+    "gpipe_create_layers": (c_int, [POINTER(c_void_p), c_int, c_int, c_int, POINTER(Dims), POINTER(c_int32),
+                                    POINTER(c_int64)]),
     "gpipe_partition": (c_int, [c_void_p, POINTER(c_int32)]),
     "gpipe_sizes": (c_int, [c_void_p, POINTER(c_size_t), POINTER(c_size_t)]),
     "gpipe_init_params": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -62,6 +65,7 @@ _SIGS = {
                                      POINTER(c_double)]),
     "gpipe_memory_report": (c_int, [c_void_p, POINTER(c_size_t), POINTER(c_size_t)]),
     "gpipe_issue_order": (c_int, [c_void_p, POINTER(c_int32), c_int]),
+    "gpipe_layer_times": (c_int, [c_void_p, POINTER(c_float), POINTER(c_float), c_int]),
     "gpipe_set_option": (c_int, [c_void_p, c_int, c_int64]),
     "gpipe_debug_counters": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_uint64), POINTER(c_int)]),
     "gpipe_loss_rows": (c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float), c_size_t]),
@@ -146,14 +150,15 @@ class GPipe:
     """Owns one gpipe_ctx (host state only).  Names mirror the C ABI."""
 
     def __init__(self, L, K, M, *, kind, d, heads, ffn, seq, vocab, n, dtype, lr=1e-3, decay=0.9, eps=1e-8,
-                 cost=None):
+                 cost=None, ffn_layers=None):
         self.dims = Dims(kind, d, heads, ffn, seq, vocab, n, dtype, lr, decay, eps)
         self.L, self.K, self.M = L, K, M
         h = c_void_p()
         carr = None
         if cost is not None:
             carr = (c_int64 * L)(*[int(c) for c in cost])
-        rc = lib().gpipe_create(ctypes.byref(h), L, K, M, ctypes.byref(self.dims), carr)
+        farr = (c_int32 * L)(*[int(f) for f in ffn_layers]) if ffn_layers else None
+        rc = lib().gpipe_create_layers(ctypes.byref(h), L, K, M, ctypes.byref(self.dims), farr, carr)
         if rc != OK:
             raise GpipeError(rc, lib().gpipe_last_error(None).decode())
         self.h = h
@@ -162,7 +167,7 @@ class GPipe:
     def from_workload(cls, w, cost=None, K=None, M=None):
         g = cls(w.L, K or w.K, M or w.M, kind=w.kind, d=w.d, heads=w.heads, ffn=w.ffn,
                 seq=w.seq if w.kind == 1 else 1, vocab=w.vocab, n=w.n, dtype=0 if w.dtype == "f32" else 1,
-                lr=w.lr, decay=w.decay, eps=w.eps, cost=cost)
+                lr=w.lr, decay=w.decay, eps=w.eps, cost=cost, ffn_layers=tuple(getattr(w, "ffn_layers", ())))
         if getattr(w, "logit_clip_milli", 0):
             g.set_option(OPT_LOGIT_CLIP, w.logit_clip_milli)
         return g
@@ -216,6 +221,15 @@ class GPipe:
         buf = (c_int32 * (4 * n))()
         _check(min(lib().gpipe_issue_order(self.h, buf, n), 0), self.h)
         return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
+
+    def layer_times(self):
+        """(forward ms, backward ms) per layer of the last step taken with
+        OPT_LAYER_TIMES (empty arrays if none)."""
+        fw = (c_float * self.L)()
+        bw = (c_float * self.L)()
+        n = lib().gpipe_layer_times(self.h, fw, bw, self.L)
+        _check(min(n, 0), self.h)
+        return np.array(fw[:n], dtype=np.float64), np.array(bw[:n], dtype=np.float64)
 
     def memory_report(self):
         a, b = c_size_t(), c_size_t()

@@ -59,7 +59,7 @@ struct StepPtrs {
 
 struct GraphKey {
   StepPtrs p;
-  int64_t opts[14];
+  int64_t opts[15];
   bool operator==(const GraphKey& o) const { return std::memcmp(this, &o, sizeof(GraphKey)) == 0; }
 };
 
@@ -70,6 +70,7 @@ struct gpipe_ctx {
   Dims dm{};
   std::vector<int64_t> cost;
   std::vector<int32_t> bounds;
+  std::vector<int> ffn;    // per-layer FFN width (dm.ffn holds the widest, which sizes the workspace)
   int max_cell = 0;
   ParamLayout pl;
   Workspace ws;
@@ -102,6 +103,9 @@ struct gpipe_ctx {
   std::vector<double> kt_flops;
   std::vector<int32_t> kt_mnk;
   int kt_n = 0;  // timed launches issued by the last issued (or captured) step
+  bool layer_times = false;        // event pairs around every layer's forward and backward of micro-batch 0
+  std::vector<cudaEvent_t> lt_ev;  // 4 per layer: forward start/end, backward start/end
+  bool lt_valid = false;           // the last issued (or captured) step recorded them
   static constexpr int kMaxLanes = 128;
   static constexpr int kLaneEvents = 13;
   static constexpr int kSides = 4;  // most side streams per lane
@@ -263,6 +267,12 @@ class Executor {
     const int M = c_->M, K = c_->K;
     set_pdl_enabled(c_->pdl);
     c_->kt_n = 0;
+    c_->lt_valid = false;
+    if (c_->layer_times) {
+      if (c_->lt_ev.size() < static_cast<size_t>(4) * c_->L) c_->lt_ev.resize(static_cast<size_t>(4) * c_->L, nullptr);
+      for (cudaEvent_t& e : c_->lt_ev)
+        if (!e && cudaEventCreate(&e) != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "cannot create a layer event");
+    }
     std::vector<Op> ops;
     if (!issue_order(K, M, c_->schedule, w.ring, ops)) return set_error(GPIPE_ERR_INVALID_ARG, "no issue order");
     // cells busy at each tick of the order (ops of one tick can run at once)
@@ -307,6 +317,7 @@ class Executor {
     TRY(launch_sum(reinterpret_cast<float*>(ws(w.loss_rows)), c_->T(), reinterpret_cast<float*>(ws(w.misc)),
                    origin_));
     if (c_->trace) TRY(launch_stamp(stamp(1), origin_));
+    c_->lt_valid = c_->layer_times;
     return GPIPE_OK;
   }
 
@@ -400,7 +411,10 @@ class Executor {
         dx_buf = cur_buf == 0 ? 1 : 0;
         dx = lbuf(lk, dx_buf);
       }
+      const bool timed = c_->layer_times && m == 0;
+      if (timed) TRY(record_timed(c_->lt_ev[4 * (first + j) + 2]));
       TRY(layer_backward(first + j, x, slot(k, m, j), dy, cur_buf, dx, dx_buf));
+      if (timed) TRY(record_timed(c_->lt_ev[4 * (first + j) + 3]));
       dy = dx;
       cur_buf = dx_buf;
     }
@@ -670,7 +684,10 @@ class Executor {
     for (int j = 0; j < n; ++j) {
       const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
       void* out = j == n - 1 ? static_cast<void*>(stash(k + 1, m)) : static_cast<void*>(slot(k, m, j).y);
+      const bool timed = c_->layer_times && m == 0 && !recompute;
+      if (timed) TRY(record_timed(c_->lt_ev[4 * (first + j)]));
       TRY(layer_forward(first + j, x, slot(k, m, j), out, recompute && j == n - 1));
+      if (timed) TRY(record_timed(c_->lt_ev[4 * (first + j) + 1]));
     }
     if (c_->remat_check_m == m && !c_->no_remat) TRY(remat_check(k, m, n, recompute));
     return GPIPE_OK;
@@ -697,7 +714,7 @@ class Executor {
   int layer_forward(int l, const void* x, const Slot& s, void* out, bool skip_out_proj) {
     const Dims& dm = c_->dm;
     const LayerOff& o = c_->pl.layers[l];
-    const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = dm.ffn;
+    const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = c_->ffn[l];
     const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
     TRY(launch_layernorm_fwd(dt, T, d, x, p32(o.ln1_g), p32(o.ln1_b), s.u, s.mean1, s.rstd1, st()));
     const void* ffn_in = s.u;
@@ -727,7 +744,7 @@ class Executor {
     const LaneLayout& ll = c_->ws.lane;
     const int lane = cur_lane_;
     char* lb = lane_base(lane);
-    const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = dm.ffn;
+    const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = c_->ffn[l];
     const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
     float* scratch = reinterpret_cast<float*>(lb + ll.scratch);
     float* lnp0 = reinterpret_cast<float*>(lb + ll.lnp[0]);
@@ -821,6 +838,15 @@ class Executor {
   }
 };
 
+int validate_ffn(int kind, int ffn, std::string& why) {
+  if (kind == GPIPE_KIND_FFN) {
+    if (ffn < 8 || ffn % 8) return why = "kind 0 needs ffn % 8 == 0 and ffn >= 8", GPIPE_ERR_INVALID_ARG;
+  } else if (ffn < 64 || ffn % 64) {
+    return why = "ffn must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
+  }
+  return GPIPE_OK;
+}
+
 int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
   if (!dm) return why = "dims is NULL", GPIPE_ERR_INVALID_ARG;
   if (L < 1) return why = "L must be >= 1", GPIPE_ERR_INVALID_ARG;
@@ -831,8 +857,8 @@ int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
     return why = "need lr > 0, 0 <= decay < 1, eps > 0", GPIPE_ERR_INVALID_ARG;
   if (dm->kind == GPIPE_KIND_FFN) {
     if (dm->dtype != GPIPE_DTYPE_F32) return why = "the FFN-block model runs in fp32 (dtype 0)", GPIPE_ERR_UNSUPPORTED;
-    if (dm->d < 8 || dm->d % 8 || dm->d > 1024 || dm->ffn < 8 || dm->ffn % 8)
-      return why = "kind 0 needs d % 8 == 0, 8 <= d <= 1024, ffn % 8 == 0", GPIPE_ERR_INVALID_ARG;
+    if (dm->d < 8 || dm->d % 8 || dm->d > 1024)
+      return why = "kind 0 needs d % 8 == 0, 8 <= d <= 1024", GPIPE_ERR_INVALID_ARG;
     return GPIPE_OK;
   }
   if (dm->kind != GPIPE_KIND_LM) return why = "unknown kind", GPIPE_ERR_INVALID_ARG;
@@ -840,7 +866,6 @@ int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
   if (dm->d < 64 || dm->d % 64 || dm->d > 1024 || dm->heads < 1 || dm->d / dm->heads != 64 || dm->d % dm->heads)
     return why = "kind 1 needs d % 64 == 0, d <= 1024 and d/heads == 64", GPIPE_ERR_INVALID_ARG;
   if (dm->seq < 64 || dm->seq % 64) return why = "seq must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
-  if (dm->ffn < 64 || dm->ffn % 64) return why = "ffn must be a positive multiple of 64", GPIPE_ERR_INVALID_ARG;
   if (dm->vocab < 8 || dm->vocab % 8) return why = "vocab must be a positive multiple of 8", GPIPE_ERR_INVALID_ARG;
   return GPIPE_OK;
 }
@@ -850,23 +875,41 @@ int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
 extern "C" {
 
 int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims, const int64_t* cost) {
+  return gpipe_create_layers(out, L, K, M, dims, nullptr, cost);
+}
+
+int gpipe_create_layers(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims, const int32_t* ffn,
+                        const int64_t* cost) {
   if (!out) return set_error(GPIPE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   std::string why;
   int rc = validate(L, K, M, dims, why);
   if (rc) return set_error(rc, "%s", why.c_str());
+  std::vector<int> widths(L, dims->ffn);
+  if (!ffn) {
+    rc = validate_ffn(dims->kind, dims->ffn, why);
+    if (rc) return set_error(rc, "%s", why.c_str());
+  } else {
+    for (int l = 0; l < L; ++l) {
+      rc = validate_ffn(dims->kind, ffn[l], why);
+      if (rc) return set_error(rc, "layer %d: %s", l, why.c_str());
+      widths[l] = ffn[l];
+    }
+  }
   gpipe_ctx* c = new gpipe_ctx();
   c->L = L;
   c->K = K;
   c->M = M;
-  c->dm = Dims{dims->kind, dims->d, dims->heads, dims->ffn, dims->seq, dims->vocab, dims->n, dims->dtype,
-               dims->lr, dims->decay, dims->eps};
-  // default cost: the layer's forward FLOPs per token (all layers identical)
-  const int64_t d = dims->d, f = dims->ffn;
-  const int64_t default_cost =
-      dims->kind == 1 ? 2 * (4 * d * d + 2 * d * f) + 2 * d * (dims->seq + 1) : 2 * (2 * d * f);
+  c->ffn = widths;
+  c->dm = Dims{dims->kind, dims->d, dims->heads, *std::max_element(widths.begin(), widths.end()), dims->seq,
+               dims->vocab, dims->n, dims->dtype, dims->lr, dims->decay, dims->eps};
+  // default cost: the layer's forward FLOPs per token
+  const int64_t d = dims->d;
   c->cost.resize(L);
   for (int i = 0; i < L; ++i) {
+    const int64_t f = widths[i];
+    const int64_t default_cost =
+        dims->kind == 1 ? 2 * (4 * d * d + 2 * d * f) + 2 * d * (dims->seq + 1) : 2 * (2 * d * f);
     c->cost[i] = cost ? cost[i] : default_cost;
     if (c->cost[i] < 1) {
       delete c;
@@ -879,7 +922,7 @@ int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims, c
   }
   c->max_cell = 0;
   for (int k = 0; k < K; ++k) c->max_cell = std::max(c->max_cell, c->bounds[k + 1] - c->bounds[k]);
-  c->pl = make_param_layout(c->dm, L);
+  c->pl = make_param_layout(c->dm, L, c->ffn);
   c->refresh_ws();
   *out = c;
   return GPIPE_OK;
@@ -962,6 +1005,7 @@ int gpipe_step(gpipe_ctx* c, float* p32, void* p16, float* g32, float* v32, cons
     key.opts[11] = c->nside;
     key.opts[12] = c->schedule;
     key.opts[13] = c->clip_milli;
+    key.opts[14] = c->layer_times;
     if (!c->have_key || !(key == c->key)) {
       c->drop_graph();
       if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -1076,6 +1120,7 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
+    case GPIPE_OPT_LAYER_TIMES: c->layer_times = value != 0; break;
     case GPIPE_OPT_LOGIT_CLIP:
       if (value < 0 || value > 1000000000)
         return c->fail(GPIPE_ERR_INVALID_ARG, "logit clip must be 0 (none) or a threshold in thousandths up to 1e9");
@@ -1129,6 +1174,22 @@ int gpipe_kernel_times(gpipe_ctx* c, float* ms_out, double* flops_out, int32_t* 
       for (int j = 0; j < 3; ++j) mnk_out[3 * i + j] = c->kt_mnk[3 * i + j];
   }
   return n;
+}
+
+int gpipe_layer_times(gpipe_ctx* c, float* fwd_ms, float* bwd_ms, int count) {
+  if (!c || count < 0) return GPIPE_ERR_INVALID_ARG;
+  if (!c->lt_valid) return 0;
+  for (int l = 0; l < c->L && l < count; ++l) {
+    float t[2] = {0.f, 0.f};
+    for (int ph = 0; ph < 2; ++ph) {
+      cudaError_t ce = cudaEventSynchronize(c->lt_ev[4 * l + 2 * ph + 1]);
+      if (ce == cudaSuccess) ce = cudaEventElapsedTime(&t[ph], c->lt_ev[4 * l + 2 * ph], c->lt_ev[4 * l + 2 * ph + 1]);
+      if (ce != cudaSuccess) return c->fail(GPIPE_ERR_CUDA, std::string("layer times: ") + cudaGetErrorString(ce));
+    }
+    if (fwd_ms) fwd_ms[l] = t[0];
+    if (bwd_ms) bwd_ms[l] = t[1];
+  }
+  return c->L;
 }
 
 int gpipe_debug_counters(gpipe_ctx* c, void* workspace, void* stream, uint64_t* remat_mismatch, int* error_flag) {
@@ -1197,6 +1258,8 @@ void gpipe_destroy(gpipe_ctx* c) {
   for (const auto* v : {&c->ev_hdone, &c->ev_fwd, &c->ev_sfree, &c->ev_hfree})
     for (cudaEvent_t e : *v)
       if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->lt_ev)
+    if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : c->kt_ev)
     if (e) cudaEventDestroy(e);
   delete c;

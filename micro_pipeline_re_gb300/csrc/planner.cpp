@@ -197,11 +197,12 @@ double simulate_order(int K, int M, const std::vector<Op>& ops, const double* t_
   return makespan;
 }
 
-ParamLayout make_param_layout(const Dims& dm, int L) {
+ParamLayout make_param_layout(const Dims& dm, int L, const std::vector<int>& ffn) {
   ParamLayout p;
-  const size_t d = dm.d, f = dm.ffn;
+  const size_t d = dm.d;
   size_t o = 0;
   for (int l = 0; l < L; ++l) {
+    const size_t f = ffn.empty() ? static_cast<size_t>(dm.ffn) : static_cast<size_t>(ffn[l]);
     LayerOff lo{};
     if (dm.kind == 0) {
       lo.ln1_g = o; o += d;

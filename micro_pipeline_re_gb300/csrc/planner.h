@@ -67,7 +67,8 @@ struct ParamLayout {
   size_t lnf_g = 0, lnf_b = 0, emb = 0;
   size_t total = 0;
 };
-ParamLayout make_param_layout(const Dims& dm, int L);
+// ffn: per-layer FFN widths (empty: dm.ffn for every layer).
+ParamLayout make_param_layout(const Dims& dm, int L, const std::vector<int>& ffn = {});
 
 // Byte offsets of one layer's kept internals inside a slot.
 struct SlotLayout {

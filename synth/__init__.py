@@ -56,6 +56,7 @@ class Workload:
     seed: int = 0
     ffn_init_depth_scaled: bool = False
     logit_clip_milli: int = 0
+    ffn_layers: tuple = ()   # per-layer FFN widths (heterogeneous layers); empty: ffn everywhere
 
     @property
     def tokens(self) -> int:
@@ -90,6 +91,15 @@ WORKLOADS = {
 SWEEP_GRID = [(k, m) for k in (2, 4, 8) for m in (1, 4, 32)]
 
 
+def layer_ffn(w: Workload):
+    """FFN width of every layer."""
+    if w.ffn_layers:
+        if len(w.ffn_layers) != w.L:
+            raise ValueError("ffn_layers needs one width per layer")
+        return [int(f) for f in w.ffn_layers]
+    return [w.ffn] * w.L
+
+
 def param_specs(w: Workload):
     """Parameters in flat packing order: list of (name, shape, init).
 
@@ -98,9 +108,9 @@ def param_specs(w: Workload):
     The fused QKV matrix stacks the query, key and value rows in that order,
     each block d rows with heads contiguous (head h owns rows h*dh..(h+1)*dh-1).
     """
-    d, f = w.d, w.ffn
+    d = w.d
     specs = []
-    for l in range(w.L):
+    for l, f in enumerate(layer_ffn(w)):
         p = f"l{l}."
         if w.kind == KIND_FFN:
             specs += [(p + "ln_g", (d,), "ones"), (p + "ln_b", (d,), "zeros"),

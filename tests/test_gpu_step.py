@@ -126,6 +126,56 @@ def test_small_lm_trainability_options_match_oracle(b):
     assert abs(ref["loss"] - ref_plain) > 1e-2 * abs(ref_plain)   # the clip is active
 
 
+def test_heterogeneous_ffn_widths_match_oracle(b):
+    """Layers of unequal FFN width (heterogeneous cells): LM in bf16 and the FFN
+    model in fp32 against the oracle."""
+    w = SMALL_LM.replace(ffn_layers=(256, 512, 128, 384), M=4, n=8)
+    gp, _, _ = _lm_parity(b, w, make_inputs(w))
+    assert gp.partition() == [0, 2, 4]
+    wf = WORKLOADS["tiny_ffn"].replace(ffn_layers=(64, 256, 128, 192))
+    inp = make_inputs(wf)
+    _, st, p0, (loss,) = _run(b, wf, inp)
+    ref = om.step(wf, inp["params"], inp)
+    assert abs(loss - ref["loss"]) <= 1e-5 * abs(ref["loss"])
+    for name, got in b.unpack(wf, st.host(st.g32)).items():
+        assert rel(got, ref["grads"][name]) <= 1e-5, name
+
+
+def test_partition_does_not_change_the_result(b):
+    """Where the layers are cut changes where they run, not what they compute:
+    two partitions of the same heterogeneous model give identical bits."""
+    w = SMALL_LM.replace(ffn_layers=(256, 512, 128, 384), M=4, n=8)
+    inp = make_inputs(w)
+    outs = []
+    for cost in ([1, 1, 1, 1], [1, 1, 1, 5], None):
+        gp, st, _, (loss,) = _run(b, w, inp, cost=cost)
+        outs.append((gp.partition(), loss, st.host(st.g32).copy(), st.host(st.p32).copy()))
+    assert outs[0][0] == [0, 2, 4] and outs[1][0] == [0, 3, 4]
+    for o in outs[1:]:
+        assert o[1] == outs[0][1] and np.array_equal(o[2], outs[0][2]) and np.array_equal(o[3], outs[0][3])
+
+
+def test_partition_on_measured_layer_times(b):
+    """Per-layer costs measured on the GPU (events around each layer's forward
+    and backward, one stream) see the wide layers as the expensive ones; the
+    partition on those costs runs, with the same result."""
+    w = Workload("hetero_wide", KIND_LM, L=8, K=2, M=2, d=1024, heads=16, ffn=256, seq=128, vocab=1000, n=16,
+                 dtype="bf16", ffn_layers=(8192, 256, 256, 256, 8192, 256, 8192, 256))
+    inp = make_inputs(w)
+    gp, st, _, (loss,) = _run(b, w, inp, options=[(b.OPT_PIPELINE, 0), (b.OPT_CONCURRENT, 0),
+                                                  (b.OPT_LAYER_TIMES, 1)])
+    fwd, bwd = gp.layer_times()
+    assert fwd.size == w.L and np.all(fwd > 0) and np.all(bwd > 0)
+    t = fwd + bwd
+    wide = np.array(w.ffn_layers) == 8192
+    assert t[wide].min() > t[~wide].max(), t
+    cost = [int(x) for x in np.rint(t * 1e6)]
+    gm, st2, _, (loss2,) = _run(b, w, inp, cost=cost)
+    from oracle import partition as opart
+    assert gm.partition() == opart.partition(cost, w.K)[0]
+    assert loss2 == loss and np.array_equal(st2.host(st2.g32), st.host(st.g32))
+
+
 def test_small_lm_uneven_partition(b):
     """Costs that force unequal cells (3 + 1 layers)."""
     w = SMALL_LM

@@ -360,3 +360,37 @@ def test_one_f_one_b_keeps_a_shorter_stash(binding, name):
     assert peak1 <= bound1 and bound0 - bound1 == peak0 - peak1
     with pytest.raises(binding.GpipeError):
         g.set_option(binding.OPT_SCHEDULE, 2)
+
+
+def test_heterogeneous_ffn_widths_partition_and_packing(binding):
+    """Layers of unequal FFN width (the review's "Limitations 3: load
+    imbalance"): the default costs are each layer's forward FLOPs per token
+    (the documented formula, evaluated here), the partition is the exact
+    variance-minimising one for those costs, and the packing holds each layer's
+    own W1/b1/W2."""
+    from synth import KIND_LM, Workload, param_count
+    widths = (256, 2048, 512, 1024, 64, 1536, 768, 128)
+    w = Workload("hetero", KIND_LM, L=8, K=3, M=2, d=128, heads=2, ffn=64, seq=64, vocab=256, n=4, dtype="bf16",
+                 ffn_layers=widths)
+    g = binding.GPipe.from_workload(w)
+    d, s = w.d, w.seq
+    costs = [2 * (4 * d * d + 2 * d * f) + 2 * d * (s + 1) for f in widths]
+    assert g.partition() == op.partition(costs, w.K)[0]
+    assert g.sizes()[0] == param_count(w)
+    peak, bound = g.memory_report()
+    assert peak <= bound
+    # the widest layer sizes the workspace: the same as all layers at 2048
+    g_wide = binding.GPipe.from_workload(w.replace(ffn=2048, ffn_layers=()))
+    assert g.sizes()[1] == g_wide.sizes()[1]
+    # FFN model too, with explicit costs overriding the default
+    wf = Workload("hetero_ffn", 0, L=4, K=2, M=2, d=64, heads=0, ffn=8, seq=1, vocab=0, n=4, dtype="f32",
+                  ffn_layers=(64, 256, 8, 128))
+    gf = binding.GPipe.from_workload(wf)
+    assert gf.partition() == op.partition([4 * 64 * f for f in wf.ffn_layers], 2)[0]
+    assert gf.sizes()[0] == param_count(wf)
+    assert binding.GPipe.from_workload(wf, cost=[1, 1, 1, 1]).partition() == [0, 2, 4]
+    for bad in ((256, 100, 512, 64, 64, 64, 64, 64), (256, 0, 512, 64, 64, 64, 64, 64)):
+        with pytest.raises(binding.GpipeError):
+            binding.GPipe.from_workload(w.replace(ffn_layers=bad))
+    with pytest.raises(ValueError):
+        param_count(w.replace(ffn_layers=(64, 64)))

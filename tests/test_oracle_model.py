@@ -37,7 +37,8 @@ def _flat(grads, names):
     return np.concatenate([np.ravel(grads[n]) for n in names])
 
 
-@pytest.mark.parametrize("w", [TINY_LM, TINY_FFN], ids=["lm", "ffn"])
+@pytest.mark.parametrize("w", [TINY_LM, TINY_FFN, TINY_LM.replace(ffn_layers=(16, 24)),
+                               TINY_FFN.replace(ffn_layers=(8, 32))], ids=["lm", "ffn", "lm_hetero", "ffn_hetero"])
 def test_finite_differences_every_parameter(w):
     params = _random_params(w, 1)
     batch = _batch(w, 1)
@@ -125,8 +126,10 @@ def _torch_loss(w, params_t, batch, want_logits=False):
 
 
 @pytest.mark.parametrize("w", [TINY_LM, TINY_FFN,
-                               TINY_LM.replace(L=3, d=16, heads=4, ffn=24, seq=9, vocab=29, n=4)],
-                         ids=["lm", "ffn", "lm_wider"])
+                               TINY_LM.replace(L=3, d=16, heads=4, ffn=24, seq=9, vocab=29, n=4),
+                               TINY_LM.replace(L=3, d=16, heads=4, ffn=24, seq=9, vocab=29, n=4,
+                                               ffn_layers=(8, 40, 24))],
+                         ids=["lm", "ffn", "lm_wider", "lm_hetero"])
 def test_independent_autograd_library(w):
     torch = pytest.importorskip("torch")
     params = _random_params(w, 3)
