@@ -16,8 +16,8 @@ cells, no re-materialisation.
 Modules:
   model      full-batch forward / hand-written backward / RMSProp in fp64
   partition  brute-force variance-minimising contiguous partition
-  schedule   discrete-event simulation of the GPipe clock (bubble fraction)
-  memory     the review's activation-memory bound O(N + (L/K)(N/M)) in bytes
+  schedule   discrete-event simulation of the pipeline clock (bubble fraction),
+             in the GPipe order and the one-forward-one-backward order
 
 Every function here has at least one pin in ``tests/test_oracle_*.py`` that is
 independent of the oracle itself (finite differences, an independent autograd

@@ -19,12 +19,18 @@ micro-batch 1 has passed all cells", which would interleave forward and
 backward on that cell; the figure and the bubble formula
 (K-1)/(M+K-1) both describe the all-forward-then-all-backward order.)
 
+simulate_1f1b takes the same rules for the one-forward-one-backward order
+(the review's "Historical impact" section: PipeDream-2BW interleaves forward
+and backward to lower the activation peak); its warm-up reading: cell k runs
+min(M, K+1-k) forwards before its first backward.
+
 The bubble fraction is the idle share of the K cells' time between the first
 forward's start and the last backward's end.  Times are kept as exact
 rationals.
 """
 from __future__ import annotations
 
+import sys
 from fractions import Fraction
 
 
@@ -65,3 +71,64 @@ def simulate(K, M, t_f, t_b):
 def bubble_closed_form(K, M):
     """The review's bubble fraction (K-1)/(M+K-1) for equal cells."""
     return Fraction(K - 1, M + K - 1)
+
+
+def one_f_one_b_sequence(K, M, k):
+    """Cell k's operations in the one-forward-one-backward order, as
+    ("F" | "B", m): min(M, K+1-k) forwards (the head counts as the stage after
+    the last cell), then a backward and a forward in turn, backwards in
+    ascending micro-batch order, then the remaining backwards."""
+    warm = min(M, K + 1 - k)
+    seq = [("F", m) for m in range(warm)]
+    nxt = warm
+    for m in range(M):
+        seq.append(("B", m))
+        if nxt < M:
+            seq.append(("F", nxt))
+            nxt += 1
+    return seq
+
+
+def simulate_1f1b(K, M, t_f, t_b):
+    """Clock of the one-forward-one-backward order with the same rules as
+    ``simulate``: a cell runs its operations in its order, each one as soon as
+    the cell is free and its producer has finished (the forward of m on cell
+    k-1; for a backward, the backward of m on cell k+1, or for the last cell
+    the head, which takes no time and follows the last cell's forward).
+    Finish times are computed by memoised recursion over each operation's two
+    predecessors.  Returns dict(makespan, busy[K], bubble) as exact Fractions.
+    """
+    if K < 1 or M < 1:
+        raise ValueError("need K >= 1 and M >= 1")
+    tf = [Fraction(t_f)] * K if not hasattr(t_f, "__len__") else [Fraction(x) for x in t_f]
+    tb = [Fraction(t_b)] * K if not hasattr(t_b, "__len__") else [Fraction(x) for x in t_b]
+    seqs = [one_f_one_b_sequence(K, M, k) for k in range(K)]
+    prev = {}
+    for k, seq in enumerate(seqs):
+        for i, op in enumerate(seq):
+            prev[(k,) + op] = (k,) + seq[i - 1] if i else None
+    memo = {}
+
+    def finish(k, kind, m):
+        key = (k, kind, m)
+        if key in memo:
+            return memo[key]
+        start = Fraction(0)
+        p = prev[key]
+        if p is not None:
+            start = max(start, finish(*p))
+        if kind == "F":
+            if k > 0:
+                start = max(start, finish(k - 1, "F", m))
+            end = start + tf[k]
+        else:
+            start = max(start, finish(K - 1, "F", m) if k == K - 1 else finish(k + 1, "B", m))
+            end = start + tb[k]
+        memo[key] = end
+        return end
+
+    sys.setrecursionlimit(max(sys.getrecursionlimit(), 20 * K * M + 1000))
+    makespan = max(finish(k, "B", M - 1) for k in range(K))
+    busy = [M * (tf[k] + tb[k]) for k in range(K)]
+    bubble = 1 - Fraction(sum(busy)) / (K * makespan)
+    return dict(makespan=makespan, busy=busy, bubble=bubble)

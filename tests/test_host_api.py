@@ -341,6 +341,22 @@ def test_one_f_one_b_clock_equals_gpipe_for_equal_cells(binding, K, M):
     assert bub == pytest.approx(float(Fraction(K - 1, M + K - 1)), abs=1e-12)
 
 
+def test_one_f_one_b_clock_model_unequal_cells(binding):
+    """The library's clock of its one-forward-one-backward issue order against
+    the oracle's independent simulation, on random unequal cells."""
+    rng = np.random.default_rng(7)
+    for _ in range(25):
+        K, M = int(rng.integers(1, 7)), int(rng.integers(1, 12))
+        tf = [float(x) for x in rng.integers(1, 9, size=K)]
+        tb = [float(x) for x in rng.integers(1, 9, size=K)]
+        g = binding.GPipe(K, K, M, kind=0, d=64, heads=0, ffn=64, seq=1, vocab=0, n=M, dtype=0)
+        g.set_option(binding.OPT_SCHEDULE, 1)
+        mk, bub = g.schedule_model(tf, tb)
+        sim = osch.simulate_1f1b(K, M, [int(x) for x in tf], [int(x) for x in tb])
+        assert mk == pytest.approx(float(sim["makespan"]), rel=1e-12), (K, M, tf, tb)
+        assert bub == pytest.approx(float(sim["bubble"]), abs=1e-12)
+
+
 @pytest.mark.parametrize("name", ["lm_small", "lm_wide", "lm_deep"])
 def test_one_f_one_b_keeps_a_shorter_stash(binding, name):
     """The interleaved order holds min(M, K+1) micro-batches per cell boundary

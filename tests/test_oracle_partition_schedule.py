@@ -79,3 +79,25 @@ def test_simulation_unequal_cells_hand_worked():
     assert sim["makespan"] == 14
     assert sim["busy"] == [4, 12]
     assert sim["bubble"] == 1 - Fraction(16, 28)
+
+
+@pytest.mark.parametrize("K,M", [(1, 4), (4, 1), (4, 16), (8, 32), (3, 7), (5, 2)])
+@pytest.mark.parametrize("tf,tb", [(1, 2), (1, 1), (3, 5)])
+def test_one_f_one_b_clock_closed_form(K, M, tf, tb):
+    """With equal cells the interleaved order takes (M+K-1)(t_f+t_b), as GPipe
+    does: the same bubble (K-1)/(M+K-1)."""
+    sim = osch.simulate_1f1b(K, M, tf, tb)
+    assert sim["makespan"] == (M + K - 1) * (tf + tb)
+    assert sim["bubble"] == Fraction(K - 1, M + K - 1)
+
+
+def test_one_f_one_b_clock_hand_worked():
+    """K = 2, M = 3, t_f = (1, 2), t_b = (2, 3).  Cell 0: F0 F1 F2 B0 B1 B2,
+    cell 1: F0 F1 B0 F2 B1 B2.  Cell 0 forwards in [0,1] [1,2] [2,3]; cell 1:
+    F0 [1,3], F1 [3,5], B0 [5,8], F2 [8,10], B1 [10,13], B2 [13,16]; cell 0's
+    backwards wait for cell 1's: B0 [8,10], B1 [13,15], B2 [16,18].  Makespan
+    18, busy 3(1+2) + 3(2+3) = 24 of 2 x 18, bubble 1/3."""
+    assert osch.one_f_one_b_sequence(2, 3, 0) == [("F", 0), ("F", 1), ("F", 2), ("B", 0), ("B", 1), ("B", 2)]
+    assert osch.one_f_one_b_sequence(2, 3, 1) == [("F", 0), ("F", 1), ("B", 0), ("F", 2), ("B", 1), ("B", 2)]
+    sim = osch.simulate_1f1b(2, 3, [1, 2], [2, 3])
+    assert sim["makespan"] == 18 and sim["bubble"] == Fraction(1, 3)
