@@ -1120,7 +1120,10 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
     case GPIPE_OPT_PIPELINE: c->pipelined = value != 0; c->ws_stale = true; break;
     case GPIPE_OPT_PDL: c->pdl = value != 0; break;
     case GPIPE_OPT_TRACE: c->trace = value != 0; break;
-    case GPIPE_OPT_LAYER_TIMES: c->layer_times = value != 0; break;
+    case GPIPE_OPT_LAYER_TIMES:
+      c->layer_times = value != 0;
+      c->lt_valid = false;
+      break;
     case GPIPE_OPT_LOGIT_CLIP:
       if (value < 0 || value > 1000000000)
         return c->fail(GPIPE_ERR_INVALID_ARG, "logit clip must be 0 (none) or a threshold in thousandths up to 1e9");

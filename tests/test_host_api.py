@@ -248,6 +248,9 @@ def test_options_are_validated_and_kernel_times_start_empty(binding):
     g.set_option(binding.OPT_KERNEL_TIMES, binding.EPI_BIAS_GELU + 1)
     ms, fl = g.kernel_times()   # no step taken yet: nothing timed, no CUDA call made
     assert ms.size == 0 and fl.size == 0
+    g.set_option(binding.OPT_LAYER_TIMES, 1)
+    fw, bw = g.layer_times()
+    assert fw.size == 0 and bw.size == 0
     g.close()
     # the op API's SM share for gpipe_op_gemm: >= 0 (0 = the whole GPU)
     assert binding.lib().gpipe_op_gemm_set_sm_share(-1) == -1
