@@ -103,6 +103,13 @@ int gpipe_create(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims,
 int gpipe_create_layers(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* dims,
                         const int32_t* ffn, const int64_t* cost);
 
+/* Re-partition an existing context on new per-layer costs (L host int64, each
+ * >= 1), e.g. times measured with GPIPE_OPT_LAYER_TIMES: the same exact
+ * variance-minimising cut as gpipe_create.  The workspace size may change
+ * (the largest cell sizes it): query gpipe_sizes again before the next step.
+ * The parameter packing does not change.  Host only, no CUDA call. */
+int gpipe_repartition(gpipe_ctx* ctx, const int64_t* cost);
+
 /* Cell bounds of the variance-minimising partition ("minimal interface"):
  * bounds_out[0] = 0 < bounds_out[1] < ... < bounds_out[K] = L; cell k holds
  * layers [bounds_out[k], bounds_out[k+1]).  Exact integer objective

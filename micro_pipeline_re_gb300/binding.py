@@ -56,6 +56,7 @@ _SIGS = {
     "gpipe_create_layers": (c_int, [POINTER(c_void_p), c_int, c_int, c_int, POINTER(Dims), POINTER(c_int32),
                                     POINTER(c_int64)]),
     "gpipe_partition": (c_int, [c_void_p, POINTER(c_int32)]),
+    "gpipe_repartition": (c_int, [c_void_p, POINTER(c_int64)]),
     "gpipe_sizes": (c_int, [c_void_p, POINTER(c_size_t), POINTER(c_size_t)]),
     "gpipe_init_params": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
     "gpipe_step": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -188,6 +189,10 @@ class GPipe:
         out = (c_int32 * (self.K + 1))()
         _check(lib().gpipe_partition(self.h, out), self.h)
         return list(out)
+
+    def repartition(self, cost):
+        arr = (c_int64 * self.L)(*[int(c) for c in cost])
+        _check(lib().gpipe_repartition(self.h, arr), self.h)
 
     def sizes(self):
         p, w = c_size_t(), c_size_t()

@@ -928,6 +928,22 @@ int gpipe_create_layers(gpipe_ctx** out, int L, int K, int M, const gpipe_dims* 
   return GPIPE_OK;
 }
 
+int gpipe_repartition(gpipe_ctx* c, const int64_t* cost) {
+  if (!c || !cost) return GPIPE_ERR_INVALID_ARG;
+  std::vector<int64_t> costs(cost, cost + c->L);
+  for (int64_t x : costs)
+    if (x < 1) return c->fail(GPIPE_ERR_INVALID_ARG, "layer costs must be >= 1");
+  std::vector<int32_t> bounds;
+  if (!partition_min_variance(costs, c->K, bounds)) return c->fail(GPIPE_ERR_INVALID_ARG, "partition failed");
+  c->cost = costs;
+  c->bounds = bounds;
+  c->max_cell = 0;
+  for (int k = 0; k < c->K; ++k) c->max_cell = std::max(c->max_cell, bounds[k + 1] - bounds[k]);
+  c->ws_stale = true;
+  c->drop_graph();
+  return GPIPE_OK;
+}
+
 int gpipe_partition(gpipe_ctx* c, int32_t* bounds_out) {
   if (!c || !bounds_out) return GPIPE_ERR_INVALID_ARG;
   std::copy(c->bounds.begin(), c->bounds.end(), bounds_out);

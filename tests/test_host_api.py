@@ -413,3 +413,25 @@ def test_heterogeneous_ffn_widths_partition_and_packing(binding):
             binding.GPipe.from_workload(w.replace(ffn_layers=bad))
     with pytest.raises(ValueError):
         param_count(w.replace(ffn_layers=(64, 64)))
+
+
+def test_repartition_on_new_costs(binding):
+    """Re-partitioning a context on measured (here: given) costs gives the same
+    exact cut as creating it with them; the clock model follows the new cells;
+    the packing stays, the workspace follows the largest cell."""
+    rng = np.random.default_rng(13)
+    w = WORKLOADS["lm_small"]
+    g = binding.GPipe.from_workload(w)
+    P0, ws0 = g.sizes()
+    for _ in range(10):
+        cost = [int(c) for c in rng.integers(1, 10**6, size=w.L)]
+        g.repartition(cost)
+        assert g.partition() == op.partition(cost, w.K)[0]
+        fresh = binding.GPipe.from_workload(w, cost=cost)
+        assert g.sizes() == fresh.sizes() and g.sizes()[0] == P0
+        assert g.schedule_model() == fresh.schedule_model()
+    g.repartition([1] * w.L)
+    assert g.sizes() == (P0, ws0)
+    with pytest.raises(binding.GpipeError):
+        g.repartition([1] * (w.L - 1) + [0])
+    assert g.partition() == [0, 2, 4, 6, 8]
