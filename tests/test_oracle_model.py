@@ -145,7 +145,8 @@ def test_independent_autograd_library(w):
 
 
 @pytest.mark.parametrize("w,M", [(TINY_LM.replace(n=6), 3), (TINY_LM.replace(n=6), 6),
-                                 (TINY_FFN.replace(n=8), 4)])
+                                 (TINY_FFN.replace(n=8), 4),
+                                 (TINY_LM.replace(n=6, ffn_layers=(16, 40), logit_clip_milli=800), 3)])
 def test_micro_batch_sum_equals_full_batch(w, M):
     """The review's synchronous-update claim: the sum over M disjoint micro-batches
     of their gradients (each normalised by the whole mini-batch's count) is the
