@@ -1,0 +1,242 @@
+"""The step executor's ordering and memory bounds, checked on the CPU.
+
+The library's own executor (gpipe.cpp) and planner are compiled with g++
+against a stand-in CUDA runtime (tests/dryrun) that records, in host issue
+order, every stream work item with the byte ranges it reads, writes or
+accumulates into, and every event record and wait.  From that log:
+
+* bounds: every range lies inside one of the buffers passed to gpipe_step
+  (parameters, their bf16 copy, gradients, RMSProp state, batch, targets,
+  workspace of gpipe_sizes bytes);
+* races: any two accesses to overlapping bytes, one of them a write or an
+  accumulation (two accumulations too: their order fixes the fp32 result;
+  only integer atomic counts may meet unordered), are ordered by
+  happens-before: stream order plus event edges (a wait orders after the work
+  its event's last record followed).  Vector clocks over the streams decide
+  the order.
+
+This covers every issue order, in-flight count, side-stream count and lane
+arrangement without a GPU; the GPU tests check the same schedules for
+identical bits.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from synth import KIND_FFN, KIND_LM, WORKLOADS, Workload, param_count
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(ROOT, "micro_pipeline_re_gb300", "csrc")
+SOURCES = [os.path.join(CSRC, "gpipe.cpp"), os.path.join(CSRC, "planner.cpp"),
+           os.path.join(HERE, "dryrun", "dryrun.cpp")]
+HEADERS = [os.path.join(HERE, "dryrun", "cuda_runtime.h"), os.path.join(CSRC, "kernels.h"),
+           os.path.join(CSRC, "planner.h"), os.path.join(CSRC, "launch_util.cuh"),
+           os.path.join(ROOT, "include", "gpipe.h")]
+OUT = os.path.join(HERE, "dryrun", "_build", "libgpipe_dry.so")
+
+OPT = dict(KEEP_GRADS=1, GRAPH=2, NO_REMAT=3, REMAT_CHECK=4, SKIP_UPDATE=5, CONCURRENT=6, PIPELINE=7, PDL=8,
+           TRACE=9, KERNEL_TIMES=10, SM_SHARE=11, INFLIGHT=12, SIDE_SHARE=13, SIDE_STREAMS=14, SCHEDULE=15,
+           LOGIT_CLIP=16, LAYER_TIMES=17)
+
+
+@pytest.fixture(scope="module")
+def dry():
+    newest = max(os.path.getmtime(p) for p in SOURCES + HEADERS)
+    if not os.path.exists(OUT) or os.path.getmtime(OUT) < newest:
+        os.makedirs(os.path.dirname(OUT), exist_ok=True)
+        subprocess.run(["g++", "-std=c++17", "-O1", "-shared", "-fPIC", "-I", os.path.join(HERE, "dryrun"),
+                        "-I", CSRC] + SOURCES + ["-Wl,--no-undefined", "-o", OUT + ".tmp"], check=True)
+        os.replace(OUT + ".tmp", OUT)
+    lib = ctypes.CDLL(OUT)
+    from micro_pipeline_re_gb300.binding import Dims
+    c_int, c_vp, c_sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    lib.gpipe_create_layers.argtypes = [ctypes.POINTER(c_vp), c_int, c_int, c_int, ctypes.POINTER(Dims),
+                                        ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]
+    lib.gpipe_set_option.argtypes = [c_vp, c_int, ctypes.c_int64]
+    lib.gpipe_sizes.argtypes = [c_vp, ctypes.POINTER(c_sz), ctypes.POINTER(c_sz)]
+    lib.gpipe_step.argtypes = [c_vp] * 9 + [ctypes.POINTER(ctypes.c_float)]
+    lib.gpipe_destroy.argtypes = [c_vp]
+    lib.gpipe_last_error.argtypes = [c_vp]
+    lib.gpipe_last_error.restype = ctypes.c_char_p
+    lib.dry_entry.argtypes = [c_int] + [ctypes.POINTER(c_int)] * 4 + [ctypes.c_char_p, c_int]
+    lib.dry_access.argtypes = [c_int, c_int, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64),
+                               ctypes.c_char_p]
+    lib.Dims = Dims
+    return lib
+
+
+def _log(lib):
+    entries = []
+    t, s, e, n = (ctypes.c_int() for _ in range(4))
+    name = ctypes.create_string_buffer(64)
+    lo, hi = ctypes.c_uint64(), ctypes.c_uint64()
+    mode = ctypes.create_string_buffer(2)
+    for i in range(lib.dry_entries()):
+        assert lib.dry_entry(i, t, s, e, n, name, 64) == 0
+        acc = []
+        for j in range(n.value):
+            assert lib.dry_access(i, j, lo, hi, mode) == 0
+            acc.append((lo.value, hi.value, mode.value.decode()))
+        entries.append((t.value, s.value, e.value, name.value.decode(), acc))
+    return entries
+
+
+def run_step(lib, w, options=(), K=None, M=None):
+    """Create a context, take one dry step; returns (log, buffers)."""
+    K, M = K or w.K, M or w.M
+    dims = lib.Dims(w.kind, w.d, w.heads, w.ffn, w.seq if w.kind == KIND_LM else 1, w.vocab, w.n,
+                    0 if w.dtype == "f32" else 1, w.lr, w.decay, w.eps)
+    h = ctypes.c_void_p()
+    widths = (ctypes.c_int32 * w.L)(*w.ffn_layers) if w.ffn_layers else None
+    rc = lib.gpipe_create_layers(ctypes.byref(h), w.L, K, M, ctypes.byref(dims), widths, None)
+    assert rc == 0, lib.gpipe_last_error(None)
+    try:
+        for opt, val in options:
+            assert lib.gpipe_set_option(h, OPT[opt], val) == 0, (opt, val)
+        P, ws = ctypes.c_size_t(), ctypes.c_size_t()
+        assert lib.gpipe_sizes(h, ctypes.byref(P), ctypes.byref(ws)) == 0
+        assert P.value == param_count(w)
+        sizes = {"p32": P.value * 4, "p16": P.value * 2, "g32": P.value * 4, "v32": P.value * 4,
+                 "batch": w.n * (w.seq * 4 if w.kind == KIND_LM else w.d * 4),
+                 "targets": w.n * w.d * 4 if w.kind == KIND_FFN else 0, "ws": ws.value}
+        bufs, at = {}, 1 << 40
+        for k, v in sizes.items():
+            bufs[k] = (at, at + v)
+            at += (v + (1 << 20)) & ~0xFFFF  # a gap after every buffer
+        lib.dry_reset()
+        ptr = lambda k: ctypes.c_void_p(bufs[k][0]) if sizes[k] else None
+        rc = lib.gpipe_step(h, ptr("p32"), ptr("p16") if w.dtype == "bf16" else None, ptr("g32"), ptr("v32"),
+                            ptr("batch"), ptr("targets"), ptr("ws"), None, None)
+        assert rc == 0, lib.gpipe_last_error(h)
+        return _log(lib), bufs
+    finally:
+        lib.gpipe_destroy(h)
+
+
+def check_bounds(log, bufs):
+    spans = sorted(v for v in bufs.values() if v[1] > v[0])
+    for _, _, _, name, acc in log:
+        for lo, hi, mode in acc:
+            if hi == lo:
+                continue
+            assert any(a <= lo and hi <= b for a, b in spans), (name, hex(lo), hi - lo, mode)
+
+
+def check_races(log):
+    """Returns the number of work items; raises on an unordered conflict."""
+    dense = {s: i for i, s in enumerate(sorted({e[1] for e in log}))}
+    log = [(t, dense[s], e, n, a) for t, s, e, n, a in log]
+    nstreams = len(dense)
+    vc = np.zeros((nstreams, nstreams), dtype=np.int64)   # per stream: its vector clock
+    ev = {}
+    op_stream, op_vc, op_name = [], [], []
+    lo_l, hi_l, md_l, cnt_l, op_l = [], [], [], [], []
+    for typ, s, e, name, acc in log:
+        if typ == 0:
+            vc[s, s] += 1
+            k = len(op_stream)
+            op_stream.append(s)
+            op_vc.append(vc[s].copy())
+            op_name.append(name)
+            for lo, hi, mode in acc:
+                if hi > lo:
+                    lo_l.append(lo), hi_l.append(hi), md_l.append(mode != "R"), cnt_l.append(mode == "I")
+                    op_l.append(k)
+        elif typ == 1:
+            ev[e] = vc[s].copy()
+        elif e in ev:
+            np.maximum(vc[s], ev[e], out=vc[s])
+    op_stream = np.array(op_stream)
+    op_vc = np.array(op_vc)
+    lo, hi = np.array(lo_l, dtype=np.uint64), np.array(hi_l, dtype=np.uint64)
+    wr, cnt, op = np.array(md_l), np.array(cnt_l), np.array(op_l)
+    own = op_vc[np.arange(len(op_stream)), op_stream]     # each op's own clock component
+    for j in range(len(lo)):
+        i = np.arange(j)
+        cand = i[(op[i] != op[j]) & (lo[i] < hi[j]) & (lo[j] < hi[i]) & (wr[i] | wr[j]) & ~(cnt[i] & cnt[j])]
+        if cand.size == 0:
+            continue
+        a = op[cand]
+        ordered = own[a] <= op_vc[op[j], op_stream[a]]
+        if not np.all(ordered):
+            bad = a[~ordered][0]
+            raise AssertionError(f"unordered conflict: {op_name[bad]} (stream {op_stream[bad]}) and "
+                                 f"{op_name[op[j]]} (stream {op_stream[op[j]]}) on [{hex(int(lo[j]))}, +{int(hi[j] - lo[j])})")
+    return len(op_stream)
+
+
+SMALL = Workload("dry_lm", KIND_LM, L=4, K=2, M=4, d=128, heads=2, ffn=256, seq=64, vocab=512, n=8, dtype="bf16")
+FFN = WORKLOADS["tiny_ffn"]
+
+CASES = [
+    ("lm", SMALL, []),
+    ("lm_1f1b", SMALL, [("SCHEDULE", 1)]),
+    ("lm_k4_m8_1f1b", SMALL.replace(K=4, M=8, n=16), [("SCHEDULE", 1)]),
+    ("lm_k4_m8", SMALL.replace(K=4, M=8, n=16), []),
+    ("lm_inflight2", SMALL.replace(K=4, M=8, n=16), [("INFLIGHT", 2)]),
+    ("lm_inflight3_1f1b", SMALL.replace(K=4, M=8, n=16), [("INFLIGHT", 3), ("SCHEDULE", 1)]),
+    ("lm_inflight4_sides4", SMALL.replace(K=4, M=8, n=16), [("INFLIGHT", 4), ("SIDE_STREAMS", 4)]),
+    ("lm_inflight2_1f1b_sides1", SMALL.replace(K=4, M=8, n=16), [("INFLIGHT", 2), ("SCHEDULE", 1),
+                                                                 ("SIDE_STREAMS", 1)]),
+    ("lm_not_concurrent", SMALL.replace(K=4, M=8, n=16), [("CONCURRENT", 0), ("INFLIGHT", 1)]),
+    ("lm_not_concurrent_inflight2", SMALL.replace(K=4, M=8, n=16), [("CONCURRENT", 0), ("INFLIGHT", 2)]),
+    ("lm_one_lane", SMALL.replace(K=4, M=8, n=16), [("PIPELINE", 0)]),
+    ("lm_one_lane_1f1b", SMALL.replace(K=4, M=8, n=16), [("PIPELINE", 0), ("SCHEDULE", 1)]),
+    ("lm_one_stream", SMALL.replace(K=4, M=8, n=16), [("PIPELINE", 0), ("CONCURRENT", 0)]),
+    ("lm_direct", SMALL.replace(K=4, M=8, n=16), [("GRAPH", 0), ("SCHEDULE", 1)]),
+    ("lm_no_remat", SMALL.replace(K=4, M=8, n=16), [("NO_REMAT", 1), ("SCHEDULE", 1)]),
+    ("lm_remat_check", SMALL.replace(K=4, M=8, n=16), [("REMAT_CHECK", 5), ("SCHEDULE", 1)]),
+    ("lm_trace_times", SMALL.replace(K=4, M=8, n=16), [("TRACE", 1), ("KERNEL_TIMES", 4), ("LAYER_TIMES", 1)]),
+    ("lm_k_eq_l", SMALL.replace(K=4, M=6, n=12), [("SCHEDULE", 1), ("INFLIGHT", 2)]),
+    ("lm_k1", SMALL.replace(K=1, M=3, n=6), [("SCHEDULE", 1)]),
+    ("lm_m1", SMALL.replace(M=1, n=2), [("SCHEDULE", 1)]),
+    ("lm_hetero", SMALL.replace(L=6, K=3, M=8, n=16, ffn_layers=(256, 64, 512, 128, 192, 320)),
+     [("SCHEDULE", 1), ("INFLIGHT", 2)]),
+    ("ffn", FFN, []),
+    ("ffn_1f1b", FFN, [("SCHEDULE", 1)]),
+    ("ffn_1f1b_inflight2", FFN.replace(M=8), [("SCHEDULE", 1), ("INFLIGHT", 2)]),
+    ("ffn_not_concurrent", FFN, [("CONCURRENT", 0), ("SCHEDULE", 1)]),
+]
+
+
+@pytest.mark.parametrize("name,w,options", CASES, ids=[c[0] for c in CASES])
+def test_executor_stays_in_bounds_and_orders_every_conflict(dry, name, w, options):
+    log, bufs = run_step(dry, w, options)
+    check_bounds(log, bufs)
+    n = check_races(log)
+    assert n > 10 * w.L
+
+
+@pytest.mark.parametrize("sched", [0, 1])
+def test_lm_small_full_size_orders_every_conflict(dry, sched):
+    w = WORKLOADS["lm_small"]
+    log, bufs = run_step(dry, w, [("SCHEDULE", sched)])
+    check_bounds(log, bufs)
+    assert check_races(log) > 3000
+
+
+def test_checker_catches_a_missing_order(dry):
+    """The checker itself: the same log with one event wait dropped (the wait
+    that orders the last cell's backward after the head's gradient of
+    micro-batch 0) reports an unordered conflict."""
+    w = SMALL
+    log, bufs = run_step(dry, w)
+    check_races(log)
+    # the first wait on a cell lane issued after the first cross_entropy
+    ce = next(i for i, e in enumerate(log) if e[3] == "cross_entropy")
+    rec_events = {e[2] for e in log[:ce + 60] if e[0] == 1}
+    dropped = False
+    for i in range(ce, len(log)):
+        typ, s, e, name, _ = log[i]
+        if typ == 2 and e in rec_events and s != log[ce][1]:
+            trial = log[:i] + log[i + 1:]
+            try:
+                check_races(trial)
+            except AssertionError:
+                dropped = True
+                break
+    assert dropped
