@@ -220,9 +220,10 @@ def test_lm_small_full_size_orders_every_conflict(dry, sched):
 
 
 def test_checker_catches_a_missing_order(dry):
-    """The checker itself: the same log with one event wait dropped (the wait
-    that orders the last cell's backward after the head's gradient of
-    micro-batch 0) reports an unordered conflict."""
+    """The checker itself: dropping from the log a cross-stream event wait
+    issued after the first head (the first one whose loss matters) leaves a
+    conflicting pair unordered, and the checker reports it; with every wait
+    dropped it reports one too."""
     w = SMALL
     log, bufs = run_step(dry, w)
     check_races(log)
@@ -240,3 +241,5 @@ def test_checker_catches_a_missing_order(dry):
                 dropped = True
                 break
     assert dropped
+    with pytest.raises(AssertionError):
+        check_races([e for e in log if e[0] != 2])
