@@ -271,7 +271,8 @@ enum {
                                 "Training stability"): the cross-entropy sees each
                                 logit clamped to [-c, c], c = v / 1000 rounded to
                                 fp32, and its gradient is zero where |z| > c.  0: no
-                                clipping.  0 <= v <= 1e9.  Only the LM (kind 1).     */
+                                clipping.  0 <= v <= 1e9.  The FFN model (kind 0,
+                                MSE loss) has no logits and ignores it.              */
   GPIPE_OPT_LAYER_TIMES = 17 /* [0] 1: bracket every layer's first forward and its
                                 backward of micro-batch 0 with CUDA events (read by
                                 gpipe_layer_times), to measure per-layer costs for
