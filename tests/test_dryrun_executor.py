@@ -169,6 +169,45 @@ def check_races(log):
     return len(op_stream)
 
 
+def accumulation_order(log, bufs, w, M):
+    """Per gradient tensor (byte range in the gradient buffer), the sequence of
+    (kernel, micro-batch) that accumulate into it, in issue order (which is
+    their happens-before order: check_races has shown they are ordered).  A
+    kernel's micro-batch follows the data: the kernels that read a micro-batch's
+    own inputs (its tokens or rows, its targets) carry its index, and any other
+    kernel carries the largest index among the last writers of what it reads."""
+    check_races(log)
+    tmb = w.tokens // M
+    b0, b1 = bufs["batch"]
+    t0, t1 = bufs["targets"]
+    g0, g1 = bufs["g32"]
+    row_bytes = 4 if w.kind == KIND_LM else 4 * w.d
+    wlo, whi, wtag = [], [], []
+    order = {}
+    for typ, s, e, name, acc in log:
+        if typ != 0:
+            continue
+        tag = -1
+        for lo, hi, mode in acc:
+            if mode != "R" or hi <= lo:
+                continue
+            if b0 <= lo < b1:
+                tag = max(tag, (lo - b0) // row_bytes // tmb)
+            elif t0 <= lo < t1:
+                tag = max(tag, (lo - t0) // (4 * w.d) // tmb)
+            elif wlo:
+                L_, H_ = np.array(wlo, dtype=np.uint64), np.array(whi, dtype=np.uint64)
+                hit = np.nonzero((L_ < hi) & (lo < H_))[0]
+                if hit.size:
+                    tag = max(tag, wtag[hit[-1]])
+        for lo, hi, mode in acc:
+            if mode in "WA" and hi > lo:
+                wlo.append(lo), whi.append(hi), wtag.append(tag)
+                if mode == "A" and g0 <= lo and hi <= g1:
+                    order.setdefault((lo - g0, hi - g0), []).append((name, tag))
+    return order
+
+
 SMALL = Workload("dry_lm", KIND_LM, L=4, K=2, M=4, d=128, heads=2, ffn=256, seq=64, vocab=512, n=8, dtype="bf16")
 FFN = WORKLOADS["tiny_ffn"]
 
@@ -243,3 +282,29 @@ def test_checker_catches_a_missing_order(dry):
     assert dropped
     with pytest.raises(AssertionError):
         check_races([e for e in log if e[0] != 2])
+
+
+@pytest.mark.parametrize("w", [SMALL.replace(K=4, M=8, n=16), FFN.replace(M=8),
+                               SMALL.replace(L=6, K=3, M=8, n=16, ffn_layers=(256, 64, 512, 128, 192, 320))],
+                         ids=["lm", "ffn", "lm_hetero"])
+def test_every_gradient_accumulates_in_micro_batch_order_in_every_schedule(dry, w):
+    """The reason every schedule gives identical bits: for every parameter
+    tensor the same kernels add into its fp32 gradient in the same order,
+    micro-batch by micro-batch (0, 1, ..., M-1), whatever the issue order,
+    lanes, side streams or graph."""
+    configs = [[], [("SCHEDULE", 1)], [("INFLIGHT", 2)], [("INFLIGHT", 3), ("SCHEDULE", 1)],
+               [("INFLIGHT", 4), ("SIDE_STREAMS", 4)], [("PIPELINE", 0)], [("PIPELINE", 0), ("CONCURRENT", 0)],
+               [("GRAPH", 0), ("SCHEDULE", 1), ("INFLIGHT", 2)], [("CONCURRENT", 0), ("SIDE_STREAMS", 1)]]
+    ref = None
+    for opts in configs:
+        log, bufs = run_step(dry, w, opts)
+        order = accumulation_order(log, bufs, w, w.M)
+        for rng_, seq in order.items():
+            ms = [m for name, m in seq if name != "embedding_bwd"]
+            assert ms == sorted(ms) and ms[0] == 0 and ms[-1] == w.M - 1, (opts, rng_, seq)
+        if ref is None:
+            ref = order
+            n_params = len(order)
+        else:
+            assert order == ref, opts
+    assert n_params >= 4 * w.L
