@@ -291,13 +291,14 @@ def test_every_gradient_accumulates_in_micro_batch_order_in_every_schedule(dry, 
     """The reason every schedule gives identical bits: for every parameter
     tensor the same kernels add into its fp32 gradient in the same order,
     micro-batch by micro-batch (0, 1, ..., M-1), whatever the issue order,
-    lanes, side streams or graph."""
+    lanes, side streams, graph or number of cells (K = 1 and K = L too)."""
     configs = [[], [("SCHEDULE", 1)], [("INFLIGHT", 2)], [("INFLIGHT", 3), ("SCHEDULE", 1)],
                [("INFLIGHT", 4), ("SIDE_STREAMS", 4)], [("PIPELINE", 0)], [("PIPELINE", 0), ("CONCURRENT", 0)],
                [("GRAPH", 0), ("SCHEDULE", 1), ("INFLIGHT", 2)], [("CONCURRENT", 0), ("SIDE_STREAMS", 1)]]
     ref = None
-    for opts in configs:
-        log, bufs = run_step(dry, w, opts)
+    cells = [(w.K, opts) for opts in configs] + [(1, []), (w.L, [("SCHEDULE", 1)]), (w.L, [("INFLIGHT", 2)])]
+    for K, opts in cells:
+        log, bufs = run_step(dry, w, opts, K=K)
         order = accumulation_order(log, bufs, w, w.M)
         for rng_, seq in order.items():
             ms = [m for name, m in seq if name != "embedding_bwd"]

@@ -143,14 +143,16 @@ def test_heterogeneous_ffn_widths_match_oracle(b):
 
 def test_partition_does_not_change_the_result(b):
     """Where the layers are cut changes where they run, not what they compute:
-    two partitions of the same heterogeneous model give identical bits."""
+    partitions of the same heterogeneous model into 2 cells two ways, into one
+    cell and into one cell per layer give identical bits."""
     w = SMALL_LM.replace(ffn_layers=(256, 512, 128, 384), M=4, n=8)
     inp = make_inputs(w)
     outs = []
-    for cost in ([1, 1, 1, 1], [1, 1, 1, 5], None):
-        gp, st, _, (loss,) = _run(b, w, inp, cost=cost)
+    for cost, K in (([1, 1, 1, 1], None), ([1, 1, 1, 5], None), (None, None), (None, 1), (None, 4)):
+        gp, st, _, (loss,) = _run(b, w, inp, cost=cost, K=K)
         outs.append((gp.partition(), loss, st.host(st.g32).copy(), st.host(st.p32).copy()))
     assert outs[0][0] == [0, 2, 4] and outs[1][0] == [0, 3, 4]
+    assert outs[3][0] == [0, 4] and outs[4][0] == [0, 1, 2, 3, 4]
     for o in outs[1:]:
         assert o[1] == outs[0][1] and np.array_equal(o[2], outs[0][2]) and np.array_equal(o[3], outs[0][3])
 
