@@ -43,8 +43,8 @@ OPT = dict(KEEP_GRADS=1, GRAPH=2, NO_REMAT=3, REMAT_CHECK=4, SKIP_UPDATE=5, CONC
            LOGIT_CLIP=16, LAYER_TIMES=17)
 
 
-@pytest.fixture(scope="module")
-def dry():
+def load_dry():
+    """Build (when a source is newer) and load the dry-run library."""
     newest = max(os.path.getmtime(p) for p in SOURCES + HEADERS)
     if not os.path.exists(OUT) or os.path.getmtime(OUT) < newest:
         os.makedirs(os.path.dirname(OUT), exist_ok=True)
@@ -67,6 +67,11 @@ def dry():
                                ctypes.c_char_p]
     lib.Dims = Dims
     return lib
+
+
+@pytest.fixture(scope="module")
+def dry():
+    return load_dry()
 
 
 def _log(lib):
@@ -309,3 +314,36 @@ def test_every_gradient_accumulates_in_micro_batch_order_in_every_schedule(dry, 
         else:
             assert order == ref, opts
     assert n_params >= 4 * w.L
+
+
+def touched_bytes(log, lo0, hi0):
+    """Bytes of [lo0, hi0) that at least one work item of the log touches."""
+    iv = sorted((max(lo, lo0), min(hi, hi0)) for _, _, _, _, acc in log for lo, hi, _ in acc if lo < hi0 and hi > lo0)
+    total, cur_lo, cur_hi = 0, None, None
+    for lo, hi in iv:
+        if cur_hi is None or lo > cur_hi:
+            if cur_hi is not None:
+                total += cur_hi - cur_lo
+            cur_lo, cur_hi = lo, hi
+        else:
+            cur_hi = max(cur_hi, hi)
+    return total + (cur_hi - cur_lo if cur_hi is not None else 0)
+
+
+@pytest.mark.parametrize("name", ["lm_small", "lm_wide"])
+@pytest.mark.parametrize("sched", [0, 1])
+def test_workspace_the_step_touches_matches_the_plan(dry, name, sched):
+    """The activation memory the step actually uses (the union of the byte
+    ranges its kernels touch in the workspace) against the planner's peak and
+    the review's bound: used <= planned <= bound, and the plan holds no more
+    than alignment and a few unused slot fields beyond what is used."""
+    from micro_pipeline_re_gb300 import binding as b
+    w = WORKLOADS[name]
+    log, bufs = run_step(dry, w, [("SCHEDULE", sched)])
+    check_bounds(log, bufs)
+    g = b.GPipe.from_workload(w)
+    g.set_option(b.OPT_SCHEDULE, sched)
+    peak, bound = g.memory_report()
+    used = touched_bytes(log, bufs["ws"][0], bufs["ws"][0] + peak)
+    assert used <= peak <= bound
+    assert used >= 0.97 * peak, used / peak
