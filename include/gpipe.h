@@ -60,7 +60,9 @@ enum {
   GPIPE_ERR_CUDA = -3,            /* a CUDA runtime/driver call failed                 */
   GPIPE_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait gave up (error flag)   */
   GPIPE_ERR_NONFINITE_LOSS = -5,  /* the step's loss is NaN or Inf                     */
-  GPIPE_ERR_UNSUPPORTED = -6      /* valid request this build does not implement       */
+  GPIPE_ERR_UNSUPPORTED = -6,     /* valid request this build does not implement       */
+  GPIPE_ERR_IO = -7               /* a checkpoint file cannot be read or written, is
+                                     corrupt, or belongs to another model            */
 };
 
 enum { GPIPE_KIND_FFN = 0, GPIPE_KIND_LM = 1 };
@@ -292,6 +294,23 @@ int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
  * Measured costs, e.g. round(1e6 (fwd_ms + bwd_ms)), can be given to
  * gpipe_create as cost estimates (partitioning on measured times). */
 int gpipe_layer_times(gpipe_ctx* ctx, float* fwd_ms, float* bwd_ms, int count);
+
+/* Checkpoints of the training state between steps (host buffers, no CUDA
+ * call; the review leaves checkpointing to later systems).  The state is the
+ * fp32 master weights and the RMSProp state, P floats each in the packing
+ * order (the gradient buffer is zero after every update), plus a step count
+ * chosen by the caller; with the bf16 copy re-derived by gpipe_init_params, a
+ * run resumed from it takes exactly the steps an uninterrupted run would.
+ * write: to path (via path.tmp, then renamed), with the model's shape
+ *        fingerprint (kind, L, d, heads, seq, vocab, dtype, every layer's FFN
+ *        width) and a checksum of the payload.
+ * read:  checks magic, version, parameter count, shape fingerprint, length and
+ *        checksum before it writes params_fp32 / rms_v_fp32 / step_out (any
+ *        failure leaves them untouched and returns GPIPE_ERR_IO).          */
+int gpipe_checkpoint_write(const gpipe_ctx* ctx, const char* path, const float* params_fp32,
+                           const float* rms_v_fp32, uint64_t step);
+int gpipe_checkpoint_read(const gpipe_ctx* ctx, const char* path, float* params_fp32,
+                          float* rms_v_fp32, uint64_t* step_out);
 
 /* Debug read-back after a step (synchronises `stream`):
  *   remat_mismatch_bytes: bytes of re-computed internals that differ from the

@@ -13,7 +13,7 @@ LIB = os.path.join(PKG, "libgpipe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CUDA_SOURCES = ["gemm_tc.cu", "gemm_persistent.cu", "gemm_simt.cu", "attention.cu", "elementwise.cu", "launch.cu"]
-CXX_SOURCES = ["planner.cpp", "gpipe.cpp"]
+CXX_SOURCES = ["planner.cpp", "gpipe.cpp", "checkpoint.cpp"]
 
 
 def _nvcc() -> str:

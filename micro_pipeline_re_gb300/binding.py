@@ -18,7 +18,7 @@ from ._build import LIB
 
 OK = 0
 ERR = {-1: "INVALID_ARG", -2: "NOT_PARTITIONED", -3: "CUDA", -4: "DEVICE_TIMEOUT", -5: "NONFINITE_LOSS",
-       -6: "UNSUPPORTED"}
+       -6: "UNSUPPORTED", -7: "IO"}
 
 OPT_KEEP_GRADS, OPT_GRAPH, OPT_NO_REMAT, OPT_REMAT_CHECK, OPT_SKIP_UPDATE, OPT_CONCURRENT, OPT_PIPELINE, OPT_PDL = \
     1, 2, 3, 4, 5, 6, 7, 8
@@ -57,6 +57,8 @@ _SIGS = {
                                     POINTER(c_int64)]),
     "gpipe_partition": (c_int, [c_void_p, POINTER(c_int32)]),
     "gpipe_repartition": (c_int, [c_void_p, POINTER(c_int64)]),
+    "gpipe_checkpoint_write": (c_int, [c_void_p, ctypes.c_char_p, c_void_p, c_void_p, c_uint64]),
+    "gpipe_checkpoint_read": (c_int, [c_void_p, ctypes.c_char_p, c_void_p, c_void_p, POINTER(c_uint64)]),
     "gpipe_sizes": (c_int, [c_void_p, POINTER(c_size_t), POINTER(c_size_t)]),
     "gpipe_init_params": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p]),
     "gpipe_step": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -189,6 +191,23 @@ class GPipe:
         out = (c_int32 * (self.K + 1))()
         _check(lib().gpipe_partition(self.h, out), self.h)
         return list(out)
+
+    def checkpoint_write(self, path, params, rms_v, step):
+        """Write host float32 arrays (P each, packing order) and a step count."""
+        p = np.ascontiguousarray(params, dtype=np.float32)
+        v = np.ascontiguousarray(rms_v, dtype=np.float32)
+        _check(lib().gpipe_checkpoint_write(self.h, os.fsencode(path), p.ctypes.data, v.ctypes.data, int(step)),
+               self.h)
+
+    def checkpoint_read(self, path):
+        """(params, rms_v, step) from a checkpoint of this model (host arrays)."""
+        P, _ = self.sizes()
+        p = np.empty(P, dtype=np.float32)
+        v = np.empty(P, dtype=np.float32)
+        step = c_uint64()
+        _check(lib().gpipe_checkpoint_read(self.h, os.fsencode(path), p.ctypes.data, v.ctypes.data,
+                                           ctypes.byref(step)), self.h)
+        return p, v, step.value
 
     def repartition(self, cost):
         arr = (c_int64 * self.L)(*[int(c) for c in cost])
@@ -336,3 +355,18 @@ class DeviceState:
 
     def host(self, t):
         return t.detach().float().cpu().numpy() if t is not None else None
+
+    def save(self, path, step):
+        """Checkpoint the state between steps (weights and RMSProp state)."""
+        self.torch.cuda.synchronize()
+        self.gp.checkpoint_write(path, self.host(self.p32), self.host(self.v32), step)
+
+    def load(self, path):
+        """Restore a checkpoint of this model: weights, RMSProp state and the
+        bf16 copy; the gradient buffer is zeroed.  Returns the step count."""
+        p, v, step = self.gp.checkpoint_read(path)
+        self.p32.copy_(self.torch.from_numpy(p))
+        self.v32.copy_(self.torch.from_numpy(v))
+        self.g32.zero_()
+        self.gp.init_params(self.p32, self.p16, self.stream)
+        return step

@@ -39,6 +39,7 @@
 #include <vector>
 
 #include "../../include/gpipe.h"
+#include "context_info.h"
 #include "kernels.h"
 #include "launch_util.cuh"
 #include "planner.h"
@@ -871,6 +872,19 @@ int validate(int L, int K, int M, const gpipe_dims* dm, std::string& why) {
 }
 
 }  // namespace
+
+namespace gp {
+
+void describe_context(const gpipe_ctx* c, Dims* dm, int* L, std::vector<int>* ffn, size_t* params) {
+  *dm = c->dm;
+  *L = c->L;
+  *ffn = c->ffn;
+  *params = c->pl.total;
+}
+
+int context_fail(gpipe_ctx* c, int code, const char* msg) { return c->fail(code, msg); }
+
+}  // namespace gp
 
 extern "C" {
 

@@ -178,6 +178,31 @@ def test_partition_on_measured_layer_times(b):
     assert loss2 == loss and np.array_equal(st2.host(st2.g32), st.host(st.g32))
 
 
+def test_checkpoint_resume_is_bit_identical(b):
+    """Two steps straight, or one step, a checkpoint, a fresh context (in the
+    other issue order) with buffers restored from it, and the second step:
+    identical losses, weights and RMSProp state."""
+    import os
+    import torch
+    w = SMALL_LM
+    inp = make_inputs(w)
+    _, st, _, losses = _run(b, w, inp, steps=2, keep_grads=False)
+    p_ref, v_ref = st.host(st.p32).copy(), st.host(st.v32).copy()
+    _, st1, _, (l1,) = _run(b, w, inp, steps=1, keep_grads=False)
+    tmp = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_tmp")
+    os.makedirs(tmp, exist_ok=True)
+    path = os.path.join(tmp, "resume.ck")
+    st1.save(path, 1)
+    gp2 = b.GPipe.from_workload(w)
+    gp2.set_option(b.OPT_SCHEDULE, 1)
+    st2 = b.DeviceState(gp2, w, inp)
+    assert st2.load(path) == 1
+    l2 = st2.step()
+    torch.cuda.synchronize()
+    assert l1 == losses[0] and l2 == losses[1]
+    assert np.array_equal(st2.host(st2.p32), p_ref) and np.array_equal(st2.host(st2.v32), v_ref)
+
+
 def test_small_lm_uneven_partition(b):
     """Costs that force unequal cells (3 + 1 layers)."""
     w = SMALL_LM
