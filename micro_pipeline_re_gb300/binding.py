@@ -368,5 +368,6 @@ class DeviceState:
         self.p32.copy_(self.torch.from_numpy(p))
         self.v32.copy_(self.torch.from_numpy(v))
         self.g32.zero_()
+        self.torch.cuda.synchronize()   # the copies ran on torch's current stream, the cast runs on ours
         self.gp.init_params(self.p32, self.p16, self.stream)
         return step
