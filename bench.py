@@ -165,7 +165,23 @@ def cfg(w, args):
             "seq_len": w.seq, "vocab": w.vocab, "global_batch": w.n * max(args.gpus, 1),
             "parallelism": "replicas" if args.gpus > 1 else "single-gpu (all K cells on one GPU)",
             "l2": "working set larger than L2 (parameters, gradients and RMSProp state alone exceed 129 MB)",
-            "schedule": getattr(args, "schedule", "gpipe")}
+            "schedule": getattr(args, "schedule", "gpipe"), **({"options": dict(parse_opts(args.opt))}
+                                                             if getattr(args, "opt", None) else {})}
+
+
+def parse_opts(opts):
+    """--opt NAME=VALUE pairs (NAME: a GPIPE_OPT_* suffix, e.g. INFLIGHT=1)."""
+    out = []
+    for o in opts or []:
+        name, _, val = o.partition("=")
+        out.append((name.strip().upper(), int(val)))
+    return out
+
+
+def apply_options(b, gp, args):
+    gp.set_option(b.OPT_SCHEDULE, SCHEDULES[args.schedule])
+    for name, val in parse_opts(getattr(args, "opt", None)):
+        gp.set_option(getattr(b, "OPT_" + name), val)
 
 
 # issue orders of the step (GPIPE_OPT_SCHEDULE): the review's GPipe order, or
@@ -335,7 +351,7 @@ def run_ours(args, w):
     peaks = load_peaks()
     inp = make_inputs(w)
     gp = b.GPipe.from_workload(w)
-    gp.set_option(b.OPT_SCHEDULE, SCHEDULES[args.schedule])
+    apply_options(b, gp, args)
     st = b.DeviceState(gp, w, inp)
     stream = st.stream
     for _ in range(args.warmup):
@@ -430,7 +446,7 @@ def run_sweep(args):
     for K, M in SWEEP_GRID:
         w = w0.replace(K=K, M=M)
         gp = b.GPipe.from_workload(w)
-        gp.set_option(b.OPT_SCHEDULE, SCHEDULES[args.schedule])
+        apply_options(b, gp, args)
         free0 = torch.cuda.mem_get_info()[0]
         st = b.DeviceState(gp, w, inp)
         free1 = torch.cuda.mem_get_info()[0]
@@ -477,6 +493,8 @@ def main():
     ap.add_argument("--reps", type=int, default=100)
     ap.add_argument("--schedule", default="gpipe", choices=sorted(SCHEDULES),
                     help="issue order: gpipe (all forwards, then all backwards) or 1f1b (interleaved, shorter stash)")
+    ap.add_argument("--opt", action="append", default=[], metavar="NAME=VALUE",
+                    help="a library option for the step, e.g. --opt INFLIGHT=1 --opt PIPELINE=0 (repeatable)")
     ap.add_argument("--sweep", action="store_true",
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
     args = ap.parse_args()
