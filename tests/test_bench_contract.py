@@ -37,3 +37,11 @@ def test_reference_arm_prints_the_contract_line():
 def test_reference_arm_other_ranks_exit_quietly():
     r = _run(["--impl", "reference", "--workload", "tiny_ffn", "--steps", "1", "--warmup", "1"], {"RANK": "1"})
     assert r.returncode == 0 and not r.stdout.strip()
+
+
+def test_library_options_are_named_in_the_config():
+    r = _run(["--impl", "reference", "--workload", "tiny_ffn", "--steps", "1", "--warmup", "1",
+              "--opt", "inflight=1", "--opt", "PIPELINE=0", "--schedule", "1f1b"])
+    assert r.returncode == 0, r.stderr
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    assert d["config"]["options"] == {"INFLIGHT": 1, "PIPELINE": 0} and d["config"]["schedule"] == "1f1b"
