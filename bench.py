@@ -41,15 +41,17 @@ def model_flops(w):
 
 def recompute_flops(w, bounds):
     """FLOPs the re-materialisation adds: every cell's forward again, except
-    the output projection of each cell's last layer; plus the head forward."""
-    d, f, S, V = w.d, w.ffn, w.seq, w.vocab
+    the output projection of each cell's last layer (its result is the
+    stashed cell output).  The head is not re-computed: it runs once per
+    micro-batch, loss and gradient together."""
+    d, f, S = w.d, w.ffn, w.seq
     layer = 2 * (4 * d * d + 2 * d * f) + 2 * 2 * d * (S + 1) / 2
     out_proj = 2 * d * f
     tot = 0.0
     for k in range(len(bounds) - 1):
         n = bounds[k + 1] - bounds[k]
         tot += n * layer - out_proj
-    return (tot + 2 * d * V) * w.tokens
+    return tot * w.tokens
 
 
 def load_peaks():

@@ -201,7 +201,8 @@ int launch_gemm(const GemmDesc& g, cudaStream_t s) {
   if (g.resid) a.push_back(mat(g.resid, g.M, g.N, g.ldr, es, 'R'));
   if (g.C2) a.push_back(mat(g.C2, g.M, g.N, g.ldc, es, 'W'));
   if (g.aux) a.push_back(mat(g.aux, g.M, g.N, g.ldaux, es, 'R'));
-  work(s, "gemm", a);
+  const std::string name = "gemm:" + std::to_string(g.M) + ":" + std::to_string(g.N) + ":" + std::to_string(g.K);
+  work(s, name.c_str(), a);
   return 0;
 }
 

@@ -347,3 +347,28 @@ def test_workspace_the_step_touches_matches_the_plan(dry, name, sched):
     used = touched_bytes(log, bufs["ws"][0], bufs["ws"][0] + peak)
     assert used <= peak <= bound
     assert used >= 0.97 * peak, used / peak
+
+
+@pytest.mark.parametrize("name", ["lm_small", "lm_wide"])
+@pytest.mark.parametrize("remat", [True, False])
+def test_flop_accounting_matches_the_launched_gemms(dry, name, remat):
+    """The benchmark's FLOP model (MFU counts 3 F_fwd T, HFU adds the
+    re-computation) against the GEMMs the step actually launches: the sum of
+    2 M N K over every GEMM equals the model's GEMM part (all but attention,
+    2 d (seq+1) per token and layer in each of forward, backward x2 and
+    re-computation)."""
+    import bench
+    w = WORKLOADS[name]
+    opts = [] if remat else [("NO_REMAT", 1)]
+    log, _ = run_step(dry, w, opts)
+    launched = 0
+    for typ, _, _, nm, _ in log:
+        if typ == 0 and nm.startswith("gemm:"):
+            M, N, K = (int(x) for x in nm.split(":")[1:])
+            launched += 2 * M * N * K
+    bounds = [k * (w.L // w.K) for k in range(w.K + 1)]
+    attn_per_pass = 2 * w.d * (w.seq + 1) * w.L * w.tokens
+    want = bench.model_flops(w) - 3 * attn_per_pass
+    if remat:
+        want += bench.recompute_flops(w, bounds) - attn_per_pass
+    assert launched == pytest.approx(want, rel=1e-12)
