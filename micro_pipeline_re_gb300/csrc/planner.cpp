@@ -317,13 +317,16 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.stash_bytes = Tmb * d * es;
   w.stash = take(static_cast<size_t>(K + 1) * w.depth * w.stash_bytes);
   w.dx0 = take(dm.kind == 1 ? static_cast<size_t>(M) * w.stash_bytes : 0);
-  w.ring = w.inflight > 2 ? w.inflight : 2;
+  // the gradient ring: as deep as the micro-batches in flight (at least 2, so
+  // a cell can hand over m+1 while its neighbour still reads m), never deeper
+  // than the micro-batches there are
+  w.ring = std::min(std::max(w.inflight, 2), M);
   w.bgrad = take(static_cast<size_t>(K) * w.ring * w.stash_bytes);
   w.lanes = take(static_cast<size_t>(w.nlanes) * ln.bytes);
   w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
   w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
   w.hdy = take(static_cast<size_t>(w.depth) * w.stash_bytes);
-  w.nheads = dm.kind == 1 && w.nlanes > 1 ? 2 : 1;
+  w.nheads = dm.kind == 1 && w.nlanes > 1 && M > 1 ? 2 : 1;  // a second head lane needs a second micro-batch
   for (int h = 0; h < w.nheads && dm.kind == 1; ++h) {
     Workspace::Head& hb = w.head[h];
     hb.hf = take(Tmb * d * es);

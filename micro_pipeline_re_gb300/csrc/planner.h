@@ -93,7 +93,7 @@ struct Workspace {
   int depth = 1;                            // stash ring depth (micro-batch m in slot m mod depth)
   size_t dx0 = 0;                           // M x [Tmb, d]: gradient w.r.t. the embedding output (kind 1)
   size_t bgrad = 0;                         // K x ring x [Tmb, d]: gradient w.r.t. cell k's input
-  int ring = 2;                             // depth of that ring: max(2, micro-batches in flight per cell)
+  int ring = 2;                             // depth of that ring: max(2, in flight per cell), at most M
   size_t lanes = 0;                         // nlanes x lane
   int nlanes = 1;                           // K x inflight when the cells are pipelined, else 1
   int inflight = 1;                         // micro-batches a cell works on at once (its lanes)
@@ -107,7 +107,7 @@ struct Workspace {
     size_t hlnp[2] = {0, 0};                // LayerNorm-backward partials, alternating
   };
   Head head[2]{};
-  int nheads = 1;                           // head lanes: 2 (alternate micro-batches) when pipelined
+  int nheads = 1;                           // head lanes: 2 (alternate micro-batches) when pipelined and M > 1
   size_t lnp_bytes = 0;                     // ceil(Tmb / 8) x 2d fp32
   size_t hdy = 0;                           // depth x [Tmb, d]: gradient of the last cell's output per micro-batch
   size_t scratch_bytes = 0;

@@ -238,6 +238,10 @@ CASES = [
     ("lm_k_eq_l", SMALL.replace(K=4, M=6, n=12), [("SCHEDULE", 1), ("INFLIGHT", 2)]),
     ("lm_k1", SMALL.replace(K=1, M=3, n=6), [("SCHEDULE", 1)]),
     ("lm_m1", SMALL.replace(M=1, n=2), [("SCHEDULE", 1)]),
+    ("lm_m1_gpipe_inflight2", SMALL.replace(K=4, M=1, n=2), [("INFLIGHT", 2)]),
+    ("lm_m2_inflight4", SMALL.replace(K=4, M=2, n=4), [("INFLIGHT", 4)]),
+    ("lm_m3_inflight4_1f1b", SMALL.replace(K=4, M=3, n=6), [("INFLIGHT", 4), ("SCHEDULE", 1)]),
+    ("ffn_m1", FFN.replace(M=1), []),
     ("lm_hetero", SMALL.replace(L=6, K=3, M=8, n=16, ffn_layers=(256, 64, 512, 128, 192, 320)),
      [("SCHEDULE", 1), ("INFLIGHT", 2)]),
     ("ffn", FFN, []),
@@ -372,3 +376,31 @@ def test_flop_accounting_matches_the_launched_gemms(dry, name, remat):
     if remat:
         want += bench.recompute_flops(w, bounds) - attn_per_pass
     assert launched == pytest.approx(want, rel=1e-12)
+
+
+def test_measured_activation_bytes_scale_as_the_review_bound_over_the_sweep_grid(dry):
+    """The review's O(N + (L/K)(N/M)) with the bytes the step actually touches
+    (dry run) over the micro-batch sweep grid: a (K+2) N + b L (N/M) + c K (N/M)
+    + e H (N/M) (K lanes of one cell's internals and gradients, H head lanes
+    of one micro-batch's logits: two when there are two micro-batches to
+    alternate) fits every point within 10%, and every point is within its
+    bound."""
+    from micro_pipeline_re_gb300 import binding as b
+    from synth import SWEEP_GRID
+    w0 = WORKLOADS["lm_sweep"]
+    rows, ys = [], []
+    for K, M in SWEEP_GRID:
+        w = w0.replace(K=K, M=M)
+        log, bufs = run_step(dry, w)
+        g = b.GPipe.from_workload(w)
+        peak, bound = g.memory_report()
+        used = touched_bytes(log, bufs["ws"][0], bufs["ws"][0] + peak)
+        assert used <= peak <= bound
+        T = w.tokens
+        rows.append([(K + 2) * T, w.L * T / M, K * T / M, (2 if M > 1 else 1) * T / M])
+        ys.append(used)
+    A, y = np.array(rows, dtype=float), np.array(ys, dtype=float)
+    coef, *_ = np.linalg.lstsq(A, y, rcond=None)
+    resid = np.abs(A @ coef - y) / y
+    assert resid.max() <= 0.10, resid
+    assert np.all(coef > 0)

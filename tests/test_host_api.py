@@ -175,7 +175,9 @@ def test_memory_scales_as_review_bound_over_sweep_grid(binding, pipelined):
     review's O(N + (L/K)(N/M)) per accelerator: boundary tensors a (K+2) N,
     plus per lane (L/K)(N/M) kept internals and (N/M) gradient buffers.  One
     lane (cells in turn): a (K+2)N + b (L/K)(N/M) + c (N/M); K concurrent
-    lanes: a (K+2)N + b L (N/M) + c K (N/M)."""
+    lanes: a (K+2)N + b L (N/M) + c K (N/M) + e H (N/M), with H head lanes
+    (two when there are two micro-batches to alternate, each holding one
+    micro-batch's logits)."""
     w = WORKLOADS["lm_sweep"]
     rows, ys = [], []
     for K, M in SWEEP_GRID:
@@ -183,7 +185,10 @@ def test_memory_scales_as_review_bound_over_sweep_grid(binding, pipelined):
         assert peak <= bound
         T = w.tokens
         lanes = K if pipelined else 1
-        rows.append([(K + 2) * T, lanes * (w.L / K) * T / M, lanes * T / M])
+        row = [(K + 2) * T, lanes * (w.L / K) * T / M, lanes * T / M]
+        if pipelined:
+            row.append((2 if M > 1 else 1) * T / M)
+        rows.append(row)
         ys.append(peak)
     A, y = np.array(rows, dtype=float), np.array(ys, dtype=float)
     coef, *_ = np.linalg.lstsq(A, y, rcond=None)
