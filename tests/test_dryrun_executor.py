@@ -48,9 +48,10 @@ def load_dry():
     newest = max(os.path.getmtime(p) for p in SOURCES + HEADERS)
     if not os.path.exists(OUT) or os.path.getmtime(OUT) < newest:
         os.makedirs(os.path.dirname(OUT), exist_ok=True)
+        tmp = "%s.%d.tmp" % (OUT, os.getpid())   # concurrent test processes each build their own
         subprocess.run(["g++", "-std=c++17", "-O1", "-shared", "-fPIC", "-I", os.path.join(HERE, "dryrun"),
-                        "-I", CSRC] + SOURCES + ["-Wl,--no-undefined", "-o", OUT + ".tmp"], check=True)
-        os.replace(OUT + ".tmp", OUT)
+                        "-I", CSRC] + SOURCES + ["-Wl,--no-undefined", "-o", tmp], check=True)
+        os.replace(tmp, OUT)
     lib = ctypes.CDLL(OUT)
     from micro_pipeline_re_gb300.binding import Dims
     c_int, c_vp, c_sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
