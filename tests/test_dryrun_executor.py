@@ -405,3 +405,39 @@ def test_measured_activation_bytes_scale_as_the_review_bound_over_the_sweep_grid
     resid = np.abs(A @ coef - y) / y
     assert resid.max() <= 0.10, resid
     assert np.all(coef > 0)
+
+
+def critical_path(log):
+    """Length, in work items, of the longest chain through stream order and
+    event edges: the number of kernels that must run one after another."""
+    last_on, ev, pending, best = {}, {}, {}, 0
+    for typ, s, e, _, _ in log:
+        if typ == 0:
+            d = max(last_on.get(s, 0), pending.pop(s, 0)) + 1
+            last_on[s] = d
+            best = max(best, d)
+        elif typ == 1:
+            ev[e] = max(last_on.get(s, 0), pending.get(s, 0))
+        elif e in ev:
+            pending[s] = max(pending.get(s, 0), ev[e])
+    return best
+
+
+def test_lanes_shorten_the_critical_path(dry):
+    """What the lanes buy on a latency-bound step (`lm_small`, ≈ 3500
+    kernels): the chain of kernels that must run one after another is the
+    whole step on one stream, shorter with side streams, far shorter with the
+    cells as lanes, and shorter again with two micro-batches in flight per
+    cell; the interleaved order lengthens it (a lane's forward waits behind its
+    backward)."""
+    w = WORKLOADS["lm_small"]
+    cp = {}
+    for key, opts in (("one_stream", [("PIPELINE", 0), ("CONCURRENT", 0)]), ("one_lane", [("PIPELINE", 0)]),
+                      ("lanes", [("INFLIGHT", 1)]), ("lanes_s2", [("INFLIGHT", 2)]),
+                      ("lanes_s2_1f1b", [("INFLIGHT", 2), ("SCHEDULE", 1)])):
+        log, _ = run_step(dry, w, opts)
+        cp[key] = critical_path(log)
+        if key == "one_stream":
+            assert cp[key] == sum(1 for e in log if e[0] == 0)
+    assert cp["one_stream"] > cp["one_lane"] > 3 * cp["lanes"]
+    assert cp["lanes_s2"] < cp["lanes"] and cp["lanes_s2"] < cp["lanes_s2_1f1b"]
