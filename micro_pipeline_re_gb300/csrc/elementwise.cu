@@ -743,8 +743,9 @@ int launch_mse(int rows, int d, const float* y, const float* t, float inv_count,
 
 int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb, void* x,
                          cudaStream_t s) {
-  if (rows < 1 || d < 8 || d % 8 || !al16(emb) || !al16(x))
-    return set_error(GPIPE_ERR_INVALID_ARG, "embedding_fwd: need d %% 8 == 0 and 16-B aligned rows");
+  if (rows < 1 || d < 8 || d % 8 || vocab < 1 || !al16(emb) || !al16(x))
+    return set_error(GPIPE_ERR_INVALID_ARG,
+                     "embedding_fwd: need rows >= 1, d %% 8 == 0, vocab >= 1 and 16-B aligned rows");
   const int64_t n = (int64_t)rows * (d / 8);
   (void)launch_k(embed_fwd_kernel, blocks_for(n, 256), 256, 0, s, rows, d, vocab, tokens,
                                                       static_cast<const __nv_bfloat16*>(emb),
@@ -755,7 +756,8 @@ int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, cons
 int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx, float* demb,
                          cudaStream_t s) {
   if (rows < 1 || d < 8 || d % 8 || vocab < 1 || !al16(dx) || !al16(demb))
-    return set_error(GPIPE_ERR_INVALID_ARG, "embedding_bwd: need d %% 8 == 0 and 16-B aligned rows");
+    return set_error(GPIPE_ERR_INVALID_ARG,
+                     "embedding_bwd: need rows >= 1, d %% 8 == 0, vocab >= 1 and 16-B aligned rows");
   int ctas = 4 * num_sms();
   const int vpc = (vocab + ctas - 1) / ctas;
   ctas = (vocab + vpc - 1) / vpc;

@@ -440,3 +440,30 @@ def test_repartition_on_new_costs(binding):
     with pytest.raises(binding.GpipeError):
         g.repartition([1] * (w.L - 1) + [0])
     assert g.partition() == [0, 2, 4, 6, 8]
+
+
+def test_ops_reject_invalid_arguments_before_any_launch(binding):
+    """Every per-kernel entry point checks its shapes and alignment on the host
+    and returns GPIPE_ERR_INVALID_ARG with a message naming the operation,
+    before any CUDA call (these run without a GPU).  16 stands for an aligned
+    address and is never dereferenced; 8 for a misaligned one."""
+    lib = binding.lib()
+    A, U = 16, 8
+    cases = [
+        ("layernorm", lambda: lib.gpipe_op_layernorm_fwd(1, 4, 12, A, A, A, A, A, A, None)),
+        ("layernorm_bwd", lambda: lib.gpipe_op_layernorm_bwd(1, 0, 64, A, A, A, A, A, None, A, A, A, A, None)),
+        ("attention", lambda: lib.gpipe_op_attention_fwd(1, 100, 1, A, A, A, None)),
+        ("attention", lambda: lib.gpipe_op_attention_bwd(1, 64, 0, A, A, A, A, A, A, None)),
+        ("cross_entropy", lambda: lib.gpipe_op_cross_entropy(4, 10, 64, A, 0, 1.0, A, A, 1, None)),
+        ("cross_entropy", lambda: lib.gpipe_op_cross_entropy(4, 16, 64, A, 0, 1.0, U, A, 1, None)),
+        ("cross_entropy", lambda: lib.gpipe_op_cross_entropy_clip(4, 16, 64, A, 0, 1.0, -1.0, A, A, 1, None)),
+        ("cross_entropy", lambda: lib.gpipe_op_cross_entropy_clip(4, 16, 64, A, 0, 1.0, float("nan"), A, A, 1,
+                                                                  None)),
+        ("mse", lambda: lib.gpipe_op_mse(0, 8, A, A, 1.0, A, A, None)),
+        ("embedding_fwd", lambda: lib.gpipe_op_embedding_fwd(4, 16, 0, A, A, A, None)),
+        ("embedding_fwd", lambda: lib.gpipe_op_embedding_fwd(4, 12, 10, A, A, A, None)),
+        ("embedding_bwd", lambda: lib.gpipe_op_embedding_bwd(4, 16, 10, A, U, A, None)),
+    ]
+    for what, call in cases:
+        assert call() == -1, what
+        assert what.encode() in lib.gpipe_last_error(None), (what, lib.gpipe_last_error(None))
