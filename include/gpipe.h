@@ -172,7 +172,8 @@ int gpipe_schedule_model(const gpipe_ctx* ctx, const double* t_f, const double* 
                          double* makespan, double* bubble);
 
 /* The order in which gpipe_step issues its operations (host only, no CUDA
- * call): (2K+1) M operations, written as int32 quadruples (kind, k, m, tick)
+ * call; the review's "Pipeline flow" order, or the interleaved order of
+ * GPIPE_OPT_SCHEDULE 1): (2K+1) M operations, written as int32 quadruples (kind, k, m, tick)
  * into ops_out (room for `count` of them; ops_out may be NULL when count is
  * 0).  kind 0 = forward of cell k for micro-batch m (the embedding first when
  * k = 0), 1 = the head of micro-batch m (k = 0), 2 = backward of cell k with
@@ -296,7 +297,8 @@ int gpipe_set_option(gpipe_ctx* ctx, int option, int64_t value);
 int gpipe_layer_times(gpipe_ctx* ctx, float* fwd_ms, float* bwd_ms, int count);
 
 /* Checkpoints of the training state between steps (host buffers, no CUDA
- * call; the review leaves checkpointing to later systems).  The state is the
+ * call).  The review's "Limitations 6" notes that GPipe itself has no fault
+ * tolerance and that later systems recover through checkpoints.  The state is the
  * fp32 master weights and the RMSProp state, P floats each in the packing
  * order (the gradient buffer is zero after every update), plus a step count
  * chosen by the caller; with the bf16 copy re-derived by gpipe_init_params, a

@@ -1,6 +1,7 @@
 // Checkpoint files of the training state: the fp32 master weights and the
-// RMSProp state, in the parameter packing order, and a step count.  The pages
-// leave checkpointing to later systems; GPipe's synchronous step makes a
+// RMSProp state, in the parameter packing order, and a step count.  The GPipe
+// technical review ("Limitations 6") notes that GPipe has no fault tolerance
+// and that later systems recover through checkpoints; its synchronous step makes a
 // resumed run identical to an uninterrupted one, since the state between
 // steps is exactly (w, v) (the gradient buffer is zero after each update).
 //
