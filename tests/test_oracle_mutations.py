@@ -94,7 +94,7 @@ def rmsprop_decay_swapped(params, grads, v, lr, decay, eps):
     return _orig_rmsprop(params, grads, v, lr, 1.0 - decay, eps)
 
 
-def partition_sum_not_squares(costs, K):
+def partition_min_largest_cell(costs, K):
     """Minimises the largest cell instead of the variance."""
     from itertools import combinations
     L = len(costs)
@@ -107,13 +107,20 @@ def partition_sum_not_squares(costs, K):
     return best_b, best
 
 
-def one_f_one_b_short_warmup(K, M, k):
-    return _orig_sequence(K + 1, M, k + 2) if k + 2 <= K else _orig_sequence(K, M, k)
+def one_f_one_b_warmup_without_head(K, M, k):
+    """The warm-up as if the last cell were the last stage (min(M, K-k)
+    forwards), forgetting the head."""
+    warm = min(M, K - k)
+    seq = [("F", m) for m in range(warm)]
+    for m in range(M):
+        seq.append(("B", m))
+        if warm + m < M:
+            seq.append(("F", warm + m))
+    return seq
 
 
 _orig_ce = om.next_token_ce
 _orig_rmsprop = om.rmsprop
-_orig_sequence = osch.one_f_one_b_sequence
 
 
 def block_backward_no_residual(kind, p, pre, x, cache, dy, grads):
@@ -168,9 +175,9 @@ CASES = [
     ("RMSProp eps inside the square root", om, "rmsprop", rmsprop_eps_inside, tm.test_rmsprop_first_step_closed_form),
     ("RMSProp decay and (1-decay) swapped", om, "rmsprop", rmsprop_decay_swapped,
      tm.test_rmsprop_first_step_closed_form),
-    ("partition minimises the largest cell", opart, "partition", partition_sum_not_squares,
+    ("partition minimises the largest cell", opart, "partition", partition_min_largest_cell,
      tps.test_partition_hand_worked_cases),
-    ("one-forward-one-backward warm-up too short", osch, "one_f_one_b_sequence", one_f_one_b_short_warmup,
+    ("one-forward-one-backward warm-up too short", osch, "one_f_one_b_sequence", one_f_one_b_warmup_without_head,
      tps.test_one_f_one_b_clock_hand_worked),
     ("GPipe clock without the all-forwards barrier", osch, "simulate", simulate_backward_without_forward_barrier,
      tps.test_simulation_unequal_cells_hand_worked),
