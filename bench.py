@@ -180,6 +180,14 @@ def parse_opts(opts):
     return out
 
 
+def gp_opt(args, name, default):
+    """The value given to library option NAME on the command line, else default."""
+    for n, v in parse_opts(getattr(args, "opt", None)):
+        if n == name:
+            return v
+    return default
+
+
 def apply_options(b, gp, args):
     gp.set_option(b.OPT_SCHEDULE, SCHEDULES[args.schedule])
     for name, val in parse_opts(getattr(args, "opt", None)):
@@ -269,10 +277,50 @@ def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
             "timing": f"CUDA events around a graph of {reps} back-to-back launches of this GEMM alone"}
 
 
-# The kernel class the roofline reports: the GEMMs with the bf16 store
-# epilogue (epilogue 0: the forward projections and the input gradients) take
-# the largest share of kernel time in the step's launch list.
-ROOF_EPI = 0
+def attention_roofline(b, peaks, nseq, seq, heads, reps=50):
+    """Time the causal-attention forward and backward alone (CUDA events
+    around a graph of `reps` back-to-back launches) at one micro-batch's shape.
+    Algorithmic work per (sequence, head): forward 4 * 64 * seq(seq+1)/2 flops
+    (S = QK^T and O = PV over the visible pairs), backward 2.5x that
+    (S re-computed, dP, dV, dQ, dK)."""
+    import torch
+    D, R = heads * 64, nseq * seq
+    qkv = (torch.randn(R, 3 * D, device="cuda") * 0.5).to(torch.bfloat16)
+    dout = torch.randn(R, D, device="cuda").to(torch.bfloat16)
+    o = torch.empty(R, D, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(R, heads, device="cuda")
+    dvec = torch.empty(R, heads, device="cuda")
+    dqkv = torch.empty(R, 3 * D, device="cuda", dtype=torch.bfloat16)
+    lib = b.lib()
+    out = {}
+    pairs = nseq * heads * seq * (seq + 1) / 2
+    for name, flops, fn in (
+            ("forward", 4.0 * 64 * pairs, lambda st: lib.gpipe_op_attention_fwd(
+                nseq, seq, heads, qkv.data_ptr(), o.data_ptr(), lse.data_ptr(), st)),
+            ("backward", 10.0 * 64 * pairs, lambda st: lib.gpipe_op_attention_bwd(
+                nseq, seq, heads, qkv.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(), dvec.data_ptr(),
+                dqkv.data_ptr(), st))):
+        st = torch.cuda.current_stream().cuda_stream
+        for _ in range(3):
+            assert fn(st) == 0
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn(torch.cuda.current_stream().cuda_stream)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        dt = e0.elapsed_time(e1) / 1e3 / reps
+        out[name] = {"us": dt * 1e6, "tflops": flops / dt / 1e12, "frac": flops / dt / 1e12 / peaks["bf16"]}
+    return {"kernel": f"causal attention nseq={nseq} seq={seq} heads={heads}", **out,
+            "peak": peaks["bf16"], "peak_source": peaks["source"] + " (burst)"}
+
+
 EPI_NAMES = {0: "bf16 store epilogue (bias / residual)", 1: "bias + GELU epilogue", 2: "GELU-backward epilogue",
              3: "fp32 TMA reduce-add epilogue (weight gradient, bias gradient)", 4: "fp32 store epilogue"}
 
@@ -287,34 +335,100 @@ ROOF_TRAFFIC = {(0, 1024, 1024, 8192): 33594368, (0, 512, 512, 2048): 4212224, (
                 (3, 512, 512, 512): 2114304}
 
 
-def live_roofline(kt, peaks, b):
-    """Roofline of the dominant kernel: of the launches of the roofline class in
-    one step (events bracket each launch on the stream it runs on, as event
-    nodes of the step's graph, so durations include the concurrency of the real
-    step), the GEMM shape with the largest total time."""
-    ms, fl, mnk = kt
-    if ms.size == 0:
+def live_roofline(b, gp, st, peaks, args):
+    """Roofline of the step's dominant kernel, measured live on the step's own
+    data: the step runs again with every launch on one stream (cells in turn,
+    weight gradients inline: GPIPE_OPT_PIPELINE = GPIPE_OPT_CONCURRENT = 0, the
+    same kernels and shapes, bit-identical results), once per GEMM epilogue
+    class with CUDA events around each of that class's launches (event nodes in
+    the step's graph, on the stream the kernel runs on).  With nothing running
+    beside it, an event pair times one kernel.  The class with the largest
+    total time is the dominant one; its achieved rate is its algorithmic flops
+    (2 M N K per launch) over its launches' summed durations, against the
+    sustained bf16 peak (the kernel runs inside a long step)."""
+    import torch
+    gp.set_option(b.OPT_PIPELINE, 0)
+    gp.set_option(b.OPT_CONCURRENT, 0)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st.step(want_loss=False)  # capture the one-stream graph
+    torch.cuda.synchronize()
+    ev0.record()
+    st.step(want_loss=False)
+    ev1.record()
+    torch.cuda.synchronize()
+    serial_ms = ev0.elapsed_time(ev1)
+    classes = {}
+    for epi in (0, 1, 2, 3, 4):
+        gp.set_option(b.OPT_KERNEL_TIMES, epi + 1)
+        st.step(want_loss=False)
+        st.step(want_loss=False)
+        ms, fl, mnk = gp.kernel_times(with_shapes=True)  # the launches of the last step
+        if ms.size:
+            shapes = {}
+            for t, f, s in zip(ms, fl, mnk):
+                g = shapes.setdefault(tuple(int(x) for x in s), [0.0, 0.0, 0])
+                g[0] += float(t)
+                g[1] += float(f)
+                g[2] += 1
+            classes[epi] = (float(ms.sum()), float(fl.sum()), int(ms.size), shapes)
+    gp.set_option(b.OPT_KERNEL_TIMES, 0)
+    gp.set_option(b.OPT_PIPELINE, gp_opt(args, "PIPELINE", 1))
+    gp.set_option(b.OPT_CONCURRENT, gp_opt(args, "CONCURRENT", 1))
+    if not classes:
         return None
-    groups = {}
-    for t, f, s in zip(ms, fl, mnk):
-        g = groups.setdefault(tuple(int(x) for x in s), [0.0, 0.0, 0])
-        g[0] += float(t)
-        g[1] += float(f)
-        g[2] += 1
-    shape, (tot_ms, tot_fl, n) = max(groups.items(), key=lambda kv: kv[1][0])
+    epi, (tot_ms, tot_fl, n, shapes) = max(classes.items(), key=lambda kv: kv[1][0])
+    shape, (sh_ms, sh_fl, sh_n) = max(shapes.items(), key=lambda kv: kv[1][0])
     ach = tot_fl / (tot_ms / 1e3) / 1e12
-    cls = float(fl.sum()) / (float(ms.sum()) / 1e3) / 1e12
+    sh_ach = sh_fl / (sh_ms / 1e3) / 1e12
     return {"bound": "tensor",
-            "kernel": f"tcgen05 GEMM {shape[0]}x{shape[1]}x{shape[2]}, {EPI_NAMES[ROOF_EPI]}",
+            "kernel": f"tcgen05 GEMM, {EPI_NAMES[epi]} ({n} launches per step, {len(shapes)} shapes)",
             "achieved": ach, "peak": peaks["bf16_sus"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_sus"],
-            "traffic": ROOF_TRAFFIC.get((ROOF_EPI,) + shape),
+            "traffic": ROOF_TRAFFIC.get((epi,) + shape),
             "peak_source": peaks["source"] + " (sustained: the kernel runs inside a long step)",
             "algorithmic_flop_per_launch": tot_fl / n, "launches_per_step": n, "avg_launch_us": tot_ms / n * 1e3,
-            "timing": "CUDA events around every launch of the class in one step (a pass after the timed region: "
-                      "the same graph plus the event nodes), on the stream it runs on",
-            "class": {"launches_per_step": int(ms.size), "achieved": cls, "frac": cls / peaks["bf16_sus"],
-                      "shapes": len(groups)},
-            "isolated": gemm_roofline(b, peaks, shape, ROOF_EPI)}
+            "share_of_one_stream_step": tot_ms / serial_ms, "one_stream_step_ms": serial_ms,
+            "timing": "CUDA events around every launch of the class in one step run on one stream (cells in turn, "
+                      "weight gradients inline), on the stream the kernel runs on",
+            "largest_shape": {"mnk": list(shape), "launches": sh_n, "achieved": sh_ach,
+                              "frac": sh_ach / peaks["bf16_sus"], "avg_launch_us": sh_ms / sh_n * 1e3},
+            "classes": {EPI_NAMES[e]: {"ms_per_step": c[0], "tflops": c[1] / (c[0] / 1e3) / 1e12, "launches": c[2]}
+                        for e, c in classes.items()}}
+
+
+def activation_memory(b, gp, st, w):
+    """Activation memory of the step against the review's bound O(N + (L/K)(N/M)).
+
+    model: the bound written out from the shapes (gpipe_memory_model); layout:
+    the workspace's activation region; touched: measured on the device, the
+    4 KiB pages of that region which one step writes (the region is filled
+    with a sentinel first, so this is the arena's high-water mark as the GPU
+    saw it); allocated_in_step: the drop in free device memory across the step
+    (the library allocates nothing itself)."""
+    import torch
+    mm = gp.memory_model()
+    layout = mm["layout"]
+    st.ws.fill_(0xA5)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    st.step(want_loss=False)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    page = 4096
+    sentinel = int.from_bytes(b"\xa5" * 4, "little", signed=True)
+    words = st.ws[: layout - layout % page].view(torch.int32).view(-1, page // 4)
+    touched = 0
+    chunk = 1 << 18  # pages per pass (1 GiB)
+    for i in range(0, words.shape[0], chunk):
+        touched += int((words[i:i + chunk] != sentinel).any(dim=1).sum().item())
+    touched *= page
+    if layout % page:
+        touched += int((st.ws[layout - layout % page: layout] != 0xA5).any().item()) * (layout % page)
+    del words
+    out = {"model_bytes": mm["total"], "survey_model_bytes": mm["survey"], "layout_bytes": layout,
+           "touched_bytes": touched, "allocated_in_step_bytes": free0 - free1,
+           "within_model": touched <= mm["total"],
+           "terms": {k: mm[k] for k in ("boundary", "cell", "head", "grads", "rows", "align")}}
+    return out
 
 
 def max_over_ranks(value, dist, device):
@@ -393,17 +507,11 @@ def run_ours(args, w):
         st.step(want_loss=True)
     t_e2e = (time.perf_counter() - t0) / e2e_steps
     t_e2e = max_over_ranks(t_e2e, dist, "cuda")
-    # roofline pass: the same step again with timing events around every launch
-    # of the roofline class (the event nodes slow the step, so not in the region above)
-    gp.set_option(b.OPT_KERNEL_TIMES, ROOF_EPI + 1)
-    for _ in range(2):
-        st.step(want_loss=False)
-    for _ in range(min(args.steps, 5)):
-        st.step(want_loss=False)
-    kt = gp.kernel_times(with_shapes=True)  # the launches of the last of these steps
-    gp.set_option(b.OPT_KERNEL_TIMES, 0)
-    roof = live_roofline(kt, peaks, b)
-    peak_act, bound = gp.memory_report()
+    # roofline pass after the timed region (the event nodes and the one-stream
+    # issue slow the step)
+    roof = live_roofline(b, gp, st, peaks, args)
+    mem = activation_memory(b, gp, st, w)
+    mem["executor"] = "single lane (cells in turn)" if gp_opt(args, "PIPELINE", 1) == 0 else "concurrent lanes"
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -419,8 +527,7 @@ def run_ours(args, w):
             "mfu": mf / t_step / (peaks["bf16_sus"] * 1e12) * 1.0,
             "hfu": hf / t_step / (peaks["bf16_sus"] * 1e12),
             "mfu_peak": f"{peaks['bf16_sus']} TFLOP/s bf16 sustained ({peaks['source']})",
-            "loss": loss, "bubble_model": gp.bubble_fraction(), "peak_activation_bytes": peak_act,
-            "activation_bound_bytes": bound,
+            "loss": loss, "bubble_model": gp.bubble_fraction(), "activation_memory": mem,
             "e2e": {"value": tokens_all / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(host_tok.numel() * 4),
                     "d2h_bytes_per_step": 4},
             "gpu_launches": int(launches * args.steps), "launches_per_step": int(launches),
@@ -434,8 +541,8 @@ def run_ours(args, w):
 
 def run_sweep(args):
     """The micro-batch sweep workload over its (K, M) grid: step throughput,
-    peak activation bytes (the workspace's activation high-water mark, which
-    is what is allocated) against the review's bound, and the modelled bubble
+    activation memory (the bound from the shapes, the layout and the bytes the
+    step writes, measured on the device) and the modelled bubble
     (K-1)/(M+K-1).  One JSON line per (K, M); not the throughput line."""
     import torch
     from micro_pipeline_re_gb300._build import build as _build
@@ -464,12 +571,11 @@ def run_sweep(args):
         e1.record()
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / 1e3 / args.steps
-        peak, bound = gp.memory_report()
         P, wsb = gp.sizes()
+        mem = activation_memory(b, gp, st, w)
         print(json.dumps({"sweep": w.name, "K": K, "M": M, "ms_per_step": t * 1e3, "tokens_per_s": w.tokens / t,
                           "mfu": model_flops(w) / t / (peaks["bf16_sus"] * 1e12), "loss": loss,
-                          "bubble_model": gp.bubble_fraction(), "peak_activation_bytes": peak,
-                          "activation_bound_bytes": bound, "workspace_bytes": wsb,
+                          "bubble_model": gp.bubble_fraction(), "activation_memory": mem, "workspace_bytes": wsb,
                           "device_bytes_taken_by_state": free0 - free1}), flush=True)
         del st
         gp.close()
@@ -499,9 +605,15 @@ def main():
                     help="a library option for the step, e.g. --opt INFLIGHT=1 --opt PIPELINE=0 (repeatable)")
     ap.add_argument("--sweep", action="store_true",
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
+    ap.add_argument("--probe-attention", action="store_true",
+                    help="only time the attention forward and backward at one micro-batch of the workload")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run the workload with this many layers instead (memory measurements at reduced L)")
     args = ap.parse_args()
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.layers:
+        w = w.replace(L=args.layers, K=min(w.K, args.layers), name=f"{w.name}_L{args.layers}")
     if args.probe_gemm:
         import torch
         from micro_pipeline_re_gb300._build import build as _build
@@ -514,6 +626,13 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.probe_attention:
+        from micro_pipeline_re_gb300._build import build as _build
+        _build()
+        from micro_pipeline_re_gb300 import binding as b
+        print(json.dumps(attention_roofline(b, load_peaks(), w.tokens_per_micro_batch // w.seq, w.seq, w.heads)),
+              flush=True)
         return
     if args.impl == "reference":
         run_reference(args, w)

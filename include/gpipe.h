@@ -181,21 +181,49 @@ int gpipe_schedule_model(const gpipe_ctx* ctx, const double* t_f, const double* 
  * Returns the number of operations, or a negative GPIPE_ERR_* code. */
 int gpipe_issue_order(const gpipe_ctx* ctx, int32_t* ops_out, int count);
 
-/* Activation memory of the step as laid out in the workspace (bytes):
- *   peak_act_bytes    the workspace's activation high-water mark (boundary
- *                     stash + the re-computed cell's internals + head + the
- *                     gradients in flight); all of it is live at the peak;
- *   model_bound_bytes the review's bound O(N + (L/K)(N/M)) with explicit
- *                     constants: (K+2) D (T/M) d e + T d e + K R (T/M) d e  +  lanes
- *                     (Lc (T/M) a + (T/M) g)  +  heads (T/M) h, T = tokens per
- *                     step, e = activation element bytes, D = stash-ring depth
- *                     (M, or min(M, K+1) with GPIPE_OPT_SCHEDULE 1), R = gradient-ring
- *                     depth, lanes = K x micro-batches in flight (1 without
- *                     lanes), Lc = largest cell's layer count, a = bytes one
- *                     layer keeps per token, g = per-token gradient bytes of a
- *                     lane, h = per-token head bytes (logits included).
+/* Activation memory of the step (bytes).  Source: the GPipe review's
+ * "Preliminaries 5: re-materialisation" (only cell-boundary activations are
+ * kept, so the peak falls from O(N L) to O(N + (L/K)(N/M))).
+ *   peak_act_bytes    the workspace's activation region as laid out for the
+ *                     current options: every byte of it is written by a step
+ *                     (the high-water mark of the caller's arena);
+ *   model_bound_bytes that bound written out in bytes from the model's shapes
+ *                     alone (gpipe_memory_model's total), independent of the
+ *                     layout: with all K cells on one device and one cell
+ *                     differentiated at a time.  The single-lane executor
+ *                     (GPIPE_OPT_PIPELINE 0) stays within it; the default
+ *                     executor runs the K cells as concurrent lanes, each
+ *                     with its own cell workspace, and exceeds it by about
+ *                     (lanes - 1) cell workspaces (the price of running the
+ *                     K cells at once, as K accelerators would).
  * Either output may be NULL. */
 int gpipe_memory_report(const gpipe_ctx* ctx, size_t* peak_act_bytes, size_t* model_bound_bytes);
+
+/* The terms of that bound, and the layout's total, in bytes (T tokens per
+ * step, Tmb = T/M, e = activation element bytes, D = stash depth: M in the
+ * GPipe order, min(M, K+1) with GPIPE_OPT_SCHEDULE 1):
+ *   [0] boundary  O(N): every cell's input for D micro-batches, the head's
+ *                 output gradient (D) and, for the LM, the embedding's input
+ *                 gradient (M), two head inputs, and the gradient each cell
+ *                 receives, double-buffered: (K D + D + M + 2 + 2K) Tmb d e
+ *   [1] cell      O((L/K)(N/M)): one cell of Lc layers of internals for one
+ *                 micro-batch, Lc Tmb a, a = e (8d + 2 ffn) + 16 + 4 heads
+ *                 (FFN block: e (2d + 2 ffn) + 8); without
+ *                 re-materialisation L M Tmb a
+ *   [2] head      one micro-batch's fp32 logits, final-LN output, gradient
+ *                 and statistics, and its LayerNorm partial sums:
+ *                 Tmb (4 V + 2 d e + 8) + 2 ceil(Tmb/8) 2d 4 (LM only)
+ *   [3] grads     one layer's backward working set for one micro-batch
+ *   [4] rows      per-token losses, 4 T
+ *   [5] align     256-byte alignment of the arena's regions, 256 (13 Lc + 48)
+ *   [6] total     [0] + ... + [5]  (= model_bound_bytes)
+ *   [7] survey    the scoping survey's concrete form of the same bound:
+ *                 K T d e + (L/K) Tmb ((8d + 2 ffn) e + 8) + 4 Tmb V + 3 Tmb d e
+ *   [8] layout    the workspace's activation region (= peak_act_bytes)
+ * Writes min(count, GPIPE_MEMORY_TERMS) values; returns GPIPE_MEMORY_TERMS
+ * or a negative GPIPE_ERR_* code. */
+#define GPIPE_MEMORY_TERMS 9
+int gpipe_memory_model(const gpipe_ctx* ctx, size_t* terms_out, int count);
 
 /* Options (defaults in brackets). */
 enum {

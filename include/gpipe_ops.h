@@ -90,7 +90,10 @@ int gpipe_op_layernorm_bwd(int dtype, int rows, int d, const void* dy, const voi
  * allocation routine.  Limit: ceil(rows / 8) * 2 * d <= 2^20 (for d = 1024,
  * rows <= 4096); larger sizes return GPIPE_ERR_INVALID_ARG with a message.
  * The first call on each device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  All calls
+ * device current) and keeps it for the life of the process; make that first
+ * call before any stream capture.  cudaDeviceReset (or anything else that
+ * destroys the device's primary context) invalidates the kept address: do not
+ * call this entry point on a device after resetting it.  All calls
  * share the one array: every partial sum the call reads is written by the
  * same call, so nothing needs clearing, but calls that overlap on the GPU (on
  * different streams, or from different threads) race on it. */

@@ -67,6 +67,7 @@ _SIGS = {
     "gpipe_schedule_model": (c_int, [c_void_p, POINTER(c_double), POINTER(c_double), POINTER(c_double),
                                      POINTER(c_double)]),
     "gpipe_memory_report": (c_int, [c_void_p, POINTER(c_size_t), POINTER(c_size_t)]),
+    "gpipe_memory_model": (c_int, [c_void_p, POINTER(c_size_t), c_int]),
     "gpipe_issue_order": (c_int, [c_void_p, POINTER(c_int32), c_int]),
     "gpipe_layer_times": (c_int, [c_void_p, POINTER(c_float), POINTER(c_float), c_int]),
     "gpipe_set_option": (c_int, [c_void_p, c_int, c_int64]),
@@ -259,6 +260,15 @@ class GPipe:
         a, b = c_size_t(), c_size_t()
         _check(lib().gpipe_memory_report(self.h, ctypes.byref(a), ctypes.byref(b)), self.h)
         return a.value, b.value
+
+    MEMORY_TERMS = ("boundary", "cell", "head", "grads", "rows", "align", "total", "survey", "layout")
+
+    def memory_model(self):
+        """The review's activation bound term by term (gpipe_memory_model), in bytes."""
+        buf = (c_size_t * len(self.MEMORY_TERMS))()
+        n = lib().gpipe_memory_model(self.h, buf, len(buf))
+        _check(min(n, 0), self.h)
+        return dict(zip(self.MEMORY_TERMS, (int(x) for x in buf[:n])))
 
     def set_option(self, opt, value):
         _check(lib().gpipe_set_option(self.h, opt, int(value)), self.h)

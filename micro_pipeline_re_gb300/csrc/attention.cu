@@ -1,18 +1,45 @@
-// Causal multi-head attention, head width 64, bf16 operands, fp32 softmax.
+// Causal multi-head attention on the 5th-generation tensor cores (tcgen05),
+// head width 64, bf16 operands, fp32 softmax.  Scale 1/sqrt(64) = 0.125;
+// query i sees keys j <= i.
 //
-// Forward: one CTA per (64-query block, head, sequence); 4 warps, 16 query
-// rows each.  Key/value blocks of 64 stream through double-buffered shared
-// memory (cp.async); S = Q K^T and O += P V run on the tensor cores
-// (mma.sync m16n8k16, bf16 in, fp32 accumulate) with an online softmax in
-// the log2 domain.  Saves the natural-log LSE per (row, head).
+// Every matrix product runs as tcgen05.mma kind::f16 (bf16 in, fp32 in tensor
+// memory), issued by one thread; Q, K, V and dO tiles arrive by TMA with the
+// 128-byte swizzle (no multicast); the softmax-side tiles (P, dS) are written
+// by the threads into shared memory in the same swizzled layout and fed back
+// to the tensor cores.  Thread r of the CTA's 128 owns row r of every
+// accumulator (tensor-memory lane r): no cross-thread reductions.
 //
-// Backward, without atomics (bit-reproducible):
-//   dq kernel   per (query block, head, sequence): D = rowsum(dO o O), then for
-//               every visible key block P = exp(S - LSE), dP = dO V^T,
-//               dS = P o (dP - D), dQ += dS K.
-//   dkv kernel  per (key block, head, sequence): for every query block that
-//               sees it, P^T, dV += P^T dO, dP^T = V dO^T, dS^T, dK += dS^T Q.
-// Scale 1/sqrt(64) = 0.125.  Causal: query i sees keys j <= i.
+// Forward: a CTA per (128-query block, head, sequence).  For each 128-key
+// block: S = Q K^T into TMEM; the threads read their row of S, update the
+// running maximum (log2 domain), rescale their row of O in TMEM when it
+// grows, write P = exp2(S - m) as bf16 and add its row sum; then
+// O += P V.  Saves the natural-log log-sum-exp per (row, head).
+//
+// Backward, without atomics (bit-reproducible), one launch of two CTA kinds:
+//   dQ CTA    per (128-query block, head, sequence): D = rowsum(dO o O) per
+//             row (also written out), then for every visible 64-key block
+//             S = Q K^T, dP = dO V^T, P = exp2(S - LSE), dS = P o (dP - D),
+//             dQ += dS K.
+//   dK/dV CTA per (128-key block, head, sequence): for every 64-query block
+//             that sees it, S^T = K Q^T, dP^T = V dO^T, P^T, dS^T (with the
+//             same D, computed by the same arithmetic), dV += P^T dO,
+//             dK += dS^T Q.
+//
+// Shared-memory tiles (1024-B aligned, 128-B rows, 16-B unit u of row r at
+// r*128 + ((u ^ (r&7)) * 16)):
+//   as a K-major operand (rows = M or N, 64 head columns or 64 keys per row):
+//     the 16-wide k slice kk starts 32*kk bytes into each row; 8-row groups
+//     are 1024 B apart;
+//   as an MN-major operand (rows = K, 64 head columns = N per row): the
+//     16-deep k slice kk starts 2048*kk bytes further.
+// Every mbarrier wait is bounded (2 s); a wait that gives up sets the
+// library's device error word, the CTA leaves its loop at the next barrier
+// (the decision is made uniform with __syncthreads_and), waits (bounded) for
+// its own copies and products in flight, and frees its tensor memory.
+#include <cuda.h>
+
+#include <atomic>
+
 #include "../../include/gpipe.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -21,471 +48,640 @@
 namespace gp {
 namespace {
 
-constexpr int HD = 64;         // head width
-constexpr int BQ = 64;         // rows per block (queries or keys)
-constexpr int LDS = HD + 8;    // padded shared row (bf16 elements)
+constexpr int HD = 64;                                      // head width
 constexpr float kScaleLog2 = 0.125f * 1.4426950408889634f;  // scale * log2(e)
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int T128 = 128 * 128;  // bytes of a 128-row tile (128 B per row)
+constexpr int T64 = 64 * 128;    // bytes of a 64-row tile
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+__device__ __forceinline__ uint32_t swz(int r, int u) { return static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4)); }
+// K-major operand tile, 16-wide k slice kk (0..3)
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) { return sw128_desc(tile + kk * 32, 16, 1024); }
+// MN-major operand tile (64 wide), 16-deep k slice kk
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, 8192, 1024); }
 
-__device__ __forceinline__ void ldm_x4(uint32_t* r, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldm_x4_t(uint32_t* r, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Copy a 64 x 64 bf16 tile (global row stride ld elements) into padded smem.
-__device__ __forceinline__ void load_tile(__nv_bfloat16 (*dst)[LDS], const __nv_bfloat16* src, int64_t ld) {
+// Load 32 fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void ld_row32(uint32_t taddr, float* v) {
+  uint32_t u[32];
+  tmem_ld32(taddr, u);
+  tmem_ld_wait();
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + i * 128;  // 512 16-B chunks
-    const int r = idx >> 3, c = (idx & 7) * 8;
-    cp_async16(&dst[r][c], src + (int64_t)r * ld + c);
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
+}
+
+// Write 32 values of row r as bf16 into a swizzled tile at units u0..u0+3.
+__device__ __forceinline__ void st_row32_bf16(uint8_t* tile, int r, int u0, const float* v) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * u + 0], v[8 * u + 1]);
+    w.y = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
+    w.z = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
+    w.w = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
+    *reinterpret_cast<uint4*>(tile + swz(r, u0 + u)) = w;
   }
 }
 
-// A fragments (16 rows x 64) of rows r0.. from a smem tile: af[kk][4] for k16 step kk.
-__device__ __forceinline__ void load_a_frags(uint32_t (*af)[4], __nv_bfloat16 (*t)[LDS], int r0) {
-  const int lane = threadIdx.x & 31;
+// Store 64 fp32 TMEM columns of this thread's lane, times scale, as bf16 to
+// dst when `valid`.  Every thread of the warp calls it (the TMEM loads are
+// warp-collective); only the stores depend on `valid`.
+__device__ __forceinline__ void store_row64(uint32_t taddr, __nv_bfloat16* dst, float scale, bool valid) {
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-    ldm_x4(af[kk], &t[r0 + (lane & 7) + ((lane >> 3) & 1) * 8][kk * 16 + ((lane >> 4) & 1) * 8]);
-}
-
-// acc[nt][4] (16 x 64) += A (16 x 64, fragments) * T^T where T is a 64 x 64
-// smem tile whose rows are the n index (B "col" layout, non-transposed ldmatrix).
-__device__ __forceinline__ void mma_abt(float (*acc)[4], const uint32_t (*af)[4], __nv_bfloat16 (*t)[LDS]) {
-  const int lane = threadIdx.x & 31;
+  for (int h = 0; h < 2; ++h) {
+    float v[32];
+    ld_row32(taddr + 32 * h, v);
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
+    for (int i = 0; i < 32; ++i) v[i] *= scale;
+    if (valid) {
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      uint32_t b[4];
-      ldm_x4(b, &t[np * 16 + ((lane >> 4) & 1) * 8 + (lane & 7)][kk * 16 + ((lane >> 3) & 1) * 8]);
-      mma16816(acc[2 * np], af[kk], b[0], b[1]);
-      mma16816(acc[2 * np + 1], af[kk], b[2], b[3]);
+      for (int u = 0; u < 4; ++u) store8(dst + 32 * h + 8 * u, v + 8 * u);
     }
   }
 }
 
-// acc[nt][4] (16 x 64) += P (16 x 64 over k, as fp32 accumulator fragments
-// converted to bf16) * T where T is a 64 x 64 smem tile with rows = k
-// (transposed ldmatrix).
-__device__ __forceinline__ void mma_pt(float (*acc)[4], const float (*p)[4], __nv_bfloat16 (*t)[LDS]) {
-  const int lane = threadIdx.x & 31;
+// rowsum(dO o O) of one 64-wide head row, in a fixed order (shared by the dQ
+// and dK/dV CTAs, so both see the same bits).
+__device__ __forceinline__ float row_dot64(const __nv_bfloat16* o, const __nv_bfloat16* d) {
+  float acc = 0.f;
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    uint32_t a[4];
-    a[0] = pack_bf16x2(p[2 * kk][0], p[2 * kk][1]);
-    a[1] = pack_bf16x2(p[2 * kk][2], p[2 * kk][3]);
-    a[2] = pack_bf16x2(p[2 * kk + 1][0], p[2 * kk + 1][1]);
-    a[3] = pack_bf16x2(p[2 * kk + 1][2], p[2 * kk + 1][3]);
+  for (int c = 0; c < HD; c += 8) {
+    float ov[8], dv[8];
+    load8(o + c, ov);
+    load8(d + c, dv);
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      uint32_t b[4];
-      ldm_x4_t(b, &t[kk * 16 + (lane >> 3 & 1) * 8 + (lane & 7)][np * 16 + ((lane >> 4) & 1) * 8]);
-      mma16816(acc[2 * np], a, b[0], b[1]);
-      mma16816(acc[2 * np + 1], a, b[2], b[3]);
-    }
+    for (int j = 0; j < 8; ++j) acc = fmaf(ov[j], dv[j], acc);
   }
-}
-
-__device__ __forceinline__ void zero_acc(float (*a)[4]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i][0] = a[i][1] = a[i][2] = a[i][3] = 0.f;
-}
-
-// Store a 16 x 64 fp32 fragment block (rows r0.., scaled) as bf16 at dst (row stride ld).
-__device__ __forceinline__ void store_frag(__nv_bfloat16* dst, int64_t ld, const float (*a)[4], float scale) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int c = nt * 8 + 2 * t;
-    *reinterpret_cast<uint32_t*>(dst + (int64_t)g * ld + c) = pack_bf16x2(a[nt][0] * scale, a[nt][1] * scale);
-    *reinterpret_cast<uint32_t*>(dst + (int64_t)(g + 8) * ld + c) = pack_bf16x2(a[nt][2] * scale, a[nt][3] * scale);
-  }
+  return acc;
 }
 
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __restrict__ qkv,
+constexpr int FWD_SMEM = 1024 + 6 * T128 + 128;  // Q, K, V x2, P (2 sub-tiles), barriers
+
+__global__ void __launch_bounds__(128) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq,
                                                        __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                                                       int seq, int heads) {
+                                                       int seq, int heads, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* sQ = sm;
+  uint8_t* sK = sm + T128;
+  uint8_t* sV = sm + 2 * T128;  // two buffers
+  uint8_t* sP = sm + 4 * T128;  // keys 0..63 | keys 64..127
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 6 * T128);
+  uint64_t *bq = bar, *bk = bar + 1, *bv = bar + 2, *bs = bar + 4, *bo = bar + 5;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
+
+  const int r = threadIdx.x, warp = r >> 5;
+  const int nqb = (seq + 127) / 128;
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.x);  // the longest rows first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int D = heads * HD;
+  const int row0 = b * seq;  // the sequence's first row
+  const int q0 = qb * 128;
+  const int nkb = qb + 1;    // key blocks 0..qb (the last one holds the diagonal)
+  const int qi = q0 + r;     // this thread's query
+
+  if (r == 0) {
+    prefetch_tmap(&tq);
+    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
   griddep_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tS = tmem, tO = tmem + 128;
+
+  int nk_issued = 0, nv_issued[2] = {0, 0};
+  if (r == 0) {
+    mbar_arrive_expect_tx(bq, T128);
+    tma_load_2d(sQ, &tq, h * HD, row0 + q0, bq);
+    mbar_arrive_expect_tx(bk, T128);
+    tma_load_2d(sK, &tq, D + h * HD, row0, bk);
+    nk_issued = 1;
+    for (int j = 0; j < 2 && j < nkb; ++j) {
+      mbar_arrive_expect_tx(&bv[j], T128);
+      tma_load_2d(sV + j * T128, &tq, 2 * D + h * HD, row0 + j * 128, &bv[j]);
+      nv_issued[j] = 1;
+    }
+  }
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  constexpr uint32_t idS = mma_idesc_bf16(128, 128, false, false);
+  constexpr uint32_t idO = mma_idesc_bf16(128, 64, false, true);
+  for (int j = 0; j < nkb; ++j) {
+    if (r == 0) {  // S = Q K_j^T
+      bool w = (j > 0 || mbar_wait_bounded(bq, 0, err, DERR_MMA_WAIT)) &&
+               mbar_wait_bounded(bk, j & 1, err, DERR_MMA_WAIT);
+      if (w) {
+        tc_fence_after();
+        const uint32_t q = smem_u32(sQ), k = smem_u32(sK);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(q, kk), kdesc(k, kk), idS, kk ? 1u : 0u);
+        tc_commit(bs);  // also covers the previous block's O += P V
+      }
+    }
+    ok = mbar_wait_bounded(bs, j & 1, err, DERR_ACC_WAIT);
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    tc_fence_after();
+    if (r == 0) {
+      if (j + 1 < nkb) {  // K buffer free: S_j is done
+        mbar_arrive_expect_tx(bk, T128);
+        tma_load_2d(sK, &tq, D + h * HD, row0 + (j + 1) * 128, bk);
+        ++nk_issued;
+      }
+      if (j >= 1 && j + 1 < nkb) {  // V buffer of block j-1 free: O += P_{j-1} V_{j-1} is done
+        const int vb = (j + 1) & 1;
+        mbar_arrive_expect_tx(&bv[vb], T128);
+        tma_load_2d(sV + vb * T128, &tq, 2 * D + h * HD, row0 + (j + 1) * 128, &bv[vb]);
+        ++nv_issued[vb];
+      }
+    }
+    const bool diag = j == qb;
+    // pass 1: row maximum of the scaled scores (log2 domain)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float s[32];
+      ld_row32(tS + lane + 32 * c, s);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const bool vis = !diag || (j * 128 + 32 * c + i <= qi);
+        mx = fmaxf(mx, vis ? s[i] * kScaleLog2 : -INFINITY);
+      }
+    }
+    const float mn = fmaxf(m, mx);
+    const float alpha = exp2f(m - mn);  // 0 for the first block
+    m = mn;
+    // rescale this row of O (warp-uniform: tcgen05 loads/stores are per warp)
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tO + lane + 32 * c, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+        tmem_st32(tO + lane + 32 * c, u);
+      }
+      tmem_st_wait();
+    }
+    // pass 2: P = exp2(s - m) as bf16 into shared memory, and its row sum
+    float rs = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float s[32];
+      ld_row32(tS + lane + 32 * c, s);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const bool vis = !diag || (j * 128 + 32 * c + i <= qi);
+        const float p = vis ? exp2f(s[i] * kScaleLog2 - m) : 0.f;
+        s[i] = p;
+        rs += p;
+      }
+      st_row32_bf16(sP + (c >> 1) * T128, r, (c & 1) * 4, s);
+    }
+    l = l * alpha + rs;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (r == 0) {  // O += P V_j
+      tc_fence_after();
+      const int vb = j & 1;
+      if (mbar_wait_bounded(&bv[vb], (j >> 1) & 1, err, DERR_MMA_WAIT)) {
+        const uint32_t p = smem_u32(sP), v = smem_u32(sV + vb * T128);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tO, kdesc(p + (kk >> 2) * T128, kk & 3), mndesc(v, kk), idO, (j | kk) ? 1u : 0u);
+      }
+    }
+  }
+  if (r == 0) tc_commit(bo);  // every product issued above
+  const bool okd = __syncthreads_and(mbar_wait_bounded(bo, 0, err, DERR_ACC_WAIT));
+  tc_fence_after();
+  if (ok && okd) {
+    // rows past the sequence end (a last block of 64) are computed, not stored
+    const int64_t row = static_cast<int64_t>(row0) + qi;
+    store_row64(tO + lane, out + row * D + h * HD, 1.0f / l, qi < seq);
+    if (qi < seq) lse[row * heads + h] = (m + log2f(l)) * kLn2;
+  }
+  if (r == 0) {  // no copy may still be landing when the CTA exits
+    if (nk_issued) mbar_wait_bounded(bk, (nk_issued - 1) & 1, err, DERR_DRAIN_WAIT);
+    for (int vb = 0; vb < 2; ++vb)
+      if (nv_issued[vb]) mbar_wait_bounded(&bv[vb], (nv_issued[vb] - 1) & 1, err, DERR_DRAIN_WAIT);
+    mbar_wait_bounded(bq, 0, err, DERR_DRAIN_WAIT);
+  }
+  tc_fence_before();
+  __syncthreads();
   griddep_launch();
-  __shared__ __align__(16) __nv_bfloat16 Qs[BQ][LDS];
-  __shared__ __align__(16) __nv_bfloat16 Ks[2][BQ][LDS];
-  __shared__ __align__(16) __nv_bfloat16 Vs[2][BQ][LDS];
-  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward
+// ---------------------------------------------------------------------------
+// dQ CTA: Q, dO (128 rows), K and V blocks of 64 keys (two buffers each), dS
+// (128 x 64).  dK/dV CTA: K, V (128 rows), Q and dO blocks of 64 queries (two
+// buffers each), P^T and dS^T (128 x 64), LSE and D of the query block.
+constexpr int BWD_TILES = 4 * T128 + 4 * T64;  // the larger of the two kinds' tiles (dK/dV: 96 KB)
+constexpr int BWD_LD = BWD_TILES;               // dK/dV: LSE and D of two query blocks (1 KB)
+constexpr int BWD_BAR = BWD_LD + 4 * 64 * 4;
+constexpr int BWD_SMEM = 1024 + BWD_BAR + 128;
+
+__device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, const CUtensorMap* td128,
+                            const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+                            const float* __restrict__ lse, float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv,
+                            int seq, int heads, int b, int* err, uint8_t* sm) {
+  uint8_t* sQ = sm;
+  uint8_t* sdO = sm + T128;
+  uint8_t* sK = sm + 2 * T128;        // two 64-row buffers
+  uint8_t* sV = sK + 2 * T64;         // two 64-row buffers
+  uint8_t* sdS = sV + 2 * T64;        // 128 rows x 64 keys (ends at 80 KB)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + BWD_BAR);
+  uint64_t *bq = bar, *bkv = bar + 1, *bs = bar + 3, *bo = bar + 4;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
+
+  const int r = threadIdx.x, warp = r >> 5;
+  const int nqb = (seq + 127) / 128;
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y;
   const int D = heads * HD;
-  const int64_t ld = 3 * (int64_t)D;
-  const __nv_bfloat16* base = qkv + (int64_t)b * seq * ld;
-  const __nv_bfloat16* Qg = base + (int64_t)qb * BQ * ld + h * HD;
-  const __nv_bfloat16* Kg = base + D + h * HD;
-  const __nv_bfloat16* Vg = base + 2 * D + h * HD;
+  const int64_t ld = 3 * static_cast<int64_t>(D);
+  const int row0 = b * seq;
+  const int q0 = qb * 128;
+  const int qi = q0 + r;
+  const int nkb = (min(q0 + 127, seq - 1)) / 64 + 1;  // 64-key blocks that any row of the block sees
 
-  load_tile(Qs, Qg, ld);
-  load_tile(Ks[0], Kg, ld);
-  load_tile(Vs[0], Vg, ld);
-  cp_async_commit();
+  if (r == 0) {
+    prefetch_tmap(tq64);
+    prefetch_tmap(tq128);
+    prefetch_tmap(td128);
+    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  griddep_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tS = tmem, tP = tmem + 64, tQ = tmem + 128;
 
-  uint32_t qf[4][4];
-  float o[8][4];
-  zero_acc(o);
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int qrow0 = warp * 16 + g;  // local query rows qrow0, qrow0 + 8
-
-  for (int kb = 0; kb <= qb; ++kb) {
-    if (kb + 1 <= qb) {
-      load_tile(Ks[(kb + 1) & 1], Kg + (int64_t)(kb + 1) * BQ * ld, ld);
-      load_tile(Vs[(kb + 1) & 1], Vg + (int64_t)(kb + 1) * BQ * ld, ld);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  int nkv_issued[2] = {0, 0};
+  if (r == 0) {
+    mbar_arrive_expect_tx(bq, 2 * T128);
+    tma_load_2d(sQ, tq128, h * HD, row0 + q0, bq);
+    tma_load_2d(sdO, td128, h * HD, row0 + q0, bq);
+    for (int j = 0; j < 2 && j < nkb; ++j) {
+      mbar_arrive_expect_tx(&bkv[j], 2 * T64);
+      tma_load_2d(sK + j * T64, tq64, D + h * HD, row0 + j * 64, &bkv[j]);
+      tma_load_2d(sV + j * T64, tq64, 2 * D + h * HD, row0 + j * 64, &bkv[j]);
+      nkv_issued[j] = 1;
     }
-    __syncthreads();
-    if (kb == 0) load_a_frags(qf, Qs, warp * 16);
-    float s[8][4];
-    zero_acc(s);
-    mma_abt(s, qf, Ks[kb & 1]);
-    // scale into the log2 domain, mask the diagonal block
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+  }
+  // this row's log-sum-exp (log2 domain) and D = rowsum(dO o O)
+  float L2 = 0.f, Dr = 0.f;
+  if (qi < seq) {
+    const int64_t row = static_cast<int64_t>(row0) + qi;
+    L2 = lse[row * heads + h] * kLog2e;
+    Dr = row_dot64(out + row * D + h * HD, dout + row * D + h * HD);
+    dvec[row * heads + h] = Dr;
+  }
+  bool ok = true;
+  constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
+  constexpr uint32_t idQ = mma_idesc_bf16(128, 64, false, true);
+  for (int j = 0; j < nkb; ++j) {
+    const int kb = j & 1;
+    if (r == 0) {  // S = Q K_j^T, dP = dO V_j^T
+      bool w = (j > 0 || mbar_wait_bounded(bq, 0, err, DERR_MMA_WAIT)) &&
+               mbar_wait_bounded(&bkv[kb], (j >> 1) & 1, err, DERR_MMA_WAIT);
+      if (w) {
+        tc_fence_after();
+        const uint32_t q = smem_u32(sQ), dO = smem_u32(sdO), k = smem_u32(sK + kb * T64), v = smem_u32(sV + kb * T64);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+        for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(q, kk), kdesc(k, kk), idSP, kk ? 1u : 0u);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = s[nt][e] * kScaleLog2;
-        if (kb == qb) {
-          const int key = nt * 8 + 2 * t + (e & 1);
-          const int q = qrow0 + (e >> 1) * 8;
-          if (key > q) v = -INFINITY;
-        }
-        s[nt][e] = v;
+        for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tP, kdesc(dO, kk), kdesc(v, kk), idSP, kk ? 1u : 0u);
+        tc_commit(bs);  // also covers the previous block's dQ += dS K
       }
-      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
-    const float c0 = exp2f(m0 - nm0), c1 = exp2f(m1 - nm1);
-    m0 = nm0;
-    m1 = nm1;
-    float rs0 = 0.f, rs1 = 0.f;
+    ok = mbar_wait_bounded(bs, j & 1, err, DERR_ACC_WAIT);
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    tc_fence_after();
+    if (r == 0 && j >= 1 && j + 1 < nkb) {  // buffers of block j-1 are free
+      const int nb = (j + 1) & 1;
+      mbar_arrive_expect_tx(&bkv[nb], 2 * T64);
+      tma_load_2d(sK + nb * T64, tq64, D + h * HD, row0 + (j + 1) * 64, &bkv[nb]);
+      tma_load_2d(sV + nb * T64, tq64, 2 * D + h * HD, row0 + (j + 1) * 64, &bkv[nb]);
+      ++nkv_issued[nb];
+    }
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - m0);
-      s[nt][1] = exp2f(s[nt][1] - m0);
-      s[nt][2] = exp2f(s[nt][2] - m1);
-      s[nt][3] = exp2f(s[nt][3] - m1);
-      rs0 += s[nt][0] + s[nt][1];
-      rs1 += s[nt][2] + s[nt][3];
-      o[nt][0] *= c0;
-      o[nt][1] *= c0;
-      o[nt][2] *= c1;
-      o[nt][3] *= c1;
+    for (int c = 0; c < 2; ++c) {
+      float s[32], dp[32];
+      ld_row32(tS + lane + 32 * c, s);
+      ld_row32(tP + lane + 32 * c, dp);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const bool vis = j * 64 + 32 * c + i <= qi;
+        const float p = vis ? exp2f(s[i] * kScaleLog2 - L2) : 0.f;
+        s[i] = p * (dp[i] - Dr);  // dS
+      }
+      st_row32_bf16(sdS, r, c * 4, s);
     }
-    l0 = l0 * c0 + rs0;
-    l1 = l1 * c1 + rs1;
-    mma_pt(o, s, Vs[kb & 1]);
+    fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
-  }
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
+    if (r == 0) {  // dQ += dS K_j
+      tc_fence_after();
+      const uint32_t ds = smem_u32(sdS), k = smem_u32(sK + kb * T64);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    o[nt][0] *= inv0;
-    o[nt][1] *= inv0;
-    o[nt][2] *= inv1;
-    o[nt][3] *= inv1;
+      for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tQ, kdesc(ds, kk), mndesc(k, kk), idQ, (j | kk) ? 1u : 0u);
+    }
   }
-  const int64_t row = (int64_t)b * seq + qb * BQ + warp * 16;
-  store_frag(out + row * D + h * HD, D, o, 1.0f);
-  if (t == 0) {
-    lse[(row + g) * heads + h] = (m0 + log2f(l0)) * kLn2;
-    lse[(row + g + 8) * heads + h] = (m1 + log2f(l1)) * kLn2;
+  if (r == 0) tc_commit(bo);
+  const bool okd = __syncthreads_and(mbar_wait_bounded(bo, 0, err, DERR_ACC_WAIT));
+  tc_fence_after();
+  if (ok && okd) {
+    const int64_t row = static_cast<int64_t>(row0) + qi;
+    store_row64(tQ + lane, dqkv + row * ld + h * HD, 0.125f, qi < seq);
+  }
+  if (r == 0) {
+    for (int kb = 0; kb < 2; ++kb)
+      if (nkv_issued[kb]) mbar_wait_bounded(&bkv[kb], (nkv_issued[kb] - 1) & 1, err, DERR_DRAIN_WAIT);
+    mbar_wait_bounded(bq, 0, err, DERR_DRAIN_WAIT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 
-// Shared storage of the backward kernels (above the 48 KB static limit, so
-// allocated dynamically).
-struct DqSmem {
-  __nv_bfloat16 Qs[BQ][LDS];
-  __nv_bfloat16 dOs[BQ][LDS];
-  __nv_bfloat16 Ks[2][BQ][LDS];
-  __nv_bfloat16 Vs[2][BQ][LDS];
-  float Ls[BQ], Ds[BQ];
-};
-struct DkvSmem {
-  __nv_bfloat16 Ks[BQ][LDS];
-  __nv_bfloat16 Vs[BQ][LDS];
-  __nv_bfloat16 Qs[2][BQ][LDS];
-  __nv_bfloat16 dOs[2][BQ][LDS];
-  float Ls[2][BQ], Ds[2][BQ];
-};
+__device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, const CUtensorMap* td64,
+                             const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+                             const float* __restrict__ lse, __nv_bfloat16* __restrict__ dqkv, int seq, int heads,
+                             int b, int* err, uint8_t* sm) {
+  uint8_t* sK = sm;
+  uint8_t* sV = sm + T128;
+  uint8_t* sQ = sm + 2 * T128;     // two 64-row buffers
+  uint8_t* sdO = sQ + 2 * T64;     // two 64-row buffers
+  uint8_t* sPt = sdO + 2 * T64;    // 128 keys x 64 queries
+  uint8_t* sdSt = sPt + T128;      // 128 keys x 64 queries (ends at 96 KB)
+  float* sL = reinterpret_cast<float*>(sm + BWD_LD);  // [2][64]
+  float* sD = sL + 128;                               // [2][64]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + BWD_BAR);
+  uint64_t *bkv = bar, *bq = bar + 1, *bs = bar + 3, *bo = bar + 4;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
 
-// D = rowsum(dO o O) of head h for the 64 rows row0..row0+63, by the block's
-// 128 threads (two per row, 32 columns each, then one shuffle): the same
-// arithmetic wherever it runs, so the dQ and dK/dV blocks agree bit for bit.
-__device__ __forceinline__ float row_dot_o_do(const __nv_bfloat16* __restrict__ out,
-                                              const __nv_bfloat16* __restrict__ dout, int64_t row0, int h, int D) {
-  const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 32;
-  const __nv_bfloat16* orow = out + (row0 + r) * D + h * HD + c0;
-  const __nv_bfloat16* drow = dout + (row0 + r) * D + h * HD + c0;
-  float acc = 0.f;
-#pragma unroll
-  for (int c = 0; c < 32; c += 8) {
-    float ov[8], dv[8];
-    load8(orow + c, ov);
-    load8(drow + c, dv);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc = fmaf(ov[j], dv[j], acc);
-  }
-  return acc + __shfl_xor_sync(0xffffffffu, acc, 1);
-}
-
-// ---------------------------------------------------------------------------
-// Backward: dQ (and D = rowsum(dO o O)) for sequence b
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void attn_bwd_dq(const __nv_bfloat16* __restrict__ qkv,
-                                            const __nv_bfloat16* __restrict__ out,
-                                            const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                                            float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv, int seq,
-                                            int heads, int b, uint8_t* dyn_smem) {
-  DqSmem& S = *reinterpret_cast<DqSmem*>(dyn_smem);
-  auto& Qs = S.Qs;
-  auto& dOs = S.dOs;
-  auto& Ks = S.Ks;
-  auto& Vs = S.Vs;
-  auto& Ls = S.Ls;
-  auto& Ds = S.Ds;
-  const int qb = blockIdx.x, h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int r = threadIdx.x, warp = r >> 5;
+  const int kb = blockIdx.x;  // the key blocks with the most queries first
+  const int h = blockIdx.y;
   const int D = heads * HD;
-  const int64_t ld = 3 * (int64_t)D;
-  const int64_t row0 = (int64_t)b * seq + qb * BQ;  // first global row of this block
-  const __nv_bfloat16* base = qkv + (int64_t)b * seq * ld;
-  const __nv_bfloat16* Kg = base + D + h * HD;
-  const __nv_bfloat16* Vg = base + 2 * D + h * HD;
+  const int64_t ld = 3 * static_cast<int64_t>(D);
+  const int row0 = b * seq;
+  const int k0 = kb * 128;
+  const int kr = k0 + r;  // this thread's key
+  const int i0 = k0 / 64, nq = seq / 64;  // 64-query blocks i0..nq-1 see this key block
+  const int niter = nq - i0;
 
-  load_tile(Qs, qkv + row0 * ld + h * HD, ld);
-  load_tile(dOs, dout + row0 * D + h * HD, D);
-  load_tile(Ks[0], Kg, ld);
-  load_tile(Vs[0], Vg, ld);
-  cp_async_commit();
+  if (r == 0) {
+    prefetch_tmap(tq64);
+    prefetch_tmap(tq128);
+    prefetch_tmap(td64);
+    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  griddep_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tS = tmem, tP = tmem + 64, tV = tmem + 128, tK = tmem + 192;
 
-  // D for the block's rows
-  {
-    const int r = threadIdx.x >> 1;
-    const float acc = row_dot_o_do(out, dout, row0, h, D);
-    if ((threadIdx.x & 1) == 0) {
-      Ds[r] = acc;
-      dvec[(row0 + r) * heads + h] = acc;
-      Ls[r] = lse[(row0 + r) * heads + h] * 1.4426950408889634f;
+  int nq_issued[2] = {0, 0};
+  if (r == 0) {
+    mbar_arrive_expect_tx(bkv, 2 * T128);
+    tma_load_2d(sK, tq128, D + h * HD, row0 + k0, bkv);
+    tma_load_2d(sV, tq128, 2 * D + h * HD, row0 + k0, bkv);
+    for (int t = 0; t < 2 && t < niter; ++t) {
+      mbar_arrive_expect_tx(&bq[t], 2 * T64);
+      tma_load_2d(sQ + t * T64, tq64, h * HD, row0 + (i0 + t) * 64, &bq[t]);
+      tma_load_2d(sdO + t * T64, td64, h * HD, row0 + (i0 + t) * 64, &bq[t]);
+      nq_issued[t] = 1;
     }
   }
-
-  uint32_t qf[4][4], df[4][4];
-  float dq[8][4];
-  zero_acc(dq);
-  const int qr = warp * 16 + g;
-  for (int kb = 0; kb <= qb; ++kb) {
-    if (kb + 1 <= qb) {
-      load_tile(Ks[(kb + 1) & 1], Kg + (int64_t)(kb + 1) * BQ * ld, ld);
-      load_tile(Vs[(kb + 1) & 1], Vg + (int64_t)(kb + 1) * BQ * ld, ld);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  bool ok = true;
+  constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
+  constexpr uint32_t idKV = mma_idesc_bf16(128, 64, false, true);
+  for (int t = 0; t < niter; ++t) {
+    const int i = i0 + t, qbuf = t & 1;
+    // LSE (log2 domain) and D of the 64 queries of block i
+    if (r < 64) {
+      const int64_t row = static_cast<int64_t>(row0) + i * 64 + r;
+      sL[qbuf * 64 + r] = lse[row * heads + h] * kLog2e;
+      sD[qbuf * 64 + r] = row_dot64(out + row * D + h * HD, dout + row * D + h * HD);
     }
-    __syncthreads();
-    if (kb == 0) {
-      load_a_frags(qf, Qs, warp * 16);
-      load_a_frags(df, dOs, warp * 16);
-    }
-    const float L0 = Ls[qr], L1 = Ls[qr + 8], D0 = Ds[qr], D1 = Ds[qr + 8];
-    float p[8][4], dp[8][4];
-    zero_acc(p);
-    zero_acc(dp);
-    mma_abt(p, qf, Ks[kb & 1]);
-    mma_abt(dp, df, Vs[kb & 1]);
+    if (r == 0) {  // S^T = K Q_i^T, dP^T = V dO_i^T
+      bool w = (t > 0 || mbar_wait_bounded(bkv, 0, err, DERR_MMA_WAIT)) &&
+               mbar_wait_bounded(&bq[qbuf], (t >> 1) & 1, err, DERR_MMA_WAIT);
+      if (w) {
+        tc_fence_after();
+        const uint32_t k = smem_u32(sK), v = smem_u32(sV), q = smem_u32(sQ + qbuf * T64),
+                       dO = smem_u32(sdO + qbuf * T64);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+        for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(k, kk), kdesc(q, kk), idSP, kk ? 1u : 0u);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool lo = e < 2;
-        float pv = exp2f(p[nt][e] * kScaleLog2 - (lo ? L0 : L1));
-        if (kb == qb) {
-          const int key = nt * 8 + 2 * t + (e & 1);
-          if (key > qr + (lo ? 0 : 8)) pv = 0.f;
-        }
-        p[nt][e] = pv * (dp[nt][e] - (lo ? D0 : D1));  // dS
+        for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tP, kdesc(v, kk), kdesc(dO, kk), idSP, kk ? 1u : 0u);
+        tc_commit(bs);  // also covers the previous block's dV, dK products
       }
     }
-    mma_pt(dq, p, Ks[kb & 1]);
+    ok = mbar_wait_bounded(bs, t & 1, err, DERR_ACC_WAIT);
+    ok = __syncthreads_and(ok);  // also publishes sL / sD of this block
+    if (!ok) break;
+    tc_fence_after();
+    if (r == 0 && t >= 1 && t + 1 < niter) {  // buffers of block i-1 are free
+      const int nb = (t + 1) & 1;
+      mbar_arrive_expect_tx(&bq[nb], 2 * T64);
+      tma_load_2d(sQ + nb * T64, tq64, h * HD, row0 + (i + 1) * 64, &bq[nb]);
+      tma_load_2d(sdO + nb * T64, td64, h * HD, row0 + (i + 1) * 64, &bq[nb]);
+      ++nq_issued[nb];
+    }
+    const float* L = sL + qbuf * 64;
+    const float* Dq = sD + qbuf * 64;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float s[32], dp[32];
+      ld_row32(tS + lane + 32 * c, s);
+      ld_row32(tP + lane + 32 * c, dp);
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const int q = 32 * c + x;
+        const bool vis = i * 64 + q >= kr;
+        const float p = vis ? exp2f(s[x] * kScaleLog2 - L[q]) : 0.f;
+        s[x] = p;                   // P^T
+        dp[x] = p * (dp[x] - Dq[q]);  // dS^T
+      }
+      st_row32_bf16(sPt, r, c * 4, s);
+      st_row32_bf16(sdSt, r, c * 4, dp);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
+    if (r == 0) {  // dV += P^T dO_i, dK += dS^T Q_i
+      tc_fence_after();
+      const uint32_t pt = smem_u32(sPt), dst = smem_u32(sdSt), q = smem_u32(sQ + qbuf * T64),
+                     dO = smem_u32(sdO + qbuf * T64);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tV, kdesc(pt, kk), mndesc(dO, kk), idKV, (t | kk) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tK, kdesc(dst, kk), mndesc(q, kk), idKV, (t | kk) ? 1u : 0u);
+    }
   }
-  store_frag(dqkv + (row0 + warp * 16) * ld + h * HD, ld, dq, 0.125f);
+  if (r == 0) tc_commit(bo);
+  const bool okd = __syncthreads_and(mbar_wait_bounded(bo, 0, err, DERR_ACC_WAIT));
+  tc_fence_after();
+  if (ok && okd) {
+    const int64_t row = static_cast<int64_t>(row0) + kr;
+    store_row64(tK + lane, dqkv + row * ld + D + h * HD, 0.125f, kr < seq);
+    store_row64(tV + lane, dqkv + row * ld + 2 * D + h * HD, 1.0f, kr < seq);
+  }
+  if (r == 0) {
+    for (int qb = 0; qb < 2; ++qb)
+      if (nq_issued[qb]) mbar_wait_bounded(&bq[qb], (nq_issued[qb] - 1) & 1, err, DERR_DRAIN_WAIT);
+    mbar_wait_bounded(bkv, 0, err, DERR_DRAIN_WAIT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
 }
 
-// ---------------------------------------------------------------------------
-// Backward: dK, dV
-// ---------------------------------------------------------------------------
-// (D of the query rows recomputed here, so this part does not wait for the dQ part)
-__device__ __forceinline__ void attn_bwd_dkv(const __nv_bfloat16* __restrict__ qkv,
-                                             const __nv_bfloat16* __restrict__ out,
-                                             const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                                             __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int b,
-                                             uint8_t* dyn_smem) {
-  DkvSmem& S = *reinterpret_cast<DkvSmem*>(dyn_smem);
-  auto& Ks = S.Ks;
-  auto& Vs = S.Vs;
-  auto& Qs = S.Qs;
-  auto& dOs = S.dOs;
-  auto& Ls = S.Ls;
-  auto& Ds = S.Ds;
-  const int kb = blockIdx.x, h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int D = heads * HD;
-  const int64_t ld = 3 * (int64_t)D;
-  const int nqb = seq / BQ;
-  const int64_t srow = (int64_t)b * seq;  // first global row of the sequence
-  const __nv_bfloat16* Qg = qkv + srow * ld + h * HD;
-  const __nv_bfloat16* dOg = dout + srow * D + h * HD;
-
-  load_tile(Ks, qkv + (srow + kb * BQ) * ld + D + h * HD, ld);
-  load_tile(Vs, qkv + (srow + kb * BQ) * ld + 2 * D + h * HD, ld);
-  load_tile(Qs[0], Qg + (int64_t)kb * BQ * ld, ld);
-  load_tile(dOs[0], dOg + (int64_t)kb * BQ * D, D);
-  cp_async_commit();
-  {
-    const float dd = row_dot_o_do(out, dout, srow + kb * BQ, h, D);
-    if ((threadIdx.x & 1) == 0) Ds[0][threadIdx.x >> 1] = dd;
-  }
-  if (threadIdx.x < BQ) {
-    const int64_t r = srow + kb * BQ + threadIdx.x;
-    Ls[0][threadIdx.x] = lse[r * heads + h] * 1.4426950408889634f;
-  }
-
-  uint32_t kf[4][4], vf[4][4];
-  float dk[8][4], dv[8][4];
-  zero_acc(dk);
-  zero_acc(dv);
-  const int kr = warp * 16 + g;  // local key rows kr, kr + 8
-  for (int qb = kb; qb < nqb; ++qb) {
-    const int buf = (qb - kb) & 1;
-    if (qb + 1 < nqb) {
-      const int nb = buf ^ 1;
-      load_tile(Qs[nb], Qg + (int64_t)(qb + 1) * BQ * ld, ld);
-      load_tile(dOs[nb], dOg + (int64_t)(qb + 1) * BQ * D, D);
-      cp_async_commit();
-      {
-        const float dd = row_dot_o_do(out, dout, srow + (qb + 1) * BQ, h, D);
-        if ((threadIdx.x & 1) == 0) Ds[nb][threadIdx.x >> 1] = dd;
-      }
-      if (threadIdx.x < BQ) {
-        const int64_t r = srow + (qb + 1) * BQ + threadIdx.x;
-        Ls[nb][threadIdx.x] = lse[r * heads + h] * 1.4426950408889634f;
-      }
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (qb == kb) {
-      load_a_frags(kf, Ks, warp * 16);
-      load_a_frags(vf, Vs, warp * 16);
-    }
-    float pt[8][4], dpt[8][4];
-    zero_acc(pt);
-    zero_acc(dpt);
-    mma_abt(pt, kf, Qs[buf]);   // S^T (keys x queries)
-    mma_abt(dpt, vf, dOs[buf]); // dP^T = V dO^T
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int q = nt * 8 + 2 * t + (e & 1);
-        float pv = exp2f(pt[nt][e] * kScaleLog2 - Ls[buf][q]);
-        if (qb == kb && q < kr + (e >= 2 ? 8 : 0)) pv = 0.f;
-        pt[nt][e] = pv;
-        dpt[nt][e] = pv * (dpt[nt][e] - Ds[buf][q]);  // dS^T
-      }
-    }
-    mma_pt(dv, pt, dOs[buf]);
-    mma_pt(dk, dpt, Qs[buf]);
-    __syncthreads();
-  }
-  const int64_t row = srow + kb * BQ + warp * 16;
-  store_frag(dqkv + row * ld + D + h * HD, ld, dk, 0.125f);
-  store_frag(dqkv + row * ld + 2 * D + h * HD, ld, dv, 1.0f);
-}
-
-// One launch for both parts: blocks with z < nseq compute dQ of sequence z,
-// the others dK/dV of sequence z - nseq; the two parts share no data.
-constexpr size_t kBwdSmem = sizeof(DqSmem) > sizeof(DkvSmem) ? sizeof(DqSmem) : sizeof(DkvSmem);
-__global__ void __launch_bounds__(128) attn_bwd_kernel(const __nv_bfloat16* __restrict__ qkv,
+// One launch for both kinds: blocks with z < nseq compute dQ of sequence z,
+// the others dK/dV of sequence z - nseq; the two kinds share no data.
+__global__ void __launch_bounds__(128) attn_bwd_kernel(const __grid_constant__ CUtensorMap tq64,
+                                                       const __grid_constant__ CUtensorMap tq128,
+                                                       const __grid_constant__ CUtensorMap td64,
+                                                       const __grid_constant__ CUtensorMap td128,
                                                        const __nv_bfloat16* __restrict__ out,
                                                        const __nv_bfloat16* __restrict__ dout,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
-                                                       __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int nseq) {
-  griddep_wait();
-  griddep_launch();
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
+                                                       __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int nseq,
+                                                       int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
   const int z = blockIdx.z;
   if (z < nseq)
-    attn_bwd_dq(qkv, out, dout, lse, dvec, dqkv, seq, heads, z, dyn_smem);
+    attn_bwd_dq(&tq64, &tq128, &td128, out, dout, lse, dvec, dqkv, seq, heads, z, err, sm);
   else
-    attn_bwd_dkv(qkv, out, dout, lse, dqkv, seq, heads, z - nseq, dyn_smem);
+    attn_bwd_dkv(&tq64, &tq128, &td64, out, dout, lse, dqkv, seq, heads, z - nseq, err, sm);
+  griddep_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static std::atomic<EncodeFn> fn{nullptr};
+  EncodeFn f = fn.load(std::memory_order_acquire);
+  if (!f) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeFn>(p);
+      fn.store(f, std::memory_order_release);
+    }
+  }
+  return f;
+}
+
+// bf16 matrix [rows][cols] (row stride ld elements), boxes of 64 columns x
+// box_rows rows, 128-byte swizzle.
+bool amake_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld, int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_args(int nseq, int seq, int heads) {
+  if (nseq < 1 || seq < 64 || seq % 64 || heads < 1 || heads > 65535)
+    return set_error(GPIPE_ERR_INVALID_ARG, "attention: need nseq >= 1, seq %% 64 == 0, heads >= 1");
+  if (static_cast<int64_t>(nseq) * seq > (int64_t(1) << 30))
+    return set_error(GPIPE_ERR_INVALID_ARG, "attention: nseq * seq must be at most 2^30");
+  return GPIPE_OK;
+}
 
 }  // namespace
 
 int prepare_attention() {
   static std::atomic<unsigned long long> done{0};
-  return once_per_device(done, [] {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem);
-    return e == cudaSuccess ? GPIPE_OK : set_error(GPIPE_ERR_CUDA, "attention_bwd: shared-memory attribute failed");
+  return once_per_device(done, []() -> int {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
+    if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention: shared-memory attribute failed");
+    if (!encode_fn()) return set_error(GPIPE_ERR_CUDA, "attention: cuTensorMapEncodeTiled entry point not found");
+    return static_cast<int>(GPIPE_OK);
   });
 }
 
 int launch_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o, float* lse, cudaStream_t s) {
-  if (nseq < 1 || seq < BQ || seq % BQ || heads < 1 || heads > 65535)
-    return set_error(GPIPE_ERR_INVALID_ARG, "attention: need nseq >= 1, seq %% 64 == 0, heads >= 1");
+  int rc = check_args(nseq, seq, heads);
+  if (rc) return rc;
   if (!al16(qkv) || !al16(o)) return set_error(GPIPE_ERR_INVALID_ARG, "attention: pointers must be 16-B aligned");
-  dim3 grid(seq / BQ, heads, nseq);
-  (void)launch_k(attn_fwd_kernel, grid, 128, 0, s, static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(o), lse,
-                                       seq, heads);
+  rc = prepare_attention();
+  if (rc) return rc;
+  int* err = device_error_ptr();
+  if (!err) return set_error(GPIPE_ERR_CUDA, "attention: no device error word");
+  const int64_t D = static_cast<int64_t>(heads) * HD, rows = static_cast<int64_t>(nseq) * seq;
+  CUtensorMap tq;
+  if (!amake_tmap(&tq, qkv, 3 * D, rows, 3 * D, 128))
+    return set_error(GPIPE_ERR_CUDA, "attention_fwd: tensor map creation failed");
+  dim3 grid((seq + 127) / 128, heads, nseq);
+  (void)launch_k<true>(attn_fwd_kernel, grid, 128, FWD_SMEM, s, tq, static_cast<__nv_bfloat16*>(o), lse, seq, heads,
+                       err);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention_fwd launch: %s", cudaGetErrorString(e));
@@ -494,17 +690,24 @@ int launch_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o,
 
 int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const void* o, const void* dout,
                          const float* lse, float* dvec, void* dqkv, cudaStream_t s) {
-  if (nseq < 1 || seq < BQ || seq % BQ || heads < 1 || heads > 65535)
-    return set_error(GPIPE_ERR_INVALID_ARG, "attention: need nseq >= 1, seq %% 64 == 0, heads >= 1");
+  int rc = check_args(nseq, seq, heads);
+  if (rc) return rc;
   if (!al16(qkv) || !al16(o) || !al16(dout) || !al16(dqkv))
     return set_error(GPIPE_ERR_INVALID_ARG, "attention: pointers must be 16-B aligned");
-  int rc = prepare_attention();
-  if (rc) return rc;
   if (nseq > 32767) return set_error(GPIPE_ERR_INVALID_ARG, "attention: nseq must be <= 32767");
-  dim3 grid(seq / BQ, heads, 2 * nseq);
-  (void)launch_k(attn_bwd_kernel, grid, 128, kBwdSmem, s, static_cast<const __nv_bfloat16*>(qkv),
-                 static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, dvec,
-                 static_cast<__nv_bfloat16*>(dqkv), seq, heads, nseq);
+  rc = prepare_attention();
+  if (rc) return rc;
+  int* err = device_error_ptr();
+  if (!err) return set_error(GPIPE_ERR_CUDA, "attention: no device error word");
+  const int64_t D = static_cast<int64_t>(heads) * HD, rows = static_cast<int64_t>(nseq) * seq;
+  CUtensorMap tq64, tq128, td64, td128;
+  bool ok = amake_tmap(&tq64, qkv, 3 * D, rows, 3 * D, 64) && amake_tmap(&tq128, qkv, 3 * D, rows, 3 * D, 128) &&
+            amake_tmap(&td64, dout, D, rows, D, 64) && amake_tmap(&td128, dout, D, rows, D, 128);
+  if (!ok) return set_error(GPIPE_ERR_CUDA, "attention_bwd: tensor map creation failed");
+  dim3 grid((seq + 127) / 128, heads, 2 * nseq);
+  (void)launch_k<true>(attn_bwd_kernel, grid, 128, BWD_SMEM, s, tq64, tq128, td64, td128,
+                       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, dvec,
+                       static_cast<__nv_bfloat16*>(dqkv), seq, heads, nseq, err);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention_bwd launch: %s", cudaGetErrorString(e));

@@ -9,7 +9,13 @@
 // heads, seq, vocab, dtype, u64 parameter count, u64 layout fingerprint
 // (FNV-1a over the shape fields and every layer's FFN width), u64 step,
 // u64 payload checksum (FNV-1a over the bytes that follow), then P floats of
-// weights and P floats of RMSProp state.  Written to path.tmp and renamed.
+// weights and P floats of RMSProp state.  Written to path.tmp, flushed to the
+// disk (fsync), renamed over path, and the directory flushed too: after a
+// crash or power loss at any point, path holds either the previous complete
+// checkpoint or the new one, never a renamed file whose data did not land.
+#include <fcntl.h>
+#include <unistd.h>
+
 #include <cerrno>
 #include <cstdio>
 #include <cstring>
@@ -78,6 +84,16 @@ int io_fail(const gpipe_ctx* c, const std::string& msg) {
   return gp::context_fail(const_cast<gpipe_ctx*>(c), GPIPE_ERR_IO, msg.c_str());
 }
 
+// Flush the directory that holds path, so that a rename inside it is durable.
+bool sync_parent_dir(const std::string& path) {
+  const size_t slash = path.find_last_of('/');
+  const std::string dir = slash == std::string::npos ? "." : (slash == 0 ? "/" : path.substr(0, slash));
+  const int fd = open(dir.c_str(), O_RDONLY | O_DIRECTORY);
+  if (fd < 0) return false;
+  const bool ok = fsync(fd) == 0;
+  return (close(fd) == 0) && ok;
+}
+
 }  // namespace
 
 extern "C" {
@@ -97,11 +113,14 @@ int gpipe_checkpoint_write(const gpipe_ctx* c, const char* path, const float* pa
   if (!f) return io_fail(c, "cannot open " + tmp + ": " + std::strerror(errno));
   bool ok = std::fwrite(head.data(), 1, head.size(), f) == head.size() &&
             std::fwrite(params, 1, bytes, f) == bytes && std::fwrite(rms_v, 1, bytes, f) == bytes;
+  // the data reaches the disk before the rename can make it the checkpoint
+  ok = ok && std::fflush(f) == 0 && fsync(fileno(f)) == 0;
   ok = (std::fclose(f) == 0) && ok;
   if (!ok || std::rename(tmp.c_str(), path) != 0) {
     std::remove(tmp.c_str());
     return io_fail(c, std::string("cannot write ") + path);
   }
+  if (!sync_parent_dir(path)) return io_fail(c, std::string("cannot flush the directory of ") + path);
   return GPIPE_OK;
 }
 

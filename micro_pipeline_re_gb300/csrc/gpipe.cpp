@@ -138,6 +138,9 @@ struct gpipe_ctx {
     err = last_error_message();
     return code;
   }
+  MemoryModel memory_model() const {
+    return review_memory_model(dm, L, K, M, max_cell, stash_depth(K, M, schedule), !no_remat);
+  }
   void refresh_ws() {
     if (ws_stale) {
       const int nin = inflight_eff();
@@ -275,7 +278,8 @@ class Executor {
         if (!e && cudaEventCreate(&e) != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "cannot create a layer event");
     }
     std::vector<Op> ops;
-    if (!issue_order(K, M, c_->schedule, w.ring, ops)) return set_error(GPIPE_ERR_INVALID_ARG, "no issue order");
+    if (!issue_order(K, M, c_->schedule, w.ring, ops, w.head_depth))
+      return set_error(GPIPE_ERR_INVALID_ARG, "no issue order");
     // cells busy at each tick of the order (ops of one tick can run at once)
     int ticks = 0;
     for (const Op& o : ops) ticks = std::max(ticks, o.tick + 1);
@@ -448,11 +452,11 @@ class Executor {
   size_t fwd_i(int k, int m) const { return static_cast<size_t>(k) * c_->ws.depth + m % c_->ws.depth; }
   cudaEvent_t fwd_ev(int k, int m) const { return c_->ev_fwd[fwd_i(k, m)]; }
   int slot_free_wait(int lane, int lev, int m) {
-    const int D = c_->ws.depth;
+    const int D = lev == c_->K ? c_->ws.head_depth : c_->ws.depth;
     if (m < D || c_->ws.nlanes == 1) return GPIPE_OK;
     cudaEvent_t e;
     if (lev == c_->K) {
-      e = c_->ev_hdone[m - D];
+      e = c_->ev_hdone[m - D];  // the head has read its input (recorded: the issue order put it earlier)
     } else {
       const size_t i = static_cast<size_t>(lev) * D + (m - D) % D;
       if (!sfree_rec_[i]) return set_error(GPIPE_ERR_INVALID_ARG, "issue order reuses a stash slot early");
@@ -568,8 +572,13 @@ class Executor {
   const int32_t* tokens(int m) const {
     return static_cast<const int32_t*>(p_.batch) + static_cast<size_t>(m) * c_->Tmb();
   }
+  // cell k's input (k < K; level 0 is the embedding's output) or, for k = K,
+  // the last cell's output in the head's shorter ring
   char* stash(int k, int m) const {
-    return ws(c_->ws.stash) + (static_cast<size_t>(k) * c_->ws.depth + m % c_->ws.depth) * c_->ws.stash_bytes;
+    const Workspace& w = c_->ws;
+    const size_t i = k < c_->K ? static_cast<size_t>(k) * w.depth + m % w.depth
+                               : static_cast<size_t>(c_->K) * w.depth + m % w.head_depth;
+    return ws(w.stash) + i * w.stash_bytes;
   }
   char* dx0(int m) const { return ws(c_->ws.dx0) + static_cast<size_t>(m) * c_->ws.stash_bytes; }
   char* bgrad(int k, int p) const {
@@ -1115,7 +1124,8 @@ int gpipe_issue_order(const gpipe_ctx* cc, int32_t* ops_out, int count) {
   gpipe_ctx* c = const_cast<gpipe_ctx*>(cc);
   c->refresh_ws();
   std::vector<Op> ops;
-  if (!issue_order(c->K, c->M, c->schedule, c->ws.ring, ops)) return c->fail(GPIPE_ERR_INVALID_ARG, "no issue order");
+  if (!issue_order(c->K, c->M, c->schedule, c->ws.ring, ops, c->ws.head_depth))
+    return c->fail(GPIPE_ERR_INVALID_ARG, "no issue order");
   for (int i = 0; i < count && i < static_cast<int>(ops.size()); ++i) {
     ops_out[4 * i] = ops[i].kind;
     ops_out[4 * i + 1] = ops[i].k;
@@ -1130,8 +1140,19 @@ int gpipe_memory_report(const gpipe_ctx* cc, size_t* peak_act_bytes, size_t* mod
   gpipe_ctx* c = const_cast<gpipe_ctx*>(cc);
   c->refresh_ws();
   if (peak_act_bytes) *peak_act_bytes = c->ws.act_bytes;
-  if (model_bound_bytes) *model_bound_bytes = c->ws.bound_bytes;
+  if (model_bound_bytes) *model_bound_bytes = c->memory_model().total;
   return GPIPE_OK;
+}
+
+int gpipe_memory_model(const gpipe_ctx* cc, size_t* terms_out, int count) {
+  if (!cc || count < 0 || (count > 0 && !terms_out)) return GPIPE_ERR_INVALID_ARG;
+  gpipe_ctx* c = const_cast<gpipe_ctx*>(cc);
+  c->refresh_ws();
+  const MemoryModel mm = c->memory_model();
+  const size_t t[GPIPE_MEMORY_TERMS] = {mm.boundary, mm.cell, mm.head, mm.grads, mm.rows, mm.align, mm.total,
+                                        mm.survey, c->ws.act_bytes};
+  for (int i = 0; i < count && i < GPIPE_MEMORY_TERMS; ++i) terms_out[i] = t[i];
+  return GPIPE_MEMORY_TERMS;
 }
 
 int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {

@@ -101,7 +101,7 @@ inline size_t op_index(int kind, int k, int m, int K, int M) {
 }
 }  // namespace
 
-bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops) {
+bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops, int head_depth) {
   ops.clear();
   if (K < 1 || M < 1 || ring < 1) return false;
   if (schedule == 0) {
@@ -116,6 +116,7 @@ bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops) {
   }
   if (schedule != 1) return false;
   const int D = stash_depth(K, M, schedule);
+  const int DK = head_depth > 0 ? std::min(head_depth, D) : D;
   // per-stage sequences: cells 0..K-1, then the head (stage K)
   std::vector<std::vector<Op>> seq(K + 1);
   for (int k = 0; k < K; ++k) {
@@ -139,9 +140,11 @@ bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops) {
       // was released by the previous micro-batch in it
       if (o.m >= D) {
         const int pm = o.m - D;
-        if (o.k + 1 < K ? !issued_before(OP_BWD, o.k + 1, pm, r) : !issued_before(OP_HEAD, 0, pm, r)) return false;
+        if (o.k + 1 < K && !issued_before(OP_BWD, o.k + 1, pm, r)) return false;
         if (o.k == 0 && !issued_before(OP_BWD, 0, pm, r)) return false;
       }
+      // the last cell's output goes to the head's input ring
+      if (o.k == K - 1 && o.m >= DK && !issued_before(OP_HEAD, 0, o.m - DK, r)) return false;
       return true;
     }
     if (o.kind == OP_HEAD) {
@@ -315,7 +318,12 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     return at;
   };
   w.stash_bytes = Tmb * d * es;
-  w.stash = take(static_cast<size_t>(K + 1) * w.depth * w.stash_bytes);
+  // the last cell's output is read only by the head, right after the cell
+  // forwarded it: a ring as deep as the head's lanes plus one (the cell can
+  // write the next micro-batch while the head lanes read theirs)
+  w.nheads = dm.kind == 1 && w.nlanes > 1 && M > 1 ? 2 : 1;  // a second head lane needs a second micro-batch
+  w.head_depth = std::min(w.depth, w.nheads + 1);
+  w.stash = take((static_cast<size_t>(K) * w.depth + w.head_depth) * w.stash_bytes);
   w.dx0 = take(dm.kind == 1 ? static_cast<size_t>(M) * w.stash_bytes : 0);
   // the gradient ring: as deep as the micro-batches in flight (at least 2, so
   // a cell can hand over m+1 while its neighbour still reads m), never deeper
@@ -326,7 +334,6 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
   w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
   w.hdy = take(static_cast<size_t>(w.depth) * w.stash_bytes);
-  w.nheads = dm.kind == 1 && w.nlanes > 1 && M > 1 ? 2 : 1;  // a second head lane needs a second micro-batch
   for (int h = 0; h < w.nheads && dm.kind == 1; ++h) {
     Workspace::Head& hb = w.head[h];
     hb.hf = take(Tmb * d * es);
@@ -347,23 +354,37 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     w.check = take(w.check_bytes);
   }
   w.total = off;
-  // The review's bound O(N + (L/K)(N/M)) per accelerator, with explicit
-  // constants, summed over the lanes: the boundary tensors (stash and the
-  // head's output gradient, depth micro-batches each; the embedding's input
-  // gradient; the gradient ring; proportional to N), and
-  // per lane one cell of Lc layers of kept internals for one micro-batch plus
-  // that lane's gradient buffers (proportional to (L/K)(N/M)); per head lane
-  // the logits of one micro-batch and its temporaries; the per-row losses.
-  const size_t boundary = static_cast<size_t>(K + 2) * w.depth * Tmb * d * es + T * d * es +
-                          static_cast<size_t>(K) * w.ring * Tmb * d * es;
-  const size_t per_lane = ln.bytes + 4096;
-  const size_t head =
-      dm.kind == 1
-          ? w.nheads * (Tmb * (2 * d * es + 8 + static_cast<size_t>(dm.vocab) * 4) + 2 * w.lnp_bytes + 8192)
-          : 0;
-  const size_t cell_all = remat ? 0 : static_cast<size_t>(L) * M * w.slot_bytes;
-  w.bound_bytes = boundary + static_cast<size_t>(w.nlanes) * per_lane + cell_all + head + T * 4 + 8192;
   return w;
+}
+
+MemoryModel review_memory_model(const Dims& dm, int L, int K, int M, int max_cell_layers, int depth, bool remat) {
+  MemoryModel mm;
+  const bool lm = dm.kind == 1;
+  const size_t e = dm.dtype == 0 ? 4 : 2;
+  const size_t T = static_cast<size_t>(dm.n) * (lm ? dm.seq : 1);
+  const size_t Tmb = T / M;
+  const size_t d = dm.d, f = dm.ffn, H = lm ? dm.heads : 0, V = lm ? dm.vocab : 0;
+  const size_t D = depth > 0 && depth < M ? depth : M;
+  const size_t act = Tmb * d * e;  // one boundary tensor of one micro-batch
+  mm.boundary = static_cast<size_t>(K) * D * act + D * act + (lm ? static_cast<size_t>(M) * act : 0) + 2 * act +
+                2 * static_cast<size_t>(K) * act;
+  const size_t a = lm ? e * (8 * d + 2 * f) + 16 + 4 * H : e * (2 * d + 2 * f) + 8;
+  mm.cell = remat ? static_cast<size_t>(max_cell_layers) * Tmb * a : static_cast<size_t>(L) * M * Tmb * a;
+  const size_t lnp = 2 * ((Tmb + 7) / 8) * 2 * d * 4;  // LayerNorm partial sums: a row of 2d per 8 tokens, x2
+  mm.head = lm ? Tmb * (V * 4 + 2 * d * e + 8) + lnp : 0;
+  mm.grads = 3 * act + 2 * Tmb * (f + (lm ? 4 * d : 0)) * e + Tmb * std::max<size_t>(H, 1) * 4 + lnp;
+  mm.rows = T * 4;
+  // every region of the arena starts on a 256-byte boundary (TMA and vector
+  // access): at most 255 bytes of padding for each of the <= 13 regions of a
+  // layer's internals and the <= 48 others
+  mm.align = 256 * (13 * static_cast<size_t>(remat ? max_cell_layers : L * M) + 48);
+  mm.total = mm.boundary + mm.cell + mm.head + mm.grads + mm.rows + mm.align;
+  const size_t a_survey = e * ((lm ? 8 * d : 2 * d) + 2 * f) + 8;
+  mm.survey = static_cast<size_t>(K) * T * d * e +
+              (remat ? static_cast<size_t>(L) * Tmb * a_survey / static_cast<size_t>(K)
+                     : static_cast<size_t>(L) * T * a_survey) +
+              Tmb * V * 4 + 3 * act;
+  return mm;
 }
 
 }  // namespace gp

@@ -41,10 +41,12 @@ int stash_depth(int K, int M, int schedule);
 // micro-batch order), then its remaining backwards; the head is a stage after
 // the last cell.  The per-stage sequences are merged by a list scheduler that
 // issues, round by round, every stage's next op whose producers were issued in
-// earlier rounds and whose buffer slot (stash ring of depth stash_depth, input-
-// gradient ring of depth ring) its previous user has released.  Returns false
-// on a deadlock (cannot happen for ring >= 2 and depth >= min(M, K + 1)).
-bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops);
+// earlier rounds and whose buffer slot (stash ring of depth stash_depth, the
+// head's input ring of depth head_depth, input-gradient ring of depth ring)
+// its previous user has released.  head_depth <= 0: stash_depth.  Returns
+// false on a deadlock (cannot happen for ring >= 2, head_depth >= 1 and
+// depth >= min(M, K + 1)).
+bool issue_order(int K, int M, int schedule, int ring, std::vector<Op>& ops, int head_depth = 0);
 
 // Clock of an issue order: each stage runs its ops in order; an op starts when
 // its stage is free and its producers have finished (forward of cell k: t_f[k],
@@ -89,8 +91,9 @@ struct LaneLayout {
 };
 
 struct Workspace {
-  size_t stash = 0, stash_bytes = 0;        // (K+1) x depth boundary tensors [Tmb, d]
+  size_t stash = 0, stash_bytes = 0;        // K x depth cell inputs [Tmb, d], then head_depth head inputs
   int depth = 1;                            // stash ring depth (micro-batch m in slot m mod depth)
+  int head_depth = 1;                       // ring of the last cell's output (read only by the head)
   size_t dx0 = 0;                           // M x [Tmb, d]: gradient w.r.t. the embedding output (kind 1)
   size_t bgrad = 0;                         // K x ring x [Tmb, d]: gradient w.r.t. cell k's input
   int ring = 2;                             // depth of that ring: max(2, in flight per cell), at most M
@@ -116,11 +119,41 @@ struct Workspace {
   size_t check = 0, check_bytes = 0;         // re-materialisation check copies (debug)
   size_t act_bytes = 0;                      // activation bytes (everything but misc/check)
   size_t total = 0;
-  // the review's bound O(N + (L/K)(N/M)) per lane, with explicit constants
-  size_t bound_bytes = 0;
 };
 
 Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layers, bool remat, bool remat_check,
                          bool pipelined, int inflight = 1, int depth = 0 /* 0: M */);
+
+// The review's activation bound O(N + (L/K)(N/M)) ("Preliminaries 5:
+// re-materialisation") written out in bytes from the model's shapes alone
+// (nothing of the workspace layout enters it), for one device holding all K
+// cells.  T tokens per step, Tmb = T/M, e activation element bytes, D the
+// stash depth (M, or min(M, K+1) in the one-forward-one-backward order).
+//   boundary  the O(N) term: every cell's input for D micro-batches (K D Tmb d
+//             e), the head's output gradient for D micro-batches and, for the
+//             LM, the embedding's input gradient of all M (D Tmb d e + M Tmb d
+//             e), the head's input for two micro-batches and the gradient each
+//             cell receives from the next, double-buffered (2 Tmb d e + 2 K
+//             Tmb d e)
+//   cell      the O((L/K)(N/M)) term: one cell (Lc layers) of kept internals
+//             for one micro-batch, a bytes per token and layer (Transformer:
+//             e (8d + 2 ffn) + 16 + 4 heads; FFN block: e (2d + 2 ffn) + 8);
+//             without re-materialisation every layer of every micro-batch,
+//             L M Tmb a, the O(N L) the review starts from
+//   head      one micro-batch's fp32 logits and the final LayerNorm's output,
+//             gradient and statistics (LM only)
+//   grads     one layer's backward working set for one micro-batch: the
+//             gradient chain (3 Tmb d e), the FFN-hidden, attention-output and
+//             QKV gradients double-buffered (2 Tmb (ffn + 4d) e), attention
+//             row sums and LayerNorm partial sums
+//   rows      per-token losses (4 T)
+//   align     256-byte alignment of the arena's regions
+// survey: the same bound with the constants of the scoping survey's formula
+// (K T d e + (L/K) Tmb ((8d + 2 ffn) e + 8) + Tmb V 4 + 3 Tmb d e), reported
+// for comparison.
+struct MemoryModel {
+  size_t boundary = 0, cell = 0, head = 0, grads = 0, rows = 0, align = 0, total = 0, survey = 0;
+};
+MemoryModel review_memory_model(const Dims& dm, int L, int K, int M, int max_cell_layers, int depth, bool remat);
 
 }  // namespace gp

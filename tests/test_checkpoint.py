@@ -85,3 +85,22 @@ def test_damaged_or_foreign_files_are_refused(binding):
     # the good file still reads
     p2, v2, step = g.checkpoint_read(path)
     assert step == 7 and np.array_equal(p2, p) and np.array_equal(v2, v)
+
+
+def test_interrupted_write_leaves_the_previous_checkpoint(binding):
+    """A write that died before its rename leaves a truncated path.tmp behind:
+    the previous checkpoint at path still reads back whole, and the next write
+    replaces both."""
+    g = binding.GPipe.from_workload(WORKLOADS["tiny_ffn"])
+    p, v = _state(g, 3)
+    path = os.path.join(TMP, "interrupted.ck")
+    g.checkpoint_write(path, p, v, 5)
+    with open(path + ".tmp", "wb") as f:
+        f.write(open(path, "rb").read()[:1000])
+    p2, v2, step = g.checkpoint_read(path)
+    assert step == 5 and np.array_equal(p2, p) and np.array_equal(v2, v)
+    q, u = _state(g, 4)
+    g.checkpoint_write(path, q, u, 6)
+    q2, u2, step = g.checkpoint_read(path)
+    assert step == 6 and np.array_equal(q2, q) and np.array_equal(u2, u)
+    assert not os.path.exists(path + ".tmp")

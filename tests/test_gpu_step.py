@@ -18,7 +18,7 @@ import pytest
 
 from oracle import model as om
 from synth import KIND_LM, WORKLOADS, Workload, make_inputs
-from tests.gpu_util import rel
+from tests.gpu_util import assert_elementwise, local_scale, rel
 
 pytestmark = pytest.mark.gpu
 
@@ -52,21 +52,71 @@ def _run(b, w, inp, steps=1, keep_grads=True, options=(), K=None, M=None, cost=N
     return gp, st, p0, losses
 
 
-def _flat(w, d):
+# Element-wise bounds, next to the rel-L2 norms: every element of a group
+# (one parameter of one layer) within a |ref| + b rms(its row of ref), but for
+# at most a fraction of outliers.  bf16: activations are rounded to 8
+# significant bits at every store, through up to 96 layers; the measured
+# per-group rel-L2 is 0.3-2%, and against the row's scale the errors reach
+# 20% only for about one element in 10^4 (the attention weights of the deep
+# stacks, whose gradients go through the softmax's cancellations), so
+# a = b = 0.25 with 3 outliers in 10^4 allowed.  A zeroed or misplaced row of
+# 1024 elements puts most of its elements outside that bound, more than a
+# layer's allowance.  fp32: errors ~1e-6 of the row's scale, bounds at 1e-4
+# with none allowed.
+BF16_ELEM = (0.25, 0.25, 3e-4)
+FP32_ELEM = (1e-4, 1e-4, 0.0)
+
+
+def _offsets(w):
     from synth import param_specs
-    return np.concatenate([np.asarray(d[n], dtype=np.float64).ravel() for n, _, _ in param_specs(w)])
+    out, o = {}, 0
+    for name, shape, _ in param_specs(w):
+        out[name] = (o, shape)
+        o += int(np.prod(shape))
+    return out
 
 
-def _check_update(w, p0, g_ref, p_ref, p_gpu, v_ref, v_gpu, tol_w, tol_v, thresh):
-    dw_gpu = p_gpu - p0
-    dw_ref = p_ref - p0
-    mask = np.abs(g_ref) > thresh * np.sqrt(np.mean(g_ref ** 2))
-    assert mask.mean() > 0.5
-    assert rel(dw_gpu[mask], dw_ref[mask]) <= tol_w
+def _compare_step(w, st, p0, loss, ref_loss, ref_grads, loss_tol, grad_tol, group_tol, elem, upd_thresh):
+    """GPU step against the oracle's full-batch step, group by group (host
+    memory stays at one group at a time): the loss; every gradient group by
+    rel-L2 and element-wise; the whole gradient by rel-L2; and the RMSProp
+    update of every group from the oracle's gradient (v0 = 0), compared where
+    |g| > upd_thresh rms(g) (elsewhere the sign of a first RMSProp step is
+    not fixed by the oracle), and checked to be a valid step everywhere."""
+    assert abs(loss - ref_loss) <= loss_tol * abs(ref_loss), (loss, ref_loss)
+    offs = _offsets(w)
+    a, bb, frac = elem
+    num = den = 0.0
+    worst = (0.0, "")
     step_max = w.lr / math.sqrt(1 - w.decay)
-    assert np.all(np.abs(dw_gpu) <= step_max * (1 + 1e-3))
-    assert rel(p_gpu, p_ref) <= tol_w
-    assert rel(v_gpu[mask], v_ref[mask]) <= tol_v
+    masked = 0
+    for name, (o, shape) in offs.items():
+        n = int(np.prod(shape))
+        g = st.g32[o:o + n].double().cpu().numpy().reshape(shape)
+        gr = np.asarray(ref_grads[name], dtype=np.float64)
+        num += float(np.sum((g - gr) ** 2))
+        den += float(np.sum(gr ** 2))
+        r = rel(g, gr)
+        worst = max(worst, (r, name))
+        assert_elementwise(g, gr, a, bb, frac, f"gradient {name}")
+        # the update of this group from the oracle's gradient, where the
+        # gradient's sign is fixed by the bound above (|g| > upd_thresh times
+        # its row's rms): RMSProp's first step moves each such weight by
+        # lr g / (sqrt(1 - decay) |g| + eps), the same within fp32 rounding
+        p_init = np.asarray(p0[name], dtype=np.float64)
+        p_ref, v_ref = om.rmsprop({name: p_init}, {name: gr}, {name: np.zeros(shape)}, w.lr, w.decay, w.eps)
+        p_gpu = st.p32[o:o + n].double().cpu().numpy().reshape(shape)
+        v_gpu = st.v32[o:o + n].double().cpu().numpy().reshape(shape)
+        dw_gpu, dw_ref = p_gpu - p_init, p_ref[name] - p_init
+        mask = np.abs(gr) > upd_thresh * local_scale(gr)
+        masked += int(mask.sum())
+        if mask.any():
+            assert_elementwise(dw_gpu[mask], dw_ref[mask], 1e-2, 0.0, frac, f"update {name}")
+            assert rel(v_gpu[mask], v_ref[name][mask]) <= 4 * group_tol, f"RMSProp state {name}"
+        assert np.all(np.abs(dw_gpu) <= step_max * (1 + 1e-3)), name
+    assert math.sqrt(num / den) <= grad_tol
+    assert worst[0] <= group_tol, worst
+    assert masked > 0.3 * sum(int(np.prod(s)) for _, s in offs.values())
 
 
 def test_tiny_ffn_fp32_step_matches_oracle(b):
@@ -74,14 +124,7 @@ def test_tiny_ffn_fp32_step_matches_oracle(b):
     inp = make_inputs(w)
     gp, st, p0, (loss,) = _run(b, w, inp)
     ref = om.step(w, inp["params"], inp)
-    assert abs(loss - ref["loss"]) <= 1e-5 * abs(ref["loss"])
-    g = st.host(st.g32)
-    gref = _flat(w, ref["grads"])
-    assert rel(g, gref) <= 1e-5
-    for name, got in b.unpack(w, g).items():
-        assert rel(got, ref["grads"][name]) <= 1e-5, name
-    _check_update(w, p0, gref, _flat(w, ref["params"]), st.host(st.p32), _flat(w, ref["v"]), st.host(st.v32),
-                  1e-5, 1e-5, 1e-3)
+    _compare_step(w, st, inp["params"], loss, ref["loss"], ref["grads"], 1e-5, 1e-5, 1e-5, FP32_ELEM, 1e-2)
 
 
 def test_tiny_ffn_two_steps(b):
@@ -95,18 +138,17 @@ def test_tiny_ffn_two_steps(b):
     assert not np.any(st.host(st.g32))   # the update leaves the accumulator zeroed
 
 
-def _lm_parity(b, w, inp, loss_tol=1e-3, grad_tol=2e-2, group_tol=5e-2, **kw):
-    gp, st, p0, (loss,) = _run(b, w, inp, **kw)
-    ref = om.step(w, inp["params"], inp)
-    assert abs(loss - ref["loss"]) <= loss_tol * abs(ref["loss"]), (loss, ref["loss"])
-    g = st.host(st.g32)
-    gref = _flat(w, ref["grads"])
-    assert rel(g, gref) <= grad_tol
-    worst = max((rel(got, ref["grads"][name]), name) for name, got in b.unpack(w, g).items())
-    assert worst[0] <= group_tol, worst
-    _check_update(w, p0, gref, _flat(w, ref["params"]), st.host(st.p32), _flat(w, ref["v"]), st.host(st.v32),
-                  2e-2, 5e-2, 0.1)
-    return gp, st, ref
+def _lm_parity(b, w, inp, loss_tol=1e-3, grad_tol=2e-2, group_tol=5e-2, ref=None, **kw):
+    """A bf16 LM step against the oracle: loss, every gradient group (rel-L2
+    and element-wise), the whole gradient, and the update.  ref: the oracle's
+    (loss, grads) if already computed for these inputs."""
+    gp, st, _, (loss,) = _run(b, w, inp, **kw)
+    if ref is None:
+        ref_loss, ref_grads, _ = om.loss_and_grads(w, inp["params"], inp)
+    else:
+        ref_loss, ref_grads = ref
+    _compare_step(w, st, inp["params"], loss, ref_loss, ref_grads, loss_tol, grad_tol, group_tol, BF16_ELEM, 0.75)
+    return gp, st, {"loss": ref_loss, "grads": ref_grads}
 
 
 def test_small_lm_bf16_step_matches_oracle(b):
@@ -215,31 +257,104 @@ def test_lm_small_full_size_matches_oracle(b):
     _lm_parity(b, w, make_inputs(w))
 
 
-def test_lm_wide_layers_sub_batch(b):
-    """The wide workload's layers (L=24, d=1024, ffn=8192, seq=256, K=8) on a
-    sub-batch of N=2 sequences, M=2, which the fp64 oracle finishes in seconds."""
-    w = WORKLOADS["lm_wide"].replace(n=2, M=2)
+def test_lm_wide_all_layers_sub_batch(b):
+    """The wide workload (L=24, d=1024, ffn=8192, seq=256, K=8) with all its
+    layers on a sub-batch of N=4 sequences in M=4 micro-batches (the full
+    batch of 128 sequences is 36 GiB of fp64 activations on the host)."""
+    w = WORKLOADS["lm_wide"].replace(n=4, M=4)
     _lm_parity(b, w, make_inputs(w))
 
 
-def test_sweep_layers_single_micro_batch(b):
-    """The sweep workload's layer (d=1024, ffn=8192, seq=256) with K=8 cells and
-    the degenerate M=1 (no micro-batching), 16 layers on one sequence (the fp64
-    oracle's time grows with layers x tokens)."""
-    w = WORKLOADS["lm_sweep"].replace(L=16, n=1, M=1, K=8)
+def test_sweep_all_layers_two_partitions(b):
+    """The micro-batch-sweep workload's 48 layers (d=1024, ffn=8192, seq=256)
+    on a sub-batch of N=2 sequences in M=2 micro-batches, cut into K=2 and
+    K=8 cells: both match the one oracle step (the oracle has no K)."""
+    w = WORKLOADS["lm_sweep"].replace(n=2, M=2)
+    inp = make_inputs(w)
+    ref = None
+    for K in (2, 8):
+        _, _, r = _lm_parity(b, w.replace(K=K), inp, ref=ref)
+        ref = (r["loss"], r["grads"])
+
+
+def test_memory_scaling_all_layers_sub_batch(b):
+    """The memory-scaling workload's 96 layers (d=1024, ffn=8192, seq=512,
+    K=16 cells of 6 layers) on a sub-batch of N=2 sequences in M=2
+    micro-batches: gradients accumulate over micro-batches at the full depth."""
+    w = WORKLOADS["lm_deep"].replace(n=2, M=2)
     _lm_parity(b, w, make_inputs(w))
 
 
-def test_memory_scaling_layers_sub_batch(b):
-    """The memory-scaling workload's layer at seq 512 with K=16 cells (one layer
-    each) on one sequence, M=1."""
-    w = WORKLOADS["lm_deep"].replace(L=16, n=1, M=1)
-    _lm_parity(b, w, make_inputs(w))
+def _golden_losses():
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "full_batch_losses.json")
+    with open(path) as fh:
+        return json.load(fh)
 
 
+@pytest.mark.parametrize("name", ["lm_sweep", "lm_deep"])
+def test_full_batch_loss_matches_oracle(b, name):
+    """The full mini-batch (N=128 at L=48; N=256 at L=96, seq 512) in the
+    workload's own configuration: its loss and every sequence's loss against
+    the fp64 oracle's forward, stored by tests/golden/make_full_batch_losses.py
+    (a script that calls only the oracle)."""
+    w = WORKLOADS[name]
+    gold = _golden_losses()[name]
+    assert (gold["L"], gold["n"], gold["seq"], gold["seed"]) == (w.L, w.n, w.seq, w.seed)
+    inp = make_inputs(w)
+    gp, st, _, (loss,) = _run(b, w, inp, keep_grads=False, options=[(b.OPT_SKIP_UPDATE, 1)])
+    assert abs(loss - gold["loss"]) <= 1e-3 * abs(gold["loss"]), (loss, gold["loss"])
+    rows = gp.loss_rows(st.ws, w.n * w.seq, st.stream).reshape(w.n, w.seq)
+    per_seq = rows.astype(np.float64).sum(axis=1) * w.n   # rows are divided by N (seq - 1)
+    ref = np.array(gold["per_seq_loss"])
+    assert np.all(np.abs(per_seq - ref) <= 2e-3 * ref), np.max(np.abs(per_seq - ref) / ref)
+
+
+def test_memory_scaling_micro_batch_count_does_not_change_the_full_batch_step(b):
+    """The review's equivalence claim at the memory-scaling workload's full
+    size (N=256, seq 512, 96 layers): M=64 and M=16 micro-batches give the same
+    loss and gradients within the bf16 tolerance (one update equals the
+    full-batch step for any M).  Compared on the device."""
+    import torch
+    w = WORKLOADS["lm_deep"]
+    inp = make_inputs(w)
+    gp, st, _, (l64,) = _run(b, w, inp)
+    g64 = st.g32.clone()
+    del st
+    gp.close()
+    torch.cuda.empty_cache()
+    gp, st, _, (l16,) = _run(b, w, inp, M=16, options=[(b.OPT_PIPELINE, 0)])
+    assert abs(l16 - l64) <= 1e-4 * abs(l64), (l16, l64)
+    d = float(torch.linalg.vector_norm((st.g32 - g64).double()) / torch.linalg.vector_norm(g64.double()))
+    assert d <= 1e-2, d
+    offs = _offsets(w)
+    for name in ("l0.w_qkv", "l47.w1", "l95.w2", "emb", "l95.ln2_g"):
+        o, shape = offs[name]
+        n = int(np.prod(shape))
+        x, y = st.g32[o:o + n].double(), g64[o:o + n].double()
+        assert float(torch.linalg.vector_norm(x - y) / torch.linalg.vector_norm(y)) <= 2e-2, name
+
+
+REMAT_SHAPES = {
+    "small_lm": SMALL_LM,
+    # the wide layer (d=1024, ffn=8192, seq 256): 1024-token micro-batches take
+    # the persistent 128 x 256 GEMM, the separate bias-gradient reduction of
+    # the wide weight gradients and the seq-256 attention
+    "wide_layer": WORKLOADS["lm_wide"].replace(L=4, K=2, n=8, M=2),
+    # the memory-scaling layer (seq 512)
+    "deep_layer": WORKLOADS["lm_deep"].replace(L=4, K=2, n=4, M=2),
+}
+
+
+@pytest.mark.parametrize("shape", sorted(REMAT_SHAPES))
 @pytest.mark.parametrize("m_check", [0, 1])
-def test_rematerialised_internals_bit_identical(b, m_check):
-    w = SMALL_LM
+def test_rematerialised_internals_bit_identical(b, shape, m_check):
+    """Every internal the backward's re-computation produces (LayerNorm
+    outputs and statistics, QKV, attention output and log-sum-exp, the FFN
+    pre-activation and GELU output, layer outputs) equals the first forward's
+    byte for byte, for every cell, at micro-batch m_check."""
+    w = REMAT_SHAPES[shape]
     gp, st, _, _ = _run(b, w, make_inputs(w), options=[(b.OPT_REMAT_CHECK, m_check)])
     mism, err = gp.debug_counters(st.ws, st.stream)
     assert err == 0
