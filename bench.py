@@ -321,8 +321,9 @@ def attention_roofline(b, peaks, nseq, seq, heads, reps=50):
             "peak": peaks["bf16"], "peak_source": peaks["source"] + " (burst)"}
 
 
-EPI_NAMES = {0: "bf16 store epilogue (bias / residual)", 1: "bias + GELU epilogue", 2: "GELU-backward epilogue",
-             3: "fp32 TMA reduce-add epilogue (weight gradient, bias gradient)", 4: "fp32 store epilogue"}
+EPI_NAMES = {0: "bf16 store epilogue (bias)", 1: "bias + GELU epilogue", 2: "GELU-backward epilogue",
+             3: "fp32 TMA reduce-add epilogue (weight gradient, bias gradient)", 4: "fp32 store epilogue",
+             5: "fp32 residual epilogue (bias + fp32 residual, fp32 store)"}
 
 
 # Per-launch DRAM traffic (read + write bytes) of GEMMs of the step's shapes,
@@ -358,7 +359,7 @@ def live_roofline(b, gp, st, peaks, args):
     torch.cuda.synchronize()
     serial_ms = ev0.elapsed_time(ev1)
     classes = {}
-    for epi in (0, 1, 2, 3, 4):
+    for epi in sorted(EPI_NAMES):
         gp.set_option(b.OPT_KERNEL_TIMES, epi + 1)
         st.step(want_loss=False)
         st.step(want_loss=False)

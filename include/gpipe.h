@@ -200,24 +200,28 @@ int gpipe_issue_order(const gpipe_ctx* ctx, int32_t* ops_out, int count);
 int gpipe_memory_report(const gpipe_ctx* ctx, size_t* peak_act_bytes, size_t* model_bound_bytes);
 
 /* The terms of that bound, and the layout's total, in bytes (T tokens per
- * step, Tmb = T/M, e = activation element bytes, D = stash depth: M in the
- * GPipe order, min(M, K+1) with GPIPE_OPT_SCHEDULE 1):
- *   [0] boundary  O(N): every cell's input for D micro-batches, the head's
- *                 output gradient (D) and, for the LM, the embedding's input
- *                 gradient (M), two head inputs, and the gradient each cell
- *                 receives, double-buffered: (K D + D + M + 2 + 2K) Tmb d e
+ * step, Tmb = T/M, e = GEMM operand element bytes, r = 4: the residual stream
+ * and its gradient are kept in fp32, c = 2 (0 for the fp32 model): the bf16
+ * copy of a gradient that a GEMM reads, D = stash depth: M in the GPipe
+ * order, min(M, K+1) with GPIPE_OPT_SCHEDULE 1):
+ *   [0] boundary  O(N): every cell's input for D micro-batches (K D Tmb d r),
+ *                 the head's output gradient (D Tmb d (r + c)), for the LM the
+ *                 embedding's input gradient (M Tmb d r), two head inputs
+ *                 (2 Tmb d r), and the gradient each cell receives,
+ *                 double-buffered (2 K Tmb d (r + c))
  *   [1] cell      O((L/K)(N/M)): one cell of Lc layers of internals for one
- *                 micro-batch, Lc Tmb a, a = e (8d + 2 ffn) + 16 + 4 heads
- *                 (FFN block: e (2d + 2 ffn) + 8); without
+ *                 micro-batch, Lc Tmb a, a = e (6d + 2 ffn) + 2 d r + 16 + 4 heads
+ *                 (FFN block: e (d + 2 ffn) + d r + 8); without
  *                 re-materialisation L M Tmb a
  *   [2] head      one micro-batch's fp32 logits, final-LN output, gradient
  *                 and statistics, and its LayerNorm partial sums:
  *                 Tmb (4 V + 2 d e + 8) + 2 ceil(Tmb/8) 2d 4 (LM only)
  *   [3] grads     one layer's backward working set for one micro-batch
  *   [4] rows      per-token losses, 4 T
- *   [5] align     256-byte alignment of the arena's regions, 256 (13 Lc + 48)
+ *   [5] align     256-byte alignment of the arena's regions, 256 (13 Lc + 56)
  *   [6] total     [0] + ... + [5]  (= model_bound_bytes)
- *   [7] survey    the scoping survey's concrete form of the same bound:
+ *   [7] survey    the scoping survey's concrete form of the same bound, all
+ *                 activations of e bytes:
  *                 K T d e + (L/K) Tmb ((8d + 2 ffn) e + 8) + 4 Tmb V + 3 Tmb d e
  *   [8] layout    the workspace's activation region (= peak_act_bytes)
  * Writes min(count, GPIPE_MEMORY_TERMS) values; returns GPIPE_MEMORY_TERMS
@@ -255,7 +259,7 @@ enum {
   GPIPE_OPT_TRACE = 9,       /* [0] 1: write the GPU clock (ns) when every cell (and
                                 the head) finishes each micro-batch's forward and
                                 backward; read with gpipe_trace                      */
-  GPIPE_OPT_KERNEL_TIMES = 10, /* [0] e+1: bracket every GEMM launch of the step whose
+  GPIPE_OPT_KERNEL_TIMES = 10, /* [0] e+1 (e <= 5): bracket every GEMM launch of the step whose
                                 epilogue is e (GPIPE_EPI_* of gpipe_ops.h) with timing
                                 events on the stream it is launched on (recorded as
                                 event nodes of the step's graph); read with

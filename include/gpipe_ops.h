@@ -30,7 +30,8 @@ enum {
   GPIPE_EPI_BIAS_GELU = 1, /* C = z = acc + bias[n];  C2 = GELU(z)  (exact erf)    */
   GPIPE_EPI_GELU_BWD = 2,  /* C = acc * GELU'(aux[m,n])                              */
   GPIPE_EPI_ACC_F32 = 3,   /* C (fp32) += acc                                        */
-  GPIPE_EPI_STORE_F32 = 4  /* C (fp32) = acc                                         */
+  GPIPE_EPI_STORE_F32 = 4, /* C (fp32) = acc                                         */
+  GPIPE_EPI_RESID_F32 = 5  /* C (fp32) = (acc + bias[n]) + resid (fp32)[m,n]         */
 };
 
 /* C[m,n] = epilogue( sum_k A(m,k) B(n,k) ), 0 <= m < M, 0 <= n < N.
@@ -45,7 +46,8 @@ enum {
  * gradient dY^T X, computed by the same launch).  resid may be NULL.
  * dtype 1 runs the tcgen05/TMEM tensor-core kernel fed by TMA and needs every
  * leading dimension a multiple of 8 elements and 16-byte aligned bases; it is
- * built for (1,1) with STORE, BIAS_GELU, STORE_F32, ACC_F32; (1,0) with STORE,
+ * built for (1,1) with STORE, BIAS_GELU, STORE_F32, ACC_F32, RESID_F32 (resid
+ * required, fp32 like C); (1,0) with STORE,
  * GELU_BWD, ACC_F32; (0,0) with STORE, ACC_F32 (others: GPIPE_ERR_UNSUPPORTED).
  * dtype 0 runs an fp32 FFMA kernel (any layout and epilogue).
  * Requires M, N, K >= 1. */
@@ -107,18 +109,18 @@ int gpipe_op_layernorm_bwd_noalloc(int dtype, int rows, int d, const void* dy, c
 int gpipe_op_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy,
                     float* out_acc, float* scratch, void* stream);
 
-/* Causal multi-head attention forward, bf16, head width 64, scale 1/8.
+/* Causal multi-head attention forward, bf16, head width 64, scale 1/8, on
+ * the tcgen05 tensor cores (S and O accumulate in tensor memory).
  * qkv [nseq*seq, 3*heads*64] (query | key | value column blocks), output
  * o [nseq*seq, heads*64], lse [nseq*seq, heads] fp32 natural-log
- * log-sum-exp of the scaled scores.  seq % 64 == 0. */
+ * log-sum-exp of the scaled scores.  seq % 64 == 0, nseq * seq <= 2^30. */
 int gpipe_op_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o,
                            float* lse, void* stream);
 
 /* Backward: dqkv [nseq*seq, 3*heads*64] gets dQ | dK | dV.  dvec is fp32
- * [nseq*seq, heads] output of rowsum(dO o O).  One launch: its dQ blocks and
- * its dK/dV blocks each compute what they need of rowsum(dO o O) themselves
- * (same arithmetic), so they run side by side; no atomics, so results are
- * bit-reproducible.  nseq <= 32767. */
+ * [nseq*seq, heads]: rowsum(dO o O), written first by a small kernel, then
+ * read by one launch whose dQ blocks and dK/dV blocks run side by side; no
+ * atomics, so results are bit-reproducible.  nseq <= 32767. */
 int gpipe_op_attention_bwd(int nseq, int seq, int heads, const void* qkv, const void* o,
                            const void* dout, const float* lse, float* dvec, void* dqkv,
                            void* stream);
@@ -173,7 +175,9 @@ int gpipe_op_cast_bf16(size_t n, const float* src, void* dst, void* stream);
  * the GPU is bounded (2 s); one that gives up, or a kernel that meets an
  * invalid input it skips (a token id outside [0, vocab)), sets the device error
  * word of the current device: 1-4 a bounded wait (TMA producer, MMA issuer,
- * epilogue, exit drain), 5 an invalid token id, 6 this probe.
+ * epilogue, exit drain), 5 an invalid token id, 6 this probe, 7 a kernel whose
+ * shared memory was less aligned than its swizzled tiles need (its work is
+ * skipped).
  *   gpipe_op_wait_probe: launches one CTA whose bounded wait on an mbarrier
  *     that nothing completes gives up after the limit and sets code 6; the
  *     kernel returns normally and the context stays usable.

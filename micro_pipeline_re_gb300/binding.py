@@ -33,7 +33,7 @@ OPT_LOGIT_CLIP = 16
 OPT_LAYER_TIMES = 17
 SCHEDULE_GPIPE, SCHEDULE_1F1B = 0, 1
 OP_FWD, OP_HEAD, OP_BWD = 0, 1, 2
-EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32 = 0, 1, 2, 3, 4
+EPI_STORE, EPI_BIAS_GELU, EPI_GELU_BWD, EPI_ACC_F32, EPI_STORE_F32, EPI_RESID_F32 = 0, 1, 2, 3, 4, 5
 
 
 class GpipeError(RuntimeError):

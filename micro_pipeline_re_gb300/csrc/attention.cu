@@ -15,15 +15,14 @@
 // grows, write P = exp2(S - m) as bf16 and add its row sum; then
 // O += P V.  Saves the natural-log log-sum-exp per (row, head).
 //
-// Backward, without atomics (bit-reproducible), one launch of two CTA kinds:
-//   dQ CTA    per (128-query block, head, sequence): D = rowsum(dO o O) per
-//             row (also written out), then for every visible 64-key block
-//             S = Q K^T, dP = dO V^T, P = exp2(S - LSE), dS = P o (dP - D),
-//             dQ += dS K.
+// Backward, without atomics (bit-reproducible): D = rowsum(dO o O) for every
+// (row, head) by a small kernel, then one launch of two CTA kinds:
+//   dQ CTA    per (128-query block, head, sequence): for every visible
+//             64-key block S = Q K^T, dP = dO V^T, P = exp2(S - LSE),
+//             dS = P o (dP - D), dQ += dS K.
 //   dK/dV CTA per (128-key block, head, sequence): for every 64-query block
 //             that sees it, S^T = K Q^T, dP^T = V dO^T, P^T, dS^T (with the
-//             same D, computed by the same arithmetic), dV += P^T dO,
-//             dK += dS^T Q.
+//             same D), dV += P^T dO, dK += dS^T Q.
 //
 // Shared-memory tiles (1024-B aligned, 128-B rows, 16-B unit u of row r at
 // r*128 + ((u ^ (r&7)) * 16)):
@@ -74,6 +73,27 @@ __device__ __forceinline__ void ld_row32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
 }
 
+// Load 32 * N fp32 columns of this thread's lane from the column addresses
+// a[0..N-1]: every load is issued before the one wait, so their latencies
+// overlap (a TMEM load takes a few hundred cycles to return).
+template <int N>
+__device__ __forceinline__ void ld_rows(const uint32_t* a, float* v) {
+  uint32_t u[32 * N];
+#pragma unroll
+  for (int c = 0; c < N; ++c) tmem_ld32(a[c], u + 32 * c);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32 * N; ++i) v[i] = __uint_as_float(u[i]);
+}
+
+// 2^x on the special-function unit (ex2.approx, relative error about 2^-22;
+// 2^-inf = 0): the softmax's exponentials.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Write 32 values of row r as bf16 into a swizzled tile at units u0..u0+3.
 __device__ __forceinline__ void st_row32_bf16(uint8_t* tile, int r, int u0, const float* v) {
 #pragma unroll
@@ -122,20 +142,52 @@ __device__ __forceinline__ float row_dot64(const __nv_bfloat16* o, const __nv_bf
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
-constexpr int FWD_SMEM = 1024 + 6 * T128 + 128;  // Q, K, V x2, P (2 sub-tiles), barriers
+// Warps 0-3 (128 threads) own the rows; warp 4's lane 0 issues every TMA copy
+// and every MMA, so that waiting on a copy never stalls the softmax.  Per key
+// block j, hand-offs through mbarriers:
+//   issuer:  S_j = Q K_j^T (once the rows have read S_{j-1} out of TMEM)
+//            -> commit bs;  K_{j+1} into the other K buffer;
+//            O += P_j V_j (once the rows wrote P_j and rescaled O, and
+//            O += P_{j-1} V_{j-1} is done) -> commit bo;  V_{j+1}.
+//   rows:    wait bs; read S_j; arrive bsc (S consumed); the running max;
+//            wait bo (the previous O product, which reads P and writes O);
+//            rescale O; write P_j; arrive bp.
+// So S_{j+1} computes while the rows work on block j.
+constexpr int FWD_THREADS = 160;
+// Q, K x2, V x2, P (2 sub-tiles), barriers.  No slack for aligning the base:
+// with no static shared memory the dynamic window starts 1024-byte aligned
+// (checked at run time), and without the slack two CTAs fit on an SM.
+constexpr int FWD_SMEM = 7 * T128 + 128;
 
-__global__ void __launch_bounds__(128) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq,
-                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                                                       int seq, int heads, int* err) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
+// Bounded wait that gives up at once after any earlier give-up in the CTA.
+__device__ __forceinline__ bool await(uint64_t* bar, uint32_t parity, int* err, int code, volatile int* abort) {
+  if (*abort) return false;
+  if (mbar_wait_bounded(bar, parity, err, code)) return true;
+  *abort = 1;
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(FWD_THREADS) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq,
+                                                               __nv_bfloat16* __restrict__ out,
+                                                               float* __restrict__ lse, int seq, int heads, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (reinterpret_cast<uintptr_t>(smem_raw) & 1023u) {  // the tiles' swizzle needs 1024-byte alignment
+    if (threadIdx.x == 0) atomicExch(err, DERR_ALIGN);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   uint8_t* sQ = sm;
-  uint8_t* sK = sm + T128;
-  uint8_t* sV = sm + 2 * T128;  // two buffers
-  uint8_t* sP = sm + 4 * T128;  // keys 0..63 | keys 64..127
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 6 * T128);
-  uint64_t *bq = bar, *bk = bar + 1, *bv = bar + 2, *bs = bar + 4, *bo = bar + 5;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
+  uint8_t* sK = sm + T128;      // two buffers
+  uint8_t* sV = sm + 3 * T128;  // two buffers
+  uint8_t* sP = sm + 5 * T128;  // keys 0..63 | keys 64..127
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 7 * T128);
+  uint64_t *bq = bar, *bk = bar + 1, *bv = bar + 3, *bs = bar + 5, *bsc = bar + 6, *bp = bar + 7, *bo = bar + 8,
+           *bfin = bar + 9;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 10);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int r = threadIdx.x, warp = r >> 5;
   const int nqb = (seq + 127) / 128;
@@ -145,11 +197,16 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __grid_constant__ C
   const int row0 = b * seq;  // the sequence's first row
   const int q0 = qb * 128;
   const int nkb = qb + 1;    // key blocks 0..qb (the last one holds the diagonal)
-  const int qi = q0 + r;     // this thread's query
+  const int qi = q0 + r;     // the query of row thread r (r < 128)
 
   if (r == 0) {
     prefetch_tmap(&tq);
     for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    mbar_init(bsc, 128);
+    mbar_init(bp, 128);
+    mbar_init(bo, 1);
+    mbar_init(bfin, 1);
+    *abort = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -161,128 +218,136 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t tS = tmem, tO = tmem + 128;
 
-  int nk_issued = 0, nv_issued[2] = {0, 0};
-  if (r == 0) {
-    mbar_arrive_expect_tx(bq, T128);
-    tma_load_2d(sQ, &tq, h * HD, row0 + q0, bq);
-    mbar_arrive_expect_tx(bk, T128);
-    tma_load_2d(sK, &tq, D + h * HD, row0, bk);
-    nk_issued = 1;
-    for (int j = 0; j < 2 && j < nkb; ++j) {
-      mbar_arrive_expect_tx(&bv[j], T128);
-      tma_load_2d(sV + j * T128, &tq, 2 * D + h * HD, row0 + j * 128, &bv[j]);
-      nv_issued[j] = 1;
-    }
-  }
-  float m = -INFINITY, l = 0.f;
-  bool ok = true;
-  constexpr uint32_t idS = mma_idesc_bf16(128, 128, false, false);
-  constexpr uint32_t idO = mma_idesc_bf16(128, 64, false, true);
-  for (int j = 0; j < nkb; ++j) {
-    if (r == 0) {  // S = Q K_j^T
-      bool w = (j > 0 || mbar_wait_bounded(bq, 0, err, DERR_MMA_WAIT)) &&
-               mbar_wait_bounded(bk, j & 1, err, DERR_MMA_WAIT);
-      if (w) {
+  if (warp == 4) {
+    if (r == 128) {  // ---- issuer ----
+      constexpr uint32_t idS = mma_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idO = mma_idesc_bf16(128, 64, false, true);
+      int nk[2] = {0, 0}, nv[2] = {0, 0};
+      mbar_arrive_expect_tx(bq, T128);
+      tma_load_2d(sQ, &tq, h * HD, row0 + q0, bq);
+      for (int j = 0; j < 2 && j < nkb; ++j) {
+        mbar_arrive_expect_tx(&bk[j], T128);
+        tma_load_2d(sK + j * T128, &tq, D + h * HD, row0 + j * 128, &bk[j]);
+        ++nk[j];
+        mbar_arrive_expect_tx(&bv[j], T128);
+        tma_load_2d(sV + j * T128, &tq, 2 * D + h * HD, row0 + j * 128, &bv[j]);
+        ++nv[j];
+      }
+      for (int j = 0; j < nkb; ++j) {
+        const int kb = j & 1;
+        if (j == 0 && !await(bq, 0, err, DERR_MMA_WAIT, abort)) break;
+        if (!await(&bk[kb], (j >> 1) & 1, err, DERR_MMA_WAIT, abort)) break;
+        if (j > 0 && !await(bsc, (j - 1) & 1, err, DERR_MMA_WAIT, abort)) break;  // S_{j-1} read out
         tc_fence_after();
-        const uint32_t q = smem_u32(sQ), k = smem_u32(sK);
+        {
+          const uint32_t q = smem_u32(sQ), k = smem_u32(sK + kb * T128);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(q, kk), kdesc(k, kk), idS, kk ? 1u : 0u);
-        tc_commit(bs);  // also covers the previous block's O += P V
+          for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(q, kk), kdesc(k, kk), idS, kk ? 1u : 0u);
+          tc_commit(bs);
+        }
+        if (j >= 1 && j + 1 < nkb) {  // K buffer of block j-1: its product S_{j-1} is done
+          const int nb = (j + 1) & 1;
+          mbar_arrive_expect_tx(&bk[nb], T128);
+          tma_load_2d(sK + nb * T128, &tq, D + h * HD, row0 + (j + 1) * 128, &bk[nb]);
+          ++nk[nb];
+        }
+        if (!await(bp, j & 1, err, DERR_MMA_WAIT, abort)) break;              // P_j written, O rescaled
+        if (j > 0 && !await(bo, (j - 1) & 1, err, DERR_MMA_WAIT, abort)) break;  // O += P_{j-1} V_{j-1} done
+        if (j >= 1 && j + 1 < nkb) {  // V buffer of block j-1 is free
+          const int nb = (j + 1) & 1;
+          mbar_arrive_expect_tx(&bv[nb], T128);
+          tma_load_2d(sV + nb * T128, &tq, 2 * D + h * HD, row0 + (j + 1) * 128, &bv[nb]);
+          ++nv[nb];
+        }
+        if (!await(&bv[kb], (j >> 1) & 1, err, DERR_MMA_WAIT, abort)) break;
+        tc_fence_after();
+        {
+          const uint32_t p = smem_u32(sP), v = smem_u32(sV + kb * T128);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_f16(tO, kdesc(p + (kk >> 2) * T128, kk & 3), mndesc(v, kk), idO, (j | kk) ? 1u : 0u);
+          tc_commit(bo);
+        }
       }
+      // no copy may still be landing, and no product still running, when the CTA exits
+      tc_commit(bfin);
+      mbar_wait_bounded(bfin, 0, err, DERR_DRAIN_WAIT);
+      for (int bb = 0; bb < 2; ++bb) {
+        if (nk[bb]) mbar_wait_bounded(&bk[bb], (nk[bb] - 1) & 1, err, DERR_DRAIN_WAIT);
+        if (nv[bb]) mbar_wait_bounded(&bv[bb], (nv[bb] - 1) & 1, err, DERR_DRAIN_WAIT);
+      }
+      mbar_wait_bounded(bq, 0, err, DERR_DRAIN_WAIT);
     }
-    ok = mbar_wait_bounded(bs, j & 1, err, DERR_ACC_WAIT);
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    tc_fence_after();
-    if (r == 0) {
-      if (j + 1 < nkb) {  // K buffer free: S_j is done
-        mbar_arrive_expect_tx(bk, T128);
-        tma_load_2d(sK, &tq, D + h * HD, row0 + (j + 1) * 128, bk);
-        ++nk_issued;
-      }
-      if (j >= 1 && j + 1 < nkb) {  // V buffer of block j-1 free: O += P_{j-1} V_{j-1} is done
-        const int vb = (j + 1) & 1;
-        mbar_arrive_expect_tx(&bv[vb], T128);
-        tma_load_2d(sV + vb * T128, &tq, 2 * D + h * HD, row0 + (j + 1) * 128, &bv[vb]);
-        ++nv_issued[vb];
-      }
-    }
-    const bool diag = j == qb;
-    // pass 1: row maximum of the scaled scores (log2 domain)
-    float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float s[32];
-      ld_row32(tS + lane + 32 * c, s);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const bool vis = !diag || (j * 128 + 32 * c + i <= qi);
-        mx = fmaxf(mx, vis ? s[i] * kScaleLog2 : -INFINITY);
-      }
-    }
-    const float mn = fmaxf(m, mx);
-    const float alpha = exp2f(m - mn);  // 0 for the first block
-    m = mn;
-    // rescale this row of O (warp-uniform: tcgen05 loads/stores are per warp)
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tO + lane + 32 * c, u);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-        tmem_st32(tO + lane + 32 * c, u);
-      }
-      tmem_st_wait();
-    }
-    // pass 2: P = exp2(s - m) as bf16 into shared memory, and its row sum
-    float rs = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float s[32];
-      ld_row32(tS + lane + 32 * c, s);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const bool vis = !diag || (j * 128 + 32 * c + i <= qi);
-        const float p = vis ? exp2f(s[i] * kScaleLog2 - m) : 0.f;
-        s[i] = p;
-        rs += p;
-      }
-      st_row32_bf16(sP + (c >> 1) * T128, r, (c & 1) * 4, s);
-    }
-    l = l * alpha + rs;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (r == 0) {  // O += P V_j
+  } else {  // ---- rows ----
+    const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkb && ok; ++j) {
+      ok = __all_sync(0xffffffffu, await(bs, j & 1, err, DERR_ACC_WAIT, abort));
+      if (!ok) break;
       tc_fence_after();
-      const int vb = j & 1;
-      if (mbar_wait_bounded(&bv[vb], (j >> 1) & 1, err, DERR_MMA_WAIT)) {
-        const uint32_t p = smem_u32(sP), v = smem_u32(sV + vb * T128);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tO, kdesc(p + (kk >> 2) * T128, kk & 3), mndesc(v, kk), idO, (j | kk) ? 1u : 0u);
+      const bool diag = j == qb;
+      // this row of S, all 128 columns in one round trip
+      float sv[128];
+      {
+        const uint32_t a[4] = {tS + lane, tS + lane + 32, tS + lane + 64, tS + lane + 96};
+        ld_rows<4>(a, sv);
       }
+      tc_fence_before();
+      mbar_arrive1(bsc);  // S may be overwritten by the next block's product
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        const bool vis = !diag || (j * 128 + i <= qi);
+        sv[i] = vis ? sv[i] * kScaleLog2 : -INFINITY;
+        mx = fmaxf(mx, sv[i]);
+      }
+      const float mn = fmaxf(m, mx);
+      const float alpha = fast_exp2(m - mn);  // 0 for the first block
+      m = mn;
+      if (j > 0) {  // the previous O product reads P and writes O
+        ok = __all_sync(0xffffffffu, await(bo, (j - 1) & 1, err, DERR_ACC_WAIT, abort));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {  // warp-uniform: tcgen05 loads/stores are per warp
+          uint32_t u[64];
+          tmem_ld32(tO + lane, u);
+          tmem_ld32(tO + lane + 32, u + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(tO + lane, u);
+          tmem_st32(tO + lane + 32, u + 32);
+          tmem_st_wait();
+        }
+      }
+      // P = exp2(s - m) as bf16 into shared memory, and its row sum
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float* pc = sv + 32 * c;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          pc[i] = fast_exp2(pc[i] - m);
+          rs += pc[i];
+        }
+        st_row32_bf16(sP + (c >> 1) * T128, r, (c & 1) * 4, pc);
+      }
+      l = l * alpha + rs;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive1(bp);
     }
-  }
-  if (r == 0) tc_commit(bo);  // every product issued above
-  const bool okd = __syncthreads_and(mbar_wait_bounded(bo, 0, err, DERR_ACC_WAIT));
-  tc_fence_after();
-  if (ok && okd) {
-    // rows past the sequence end (a last block of 64) are computed, not stored
-    const int64_t row = static_cast<int64_t>(row0) + qi;
-    store_row64(tO + lane, out + row * D + h * HD, 1.0f / l, qi < seq);
-    if (qi < seq) lse[row * heads + h] = (m + log2f(l)) * kLn2;
-  }
-  if (r == 0) {  // no copy may still be landing when the CTA exits
-    if (nk_issued) mbar_wait_bounded(bk, (nk_issued - 1) & 1, err, DERR_DRAIN_WAIT);
-    for (int vb = 0; vb < 2; ++vb)
-      if (nv_issued[vb]) mbar_wait_bounded(&bv[vb], (nv_issued[vb] - 1) & 1, err, DERR_DRAIN_WAIT);
-    mbar_wait_bounded(bq, 0, err, DERR_DRAIN_WAIT);
+    if (ok) ok = __all_sync(0xffffffffu, await(bo, (nkb - 1) & 1, err, DERR_ACC_WAIT, abort));
+    tc_fence_after();
+    if (ok) {
+      // rows past the sequence end (a last block of 64) are computed, not stored
+      const int64_t row = static_cast<int64_t>(row0) + qi;
+      store_row64(tO + lane, out + row * D + h * HD, 1.0f / l, qi < seq);
+      if (qi < seq) lse[row * heads + h] = (m + log2f(l)) * kLn2;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -296,6 +361,19 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __grid_constant__ C
 // ---------------------------------------------------------------------------
 // Backward
 // ---------------------------------------------------------------------------
+// D = rowsum(dO o O) for every (row, head), once, before the backward kernel
+// (stream order): both kinds of backward CTA read the same values.
+__global__ void __launch_bounds__(256) attn_dvec_kernel(const __nv_bfloat16* __restrict__ out,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ dvec, int64_t n, int heads) {
+  griddep_wait();
+  griddep_launch();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (row, head) = (i / heads, i % heads)
+  if (i >= n) return;
+  const int64_t off = i * HD;  // row * heads * 64 + head * 64
+  dvec[i] = row_dot64(out + off, dout + off);
+}
+
 // dQ CTA: Q, dO (128 rows), K and V blocks of 64 keys (two buffers each), dS
 // (128 x 64).  dK/dV CTA: K, V (128 rows), Q and dO blocks of 64 queries (two
 // buffers each), P^T and dS^T (128 x 64), LSE and D of the query block.
@@ -305,9 +383,8 @@ constexpr int BWD_BAR = BWD_LD + 4 * 64 * 4;
 constexpr int BWD_SMEM = 1024 + BWD_BAR + 128;
 
 __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, const CUtensorMap* td128,
-                            const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
-                            const float* __restrict__ lse, float* __restrict__ dvec, __nv_bfloat16* __restrict__ dqkv,
-                            int seq, int heads, int b, int* err, uint8_t* sm) {
+                            const float* __restrict__ lse, const float* __restrict__ dvec,
+                            __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int b, int* err, uint8_t* sm) {
   uint8_t* sQ = sm;
   uint8_t* sdO = sm + T128;
   uint8_t* sK = sm + 2 * T128;        // two 64-row buffers
@@ -364,8 +441,7 @@ __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, c
   if (qi < seq) {
     const int64_t row = static_cast<int64_t>(row0) + qi;
     L2 = lse[row * heads + h] * kLog2e;
-    Dr = row_dot64(out + row * D + h * HD, dout + row * D + h * HD);
-    dvec[row * heads + h] = Dr;
+    Dr = dvec[row * heads + h];
   }
   bool ok = true;
   constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
@@ -396,18 +472,18 @@ __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, c
       tma_load_2d(sV + nb * T64, tq64, 2 * D + h * HD, row0 + (j + 1) * 64, &bkv[nb]);
       ++nkv_issued[nb];
     }
+    {
+      float v[128];  // S (64 columns), then dP (64 columns), one round trip
+      const uint32_t a[4] = {tS + lane, tS + lane + 32, tP + lane, tP + lane + 32};
+      ld_rows<4>(a, v);
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float s[32], dp[32];
-      ld_row32(tS + lane + 32 * c, s);
-      ld_row32(tP + lane + 32 * c, dp);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const bool vis = j * 64 + 32 * c + i <= qi;
-        const float p = vis ? exp2f(s[i] * kScaleLog2 - L2) : 0.f;
-        s[i] = p * (dp[i] - Dr);  // dS
+      for (int i = 0; i < 64; ++i) {
+        const bool vis = j * 64 + i <= qi;
+        const float p = vis ? fast_exp2(v[i] * kScaleLog2 - L2) : 0.f;
+        v[i] = p * (v[64 + i] - Dr);  // dS
       }
-      st_row32_bf16(sdS, r, c * 4, s);
+      st_row32_bf16(sdS, r, 0, v);
+      st_row32_bf16(sdS, r, 4, v + 32);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -440,9 +516,8 @@ __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, c
 }
 
 __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, const CUtensorMap* td64,
-                             const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
-                             const float* __restrict__ lse, __nv_bfloat16* __restrict__ dqkv, int seq, int heads,
-                             int b, int* err, uint8_t* sm) {
+                             const float* __restrict__ lse, const float* __restrict__ dvec,
+                             __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int b, int* err, uint8_t* sm) {
   uint8_t* sK = sm;
   uint8_t* sV = sm + T128;
   uint8_t* sQ = sm + 2 * T128;     // two 64-row buffers
@@ -500,13 +575,21 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
   bool ok = true;
   constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
   constexpr uint32_t idKV = mma_idesc_bf16(128, 64, false, true);
+  // LSE (log2 domain) and D of the 64 queries of a block: block i0's now,
+  // each next block's read one iteration ahead (its loads in flight while
+  // this block's products run)
+  if (r < 64) {
+    const int64_t row = static_cast<int64_t>(row0) + i0 * 64 + r;
+    sL[r] = lse[row * heads + h] * kLog2e;
+    sD[r] = dvec[row * heads + h];
+  }
   for (int t = 0; t < niter; ++t) {
     const int i = i0 + t, qbuf = t & 1;
-    // LSE (log2 domain) and D of the 64 queries of block i
-    if (r < 64) {
-      const int64_t row = static_cast<int64_t>(row0) + i * 64 + r;
-      sL[qbuf * 64 + r] = lse[row * heads + h] * kLog2e;
-      sD[qbuf * 64 + r] = row_dot64(out + row * D + h * HD, dout + row * D + h * HD);
+    float nL = 0.f, nD = 0.f;
+    if (r < 64 && t + 1 < niter) {
+      const int64_t row = static_cast<int64_t>(row0) + (i + 1) * 64 + r;
+      nL = lse[row * heads + h] * kLog2e;
+      nD = dvec[row * heads + h];
     }
     if (r == 0) {  // S^T = K Q_i^T, dP^T = V dO_i^T
       bool w = (t > 0 || mbar_wait_bounded(bkv, 0, err, DERR_MMA_WAIT)) &&
@@ -535,21 +618,25 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
     }
     const float* L = sL + qbuf * 64;
     const float* Dq = sD + qbuf * 64;
+    {
+      float v[128];  // S^T (64 columns), then dP^T (64 columns), one round trip
+      const uint32_t a[4] = {tS + lane, tS + lane + 32, tP + lane, tP + lane + 32};
+      ld_rows<4>(a, v);
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float s[32], dp[32];
-      ld_row32(tS + lane + 32 * c, s);
-      ld_row32(tP + lane + 32 * c, dp);
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const int q = 32 * c + x;
+      for (int q = 0; q < 64; ++q) {
         const bool vis = i * 64 + q >= kr;
-        const float p = vis ? exp2f(s[x] * kScaleLog2 - L[q]) : 0.f;
-        s[x] = p;                   // P^T
-        dp[x] = p * (dp[x] - Dq[q]);  // dS^T
+        const float p = vis ? fast_exp2(v[q] * kScaleLog2 - L[q]) : 0.f;
+        v[q] = p;                          // P^T
+        v[64 + q] = p * (v[64 + q] - Dq[q]);  // dS^T
       }
-      st_row32_bf16(sPt, r, c * 4, s);
-      st_row32_bf16(sdSt, r, c * 4, dp);
+      st_row32_bf16(sPt, r, 0, v);
+      st_row32_bf16(sPt, r, 4, v + 32);
+      st_row32_bf16(sdSt, r, 0, v + 64);
+      st_row32_bf16(sdSt, r, 4, v + 96);
+    }
+    if (r < 64 && t + 1 < niter) {  // the next block's, published by the barriers below
+      sL[(qbuf ^ 1) * 64 + r] = nL;
+      sD[(qbuf ^ 1) * 64 + r] = nD;
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -591,18 +678,16 @@ __global__ void __launch_bounds__(128) attn_bwd_kernel(const __grid_constant__ C
                                                        const __grid_constant__ CUtensorMap tq128,
                                                        const __grid_constant__ CUtensorMap td64,
                                                        const __grid_constant__ CUtensorMap td128,
-                                                       const __nv_bfloat16* __restrict__ out,
-                                                       const __nv_bfloat16* __restrict__ dout,
-                                                       const float* __restrict__ lse, float* __restrict__ dvec,
+                                                       const float* __restrict__ lse, const float* __restrict__ dvec,
                                                        __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int nseq,
                                                        int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int z = blockIdx.z;
   if (z < nseq)
-    attn_bwd_dq(&tq64, &tq128, &td128, out, dout, lse, dvec, dqkv, seq, heads, z, err, sm);
+    attn_bwd_dq(&tq64, &tq128, &td128, lse, dvec, dqkv, seq, heads, z, err, sm);
   else
-    attn_bwd_dkv(&tq64, &tq128, &td64, out, dout, lse, dqkv, seq, heads, z - nseq, err, sm);
+    attn_bwd_dkv(&tq64, &tq128, &td64, lse, dvec, dqkv, seq, heads, z - nseq, err, sm);
   griddep_launch();
 }
 
@@ -680,8 +765,8 @@ int launch_attention_fwd(int nseq, int seq, int heads, const void* qkv, void* o,
   if (!amake_tmap(&tq, qkv, 3 * D, rows, 3 * D, 128))
     return set_error(GPIPE_ERR_CUDA, "attention_fwd: tensor map creation failed");
   dim3 grid((seq + 127) / 128, heads, nseq);
-  (void)launch_k<true>(attn_fwd_kernel, grid, 128, FWD_SMEM, s, tq, static_cast<__nv_bfloat16*>(o), lse, seq, heads,
-                       err);
+  (void)launch_k<true>(attn_fwd_kernel, grid, FWD_THREADS, FWD_SMEM, s, tq, static_cast<__nv_bfloat16*>(o), lse, seq,
+                       heads, err);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention_fwd launch: %s", cudaGetErrorString(e));
@@ -704,10 +789,15 @@ int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const vo
   bool ok = amake_tmap(&tq64, qkv, 3 * D, rows, 3 * D, 64) && amake_tmap(&tq128, qkv, 3 * D, rows, 3 * D, 128) &&
             amake_tmap(&td64, dout, D, rows, D, 64) && amake_tmap(&td128, dout, D, rows, D, 128);
   if (!ok) return set_error(GPIPE_ERR_CUDA, "attention_bwd: tensor map creation failed");
+  const int64_t nd = rows * heads;
+  (void)launch_k(attn_dvec_kernel, static_cast<int>((nd + 255) / 256), 256, 0, s, static_cast<const __nv_bfloat16*>(o),
+                 static_cast<const __nv_bfloat16*>(dout), dvec, nd, heads);
+  count_launch();
+  cudaError_t e0 = cudaGetLastError();
+  if (e0 != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention_bwd (D) launch: %s", cudaGetErrorString(e0));
   dim3 grid((seq + 127) / 128, heads, 2 * nseq);
-  (void)launch_k<true>(attn_bwd_kernel, grid, 128, BWD_SMEM, s, tq64, tq128, td64, td128,
-                       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, dvec,
-                       static_cast<__nv_bfloat16*>(dqkv), seq, heads, nseq, err);
+  (void)launch_k<true>(attn_bwd_kernel, grid, 128, BWD_SMEM, s, tq64, tq128, td64, td128, lse,
+                       static_cast<const float*>(dvec), static_cast<__nv_bfloat16*>(dqkv), seq, heads, nseq, err);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention_bwd launch: %s", cudaGetErrorString(e));

@@ -20,7 +20,8 @@ enum DeviceError : int {
   DERR_ACC_WAIT = 3,   // epilogue waited too long for the accumulator
   DERR_DRAIN_WAIT = 4, // exit-time wait for in-flight copies gave up
   DERR_BAD_TOKEN = 5,  // a token id outside [0, vocab) (the read is skipped)
-  DERR_PROBE = 6       // the failure-detection probe's wait gave up (as it must)
+  DERR_PROBE = 6,      // the failure-detection probe's wait gave up (as it must)
+  DERR_ALIGN = 7       // a kernel found its shared memory less aligned than its tiles need (work skipped)
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait

@@ -33,9 +33,9 @@ int check_launch(const char* what) {
 // (c*32 + lane)*8 for chunk c.  Two passes over registers (mean, then
 // centred variance), fp32 statistics.
 // ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, const float* __restrict__ g,
-                                                     const float* __restrict__ b, T* __restrict__ y,
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) ln_fwd_kernel(const TI* __restrict__ x, const float* __restrict__ g,
+                                                     const float* __restrict__ b, TO* __restrict__ y,
                                                      float* __restrict__ mean, float* __restrict__ rstd, int rows,
                                                      int d) {
   griddep_wait();
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
   if (row >= rows) return;
-  const T* xr = x + (int64_t)row * d;
+  const TI* xr = x + (int64_t)row * d;
   float v[kMaxChunks][8];
   float s = 0.f;
 #pragma unroll
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, co
   }
   const float var = warp_sum(q) / d;
   const float rs = 1.0f / sqrtf(var + kLnEps);
-  T* yr = y + (int64_t)row * d;
+  TO* yr = y + (int64_t)row * d;
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     const int col = (c * 32 + lane) * 8;
@@ -97,12 +97,12 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const T* __restrict__ x, co
 // scratch; col_reduce adds the partial rows in order.  Both orders are fixed,
 // so results are bit-reproducible.
 // ---------------------------------------------------------------------------
-template <typename T, int CH>
-__global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ x,
+template <typename TD, typename TX, typename TO, int CH>
+__global__ void __launch_bounds__(256) ln_bwd_kernel(const TD* __restrict__ dy, const TX* __restrict__ x,
                                                      const float* __restrict__ mean, const float* __restrict__ rstd,
-                                                     const float* __restrict__ g, const T* __restrict__ dres,
-                                                     T* __restrict__ dx, float* __restrict__ partial, int rows,
-                                                     int d) {
+                                                     const float* __restrict__ g, const TO* __restrict__ dres,
+                                                     TO* __restrict__ dx, __nv_bfloat16* __restrict__ dx16,
+                                                     float* __restrict__ partial, int rows, int d) {
   griddep_wait();
   griddep_launch();
   __shared__ __align__(16) float stage[kLnRowsPerWarp][32 * 8 * CH];
@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const T* __restrict__ dy, c
           for (int j = 0; j < 8; ++j) o[j] += rv[j];
         }
         store8(dx + (int64_t)r * d + col, o);
+        if (dx16) store8(dx16 + (int64_t)r * d + col, o);  // the same values as bf16 (GEMM operands)
       }
     }
   }
@@ -428,8 +429,9 @@ __global__ void mse_kernel(const float* __restrict__ y, const float* __restrict_
 // ---------------------------------------------------------------------------
 // Embedding
 // ---------------------------------------------------------------------------
+template <typename TO>
 __global__ void embed_fwd_kernel(int rows, int d, int vocab, const int32_t* __restrict__ tokens,
-                                 const __nv_bfloat16* __restrict__ emb, __nv_bfloat16* __restrict__ x, int* err) {
+                                 const __nv_bfloat16* __restrict__ emb, TO* __restrict__ x, int* err) {
   griddep_wait();
   griddep_launch();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element group
@@ -437,21 +439,22 @@ __global__ void embed_fwd_kernel(int rows, int d, int vocab, const int32_t* __re
   if (i >= (int64_t)rows * groups) return;
   const int r = static_cast<int>(i / groups), c = static_cast<int>(i % groups) * 8;
   const int tok = tokens[r];
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (tok >= 0 && tok < vocab)
-    v = *reinterpret_cast<const uint4*>(emb + (int64_t)tok * d + c);
+    load8(emb + (int64_t)tok * d + c, v);
   else if (c == 0)
     atomicExch(err, DERR_BAD_TOKEN);
-  *reinterpret_cast<uint4*>(x + (int64_t)r * d + c) = v;
+  store8(x + (int64_t)r * d + c, v);  // exact: a bf16 value is an fp32 value
 }
 
 // CTA b owns embedding rows [b*vpc, (b+1)*vpc).  It scans the token list in
 // order, compacts the positions whose token it owns (order kept), and adds
 // each such dx row into its own embedding rows: one owner per row and a fixed
 // order, hence no atomics and a deterministic result.
+template <typename TI>
 __global__ void __launch_bounds__(256) embed_bwd_kernel(int rows, int d, int vocab, int vpc,
                                                         const int32_t* __restrict__ tokens,
-                                                        const __nv_bfloat16* __restrict__ dx,
+                                                        const TI* __restrict__ dx,
                                                         float* __restrict__ demb) {
   griddep_wait();
   griddep_launch();
@@ -635,52 +638,77 @@ size_t colred_scratch_floats(int rows, int cols) {
   return parts * static_cast<size_t>(cols);
 }
 
-int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
-                         float* mean, float* rstd, cudaStream_t s) {
+int launch_layernorm_fwd_io(int in_dtype, int out_dtype, int rows, int d, const void* x, const float* g,
+                            const float* b, void* y, float* mean, float* rstd, cudaStream_t s) {
   if (rows < 1 || d < 8 || d % 8 || d > 32 * 8 * kMaxChunks)
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm: need rows >= 1, d %% 8 == 0, 8 <= d <= 1024");
   if (!al16(x) || !al16(y) || !al16(g) || !al16(b))
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm: pointers must be 16-B aligned");
   const int grid = blocks_for(rows, 8);
-  if (dtype == DT_F32)
-    (void)launch_k(ln_fwd_kernel<float>, grid, 256, 0, s, static_cast<const float*>(x), g, b, static_cast<float*>(y), mean,
-                                              rstd, rows, d);
+  using bf = __nv_bfloat16;
+  if (in_dtype == DT_F32 && out_dtype == DT_F32)
+    (void)launch_k(ln_fwd_kernel<float, float>, grid, 256, 0, s, static_cast<const float*>(x), g, b,
+                   static_cast<float*>(y), mean, rstd, rows, d);
+  else if (in_dtype == DT_F32 && out_dtype == DT_BF16)
+    (void)launch_k(ln_fwd_kernel<float, bf>, grid, 256, 0, s, static_cast<const float*>(x), g, b,
+                   static_cast<bf*>(y), mean, rstd, rows, d);
+  else if (in_dtype == DT_BF16 && out_dtype == DT_BF16)
+    (void)launch_k(ln_fwd_kernel<bf, bf>, grid, 256, 0, s, static_cast<const bf*>(x), g, b, static_cast<bf*>(y),
+                   mean, rstd, rows, d);
   else
-    (void)launch_k(ln_fwd_kernel<__nv_bfloat16>, grid, 256, 0, s, static_cast<const __nv_bfloat16*>(x), g, b,
-                                                      static_cast<__nv_bfloat16*>(y), mean, rstd, rows, d);
+    return set_error(GPIPE_ERR_UNSUPPORTED, "layernorm: bf16 input with fp32 output is not built");
   return check_launch("layernorm_fwd");
+}
+
+int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
+                         float* mean, float* rstd, cudaStream_t s) {
+  return launch_layernorm_fwd_io(dtype, dtype, rows, d, x, g, b, y, mean, rstd, s);
+}
+
+namespace {
+template <typename TD, typename TX, typename TO>
+void ln_bwd_launch(int grid, int d, cudaStream_t s, const void* dy, const void* x, const float* mean, const float* rstd,
+                   const float* g, const void* dres, void* dx, void* dx16, float* scratch, int rows) {
+  const TD* dyp = static_cast<const TD*>(dy);
+  const TX* xp = static_cast<const TX*>(x);
+  const TO* rp = static_cast<const TO*>(dres);
+  TO* dxp = static_cast<TO*>(dx);
+  __nv_bfloat16* d16 = static_cast<__nv_bfloat16*>(dx16);
+  if (d <= 256)
+    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 1>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
+  else if (d <= 512)
+    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 2>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
+  else
+    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 4>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
+}
+}  // namespace
+
+int launch_layernorm_bwd_rows_io(int dy_dtype, int x_dtype, int out_dtype, int rows, int d, const void* dy,
+                                 const void* x, const float* mean, const float* rstd, const float* g, const void* dres,
+                                 void* dx, void* dx16, float* scratch, cudaStream_t s) {
+  if (rows < 1 || d < 8 || d % 8 || d > 32 * 8 * kMaxChunks)
+    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: need rows >= 1, d %% 8 == 0, 8 <= d <= 1024");
+  if (!al16(dy) || !al16(x) || !al16(dx) || !al16(g) || (dres && !al16(dres)) || (dx16 && !al16(dx16)) ||
+      !al16(scratch))
+    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: pointers must be 16-B aligned");
+  const int grid = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
+  using bf = __nv_bfloat16;
+  if (dy_dtype == DT_F32 && x_dtype == DT_F32 && out_dtype == DT_F32)
+    ln_bwd_launch<float, float, float>(grid, d, s, dy, x, mean, rstd, g, dres, dx, dx16, scratch, rows);
+  else if (dy_dtype == DT_BF16 && x_dtype == DT_BF16 && out_dtype == DT_BF16)
+    ln_bwd_launch<bf, bf, bf>(grid, d, s, dy, x, mean, rstd, g, dres, dx, dx16, scratch, rows);
+  else if (dy_dtype == DT_BF16 && x_dtype == DT_F32 && out_dtype == DT_F32)
+    ln_bwd_launch<bf, float, float>(grid, d, s, dy, x, mean, rstd, g, dres, dx, dx16, scratch, rows);
+  else
+    return set_error(GPIPE_ERR_UNSUPPORTED, "layernorm_bwd: this combination of element types is not built");
+  return check_launch("layernorm_bwd");
 }
 
 int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
                               const float* rstd, const float* g, const void* dres, void* dx, float* scratch,
                               cudaStream_t s) {
-  if (rows < 1 || d < 8 || d % 8 || d > 32 * 8 * kMaxChunks)
-    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: need rows >= 1, d %% 8 == 0, 8 <= d <= 1024");
-  if (!al16(dy) || !al16(x) || !al16(dx) || !al16(g) || (dres && !al16(dres)) || !al16(scratch))
-    return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: pointers must be 16-B aligned");
-  const int grid = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
-  if (dtype == DT_F32) {
-    const float *dyp = static_cast<const float*>(dy), *xp = static_cast<const float*>(x),
-                *rp = static_cast<const float*>(dres);
-    float* dxp = static_cast<float*>(dx);
-    if (d <= 256)
-      (void)launch_k(ln_bwd_kernel<float, 1>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
-    else if (d <= 512)
-      (void)launch_k(ln_bwd_kernel<float, 2>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
-    else
-      (void)launch_k(ln_bwd_kernel<float, 4>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
-  } else {
-    const __nv_bfloat16 *dyp = static_cast<const __nv_bfloat16*>(dy), *xp = static_cast<const __nv_bfloat16*>(x),
-                        *rp = static_cast<const __nv_bfloat16*>(dres);
-    __nv_bfloat16* dxp = static_cast<__nv_bfloat16*>(dx);
-    if (d <= 256)
-      (void)launch_k(ln_bwd_kernel<__nv_bfloat16, 1>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
-    else if (d <= 512)
-      (void)launch_k(ln_bwd_kernel<__nv_bfloat16, 2>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
-    else
-      (void)launch_k(ln_bwd_kernel<__nv_bfloat16, 4>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, scratch, rows, d);
-  }
-  return check_launch("layernorm_bwd");
+  return launch_layernorm_bwd_rows_io(dtype, dtype, dtype, rows, d, dy, x, mean, rstd, g, dres, dx, nullptr, scratch,
+                                      s);
 }
 
 int launch_layernorm_bwd_reduce(int rows, int d, const float* scratch, float* dg_acc, float* db_acc, cudaStream_t s) {
@@ -741,28 +769,47 @@ int launch_mse(int rows, int d, const float* y, const float* t, float inv_count,
   return check_launch("mse");
 }
 
-int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb, void* x,
-                         cudaStream_t s) {
+int launch_embedding_fwd_io(int out_dtype, int rows, int d, int vocab, const int32_t* tokens, const void* emb,
+                            void* x, cudaStream_t s) {
   if (rows < 1 || d < 8 || d % 8 || vocab < 1 || !al16(emb) || !al16(x))
     return set_error(GPIPE_ERR_INVALID_ARG,
                      "embedding_fwd: need rows >= 1, d %% 8 == 0, vocab >= 1 and 16-B aligned rows");
   const int64_t n = (int64_t)rows * (d / 8);
-  (void)launch_k(embed_fwd_kernel, blocks_for(n, 256), 256, 0, s, rows, d, vocab, tokens,
-                                                      static_cast<const __nv_bfloat16*>(emb),
-                                                      static_cast<__nv_bfloat16*>(x), device_error_ptr());
+  const __nv_bfloat16* e = static_cast<const __nv_bfloat16*>(emb);
+  if (out_dtype == DT_F32)
+    (void)launch_k(embed_fwd_kernel<float>, blocks_for(n, 256), 256, 0, s, rows, d, vocab, tokens, e,
+                   static_cast<float*>(x), device_error_ptr());
+  else
+    (void)launch_k(embed_fwd_kernel<__nv_bfloat16>, blocks_for(n, 256), 256, 0, s, rows, d, vocab, tokens, e,
+                   static_cast<__nv_bfloat16*>(x), device_error_ptr());
   return check_launch("embedding_fwd");
 }
 
-int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx, float* demb,
+int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb, void* x,
                          cudaStream_t s) {
+  return launch_embedding_fwd_io(DT_BF16, rows, d, vocab, tokens, emb, x, s);
+}
+
+int launch_embedding_bwd_io(int dx_dtype, int rows, int d, int vocab, const int32_t* tokens, const void* dx,
+                            float* demb, cudaStream_t s) {
   if (rows < 1 || d < 8 || d % 8 || vocab < 1 || !al16(dx) || !al16(demb))
     return set_error(GPIPE_ERR_INVALID_ARG,
                      "embedding_bwd: need rows >= 1, d %% 8 == 0, vocab >= 1 and 16-B aligned rows");
   int ctas = 4 * num_sms();
   const int vpc = (vocab + ctas - 1) / ctas;
   ctas = (vocab + vpc - 1) / vpc;
-  (void)launch_k(embed_bwd_kernel, ctas, 256, 0, s, rows, d, vocab, vpc, tokens, static_cast<const __nv_bfloat16*>(dx), demb);
+  if (dx_dtype == DT_F32)
+    (void)launch_k(embed_bwd_kernel<float>, ctas, 256, 0, s, rows, d, vocab, vpc, tokens, static_cast<const float*>(dx),
+                   demb);
+  else
+    (void)launch_k(embed_bwd_kernel<__nv_bfloat16>, ctas, 256, 0, s, rows, d, vocab, vpc, tokens,
+                   static_cast<const __nv_bfloat16*>(dx), demb);
   return check_launch("embedding_bwd");
+}
+
+int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx, float* demb,
+                         cudaStream_t s) {
+  return launch_embedding_bwd_io(DT_BF16, rows, d, vocab, tokens, dx, demb, s);
 }
 
 int launch_rmsprop(size_t n, float* w, float* g, float* v, void* wb, float lr, float decay, float eps,

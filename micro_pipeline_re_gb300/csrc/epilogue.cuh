@@ -6,6 +6,8 @@
 //   EPI_ACC_F32    C(fp32) += acc                              (weight gradients,
 //                  accumulated across micro-batches in the fp32 gradient buffer)
 //   EPI_STORE_F32  C(fp32) = acc                               (logits)
+//   EPI_RESID_F32  C(fp32) = (acc + bias[n]) + resid(fp32)[m,n] (residual adds
+//                  that keep the residual stream in fp32)
 #pragma once
 #include "common.cuh"
 #include "kernels.h"
@@ -37,6 +39,11 @@ __device__ __forceinline__ void epi_scalar(const EpiArgs& ep, int m, int n, floa
     return;
   }
   if (ep.bias) acc += ep.bias[n];
+  if (EPI == EPI_RESID_F32) {
+    if (ep.resid) acc += static_cast<const float*>(ep.resid)[(int64_t)m * ep.ldr + n];
+    static_cast<float*>(ep.C)[(int64_t)m * ep.ldc + n] = acc;
+    return;
+  }
   if (EPI == EPI_STORE) {
     if (ep.resid) acc += Elem<T>::ld(static_cast<const T*>(ep.resid) + (int64_t)m * ep.ldr + n);
     Elem<T>::st(static_cast<T*>(ep.C) + (int64_t)m * ep.ldc + n, acc);

@@ -42,7 +42,7 @@ constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
 // the fourth operand stage that single buffering leaves room for pays more.
 template <int BN, int EPI, bool SK = false>
 struct PCfg {
-  static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
+  static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32 || EPI == EPI_RESID_F32);
   static constexpr int A_BYTES = PM * PK * 2;
   static constexpr int B_BYTES = BN * PK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -294,6 +294,29 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         if (Cfg::F32_OUT) {
+          if (EPI == EPI_RESID_F32 && m < args.M) {  // + bias + the fp32 residual (global loads)
+            const float* xr = static_cast<const float*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx + ncol0;
+            // (acc + bias) + residual, the single-tile kernel's order
+            if (full_cols) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                float bb8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, t[8];
+                if (args.bias) load8(args.bias + ncol0 + j, bb8);
+                load8(xr + j, t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  v[j + e] += bb8[e];
+                  v[j + e] += t[e];
+                }
+              }
+            } else {
+              for (int j = 0; j < 32; ++j)
+                if (ncol0 + j < args.N) {
+                  v[j] += args.bias ? args.bias[ncol0 + j] : 0.f;
+                  v[j] += xr[j];
+                }
+            }
+          }
           uint8_t* box = stg + h * PBOX;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -427,12 +450,13 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   int rc = pset_attr<A_K, B_K, BN, EPI, SK>();
   if (rc) return rc;
   PArgs args{};
-  args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU) ? g.bias : nullptr;
+  args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU || EPI == EPI_RESID_F32) ? g.bias : nullptr;
   args.dbias = EPI == EPI_ACC_F32 ? g.dbias : nullptr;
   if (EPI == EPI_ACC_F32 && !Cfg::DB_MMA && g.dbias)
     return set_error(GPIPE_ERR_UNSUPPORTED, "persistent gemm: no bias gradient with 256-wide tiles");
-  args.xsrc = EPI == EPI_STORE ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : nullptr);
-  args.ldx = EPI == EPI_STORE ? g.ldr : g.ldaux;
+  const bool resid = EPI == EPI_STORE || EPI == EPI_RESID_F32;
+  args.xsrc = resid ? g.resid : (EPI == EPI_GELU_BWD ? g.aux : nullptr);
+  args.ldx = resid ? g.ldr : g.ldaux;
   args.M = g.M;
   args.N = g.N;
   args.K = g.K;
@@ -469,6 +493,7 @@ int dispatch(const GemmDesc& g, cudaStream_t s, int ctas) {
                                         : prun<true, true, BN, EPI_BIAS_GELU>(g, s, ctas);
       case EPI_STORE_F32: return prun<true, true, BN, EPI_STORE_F32>(g, s, ctas);
       case EPI_ACC_F32: return prun<true, true, BN, EPI_ACC_F32>(g, s, ctas);
+      case EPI_RESID_F32: return prun<true, true, BN, EPI_RESID_F32>(g, s, ctas);
     }
   } else if (g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
@@ -493,6 +518,7 @@ int prepare_bn() {
   rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU, true>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE_F32>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_ACC_F32>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_RESID_F32>();
   rc = rc ? rc : pset_attr<true, false, BN, EPI_STORE>();
   rc = rc ? rc : pset_attr<true, false, BN, EPI_GELU_BWD>();
   rc = rc ? rc : pset_attr<true, false, BN, EPI_ACC_F32>();

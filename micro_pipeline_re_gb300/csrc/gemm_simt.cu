@@ -101,6 +101,7 @@ int run_simt(const GemmDesc& g, cudaStream_t s) {
     case EPI_GELU_BWD: (void)launch_k(simt_gemm_kernel<T, EPI_GELU_BWD>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
     case EPI_ACC_F32: (void)launch_k(simt_gemm_kernel<T, EPI_ACC_F32>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
     case EPI_STORE_F32: (void)launch_k(simt_gemm_kernel<T, EPI_STORE_F32>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
+    case EPI_RESID_F32: (void)launch_k(simt_gemm_kernel<T, EPI_RESID_F32>, grid, 256, 0, s, A, g.lda, ak, B, g.ldb, bk, g.M, g.N, g.K, ep, db); break;
     default: return set_error(GPIPE_ERR_INVALID_ARG, "gemm: unknown epilogue %d", g.epi);
   }
   count_launch();

@@ -51,7 +51,7 @@ struct TcCfg {
   static constexpr int STAGES = BN == 64 ? 3 : 4;  // BN=64: two CTAs fit on one SM
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32);
+  static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32 || EPI == EPI_RESID_F32);
   static constexpr int OUT_BOXES = F32_OUT ? BN / 32 : BN / 64;            // boxes of one output tile
   static constexpr int EPI_BYTES = (EPI == EPI_BIAS_GELU ? 2 : 1) * OUT_BOXES * BOX;
   static constexpr int ONES_BYTES = (EPI == EPI_ACC_F32) ? 2048 : 0;
@@ -290,6 +290,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
       if (Cfg::F32_OUT) {
+        if (EPI == EPI_RESID_F32) {  // + bias + the fp32 residual, read straight from global memory
+          const int m = m0 + r, n = n0 + c * 32;  // (acc + bias) + residual
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += sBias[c * 32 + j];
+          if (m < args.M) {
+            const float* xr = static_cast<const float*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx + n;
+            if (n + 32 <= args.N) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                float t[8];
+                load8(xr + j, t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[j + e] += t[e];
+              }
+            } else {
+              for (int j = 0; j < 32; ++j)
+                if (n + j < args.N) v[j] += xr[j];
+            }
+          }
+        }
         uint8_t* box = sE + c * BOX;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -419,7 +439,7 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
   int has_x = 0;
   const void* xsrc = nullptr;
   int64_t ldx = 0;
-  if (EPI == EPI_STORE && g.resid) {
+  if ((EPI == EPI_STORE || EPI == EPI_RESID_F32) && g.resid) {
     xsrc = g.resid;
     ldx = g.ldr;
   }
@@ -427,7 +447,7 @@ int run(const GemmDesc& g, cudaStream_t stream, int S = 1) {
     xsrc = g.aux;
     ldx = g.ldaux;
   }
-  if (xsrc && !SPLIT) {
+  if (xsrc && !SPLIT && EPI != EPI_RESID_F32) {  // the fp32 residual is read in the epilogue itself
     ok = ok && make_tmap(&tx, xsrc, false, g.N, g.M, ldx, 64, BM);
     has_x = 1;
   }
@@ -499,6 +519,7 @@ int run_epi_bn(const GemmDesc& g, cudaStream_t s, int S) {
       case EPI_BIAS_GELU: return run<true, true, BN, EPI_BIAS_GELU>(g, s);
       case EPI_STORE_F32: return run<true, true, BN, EPI_STORE_F32>(g, s);
       case EPI_ACC_F32: return run<true, true, BN, EPI_ACC_F32>(g, s);
+      case EPI_RESID_F32: return run<true, true, BN, EPI_RESID_F32>(g, s);
     }
   } else if (g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
@@ -564,6 +585,7 @@ int prepare_bn() {
   rc = rc ? rc : set_attr<true, true, BN, EPI_BIAS_GELU>();
   rc = rc ? rc : set_attr<true, true, BN, EPI_STORE_F32>();
   rc = rc ? rc : set_attr<true, true, BN, EPI_ACC_F32>();
+  rc = rc ? rc : set_attr<true, true, BN, EPI_RESID_F32>();
   rc = rc ? rc : set_attr<true, false, BN, EPI_STORE>();
   rc = rc ? rc : set_attr<true, false, BN, EPI_GELU_BWD>();
   rc = rc ? rc : set_attr<true, false, BN, EPI_ACC_F32>();
@@ -595,6 +617,8 @@ int launch_gemm_tc(const GemmDesc& g, cudaStream_t stream) {
     return set_error(GPIPE_ERR_INVALID_ARG, "gemm: GELU backward needs an aligned aux");
   if (g.resid && (g.ldr % 8 || g.ldr < g.N || !aligned16(g.resid)))
     return set_error(GPIPE_ERR_INVALID_ARG, "gemm: residual must be aligned");
+  if (g.epi == EPI_RESID_F32 && (!g.resid || !g.a_kmajor || !g.b_kmajor))
+    return set_error(GPIPE_ERR_INVALID_ARG, "gemm: the fp32 residual epilogue needs a residual and K-major operands");
   return run_epi(g, stream);
 }
 

@@ -314,8 +314,8 @@ class Executor {
     // phase 3: the embedding scatter of all micro-batches (after the head's
     // contributions, in token order), then one update of every parameter
     if (c_->dm.kind == 1)
-      TRY(launch_embedding_bwd(static_cast<int>(c_->T()), c_->dm.d, c_->dm.vocab,
-                               static_cast<const int32_t*>(p_.batch), dx0(0), grad(c_->pl.emb), origin_));
+      TRY(launch_embedding_bwd_io(DT_F32, static_cast<int>(c_->T()), c_->dm.d, c_->dm.vocab,
+                                  static_cast<const int32_t*>(p_.batch), dx0(0), grad(c_->pl.emb), origin_));
     if (!c_->skip_update)
       TRY(launch_rmsprop(c_->pl.total, p_.p32, p_.g32, p_.v32, c_->dm.dtype == 1 ? p_.p16 : nullptr, c_->dm.lr,
                          c_->dm.decay, c_->dm.eps, c_->keep_grads ? 0 : 1, origin_));
@@ -388,39 +388,45 @@ class Executor {
     cur_lane_ = lk;
     TRY(join_all(lk));  // side work still reading this lane's slots
     if (!c_->no_remat) TRY(cell_forward(k, m, /*recompute=*/true));
-    // gradient of the cell's output
-    char* dy;
+    // gradient of the cell's output (fp32, with its bf16 copy for the GEMMs)
+    char *dy, *dy16;
     const int dy_buf = BUF_EXT;
     if (k == K - 1) {
       if (head_lane(m) != lk) TRY(cuda_ok(cudaStreamWaitEvent(main_s(lk), c_->ev_hdone[m], 0), "stream wait"));
       dy = hdy(m);
+      dy16 = hdy16(m);
     } else {
       TRY(cross_wait(k, m, c_->ev_bdone[k + 1][p], bdone_rec_[k + 1][p], k + 1));
       dy = bgrad(k + 1, p);
+      dy16 = bgrad16(k + 1, p);
     }
     int cur_buf = dy_buf;
     const int first = c_->bounds[k], n = c_->bounds[k + 1] - first;
     for (int j = n - 1; j >= 0; --j) {
       const void* x = j == 0 ? cell_input(k, m) : slot(k, m, j - 1).y;
-      char* dx;
+      char *dx, *dx16;
       int dx_buf;
       if (j == 0 && k > 0) {
         // hand the input gradient to cell k-1 through the ring
         if (bfree_rec_[k][p]) TRY(cross_wait(k, m, c_->ev_bfree[k][p], bfree_rec_[k][p], k - 1));
         dx = bgrad(k, p);
+        dx16 = bgrad16(k, p);
         dx_buf = BUF_EXT;
       } else if (j == 0 && c_->dm.kind == 1) {
-        dx = dx0(m);  // the embedding's input gradient, scattered once at the end
+        dx = dx0(m);  // the embedding's input gradient, scattered once at the end (fp32 only)
+        dx16 = dx;
         dx_buf = BUF_EXT;
       } else {
         dx_buf = cur_buf == 0 ? 1 : 0;
         dx = lbuf(lk, dx_buf);
+        dx16 = lbuf16(lk, dx_buf);
       }
       const bool timed = c_->layer_times && m == 0;
       if (timed) TRY(record_timed(c_->lt_ev[4 * (first + j) + 2]));
-      TRY(layer_backward(first + j, x, slot(k, m, j), dy, cur_buf, dx, dx_buf));
+      TRY(layer_backward(first + j, x, slot(k, m, j), dy, dy16, cur_buf, dx, copy_of(dx16, dx), dx_buf));
       if (timed) TRY(record_timed(c_->lt_ev[4 * (first + j) + 3]));
       dy = dx;
+      dy16 = dx16;
       cur_buf = dx_buf;
     }
     if (c_->trace) TRY(launch_stamp(stamp(2 + (static_cast<size_t>(k) * M + m) * 2 + 1), st()));
@@ -476,6 +482,12 @@ class Executor {
   // micro-batch order.
   int side_of(int lane) const { return lane < c_->ws.nlanes ? lane - lane % c_->ws.inflight : c_->ws.nlanes; }
   char* hdy(int m) const { return ws(c_->ws.hdy) + static_cast<size_t>(m % c_->ws.depth) * c_->ws.stash_bytes; }
+  // The GEMM operand of a residual gradient: its bf16 copy, or the fp32
+  // buffer itself for the fp32 model (copy_bytes 0).
+  char* hdy16(int m) const {
+    if (!c_->ws.copy_bytes) return hdy(m);
+    return ws(c_->ws.hdy16) + static_cast<size_t>(m % c_->ws.depth) * c_->ws.copy_bytes;
+  }
   cudaStream_t main_s(int lane) const { return c_->lane_main[lane]; }
   // Weight-gradient work goes to a side stream when CONCURRENT is on, and
   // always when a cell or the head has more than one lane (its lanes must not
@@ -547,14 +559,17 @@ class Executor {
   // side stream, in issue order like the weight gradients.  The two partial
   // buffers alternate, so the next LayerNorm backward need not wait for this
   // reduction, only for the one that read its buffer before.
+  // dy: a GEMM output of the compute type (dt); x, dres and dx: the fp32
+  // residual stream and its gradient; dx16: the bf16 copy of dx (or nullptr).
   int ln_backward(int dt, int T, int d, const void* dy, const void* x, const float* mean, const float* rstd,
-                  const float* g, const void* dres, void* dx, float* dg, float* db, float* part0, float* part1) {
+                  const float* g, const void* dres, void* dx, void* dx16, float* dg, float* db, float* part0,
+                  float* part1) {
     const int lane = cur_lane_;
     const int b = ln_buf_[lane];
     ln_buf_[lane] ^= 1;
     float* part = b ? part1 : part0;
     TRY(join(lane, EV_LN0 + b));
-    TRY(launch_layernorm_bwd_rows(dt, T, d, dy, x, mean, rstd, g, dres, dx, part, st()));
+    TRY(launch_layernorm_bwd_rows_io(dt, DT_F32, DT_F32, T, d, dy, x, mean, rstd, g, dres, dx, dx16, part, st()));
     return on_side(EV_LN0 + b, [&] { return launch_layernorm_bwd_reduce(T, d, part, dg, db, st()); });
   }
 
@@ -584,8 +599,18 @@ class Executor {
   char* bgrad(int k, int p) const {
     return ws(c_->ws.bgrad) + (static_cast<size_t>(k) * c_->ws.ring + p) * c_->ws.stash_bytes;
   }
+  char* bgrad16(int k, int p) const {
+    if (!c_->ws.copy_bytes) return bgrad(k, p);
+    return ws(c_->ws.bgrad16) + (static_cast<size_t>(k) * c_->ws.ring + p) * c_->ws.copy_bytes;
+  }
   char* lane_base(int lane) const { return ws(c_->ws.lanes) + static_cast<size_t>(lane) * c_->ws.lane.bytes; }
   char* lbuf(int lane, int i) const { return lane_base(lane) + (i == 0 ? c_->ws.lane.g0 : c_->ws.lane.g1); }
+  char* lbuf16(int lane, int i) const {
+    if (!c_->ws.copy_bytes) return lbuf(lane, i);
+    return lane_base(lane) + (i == 0 ? c_->ws.lane.g0b : c_->ws.lane.g1b);
+  }
+  // bf16 copy to write beside a residual gradient (nullptr for the fp32 model)
+  void* copy_of(char* op, char* f32) const { return op == f32 ? nullptr : op; }
   const void* cell_input(int k, int m) const {
     if (k == 0 && c_->dm.kind == 0)
       return static_cast<const char*>(p_.batch) + static_cast<size_t>(m) * c_->Tmb() * c_->dm.d * 4;
@@ -680,8 +705,8 @@ class Executor {
   int cell0_input(int m) {
     if (c_->dm.kind != 1) return GPIPE_OK;  // kind 0 reads the caller's x directly
     cur_lane_ = lane_of(0, m);
-    return launch_embedding_fwd(static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m), wgt(c_->pl.emb),
-                                stash(0, m), st());
+    return launch_embedding_fwd_io(DT_F32, static_cast<int>(c_->Tmb()), c_->dm.d, c_->dm.vocab, tokens(m),
+                                   wgt(c_->pl.emb), stash(0, m), st());
   }
 
   // Forward of cell k for micro-batch m.  recompute: re-materialisation pass
@@ -726,20 +751,23 @@ class Executor {
     const LayerOff& o = c_->pl.layers[l];
     const int T = static_cast<int>(c_->Tmb()), d = dm.d, f = c_->ffn[l];
     const int dt = dm.dtype == 0 ? DT_F32 : DT_BF16;
-    TRY(launch_layernorm_fwd(dt, T, d, x, p32(o.ln1_g), p32(o.ln1_b), s.u, s.mean1, s.rstd1, st()));
+    // the residual stream (x, h1, the layer's output) is fp32; the residual
+    // adds happen in the output projections' epilogues, in fp32
+    const int resid_epi = dt == DT_F32 ? EPI_STORE : EPI_RESID_F32;
+    TRY(launch_layernorm_fwd_io(DT_F32, dt, T, d, x, p32(o.ln1_g), p32(o.ln1_b), s.u, s.mean1, s.rstd1, st()));
     const void* ffn_in = s.u;
     const void* resid2 = x;
     if (dm.kind == 1) {
       TRY(gemm(T, 3 * d, d, s.u, d, true, wgt(o.w_qkv), d, true, EPI_STORE, s.qkv, 3 * d, p32(o.b_qkv)));
       TRY(launch_attention_fwd(T / dm.seq, dm.seq, dm.heads, s.qkv, s.o, s.lse, st()));
-      TRY(gemm(T, d, d, s.o, d, true, wgt(o.w_o), d, true, EPI_STORE, s.h1, d, p32(o.b_o), x, d));
-      TRY(launch_layernorm_fwd(dt, T, d, s.h1, p32(o.ln2_g), p32(o.ln2_b), s.u2, s.mean2, s.rstd2, st()));
+      TRY(gemm(T, d, d, s.o, d, true, wgt(o.w_o), d, true, resid_epi, s.h1, d, p32(o.b_o), x, d));
+      TRY(launch_layernorm_fwd_io(DT_F32, dt, T, d, s.h1, p32(o.ln2_g), p32(o.ln2_b), s.u2, s.mean2, s.rstd2, st()));
       ffn_in = s.u2;
       resid2 = s.h1;
     }
     TRY(gemm(T, f, d, ffn_in, d, true, wgt(o.w1), d, true, EPI_BIAS_GELU, s.z1, f, p32(o.b1), nullptr, 0, s.g));
     if (!skip_out_proj)
-      TRY(gemm(T, d, f, s.g, f, true, wgt(o.w2), f, true, EPI_STORE, out, d, p32(o.b2), resid2, d));
+      TRY(gemm(T, d, f, s.g, f, true, wgt(o.w2), f, true, resid_epi, out, d, p32(o.b2), resid2, d));
     return GPIPE_OK;
   }
 
@@ -748,7 +776,11 @@ class Executor {
   // input into dx (lane buffer dx_buf, or outside).  Weight gradients run on
   // the lane's side stream; before the main stream overwrites a buffer that a
   // side GEMM reads, it joins that GEMM's event.
-  int layer_backward(int l, const void* x, const Slot& s, const void* dy, int dy_buf, void* dx, int dx_buf) {
+  // dy / dx: the fp32 residual gradient of the layer's output / input; dy16:
+  // dy as the GEMMs read it (its bf16 copy, or dy itself for the fp32 model);
+  // dx16: where to write dx's bf16 copy (nullptr: none).
+  int layer_backward(int l, const void* x, const Slot& s, const void* dy, const void* dy16, int dy_buf, void* dx,
+                     void* dx16, int dx_buf) {
     const Dims& dm = c_->dm;
     const LayerOff& o = c_->pl.layers[l];
     const LaneLayout& ll = c_->ws.lane;
@@ -769,11 +801,11 @@ class Executor {
     const int ev_dy = dy_buf == 0 ? EV_DY0 : (dy_buf == 1 ? EV_DY1 : EV_DYB);
     // FFN: y = r + W2 GELU(W1 u + b1) + b2
     TRY(on_side(ev_dy, [&] {
-      return gemm(d, f, T, dy, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f, nullptr, nullptr, 0, nullptr,
+      return gemm(d, f, T, dy16, d, false, s.g, f, false, EPI_ACC_F32, grad(o.w2), f, nullptr, nullptr, 0, nullptr,
                   nullptr, 0, grad(o.b2));
     }));
     TRY(join(lane, EV_GF + gb));
-    TRY(gemm(T, f, d, dy, d, true, wgt(o.w2), f, false, EPI_GELU_BWD, gf, f, nullptr, nullptr, 0, nullptr, s.z1, f));
+    TRY(gemm(T, f, d, dy16, d, true, wgt(o.w2), f, false, EPI_GELU_BWD, gf, f, nullptr, nullptr, 0, nullptr, s.z1, f));
     TRY(on_side(EV_GF + gb, [&] {
       return gemm(f, d, T, gf, f, false, ffn_in, d, false, EPI_ACC_F32, grad(o.w1), d, nullptr, nullptr, 0, nullptr,
                   nullptr, 0, grad(o.b1));
@@ -781,15 +813,16 @@ class Executor {
     TRY(gemm(T, d, f, gf, f, true, wgt(o.w1), d, false, EPI_STORE, gt, d));
     if (dm.kind == 0) {
       if (dx_buf != BUF_EXT) TRY(join(lane, dx_buf == 0 ? EV_DY0 : EV_DY1));
-      return ln_backward(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, grad(o.ln1_g), grad(o.ln1_b),
-                         lnp0, lnp1);
+      return ln_backward(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), dy, dx, dx16, grad(o.ln1_g),
+                         grad(o.ln1_b), lnp0, lnp1);
     }
-    char* gh = lb + ll.gh[gb];
+    char* gh = lb + ll.gh[gb];    // bf16 copy of dh1 (the GEMMs' operand)
+    char* gh32 = lb + ll.gh32;    // dh1 in fp32 (the residual gradient)
     char* gq = lb + ll.gq[gb];
     // h1 -> LN2: dh1 = LN2'(du2) + dy
     TRY(join(lane, EV_GH + gb));
-    TRY(ln_backward(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh, grad(o.ln2_g), grad(o.ln2_b),
-                    lnp0, lnp1));
+    TRY(ln_backward(dt, T, d, gt, s.h1, s.mean2, s.rstd2, p32(o.ln2_g), dy, gh32, gh, grad(o.ln2_g),
+                    grad(o.ln2_b), lnp0, lnp1));
     // attention output projection
     TRY(on_side(EV_GH + gb, [&] {
       return gemm(d, d, T, gh, d, false, s.o, d, false, EPI_ACC_F32, grad(o.w_o), d, nullptr, nullptr, 0, nullptr,
@@ -804,8 +837,8 @@ class Executor {
     }));
     TRY(gemm(T, d, 3 * d, gq, 3 * d, true, wgt(o.w_qkv), d, false, EPI_STORE, gt, d));
     if (dx_buf != BUF_EXT) TRY(join(lane, dx_buf == 0 ? EV_DY0 : EV_DY1));
-    return ln_backward(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh, dx, grad(o.ln1_g), grad(o.ln1_b), lnp0,
-                       lnp1);
+    return ln_backward(dt, T, d, gt, x, s.mean1, s.rstd1, p32(o.ln1_g), gh32, dx, dx16, grad(o.ln1_g),
+                       grad(o.ln1_b), lnp0, lnp1);
   }
 
   // The head of micro-batch m, once: loss rows from the last cell's output
@@ -829,8 +862,9 @@ class Executor {
     TRY(join(cur_lane_, EV_HEAD));  // the previous micro-batch's dE GEMM has read the logits and hf
     const float inv = 1.0f / (static_cast<float>(dm.n) * (dm.seq - 1));
     float* logits = reinterpret_cast<float*>(ws(hb.logits));
-    TRY(launch_layernorm_fwd(DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(hb.hf),
-                             reinterpret_cast<float*>(ws(hb.meanf)), reinterpret_cast<float*>(ws(hb.rstdf)), st()));
+    TRY(launch_layernorm_fwd_io(DT_F32, DT_BF16, T, d, xf, p32(c_->pl.lnf_g), p32(c_->pl.lnf_b), ws(hb.hf),
+                                reinterpret_cast<float*>(ws(hb.meanf)), reinterpret_cast<float*>(ws(hb.rstdf)),
+                                st()));
     TRY(gemm(T, dm.vocab, d, ws(hb.hf), d, true, wgt(c_->pl.emb), d, true, EPI_STORE_F32, logits, dm.vocab));
     TRY(launch_cross_entropy(T, dm.vocab, dm.seq, static_cast<const int32_t*>(p_.batch), m * T, inv, logits,
                              loss_rows, 1, st(), static_cast<float>(static_cast<double>(c_->clip_milli) / 1000.0)));
@@ -842,8 +876,8 @@ class Executor {
       return gemm(dm.vocab, d, T, logits, ldz, false, ws(hb.hf), d, false, EPI_ACC_F32, grad(c_->pl.emb), d);
     }));
     return ln_backward(DT_BF16, T, d, gt, xf, reinterpret_cast<float*>(ws(hb.meanf)),
-                       reinterpret_cast<float*>(ws(hb.rstdf)), p32(c_->pl.lnf_g), nullptr, dy, grad(c_->pl.lnf_g),
-                       grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(hb.hlnp[0])),
+                       reinterpret_cast<float*>(ws(hb.rstdf)), p32(c_->pl.lnf_g), nullptr, dy, copy_of(hdy16(m), dy),
+                       grad(c_->pl.lnf_g), grad(c_->pl.lnf_b), reinterpret_cast<float*>(ws(hb.hlnp[0])),
                        reinterpret_cast<float*>(ws(hb.hlnp[1])));
   }
 };
@@ -1205,7 +1239,7 @@ int gpipe_set_option(gpipe_ctx* c, int option, int64_t value) {
       c->sm_share = static_cast<int>(value);
       break;
     case GPIPE_OPT_KERNEL_TIMES:
-      if (value < 0 || value > 5) return c->fail(GPIPE_ERR_INVALID_ARG, "kernel-times selector out of range");
+      if (value < 0 || value > 6) return c->fail(GPIPE_ERR_INVALID_ARG, "kernel-times selector out of range");
       c->ktime = static_cast<int>(value);
       break;
     default: return c->fail(GPIPE_ERR_INVALID_ARG, "unknown option");

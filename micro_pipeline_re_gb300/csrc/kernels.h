@@ -10,7 +10,9 @@
 namespace gp {
 
 enum { DT_F32 = 0, DT_BF16 = 1 };
-enum { EPI_STORE = 0, EPI_BIAS_GELU = 1, EPI_GELU_BWD = 2, EPI_ACC_F32 = 3, EPI_STORE_F32 = 4 };
+// EPI_RESID_F32: C(fp32) = acc + bias[n] + resid(fp32)[m, n], the step's
+// residual adds, which keep the residual stream in fp32.
+enum { EPI_STORE = 0, EPI_BIAS_GELU = 1, EPI_GELU_BWD = 2, EPI_ACC_F32 = 3, EPI_STORE_F32 = 4, EPI_RESID_F32 = 5 };
 
 // Error reporting (thread-local message; see launch.cu).
 int set_error(int code, const char* fmt, ...);
@@ -60,12 +62,24 @@ size_t colred_scratch_floats(int rows, int cols);
 
 int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
                          float* mean, float* rstd, cudaStream_t stream);
+// The same with separate input and output element types: the step reads the
+// fp32 residual stream and writes the bf16 GEMM operand (fp32 -> bf16;
+// fp32 -> fp32 and bf16 -> bf16 as above).
+int launch_layernorm_fwd_io(int in_dtype, int out_dtype, int rows, int d, const void* x, const float* g,
+                            const float* b, void* y, float* mean, float* rstd, cudaStream_t stream);
 // LayerNorm backward in two launches: the rows (dx, and one partial row of the
 // gamma/beta column sums per 8 rows into scratch), then the fixed-order
 // reduction of the partials into dg_acc / db_acc (+=).
 int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
                               const float* rstd, const float* g, const void* dres, void* dx, float* scratch,
                               cudaStream_t s);
+// The same with dy of dy_dtype, x of x_dtype, and dres and dx of out_dtype;
+// dx16 (may be NULL) receives a bf16 copy of dx.  The step: a bf16 GEMM output
+// dy, the fp32 residual stream x, the fp32 residual gradient dres -> dx in
+// fp32 (the residual gradient stream) and in bf16 (the next GEMMs' operand).
+int launch_layernorm_bwd_rows_io(int dy_dtype, int x_dtype, int out_dtype, int rows, int d, const void* dy,
+                                 const void* x, const float* mean, const float* rstd, const float* g, const void* dres,
+                                 void* dx, void* dx16, float* scratch, cudaStream_t s);
 int launch_gelu(size_t n, const float* z, float* y, float* dy, cudaStream_t s);
 // One CTA whose bounded wait on an mbarrier nothing completes gives up and
 // sets the device error word (code 6): checks the failure path without a fault.
@@ -99,6 +113,11 @@ int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, cons
                          cudaStream_t stream);
 int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx_bf16, float* demb,
                          cudaStream_t stream);
+// The same with the residual stream's element type (x written, dx read) given.
+int launch_embedding_fwd_io(int out_dtype, int rows, int d, int vocab, const int32_t* tokens, const void* emb_bf16,
+                            void* x, cudaStream_t stream);
+int launch_embedding_bwd_io(int dx_dtype, int rows, int d, int vocab, const int32_t* tokens, const void* dx,
+                            float* demb, cudaStream_t stream);
 
 int launch_rmsprop(size_t n, float* w, float* g, float* v, void* w_bf16, float lr, float decay, float eps,
                    int zero_grad, cudaStream_t stream);

@@ -248,6 +248,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   Workspace w;
   w.depth = depth > 0 && depth < M ? depth : M;
   const size_t es = dm.dtype == 0 ? 4 : 2;
+  const size_t rs = 4;                          // the residual stream and its gradient: fp32
+  const size_t cs = dm.dtype == 0 ? 0 : 2;      // bf16 copies of the gradient for the GEMMs
   const size_t T = static_cast<size_t>(dm.n) * (dm.kind == 1 ? dm.seq : 1);
   const size_t Tmb = T / M;
   const size_t d = dm.d, f = dm.ffn, H = dm.kind == 1 ? dm.heads : 0;
@@ -263,7 +265,7 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   if (dm.kind == 1) {
     s.qkv = stake(Tmb * 3 * d * es);
     s.o = stake(Tmb * d * es);
-    s.h1 = stake(Tmb * d * es);
+    s.h1 = stake(Tmb * d * rs);
     s.u2 = stake(Tmb * d * es);
   }
   s.z1 = stake(Tmb * f * es);
@@ -276,7 +278,7 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     s.lse = stake(Tmb * H * 4);
   }
   s.compare_bytes_last = so;
-  s.y = stake(Tmb * d * es);
+  s.y = stake(Tmb * d * rs);
   s.bytes = so;
   w.slot = s;
   w.slot_bytes = s.bytes;
@@ -290,8 +292,15 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     return at;
   };
   ln.slots = ltake(remat ? static_cast<size_t>(max_cell_layers) * w.slot_bytes : 0);
-  ln.g0 = ltake(Tmb * d * es);
-  ln.g1 = ltake(Tmb * d * es);
+  // a cell's gradient chain alternates g0 and g1 between its layers; the
+  // first layer's input gradient goes out of the lane, so g1 is used only by
+  // cells of three layers or more
+  const size_t g1_rows = max_cell_layers >= 3 ? Tmb : 0;
+  ln.g0 = ltake(Tmb * d * rs);
+  ln.g1 = ltake(g1_rows * d * rs);
+  ln.g0b = ltake(Tmb * d * cs);
+  ln.g1b = ltake(g1_rows * d * cs);
+  ln.gh32 = ltake(dm.kind == 1 ? Tmb * d * rs : 0);
   ln.gt = ltake(Tmb * d * es);
   for (int i = 0; i < 2; ++i) {
     ln.gf[i] = ltake(Tmb * f * es);
@@ -317,7 +326,8 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
     off += align256(bytes);
     return at;
   };
-  w.stash_bytes = Tmb * d * es;
+  w.stash_bytes = Tmb * d * rs;
+  w.copy_bytes = Tmb * d * cs;
   // the last cell's output is read only by the head, right after the cell
   // forwarded it: a ring as deep as the head's lanes plus one (the cell can
   // write the next micro-batch while the head lanes read theirs)
@@ -330,10 +340,12 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
   // than the micro-batches there are
   w.ring = std::min(std::max(w.inflight, 2), M);
   w.bgrad = take(static_cast<size_t>(K) * w.ring * w.stash_bytes);
+  w.bgrad16 = take(static_cast<size_t>(K) * w.ring * w.copy_bytes);
   w.lanes = take(static_cast<size_t>(w.nlanes) * ln.bytes);
   w.nslots_noremat = remat ? 0 : static_cast<size_t>(L) * M;
   w.noremat_slots = take(w.nslots_noremat * w.slot_bytes);
   w.hdy = take(static_cast<size_t>(w.depth) * w.stash_bytes);
+  w.hdy16 = take(static_cast<size_t>(w.depth) * w.copy_bytes);
   for (int h = 0; h < w.nheads && dm.kind == 1; ++h) {
     Workspace::Head& hb = w.head[h];
     hb.hf = take(Tmb * d * es);
@@ -365,25 +377,28 @@ MemoryModel review_memory_model(const Dims& dm, int L, int K, int M, int max_cel
   const size_t Tmb = T / M;
   const size_t d = dm.d, f = dm.ffn, H = lm ? dm.heads : 0, V = lm ? dm.vocab : 0;
   const size_t D = depth > 0 && depth < M ? depth : M;
-  const size_t act = Tmb * d * e;  // one boundary tensor of one micro-batch
-  mm.boundary = static_cast<size_t>(K) * D * act + D * act + (lm ? static_cast<size_t>(M) * act : 0) + 2 * act +
-                2 * static_cast<size_t>(K) * act;
-  const size_t a = lm ? e * (8 * d + 2 * f) + 16 + 4 * H : e * (2 * d + 2 * f) + 8;
+  const size_t r = 4, c = dm.dtype == 0 ? 0 : 2;  // residual stream (fp32) and bf16 gradient copies
+  const size_t act = Tmb * d * r;                  // one boundary tensor of one micro-batch
+  const size_t gcp = Tmb * d * (r + c);            // one residual gradient with its copy
+  mm.boundary = static_cast<size_t>(K) * D * act + D * gcp + (lm ? static_cast<size_t>(M) * act : 0) + 2 * act +
+                2 * static_cast<size_t>(K) * gcp;
+  const size_t a = lm ? e * (6 * d + 2 * f) + 2 * d * r + 16 + 4 * H : e * (d + 2 * f) + d * r + 8;
   mm.cell = remat ? static_cast<size_t>(max_cell_layers) * Tmb * a : static_cast<size_t>(L) * M * Tmb * a;
   const size_t lnp = 2 * ((Tmb + 7) / 8) * 2 * d * 4;  // LayerNorm partial sums: a row of 2d per 8 tokens, x2
   mm.head = lm ? Tmb * (V * 4 + 2 * d * e + 8) + lnp : 0;
-  mm.grads = 3 * act + 2 * Tmb * (f + (lm ? 4 * d : 0)) * e + Tmb * std::max<size_t>(H, 1) * 4 + lnp;
+  mm.grads = 2 * gcp + (lm ? act : 0) + Tmb * d * e + 2 * Tmb * (f + (lm ? 4 * d : 0)) * e +
+             Tmb * std::max<size_t>(H, 1) * 4 + lnp;
   mm.rows = T * 4;
   // every region of the arena starts on a 256-byte boundary (TMA and vector
   // access): at most 255 bytes of padding for each of the <= 13 regions of a
-  // layer's internals and the <= 48 others
-  mm.align = 256 * (13 * static_cast<size_t>(remat ? max_cell_layers : L * M) + 48);
+  // layer's internals and the <= 56 others
+  mm.align = 256 * (13 * static_cast<size_t>(remat ? max_cell_layers : L * M) + 56);
   mm.total = mm.boundary + mm.cell + mm.head + mm.grads + mm.rows + mm.align;
   const size_t a_survey = e * ((lm ? 8 * d : 2 * d) + 2 * f) + 8;
   mm.survey = static_cast<size_t>(K) * T * d * e +
               (remat ? static_cast<size_t>(L) * Tmb * a_survey / static_cast<size_t>(K)
                      : static_cast<size_t>(L) * T * a_survey) +
-              Tmb * V * 4 + 3 * act;
+              Tmb * V * 4 + 3 * Tmb * d * e;
   return mm;
 }
 

@@ -83,19 +83,27 @@ struct SlotLayout {
 // concurrent lanes; a single lane shared by all cells otherwise).
 struct LaneLayout {
   size_t slots = 0;                             // re-materialised internals of one cell (Lc slots)
-  size_t g0 = 0, g1 = 0, gt = 0;                // gradients in flight
+  size_t g0 = 0, g1 = 0, gt = 0;                // gradients in flight (g0/g1: the residual gradient, fp32)
+  size_t g0b = 0, g1b = 0;                      // bf16 copies of g0/g1 (GEMM operands; bf16 models only)
+  size_t gh32 = 0;                              // fp32 gradient of a layer's mid-residual h1 (Transformer)
   size_t gf[2] = {0, 0}, gh[2] = {0, 0}, gq[2] = {0, 0};  // weight-gradient operands, alternating by layer
   size_t scratch = 0;                           // attention row sums
   size_t lnp[2] = {0, 0};                       // LayerNorm-backward gamma/beta partials, alternating
   size_t bytes = 0;
 };
 
+// The residual stream (cell inputs, layer outputs, a layer's mid-residual h1)
+// and the gradient flowing along it are kept in fp32 whatever the compute
+// type: they add up every layer's contribution, the step's longest chains of
+// additions.  Where a bf16 GEMM reads the gradient, a bf16 copy sits beside it.
 struct Workspace {
-  size_t stash = 0, stash_bytes = 0;        // K x depth cell inputs [Tmb, d], then head_depth head inputs
+  size_t stash = 0, stash_bytes = 0;        // K x depth cell inputs [Tmb, d] fp32, then head_depth head inputs
+  size_t copy_bytes = 0;                    // one bf16 copy of a [Tmb, d] gradient (0: fp32 model, no copies)
   int depth = 1;                            // stash ring depth (micro-batch m in slot m mod depth)
   int head_depth = 1;                       // ring of the last cell's output (read only by the head)
   size_t dx0 = 0;                           // M x [Tmb, d]: gradient w.r.t. the embedding output (kind 1)
   size_t bgrad = 0;                         // K x ring x [Tmb, d]: gradient w.r.t. cell k's input
+  size_t bgrad16 = 0;                       // its bf16 copies
   int ring = 2;                             // depth of that ring: max(2, in flight per cell), at most M
   size_t lanes = 0;                         // nlanes x lane
   int nlanes = 1;                           // K x inflight when the cells are pipelined, else 1
@@ -113,6 +121,7 @@ struct Workspace {
   int nheads = 1;                           // head lanes: 2 (alternate micro-batches) when pipelined and M > 1
   size_t lnp_bytes = 0;                     // ceil(Tmb / 8) x 2d fp32
   size_t hdy = 0;                           // depth x [Tmb, d]: gradient of the last cell's output per micro-batch
+  size_t hdy16 = 0;                         // its bf16 copies
   size_t scratch_bytes = 0;
   size_t loss_rows = 0, misc = 0;            // misc: loss (float) at +0, remat counter (u64) at +8
   size_t trace = 0, trace_count = 0;         // phase timestamps (u64): start, end, then per (cell/head, m, phase)
@@ -129,23 +138,28 @@ Workspace make_workspace(const Dims& dm, int L, int K, int M, int max_cell_layer
 // (nothing of the workspace layout enters it), for one device holding all K
 // cells.  T tokens per step, Tmb = T/M, e activation element bytes, D the
 // stash depth (M, or min(M, K+1) in the one-forward-one-backward order).
+// The residual stream and its gradient take r = 4 bytes an element, with a
+// bf16 copy (c = 2 bytes; 0 for the fp32 model) of every gradient a GEMM reads.
 //   boundary  the O(N) term: every cell's input for D micro-batches (K D Tmb d
-//             e), the head's output gradient for D micro-batches and, for the
-//             LM, the embedding's input gradient of all M (D Tmb d e + M Tmb d
-//             e), the head's input for two micro-batches and the gradient each
-//             cell receives from the next, double-buffered (2 Tmb d e + 2 K
-//             Tmb d e)
+//             r), the head's output gradient for D micro-batches (D Tmb d (r +
+//             c)) and, for the LM, the embedding's input gradient of all M
+//             (M Tmb d r), the head's input for two micro-batches (2 Tmb d r)
+//             and the gradient each cell receives from the next,
+//             double-buffered (2 K Tmb d (r + c))
 //   cell      the O((L/K)(N/M)) term: one cell (Lc layers) of kept internals
 //             for one micro-batch, a bytes per token and layer (Transformer:
-//             e (8d + 2 ffn) + 16 + 4 heads; FFN block: e (2d + 2 ffn) + 8);
+//             e (6d + 2 ffn) + 2d r + 16 + 4 heads, the layer's output and
+//             mid-residual in fp32; FFN block: e (d + 2 ffn) + d r + 8);
 //             without re-materialisation every layer of every micro-batch,
 //             L M Tmb a, the O(N L) the review starts from
 //   head      one micro-batch's fp32 logits and the final LayerNorm's output,
 //             gradient and statistics (LM only)
 //   grads     one layer's backward working set for one micro-batch: the
-//             gradient chain (3 Tmb d e), the FFN-hidden, attention-output and
-//             QKV gradients double-buffered (2 Tmb (ffn + 4d) e), attention
-//             row sums and LayerNorm partial sums
+//             residual gradient in and out (2 Tmb d (r + c)) and the
+//             mid-residual one (Tmb d r, Transformer), a GEMM output (Tmb d
+//             e), the FFN-hidden, attention-output and QKV gradients
+//             double-buffered (2 Tmb (ffn + 4d) e), attention row sums and
+//             LayerNorm partial sums
 //   rows      per-token losses (4 T)
 //   align     256-byte alignment of the arena's regions
 // survey: the same bound with the constants of the scoping survey's formula

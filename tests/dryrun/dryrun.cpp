@@ -191,14 +191,14 @@ int num_sms() { return g_sms; }
 
 int launch_gemm(const GemmDesc& g, cudaStream_t s) {
   const int es = g.dtype == DT_BF16 ? 2 : 4;
-  const bool f32_out = g.epi == EPI_ACC_F32 || g.epi == EPI_STORE_F32;
+  const bool f32_out = g.epi == EPI_ACC_F32 || g.epi == EPI_STORE_F32 || g.epi == EPI_RESID_F32;
   std::vector<Access> a;
   a.push_back(g.a_kmajor ? mat(g.A, g.M, g.K, g.lda, es, 'R') : mat(g.A, g.K, g.M, g.lda, es, 'R'));
   a.push_back(g.b_kmajor ? mat(g.B, g.N, g.K, g.ldb, es, 'R') : mat(g.B, g.K, g.N, g.ldb, es, 'R'));
   a.push_back(mat(g.C, g.M, g.N, g.ldc, f32_out ? 4 : es, g.epi == EPI_ACC_F32 ? 'A' : 'W'));
   if (g.bias) a.push_back(rng(g.bias, static_cast<uint64_t>(g.N) * 4, 'R'));
   if (g.dbias) a.push_back(rng(g.dbias, static_cast<uint64_t>(g.M) * 4, 'A'));
-  if (g.resid) a.push_back(mat(g.resid, g.M, g.N, g.ldr, es, 'R'));
+  if (g.resid) a.push_back(mat(g.resid, g.M, g.N, g.ldr, g.epi == EPI_RESID_F32 ? 4 : es, 'R'));
   if (g.C2) a.push_back(mat(g.C2, g.M, g.N, g.ldc, es, 'W'));
   if (g.aux) a.push_back(mat(g.aux, g.M, g.N, g.ldaux, es, 'R'));
   const std::string name = "gemm:" + std::to_string(g.M) + ":" + std::to_string(g.N) + ":" + std::to_string(g.K);
@@ -206,27 +206,40 @@ int launch_gemm(const GemmDesc& g, cudaStream_t s) {
   return 0;
 }
 
+int launch_layernorm_fwd_io(int in_dtype, int out_dtype, int rows, int d, const void* x, const float* g,
+                            const float* b, void* y, float* mean, float* rstd, cudaStream_t s) {
+  const uint64_t n = static_cast<uint64_t>(rows) * d;
+  const int ei = in_dtype == DT_BF16 ? 2 : 4, eo = out_dtype == DT_BF16 ? 2 : 4;
+  work(s, "layernorm_fwd",
+       {rng(x, n * ei, 'R'), rng(g, d * 4ull, 'R'), rng(b, d * 4ull, 'R'), rng(y, n * eo, 'W'),
+        rng(mean, rows * 4ull, 'W'), rng(rstd, rows * 4ull, 'W')});
+  return 0;
+}
+
 int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g, const float* b, void* y,
                          float* mean, float* rstd, cudaStream_t s) {
-  const int es = dtype == DT_BF16 ? 2 : 4;
-  const uint64_t n = static_cast<uint64_t>(rows) * d * es;
-  work(s, "layernorm_fwd",
-       {rng(x, n, 'R'), rng(g, d * 4ull, 'R'), rng(b, d * 4ull, 'R'), rng(y, n, 'W'), rng(mean, rows * 4ull, 'W'),
-        rng(rstd, rows * 4ull, 'W')});
+  return launch_layernorm_fwd_io(dtype, dtype, rows, d, x, g, b, y, mean, rstd, s);
+}
+
+int launch_layernorm_bwd_rows_io(int dy_dtype, int x_dtype, int out_dtype, int rows, int d, const void* dy,
+                                 const void* x, const float* mean, const float* rstd, const float* g, const void* dres,
+                                 void* dx, void* dx16, float* scratch, cudaStream_t s) {
+  const uint64_t n = static_cast<uint64_t>(rows) * d;
+  const int ed = dy_dtype == DT_BF16 ? 2 : 4, ex = x_dtype == DT_BF16 ? 2 : 4, eo = out_dtype == DT_BF16 ? 2 : 4;
+  std::vector<Access> a{rng(dy, n * ed, 'R'),        rng(x, n * ex, 'R'),     rng(mean, rows * 4ull, 'R'),
+                        rng(rstd, rows * 4ull, 'R'), rng(g, d * 4ull, 'R'), rng(dx, n * eo, 'W'),
+                        rng(scratch, static_cast<uint64_t>((rows + 7) / 8) * 2 * d * 4, 'W')};
+  if (dres) a.push_back(rng(dres, n * eo, 'R'));
+  if (dx16) a.push_back(rng(dx16, n * 2, 'W'));
+  work(s, "layernorm_bwd_rows", a);
   return 0;
 }
 
 int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const void* x, const float* mean,
                               const float* rstd, const float* g, const void* dres, void* dx, float* scratch,
                               cudaStream_t s) {
-  const int es = dtype == DT_BF16 ? 2 : 4;
-  const uint64_t n = static_cast<uint64_t>(rows) * d * es;
-  std::vector<Access> a{rng(dy, n, 'R'),           rng(x, n, 'R'),          rng(mean, rows * 4ull, 'R'),
-                        rng(rstd, rows * 4ull, 'R'), rng(g, d * 4ull, 'R'), rng(dx, n, 'W'),
-                        rng(scratch, static_cast<uint64_t>((rows + 7) / 8) * 2 * d * 4, 'W')};
-  if (dres) a.push_back(rng(dres, n, 'R'));
-  work(s, "layernorm_bwd_rows", a);
-  return 0;
+  return launch_layernorm_bwd_rows_io(dtype, dtype, dtype, rows, d, dy, x, mean, rstd, g, dres, dx, nullptr, scratch,
+                                      s);
 }
 
 int launch_layernorm_bwd_reduce(int rows, int d, const float* scratch, float* dg, float* db, cudaStream_t s) {
@@ -265,20 +278,30 @@ int launch_mse(int rows, int d, const float* y, const float* t, float, float* lo
   return 0;
 }
 
-int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb, void* x,
-                         cudaStream_t s) {
+int launch_embedding_fwd_io(int out_dtype, int rows, int d, int vocab, const int32_t* tokens, const void* emb, void* x,
+                            cudaStream_t s) {
   work(s, "embedding_fwd",
        {rng(tokens, rows * 4ull, 'R'), rng(emb, static_cast<uint64_t>(vocab) * d * 2, 'R'),
-        rng(x, static_cast<uint64_t>(rows) * d * 2, 'W')});
+        rng(x, static_cast<uint64_t>(rows) * d * (out_dtype == DT_BF16 ? 2 : 4), 'W')});
+  return 0;
+}
+
+int launch_embedding_fwd(int rows, int d, int vocab, const int32_t* tokens, const void* emb, void* x,
+                         cudaStream_t s) {
+  return launch_embedding_fwd_io(DT_BF16, rows, d, vocab, tokens, emb, x, s);
+}
+
+int launch_embedding_bwd_io(int dx_dtype, int rows, int d, int vocab, const int32_t* tokens, const void* dx,
+                            float* demb, cudaStream_t s) {
+  work(s, "embedding_bwd",
+       {rng(tokens, rows * 4ull, 'R'), rng(dx, static_cast<uint64_t>(rows) * d * (dx_dtype == DT_BF16 ? 2 : 4), 'R'),
+        rng(demb, static_cast<uint64_t>(vocab) * d * 4, 'A')});
   return 0;
 }
 
 int launch_embedding_bwd(int rows, int d, int vocab, const int32_t* tokens, const void* dx, float* demb,
                          cudaStream_t s) {
-  work(s, "embedding_bwd",
-       {rng(tokens, rows * 4ull, 'R'), rng(dx, static_cast<uint64_t>(rows) * d * 2, 'R'),
-        rng(demb, static_cast<uint64_t>(vocab) * d * 4, 'A')});
-  return 0;
+  return launch_embedding_bwd_io(DT_BF16, rows, d, vocab, tokens, dx, demb, s);
 }
 
 int launch_rmsprop(size_t n, float* w, float* g, float* v, void* w16, float, float, float, int, cudaStream_t s) {

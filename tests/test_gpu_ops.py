@@ -95,7 +95,42 @@ def test_gemm_tensor_core(b, shape, ak, bk, epi):
         assert rel(host(dC), acc * om.gelu_grad(aux)) <= 6e-3
 
 
-@pytest.mark.parametrize("ak,bk,epi", [(1, 1, 0), (1, 1, 1), (1, 0, 2), (0, 0, 3), (0, 1, 0)])
+@pytest.mark.parametrize("shape", [(384, 640, 512), (200, 136, 200), (1000, 96, 72), (2056, 2568, 264),
+                                   (2048, 1024, 8192)])
+def test_gemm_fp32_residual_epilogue(b, shape):
+    """The residual adds that keep the residual stream in fp32: C (fp32) =
+    (A B^T + bias) + R (fp32), against fp64, through the single-tile and the
+    persistent kernels (ragged tiles; the memory-scaling workload's output
+    projection shape), and with the same bits whatever the SM share (so
+    whichever kernel the share picks)."""
+    t = __import__("torch")
+    M, N, K = shape
+    rng = np.random.default_rng(M + N + K)
+    A = bf16_round(rng.standard_normal((M, K)))
+    B = bf16_round(rng.standard_normal((N, K)) / np.sqrt(K))
+    bias = rng.standard_normal(N).astype(np.float32)
+    R = (rng.standard_normal((M, N)) * 4).astype(np.float32)
+    dA, dB, dbias, dR = dev(A, "bf16"), dev(B, "bf16"), dev(bias), dev(R)
+    outs = []
+    lib = b.lib()
+    for sms in (0, 16):
+        assert lib.gpipe_op_gemm_set_sm_share(sms) == 0
+        dC = t.empty((M, N), dtype=t.float32, device="cuda")
+        rc = lib.gpipe_op_gemm(1, M, N, K, dA.data_ptr(), K, 1, dB.data_ptr(), K, 1, b.EPI_RESID_F32, dC.data_ptr(),
+                               N, dbias.data_ptr(), dR.data_ptr(), N, None, None, 0, stream())
+        assert rc == 0, lib.gpipe_last_error(None)
+        sync()
+        outs.append(host(dC))
+    assert lib.gpipe_op_gemm_set_sm_share(0) == 0
+    want = A @ B.T + bias + R
+    # fp32 accumulation of bf16 products: relative to the product's scale
+    tol = 1e-5 * max(1.0, (K / 1024) ** 0.5)
+    assert np.max(np.abs(outs[0] - want)) <= tol * (np.sqrt(K) * np.abs(B).max() * 4 + 8)
+    assert rel(outs[0], want) <= 1e-5
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("ak,bk,epi", [(1, 1, 0), (1, 1, 1), (1, 0, 2), (0, 0, 3), (0, 1, 0), (1, 1, 5)])
 def test_gemm_fp32_ffma(b, ak, bk, epi):
     M, N, K = 136, 200, 72
     rng = np.random.default_rng(5 + epi)
@@ -112,12 +147,12 @@ def test_gemm_fp32_ffma(b, ak, bk, epi):
     ddb = dev(db0)
     rc = b.lib().gpipe_op_gemm(0, M, N, K, keep[0].data_ptr(), A.shape[1], ak, keep[1].data_ptr(), B.shape[1], bk,
                                epi, dC.data_ptr(), N,
-                               keep[2].data_ptr() if epi < 2 else (ddb.data_ptr() if epi == 3 else None),
-                               keep[3].data_ptr() if epi == 0 else None, N, dC2.data_ptr() if epi == 1 else None,
+                               keep[2].data_ptr() if epi in (0, 1, 5) else (ddb.data_ptr() if epi == 3 else None),
+                               keep[3].data_ptr() if epi in (0, 5) else None, N, dC2.data_ptr() if epi == 1 else None,
                                keep[4].data_ptr() if epi == 2 else None, N, stream())
     assert rc == 0
     sync()
-    if epi == 0:
+    if epi in (0, 5):
         assert rel(host(dC), acc + bias + resid) <= 1e-6
     elif epi == 1:
         assert rel(host(dC), acc + bias) <= 1e-6

@@ -18,7 +18,7 @@ import pytest
 
 from oracle import model as om
 from synth import KIND_LM, WORKLOADS, Workload, make_inputs
-from tests.gpu_util import assert_elementwise, local_scale, rel
+from tests.gpu_util import elementwise_outliers, error_profile, local_scale, rel
 
 pytestmark = pytest.mark.gpu
 
@@ -52,19 +52,19 @@ def _run(b, w, inp, steps=1, keep_grads=True, options=(), K=None, M=None, cost=N
     return gp, st, p0, losses
 
 
-# Element-wise bounds, next to the rel-L2 norms: every element of a group
-# (one parameter of one layer) within a |ref| + b rms(its row of ref), but for
-# at most a fraction of outliers.  bf16: activations are rounded to 8
-# significant bits at every store, through up to 96 layers; the measured
-# per-group rel-L2 is 0.3-2%, and against the row's scale the errors reach
-# 20% only for about one element in 10^4 (the attention weights of the deep
-# stacks, whose gradients go through the softmax's cancellations), so
-# a = b = 0.25 with 3 outliers in 10^4 allowed.  A zeroed or misplaced row of
-# 1024 elements puts most of its elements outside that bound, more than a
-# layer's allowance.  fp32: errors ~1e-6 of the row's scale, bounds at 1e-4
-# with none allowed.
-BF16_ELEM = (0.25, 0.25, 3e-4)
-FP32_ELEM = (1e-4, 1e-4, 0.0)
+# How the error is distributed, next to the rel-L2 norms (tests/gpu_util.py
+# error_profile): in every group (one parameter of one layer) the worst row's
+# rel-L2 (a corrupted row shows there), the worst 64 x 64 block's rel-L2 (a
+# wrong tile shows there) and the largest element error against |ref| plus
+# its row's rms (a wild value shows there).  bf16: activations are rounded to
+# 8 significant bits at every store, through up to 96 layers, and the
+# measured per-group rel-L2 is 0.3-2%; single elements of the deep stacks'
+# attention projections reach their row's scale (their gradients go through
+# the softmax's cancellations), but a row's or a block's rel-L2 averages that
+# noise, so rows and blocks are held to 0.25 and elements to 3.  fp32: errors
+# ~1e-6, bounds 1e-4 (elements 1e-3).
+BF16_LIMITS = {"row": 0.25, "block": 0.25, "elem": 3.0}
+FP32_LIMITS = {"row": 1e-4, "block": 1e-4, "elem": 1e-3}
 
 
 def _offsets(w):
@@ -76,18 +76,21 @@ def _offsets(w):
     return out
 
 
-def _compare_step(w, st, p0, loss, ref_loss, ref_grads, loss_tol, grad_tol, group_tol, elem, upd_thresh):
+def _compare_step(w, st, p0, loss, ref_loss, ref_grads, loss_tol, grad_tol, group_tol, limits, upd_thresh,
+                  flip_frac):
     """GPU step against the oracle's full-batch step, group by group (host
     memory stays at one group at a time): the loss; every gradient group by
-    rel-L2 and element-wise; the whole gradient by rel-L2; and the RMSProp
-    update of every group from the oracle's gradient (v0 = 0), compared where
-    |g| > upd_thresh rms(g) (elsewhere the sign of a first RMSProp step is
-    not fixed by the oracle), and checked to be a valid step everywhere."""
-    assert abs(loss - ref_loss) <= loss_tol * abs(ref_loss), (loss, ref_loss)
+    rel-L2 and by the distribution of its error (rows, 64 x 64 blocks,
+    elements); the whole gradient by rel-L2; and the RMSProp update of every
+    group: its arithmetic on the GPU's own gradient, and against the oracle's
+    update where the gradient's sign is fixed (|g| > upd_thresh times its
+    row's rms; at most flip_frac of those elements flipped by the gradient's
+    own error).  Every group is measured before anything is
+    asserted, so a failure reports the worst groups of every measure."""
     offs = _offsets(w)
-    a, bb, frac = elem
     num = den = 0.0
-    worst = (0.0, "")
+    prof = {}
+    upd_bad = []
     step_max = w.lr / math.sqrt(1 - w.decay)
     masked = 0
     for name, (o, shape) in offs.items():
@@ -96,26 +99,40 @@ def _compare_step(w, st, p0, loss, ref_loss, ref_grads, loss_tol, grad_tol, grou
         gr = np.asarray(ref_grads[name], dtype=np.float64)
         num += float(np.sum((g - gr) ** 2))
         den += float(np.sum(gr ** 2))
-        r = rel(g, gr)
-        worst = max(worst, (r, name))
-        assert_elementwise(g, gr, a, bb, frac, f"gradient {name}")
-        # the update of this group from the oracle's gradient, where the
-        # gradient's sign is fixed by the bound above (|g| > upd_thresh times
-        # its row's rms): RMSProp's first step moves each such weight by
-        # lr g / (sqrt(1 - decay) |g| + eps), the same within fp32 rounding
+        prof[name] = error_profile(g, gr)
+        # the update.  (1) The RMSProp arithmetic itself, on the GPU's own
+        # gradient (v0 = 0): v = (1 - decay) g^2, w -= lr g / (sqrt(v) + eps),
+        # within fp32 rounding everywhere, and no weight moved by more than
+        # lr / sqrt(1 - decay).  (2) Against the oracle's update where the
+        # gradient's sign is fixed (|g| > upd_thresh times its row's rms): the
+        # same step, but for the few elements whose sign the gradient's own
+        # error flips (its element bound allows errors near the row's rms).
         p_init = np.asarray(p0[name], dtype=np.float64)
-        p_ref, v_ref = om.rmsprop({name: p_init}, {name: gr}, {name: np.zeros(shape)}, w.lr, w.decay, w.eps)
         p_gpu = st.p32[o:o + n].double().cpu().numpy().reshape(shape)
         v_gpu = st.v32[o:o + n].double().cpu().numpy().reshape(shape)
-        dw_gpu, dw_ref = p_gpu - p_init, p_ref[name] - p_init
+        dw_gpu = p_gpu - p_init
+        p_own, v_own = om.rmsprop({name: p_init}, {name: g}, {name: np.zeros(shape)}, w.lr, w.decay, w.eps)
+        if not (np.allclose(v_gpu, v_own[name], rtol=1e-6, atol=0.0) and
+                np.allclose(p_gpu, p_own[name], rtol=0.0, atol=1e-6 * (np.abs(p_init) + step_max))):
+            upd_bad.append((name, "RMSProp arithmetic"))
+        if not np.all(np.abs(dw_gpu) <= step_max * (1 + 1e-3)):
+            upd_bad.append((name, "step beyond lr/sqrt(1-decay)"))
+        p_ref, _ = om.rmsprop({name: p_init}, {name: gr}, {name: np.zeros(shape)}, w.lr, w.decay, w.eps)
+        dw_ref = p_ref[name] - p_init
         mask = np.abs(gr) > upd_thresh * local_scale(gr)
         masked += int(mask.sum())
         if mask.any():
-            assert_elementwise(dw_gpu[mask], dw_ref[mask], 1e-2, 0.0, frac, f"update {name}")
-            assert rel(v_gpu[mask], v_ref[name][mask]) <= 4 * group_tol, f"RMSProp state {name}"
-        assert np.all(np.abs(dw_gpu) <= step_max * (1 + 1e-3)), name
-    assert math.sqrt(num / den) <= grad_tol
-    assert worst[0] <= group_tol, worst
+            flips = elementwise_outliers(dw_gpu[mask], dw_ref[mask], 1e-2, 0.0)
+            if flips > max(2, flip_frac * mask.sum()):
+                upd_bad.append((name, flips, int(mask.sum())))
+    report = {k: sorted(((p[k], nm) for nm, p in prof.items()), reverse=True)[:4]
+              for k in ("rel", "row", "block", "elem", "frac25")}
+    assert abs(loss - ref_loss) <= loss_tol * abs(ref_loss), (loss, ref_loss)
+    assert math.sqrt(num / den) <= grad_tol, (math.sqrt(num / den), report)
+    assert report["rel"][0][0] <= group_tol, report
+    for k, lim in limits.items():
+        assert report[k][0][0] <= lim, (k, report)
+    assert not upd_bad, upd_bad
     assert masked > 0.3 * sum(int(np.prod(s)) for _, s in offs.values())
 
 
@@ -124,7 +141,7 @@ def test_tiny_ffn_fp32_step_matches_oracle(b):
     inp = make_inputs(w)
     gp, st, p0, (loss,) = _run(b, w, inp)
     ref = om.step(w, inp["params"], inp)
-    _compare_step(w, st, inp["params"], loss, ref["loss"], ref["grads"], 1e-5, 1e-5, 1e-5, FP32_ELEM, 1e-2)
+    _compare_step(w, st, inp["params"], loss, ref["loss"], ref["grads"], 1e-5, 1e-5, 1e-5, FP32_LIMITS, 1e-2, 0.0)
 
 
 def test_tiny_ffn_two_steps(b):
@@ -147,7 +164,7 @@ def _lm_parity(b, w, inp, loss_tol=1e-3, grad_tol=2e-2, group_tol=5e-2, ref=None
         ref_loss, ref_grads, _ = om.loss_and_grads(w, inp["params"], inp)
     else:
         ref_loss, ref_grads = ref
-    _compare_step(w, st, inp["params"], loss, ref_loss, ref_grads, loss_tol, grad_tol, group_tol, BF16_ELEM, 0.75)
+    _compare_step(w, st, inp["params"], loss, ref_loss, ref_grads, loss_tol, grad_tol, group_tol, BF16_LIMITS, 0.75, 1e-3)
     return gp, st, {"loss": ref_loss, "grads": ref_grads}
 
 
@@ -507,3 +524,42 @@ def test_kernel_times_bracket_the_selected_gemms(b, graph):
     assert np.all(fl == 2.0 * T * w.ffn * w.d)
     assert np.array_equal(st0.host(st0.p32), st1.host(st1.p32))
     assert gp0.kernel_times()[0].size == 0
+
+
+@pytest.mark.parametrize("sched", [0, 1])
+def test_single_lane_activation_memory_measured_within_the_review_bound(b, sched):
+    """The review's "Preliminaries 5" bound O(N + (L/K)(N/M)), written out from
+    the shapes (gpipe_memory_report), against what the GPU writes: the
+    workspace is filled with a sentinel, one step of the single-lane executor
+    (cells in turn, the review's one-accelerator setting) runs, and the 4 KiB
+    pages of the activation region that changed are counted.  They stay within
+    the bound, and the step allocates no device memory.  The concurrent-lane
+    executor writes more: one cell workspace per lane."""
+    import torch
+    w = WORKLOADS["lm_wide"].replace(n=8, M=4, L=8, K=4)
+    inp = make_inputs(w)
+
+    def touched(pipeline):
+        gp = b.GPipe.from_workload(w)
+        gp.set_option(b.OPT_SCHEDULE, sched)
+        gp.set_option(b.OPT_PIPELINE, pipeline)
+        st = b.DeviceState(gp, w, inp)   # workspace sized for this executor
+        layout, bound = gp.memory_report()
+        st.step(want_loss=False)         # captures and instantiates the step's graph
+        st.ws.fill_(0xA5)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        st.step(want_loss=False)
+        torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+        page = 4096
+        region = st.ws[: layout - layout % page].view(-1, page)
+        pages = int((region != 0xA5).any(dim=1).sum().item())
+        return pages * page + (layout % page), free0 - free1, layout, bound
+
+    used, alloc, layout, bound = touched(0)
+    assert alloc <= 0
+    assert used <= bound, (used, bound)
+    assert used >= 0.95 * layout
+    used_lanes, _, lanes_layout, lanes_bound = touched(1)
+    assert lanes_bound == bound and bound < used_lanes <= lanes_layout

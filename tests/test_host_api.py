@@ -137,22 +137,26 @@ def _report(binding, w, K, M, no_remat=False, pipelined=True, inflight=1):
 def _model_from_shapes(w, K, M, schedule, remat):
     """The review's bound O(N + (L/K)(N/M)) in bytes, evaluated here from the
     shapes as gpipe.h documents it (boundary, one cell, head, one layer's
-    backward working set, per-token losses, region alignment)."""
+    backward working set, per-token losses, region alignment; the residual
+    stream and its gradient in fp32, a bf16 copy of each gradient a GEMM
+    reads)."""
     lm = w.kind == 1
     e = 4 if w.dtype == "f32" else 2
+    r, c = 4, (0 if w.dtype == "f32" else 2)
     T = w.tokens
     Tmb = T // M
     d, f, H, V = w.d, w.ffn, (w.heads if lm else 0), (w.vocab if lm else 0)
     D = min(M, K + 1) if schedule == 1 else M
     Lc = -(-w.L // K)
-    act = Tmb * d * e
-    boundary = K * D * act + D * act + (M * act if lm else 0) + 2 * act + 2 * K * act
-    a = e * (8 * d + 2 * f) + 16 + 4 * H if lm else e * (2 * d + 2 * f) + 8
+    act, gcp = Tmb * d * r, Tmb * d * (r + c)
+    boundary = K * D * act + D * gcp + (M * act if lm else 0) + 2 * act + 2 * K * gcp
+    a = e * (6 * d + 2 * f) + 2 * d * r + 16 + 4 * H if lm else e * (d + 2 * f) + d * r + 8
     cell = Lc * Tmb * a if remat else w.L * M * Tmb * a
     lnp = 2 * (-(-Tmb // 8)) * 2 * d * 4
     head = Tmb * (4 * V + 2 * d * e + 8) + lnp if lm else 0
-    grads = 3 * act + 2 * Tmb * (f + (4 * d if lm else 0)) * e + Tmb * max(H, 1) * 4 + lnp
-    align = 256 * (13 * (Lc if remat else w.L * M) + 48)
+    grads = 2 * gcp + (act if lm else 0) + Tmb * d * e + 2 * Tmb * (f + (4 * d if lm else 0)) * e + \
+        Tmb * max(H, 1) * 4 + lnp
+    align = 256 * (13 * (Lc if remat else w.L * M) + 56)
     return boundary + cell + head + grads + 4 * T + align
 
 
@@ -199,7 +203,7 @@ def test_two_in_flight_cost_one_more_cell_workspace_per_cell(binding):
     # set) and one more slot in the head's input ring (three instead of two)
     Tmb = w.tokens // w.M
     head_set = Tmb * (2 * w.d * 2 + 8 + w.vocab * 4) + 2 * (-(-Tmb // 8)) * 2 * w.d * 4
-    lane = (one - serial - head_set - Tmb * w.d * 2) / (w.K - 1)  # one lane's workspace
+    lane = (one - serial - head_set - Tmb * w.d * 4) / (w.K - 1)  # one lane's workspace
     assert lane > 0
     assert two - one == pytest.approx(w.K * lane, rel=1e-4)
     with pytest.raises(binding.GpipeError):
@@ -212,8 +216,8 @@ def test_two_in_flight_cost_one_more_cell_workspace_per_cell(binding):
     assert auto_small == two_small and auto_wide == one
     # S in flight: S-1 more lane workspaces per cell, and the gradient ring S deep
     four, _, _ = _report(binding, w, w.K, w.M, inflight=4)
-    stash = w.tokens // w.M * w.d * 2
-    assert four - one == pytest.approx(3 * w.K * lane + 2 * w.K * stash, rel=1e-4)
+    ring_slot = w.tokens // w.M * w.d * 6  # fp32 gradient and its bf16 copy
+    assert four - one == pytest.approx(3 * w.K * lane + 2 * w.K * ring_slot, rel=1e-4)
 
 
 @pytest.mark.parametrize("pipelined", [False, True])
@@ -232,7 +236,11 @@ def test_memory_scales_as_review_bound_over_sweep_grid(binding, pipelined):
         assert peak <= bound or pipelined
         T = w.tokens
         lanes = K if pipelined else 1
-        row = [(K + 2) * T, lanes * (w.L / K) * T / M, lanes * T / M]
+        # the gradient ring between cells holds 2 K micro-batches: a K (N/M)
+        # term (within O(N)), a lane's buffers with the lanes
+        row = [(K + 2) * T, lanes * (w.L / K) * T / M, K * T / M]
+        if not pipelined:
+            row.append(T / M)
         if pipelined:
             row.append((2 if M > 1 else 1) * T / M)
         rows.append(row)
@@ -285,7 +293,7 @@ def test_options_are_validated_and_kernel_times_start_empty(binding):
     with pytest.raises(binding.GpipeError) as e:
         g.set_option(999, 1)
     assert e.value.code == -1   # GPIPE_ERR_INVALID_ARG
-    for bad in (-1, 6):
+    for bad in (-1, binding.EPI_RESID_F32 + 2):
         with pytest.raises(binding.GpipeError):
             g.set_option(binding.OPT_KERNEL_TIMES, bad)
     for bad in (24, 801):
@@ -428,9 +436,10 @@ def test_one_f_one_b_keeps_a_shorter_stash(binding, name):
     peak1, bound1 = g.memory_report()
     ws1 = g.sizes()[1]
     D = min(w.M, w.K + 1)
-    stash = w.tokens // w.M * w.d * 2
-    # K cell inputs and the head's output gradient each hold D instead of M
-    assert peak0 - peak1 == (w.K + 1) * (w.M - D) * stash
+    Tmb_d = w.tokens // w.M * w.d
+    # K cell inputs (fp32) and the head's output gradient (fp32 and its bf16
+    # copy) each hold D micro-batches instead of M
+    assert peak0 - peak1 == (w.M - D) * Tmb_d * (4 * w.K + 6)
     assert ws0 - ws1 == peak0 - peak1
     assert bound0 - bound1 == peak0 - peak1
     g.set_option(binding.OPT_PIPELINE, 0)
