@@ -116,47 +116,88 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def oracle_sample(w, budget_s=15.0):
-    """Time the oracle's full step on a sub-batch sized to about budget_s."""
-    from oracle import model as om
-    from synth import make_inputs
-    n = 1
-    sub = w.replace(n=n, M=1, K=1)
-    inp = make_inputs(sub)
-    t0 = time.perf_counter()
-    om.step(sub, inp["params"], inp)
-    dt = time.perf_counter() - t0
-    while dt < budget_s / 3 and n * 2 <= w.n:
-        n *= 2
-        sub = w.replace(n=n, M=1, K=1)
-        inp = make_inputs(sub)
+# Deeper workloads are sampled in depth: the oracle runs one sequence through
+# a few of the (identical) layers, and its time for the full depth is
+# extrapolated linearly in the layer count from two measured depths.
+SAMPLE_DEPTHS = (4, 8)
+
+
+class OracleSample:
+    """A bounded sample of a workload for timing the fp64 oracle on the host.
+
+    Up to 8 layers: the oracle's full step on a sub-batch of the workload
+    (1, 2, 4, ... sequences, doubled while a step takes under budget_s / 3).
+    Deeper: one sequence through SAMPLE_DEPTHS[0] and SAMPLE_DEPTHS[1] layers
+    of the same shape; a full-depth step's time is the deeper sample's plus
+    (L - its depth) times the measured time per layer (their difference over
+    the difference in depth)."""
+
+    def __init__(self, w, budget_s=15.0):
+        from synth import make_inputs
+        self.w = w
+        self.deep = w.L > SAMPLE_DEPTHS[1]
+        if self.deep:
+            self.subs = [w.replace(n=1, M=1, K=1, L=l) for l in SAMPLE_DEPTHS]
+            self.inps = [make_inputs(sw) for sw in self.subs]
+            self.tokens = self.subs[0].tokens
+            return
+        n = 1
+        while True:
+            sub = w.replace(n=n, M=1, K=1)
+            inp = make_inputs(sub)
+            dt = self._one(sub, inp)
+            if dt >= budget_s / 3 or n * 2 > w.n:
+                break
+            n *= 2
+        self.subs, self.inps, self.tokens = [sub], [inp], sub.tokens
+
+    @staticmethod
+    def _one(sub, inp):
+        from oracle import model as om
         t0 = time.perf_counter()
         om.step(sub, inp["params"], inp)
-        dt = time.perf_counter() - t0
-    return sub, inp, dt
+        return time.perf_counter() - t0
+
+    def warm(self):
+        """One step of every sample; returns the per-layer time (deep) or None."""
+        ts = [self._one(sw, ip) for sw, ip in zip(self.subs, self.inps)]
+        if self.deep:
+            self.t_layer = max(ts[1] - ts[0], 0.0) / (SAMPLE_DEPTHS[1] - SAMPLE_DEPTHS[0])
+        return ts
+
+    def step(self):
+        """Seconds of one full-depth oracle step (measured, or extrapolated in depth)."""
+        t = self._one(self.subs[-1], self.inps[-1])
+        if self.deep:
+            return t + (self.w.L - SAMPLE_DEPTHS[1]) * self.t_layer
+        return t
+
+    def describe(self):
+        sw = self.subs[-1]
+        if self.deep:
+            return (f"one sequence of {sw.seq} tokens of the {self.w.name} layers, fp64 full-batch step at "
+                    f"{SAMPLE_DEPTHS[0]} and {SAMPLE_DEPTHS[1]} layers; the time of the full {self.w.L} layers "
+                    f"extrapolated linearly in depth (identical layers)")
+        return (f"full-batch fp64 step on a sub-batch of {sw.n} sequence(s) x {sw.seq} tokens of the "
+                f"{self.w.name} layers (no micro-batching)")
 
 
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from oracle import model as om
-    sub, inp, _ = oracle_sample(w, budget_s=6.0)
-    for _ in range(args.warmup):
-        om.step(sub, inp["params"], inp)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        om.step(sub, inp["params"], inp)
-    dt = (time.perf_counter() - t0) / args.steps
-    toks = sub.tokens / dt
+    smp = OracleSample(w, budget_s=6.0)
+    for _ in range(max(args.warmup, 1)):
+        smp.warm()
+    dt = sum(smp.step() for _ in range(args.steps)) / args.steps
+    toks = smp.tokens / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": toks, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg(w, args),
         "cpu_baseline": {"value": toks, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"full-batch fp64 step on a sub-batch of {sub.n} sequences x {sub.seq} tokens "
-                                   f"of the {w.name} layers (no micro-batching)"},
+                         "sample": smp.describe()},
         "e2e": {"value": toks, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -231,6 +272,15 @@ def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
         args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), K, 1, 4, C.data_ptr(), N, None, None, 0,
                 None, None, 0)
         name = f"logits GEMM (fp32 store) {M}x{N}x{K}"
+    elif epi == 5:
+        A = torch.randn(M, K, device="cuda").to(bf)
+        Bw = torch.randn(N, K, device="cuda").to(bf)
+        vec = torch.zeros(N, device="cuda")
+        R = torch.randn(M, N, device="cuda")
+        C = torch.empty(M, N, device="cuda")
+        args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), K, 1, 5, C.data_ptr(), N, vec.data_ptr(),
+                R.data_ptr(), N, None, None, 0)
+        name = f"residual GEMM (bias + fp32 residual, fp32 store) {M}x{N}x{K}"
     elif epi == 3:
         A = torch.randn(K, M, device="cuda").to(bf)
         Bw = torch.randn(K, N, device="cuda").to(bf)
@@ -361,9 +411,8 @@ def live_roofline(b, gp, st, peaks, args):
     classes = {}
     for epi in sorted(EPI_NAMES):
         gp.set_option(b.OPT_KERNEL_TIMES, epi + 1)
-        st.step(want_loss=False)
-        st.step(want_loss=False)
-        ms, fl, mnk = gp.kernel_times(with_shapes=True)  # the launches of the last step
+        st.step(want_loss=False)  # captures the step with the timing events and runs it
+        ms, fl, mnk = gp.kernel_times(with_shapes=True)  # the launches of that step
         if ms.size:
             shapes = {}
             for t, f, s in zip(ms, fl, mnk):
@@ -516,10 +565,11 @@ def run_ours(args, w):
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            sub, _, dt = oracle_sample(w)
-            cpu = {"value": sub.tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                   "sample": f"one full-batch fp64 oracle step on {sub.n} sequence(s) x {sub.seq} tokens of the "
-                             f"{w.name} layers ({dt:.1f} s)"}
+            smp = OracleSample(w)
+            smp.warm()
+            dt = smp.step()
+            cpu = {"value": smp.tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": smp.describe() + f" ({dt:.1f} s per step)"}
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -551,7 +601,7 @@ def run_sweep(args):
     from micro_pipeline_re_gb300 import binding as b
     from synth import SWEEP_GRID, WORKLOADS, make_inputs
     peaks = load_peaks()
-    w0 = WORKLOADS[args.workload if args.workload != "lm_small" else "lm_sweep"]
+    w0 = WORKLOADS[args.workload if args.workload not in ("lm_small", "lm_deep") else "lm_sweep"]
     inp = make_inputs(w0)
     for K, M in SWEEP_GRID:
         w = w0.replace(K=K, M=M)
@@ -586,10 +636,11 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="lm_small")
+    ap.add_argument("--workload", default="lm_deep",
+                    help="the memory-scaling workload (the largest that one GPU holds) by default")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--probe-gemm", action="store_true",
                     help="only run the roofline GEMM (5 eager launches, then a timed graph); for profilers")
@@ -598,7 +649,7 @@ def main():
                     help="--probe-gemm: the GEMM's SM share (its grid as the step would size it); 0: all SMs")
     ap.add_argument("--epi", type=int, default=1,
                     help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 2 GELU backward, 3 weight gradient, "
-                         "4 fp32 store")
+                         "4 fp32 store, 5 bias + fp32 residual")
     ap.add_argument("--reps", type=int, default=100)
     ap.add_argument("--schedule", default="gpipe", choices=sorted(SCHEDULES),
                     help="issue order: gpipe (all forwards, then all backwards) or 1f1b (interleaved, shorter stash)")

@@ -91,11 +91,11 @@ int gpipe_op_layernorm_bwd(int dtype, int rows, int d, const void* dy, const voi
  * every GPU that loads the library keeps until the process exits; it calls no
  * allocation routine.  Limit: ceil(rows / 8) * 2 * d <= 2^20 (for d = 1024,
  * rows <= 4096); larger sizes return GPIPE_ERR_INVALID_ARG with a message.
- * The first call on each device looks up the array's device address (with that
- * device current) and keeps it for the life of the process; make that first
- * call before any stream capture.  cudaDeviceReset (or anything else that
- * destroys the device's primary context) invalidates the kept address: do not
- * call this entry point on a device after resetting it.  All calls
+ * Every call looks up the array's device address in the current context (no
+ * allocation and no stream work), so a context re-created after
+ * cudaDeviceReset is served correctly; the first lookup on a device may load
+ * the library's device image, so make the first call before any stream
+ * capture.  All calls
  * share the one array: every partial sum the call reads is written by the
  * same call, so nothing needs clearing, but calls that overlap on the GPU (on
  * different streams, or from different threads) race on it. */

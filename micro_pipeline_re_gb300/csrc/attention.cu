@@ -145,8 +145,8 @@ __device__ __forceinline__ float row_dot64(const __nv_bfloat16* o, const __nv_bf
 // Warps 0-3 (128 threads) own the rows; warp 4's lane 0 issues every TMA copy
 // and every MMA, so that waiting on a copy never stalls the softmax.  Per key
 // block j, hand-offs through mbarriers:
-//   issuer:  S_j = Q K_j^T (once the rows have read S_{j-1} out of TMEM)
-//            -> commit bs;  K_{j+1} into the other K buffer;
+//   issuer:  S_{j+1} = Q K_{j+1}^T as soon as the rows have read S_j out of
+//            TMEM -> commit bs;  K_{j+2} into S_j's K buffer;
 //            O += P_j V_j (once the rows wrote P_j and rescaled O, and
 //            O += P_{j-1} V_{j-1} is done) -> commit bo;  V_{j+1}.
 //   rows:    wait bs; read S_j; arrive bsc (S consumed); the running max;
@@ -154,6 +154,10 @@ __device__ __forceinline__ float row_dot64(const __nv_bfloat16* o, const __nv_bf
 //            rescale O; write P_j; arrive bp.
 // So S_{j+1} computes while the rows work on block j.
 constexpr int FWD_THREADS = 160;
+// Two CTAs of five warps put three warps on some of an SM's four sub-partitions,
+// each of which holds a quarter of the register file (16384): at most 170
+// registers a thread (168 after the allocation granularity) keep two CTAs per SM.
+constexpr int ATTN_MAXNREG = 168;
 // Q, K x2, V x2, P (2 sub-tiles), barriers.  No slack for aligning the base:
 // with no static shared memory the dynamic window starts 1024-byte aligned
 // (checked at run time), and without the slack two CTAs fit on an SM.
@@ -170,7 +174,7 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__global__ void __launch_bounds__(FWD_THREADS) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq,
+__global__ void __maxnreg__(ATTN_MAXNREG) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq,
                                                                __nv_bfloat16* __restrict__ out,
                                                                float* __restrict__ lse, int seq, int heads, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -235,25 +239,31 @@ __global__ void __launch_bounds__(FWD_THREADS) attn_fwd_kernel(const __grid_cons
         tma_load_2d(sV + j * T128, &tq, 2 * D + h * HD, row0 + j * 128, &bv[j]);
         ++nv[j];
       }
-      for (int j = 0; j < nkb; ++j) {
-        const int kb = j & 1;
-        if (j == 0 && !await(bq, 0, err, DERR_MMA_WAIT, abort)) break;
-        if (!await(&bk[kb], (j >> 1) & 1, err, DERR_MMA_WAIT, abort)) break;
-        if (j > 0 && !await(bsc, (j - 1) & 1, err, DERR_MMA_WAIT, abort)) break;  // S_{j-1} read out
-        tc_fence_after();
-        {
-          const uint32_t q = smem_u32(sQ), k = smem_u32(sK + kb * T128);
+      auto issue_s = [&](int jj) {  // S_jj = Q K_jj^T into TMEM (K_jj loaded, S_{jj-1} read out)
+        const uint32_t q = smem_u32(sQ), k = smem_u32(sK + (jj & 1) * T128);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(q, kk), kdesc(k, kk), idS, kk ? 1u : 0u);
-          tc_commit(bs);
+        for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(q, kk), kdesc(k, kk), idS, kk ? 1u : 0u);
+        tc_commit(bs);
+      };
+      bool go = await(bq, 0, err, DERR_MMA_WAIT, abort) && await(&bk[0], 0, err, DERR_MMA_WAIT, abort);
+      if (go) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int j = 0; j < nkb && go; ++j) {
+        const int kb = j & 1;
+        if (j + 1 < nkb) {  // S_{j+1} as soon as the rows have read S_j: it computes during block j's softmax
+          if (!await(&bk[(j + 1) & 1], ((j + 1) >> 1) & 1, err, DERR_MMA_WAIT, abort)) break;
+          if (!await(bsc, j & 1, err, DERR_MMA_WAIT, abort)) break;
+          tc_fence_after();
+          issue_s(j + 1);
+          if (j + 2 < nkb) {  // K buffer of block j: S_j is done
+            mbar_arrive_expect_tx(&bk[kb], T128);
+            tma_load_2d(sK + kb * T128, &tq, D + h * HD, row0 + (j + 2) * 128, &bk[kb]);
+            ++nk[kb];
+          }
         }
-        if (j >= 1 && j + 1 < nkb) {  // K buffer of block j-1: its product S_{j-1} is done
-          const int nb = (j + 1) & 1;
-          mbar_arrive_expect_tx(&bk[nb], T128);
-          tma_load_2d(sK + nb * T128, &tq, D + h * HD, row0 + (j + 1) * 128, &bk[nb]);
-          ++nk[nb];
-        }
-        if (!await(bp, j & 1, err, DERR_MMA_WAIT, abort)) break;              // P_j written, O rescaled
+        if (!await(bp, j & 1, err, DERR_MMA_WAIT, abort)) break;                 // P_j written, O rescaled
         if (j > 0 && !await(bo, (j - 1) & 1, err, DERR_MMA_WAIT, abort)) break;  // O += P_{j-1} V_{j-1} done
         if (j >= 1 && j + 1 < nkb) {  // V buffer of block j-1 is free
           const int nb = (j + 1) & 1;
@@ -311,17 +321,6 @@ __global__ void __launch_bounds__(FWD_THREADS) attn_fwd_kernel(const __grid_cons
         ok = __all_sync(0xffffffffu, await(bo, (j - 1) & 1, err, DERR_ACC_WAIT, abort));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {  // warp-uniform: tcgen05 loads/stores are per warp
-          uint32_t u[64];
-          tmem_ld32(tO + lane, u);
-          tmem_ld32(tO + lane + 32, u + 32);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 64; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(tO + lane, u);
-          tmem_st32(tO + lane + 32, u + 32);
-          tmem_st_wait();
-        }
       }
       // P = exp2(s - m) as bf16 into shared memory, and its row sum
       float rs = 0.f;
@@ -334,6 +333,19 @@ __global__ void __launch_bounds__(FWD_THREADS) attn_fwd_kernel(const __grid_cons
           rs += pc[i];
         }
         st_row32_bf16(sP + (c >> 1) * T128, r, (c & 1) * 4, pc);
+      }
+      // then O *= alpha, with S's registers free again
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // warp-uniform: tcgen05 loads/stores are per warp
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tO + lane + 32 * c, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(tO + lane + 32 * c, u);
+        }
+        tmem_st_wait();
       }
       l = l * alpha + rs;
       fence_proxy_async_smem();
@@ -376,12 +388,21 @@ __global__ void __launch_bounds__(256) attn_dvec_kernel(const __nv_bfloat16* __r
 
 // dQ CTA: Q, dO (128 rows), K and V blocks of 64 keys (two buffers each), dS
 // (128 x 64).  dK/dV CTA: K, V (128 rows), Q and dO blocks of 64 queries (two
-// buffers each), P^T and dS^T (128 x 64), LSE and D of the query block.
+// buffers each), P^T and dS^T (128 x 64), LSE and D of two query blocks.
+// Both: warps 0-3 the rows, warp 4's lane 0 the issuer of every copy and
+// product, hand-offs through mbarriers as in the forward:
+//   issuer:  the products S, dP of block t+1 as soon as the rows have read
+//            block t's out of TMEM -> commit bs;  the gradient product of
+//            block t (once the rows wrote its dS, or P^T and dS^T) -> commit
+//            bo;  block t+2's tiles into block t's buffers (after bo(t)).
+//   rows:    wait bs; read S, dP; arrive bsc; the elementwise gradient; wait
+//            bo(t-1) (the previous gradient product reads the same shared
+//            tile); write it; arrive bp.
+constexpr int BWD_THREADS = 160;
 constexpr int BWD_TILES = 4 * T128 + 4 * T64;  // the larger of the two kinds' tiles (dK/dV: 96 KB)
 constexpr int BWD_LD = BWD_TILES;               // dK/dV: LSE and D of two query blocks (1 KB)
 constexpr int BWD_BAR = BWD_LD + 4 * 64 * 4;
 constexpr int BWD_SMEM = 1024 + BWD_BAR + 128;
-
 __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, const CUtensorMap* td128,
                             const float* __restrict__ lse, const float* __restrict__ dvec,
                             __nv_bfloat16* __restrict__ dqkv, int seq, int heads, int b, int* err, uint8_t* sm) {
@@ -391,8 +412,9 @@ __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, c
   uint8_t* sV = sK + 2 * T64;         // two 64-row buffers
   uint8_t* sdS = sV + 2 * T64;        // 128 rows x 64 keys (ends at 80 KB)
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + BWD_BAR);
-  uint64_t *bq = bar, *bkv = bar + 1, *bs = bar + 3, *bo = bar + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
+  uint64_t *bq = bar, *bkv = bar + 1, *bs = bar + 3, *bsc = bar + 4, *bp = bar + 5, *bo = bar + 6, *bfin = bar + 7;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int r = threadIdx.x, warp = r >> 5;
   const int nqb = (seq + 127) / 128;
@@ -409,7 +431,12 @@ __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, c
     prefetch_tmap(tq64);
     prefetch_tmap(tq128);
     prefetch_tmap(td128);
-    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    mbar_init(bsc, 128);
+    mbar_init(bp, 128);
+    mbar_init(bo, 1);
+    mbar_init(bfin, 1);
+    *abort = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -421,91 +448,109 @@ __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t tS = tmem, tP = tmem + 64, tQ = tmem + 128;
 
-  int nkv_issued[2] = {0, 0};
-  if (r == 0) {
-    mbar_arrive_expect_tx(bq, 2 * T128);
-    tma_load_2d(sQ, tq128, h * HD, row0 + q0, bq);
-    tma_load_2d(sdO, td128, h * HD, row0 + q0, bq);
-    for (int j = 0; j < 2 && j < nkb; ++j) {
-      mbar_arrive_expect_tx(&bkv[j], 2 * T64);
-      tma_load_2d(sK + j * T64, tq64, D + h * HD, row0 + j * 64, &bkv[j]);
-      tma_load_2d(sV + j * T64, tq64, 2 * D + h * HD, row0 + j * 64, &bkv[j]);
-      nkv_issued[j] = 1;
-    }
-  }
-  // this row's log-sum-exp (log2 domain) and D = rowsum(dO o O)
-  float L2 = 0.f, Dr = 0.f;
-  if (qi < seq) {
-    const int64_t row = static_cast<int64_t>(row0) + qi;
-    L2 = lse[row * heads + h] * kLog2e;
-    Dr = dvec[row * heads + h];
-  }
-  bool ok = true;
-  constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
-  constexpr uint32_t idQ = mma_idesc_bf16(128, 64, false, true);
-  for (int j = 0; j < nkb; ++j) {
-    const int kb = j & 1;
-    if (r == 0) {  // S = Q K_j^T, dP = dO V_j^T
-      bool w = (j > 0 || mbar_wait_bounded(bq, 0, err, DERR_MMA_WAIT)) &&
-               mbar_wait_bounded(&bkv[kb], (j >> 1) & 1, err, DERR_MMA_WAIT);
-      if (w) {
-        tc_fence_after();
+  if (warp == 4) {
+    if (r == 128) {  // ---- issuer ----
+      constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idQ = mma_idesc_bf16(128, 64, false, true);
+      int nkv[2] = {0, 0};
+      mbar_arrive_expect_tx(bq, 2 * T128);
+      tma_load_2d(sQ, tq128, h * HD, row0 + q0, bq);
+      tma_load_2d(sdO, td128, h * HD, row0 + q0, bq);
+      for (int j = 0; j < 2 && j < nkb; ++j) {
+        mbar_arrive_expect_tx(&bkv[j], 2 * T64);
+        tma_load_2d(sK + j * T64, tq64, D + h * HD, row0 + j * 64, &bkv[j]);
+        tma_load_2d(sV + j * T64, tq64, 2 * D + h * HD, row0 + j * 64, &bkv[j]);
+        ++nkv[j];
+      }
+      auto issue_sp = [&](int jj) {  // S = Q K_jj^T, dP = dO V_jj^T (block jj loaded, block jj-1's read out)
+        const int kb = jj & 1;
         const uint32_t q = smem_u32(sQ), dO = smem_u32(sdO), k = smem_u32(sK + kb * T64), v = smem_u32(sV + kb * T64);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(q, kk), kdesc(k, kk), idSP, kk ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tP, kdesc(dO, kk), kdesc(v, kk), idSP, kk ? 1u : 0u);
-        tc_commit(bs);  // also covers the previous block's dQ += dS K
+        tc_commit(bs);
+      };
+      bool go = await(bq, 0, err, DERR_MMA_WAIT, abort) && await(&bkv[0], 0, err, DERR_MMA_WAIT, abort);
+      if (go) {
+        tc_fence_after();
+        issue_sp(0);
       }
+      for (int j = 0; j < nkb && go; ++j) {
+        const int kb = j & 1;
+        if (j + 1 < nkb) {  // the next block's S, dP as soon as the rows have read block j's
+          if (!await(&bkv[(j + 1) & 1], ((j + 1) >> 1) & 1, err, DERR_MMA_WAIT, abort)) break;
+          if (!await(bsc, j & 1, err, DERR_MMA_WAIT, abort)) break;
+          tc_fence_after();
+          issue_sp(j + 1);
+        }
+        if (!await(bp, j & 1, err, DERR_MMA_WAIT, abort)) break;  // dS_j written
+        tc_fence_after();
+        {
+          const uint32_t ds = smem_u32(sdS), k = smem_u32(sK + kb * T64);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tQ, kdesc(ds, kk), mndesc(k, kk), idQ, (j | kk) ? 1u : 0u);
+          tc_commit(bo);
+        }
+        if (j + 2 < nkb) {  // block j's buffers, once dQ += dS_j K_j is done
+          if (!await(bo, j & 1, err, DERR_MMA_WAIT, abort)) break;
+          mbar_arrive_expect_tx(&bkv[kb], 2 * T64);
+          tma_load_2d(sK + kb * T64, tq64, D + h * HD, row0 + (j + 2) * 64, &bkv[kb]);
+          tma_load_2d(sV + kb * T64, tq64, 2 * D + h * HD, row0 + (j + 2) * 64, &bkv[kb]);
+          ++nkv[kb];
+        }
+      }
+      tc_commit(bfin);
+      mbar_wait_bounded(bfin, 0, err, DERR_DRAIN_WAIT);
+      for (int bb = 0; bb < 2; ++bb)
+        if (nkv[bb]) mbar_wait_bounded(&bkv[bb], (nkv[bb] - 1) & 1, err, DERR_DRAIN_WAIT);
+      mbar_wait_bounded(bq, 0, err, DERR_DRAIN_WAIT);
     }
-    ok = mbar_wait_bounded(bs, j & 1, err, DERR_ACC_WAIT);
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    tc_fence_after();
-    if (r == 0 && j >= 1 && j + 1 < nkb) {  // buffers of block j-1 are free
-      const int nb = (j + 1) & 1;
-      mbar_arrive_expect_tx(&bkv[nb], 2 * T64);
-      tma_load_2d(sK + nb * T64, tq64, D + h * HD, row0 + (j + 1) * 64, &bkv[nb]);
-      tma_load_2d(sV + nb * T64, tq64, 2 * D + h * HD, row0 + (j + 1) * 64, &bkv[nb]);
-      ++nkv_issued[nb];
+  } else {  // ---- rows ----
+    const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
+    // this row's log-sum-exp (log2 domain) and D = rowsum(dO o O)
+    float L2 = 0.f, Dr = 0.f;
+    if (qi < seq) {
+      const int64_t row = static_cast<int64_t>(row0) + qi;
+      L2 = lse[row * heads + h] * kLog2e;
+      Dr = dvec[row * heads + h];
     }
-    {
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      ok = __all_sync(0xffffffffu, await(bs, j & 1, err, DERR_ACC_WAIT, abort));
+      if (!ok) break;
+      tc_fence_after();
       float v[128];  // S (64 columns), then dP (64 columns), one round trip
-      const uint32_t a[4] = {tS + lane, tS + lane + 32, tP + lane, tP + lane + 32};
-      ld_rows<4>(a, v);
+      {
+        const uint32_t a[4] = {tS + lane, tS + lane + 32, tP + lane, tP + lane + 32};
+        ld_rows<4>(a, v);
+      }
+      tc_fence_before();
+      mbar_arrive1(bsc);
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const bool vis = j * 64 + i <= qi;
         const float p = vis ? fast_exp2(v[i] * kScaleLog2 - L2) : 0.f;
         v[i] = p * (v[64 + i] - Dr);  // dS
       }
+      if (j > 0) {  // the previous dQ product reads the dS tile
+        ok = __all_sync(0xffffffffu, await(bo, (j - 1) & 1, err, DERR_ACC_WAIT, abort));
+        if (!ok) break;
+      }
       st_row32_bf16(sdS, r, 0, v);
       st_row32_bf16(sdS, r, 4, v + 32);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive1(bp);
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (r == 0) {  // dQ += dS K_j
-      tc_fence_after();
-      const uint32_t ds = smem_u32(sdS), k = smem_u32(sK + kb * T64);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tQ, kdesc(ds, kk), mndesc(k, kk), idQ, (j | kk) ? 1u : 0u);
+    if (ok) ok = __all_sync(0xffffffffu, await(bo, (nkb - 1) & 1, err, DERR_ACC_WAIT, abort));
+    tc_fence_after();
+    if (ok) {
+      const int64_t row = static_cast<int64_t>(row0) + qi;
+      store_row64(tQ + lane, dqkv + row * ld + h * HD, 0.125f, qi < seq);
     }
-  }
-  if (r == 0) tc_commit(bo);
-  const bool okd = __syncthreads_and(mbar_wait_bounded(bo, 0, err, DERR_ACC_WAIT));
-  tc_fence_after();
-  if (ok && okd) {
-    const int64_t row = static_cast<int64_t>(row0) + qi;
-    store_row64(tQ + lane, dqkv + row * ld + h * HD, 0.125f, qi < seq);
-  }
-  if (r == 0) {
-    for (int kb = 0; kb < 2; ++kb)
-      if (nkv_issued[kb]) mbar_wait_bounded(&bkv[kb], (nkv_issued[kb] - 1) & 1, err, DERR_DRAIN_WAIT);
-    mbar_wait_bounded(bq, 0, err, DERR_DRAIN_WAIT);
   }
   tc_fence_before();
   __syncthreads();
@@ -527,8 +572,10 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
   float* sL = reinterpret_cast<float*>(sm + BWD_LD);  // [2][64]
   float* sD = sL + 128;                               // [2][64]
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + BWD_BAR);
-  uint64_t *bkv = bar, *bq = bar + 1, *bs = bar + 3, *bo = bar + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 6);
+  uint64_t *bkv = bar, *bq = bar + 1, *bs = bar + 3, *bsc = bar + 4, *bp = bar + 5, *bo = bar + 6, *bfin = bar + 7,
+           *bld = bar + 8;  // bld[2]: the LSE and D of a block are in their slot (64 writers)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 10);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int r = threadIdx.x, warp = r >> 5;
   const int kb = blockIdx.x;  // the key blocks with the most queries first
@@ -537,7 +584,7 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
   const int64_t ld = 3 * static_cast<int64_t>(D);
   const int row0 = b * seq;
   const int k0 = kb * 128;
-  const int kr = k0 + r;  // this thread's key
+  const int kr = k0 + r;  // the key of row thread r
   const int i0 = k0 / 64, nq = seq / 64;  // 64-query blocks i0..nq-1 see this key block
   const int niter = nq - i0;
 
@@ -545,7 +592,14 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
     prefetch_tmap(tq64);
     prefetch_tmap(tq128);
     prefetch_tmap(td64);
-    for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+    mbar_init(bsc, 128);
+    mbar_init(bp, 128);
+    mbar_init(bo, 1);
+    mbar_init(bfin, 1);
+    mbar_init(&bld[0], 64);
+    mbar_init(&bld[1], 64);
+    *abort = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -557,112 +611,135 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t tS = tmem, tP = tmem + 64, tV = tmem + 128, tK = tmem + 192;
 
-  int nq_issued[2] = {0, 0};
-  if (r == 0) {
-    mbar_arrive_expect_tx(bkv, 2 * T128);
-    tma_load_2d(sK, tq128, D + h * HD, row0 + k0, bkv);
-    tma_load_2d(sV, tq128, 2 * D + h * HD, row0 + k0, bkv);
-    for (int t = 0; t < 2 && t < niter; ++t) {
-      mbar_arrive_expect_tx(&bq[t], 2 * T64);
-      tma_load_2d(sQ + t * T64, tq64, h * HD, row0 + (i0 + t) * 64, &bq[t]);
-      tma_load_2d(sdO + t * T64, td64, h * HD, row0 + (i0 + t) * 64, &bq[t]);
-      nq_issued[t] = 1;
-    }
-  }
-  bool ok = true;
-  constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
-  constexpr uint32_t idKV = mma_idesc_bf16(128, 64, false, true);
-  // LSE (log2 domain) and D of the 64 queries of a block: block i0's now,
-  // each next block's read one iteration ahead (its loads in flight while
-  // this block's products run)
-  if (r < 64) {
-    const int64_t row = static_cast<int64_t>(row0) + i0 * 64 + r;
-    sL[r] = lse[row * heads + h] * kLog2e;
-    sD[r] = dvec[row * heads + h];
-  }
-  for (int t = 0; t < niter; ++t) {
-    const int i = i0 + t, qbuf = t & 1;
-    float nL = 0.f, nD = 0.f;
-    if (r < 64 && t + 1 < niter) {
-      const int64_t row = static_cast<int64_t>(row0) + (i + 1) * 64 + r;
-      nL = lse[row * heads + h] * kLog2e;
-      nD = dvec[row * heads + h];
-    }
-    if (r == 0) {  // S^T = K Q_i^T, dP^T = V dO_i^T
-      bool w = (t > 0 || mbar_wait_bounded(bkv, 0, err, DERR_MMA_WAIT)) &&
-               mbar_wait_bounded(&bq[qbuf], (t >> 1) & 1, err, DERR_MMA_WAIT);
-      if (w) {
-        tc_fence_after();
-        const uint32_t k = smem_u32(sK), v = smem_u32(sV), q = smem_u32(sQ + qbuf * T64),
-                       dO = smem_u32(sdO + qbuf * T64);
+  if (warp == 4) {
+    if (r == 128) {  // ---- issuer ----
+      constexpr uint32_t idSP = mma_idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idKV = mma_idesc_bf16(128, 64, false, true);
+      int nqi[2] = {0, 0};
+      mbar_arrive_expect_tx(bkv, 2 * T128);
+      tma_load_2d(sK, tq128, D + h * HD, row0 + k0, bkv);
+      tma_load_2d(sV, tq128, 2 * D + h * HD, row0 + k0, bkv);
+      for (int t = 0; t < 2 && t < niter; ++t) {
+        mbar_arrive_expect_tx(&bq[t], 2 * T64);
+        tma_load_2d(sQ + t * T64, tq64, h * HD, row0 + (i0 + t) * 64, &bq[t]);
+        tma_load_2d(sdO + t * T64, td64, h * HD, row0 + (i0 + t) * 64, &bq[t]);
+        ++nqi[t];
+      }
+      auto issue_sp = [&](int tt) {  // S^T = K Q_tt^T, dP^T = V dO_tt^T
+        const int qb2 = tt & 1;
+        const uint32_t k = smem_u32(sK), v = smem_u32(sV), q = smem_u32(sQ + qb2 * T64),
+                       dO = smem_u32(sdO + qb2 * T64);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tS, kdesc(k, kk), kdesc(q, kk), idSP, kk ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tP, kdesc(v, kk), kdesc(dO, kk), idSP, kk ? 1u : 0u);
-        tc_commit(bs);  // also covers the previous block's dV, dK products
+        tc_commit(bs);
+      };
+      bool go = await(bkv, 0, err, DERR_MMA_WAIT, abort) && await(&bq[0], 0, err, DERR_MMA_WAIT, abort);
+      if (go) {
+        tc_fence_after();
+        issue_sp(0);
       }
+      for (int t = 0; t < niter && go; ++t) {
+        const int qbuf = t & 1;
+        if (t + 1 < niter) {  // the next block's S^T, dP^T as soon as the rows have read block t's
+          if (!await(&bq[(t + 1) & 1], ((t + 1) >> 1) & 1, err, DERR_MMA_WAIT, abort)) break;
+          if (!await(bsc, t & 1, err, DERR_MMA_WAIT, abort)) break;
+          tc_fence_after();
+          issue_sp(t + 1);
+        }
+        if (!await(bp, t & 1, err, DERR_MMA_WAIT, abort)) break;  // P^T, dS^T of block t written
+        tc_fence_after();
+        {
+          const uint32_t pt = smem_u32(sPt), dst = smem_u32(sdSt), q = smem_u32(sQ + qbuf * T64),
+                         dO = smem_u32(sdO + qbuf * T64);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tV, kdesc(pt, kk), mndesc(dO, kk), idKV, (t | kk) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tK, kdesc(dst, kk), mndesc(q, kk), idKV, (t | kk) ? 1u : 0u);
+          tc_commit(bo);
+        }
+        if (t + 2 < niter) {  // block t's buffers, once dV, dK of block t are done
+          if (!await(bo, t & 1, err, DERR_MMA_WAIT, abort)) break;
+          mbar_arrive_expect_tx(&bq[qbuf], 2 * T64);
+          tma_load_2d(sQ + qbuf * T64, tq64, h * HD, row0 + (i0 + t + 2) * 64, &bq[qbuf]);
+          tma_load_2d(sdO + qbuf * T64, td64, h * HD, row0 + (i0 + t + 2) * 64, &bq[qbuf]);
+          ++nqi[qbuf];
+        }
+      }
+      tc_commit(bfin);
+      mbar_wait_bounded(bfin, 0, err, DERR_DRAIN_WAIT);
+      for (int bb = 0; bb < 2; ++bb)
+        if (nqi[bb]) mbar_wait_bounded(&bq[bb], (nqi[bb] - 1) & 1, err, DERR_DRAIN_WAIT);
+      mbar_wait_bounded(bkv, 0, err, DERR_DRAIN_WAIT);
     }
-    ok = mbar_wait_bounded(bs, t & 1, err, DERR_ACC_WAIT);
-    ok = __syncthreads_and(ok);  // also publishes sL / sD of this block
-    if (!ok) break;
-    tc_fence_after();
-    if (r == 0 && t >= 1 && t + 1 < niter) {  // buffers of block i-1 are free
-      const int nb = (t + 1) & 1;
-      mbar_arrive_expect_tx(&bq[nb], 2 * T64);
-      tma_load_2d(sQ + nb * T64, tq64, h * HD, row0 + (i + 1) * 64, &bq[nb]);
-      tma_load_2d(sdO + nb * T64, td64, h * HD, row0 + (i + 1) * 64, &bq[nb]);
-      ++nq_issued[nb];
+  } else {  // ---- rows ----
+    const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
+    // LSE (log2 domain) and D of the 64 queries of a block: block i0's now,
+    // each next block's read one block ahead; block t sits in slot t & 1 and
+    // is published by the (t >> 1)-th phase of bld[t & 1]
+    if (r < 64) {
+      const int64_t row = static_cast<int64_t>(row0) + i0 * 64 + r;
+      sL[r] = lse[row * heads + h] * kLog2e;
+      sD[r] = dvec[row * heads + h];
+      mbar_arrive1(&bld[0]);
     }
-    const float* L = sL + qbuf * 64;
-    const float* Dq = sD + qbuf * 64;
-    {
+    bool ok = true;
+    for (int t = 0; t < niter; ++t) {
+      const int i = i0 + t, qbuf = t & 1;
+      ok = __all_sync(0xffffffffu, await(&bld[qbuf], (t >> 1) & 1, err, DERR_ACC_WAIT, abort));
+      if (!ok) break;
+      float nL = 0.f, nD = 0.f;
+      if (r < 64 && t + 1 < niter) {
+        const int64_t row = static_cast<int64_t>(row0) + (i + 1) * 64 + r;
+        nL = lse[row * heads + h] * kLog2e;
+        nD = dvec[row * heads + h];
+      }
+      ok = __all_sync(0xffffffffu, await(bs, t & 1, err, DERR_ACC_WAIT, abort));
+      if (!ok) break;
+      tc_fence_after();
       float v[128];  // S^T (64 columns), then dP^T (64 columns), one round trip
-      const uint32_t a[4] = {tS + lane, tS + lane + 32, tP + lane, tP + lane + 32};
-      ld_rows<4>(a, v);
+      {
+        const uint32_t a[4] = {tS + lane, tS + lane + 32, tP + lane, tP + lane + 32};
+        ld_rows<4>(a, v);
+      }
+      tc_fence_before();
+      mbar_arrive1(bsc);
+      const float* L = sL + qbuf * 64;
+      const float* Dq = sD + qbuf * 64;
 #pragma unroll
       for (int q = 0; q < 64; ++q) {
         const bool vis = i * 64 + q >= kr;
         const float p = vis ? fast_exp2(v[q] * kScaleLog2 - L[q]) : 0.f;
-        v[q] = p;                          // P^T
+        v[q] = p;                             // P^T
         v[64 + q] = p * (v[64 + q] - Dq[q]);  // dS^T
+      }
+      if (t > 0) {  // the previous dV, dK products read the P^T and dS^T tiles
+        ok = __all_sync(0xffffffffu, await(bo, (t - 1) & 1, err, DERR_ACC_WAIT, abort));
+        if (!ok) break;
       }
       st_row32_bf16(sPt, r, 0, v);
       st_row32_bf16(sPt, r, 4, v + 32);
       st_row32_bf16(sdSt, r, 0, v + 64);
       st_row32_bf16(sdSt, r, 4, v + 96);
+      if (r < 64 && t + 1 < niter) {  // the next block's
+        sL[(qbuf ^ 1) * 64 + r] = nL;
+        sD[(qbuf ^ 1) * 64 + r] = nD;
+        mbar_arrive1(&bld[qbuf ^ 1]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive1(bp);
     }
-    if (r < 64 && t + 1 < niter) {  // the next block's, published by the barriers below
-      sL[(qbuf ^ 1) * 64 + r] = nL;
-      sD[(qbuf ^ 1) * 64 + r] = nD;
+    if (ok) ok = __all_sync(0xffffffffu, await(bo, (niter - 1) & 1, err, DERR_ACC_WAIT, abort));
+    tc_fence_after();
+    if (ok) {
+      const int64_t row = static_cast<int64_t>(row0) + kr;
+      store_row64(tK + lane, dqkv + row * ld + D + h * HD, 0.125f, kr < seq);
+      store_row64(tV + lane, dqkv + row * ld + 2 * D + h * HD, 1.0f, kr < seq);
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (r == 0) {  // dV += P^T dO_i, dK += dS^T Q_i
-      tc_fence_after();
-      const uint32_t pt = smem_u32(sPt), dst = smem_u32(sdSt), q = smem_u32(sQ + qbuf * T64),
-                     dO = smem_u32(sdO + qbuf * T64);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tV, kdesc(pt, kk), mndesc(dO, kk), idKV, (t | kk) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) tc_mma_f16(tK, kdesc(dst, kk), mndesc(q, kk), idKV, (t | kk) ? 1u : 0u);
-    }
-  }
-  if (r == 0) tc_commit(bo);
-  const bool okd = __syncthreads_and(mbar_wait_bounded(bo, 0, err, DERR_ACC_WAIT));
-  tc_fence_after();
-  if (ok && okd) {
-    const int64_t row = static_cast<int64_t>(row0) + kr;
-    store_row64(tK + lane, dqkv + row * ld + D + h * HD, 0.125f, kr < seq);
-    store_row64(tV + lane, dqkv + row * ld + 2 * D + h * HD, 1.0f, kr < seq);
-  }
-  if (r == 0) {
-    for (int qb = 0; qb < 2; ++qb)
-      if (nq_issued[qb]) mbar_wait_bounded(&bq[qb], (nq_issued[qb] - 1) & 1, err, DERR_DRAIN_WAIT);
-    mbar_wait_bounded(bkv, 0, err, DERR_DRAIN_WAIT);
   }
   tc_fence_before();
   __syncthreads();
@@ -674,7 +751,7 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
 
 // One launch for both kinds: blocks with z < nseq compute dQ of sequence z,
 // the others dK/dV of sequence z - nseq; the two kinds share no data.
-__global__ void __launch_bounds__(128) attn_bwd_kernel(const __grid_constant__ CUtensorMap tq64,
+__global__ void __maxnreg__(ATTN_MAXNREG) attn_bwd_kernel(const __grid_constant__ CUtensorMap tq64,
                                                        const __grid_constant__ CUtensorMap tq128,
                                                        const __grid_constant__ CUtensorMap td64,
                                                        const __grid_constant__ CUtensorMap td128,
@@ -796,7 +873,7 @@ int launch_attention_bwd(int nseq, int seq, int heads, const void* qkv, const vo
   cudaError_t e0 = cudaGetLastError();
   if (e0 != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "attention_bwd (D) launch: %s", cudaGetErrorString(e0));
   dim3 grid((seq + 127) / 128, heads, 2 * nseq);
-  (void)launch_k<true>(attn_bwd_kernel, grid, 128, BWD_SMEM, s, tq64, tq128, td64, td128, lse,
+  (void)launch_k<true>(attn_bwd_kernel, grid, BWD_THREADS, BWD_SMEM, s, tq64, tq128, td64, td128, lse,
                        static_cast<const float*>(dvec), static_cast<__nv_bfloat16*>(dqkv), seq, heads, nseq, err);
   count_launch();
   cudaError_t e = cudaGetLastError();

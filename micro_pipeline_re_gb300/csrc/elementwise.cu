@@ -4,7 +4,6 @@
 // order (no floating-point atomics), so every result is bit-reproducible and
 // a re-computed forward equals the first one byte for byte.
 #include <algorithm>
-#include <mutex>
 
 #include "../../include/gpipe.h"
 #include "common.cuh"
@@ -886,26 +885,15 @@ int launch_layernorm_bwd_noalloc(int dtype, int rows, int d, const void* dy, con
                      "layernorm_bwd_noalloc: rows=%d, d=%d needs %zu scratch floats, more than the fixed %zu "
                      "(ceil(rows/8) * 2d must not exceed %zu)",
                      rows, d, need, kNoAllocScratchFloats, kNoAllocScratchFloats);
-  // The array's host-side name is only a stand-in; resolve its device address
-  // once per device, with that device current.
-  static std::mutex mu;
-  static float* addr[256] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 256)
-    return set_error(GPIPE_ERR_CUDA, "layernorm_bwd_noalloc: no current device");
-  float* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_ln_bwd_scratch);
-      if (e != cudaSuccess)
-        return set_error(GPIPE_ERR_CUDA, "layernorm_bwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-      addr[dev] = static_cast<float*>(p);
-    }
-    scratch = addr[dev];
-  }
+  // The array's host-side name is only a stand-in; its device address is
+  // resolved on every call (no allocation, no stream work), so that a context
+  // re-created after a device reset, whose module may sit elsewhere, is never
+  // handed a stale address.
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_ln_bwd_scratch);
+  if (e != cudaSuccess)
+    return set_error(GPIPE_ERR_CUDA, "layernorm_bwd_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+  float* scratch = static_cast<float*>(p);
   // Every partial row the reduction reads is written by this call, so nothing
   // needs clearing first.
   return launch_layernorm_bwd(dtype, rows, d, dy, x, mean, rstd, g, dres, dx, dg_acc, db_acc, scratch, s);

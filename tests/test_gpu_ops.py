@@ -500,7 +500,8 @@ def test_gelu_arithmetic_within_its_error_bound(b):
 
 @pytest.mark.parametrize("ak,bk,epi,shape", [(1, 1, 1, (1024, 2048, 512)), (1, 1, 0, (512, 1536, 512)),
                                              (1, 0, 2, (512, 2048, 512)), (0, 0, 3, (2048, 512, 512)),
-                                             (0, 0, 3, (1152, 1088, 256))])
+                                             (0, 0, 3, (1152, 1088, 256)), (1, 1, 5, (2048, 1024, 1024)),
+                                             (1, 1, 5, (1000, 1000, 264))])
 def test_gemm_bits_do_not_depend_on_sm_share(b, ak, bk, epi, shape):
     """The step sizes each GEMM's grid by its share of the SMs, which changes
     the kernel (one tile per CTA, 64/128 wide, or persistent 128/256 wide) but
@@ -512,14 +513,16 @@ def test_gemm_bits_do_not_depend_on_sm_share(b, ak, bk, epi, shape):
     B = dev(bf16_round(rng.standard_normal((N, K) if bk else (K, N)) / np.sqrt(K)), "bf16")
     bias = dev(rng.standard_normal(N if epi != 3 else M).astype(np.float32))
     aux = dev(bf16_round(rng.standard_normal((M, N))), "bf16") if epi == 2 else None
+    resid = dev(rng.standard_normal((M, N)).astype(np.float32)) if epi == 5 else None
     outs = []
     for share in (0, 16, 40, 7):
         assert b.lib().gpipe_op_gemm_set_sm_share(share) == 0
-        C = t.zeros((M, N), device="cuda", dtype=t.float32 if epi == 3 else t.bfloat16)
+        C = t.zeros((M, N), device="cuda", dtype=t.float32 if epi in (3, 5) else t.bfloat16)
         C2 = t.zeros((M, N), device="cuda", dtype=t.bfloat16) if epi == 1 else None
         db = bias.clone() if epi == 3 else bias
         rc = b.lib().gpipe_op_gemm(1, M, N, K, A.data_ptr(), K if ak else M, ak, B.data_ptr(), K if bk else N, bk,
-                                   epi, C.data_ptr(), N, db.data_ptr(), None, 0,
+                                   epi, C.data_ptr(), N, db.data_ptr(),
+                                   resid.data_ptr() if resid is not None else None, N if resid is not None else 0,
                                    C2.data_ptr() if C2 is not None else None,
                                    aux.data_ptr() if aux is not None else None, N if aux is not None else 0,
                                    stream())

@@ -318,6 +318,9 @@ def test_full_batch_loss_matches_oracle(b, name):
     (a script that calls only the oracle)."""
     w = WORKLOADS[name]
     gold = _golden_losses()[name]
+    if "loss" not in gold:
+        pytest.skip(f"the oracle's full-batch loss of {name} has {len(gold.get('parts', {}))} of its "
+                    f"{w.n // gold['group']} sequence groups so far")
     assert (gold["L"], gold["n"], gold["seq"], gold["seed"]) == (w.L, w.n, w.seq, w.seed)
     inp = make_inputs(w)
     gp, st, _, (loss,) = _run(b, w, inp, keep_grads=False, options=[(b.OPT_SKIP_UPDATE, 1)])
