@@ -10,15 +10,16 @@
 //   warp 1            allocates TMEM; lane 0 issues tcgen05.mma into one of two
 //                     accumulators (2 x BN columns), so the MMAs of tile i+1
 //                     run while the epilogue drains tile i
-//   warps 2..9        epilogue: each reads 32 TMEM lanes (rows) x 32 columns per
-//                     64-column step, applies bias / residual / GELU, writes a
-//                     128B-swizzled staging box; one thread TMA-stores each
-//                     box (staging is double-buffered, so the store of step s
-//                     overlaps step s+1), or TMA-reduce-adds the fp32 gradient
-//                     (the bias gradient, sum over k of A: with 128-wide tiles an
-//                     M=128, N=16 MMA against a tile of ones into TMEM beside
-//                     the accumulators; 256-wide tiles fill TMEM, so callers
-//                     add it with a separate reduction)
+//   warps 2..9        epilogue, each warp on its own (no barrier between
+//                     them): TMEM lane quarter warp % 4 (the lanes a warp may
+//                     read), column half (warp - 2) / 4; per 32-column chunk it
+//                     loads the accumulator (the next chunk's load in flight),
+//                     applies bias / residual / GELU, writes its own swizzled
+//                     32 x 32 staging box and TMA-stores it, or TMA-reduce-adds
+//                     the fp32 gradient (the bias gradient, sum over k of A:
+//                     with 128-wide tiles an M=128, N=16 MMA against a tile of
+//                     ones into TMEM beside the accumulators; 256-wide tiles
+//                     fill TMEM, so callers add it with a separate reduction)
 // Bounded waits as in the single-tile kernel.
 #include <cuda.h>
 
@@ -33,31 +34,28 @@ namespace {
 constexpr int PM = 128;
 constexpr int PK = 64;
 constexpr int P_THREADS = 320;      // 10 warps
-constexpr int P_EPI_THREADS = 256;  // warps 2..9
-constexpr int PBOX = 16384;         // staging box: 128 rows x 128 B
 constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
 
-// SK (short K): two-box epilogue steps double-buffered too.  With few k-blocks
-// per tile the epilogue bounds the tile rate and the overlap pays; with many,
-// the fourth operand stage that single buffering leaves room for pays more.
-template <int BN, int EPI, bool SK = false>
+template <int BN, int EPI>
 struct PCfg {
   static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32 || EPI == EPI_RESID_F32);
   static constexpr int A_BYTES = PM * PK * 2;
   static constexpr int B_BYTES = BN * PK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // per 64-column step: bf16 -> one box (two for bias+GELU: z and GELU(z)); fp32 -> two boxes
-  static constexpr int STEP_BOXES = F32_OUT ? 2 : (EPI == EPI_BIAS_GELU ? 2 : 1);
-  // one-box steps are double-buffered (a step's store overlaps the next step);
-  // two-box steps single-buffered, which leaves room for a fourth operand stage
-  // at 256 columns (measured faster than the overlap)
-  static constexpr int NBUF = (STEP_BOXES == 1 || SK) ? 2 : 1;
-  static constexpr int STAGING = NBUF * STEP_BOXES * PBOX;
+  // an epilogue warp's staging box: 32 rows x 32 columns (64-byte rows in bf16,
+  // 128-byte rows in fp32); bias+GELU writes two (z and GELU(z))
+  static constexpr int BOX_BYTES = 32 * 32 * (F32_OUT ? 4 : 2);
+  static constexpr int BOXES = EPI == EPI_BIAS_GELU ? 2 : 1;
   // bias gradient by MMA against ones (2 x 16 TMEM columns beside the accumulators) when they fit
   static constexpr bool DB_MMA = EPI == EPI_ACC_F32 && 2 * BN + 32 <= 512;
   static constexpr int ONES_BYTES = DB_MMA ? 2048 : 0;
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - STAGING - ONES_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+  static constexpr int fit(int nbuf) { return (SMEM_BUDGET - 8 * nbuf * BOXES * BOX_BYTES - ONES_BYTES) / STAGE_BYTES; }
+  // two staging buffers per warp (a chunk's store drains while the next chunk
+  // is computed) when four operand stages still fit, else one
+  static constexpr int WNB = fit(2) >= 4 ? 2 : 1;
+  static constexpr int WARP_STG = WNB * BOXES * BOX_BYTES;
+  static constexpr int STAGING = 8 * WARP_STG;
+  static constexpr int STAGES = fit(WNB) > 6 ? 6 : fit(WNB);
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
   static constexpr int OFF_ONES = OFF_STG + STAGING;
   static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
@@ -80,10 +78,17 @@ struct PArgs {
   int m_tiles, n_tiles;
 };
 
-__device__ __forceinline__ uint32_t pswz(int r, int unit) {
-  return static_cast<uint32_t>(r * 128 + ((unit ^ (r & 7)) << 4));
+// Byte offset of 16-byte unit u of row r in a staging box, in the layout of the
+// tensor map's swizzle: bf16 boxes (64-byte rows, 64-byte swizzle: unit bits
+// 4-5 XOR address bits 7-8) and fp32 boxes (128-byte rows, 128-byte swizzle:
+// unit bits 4-6 XOR address bits 7-9).  Lanes = rows, so a warp's 16-byte
+// writes of one unit hit every bank once per 8 rows.
+__device__ __forceinline__ uint32_t box_off_bf16(int r, int u) {
+  return static_cast<uint32_t>(r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
 }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(P_EPI_THREADS) : "memory"); }
+__device__ __forceinline__ uint32_t box_off_f32(int r, int u) {
+  return static_cast<uint32_t>(r * 128 + ((u ^ (r & 7)) << 4));
+}
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -108,12 +113,12 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, int* err, 
   return false;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>
+template <bool A_K, bool B_K, int BN, int EPI>
 __global__ void __launch_bounds__(P_THREADS, 1)
     tc_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                        PArgs args, int* err) {
-  using Cfg = PCfg<BN, EPI, SK>;
+  using Cfg = PCfg<BN, EPI>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -226,159 +231,146 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     griddep_launch();
   } else {
-    // ---- epilogue warps 2..9: TMEM lane quarter q, column half h of each 64-column step ----
-    const int q = warp & 3;
-    const int h = (warp - 2) >> 2;
-    const int r = q * 32 + lane;
-    const int etid = threadIdx.x - 64;
-    int step = 0, i = 0;
+    // ---- epilogue warps 2..9, each independent of the others ----
+    constexpr int HALF = BN / 2;     // columns of a warp per tile
+    constexpr int CH = HALF / 32;    // its 32-column chunks
+    constexpr bool X_F32 = EPI == EPI_RESID_F32;                                     // fp32 residual
+    constexpr bool X_BF16 = EPI == EPI_STORE || EPI == EPI_GELU_BWD;                 // bf16 residual / z
+    constexpr int XV = X_F32 ? 8 : 4;  // 16-byte words of a row's 32 inputs
+    // the next chunk's accumulator load overlaps this chunk's work, except with
+    // the fp32 residual, whose look-ahead already takes those registers
+    constexpr bool LD_AHEAD = !X_F32;
+    const int q = warp & 3;            // TMEM lane quarter this warp may read
+    const int h = (warp - 2) >> 2;     // column half
+    const int r = q * 32 + lane;       // row of the tile
+    uint8_t* wst = sStg + (warp - 2) * Cfg::WARP_STG;
+    int nst = 0;  // chunks this warp has staged (alternates its buffers)
+    int i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
       const int b = i & 1;
       int m0, n0;
       tile_origin<BN>(t, args, m0, n0);
       const int m = m0 + r;
-      // The epilogue input (residual / GELU pre-activation) of this thread's row
-      // is read one 64-column step ahead: step 0 before waiting for the
-      // accumulator, step c+1 while step c is processed.
-      const bool has_x = !Cfg::F32_OUT && args.xsrc != nullptr && m < args.M;
-      const __nv_bfloat16* xrow =
-          has_x ? static_cast<const __nv_bfloat16*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx : nullptr;
-      uint4 xnext[4];
+      const int c0 = n0 + h * HALF;  // the warp's first column
+      int nch = (args.N - c0 + 31) / 32;  // its chunks inside the matrix
+      nch = nch < 0 ? 0 : (nch > CH ? CH : nch);
+      // The epilogue input (residual / GELU pre-activation) of this thread's
+      // row is read one chunk ahead: chunk 0 before waiting for the accumulator.
+      const bool has_x = (X_F32 || X_BF16) && args.xsrc != nullptr && m < args.M;
+      const char* xrow = has_x ? static_cast<const char*>(args.xsrc) +
+                                     static_cast<int64_t>(m) * args.ldx * (X_F32 ? 4 : 2)
+                               : nullptr;
+      uint4 xnext[XV];
       auto load_x = [&](int cc, uint4* dst) {
-        const int col = n0 + cc * 64 + h * 32;
+        const int col = c0 + cc * 32;
         if (has_x && col + 32 <= args.N) {
-          const uint4* src = reinterpret_cast<const uint4*>(xrow + col);
+          const uint4* src = reinterpret_cast<const uint4*>(xrow + static_cast<int64_t>(col) * (X_F32 ? 4 : 2));
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = src[j];
+          for (int j = 0; j < XV; ++j) dst[j] = src[j];
         }
       };
-      load_x(0, xnext);
+      if (nch > 0) load_x(0, xnext);
       pwait(&accf[b], (i >> 1) & 1, err, DERR_ACC_WAIT, abort);
       tc_fence_after();
-      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
+      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN + h * HALF;
+      uint32_t ra[32];
+      if (LD_AHEAD && nch > 0) tmem_ld32(tb, ra);
 #pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c, ++step) {
-        uint4 xcur[4];
+      for (int c = 0; c < nch; ++c, ++nst) {
+        if (!LD_AHEAD) tmem_ld32(tb + c * 32, ra);
+        tmem_ld_wait32(ra);
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) xcur[j] = xnext[j];
-        if (c + 1 < BN / 64) load_x(c + 1, xnext);
-        uint8_t* stg = sStg + (Cfg::NBUF == 2 ? (step & 1) : 0) * Cfg::STEP_BOXES * PBOX;
-        if (etid == 0) {  // the store that last used this buffer has read it
-          if (Cfg::NBUF == 2) bulk_wait_read_1();
-          else bulk_wait_read_all();
-        }
-        epi_bar();
-        const int ncol0 = n0 + c * 64 + h * 32;
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
+        if (LD_AHEAD && c + 1 < nch) tmem_ld32(tb + (c + 1) * 32, ra);  // lands while this chunk is processed
+        uint4 xcur[XV];
+#pragma unroll
+        for (int j = 0; j < XV; ++j) xcur[j] = xnext[j];
+        if (c + 1 < nch) load_x(c + 1, xnext);
+        const int ncol0 = c0 + c * 32;
         const bool full_cols = ncol0 + 32 <= args.N;
-        float xv[32];
-        if (has_x) {
+        // bias, then the residual / GELU derivative, in the single-tile kernel's order
+        if ((EPI == EPI_STORE || EPI == EPI_BIAS_GELU || EPI == EPI_RESID_F32) && args.bias) {
           if (full_cols) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 32; j += 8) {
+              float bb8[8];
+              load8(args.bias + ncol0 + j, bb8);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[j + e] += bb8[e];
+            }
+          } else {
+            for (int j = 0; j < 32; ++j)
+              if (ncol0 + j < args.N) v[j] += args.bias[ncol0 + j];
+          }
+        }
+        if (has_x) {
+          auto apply = [&](float& acc, float x) {
+            if (EPI == EPI_GELU_BWD) acc *= gelu_grad_f(x);
+            else acc += x;
+          };
+          if (full_cols) {
+#pragma unroll
+            for (int j = 0; j < XV; ++j) {
               const uint32_t w4[4] = {xcur[j].x, xcur[j].y, xcur[j].z, xcur[j].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float2 f = unpack_bf16x2(w4[e]);
-                xv[8 * j + 2 * e] = f.x;
-                xv[8 * j + 2 * e + 1] = f.y;
+                if (X_F32) {
+                  apply(v[4 * j + e], __uint_as_float(w4[e]));
+                } else {
+                  const float2 f = unpack_bf16x2(w4[e]);
+                  apply(v[8 * j + 2 * e], f.x);
+                  apply(v[8 * j + 2 * e + 1], f.y);
+                }
               }
             }
           } else {
-            for (int j = 0; j < 32; ++j) xv[j] = ncol0 + j < args.N ? bf2f(xrow[ncol0 + j]) : 0.f;
+            for (int j = 0; j < 32; ++j)
+              if (ncol0 + j < args.N)
+                apply(v[j], X_F32 ? reinterpret_cast<const float*>(xrow)[ncol0 + j]
+                                  : bf2f(reinterpret_cast<const __nv_bfloat16*>(xrow)[ncol0 + j]));
           }
         }
-        uint32_t rr[32];
-        tmem_ld32(tb + c * 64 + h * 32, rr);
-        tmem_ld_wait();
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
+        // stage the chunk (the store that last read this buffer has finished reading)
+        uint8_t* stg = wst + (Cfg::WNB == 2 ? (nst & 1) : 0) * Cfg::BOXES * Cfg::BOX_BYTES;
+        if (lane == 0) {
+          if (Cfg::WNB == 2) bulk_wait_read_1();
+          else bulk_wait_read_all();
+        }
+        __syncwarp();
         if (Cfg::F32_OUT) {
-          if (EPI == EPI_RESID_F32 && m < args.M) {  // + bias + the fp32 residual (global loads)
-            const float* xr = static_cast<const float*>(args.xsrc) + static_cast<int64_t>(m) * args.ldx + ncol0;
-            // (acc + bias) + residual, the single-tile kernel's order
-            if (full_cols) {
-#pragma unroll
-              for (int j = 0; j < 32; j += 8) {
-                float bb8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, t[8];
-                if (args.bias) load8(args.bias + ncol0 + j, bb8);
-                load8(xr + j, t);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  v[j + e] += bb8[e];
-                  v[j + e] += t[e];
-                }
-              }
-            } else {
-              for (int j = 0; j < 32; ++j)
-                if (ncol0 + j < args.N) {
-                  v[j] += args.bias ? args.bias[ncol0 + j] : 0.f;
-                  v[j] += xr[j];
-                }
-            }
-          }
-          uint8_t* box = stg + h * PBOX;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<float4*>(box + pswz(r, u)) = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            *reinterpret_cast<float4*>(stg + box_off_f32(lane, u)) =
+                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         } else {
-          if ((EPI == EPI_STORE || EPI == EPI_BIAS_GELU) && args.bias) {
-            if (full_cols) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 8) {
-                float bb8[8];
-                load8(args.bias + ncol0 + j, bb8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[j + e] += bb8[e];
-              }
-            } else {
-              for (int j = 0; j < 32; ++j)
-                if (ncol0 + j < args.N) v[j] += args.bias[ncol0 + j];
-            }
-          }
-          if (has_x) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (EPI == EPI_GELU_BWD) v[j] *= gelu_grad_f(xv[j]);
-              else v[j] += xv[j];
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) store8(reinterpret_cast<__nv_bfloat16*>(stg + pswz(r, h * 4 + u)), v + 8 * u);
+          for (int u = 0; u < 4; ++u) store8(reinterpret_cast<__nv_bfloat16*>(stg + box_off_bf16(lane, u)), v + 8 * u);
           if (EPI == EPI_BIAS_GELU) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               float gv[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) gv[e] = gelu_f(v[8 * u + e]);
-              store8(reinterpret_cast<__nv_bfloat16*>(stg + PBOX + pswz(r, h * 4 + u)), gv);
+              store8(reinterpret_cast<__nv_bfloat16*>(stg + Cfg::BOX_BYTES + box_off_bf16(lane, u)), gv);
             }
           }
         }
         fence_proxy_async_smem();
-        epi_bar();
-        if (etid == 0 && !*abort) {
-          if (Cfg::F32_OUT) {
-            for (int bx = 0; bx < 2; ++bx) {
-              const int x = n0 + c * 64 + bx * 32;
-              if (x >= args.N) break;
-              if (EPI == EPI_ACC_F32) tma_reduce_add_2d(&tmC, x, m0, stg + bx * PBOX);
-              else tma_store_2d(&tmC, x, m0, stg + bx * PBOX);
-            }
-          } else {
-            const int x = n0 + c * 64;
-            if (x < args.N) {
-              tma_store_2d(&tmC, x, m0, stg);
-              if (EPI == EPI_BIAS_GELU) tma_store_2d(&tmC2, x, m0, stg + PBOX);
-            }
+        __syncwarp();
+        if (lane == 0) {
+          if (!*abort) {
+            if (EPI == EPI_ACC_F32) tma_reduce_add_2d(&tmC, ncol0, m0 + q * 32, stg);
+            else tma_store_2d(&tmC, ncol0, m0 + q * 32, stg);
+            if (EPI == EPI_BIAS_GELU) tma_store_2d(&tmC2, ncol0, m0 + q * 32, stg + Cfg::BOX_BYTES);
           }
-          bulk_commit();
+          bulk_commit();  // (empty after a give-up: the buffer count stays in step)
         }
       }
       if (Cfg::DB_MMA && args.dbias != nullptr && n0 == 0 && h == 0) {
         uint32_t rr[32];
         tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + 2 * BN + 16 * b, rr);
-        tmem_ld_wait();
+        tmem_ld_wait32(rr);
         if (m < args.M && !*abort) args.dbias[m] += __uint_as_float(rr[0]);
       }
       tc_fence_before();
@@ -386,7 +378,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       if (lane == 0) mbar_arrive(&acce[b]);  // this warp has drained accumulator b
     }
     griddep_launch();
-    if (etid == 0) bulk_wait_read_all();
+    if (lane == 0) bulk_wait_read_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -400,7 +392,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 // Host side
 // ---------------------------------------------------------------------------
 bool pmake_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64_t outer, int64_t ld, int box_inner,
-                int box_outer) {
+                int box_outer, bool swizzle64 = false) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -420,34 +412,37 @@ bool pmake_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1u, 1u};
   return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>
+template <bool A_K, bool B_K, int BN, int EPI>
 int pset_attr() {
   static std::atomic<unsigned long long> done{0};
   return once_per_device(done, [] {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI, SK>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI, SK>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI>::SMEM);
     return e == cudaSuccess
                ? GPIPE_OK
                : set_error(GPIPE_ERR_CUDA, "persistent gemm: smem attribute: %s", cudaGetErrorString(e));
   });
 }
 
-template <bool A_K, bool B_K, int BN, int EPI, bool SK = false>
+template <bool A_K, bool B_K, int BN, int EPI>
 int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
-  using Cfg = PCfg<BN, EPI, SK>;
+  using Cfg = PCfg<BN, EPI>;
   CUtensorMap ta, tb, tc, tc2;
   bool ok = A_K ? pmake_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, PM) : pmake_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
   ok = ok && (B_K ? pmake_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, BN)
                   : pmake_tmap(&tb, g.B, false, g.N, g.K, g.ldb, 64, 64));
-  ok = ok && pmake_tmap(&tc, g.C, Cfg::F32_OUT, g.N, g.M, g.ldc, Cfg::F32_OUT ? 32 : 64, PM);
+  // output boxes: 32 x 32, one per epilogue warp and chunk (64-byte swizzle for
+  // the 64-byte bf16 rows, 128-byte for the fp32 rows)
+  ok = ok && pmake_tmap(&tc, g.C, Cfg::F32_OUT, g.N, g.M, g.ldc, 32, 32, !Cfg::F32_OUT);
   tc2 = tc;
-  if (EPI == EPI_BIAS_GELU) ok = ok && pmake_tmap(&tc2, g.C2, false, g.N, g.M, g.ldc, 64, PM);
+  if (EPI == EPI_BIAS_GELU) ok = ok && pmake_tmap(&tc2, g.C2, false, g.N, g.M, g.ldc, 32, 32, true);
   if (!ok) return set_error(GPIPE_ERR_CUDA, "persistent gemm: cuTensorMapEncodeTiled failed");
-  int rc = pset_attr<A_K, B_K, BN, EPI, SK>();
+  int rc = pset_attr<A_K, B_K, BN, EPI>();
   if (rc) return rc;
   PArgs args{};
   args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU || EPI == EPI_RESID_F32) ? g.bias : nullptr;
@@ -464,7 +459,7 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   args.n_tiles = (g.N + BN - 1) / BN;
   const int tiles = args.m_tiles * args.n_tiles;
   const int grid = ctas < tiles ? ctas : tiles;
-  (void)launch_k<true>(tc_gemm_persistent<A_K, B_K, BN, EPI, SK>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
+  (void)launch_k<true>(tc_gemm_persistent<A_K, B_K, BN, EPI>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
                                                                                device_error_ptr());
   count_launch();
   cudaError_t e = cudaGetLastError();
@@ -488,9 +483,7 @@ int dispatch(const GemmDesc& g, cudaStream_t s, int ctas) {
   if (g.a_kmajor && g.b_kmajor) {
     switch (g.epi) {
       case EPI_STORE: return prun<true, true, BN, EPI_STORE>(g, s, ctas);
-      case EPI_BIAS_GELU:
-        return (g.K + PK - 1) / PK < 32 ? prun<true, true, BN, EPI_BIAS_GELU, true>(g, s, ctas)
-                                        : prun<true, true, BN, EPI_BIAS_GELU>(g, s, ctas);
+      case EPI_BIAS_GELU: return prun<true, true, BN, EPI_BIAS_GELU>(g, s, ctas);
       case EPI_STORE_F32: return prun<true, true, BN, EPI_STORE_F32>(g, s, ctas);
       case EPI_ACC_F32: return prun<true, true, BN, EPI_ACC_F32>(g, s, ctas);
       case EPI_RESID_F32: return prun<true, true, BN, EPI_RESID_F32>(g, s, ctas);
@@ -515,7 +508,6 @@ int prepare_bn() {
   int rc = GPIPE_OK;
   rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU>();
-  rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU, true>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE_F32>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_ACC_F32>();
   rc = rc ? rc : pset_attr<true, true, BN, EPI_RESID_F32>();
