@@ -86,13 +86,6 @@ __device__ __forceinline__ void ld_rows(const uint32_t* a, float* v) {
   for (int i = 0; i < 32 * N; ++i) v[i] = __uint_as_float(u[i]);
 }
 
-// 2^x on the special-function unit (ex2.approx, relative error about 2^-22;
-// 2^-inf = 0): the softmax's exponentials.
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Write 32 values of row r as bf16 into a swizzled tile at units u0..u0+3.
 __device__ __forceinline__ void st_row32_bf16(uint8_t* tile, int r, int u0, const float* v) {
@@ -307,33 +300,44 @@ __global__ void __maxnreg__(ATTN_MAXNREG) attn_fwd_kernel(const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive1(bsc);  // S may be overwritten by the next block's product
-      float mx = -INFINITY;
+      if (diag) {         // the causal mask: only the block on the diagonal has hidden keys
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const bool vis = !diag || (j * 128 + i <= qi);
-        sv[i] = vis ? sv[i] * kScaleLog2 : -INFINITY;
-        mx = fmaxf(mx, sv[i]);
+        for (int i = 0; i < 128; ++i)
+          if (j * 128 + i > qi) sv[i] = -INFINITY;
       }
-      const float mn = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - mn);  // 0 for the first block
+      // the row maximum of the raw scores (scaling by a positive constant keeps
+      // it the maximum) over 8 independent partial maxima
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; i += 2) mx8[(i >> 1) & 7] = fmax3(mx8[(i >> 1) & 7], sv[i], sv[i + 1]);
+      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+      const float mn = fmaxf(m, mx * kScaleLog2);  // the running maximum, log2 domain
+      const float alpha = ex2_approx(m - mn);       // 0 for the first block
       m = mn;
       if (j > 0) {  // the previous O product reads P and writes O
         ok = __all_sync(0xffffffffu, await(bo, (j - 1) & 1, err, DERR_ACC_WAIT, abort));
         if (!ok) break;
         tc_fence_after();
       }
-      // P = exp2(s - m) as bf16 into shared memory, and its row sum
-      float rs = 0.f;
+      // P = exp2(s * scale log2(e) - m) as bf16 into shared memory, and its row
+      // sum (8 partial sums, added pairwise at the end)
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float* pc = sv + 32 * c;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          pc[i] = fast_exp2(pc[i] - m);
-          rs += pc[i];
+        for (int i = 0; i < 32; i += 2) {
+          ffma2(pc[i], pc[i + 1], pc[i], pc[i + 1], kScaleLog2, kScaleLog2, -m, -m);
+          pc[i] = ex2_approx(pc[i]);
+          pc[i + 1] = ex2_approx(pc[i + 1]);
+          const int e = (i >> 1) & 3;
+          fadd2(rs8[2 * e], rs8[2 * e + 1], rs8[2 * e], rs8[2 * e + 1], pc[i], pc[i + 1]);
         }
         st_row32_bf16(sP + (c >> 1) * T128, r, (c & 1) * 4, pc);
       }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       // then O *= alpha, with S's registers free again
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // warp-uniform: tcgen05 loads/stores are per warp
 #pragma unroll
@@ -342,7 +346,12 @@ __global__ void __maxnreg__(ATTN_MAXNREG) attn_fwd_kernel(const __grid_constant_
           tmem_ld32(tO + lane + 32 * c, u);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            float a0, a1;
+            fmul2(a0, a1, __uint_as_float(u[i]), __uint_as_float(u[i + 1]), alpha, alpha);
+            u[i] = __float_as_uint(a0);
+            u[i + 1] = __float_as_uint(a1);
+          }
           tmem_st32(tO + lane + 32 * c, u);
         }
         tmem_st_wait();
@@ -529,11 +538,20 @@ __device__ void attn_bwd_dq(const CUtensorMap* tq64, const CUtensorMap* tq128, c
       }
       tc_fence_before();
       mbar_arrive1(bsc);
+      // P = exp2(s * scale log2(e) - LSE) (hidden keys: 2^-inf = 0), then
+      // dS = P o (dP - D), two lanes per instruction
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const bool vis = j * 64 + i <= qi;
-        const float p = vis ? fast_exp2(v[i] * kScaleLog2 - L2) : 0.f;
-        v[i] = p * (v[64 + i] - Dr);  // dS
+      for (int i = 0; i < 64; i += 2) ffma2(v[i], v[i + 1], v[i], v[i + 1], kScaleLog2, kScaleLog2, -L2, -L2);
+      if (j * 64 + 63 > q0) {  // a block that some row of this CTA sees only in part
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (j * 64 + i > qi) v[i] = -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        float d0, d1;
+        fadd2(d0, d1, v[64 + i], v[65 + i], -Dr, -Dr);
+        fmul2(v[i], v[i + 1], ex2_approx(v[i]), ex2_approx(v[i + 1]), d0, d1);  // dS
       }
       if (j > 0) {  // the previous dQ product reads the dS tile
         ok = __all_sync(0xffffffffu, await(bo, (j - 1) & 1, err, DERR_ACC_WAIT, abort));
@@ -569,8 +587,8 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
   uint8_t* sdO = sQ + 2 * T64;     // two 64-row buffers
   uint8_t* sPt = sdO + 2 * T64;    // 128 keys x 64 queries
   uint8_t* sdSt = sPt + T128;      // 128 keys x 64 queries (ends at 96 KB)
-  float* sL = reinterpret_cast<float*>(sm + BWD_LD);  // [2][64]
-  float* sD = sL + 128;                               // [2][64]
+  float* sL = reinterpret_cast<float*>(sm + BWD_LD);  // [2][64], negated
+  float* sD = sL + 128;                               // [2][64], negated
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + BWD_BAR);
   uint64_t *bkv = bar, *bq = bar + 1, *bs = bar + 3, *bsc = bar + 4, *bp = bar + 5, *bo = bar + 6, *bfin = bar + 7,
            *bld = bar + 8;  // bld[2]: the LSE and D of a block are in their slot (64 writers)
@@ -677,13 +695,13 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
     }
   } else {  // ---- rows ----
     const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
-    // LSE (log2 domain) and D of the 64 queries of a block: block i0's now,
+    // -LSE (log2 domain) and -D of the 64 queries of a block: block i0's now,
     // each next block's read one block ahead; block t sits in slot t & 1 and
     // is published by the (t >> 1)-th phase of bld[t & 1]
     if (r < 64) {
       const int64_t row = static_cast<int64_t>(row0) + i0 * 64 + r;
-      sL[r] = lse[row * heads + h] * kLog2e;
-      sD[r] = dvec[row * heads + h];
+      sL[r] = -(lse[row * heads + h] * kLog2e);
+      sD[r] = -dvec[row * heads + h];
       mbar_arrive1(&bld[0]);
     }
     bool ok = true;
@@ -694,8 +712,8 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
       float nL = 0.f, nD = 0.f;
       if (r < 64 && t + 1 < niter) {
         const int64_t row = static_cast<int64_t>(row0) + (i + 1) * 64 + r;
-        nL = lse[row * heads + h] * kLog2e;
-        nD = dvec[row * heads + h];
+        nL = -(lse[row * heads + h] * kLog2e);
+        nD = -dvec[row * heads + h];
       }
       ok = __all_sync(0xffffffffu, await(bs, t & 1, err, DERR_ACC_WAIT, abort));
       if (!ok) break;
@@ -709,12 +727,23 @@ __device__ void attn_bwd_dkv(const CUtensorMap* tq64, const CUtensorMap* tq128, 
       mbar_arrive1(bsc);
       const float* L = sL + qbuf * 64;
       const float* Dq = sD + qbuf * 64;
+      // P^T = exp2(s * scale log2(e) - LSE) (hidden pairs: 2^-inf = 0) and
+      // dS^T = P^T o (dP^T - D), two lanes per instruction; the slots hold
+      // -LSE and -D
 #pragma unroll
-      for (int q = 0; q < 64; ++q) {
-        const bool vis = i * 64 + q >= kr;
-        const float p = vis ? fast_exp2(v[q] * kScaleLog2 - L[q]) : 0.f;
-        v[q] = p;                             // P^T
-        v[64 + q] = p * (v[64 + q] - Dq[q]);  // dS^T
+      for (int q = 0; q < 64; q += 2) ffma2(v[q], v[q + 1], v[q], v[q + 1], kScaleLog2, kScaleLog2, L[q], L[q + 1]);
+      if (i * 64 < k0 + 127) {  // a query block that some key of this CTA precedes only in part
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+          if (i * 64 + q < kr) v[q] = -INFINITY;
+      }
+#pragma unroll
+      for (int q = 0; q < 64; q += 2) {
+        v[q] = ex2_approx(v[q]);  // P^T
+        v[q + 1] = ex2_approx(v[q + 1]);
+        float d0, d1;
+        fadd2(d0, d1, v[64 + q], v[65 + q], Dq[q], Dq[q + 1]);
+        fmul2(v[64 + q], v[65 + q], v[q], v[q + 1], d0, d1);  // dS^T
       }
       if (t > 0) {  // the previous dV, dK products read the P^T and dS^T tiles
         ok = __all_sync(0xffffffffu, await(bo, (t - 1) & 1, err, DERR_ACC_WAIT, abort));

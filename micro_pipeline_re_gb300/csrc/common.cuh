@@ -92,30 +92,119 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Two fp32 lanes per instruction (the packed f32x2 forms, each lane rounded
+// as the scalar instruction would): d = a * b + c, a + b, a * b.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 1/x and 2^x on the special-function unit (rcp.approx, ex2.approx: a few ulp;
+// 2^-inf = 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Exact-erf GELU, GELU(z) = z Phi(z), and its derivative Phi(z) + z phi(z),
 // with Phi(z) = 1 - erfc(z / sqrt 2) / 2 and phi(z) = e^{-z^2/2} / sqrt(2 pi).
 // erfc(a), a >= 0, by Abramowitz & Stegun, Handbook of Mathematical Functions,
 // formula 7.1.26: erfc(a) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) e^{-a^2},
 // t = 1 / (1 + p a), |error| <= 1.5e-7.  In this erfc form the negative side
 // has no cancellation and the derivative reuses e^{-a^2} (= e^{-z^2/2}).
-// Cheaper than a general erf: one reciprocal and one exponential on the SFU.
+// One reciprocal and one 2^x on the SFU.  Every step is an explicitly rounded
+// operation, so the scalar form and the two-lane form (gelu_cdf2, f32x2
+// instructions) give the same bits, whichever kernel evaluates it.
+namespace gelu_c {
+constexpr float kInvSqrt2 = 0.70710678118654752f;
+constexpr float kP = 0.3275911f;
+constexpr float kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f, kA4 = -1.453152027f,
+                kA5 = 1.061405429f;
+constexpr float kNegLog2e = -1.4426950408889634f;  // e^{-y} = 2^{-y log2 e}
+constexpr float kInvSqrt2Pi = 0.39894228040143268f;
+}  // namespace gelu_c
 __device__ __forceinline__ float gelu_cdf(float z, float& e) {
-  const float a = fabsf(z) * 0.70710678118654752f;
-  const float t = __fdividef(1.0f, fmaf(0.3275911f, a, 1.0f));
-  const float poly =
-      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
-  e = __expf(-a * a);
-  const float half_erfc = 0.5f * poly * e;
-  return z >= 0.f ? 1.0f - half_erfc : half_erfc;
+  using namespace gelu_c;
+  const float a = __fmul_rn(fabsf(z), kInvSqrt2);
+  const float t = rcp_approx(__fmaf_rn(kP, a, 1.0f));
+  float p = __fmaf_rn(t, kA5, kA4);
+  p = __fmaf_rn(t, p, kA3);
+  p = __fmaf_rn(t, p, kA2);
+  p = __fmaf_rn(t, p, kA1);
+  p = __fmul_rn(t, p);
+  e = ex2_approx(__fmul_rn(__fmul_rn(a, a), kNegLog2e));
+  const float h = __fmul_rn(__fmul_rn(0.5f, p), e);  // erfc(|z| / sqrt 2) / 2
+  return z >= 0.f ? __fmaf_rn(h, -1.0f, 1.0f) : h;
 }
 __device__ __forceinline__ float gelu_f(float z) {
   float e;
-  return z * gelu_cdf(z, e);
+  return __fmul_rn(z, gelu_cdf(z, e));
 }
 __device__ __forceinline__ float gelu_grad_f(float z) {
   float e;
   const float cdf = gelu_cdf(z, e);
-  return fmaf(z * 0.39894228040143268f, e, cdf);
+  return __fmaf_rn(__fmul_rn(z, gelu_c::kInvSqrt2Pi), e, cdf);
+}
+// The same on two values at once (z0, z1), bit for bit.
+__device__ __forceinline__ void gelu_cdf2(float z0, float z1, float& c0, float& c1, float& e0, float& e1) {
+  using namespace gelu_c;
+  float a0, a1, d0, d1, p0, p1, q0, q1, h0, h1;
+  fmul2(a0, a1, fabsf(z0), fabsf(z1), kInvSqrt2, kInvSqrt2);
+  ffma2(d0, d1, kP, kP, a0, a1, 1.0f, 1.0f);
+  const float t0 = rcp_approx(d0), t1 = rcp_approx(d1);
+  ffma2(p0, p1, t0, t1, kA5, kA5, kA4, kA4);
+  ffma2(p0, p1, t0, t1, p0, p1, kA3, kA3);
+  ffma2(p0, p1, t0, t1, p0, p1, kA2, kA2);
+  ffma2(p0, p1, t0, t1, p0, p1, kA1, kA1);
+  fmul2(p0, p1, t0, t1, p0, p1);
+  fmul2(q0, q1, a0, a1, a0, a1);
+  fmul2(q0, q1, q0, q1, kNegLog2e, kNegLog2e);
+  e0 = ex2_approx(q0);
+  e1 = ex2_approx(q1);
+  fmul2(h0, h1, 0.5f, 0.5f, p0, p1);
+  fmul2(h0, h1, h0, h1, e0, e1);
+  float o0, o1;
+  ffma2(o0, o1, h0, h1, -1.0f, -1.0f, 1.0f, 1.0f);
+  c0 = z0 >= 0.f ? o0 : h0;
+  c1 = z1 >= 0.f ? o1 : h1;
+}
+__device__ __forceinline__ void gelu2(float z0, float z1, float& g0, float& g1) {
+  float c0, c1, e0, e1;
+  gelu_cdf2(z0, z1, c0, c1, e0, e1);
+  fmul2(g0, g1, z0, z1, c0, c1);
+}
+__device__ __forceinline__ void gelu_grad2(float z0, float z1, float& g0, float& g1) {
+  float c0, c1, e0, e1, s0, s1;
+  gelu_cdf2(z0, z1, c0, c1, e0, e1);
+  fmul2(s0, s1, z0, z1, gelu_c::kInvSqrt2Pi, gelu_c::kInvSqrt2Pi);
+  ffma2(g0, g1, s0, s1, e0, e1, c0, c1);
 }
 
 // ---------------------------------------------------------------------------
@@ -199,6 +288,11 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -253,6 +347,75 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// The same for a pair of CTAs of a cluster (cta_group::2): one 256-row MMA
+// reads A (128 rows each) and B (half the columns each) from both CTAs' shared
+// memory at the same offsets and accumulates each CTA's 128 rows in its own
+// tensor memory.  Allocation and release are done by one warp in each CTA.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier at this offset in every CTA of cta_mask once the
+// pair's previously issued tcgen05 ops complete.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+// Tile load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (bar_cluster: a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, int x, int y, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// Bounded wait with acquire at cluster scope (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
+      "p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_t parity, int* err, int code) {
+  uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicExch(err, code);
+      return false;
+    }
+  }
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane

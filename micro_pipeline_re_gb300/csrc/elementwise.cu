@@ -4,6 +4,7 @@
 // order (no floating-point atomics), so every result is bit-reproducible and
 // a re-computed forward equals the first one byte for byte.
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/gpipe.h"
 #include "common.cuh"
@@ -43,19 +44,30 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const TI* __restrict__ x, c
   const int row = blockIdx.x * 8 + warp;
   if (row >= rows) return;
   const TI* xr = x + (int64_t)row * d;
-  float v[kMaxChunks][8];
-  float s = 0.f;
+  // every load of the row (x, and gamma / beta for the output) is issued
+  // before the first reduction, so the row costs one memory round trip
+  float v[kMaxChunks][8], gg[kMaxChunks][8], bb[kMaxChunks][8];
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     const int col = (c * 32 + lane) * 8;
     if (col < d) {
       load8(xr + col, v[c]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s += v[c][j];
+      load8(g + col, gg[c]);
+      load8(b + col, bb[c]);
     }
   }
-  const float mu = warp_sum(s) / d;
-  float q = 0.f;
+  // sums over 8 independent partials per lane (short dependency chains)
+  float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int col = (c * 32 + lane) * 8;
+    if (col < d) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s8[j] += v[c][j];
+    }
+  }
+  const float mu = warp_sum(((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]))) / d;
+  float q8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     const int col = (c * 32 + lane) * 8;
@@ -63,22 +75,20 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const TI* __restrict__ x, c
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float t = v[c][j] - mu;
-        q += t * t;
+        q8[j] = fmaf(t, t, q8[j]);
       }
     }
   }
-  const float var = warp_sum(q) / d;
+  const float var = warp_sum(((q8[0] + q8[1]) + (q8[2] + q8[3])) + ((q8[4] + q8[5]) + (q8[6] + q8[7]))) / d;
   const float rs = 1.0f / sqrtf(var + kLnEps);
   TO* yr = y + (int64_t)row * d;
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     const int col = (c * 32 + lane) * 8;
     if (col < d) {
-      float gg[8], bb[8], o[8];
-      load8(g + col, gg);
-      load8(b + col, bb);
+      float o[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] = (v[c][j] - mu) * rs * gg[j] + bb[j];
+      for (int j = 0; j < 8; ++j) o[j] = (v[c][j] - mu) * rs * gg[c][j] + bb[c][j];
       store8(yr + col, o);
     }
   }
@@ -90,11 +100,12 @@ __global__ void __launch_bounds__(256) ln_fwd_kernel(const TI* __restrict__ x, c
 
 // ---------------------------------------------------------------------------
 // LayerNorm backward.  Block b (8 warps) handles rows 8b .. 8b+7, one row per
-// warp, with CH 256-column chunks per row (d <= 256*CH).  The warps then put
-// their dg and db column sums in shared memory and each column is added over
-// the warps in warp order (one barrier per half) into one partial row of
-// scratch; col_reduce adds the partial rows in order.  Both orders are fixed,
-// so results are bit-reproducible.
+// warp, with CH 256-column chunks per row (d <= 256*CH).  Each warp writes its
+// row's dg and db terms (dy * x-hat, dy) to shared memory as soon as they are
+// known; after one barrier every column is added over the warps in warp order
+// into one partial row of scratch; col_reduce adds the partial rows in order.
+// Both orders are fixed, so results are bit-reproducible.  Dynamic shared
+// memory: 2 x 8 x d floats.
 // ---------------------------------------------------------------------------
 template <typename TD, typename TX, typename TO, int CH>
 __global__ void __launch_bounds__(256) ln_bwd_kernel(const TD* __restrict__ dy, const TX* __restrict__ x,
@@ -104,38 +115,53 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const TD* __restrict__ dy, 
                                                      float* __restrict__ partial, int rows, int d) {
   griddep_wait();
   griddep_launch();
-  __shared__ __align__(16) float stage[kLnRowsPerWarp][32 * 8 * CH];
+  extern __shared__ __align__(16) float ln_stage[];  // [2][8][d]: dg terms, then db terms
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * kLnRowsPerWarp + warp;
-  float pg[CH][8], pb[CH][8];
-#pragma unroll
-  for (int c = 0; c < CH; ++c)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) pg[c][j] = pb[c][j] = 0.f;
+  float* sg = ln_stage + warp * d;
+  float* sb = ln_stage + (kLnRowsPerWarp + warp) * d;
   if (r < rows) {
     const float mu = mean[r], rs = rstd[r];
-    float xh[CH][8], gd[CH][8];
-    float s1 = 0.f, s2 = 0.f;
+    // every load of the row (x, dy, gamma and the residual gradient) is issued
+    // before the first reduction: one memory round trip per row
+    float xh[CH][8], gd[CH][8], rv[CH][8];
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int col = (c * 32 + lane) * 8;
       if (col < d) {
-        float xv[8], dv[8], gg[8];
-        load8(x + (int64_t)r * d + col, xv);
+        float dv[8];
+        load8(x + (int64_t)r * d + col, xh[c]);
         load8(dy + (int64_t)r * d + col, dv);
-        load8(g + col, gg);
+        load8(g + col, gd[c]);
+        if (dres) load8(dres + (int64_t)r * d + col, rv[c]);
+        float tg[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          xh[c][j] = (xv[j] - mu) * rs;
-          gd[c][j] = gg[j] * dv[j];
-          s1 += gd[c][j];
-          s2 += gd[c][j] * xh[c][j];
-          pg[c][j] = dv[j] * xh[c][j];
-          pb[c][j] = dv[j];
+          xh[c][j] = (xh[c][j] - mu) * rs;
+          gd[c][j] = gd[c][j] * dv[j];  // gamma * dy
+          tg[j] = dv[j] * xh[c][j];     // dg term
+        }
+        *reinterpret_cast<float4*>(sg + col) = make_float4(tg[0], tg[1], tg[2], tg[3]);
+        *reinterpret_cast<float4*>(sg + col + 4) = make_float4(tg[4], tg[5], tg[6], tg[7]);
+        *reinterpret_cast<float4*>(sb + col) = make_float4(dv[0], dv[1], dv[2], dv[3]);
+        *reinterpret_cast<float4*>(sb + col + 4) = make_float4(dv[4], dv[5], dv[6], dv[7]);
+      }
+    }
+    // the two row sums over 8 independent partials per lane
+    float s1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, s2[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = (c * 32 + lane) * 8;
+      if (col < d) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          s1[j] += gd[c][j];
+          s2[j] += gd[c][j] * xh[c][j];
         }
       }
     }
-    const float m1 = warp_sum(s1) / d, m2 = warp_sum(s2) / d;
+    const float m1 = warp_sum(((s1[0] + s1[1]) + (s1[2] + s1[3])) + ((s1[4] + s1[5]) + (s1[6] + s1[7]))) / d;
+    const float m2 = warp_sum(((s2[0] + s2[1]) + (s2[2] + s2[3])) + ((s2[4] + s2[5]) + (s2[6] + s2[7]))) / d;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int col = (c * 32 + lane) * 8;
@@ -144,38 +170,28 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const TD* __restrict__ dy, 
 #pragma unroll
         for (int j = 0; j < 8; ++j) o[j] = rs * (gd[c][j] - m1 - xh[c][j] * m2);
         if (dres) {
-          float rv[8];
-          load8(dres + (int64_t)r * d + col, rv);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[j] += rv[j];
+          for (int j = 0; j < 8; ++j) o[j] += rv[c][j];
         }
         store8(dx + (int64_t)r * d + col, o);
         if (dx16) store8(dx16 + (int64_t)r * d + col, o);  // the same values as bf16 (GEMM operands)
       }
     }
+  } else {  // a row past the end adds nothing
+    for (int col = lane * 4; col < d; col += 128) {
+      *reinterpret_cast<float4*>(sg + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(sb + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
-  // fold the 8 warps' column sums in warp order: dg into partial[0, d), db into [d, 2d)
+  __syncthreads();
+  // fold the 8 rows' terms in warp order: dg into partial[0, d), db into [d, 2d)
   float* pr = partial + (int64_t)blockIdx.x * 2 * d;
+  for (int col = threadIdx.x; col < 2 * d; col += 256) {
+    const float* src = ln_stage + (col < d ? col : kLnRowsPerWarp * d + (col - d));
+    float a = src[0];
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int col = (c * 32 + lane) * 8;
-      if (col < d) {
-        float* dst = &stage[warp][col];
-        const float* src = half == 0 ? pg[c] : pb[c];
-        *reinterpret_cast<float4*>(dst) = make_float4(src[0], src[1], src[2], src[3]);
-        *reinterpret_cast<float4*>(dst + 4) = make_float4(src[4], src[5], src[6], src[7]);
-      }
-    }
-    __syncthreads();
-    for (int col = threadIdx.x; col < d; col += 256) {
-      float a = stage[0][col];
-#pragma unroll
-      for (int w = 1; w < kLnRowsPerWarp; ++w) a += stage[w][col];
-      pr[half * d + col] = a;
-    }
-    __syncthreads();
+    for (int w = 1; w < kLnRowsPerWarp; ++w) a += src[w * d];
+    pr[col] = a;
   }
 }
 
@@ -226,56 +242,67 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict
 // ---------------------------------------------------------------------------
 // Bias gradient of a weight-gradient GEMM (db[m] += sum_k A(m, k)) in one
 // launch without scratch, fixed order.
-//  - A MN-major (stored [K][M], the step's dY): block b owns the 64 columns
-//    m = 64b .. 64b+63; thread t sums the 8 columns 8(t%8).. over rows
-//    k = t/8, t/8 + 32, ... (16-B loads, a row's 128 B read by 8 threads), then
-//    the 32 row groups are added in order through shared memory.
+//  - A MN-major (stored [K][M], the step's dY): a cluster of kDbSplit CTAs
+//    owns the 64 columns m = 64x .. 64x+63, CTA s of it the rows of its K
+//    range; thread t sums the 8 columns 8(t%8).. over rows k = t/8, t/8 + 32,
+//    ... of the range (16-B loads, 8 rows in flight, a row's 128 B read by 8
+//    threads), the 32 row groups are added in order through shared memory,
+//    and CTA 0 adds the kDbSplit range sums in rank order (distributed shared
+//    memory) into db.
 //  - A K-major (stored [M][K]): one warp per row m, lanes over k, shuffle fold.
 // ---------------------------------------------------------------------------
+constexpr int kDbSplit = 8;
+
 __global__ void __launch_bounds__(256) dbias_mn_kernel(const __nv_bfloat16* __restrict__ a, int64_t lda, int M,
                                                         int K, float* __restrict__ db) {
   griddep_wait();
   griddep_launch();
   __shared__ float part[32][64 + 1];
+  __shared__ __align__(16) float tot[64];
   const int c8 = (threadIdx.x & 7) * 8, g = threadIdx.x >> 3;
   const int m0 = blockIdx.x * 64;
+  const int kper = ((K + kDbSplit - 1) / kDbSplit + 31) / 32 * 32;  // rows per CTA, a multiple of 32
+  const int kb = static_cast<int>(blockIdx.y) * kper;
+  const int ke = min(K, kb + kper);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (m0 + c8 + 8 <= M) {
-    int k = g;
-    for (; k + 96 < K; k += 128) {  // four rows in flight
-      float v0[8], v1[8], v2[8], v3[8];
-      load8(a + static_cast<int64_t>(k) * lda + m0 + c8, v0);
-      load8(a + static_cast<int64_t>(k + 32) * lda + m0 + c8, v1);
-      load8(a + static_cast<int64_t>(k + 64) * lda + m0 + c8, v2);
-      load8(a + static_cast<int64_t>(k + 96) * lda + m0 + c8, v3);
+    int k = kb + g;
+    for (; k + 224 < ke; k += 256) {  // eight rows in flight
+      float v[8][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] += v0[j];
+      for (int u = 0; u < 8; ++u) load8(a + static_cast<int64_t>(k + 32 * u) * lda + m0 + c8, v[u]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] += v1[j];
+      for (int u = 0; u < 8; ++u)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] += v2[j];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] += v3[j];
+        for (int j = 0; j < 8; ++j) acc[j] += v[u][j];
     }
-    for (; k < K; k += 32) {
+    for (; k < ke; k += 32) {
       float v[8];
       load8(a + static_cast<int64_t>(k) * lda + m0 + c8, v);
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] += v[j];
     }
   } else {
-    for (int k = g; k < K; k += 32)
+    for (int k = kb + g; k < ke; k += 32)
       for (int j = 0; j < 8; ++j)
         if (m0 + c8 + j < M) acc[j] += bf2f(a[static_cast<int64_t>(k) * lda + m0 + c8 + j]);
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[g][c8 + j] = acc[j];
   __syncthreads();
-  if (threadIdx.x < 64 && m0 + static_cast<int>(threadIdx.x) < M) {
+  if (threadIdx.x < 64) {
     float t = part[0][threadIdx.x];
     for (int r = 1; r < 32; ++r) t += part[r][threadIdx.x];
+    tot[threadIdx.x] = t;
+  }
+  cluster_sync();  // every range sum of the cluster is in place
+  if (cluster_ctarank() == 0 && threadIdx.x < 64 && m0 + static_cast<int>(threadIdx.x) < M) {
+    const uint32_t mine = smem_u32(&tot[threadIdx.x]);
+    float t = ld_peer_f32(map_peer(mine, 0));
+    for (int q = 1; q < kDbSplit; ++q) t += ld_peer_f32(map_peer(mine, static_cast<uint32_t>(q)));
     db[m0 + threadIdx.x] += t;
   }
+  cluster_sync();  // the peers keep their shared memory until CTA 0 has read it
 }
 
 __global__ void __launch_bounds__(256) dbias_k_kernel(const __nv_bfloat16* __restrict__ a, int64_t lda, int M, int K,
@@ -665,6 +692,19 @@ int launch_layernorm_fwd(int dtype, int rows, int d, const void* x, const float*
 }
 
 namespace {
+size_t ln_bwd_smem(int d) { return static_cast<size_t>(2 * kLnRowsPerWarp) * d * sizeof(float); }
+
+template <typename TD, typename TX, typename TO>
+cudaError_t ln_bwd_attr() {
+  const int mx = static_cast<int>(ln_bwd_smem(32 * 8 * kMaxChunks));
+  cudaError_t e = cudaFuncSetAttribute(ln_bwd_kernel<TD, TX, TO, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ln_bwd_kernel<TD, TX, TO, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ln_bwd_kernel<TD, TX, TO, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  return e;
+}
+
 template <typename TD, typename TX, typename TO>
 void ln_bwd_launch(int grid, int d, cudaStream_t s, const void* dy, const void* x, const float* mean, const float* rstd,
                    const float* g, const void* dres, void* dx, void* dx16, float* scratch, int rows) {
@@ -674,13 +714,25 @@ void ln_bwd_launch(int grid, int d, cudaStream_t s, const void* dy, const void* 
   TO* dxp = static_cast<TO*>(dx);
   __nv_bfloat16* d16 = static_cast<__nv_bfloat16*>(dx16);
   if (d <= 256)
-    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 1>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
+    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 1>, grid, 256, ln_bwd_smem(d), s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
   else if (d <= 512)
-    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 2>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
+    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 2>, grid, 256, ln_bwd_smem(d), s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
   else
-    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 4>, grid, 256, 0, s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
+    (void)launch_k(ln_bwd_kernel<TD, TX, TO, 4>, grid, 256, ln_bwd_smem(d), s, dyp, xp, mean, rstd, g, rp, dxp, d16, scratch, rows, d);
 }
 }  // namespace
+
+int prepare_layernorm() {
+  static std::atomic<unsigned long long> done{0};
+  return once_per_device(done, []() -> int {
+    using bf = __nv_bfloat16;
+    cudaError_t e = ln_bwd_attr<float, float, float>();
+    if (e == cudaSuccess) e = ln_bwd_attr<bf, bf, bf>();
+    if (e == cudaSuccess) e = ln_bwd_attr<bf, float, float>();
+    return e == cudaSuccess ? static_cast<int>(GPIPE_OK)
+                            : set_error(GPIPE_ERR_CUDA, "layernorm_bwd: shared-memory attribute: %s", cudaGetErrorString(e));
+  });
+}
 
 int launch_layernorm_bwd_rows_io(int dy_dtype, int x_dtype, int out_dtype, int rows, int d, const void* dy,
                                  const void* x, const float* mean, const float* rstd, const float* g, const void* dres,
@@ -690,6 +742,8 @@ int launch_layernorm_bwd_rows_io(int dy_dtype, int x_dtype, int out_dtype, int r
   if (!al16(dy) || !al16(x) || !al16(dx) || !al16(g) || (dres && !al16(dres)) || (dx16 && !al16(dx16)) ||
       !al16(scratch))
     return set_error(GPIPE_ERR_INVALID_ARG, "layernorm_bwd: pointers must be 16-B aligned");
+  const int rc = prepare_layernorm();
+  if (rc) return rc;
   const int grid = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
   using bf = __nv_bfloat16;
   if (dy_dtype == DT_F32 && x_dtype == DT_F32 && out_dtype == DT_F32)
@@ -727,8 +781,24 @@ int launch_dbias(bool a_kmajor, int M, int K, const void* a, int64_t lda, float*
   const __nv_bfloat16* ap = static_cast<const __nv_bfloat16*>(a);
   if (a_kmajor)
     (void)launch_k(dbias_k_kernel, blocks_for(M, 8), 256, 0, s, ap, lda, M, K, db);
-  else
-    (void)launch_k(dbias_mn_kernel, blocks_for(M, 64), 256, 0, s, ap, lda, M, K, db);
+  else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks_for(M, 64), kDbSplit, 1);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[3];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = kDbSplit;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    set_priority_attr(attr[2], s);
+    cfg.attrs = attr;
+    cfg.numAttrs = 3;
+    (void)cudaLaunchKernelEx(&cfg, dbias_mn_kernel, ap, lda, M, K, db);
+  }
   return check_launch("bias gradient");
 }
 

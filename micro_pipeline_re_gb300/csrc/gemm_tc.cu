@@ -326,10 +326,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int u = 0; u < 4; ++u) {
             float t[8];
             load8(reinterpret_cast<const __nv_bfloat16*>(box + swz(r, u0 + u)), t);
+            if (EPI == EPI_GELU_BWD) {  // two lanes at a time
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              if (EPI == EPI_GELU_BWD) v[8 * u + q] *= gelu_grad_f(t[q]);
-              else v[8 * u + q] += t[q];
+              for (int q = 0; q < 8; q += 2) {
+                float g0, g1;
+                gelu_grad2(t[q], t[q + 1], g0, g1);
+                fmul2(v[8 * u + q], v[8 * u + q + 1], v[8 * u + q], v[8 * u + q + 1], g0, g1);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) v[8 * u + q] += t[q];
             }
           }
         }
@@ -341,7 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int u = 0; u < 4; ++u) {
             float t[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) t[q] = gelu_f(v[8 * u + q]);
+            for (int q = 0; q < 8; q += 2) gelu2(v[8 * u + q], v[8 * u + q + 1], t[q], t[q + 1]);
             store8(reinterpret_cast<__nv_bfloat16*>(box2 + swz(r, u0 + u)), t);
           }
         }

@@ -138,6 +138,7 @@ int launch_count_diff(const void* a, const void* b, size_t bytes, unsigned long 
 int prepare_kernels();
 int prepare_gemm_tc();
 int prepare_attention();
+int prepare_layernorm();
 
 // Number of SMs of the current device (cached).
 int num_sms();

@@ -86,6 +86,8 @@ int prepare_kernels() {
   if (rc) return rc;
   rc = prepare_attention();
   if (rc) return rc;
+  rc = prepare_layernorm();
+  if (rc) return rc;
   if (!device_error_ptr()) return set_error(GPIPE_ERR_CUDA, "cannot resolve the device error flag");
   num_sms();
   return GPIPE_OK;
