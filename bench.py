@@ -371,6 +371,63 @@ def attention_roofline(b, peaks, nseq, seq, heads, reps=50):
             "peak": peaks["bf16"], "peak_source": peaks["source"] + " (burst)"}
 
 
+def layernorm_roofline(b, peaks, rows, d, reps=50):
+    """Time the LayerNorm forward and backward rows (fp32 in and out, as the
+    step's residual stream) alone: CUDA events around a graph of `reps`
+    launches that cycle through enough row blocks that every launch reads from
+    HBM (the blocks together exceed L2).  Algorithmic bytes per launch:
+    forward reads x and writes y (8 d B per row) and the row statistics (8 B);
+    backward reads dy, x, the residual gradient and the statistics and writes
+    dx (16 d B + 8 B per row) plus one partial row per 8 rows (two d-float
+    halves)."""
+    import torch
+    lib = b.lib()
+    nbuf = max(2, -(-(256 << 20) // (rows * d * 4 * 4)))  # > 256 MB across the buffers of one pass
+    xs = [torch.randn(rows, d, device="cuda") for _ in range(nbuf)]
+    dys = [torch.randn(rows, d, device="cuda") for _ in range(nbuf)]
+    res = [torch.randn(rows, d, device="cuda") for _ in range(nbuf)]
+    ys = [torch.empty(rows, d, device="cuda") for _ in range(nbuf)]
+    g = torch.ones(d, device="cuda")
+    bb = torch.zeros(d, device="cuda")
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    dg = torch.zeros(d, device="cuda")
+    db = torch.zeros(d, device="cuda")
+    scratch = torch.empty(lib.gpipe_op_scratch_bytes(rows, 2 * d) // 4 + 64, device="cuda")
+    out = {}
+
+    def fwd(i, st):
+        return lib.gpipe_op_layernorm_fwd(0, rows, d, xs[i].data_ptr(), g.data_ptr(), bb.data_ptr(),
+                                          ys[i].data_ptr(), mean.data_ptr(), rstd.data_ptr(), st)
+
+    def bwd(i, st):
+        return lib.gpipe_op_layernorm_bwd(0, rows, d, dys[i].data_ptr(), xs[i].data_ptr(), mean.data_ptr(),
+                                          rstd.data_ptr(), g.data_ptr(), res[i].data_ptr(), ys[i].data_ptr(),
+                                          dg.data_ptr(), db.data_ptr(), scratch.data_ptr(), st)
+    for name, fn, nbytes in (("forward", fwd, rows * (8 * d + 8)),
+                             ("backward", bwd, rows * (16 * d + 8) + (rows + 7) // 8 * 2 * d * 4)):
+        for i in range(nbuf):
+            assert fn(i, torch.cuda.current_stream().cuda_stream) == 0
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for r in range(reps):
+                fn(r % nbuf, torch.cuda.current_stream().cuda_stream)
+        gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        dt = e0.elapsed_time(e1) / 1e3 / reps
+        out[name] = {"us": dt * 1e6, "gbs": nbytes / dt / 1e9, "frac": nbytes / dt / 1e9 / peaks["hbm"],
+                     "bytes": nbytes}
+    return {"kernel": f"LayerNorm fp32 rows={rows} d={d} (the backward includes its column-sum reduction)",
+            **out, "peak": peaks["hbm"], "peak_source": peaks["source"],
+            "timing": f"CUDA events around a graph of {reps} launches cycling over {nbuf} buffer sets"}
+
+
 EPI_NAMES = {0: "bf16 store epilogue (bias)", 1: "bias + GELU epilogue", 2: "GELU-backward epilogue",
              3: "fp32 TMA reduce-add epilogue (weight gradient, bias gradient)", 4: "fp32 store epilogue",
              5: "fp32 residual epilogue (bias + fp32 residual, fp32 store)"}
@@ -659,6 +716,8 @@ def main():
                     help="the micro-batch sweep workload over its (K, M) grid (one line per point)")
     ap.add_argument("--probe-attention", action="store_true",
                     help="only time the attention forward and backward at one micro-batch of the workload")
+    ap.add_argument("--probe-layernorm", type=int, default=0, metavar="ROWS",
+                    help="only time the LayerNorm forward and backward alone on ROWS rows of the workload's width")
     ap.add_argument("--layers", type=int, default=0,
                     help="run the workload with this many layers instead (memory measurements at reduced L)")
     args = ap.parse_args()
@@ -685,6 +744,12 @@ def main():
         from micro_pipeline_re_gb300 import binding as b
         print(json.dumps(attention_roofline(b, load_peaks(), w.tokens_per_micro_batch // w.seq, w.seq, w.heads)),
               flush=True)
+        return
+    if args.probe_layernorm:
+        from micro_pipeline_re_gb300._build import build as _build
+        _build()
+        from micro_pipeline_re_gb300 import binding as b
+        print(json.dumps(layernorm_roofline(b, load_peaks(), args.probe_layernorm, w.d)), flush=True)
         return
     if args.impl == "reference":
         run_reference(args, w)

@@ -69,7 +69,7 @@ size_t gpipe_op_scratch_bytes(int rows, int cols);
 
 /* LayerNorm over rows of width d (eps 1e-5, biased variance):
  * y = (x - mean) * rstd * g + b; mean and rstd (fp32 [rows]) are saved.
- * d must be a multiple of 8 and at most 2048. */
+ * d must be a multiple of 8 and at most 1024 (GPIPE_ERR_INVALID_ARG otherwise). */
 int gpipe_op_layernorm_fwd(int dtype, int rows, int d, const void* x, const float* g,
                            const float* b, void* y, float* mean, float* rstd, void* stream);
 

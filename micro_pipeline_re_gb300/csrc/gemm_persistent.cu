@@ -36,18 +36,23 @@ constexpr int PK = 64;
 constexpr int P_THREADS = 320;      // 10 warps
 constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
 
-template <int BN, int EPI>
+// PAIR: a cluster of two CTAs computes 256 x BN tiles with 256-row MMAs
+// (cta_group::2); each CTA holds 128 rows of A and BN/2 columns of B per stage
+// and accumulates its own 128 rows in its tensor memory.
+template <int BN, int EPI, bool PAIR = false>
 struct PCfg {
   static constexpr bool F32_OUT = (EPI == EPI_ACC_F32 || EPI == EPI_STORE_F32 || EPI == EPI_RESID_F32);
+  static constexpr int TM = PAIR ? 2 * PM : PM;  // rows of a tile
+  static constexpr int BH = PAIR ? BN / 2 : BN;  // columns of B one CTA holds
   static constexpr int A_BYTES = PM * PK * 2;
-  static constexpr int B_BYTES = BN * PK * 2;
+  static constexpr int B_BYTES = BH * PK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // an epilogue warp's staging box: 32 rows x 32 columns (64-byte rows in bf16,
   // 128-byte rows in fp32); bias+GELU writes two (z and GELU(z))
   static constexpr int BOX_BYTES = 32 * 32 * (F32_OUT ? 4 : 2);
   static constexpr int BOXES = EPI == EPI_BIAS_GELU ? 2 : 1;
   // bias gradient by MMA against ones (2 x 16 TMEM columns beside the accumulators) when they fit
-  static constexpr bool DB_MMA = EPI == EPI_ACC_F32 && 2 * BN + 32 <= 512;
+  static constexpr bool DB_MMA = !PAIR && EPI == EPI_ACC_F32 && 2 * BN + 32 <= 512;
   static constexpr int ONES_BYTES = DB_MMA ? 2048 : 0;
   static constexpr int fit(int nbuf) { return (SMEM_BUDGET - 8 * nbuf * BOXES * BOX_BYTES - ONES_BYTES) / STAGE_BYTES; }
   // two staging buffers per warp (a chunk's store drains while the next chunk
@@ -60,6 +65,7 @@ struct PCfg {
   static constexpr int OFF_ONES = OFF_STG + STAGING;
   static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
+  static constexpr int MMA_M = PAIR ? 2 * PM : PM;
   // TMEM: two accumulators of BN columns (+ 2 x 16 bias-gradient columns)
   static constexpr int TCOLS = (2 * BN + (DB_MMA ? 32 : 0)) <= 256 ? 256 : 512;
   static_assert(STAGES >= 3, "not enough shared memory for three stages");
@@ -95,13 +101,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 // Origin (row, column) of tile t in the grouped tile order.
-template <int BN>
+template <int TM, int BN>
 __device__ __forceinline__ void tile_origin(int t, const PArgs& a, int& m0, int& n0) {
   const int per_group = PGROUP * a.n_tiles;
   const int grp = t / per_group, r = t - grp * per_group;
   const int first = grp * PGROUP;
   const int gm = a.m_tiles - first < PGROUP ? a.m_tiles - first : PGROUP;
-  m0 = (first + r % gm) * PM;
+  m0 = (first + r % gm) * TM;
   n0 = (r / gm) * BN;
 }
 
@@ -113,13 +119,14 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, int* err, 
   return false;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
+template <bool A_K, bool B_K, int BN, int EPI, bool PAIR = false>
 __global__ void __launch_bounds__(P_THREADS, 1)
     tc_gemm_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
                        PArgs args, int* err) {
-  using Cfg = PCfg<BN, EPI>;
+  using Cfg = PCfg<BN, EPI, PAIR>;
   constexpr int STAGES = Cfg::STAGES;
+  constexpr int TM = Cfg::TM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sStg = smem + Cfg::OFF_STG;
@@ -128,13 +135,19 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* accf = empty + STAGES;  // accumulator b holds a finished tile
   uint64_t* acce = accf + 2;        // accumulator b has been drained
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(acce + 2);
+  uint64_t* bfin = acce + 2;        // every MMA of the CTA (pair) has completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bfin + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int total = args.m_tiles * args.n_tiles;
   const int nk = (args.K + PK - 1) / PK;
+  // PAIR: rank 0 of the pair issues the MMAs; both load their halves and run
+  // their epilogues; the pair walks tiles pair, pair + pairs, ...
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank() & 1u) : 0;
+  const int first_tile = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -145,8 +158,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 8);  // one arrival per epilogue warp
+      mbar_init(&acce[b], PAIR ? 16 : 8);  // one arrival per epilogue warp (of both CTAs)
     }
+    mbar_init(bfin, 1);
     *abort = 0;
     fence_barrier_init();
   }
@@ -155,11 +169,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     fence_proxy_async_smem();
   }
   if (warp == 1) {
-    tmem_alloc(tslot, Cfg::TCOLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tslot, Cfg::TCOLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tslot, Cfg::TCOLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) cluster_sync();  // both CTAs' barriers exist before any copy or arrival names them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   griddep_wait();  // the previous kernel in the stream has completed; global reads from here on
@@ -167,47 +187,77 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       int it = 0;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      for (int t = first_tile; t < total && !*abort; t += tile_step) {
         int m0, n0;
-        tile_origin<BN>(t, args, m0, n0);
+        tile_origin<TM, BN>(t, args, m0, n0);
+        const int am = m0 + rank * PM;        // this CTA's rows of A
+        const int bn = n0 + rank * Cfg::BH;   // this CTA's columns of B
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           if (!pwait(&empty[s], ((it / STAGES) & 1) ^ 1, err, DERR_TMA_WAIT, abort)) break;
-          mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
           uint8_t* a = smem + s * Cfg::STAGE_BYTES;
           uint8_t* b = a + Cfg::A_BYTES;
           const int k0 = kb * PK;
-          if (A_K) {
-            tma_load_2d(a, &tmA, k0, m0, &full[s]);
-          } else {
-            tma_load_2d(a, &tmA, m0, k0, &full[s]);
-            tma_load_2d(a + 8192, &tmA, m0 + 64, k0, &full[s]);
-          }
-          if (B_K) {
-            tma_load_2d(b, &tmB, k0, n0, &full[s]);
-          } else {
+          if (PAIR) {
+            // both CTAs' copies complete on rank 0's barrier, which expects the bytes of both
+            const uint32_t fb = map_peer(smem_u32(&full[s]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * Cfg::STAGE_BYTES);
+            if (A_K) {
+              tma_load_2d_pair(a, &tmA, k0, am, fb);
+            } else {
+              tma_load_2d_pair(a, &tmA, am, k0, fb);
+              tma_load_2d_pair(a + 8192, &tmA, am + 64, k0, fb);
+            }
+            if (B_K) {
+              tma_load_2d_pair(b, &tmB, k0, bn, fb);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b + j * 8192, &tmB, n0 + 64 * j, k0, &full[s]);
+              for (int j = 0; j < Cfg::BH / 64; ++j) tma_load_2d_pair(b + j * 8192, &tmB, bn + 64 * j, k0, fb);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+            if (A_K) {
+              tma_load_2d(a, &tmA, k0, am, &full[s]);
+            } else {
+              tma_load_2d(a, &tmA, am, k0, &full[s]);
+              tma_load_2d(a + 8192, &tmA, am + 64, k0, &full[s]);
+            }
+            if (B_K) {
+              tma_load_2d(b, &tmB, k0, bn, &full[s]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(b + j * 8192, &tmB, bn + 64 * j, k0, &full[s]);
+            }
           }
         }
       }
-      // no copy may still be landing in shared memory when the CTA exits
-      for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-        mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, err, DERR_DRAIN_WAIT);
+      // no copy may still be landing in shared memory when the CTA exits (the
+      // pair's copies all complete on rank 0's barriers; rank 1 is held by the
+      // final cluster barrier until rank 0 has seen them)
+      if (rank == 0)
+        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, err, DERR_DRAIN_WAIT);
     }
     griddep_launch();
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = mma_idesc_bf16(PM, BN, !A_K, !B_K);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = mma_idesc_bf16(Cfg::MMA_M, BN, !A_K, !B_K);
       constexpr uint32_t idesc_db = mma_idesc_bf16(PM, 16, !A_K, false);
       const uint32_t ones = smem_u32(sOnes);
       int it = 0, i = 0;
-      for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+      for (int t = first_tile; t < total; t += tile_step, ++i) {
         const int b = i & 1;
-        if (!pwait(&acce[b], ((i >> 1) & 1) ^ 1, err, DERR_MMA_WAIT, abort)) break;
+        if (PAIR) {  // the peer's epilogue warps arrive from the other CTA
+          if (*abort || !mbar_wait_bounded_cluster(&acce[b], ((i >> 1) & 1) ^ 1, err, DERR_MMA_WAIT)) {
+            *abort = 1;
+            break;
+          }
+        } else if (!pwait(&acce[b], ((i >> 1) & 1) ^ 1, err, DERR_MMA_WAIT, abort)) {
+          break;
+        }
         tc_fence_after();
         int tm0, tn0;
-        tile_origin<BN>(t, args, tm0, tn0);
+        tile_origin<TM, BN>(t, args, tm0, tn0);
         const bool do_db = Cfg::DB_MMA && args.dbias != nullptr && tn0 == 0;
         const uint32_t dacc = tmem + b * BN;
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -221,13 +271,24 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             const uint64_t ad = A_K ? sw128_desc(a + kk * 32, 16, 1024) : sw128_desc(a + kk * 2048, 8192, 1024);
             const uint64_t bd = B_K ? sw128_desc(bb + kk * 32, 16, 1024) : sw128_desc(bb + kk * 2048, 8192, 1024);
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-            tc_mma_f16(dacc, ad, bd, idesc, acc);
-            if (do_db) tc_mma_f16(tmem + 2 * BN + 16 * b, ad, sw128_desc(ones + kk * 32, 16, 1024), idesc_db, acc);
+            if (PAIR) {
+              tc_mma_f16_pair(dacc, ad, bd, idesc, acc);
+            } else {
+              tc_mma_f16(dacc, ad, bd, idesc, acc);
+              if (do_db) tc_mma_f16(tmem + 2 * BN + 16 * b, ad, sw128_desc(ones + kk * 32, 16, 1024), idesc_db, acc);
+            }
           }
-          tc_commit(&empty[s]);
+          if (PAIR) tc_commit_pair(&empty[s], 3);  // both CTAs' stage s is free again
+          else tc_commit(&empty[s]);
         }
-        tc_commit(&accf[b]);  // fires once this tile's MMAs have completed
+        // fires once this tile's MMAs have completed (in both CTAs of a pair)
+        if (PAIR) tc_commit_pair(&accf[b], 3);
+        else tc_commit(&accf[b]);
       }
+      // every product issued has completed before the tensor memory is released
+      if (PAIR) tc_commit_pair(bfin, 1);
+      else tc_commit(bfin);
+      mbar_wait_bounded(bfin, 0, err, DERR_DRAIN_WAIT);
     }
     griddep_launch();
   } else {
@@ -246,10 +307,13 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     uint8_t* wst = sStg + (warp - 2) * Cfg::WARP_STG;
     int nst = 0;  // chunks this warp has staged (alternates its buffers)
     int i = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+    // rank 0's acce barrier (the MMA issuer's); a pair's epilogue warps arrive on it from both CTAs
+    const uint32_t acce_leader = PAIR ? map_peer(smem_u32(acce), 0) : 0u;
+    for (int t = first_tile; t < total; t += tile_step, ++i) {
       const int b = i & 1;
       int m0, n0;
-      tile_origin<BN>(t, args, m0, n0);
+      tile_origin<TM, BN>(t, args, m0, n0);
+      m0 += rank * PM;  // this CTA's 128 rows of the tile
       const int m = m0 + r;
       const int c0 = n0 + h * HALF;  // the warp's first column
       int nch = (args.N - c0 + 31) / 32;  // its chunks inside the matrix
@@ -317,6 +381,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
               for (int e = 0; e < 4; ++e) {
                 if (X_F32) {
                   apply(v[4 * j + e], __uint_as_float(w4[e]));
+                } else if (EPI == EPI_GELU_BWD) {  // two lanes at a time
+                  const float2 f = unpack_bf16x2(w4[e]);
+                  float g0, g1;
+                  gelu_grad2(f.x, f.y, g0, g1);
+                  fmul2(v[8 * j + 2 * e], v[8 * j + 2 * e + 1], v[8 * j + 2 * e], v[8 * j + 2 * e + 1], g0, g1);
                 } else {
                   const float2 f = unpack_bf16x2(w4[e]);
                   apply(v[8 * j + 2 * e], f.x);
@@ -351,7 +420,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             for (int u = 0; u < 4; ++u) {
               float gv[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) gv[e] = gelu_f(v[8 * u + e]);
+              for (int e = 0; e < 8; e += 2) gelu2(v[8 * u + e], v[8 * u + e + 1], gv[e], gv[e + 1]);
               store8(reinterpret_cast<__nv_bfloat16*>(stg + Cfg::BOX_BYTES + box_off_bf16(lane, u)), gv);
             }
           }
@@ -375,16 +444,21 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[b]);  // this warp has drained accumulator b
+      if (lane == 0) {  // this warp has drained accumulator b
+        if (PAIR) mbar_arrive_cluster(acce_leader + static_cast<uint32_t>(b * sizeof(uint64_t)));
+        else mbar_arrive(&acce[b]);
+      }
     }
     griddep_launch();
     if (lane == 0) bulk_wait_read_all();
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) cluster_sync();  // neither CTA leaves while the pair's products may read its shared memory
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::TCOLS);
+    if (PAIR) tmem_dealloc_pair(tmem, Cfg::TCOLS);
+    else tmem_dealloc(tmem, Cfg::TCOLS);
   }
 }
 
@@ -417,24 +491,24 @@ bool pmake_tmap(CUtensorMap* m, const void* base, bool f32, int64_t inner, int64
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
+template <bool A_K, bool B_K, int BN, int EPI, bool PAIR>
 int pset_attr() {
   static std::atomic<unsigned long long> done{0};
   return once_per_device(done, [] {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_persistent<A_K, B_K, BN, EPI, PAIR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<BN, EPI, PAIR>::SMEM);
     return e == cudaSuccess
                ? GPIPE_OK
                : set_error(GPIPE_ERR_CUDA, "persistent gemm: smem attribute: %s", cudaGetErrorString(e));
   });
 }
 
-template <bool A_K, bool B_K, int BN, int EPI>
+template <bool A_K, bool B_K, int BN, int EPI, bool PAIR>
 int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
-  using Cfg = PCfg<BN, EPI>;
+  using Cfg = PCfg<BN, EPI, PAIR>;
   CUtensorMap ta, tb, tc, tc2;
   bool ok = A_K ? pmake_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, PM) : pmake_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
-  ok = ok && (B_K ? pmake_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, BN)
+  ok = ok && (B_K ? pmake_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, Cfg::BH)
                   : pmake_tmap(&tb, g.B, false, g.N, g.K, g.ldb, 64, 64));
   // output boxes: 32 x 32, one per epilogue warp and chunk (64-byte swizzle for
   // the 64-byte bf16 rows, 128-byte for the fp32 rows)
@@ -442,7 +516,7 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   tc2 = tc;
   if (EPI == EPI_BIAS_GELU) ok = ok && pmake_tmap(&tc2, g.C2, false, g.N, g.M, g.ldc, 32, 32, true);
   if (!ok) return set_error(GPIPE_ERR_CUDA, "persistent gemm: cuTensorMapEncodeTiled failed");
-  int rc = pset_attr<A_K, B_K, BN, EPI>();
+  int rc = pset_attr<A_K, B_K, BN, EPI, PAIR>();
   if (rc) return rc;
   PArgs args{};
   args.bias = (EPI == EPI_STORE || EPI == EPI_BIAS_GELU || EPI == EPI_RESID_F32) ? g.bias : nullptr;
@@ -455,12 +529,35 @@ int prun(const GemmDesc& g, cudaStream_t stream, int ctas) {
   args.M = g.M;
   args.N = g.N;
   args.K = g.K;
-  args.m_tiles = (g.M + PM - 1) / PM;
+  args.m_tiles = (g.M + Cfg::TM - 1) / Cfg::TM;
   args.n_tiles = (g.N + BN - 1) / BN;
   const int tiles = args.m_tiles * args.n_tiles;
-  const int grid = ctas < tiles ? ctas : tiles;
-  (void)launch_k<true>(tc_gemm_persistent<A_K, B_K, BN, EPI>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc, tc2, args,
-                                                                               device_error_ptr());
+  if (!PAIR) {
+    const int grid = ctas < tiles ? ctas : tiles;
+    (void)launch_k<true>(tc_gemm_persistent<A_K, B_K, BN, EPI, PAIR>, grid, P_THREADS, Cfg::SMEM, stream, ta, tb, tc,
+                         tc2, args, device_error_ptr());
+  } else {
+    // one cluster of two CTAs per pair of SMs of the share (an odd share rounded up)
+    const int want = (ctas + 1) / 2;
+    const int pairs = want < tiles ? want : tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(P_THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[3];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 0;  // heavy: never launched early
+    set_priority_attr(attr[2], stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 3;
+    (void)cudaLaunchKernelEx(&cfg, tc_gemm_persistent<A_K, B_K, BN, EPI, PAIR>, ta, tb, tc, tc2, args,
+                             device_error_ptr());
+  }
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPIPE_ERR_CUDA, "persistent gemm launch: %s", cudaGetErrorString(e));
@@ -478,44 +575,44 @@ bool wide_tiles(const GemmDesc& g, int ctas) {
   return 3 * r256 < 2 * r128;
 }
 
-template <int BN>
+template <int BN, bool PAIR = false>
 int dispatch(const GemmDesc& g, cudaStream_t s, int ctas) {
   if (g.a_kmajor && g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return prun<true, true, BN, EPI_STORE>(g, s, ctas);
-      case EPI_BIAS_GELU: return prun<true, true, BN, EPI_BIAS_GELU>(g, s, ctas);
-      case EPI_STORE_F32: return prun<true, true, BN, EPI_STORE_F32>(g, s, ctas);
-      case EPI_ACC_F32: return prun<true, true, BN, EPI_ACC_F32>(g, s, ctas);
-      case EPI_RESID_F32: return prun<true, true, BN, EPI_RESID_F32>(g, s, ctas);
+      case EPI_STORE: return prun<true, true, BN, EPI_STORE, PAIR>(g, s, ctas);
+      case EPI_BIAS_GELU: return prun<true, true, BN, EPI_BIAS_GELU, PAIR>(g, s, ctas);
+      case EPI_STORE_F32: return prun<true, true, BN, EPI_STORE_F32, PAIR>(g, s, ctas);
+      case EPI_ACC_F32: return prun<true, true, BN, EPI_ACC_F32, PAIR>(g, s, ctas);
+      case EPI_RESID_F32: return prun<true, true, BN, EPI_RESID_F32, PAIR>(g, s, ctas);
     }
   } else if (g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return prun<true, false, BN, EPI_STORE>(g, s, ctas);
-      case EPI_GELU_BWD: return prun<true, false, BN, EPI_GELU_BWD>(g, s, ctas);
-      case EPI_ACC_F32: return prun<true, false, BN, EPI_ACC_F32>(g, s, ctas);
+      case EPI_STORE: return prun<true, false, BN, EPI_STORE, PAIR>(g, s, ctas);
+      case EPI_GELU_BWD: return prun<true, false, BN, EPI_GELU_BWD, PAIR>(g, s, ctas);
+      case EPI_ACC_F32: return prun<true, false, BN, EPI_ACC_F32, PAIR>(g, s, ctas);
     }
   } else if (!g.a_kmajor && !g.b_kmajor) {
     switch (g.epi) {
-      case EPI_STORE: return prun<false, false, BN, EPI_STORE>(g, s, ctas);
-      case EPI_ACC_F32: return prun<false, false, BN, EPI_ACC_F32>(g, s, ctas);
+      case EPI_STORE: return prun<false, false, BN, EPI_STORE, PAIR>(g, s, ctas);
+      case EPI_ACC_F32: return prun<false, false, BN, EPI_ACC_F32, PAIR>(g, s, ctas);
     }
   }
   return set_error(GPIPE_ERR_UNSUPPORTED, "persistent gemm: layout/epilogue not built");
 }
 
-template <int BN>
+template <int BN, bool PAIR = false>
 int prepare_bn() {
   int rc = GPIPE_OK;
-  rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE>();
-  rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU>();
-  rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE_F32>();
-  rc = rc ? rc : pset_attr<true, true, BN, EPI_ACC_F32>();
-  rc = rc ? rc : pset_attr<true, true, BN, EPI_RESID_F32>();
-  rc = rc ? rc : pset_attr<true, false, BN, EPI_STORE>();
-  rc = rc ? rc : pset_attr<true, false, BN, EPI_GELU_BWD>();
-  rc = rc ? rc : pset_attr<true, false, BN, EPI_ACC_F32>();
-  rc = rc ? rc : pset_attr<false, false, BN, EPI_STORE>();
-  rc = rc ? rc : pset_attr<false, false, BN, EPI_ACC_F32>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE, PAIR>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_BIAS_GELU, PAIR>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_STORE_F32, PAIR>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_ACC_F32, PAIR>();
+  rc = rc ? rc : pset_attr<true, true, BN, EPI_RESID_F32, PAIR>();
+  rc = rc ? rc : pset_attr<true, false, BN, EPI_STORE, PAIR>();
+  rc = rc ? rc : pset_attr<true, false, BN, EPI_GELU_BWD, PAIR>();
+  rc = rc ? rc : pset_attr<true, false, BN, EPI_ACC_F32, PAIR>();
+  rc = rc ? rc : pset_attr<false, false, BN, EPI_STORE, PAIR>();
+  rc = rc ? rc : pset_attr<false, false, BN, EPI_ACC_F32, PAIR>();
   return rc;
 }
 
@@ -532,14 +629,19 @@ int64_t persistent_tiles(const GemmDesc& g) {
 // tiles, and adds it with a separate reduction.
 bool wide_bias_grad_gemm(const GemmDesc& g) { return g.epi == EPI_ACC_F32 && g.dbias && g.M >= 1024 && g.N >= 1024; }
 
+// 128 x 256 tiles on SM pairs: 256 x 256 tiles computed by 256-row MMAs over
+// two CTAs, each of which loads half the operand bytes per product of one
+// 128 x 256 tile (the per-SM operand stream that bounds the single-CTA tiles).
 int launch_gemm_persistent(const GemmDesc& g, cudaStream_t s, int ctas) {
   if (g.epi == EPI_ACC_F32 && g.dbias) return dispatch<128>(g, s, ctas);  // bias gradient by ones-MMA
-  return wide_tiles(g, ctas) ? dispatch<256>(g, s, ctas) : dispatch<128>(g, s, ctas);
+  if (!wide_tiles(g, ctas)) return dispatch<128>(g, s, ctas);
+  return ctas >= 2 ? dispatch<256, true>(g, s, ctas) : dispatch<256>(g, s, ctas);
 }
 
 int prepare_gemm_persistent() {
-  const int rc = prepare_bn<128>();
-  return rc ? rc : prepare_bn<256>();
+  int rc = prepare_bn<128>();
+  rc = rc ? rc : prepare_bn<256>();
+  return rc ? rc : prepare_bn<256, true>();
 }
 
 }  // namespace gp

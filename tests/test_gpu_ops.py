@@ -46,6 +46,31 @@ SHAPES = [(384, 640, 512), (200, 136, 200), (128, 128, 64), (1000, 96, 72), (170
     (0, 0, 0), (0, 0, 3),
 ])
 def test_gemm_tensor_core(b, shape, ak, bk, epi):
+    _check_gemm(b, shape, ak, bk, epi)
+
+
+# (M, N, K) that the persistent path runs on 256 x 256 tiles over SM pairs
+# (256-row MMAs across two CTAs) at a 16-SM share: one that tiles exactly and
+# one ragged in every dimension (a pair's second CTA past the last row, its
+# half of B past the last column).
+PAIR_SHAPES = [(2048, 2048, 512), (1000, 1288, 264)]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+@pytest.mark.parametrize("ak,bk,epi", [
+    (1, 1, 0), (1, 1, 1), (1, 1, 3), (1, 1, 4),
+    (1, 0, 0), (1, 0, 2), (1, 0, 3),
+    (0, 0, 0), (0, 0, 3),
+])
+def test_gemm_sm_pair_tiles(b, shape, ak, bk, epi):
+    assert b.lib().gpipe_op_gemm_set_sm_share(16) == 0
+    try:
+        _check_gemm(b, shape, ak, bk, epi)
+    finally:
+        assert b.lib().gpipe_op_gemm_set_sm_share(0) == 0
+
+
+def _check_gemm(b, shape, ak, bk, epi):
     M, N, K = shape
     rng = np.random.default_rng(M * 7 + N * 3 + K + 10 * ak + 20 * bk + epi)
     A = bf16_round(rng.standard_normal((M, K) if ak else (K, M)))
