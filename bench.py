@@ -240,7 +240,7 @@ def apply_options(b, gp, args):
 SCHEDULES = {"gpipe": 0, "1f1b": 1}
 
 
-def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
+def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100, b_mn=False):
     """Time one GEMM of the library alone: CUDA events around a CUDA graph of
     `reps` back-to-back launches on the launching stream (host launch cost is
     not in the number; operands stay in L2 where they fit).  epi 1: the FFN
@@ -249,7 +249,14 @@ def gemm_roofline(b, peaks, shape, epi, eager_launches=5, reps=100):
     import torch
     M, N, K = shape
     bf = torch.bfloat16
-    if epi == 0:
+    if epi == 0 and b_mn:
+        A = torch.randn(M, K, device="cuda").to(bf)
+        Bw = torch.randn(K, N, device="cuda").to(bf)
+        Z = torch.empty(M, N, device="cuda", dtype=bf)
+        args = (1, M, N, K, A.data_ptr(), K, 1, Bw.data_ptr(), N, 0, 0, Z.data_ptr(), N, None, None, 0,
+                None, None, 0)
+        name = f"input-gradient GEMM (W read MN-major, bf16 store) {M}x{N}x{K}"
+    elif epi == 0:
         A = torch.randn(M, K, device="cuda").to(bf)
         Bw = torch.randn(N, K, device="cuda").to(bf)
         vec = torch.zeros(N, device="cuda")
@@ -433,12 +440,16 @@ EPI_NAMES = {0: "bf16 store epilogue (bias)", 1: "bias + GELU epilogue", 2: "GEL
              5: "fp32 residual epilogue (bias + fp32 residual, fp32 store)"}
 
 
-# Per-launch DRAM traffic (read + write bytes) of GEMMs of the step's shapes,
-# each from one ncu capture of that shape and epilogue alone (`--probe-gemm`,
-# cold L2): (epilogue, M, N, K) -> bytes.  Inside the step the operands are
-# often still in L2, so this is an upper bound of a launch's DRAM traffic.
-ROOF_TRAFFIC = {(0, 1024, 1024, 8192): 33594368, (0, 512, 512, 2048): 4212224, (0, 512, 1536, 512): 2119168, (0, 512, 512, 512): 1066496,
-                (0, 512, 512, 1536): 3163392,
+# Per-launch DRAM traffic (read + write bytes) of the roofline classes'
+# heaviest shapes, (epilogue, M, N, K) -> bytes, each from one ncu capture of
+# that GEMM alone (`--probe-gemm`, cold L2) with the grid the one-stream pass
+# gives it (the whole GPU): the memory-scaling workload's FFN input gradient
+# (W read MN-major, single-tile 128 x 64 kernel) and FFN weight gradient
+# (SM-pair kernel), and the small LM's shapes.  Inside the step the operands
+# are often still in L2, so this bounds a launch's DRAM traffic from above.
+ROOF_TRAFFIC = {(0, 2048, 1024, 8192): 50416384, (3, 8192, 1024, 2048): 71491584,
+                (0, 1024, 1024, 8192): 33594368, (0, 512, 512, 2048): 4212224, (0, 512, 1536, 512): 2119168,
+                (0, 512, 512, 512): 1066496, (0, 512, 512, 1536): 3163392,
                 (3, 512, 2048, 512): 6832896, (3, 2048, 512, 512): 6839040, (3, 1536, 512, 512): 5264128,
                 (3, 512, 512, 512): 2114304}
 
@@ -708,6 +719,8 @@ def main():
                     help="--probe-gemm epilogue: 0 bias + bf16 store, 1 bias+GELU, 2 GELU backward, 3 weight gradient, "
                          "4 fp32 store, 5 bias + fp32 residual")
     ap.add_argument("--reps", type=int, default=100)
+    ap.add_argument("--b-mn", action="store_true",
+                    help="--probe-gemm --epi 0: B read MN-major, as the step's input-gradient GEMMs read W")
     ap.add_argument("--schedule", default="gpipe", choices=sorted(SCHEDULES),
                     help="issue order: gpipe (all forwards, then all backwards) or 1f1b (interleaved, shorter stash)")
     ap.add_argument("--opt", action="append", default=[], metavar="NAME=VALUE",
@@ -733,7 +746,7 @@ def main():
         shape = tuple(int(x) for x in args.shape.split(",")) if args.shape else (w.tokens // w.M, w.ffn, w.d)
         if args.sms:
             assert b.lib().gpipe_op_gemm_set_sm_share(args.sms) == 0
-        print(json.dumps(gemm_roofline(b, load_peaks(), shape, args.epi, reps=args.reps)), flush=True)
+        print(json.dumps(gemm_roofline(b, load_peaks(), shape, args.epi, reps=args.reps, b_mn=args.b_mn)), flush=True)
         return
     if args.sweep:
         run_sweep(args)

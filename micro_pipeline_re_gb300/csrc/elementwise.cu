@@ -195,27 +195,38 @@ __global__ void __launch_bounds__(256) ln_bwd_kernel(const TD* __restrict__ dy, 
   }
 }
 
-// out[c] += sum_{p < nparts} partial[p*ncols + c], fixed order (4 interleaved
-// accumulators combined in a fixed pattern).  Columns < split go to out_a,
-// the rest to out_b.
-__global__ void col_reduce_kernel(const float* __restrict__ partial, int nparts, int ncols, float* out_a,
-                                  int split, float* out_b) {
+// out[c] += sum_{p < nparts} partial[p*ncols + c] in a fixed order: a block
+// owns 32 columns, warp w adds the parts p = w, w + 8, ... (two alternating
+// accumulators, loads of several parts in flight), and warp 0 adds the 8
+// warps' sums in warp order.  Columns < split go to out_a, the rest to out_b.
+constexpr int kColReduceWarps = 8;
+__global__ void __launch_bounds__(32 * kColReduceWarps) col_reduce_kernel(const float* __restrict__ partial,
+                                                                         int nparts, int ncols, float* out_a,
+                                                                         int split, float* out_b) {
   griddep_wait();
   griddep_launch();
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= ncols) return;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  int p = 0;
-  for (; p + 4 <= nparts; p += 4) {
-    a0 += partial[(int64_t)p * ncols + c];
-    a1 += partial[(int64_t)(p + 1) * ncols + c];
-    a2 += partial[(int64_t)(p + 2) * ncols + c];
-    a3 += partial[(int64_t)(p + 3) * ncols + c];
+  __shared__ float wsum[kColReduceWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 32 + lane;
+  float a0 = 0.f, a1 = 0.f;
+  if (c < ncols) {
+    int p = warp;
+#pragma unroll 4
+    for (; p + kColReduceWarps < nparts; p += 2 * kColReduceWarps) {
+      a0 += partial[(int64_t)p * ncols + c];
+      a1 += partial[(int64_t)(p + kColReduceWarps) * ncols + c];
+    }
+    if (p < nparts) a0 += partial[(int64_t)p * ncols + c];
   }
-  for (; p < nparts; ++p) a0 += partial[(int64_t)p * ncols + c];
-  const float s = (a0 + a1) + (a2 + a3);
-  if (c < split) out_a[c] += s;
-  else out_b[c - split] += s;
+  wsum[warp][lane] = a0 + a1;
+  __syncthreads();
+  if (warp == 0 && c < ncols) {
+    float t = wsum[0][lane];
+#pragma unroll
+    for (int w = 1; w < kColReduceWarps; ++w) t += wsum[w][lane];
+    if (c < split) out_a[c] += t;
+    else out_b[c - split] += t;
+  }
 }
 
 // Column sums of a [rows, cols] matrix: block (x, y) sums rows
@@ -766,7 +777,8 @@ int launch_layernorm_bwd_rows(int dtype, int rows, int d, const void* dy, const 
 
 int launch_layernorm_bwd_reduce(int rows, int d, const float* scratch, float* dg_acc, float* db_acc, cudaStream_t s) {
   const int parts = (rows + kLnRowsPerWarp - 1) / kLnRowsPerWarp;
-  (void)launch_k(col_reduce_kernel, blocks_for(2 * d, 256), 256, 0, s, scratch, parts, 2 * d, dg_acc, d, db_acc);
+  (void)launch_k(col_reduce_kernel, blocks_for(2 * d, 32), 32 * kColReduceWarps, 0, s, scratch, parts, 2 * d, dg_acc, d,
+                 db_acc);
   return check_launch("layernorm_bwd reduce");
 }
 
@@ -816,7 +828,8 @@ int launch_colsum(int dtype, int rows, int cols, const void* y, int64_t ldy, flo
                                                               cols, scratch);
   int rc = check_launch("colsum");
   if (rc) return rc;
-  (void)launch_k(col_reduce_kernel, blocks_for(cols, 256), 256, 0, s, scratch, chunks, cols, out_acc, cols, nullptr);
+  (void)launch_k(col_reduce_kernel, blocks_for(cols, 32), 32 * kColReduceWarps, 0, s, scratch, chunks, cols, out_acc,
+                 cols, nullptr);
   return check_launch("colsum reduce");
 }
 
