@@ -632,10 +632,13 @@ bool wide_bias_grad_gemm(const GemmDesc& g) { return g.epi == EPI_ACC_F32 && g.d
 // 128 x 256 tiles on SM pairs: 256 x 256 tiles computed by 256-row MMAs over
 // two CTAs, each of which loads half the operand bytes per product of one
 // 128 x 256 tile (the per-SM operand stream that bounds the single-CTA tiles).
+// With K < 1024 a tile's mainloop is too short to repay the pair's hand-offs
+// (measured: the small LM's vocabulary GEMMs, K = 512, ran slower on pairs).
+constexpr int kPairMinK = 1024;
 int launch_gemm_persistent(const GemmDesc& g, cudaStream_t s, int ctas) {
   if (g.epi == EPI_ACC_F32 && g.dbias) return dispatch<128>(g, s, ctas);  // bias gradient by ones-MMA
   if (!wide_tiles(g, ctas)) return dispatch<128>(g, s, ctas);
-  return ctas >= 2 ? dispatch<256, true>(g, s, ctas) : dispatch<256>(g, s, ctas);
+  return ctas >= 2 && g.K >= kPairMinK ? dispatch<256, true>(g, s, ctas) : dispatch<256>(g, s, ctas);
 }
 
 int prepare_gemm_persistent() {

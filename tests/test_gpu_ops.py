@@ -50,10 +50,10 @@ def test_gemm_tensor_core(b, shape, ak, bk, epi):
 
 
 # (M, N, K) that the persistent path runs on 256 x 256 tiles over SM pairs
-# (256-row MMAs across two CTAs) at a 16-SM share: one that tiles exactly and
-# one ragged in every dimension (a pair's second CTA past the last row, its
-# half of B past the last column).
-PAIR_SHAPES = [(2048, 2048, 512), (1000, 1288, 264)]
+# (256-row MMAs across two CTAs; K >= 1024) at a 16-SM share: one that tiles
+# exactly and one ragged in every dimension (a pair's second CTA past the last
+# row, its half of B past the last column, a partial last k-block).
+PAIR_SHAPES = [(2048, 2048, 1024), (1000, 1288, 1064)]
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES)
