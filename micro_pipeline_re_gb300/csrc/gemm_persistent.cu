@@ -20,6 +20,17 @@
 //                     with 128-wide tiles an M=128, N=16 MMA against a tile of
 //                     ones into TMEM beside the accumulators; 256-wide tiles
 //                     fill TMEM, so callers add it with a separate reduction)
+// SM pairs (PAIR): clusters of two CTAs walk 256 x BN tiles, pair p taking
+// tiles p, p + pairs, ...  Each CTA's producer loads its own 128 rows of A and
+// BN/2 columns of B per stage, both completing on rank 0's stage barrier
+// (rank 0 expects both halves' bytes); rank 0's lane issues 256-row
+// cta_group::2 products that read both CTAs' stages and accumulate each CTA's
+// rows in its own TMEM; its commits free both CTAs' stages and announce a
+// finished accumulator to both CTAs' epilogues (multicast); the 16 epilogue
+// warps of the pair arrive on rank 0's accumulator-free barrier.  A cluster
+// barrier at the start (every barrier initialised) and at the end (no CTA
+// leaves while the pair's products may still read its shared memory) frames
+// the work.
 // Bounded waits as in the single-tile kernel.
 #include <cuda.h>
 

@@ -577,6 +577,11 @@ int run_epi(const GemmDesc& g, cudaStream_t s) {
   if (persistent_tiles(g) > budget) return launch_gemm_persistent(g, s, budget);
   const int64_t tiles128 = static_cast<int64_t>((g.M + BM - 1) / BM) * ((g.N + 127) / 128);
   if (tiles128 >= budget) return run_epi_bn<128>(g, s, 1);
+  // A long mainloop (K >= 2048) repays the wider tile even on as few as half
+  // the share's SMs: 128-wide products read 128 B of operands per 64 MMA
+  // clocks, 64-wide ones 96 B per 32 (above what shared memory feeds an SM),
+  // and two 64-wide CTAs on one SM share its tensor core anyway.
+  if (g.K >= 2048 && 2 * tiles128 >= budget) return run_epi_bn<128>(g, s, 1);
   return run_epi_bn<64>(g, s, 1);
 }
 

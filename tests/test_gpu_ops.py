@@ -34,9 +34,11 @@ def _gemm_ref(A, B, ak, bk):
 # (1704^2 has enough 128-wide tiles for the 128-column variant or, for the
 # 128-wide epilogues, the persistent kernel; the others take the 64-column one;
 # the two long-K shapes split K across a cluster; 2056 x 2568 takes the
-# persistent kernel for every epilogue, ragged in M, N and K)
+# persistent kernel for every epilogue, ragged in M, N and K; 1000 x 1280 x
+# 2056 has fewer 128-wide tiles than SMs but a long K, so it takes the
+# 128-column single-tile kernel)
 SHAPES = [(384, 640, 512), (200, 136, 200), (128, 128, 64), (1000, 96, 72), (1704, 1704, 200),
-          (200, 256, 16384), (256, 136, 4096), (2056, 2568, 264)]
+          (200, 256, 16384), (256, 136, 4096), (2056, 2568, 264), (1000, 1280, 2056)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -526,7 +528,7 @@ def test_gelu_arithmetic_within_its_error_bound(b):
 @pytest.mark.parametrize("ak,bk,epi,shape", [(1, 1, 1, (1024, 2048, 512)), (1, 1, 0, (512, 1536, 512)),
                                              (1, 0, 2, (512, 2048, 512)), (0, 0, 3, (2048, 512, 512)),
                                              (0, 0, 3, (1152, 1088, 256)), (1, 1, 5, (2048, 1024, 1024)),
-                                             (1, 1, 5, (1000, 1000, 264))])
+                                             (1, 1, 5, (1000, 1000, 264)), (1, 0, 0, (1024, 1280, 2048))])
 def test_gemm_bits_do_not_depend_on_sm_share(b, ak, bk, epi, shape):
     """The step sizes each GEMM's grid by its share of the SMs, which changes
     the kernel (one tile per CTA, 64/128 wide, or persistent 128/256 wide) but
