@@ -444,10 +444,10 @@ EPI_NAMES = {0: "bf16 store epilogue (bias)", 1: "bias + GELU epilogue", 2: "GEL
 # heaviest shapes, (epilogue, M, N, K) -> bytes, each from one ncu capture of
 # that GEMM alone (`--probe-gemm`, cold L2) with the grid the one-stream pass
 # gives it (the whole GPU): the memory-scaling workload's FFN input gradient
-# (W read MN-major, single-tile 128 x 64 kernel) and FFN weight gradient
+# (W read MN-major, single-tile 128 x 128 kernel) and FFN weight gradient
 # (SM-pair kernel), and the small LM's shapes.  Inside the step the operands
 # are often still in L2, so this bounds a launch's DRAM traffic from above.
-ROOF_TRAFFIC = {(0, 2048, 1024, 8192): 50416384, (3, 8192, 1024, 2048): 71491584,
+ROOF_TRAFFIC = {(0, 2048, 1024, 8192): 50356480, (3, 8192, 1024, 2048): 71491584,
                 (0, 1024, 1024, 8192): 33594368, (0, 512, 512, 2048): 4212224, (0, 512, 1536, 512): 2119168,
                 (0, 512, 512, 512): 1066496, (0, 512, 512, 1536): 3163392,
                 (3, 512, 2048, 512): 6832896, (3, 2048, 512, 512): 6839040, (3, 1536, 512, 512): 5264128,
